@@ -1,0 +1,341 @@
+"""Plain fp64 oracle of the MoE expert layer, forward and backward.
+
+TEST INFRASTRUCTURE: imported only by tests, the smoke check and the bench's
+CPU baseline.  It is the loop-over-experts shape of the naive training forward
+(gather each expert's tokens, three small GEMMs, scatter back), with no
+blocking, fusion or reordering beyond what the definitions below state.
+
+Sources (page title, then the section a function follows):
+
+[GG]  "DeepSeek 계열 MoE 학습 가속: Python expert loop → grouped GEMM"
+[EP]  "EP: Expert를 나누고 토큰 보내기"
+[SM]  "SonicMoE: IO·타일 인식 최적화로 MoE 학습 가속하기"
+[DEP] "Deep EP"
+
+Readings where the pages are silent (listed again in the design notes):
+* top-K order: descending logit, ties to the lower expert index;
+* sort by expert is stable: within an expert, pairs keep ascending token order;
+* combine weights are the softmax renormalised over the top-K experts;
+* token rounding: r_e = M * floor((c_e + M/2) / M) capped at M * floor(T/M);
+  priority of a token for expert e is (score s[t,e] descending, token ascending);
+  padding adds the highest-priority unrouted tokens, dropping removes the
+  lowest-priority routed ones; every final pair (t,e) has weight
+  s[t,e] / sum_{j in TopK(t)} s[t,j] (the same denominator as top-K);
+* the router bias is added to the logits and is not trained.
+
+All floating point here is fp64; bf16 inputs are widened exactly.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bits (uint16) to float64."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+# ---------------------------------------------------------------- router
+
+
+def router_logits(X, W_r, bias=None) -> np.ndarray:
+    """l[t,e] = sum_i X[t,i] W_r[i,e] + b[e].
+
+    [DEP] "1) Router": the router looks at the BN x H input token-wise and
+    scores every expert ("gate weight score").
+    """
+    L = _f64(X) @ _f64(W_r)
+    if bias is not None:
+        L = L + _f64(bias)[None, :]
+    return L
+
+
+def topk_experts(logits, K: int) -> np.ndarray:
+    """Indices of the K largest logits per token, largest first, ties to the lower expert.
+
+    [DEP] "1) Router": top-k expert indices per token ([BN, k]).  The comparison
+    happens in the dtype of ``logits`` (fp32 logits from a device give the
+    device's decision; fp64 logits the exact one).
+    """
+    logits = np.asarray(logits)
+    order = np.argsort(-logits, axis=1, kind="stable")
+    return order[:, :K].astype(np.int64)
+
+
+def softmax(logits) -> np.ndarray:
+    """Full softmax over the experts, s[t,e] (fp64)."""
+    L = _f64(logits)
+    z = np.exp(L - L.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def combine_weights(logits, topk_ids) -> np.ndarray:
+    """Weights of every expert relative to the token's top-K set, w[t,e] (fp64, [T,E]).
+
+    w[t,e] = exp(l[t,e]) / sum_{j in TopK(t)} exp(l[t,j]); on the top-K set these
+    sum to 1.  [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기": the weights used to
+    combine (0.7 / 0.3 in the example) are kept apart from the selection.
+    """
+    L = _f64(logits)
+    T = L.shape[0]
+    rows = np.arange(T)[:, None]
+    m = L[rows, topk_ids].max(axis=1, keepdims=True)
+    denom = np.exp(L[rows, topk_ids] - m).sum(axis=1, keepdims=True)
+    return np.exp(L - m) / denom
+
+
+def group_by_expert(topk_ids, E: int):
+    """Flatten the (token, slot) pairs and sort them by expert, stably.
+
+    [GG] "적용 — fused MoE training forward", steps (1)-(3): topk_ids is
+    flattened to 1-D and sorted by expert id, so each expert's tokens form one
+    contiguous slice; bincount gives the per-expert token counts.
+    [DEP] table "Ragged vs Padding": the ragged layout needs offset metadata.
+
+    Returns counts[E], offsets[E+1], perm[P] (pair p = t*K + k at sorted
+    position j is perm[j]) and sorted_tok[P].
+    """
+    topk_ids = np.asarray(topk_ids)
+    K = topk_ids.shape[1]
+    flat = topk_ids.reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    perm = np.argsort(flat, kind="stable").astype(np.int64)
+    return counts, offsets, perm, perm // K
+
+
+def token_rounding(scores, topk_ids, m_tile: int):
+    """Round every expert's token count to the nearest multiple of m_tile.
+
+    [SM] "5 기여 ③ Token Rounding 라우팅": first plain top-K token choice; then,
+    per expert, sort by score and round the received count to the nearest
+    multiple of M_tile — pad with the highest-scoring tokens when short, drop
+    the lowest-scoring ones when over.
+
+    ``scores`` are the full-softmax scores s[T,E] (compared in their own
+    dtype).  Returns member[T,E] (the final pair set) and r[E].
+    """
+    scores = np.asarray(scores)
+    T, E = scores.shape
+    routed = np.zeros((T, E), dtype=bool)
+    routed[np.arange(T)[:, None], topk_ids] = True
+    counts = routed.sum(axis=0)
+    r = m_tile * ((counts + m_tile // 2) // m_tile)
+    r = np.minimum(r, m_tile * (T // m_tile))
+    member = np.zeros((T, E), dtype=bool)
+    tokens = np.arange(T)
+    for e in range(E):
+        # priority order: score descending, then token ascending
+        order = np.lexsort((tokens, -scores[:, e]))
+        routed_first = order[routed[order, e]]
+        unrouted_first = order[~routed[order, e]]
+        if r[e] <= counts[e]:
+            keep = routed_first[: r[e]]
+        else:
+            keep = np.concatenate([routed_first, unrouted_first[: r[e] - counts[e]]])
+        member[keep, e] = True
+    return member, r.astype(np.int64)
+
+
+@dataclass
+class Routing:
+    """Discrete routing state: which (token, expert) pairs exist and in which order.
+
+    topk_ids[T,K]  the top-K selection (TopK(t), largest first)
+    member[T,E]    the final pair set F(t) (= TopK(t) without token rounding)
+    counts[E], offsets[E+1]
+    sorted_tok[P], sorted_exp[P]   pairs grouped by expert, ascending token inside
+    tok_ptr[T+1], tok_pairs[P]     per token, its sorted positions in ascending expert
+    """
+
+    topk_ids: np.ndarray
+    member: np.ndarray
+    counts: np.ndarray
+    offsets: np.ndarray
+    sorted_tok: np.ndarray
+    sorted_exp: np.ndarray
+    tok_ptr: np.ndarray
+    tok_pairs: np.ndarray
+
+    @property
+    def P(self) -> int:
+        return int(self.offsets[-1])
+
+    def rows_of(self, e: int) -> np.ndarray:
+        return self.sorted_tok[self.offsets[e]:self.offsets[e + 1]]
+
+
+def route_discrete(logits, K: int, m_tile: int = 0, scores=None) -> Routing:
+    """The discrete stage of routing from a given set of logits (and scores for rounding).
+
+    Builds the expert-grouped order ([GG] steps (1)-(3)) and the per-token
+    return map ([EP] "토큰을 Expert로 보내고 원래 위치로 돌려받기": each result has to
+    be tracked back to its token).
+    """
+    logits = np.asarray(logits)
+    T, E = logits.shape
+    topk = topk_experts(logits, K)
+    if m_tile:
+        if scores is None:
+            scores = softmax(logits)
+        member, _ = token_rounding(scores, topk, m_tile)
+    else:
+        member = np.zeros((T, E), dtype=bool)
+        member[np.arange(T)[:, None], topk] = True
+    counts = member.sum(axis=0).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    # expert-major, token-ascending order of the pairs
+    e_idx, t_idx = np.nonzero(member.T)
+    sorted_exp, sorted_tok = e_idx.astype(np.int64), t_idx.astype(np.int64)
+    if not m_tile:
+        # cross-check with the flatten + stable-sort description
+        c2, o2, _, st2 = group_by_expert(topk, E)
+        assert np.array_equal(c2, counts) and np.array_equal(st2, sorted_tok)
+    P = len(sorted_tok)
+    j_of = np.full((T, E), -1, dtype=np.int64)
+    j_of[sorted_tok, sorted_exp] = np.arange(P)
+    tok_cnt = member.sum(axis=1)
+    tok_ptr = np.concatenate([[0], np.cumsum(tok_cnt)]).astype(np.int64)
+    tt, ee = np.nonzero(member)  # token-major, expert ascending
+    tok_pairs = j_of[tt, ee]
+    return Routing(topk, member, counts, offsets, sorted_tok, sorted_exp, tok_ptr, tok_pairs)
+
+
+# ---------------------------------------------------------------- experts
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn(x, Wg, Wu, Wd):
+    """One expert's SwiGLU MLP on the rows routed to it.
+
+    [GG] "(6) 세 번의 gg.gmm": gate, up and down projections with the stacked
+    (out, in) weights; [SM] "4.2 Epilogue 융합": SwiGLU, a = silu(x Wg^T) * (x Wu^T).
+    Returns h, u, a, y (all fp64).
+    """
+    x, Wg, Wu, Wd = _f64(x), _f64(Wg), _f64(Wu), _f64(Wd)
+    h = x @ Wg.T
+    u = x @ Wu.T
+    a = silu(h) * u
+    y = a @ Wd.T
+    return h, u, a, y
+
+
+def combine(y_sorted, routing: Routing, w_full, T: int) -> np.ndarray:
+    """Weighted sum of every token's expert outputs back in original token order.
+
+    [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기": y(A2) = 0.7 u0 + 0.3 u2, placed
+    back in A2's own slot; [DEP] "3) Combine": weighted sum of the k expert outputs.
+    ``y_sorted`` holds one row per pair in expert-grouped order.
+    """
+    y_sorted = _f64(y_sorted)
+    O = np.zeros((T, y_sorted.shape[1]))
+    w = w_full[routing.sorted_tok, routing.sorted_exp]
+    np.add.at(O, routing.sorted_tok, w[:, None] * y_sorted)
+    return O
+
+
+def moe_forward(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,
+                scores_for_routing=None):
+    """Forward of the layer.  Returns (O[T,d], cache).
+
+    The selection comes from ``logits_for_routing`` (and ``scores_for_routing``
+    under token rounding) when given — e.g. a device's fp32 logits, so that the
+    discrete decisions match — else from the oracle's own fp64 logits.  The
+    combine weights always come from the oracle's fp64 logits.
+    """
+    X = _f64(X)
+    T, d = X.shape
+    L = router_logits(X, W_r, bias)
+    sel = L if logits_for_routing is None else logits_for_routing
+    routing = route_discrete(sel, K, m_tile, scores=scores_for_routing)
+    w_full = combine_weights(L, routing.topk_ids)
+    E = L.shape[1]
+    y_sorted = np.zeros((routing.P, d))
+    for e in range(E):
+        lo, hi = routing.offsets[e], routing.offsets[e + 1]
+        if hi == lo:
+            continue
+        rows = routing.sorted_tok[lo:hi]
+        _, _, _, y = expert_ffn(X[rows], W_gate[e], W_up[e], W_down[e])
+        y_sorted[lo:hi] = y
+    O = combine(y_sorted, routing, w_full, T)
+    return O, dict(logits=L, routing=routing, w_full=w_full, y_sorted=y_sorted)
+
+
+def expert_block_backward(x, dO, w, Wg, Wu, Wd):
+    """Backward of one expert on the rows routed to it, by the chain rule on its definition.
+
+    O_t = sum_e w[t,e] y_e(x_t), y = a Wd^T, a = silu(h) * u, h = x Wg^T, u = x Wu^T.
+    Returns dict with y, dw (= <dO_t, y_t>), dx contribution, dWg, dWu, dWd.
+    """
+    x, dO, w = _f64(x), _f64(dO), _f64(w)
+    Wg, Wu, Wd = _f64(Wg), _f64(Wu), _f64(Wd)
+    h, u, a, y = expert_ffn(x, Wg, Wu, Wd)
+    dw = np.sum(dO * y, axis=1)
+    dy = w[:, None] * dO
+    da = dy @ Wd
+    sig = 1.0 / (1.0 + np.exp(-h))
+    du = da * (h * sig)
+    dh = da * u * (sig * (1.0 + h * (1.0 - sig)))
+    return dict(y=y, a=a, h=h, u=u, dw=dw, dh=dh, du=du,
+                dx=dh @ Wg + du @ Wu,
+                dWg=dh.T @ x, dWu=du.T @ x, dWd=dy.T @ a)
+
+
+def router_grad_rows(member, topk_ids, w_full, dw_full):
+    """d loss / d logits for the rows given.
+
+    w[t,i] = exp(l_i) / sum_{j in TopK(t)} exp(l_j) for every final pair i in F(t), so
+    dL[t,k] = [k in F(t)] w_k dw_k - [k in TopK(t)] w_k * sum_{i in F(t)} w_i dw_i.
+    """
+    T, E = member.shape
+    topk_mask = np.zeros((T, E), dtype=bool)
+    topk_mask[np.arange(T)[:, None], topk_ids] = True
+    G = np.sum(np.where(member, w_full * dw_full, 0.0), axis=1, keepdims=True)
+    return np.where(member, w_full * dw_full, 0.0) - np.where(topk_mask, w_full * G, 0.0)
+
+
+def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None):
+    """Backward of the layer given the forward cache.
+
+    Returns dX, dW_gate, dW_up, dW_down (fp64, all experts or the listed ones),
+    dw[T,E] (d loss / d combine weight, zero off the pair set), dlogits[T,E], dW_r[d,E].
+    """
+    X, dO = _f64(X), _f64(dO)
+    T, d = X.shape
+    routing: Routing = cache["routing"]
+    w_full = cache["w_full"]
+    E = w_full.shape[1]
+    n = W_gate.shape[1]
+    dX = np.zeros((T, d))
+    dw_full = np.zeros((T, E))
+    keep = range(E) if experts is None else list(experts)
+    dWg = {e: np.zeros((n, d)) for e in keep}
+    dWu = {e: np.zeros((n, d)) for e in keep}
+    dWd = {e: np.zeros((d, n)) for e in keep}
+    for e in range(E):
+        rows = routing.rows_of(e)
+        if len(rows) == 0:
+            continue
+        g = expert_block_backward(X[rows], dO[rows], w_full[rows, e], W_gate[e], W_up[e], W_down[e])
+        dw_full[rows, e] = g["dw"]
+        np.add.at(dX, rows, g["dx"])
+        if e in dWg:
+            dWg[e], dWu[e], dWd[e] = g["dWg"], g["dWu"], g["dWd"]
+    dL = router_grad_rows(routing.member, routing.topk_ids, w_full, dw_full)
+    Wr = _f64(W_r)
+    dX += dL @ Wr.T
+    dWr = X.T @ dL
+    return dict(dX=dX, dW_gate=dWg, dW_up=dWu, dW_down=dWd, dw=dw_full, dlogits=dL, dW_r=dWr)

@@ -1,0 +1,387 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each test names what fixes the expected value: a worked example printed on
+the pages (fixtures in tests/golden/), a closed form, a library routine on a
+special case (torch CPU fp64 functional ops and autograd), finite differences,
+or brute force on tiny inputs.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import moe_oracle as mo
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ep_worked_examples.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _ffn_torch(x, Wg, Wu, Wd):
+    """Dense SwiGLU MLP through torch's own linear / silu (library routines, fp64)."""
+    x, Wg, Wu, Wd = (torch.as_tensor(np.asarray(a, dtype=np.float64)) for a in (x, Wg, Wu, Wd))
+    return F.linear(F.silu(F.linear(x, Wg)) * F.linear(x, Wu), Wd).numpy()
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- worked examples
+
+
+def test_top1_round_trip_worked_example():
+    """EP page, 'Top-1 round trip': A1->E0, A2->E2, B1->E1, B2->E2, combine weight 1."""
+    g = _golden()["top1_round_trip"]
+    T, E, d, n = len(g["tokens"]), g["num_experts"], 8, 5
+    choice = np.array(g["choice"])
+    # X carries a one-hot routing code in its first E columns; W_r reads exactly those.
+    X = np.concatenate([np.eye(E)[choice] * 3.0, _rand((T, d - E), 1)], axis=1)
+    W_r = np.zeros((d, E))
+    W_r[:E, :E] = np.eye(E)
+    Wg, Wu, Wd = _rand((E, n, d), 2, 0.4), _rand((E, n, d), 3, 0.4), _rand((E, d, n), 4, 0.4)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K=1)
+    r = cache["routing"]
+    assert r.counts.tolist() == g["expected_counts"]
+    assert r.offsets.tolist() == g["expected_offsets"]
+    assert [g["tokens"][t] for t in r.sorted_tok] == g["expected_expert_order"]
+    w = cache["w_full"][np.arange(T), choice]
+    assert np.all(w == g["combine_weight"])
+    # every token gets its own expert's output back in its original slot
+    for t in range(T):
+        ref = _ffn_torch(X[t:t + 1], Wg[choice[t]], Wu[choice[t]], Wd[choice[t]])[0]
+        np.testing.assert_allclose(O[t], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_top2_weighted_sum_worked_example():
+    """EP page, 'Top-2': y(A2) = 0.7 u0 + 0.3 u2 (weights kept apart from selection)."""
+    g = _golden()["top2_weights"]
+    e0, e2 = g["experts"]
+    E, d, n = 4, 6, 3
+    # logits with l0 - l2 = ln(7/3), the other experts far below: softmax over the top-2 = (0.7, 0.3)
+    logits = np.array([[math.log(7.0 / 3.0), -40.0, 0.0, -41.0]])
+    X = _rand((1, d), 5)
+    W_r = np.linalg.lstsq(X, logits, rcond=None)[0]  # X @ W_r reproduces the logits
+    Wg, Wu, Wd = _rand((E, n, d), 6), _rand((E, n, d), 7), _rand((E, d, n), 8)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K=2)
+    assert cache["routing"].topk_ids[0].tolist() == [e0, e2]
+    w = cache["w_full"][0, [e0, e2]]
+    np.testing.assert_allclose(w, g["weights"], rtol=1e-12)
+    u0 = _ffn_torch(X, Wg[e0], Wu[e0], Wd[e0])[0]
+    u2 = _ffn_torch(X, Wg[e2], Wu[e2], Wd[e2])[0]
+    np.testing.assert_allclose(O[0], 0.7 * u0 + 0.3 * u2, rtol=1e-11, atol=1e-13)
+
+
+def test_imbalance_worked_example():
+    """EP page, 'load imbalance': E0<-A1, E1<-B1, E2<- the other six -> GPU0 2 tokens, GPU1 6."""
+    g = _golden()["imbalance"]
+    choice = np.array(g["choice"])[:, None]
+    counts, offsets, perm, sorted_tok = mo.group_by_expert(choice, g["num_experts"])
+    assert counts.tolist() == g["expected_counts"]
+    per_gpu = [int(counts[np.array(g["gpu_of_expert"]) == k].sum()) for k in (0, 1)]
+    assert per_gpu == g["expected_tokens_per_gpu"]
+    assert offsets.tolist() == [0, 1, 2, 8, 8]
+
+
+# ---------------------------------------------------------------- invariants of the discrete stage
+
+
+@pytest.mark.parametrize("T,E,K", [(97, 8, 2), (256, 16, 4), (300, 64, 8)])
+def test_grouping_invariants(T, E, K):
+    L = _rand((T, E), T + E)
+    r = mo.route_discrete(L, K)
+    assert r.counts.sum() == T * K
+    assert r.offsets[0] == 0 and r.offsets[-1] == T * K and np.all(np.diff(r.offsets) == r.counts)
+    counts, offsets, perm, sorted_tok = mo.group_by_expert(r.topk_ids, E)
+    # perm is a bijection of the T*K pairs
+    assert np.array_equal(np.sort(perm), np.arange(T * K))
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(T * K)
+    assert np.array_equal(perm[inv], np.arange(T * K))
+    # expert slices are contiguous and stable (ascending token inside an expert)
+    flat = r.topk_ids.reshape(-1)
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(flat[seg] == e) and np.all(np.diff(seg) > 0)
+    # top-K really holds the K largest values, largest first
+    srt = -np.sort(-L, axis=1)
+    np.testing.assert_array_equal(np.take_along_axis(L, r.topk_ids, 1), srt[:, :K])
+    # renormalised weights sum to one over the top-K set
+    w = mo.combine_weights(L, r.topk_ids)
+    np.testing.assert_allclose(np.take_along_axis(w, r.topk_ids, 1).sum(1), 1.0, rtol=1e-14)
+    # the per-token return map lists every pair once, in ascending expert
+    for t in range(0, T, 7):
+        js = r.tok_pairs[r.tok_ptr[t]:r.tok_ptr[t + 1]]
+        assert np.all(r.sorted_tok[js] == t)
+        assert np.all(np.diff(r.sorted_exp[js]) > 0)
+
+
+def test_topk_tie_rule_lower_expert_first():
+    """Reading: equal logits are ordered by expert index."""
+    L = np.array([[1.0, 3.0, 3.0, 0.0, 3.0], [2.0, 2.0, 2.0, 2.0, 2.0]], dtype=np.float32)
+    ids = mo.topk_experts(L, 3)
+    assert ids.tolist() == [[1, 2, 4], [0, 1, 2]]
+
+
+def test_k1_weight_is_exactly_one():
+    L = _rand((50, 7), 11)
+    r = mo.route_discrete(L, 1)
+    w = mo.combine_weights(L, r.topk_ids)
+    assert np.all(w[np.arange(50), r.topk_ids[:, 0]] == 1.0)
+
+
+# ---------------------------------------------------------------- special cases = library routines
+
+
+def test_identity_expert_combine():
+    """With every expert the identity, the combine returns X * sum(w) = X."""
+    T, d, E, K = 40, 6, 5, 3
+    X = _rand((T, d), 12)
+    L = _rand((T, E), 13)
+    r = mo.route_discrete(L, K)
+    w = mo.combine_weights(L, r.topk_ids)
+    O = mo.combine(X[r.sorted_tok], r, w, T)
+    np.testing.assert_allclose(O, X, rtol=1e-13, atol=1e-14)
+
+
+def test_single_expert_is_dense_swiglu_mlp():
+    """E=1, K=1: the layer is a dense SwiGLU MLP (torch functional ops), weight exactly 1."""
+    T, d, n = 33, 10, 7
+    X = _rand((T, d), 14)
+    W_r = _rand((d, 1), 15)
+    Wg, Wu, Wd = _rand((1, n, d), 16, 0.3), _rand((1, n, d), 17, 0.3), _rand((1, d, n), 18, 0.3)
+    O, _ = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K=1)
+    np.testing.assert_allclose(O, _ffn_torch(X, Wg[0], Wu[0], Wd[0]), rtol=1e-12, atol=1e-13)
+
+
+def test_all_experts_is_dense_softmax_mixture():
+    """K=E: the layer is sum_e softmax(l)_e * FFN_e(x) (torch softmax / functional ops)."""
+    T, d, n, E = 21, 9, 4, 5
+    X = _rand((T, d), 19)
+    W_r, b = _rand((d, E), 20), _rand((E,), 21)
+    Wg, Wu, Wd = _rand((E, n, d), 22, 0.3), _rand((E, n, d), 23, 0.3), _rand((E, d, n), 24, 0.3)
+    O, _ = mo.moe_forward(X, W_r, b, Wg, Wu, Wd, K=E)
+    s = torch.softmax(torch.as_tensor(X @ W_r + b), dim=1).numpy()
+    ref = sum(s[:, e:e + 1] * _ffn_torch(X, Wg[e], Wu[e], Wd[e]) for e in range(E))
+    np.testing.assert_allclose(O, ref, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------- backward vs autograd / finite differences
+
+
+def _dense_loss_torch(X, W_r, b, Wg, Wu, Wd, dO, member, topk):
+    """Dense formulation with fixed pair sets: O_t = sum_e [e in F(t)] w_te FFN_e(x_t),
+    w_te = exp(l_te) / sum_{j in TopK(t)} exp(l_tj).  Differentiated by torch autograd."""
+    Xt = torch.tensor(X, dtype=torch.float64, requires_grad=True)
+    Wrt = torch.tensor(W_r, dtype=torch.float64, requires_grad=True)
+    Wgt = torch.tensor(Wg, dtype=torch.float64, requires_grad=True)
+    Wut = torch.tensor(Wu, dtype=torch.float64, requires_grad=True)
+    Wdt = torch.tensor(Wd, dtype=torch.float64, requires_grad=True)
+    logits = Xt @ Wrt + torch.as_tensor(b)
+    logits.retain_grad()
+    topk_mask = torch.zeros_like(logits, dtype=torch.bool)
+    topk_mask[torch.arange(X.shape[0])[:, None], torch.as_tensor(topk)] = True
+    m = logits.masked_fill(~topk_mask, -torch.inf).max(dim=1, keepdim=True).values
+    z = torch.exp(logits - m)
+    w = z / (z * topk_mask).sum(dim=1, keepdim=True)
+    O = torch.zeros_like(Xt)
+    for e in range(Wg.shape[0]):
+        y = F.linear(F.silu(F.linear(Xt, Wgt[e])) * F.linear(Xt, Wut[e]), Wdt[e])
+        O = O + (w[:, e] * torch.as_tensor(member[:, e], dtype=torch.float64))[:, None] * y
+    loss = (O * torch.as_tensor(dO)).sum()
+    loss.backward()
+    return dict(dX=Xt.grad.numpy(), dW_r=Wrt.grad.numpy(), dWg=Wgt.grad.numpy(), dWu=Wut.grad.numpy(),
+                dWd=Wdt.grad.numpy(), dlogits=logits.grad.numpy(), O=O.detach().numpy())
+
+
+@pytest.mark.parametrize("m_tile", [0, 2])
+def test_backward_matches_autograd(m_tile):
+    T, d, E, n, K = 12, 8, 4, 5, 2
+    X, W_r, b = _rand((T, d), 30), _rand((d, E), 31, 0.5), _rand((E,), 32, 0.5)
+    Wg, Wu, Wd = _rand((E, n, d), 33, 0.4), _rand((E, n, d), 34, 0.4), _rand((E, d, n), 35, 0.4)
+    dO = _rand((T, d), 36)
+    O, cache = mo.moe_forward(X, W_r, b, Wg, Wu, Wd, K, m_tile=m_tile)
+    r = cache["routing"]
+    if m_tile:
+        assert not np.array_equal(r.member.sum(1), np.full(T, K)), "rounding should change some tokens"
+    g = mo.moe_backward(X, W_r, b, Wg, Wu, Wd, dO, cache)
+    ref = _dense_loss_torch(X, W_r, b, Wg, Wu, Wd, dO, r.member, r.topk_ids)
+    np.testing.assert_allclose(O, ref["O"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dX"], ref["dX"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dW_r"], ref["dW_r"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dlogits"], ref["dlogits"], rtol=1e-10, atol=1e-12)
+    for e in range(E):
+        np.testing.assert_allclose(g["dW_gate"][e], ref["dWg"][e], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dW_up"][e], ref["dWu"][e], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dW_down"][e], ref["dWd"][e], rtol=1e-10, atol=1e-12)
+    # router-gradient rows sum to zero (the weights over TopK sum to one)
+    np.testing.assert_allclose(g["dlogits"].sum(1), 0.0, atol=1e-12)
+
+
+def test_backward_finite_differences():
+    """Central differences in fp64 (h = 1e-6) on tiny inputs, away from routing ties."""
+    T, d, E, n, K = 4, 8, 3, 4, 2
+    X, W_r = _rand((T, d), 40), _rand((d, E), 41, 0.6)
+    Wg, Wu, Wd = _rand((E, n, d), 42, 0.5), _rand((E, n, d), 43, 0.5), _rand((E, d, n), 44, 0.5)
+    dO = _rand((T, d), 45)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    srt = -np.sort(-cache["logits"], axis=1)
+    assert np.min(srt[:, K - 1] - srt[:, K]) > 1e-3, "inputs too close to a routing tie"
+    g = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache)
+
+    def loss(X_, W_r_, Wg_, Wu_, Wd_):
+        O_, c_ = mo.moe_forward(X_, W_r_, None, Wg_, Wu_, Wd_, K)
+        assert np.array_equal(c_["routing"].member, cache["routing"].member)
+        return float(np.sum(O_ * dO))
+
+    h = 1e-6
+    args = [X, W_r, Wg, Wu, Wd]
+    grads = [g["dX"], g["dW_r"], np.stack([g["dW_gate"][e] for e in range(E)]),
+             np.stack([g["dW_up"][e] for e in range(E)]), np.stack([g["dW_down"][e] for e in range(E)])]
+    rng = np.random.default_rng(46)
+    for ai, (a, ga) in enumerate(zip(args, grads)):
+        for _ in range(6):
+            idx = tuple(rng.integers(0, s) for s in a.shape)
+            ap, am = a.copy(), a.copy()
+            ap[idx] += h
+            am[idx] -= h
+            pa = [ap if i == ai else args[i] for i in range(5)]
+            ma = [am if i == ai else args[i] for i in range(5)]
+            fd = (loss(*pa) - loss(*ma)) / (2 * h)
+            assert abs(fd - ga[idx]) <= 1e-6 * max(1.0, abs(fd)), (ai, idx, fd, ga[idx])
+
+
+def test_score_gradient_identity():
+    """<dO, y> = <dO W_down, a> since y = a W_down^T: the identity the device's dS uses."""
+    T, d, E, n, K = 30, 12, 5, 7, 2
+    X, W_r = _rand((T, d), 50), _rand((d, E), 51)
+    Wg, Wu, Wd = _rand((E, n, d), 52, 0.3), _rand((E, n, d), 53, 0.3), _rand((E, d, n), 54, 0.3)
+    dO = _rand((T, d), 55)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    r = cache["routing"]
+    for e in range(E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        blk = mo.expert_block_backward(X[rows], dO[rows], np.ones(len(rows)), Wg[e], Wu[e], Wd[e])
+        alt = np.sum((dO[rows] @ Wd[e]) * blk["a"], axis=1)
+        np.testing.assert_allclose(blk["dw"], alt, rtol=1e-11, atol=1e-12)
+
+
+def test_empty_expert_weight_gradient_is_zero():
+    T, d, E, n, K = 16, 6, 4, 3, 1
+    X = _rand((T, d), 60)
+    W_r = np.zeros((d, E))
+    W_r[:, 0] = 1.0
+    W_r[:, 1] = -1.0  # expert 2 and 3 never win
+    Wg, Wu, Wd = _rand((E, n, d), 61), _rand((E, n, d), 62), _rand((E, d, n), 63)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    assert cache["routing"].counts[2] == 0 and cache["routing"].counts[3] == 0
+    g = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, _rand((T, d), 64), cache)
+    for e in (2, 3):
+        assert not g["dW_gate"][e].any() and not g["dW_up"][e].any() and not g["dW_down"][e].any()
+
+
+# ---------------------------------------------------------------- token rounding
+
+
+def test_rounding_closed_values():
+    """r = M * floor((c + M/2) / M): nearest multiple, exact halves round up (reading)."""
+    T, E, M = 512, 6, 128
+    counts_wanted = [63, 64, 191, 192, 0, 2]
+    rows = []
+    for e, c in enumerate(counts_wanted):
+        rows += [e] * c
+    topk = np.array(rows + [5] * (T - len(rows)))[:, None]
+    s = _rand((T, E), 70)
+    member, r = mo.token_rounding(s, topk, M)
+    assert r[:4].tolist() == [0, 128, 128, 256]
+    assert np.all(member.sum(0) == r)
+
+
+def _brute_force_round(scores, topk, M):
+    """Enumerate every token subset of the rounded size; keep the one whose members, listed by
+    priority (score desc, token asc), are lexicographically best, subject to keeping all routed
+    tokens (pad) or only routed tokens (drop)."""
+    T, E = scores.shape
+    routed = np.zeros((T, E), bool)
+    routed[np.arange(T)[:, None], topk] = True
+    member = np.zeros((T, E), bool)
+    for e in range(E):
+        c = int(routed[:, e].sum())
+        r = min(M * ((c + M // 2) // M), M * (T // M))
+        best, best_key = None, None
+        for S in itertools.combinations(range(T), r):
+            S = set(S)
+            R = set(np.nonzero(routed[:, e])[0].tolist())
+            if (r <= c and not S <= R) or (r > c and not R <= S):
+                continue
+            # rank of each token in the priority order, smaller = better
+            key = sorted((-scores[t, e], t) for t in S)
+            if best_key is None or key < best_key:
+                best, best_key = S, key
+        for t in best:
+            member[t, e] = True
+    return member
+
+
+def test_token_rounding_brute_force():
+    rng = np.random.default_rng(80)
+    for trial in range(60):
+        T = int(rng.integers(2, 9))
+        E = int(rng.integers(1, 4))
+        K = int(rng.integers(1, E + 1))
+        M = 2
+        s = rng.random((T, E))
+        if trial % 3 == 0:
+            s = np.round(s * 3) / 3  # force score ties
+        topk = mo.topk_experts(s, K)
+        member, r = mo.token_rounding(s, topk, M)
+        assert np.array_equal(member, _brute_force_round(s, topk, M)), trial
+        assert np.all(r % M == 0)
+
+
+@pytest.mark.parametrize("T,E,K,M", [(1024, 16, 2, 64), (2048, 40, 4, 128)])
+def test_token_rounding_invariants(T, E, K, M):
+    L = _rand((T, E), T + E)
+    s = mo.softmax(L)
+    topk = mo.topk_experts(L, K)
+    routed = np.zeros((T, E), bool)
+    routed[np.arange(T)[:, None], topk] = True
+    member, r = mo.token_rounding(s, topk, M)
+    c = routed.sum(0)
+    assert np.all(r % M == 0) and np.all(np.abs(r - c) <= M // 2) and np.all(member.sum(0) == r)
+    for e in range(E):
+        pad = member[:, e] & ~routed[:, e]
+        unchosen = ~member[:, e] & ~routed[:, e]
+        drop = routed[:, e] & ~member[:, e]
+        kept = routed[:, e] & member[:, e]
+        if pad.any() and unchosen.any():
+            assert s[pad, e].min() >= s[unchosen, e].max()
+        if drop.any() and kept.any():
+            assert s[drop, e].max() <= s[kept, e].min()
+    # every final pair is in the expert-major order, tokens ascending
+    rt = mo.route_discrete(L, K, m_tile=M, scores=s)
+    assert np.array_equal(rt.counts, r)
+    for e in range(E):
+        assert np.all(np.diff(rt.rows_of(e)) > 0)
+
+
+# ---------------------------------------------------------------- the metric
+
+
+def test_metric_scale():
+    o = np.array([1.0, -2.0, 0.0, 4.0])
+    assert oracle.rel_error(o, o)["max"] == 0.0
+    r = oracle.rel_error(o + np.array([0.0, 0.0, 0.05, 0.0]), o)
+    # a perturbation of an exact zero is judged against the tensor's rms (sqrt(21/4))
+    assert abs(r["max"] - 0.05 / math.sqrt(21 / 4)) < 1e-12
