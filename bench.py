@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-layer hot path (forward + backward) on GB300.
+
+One step = routing, grouping, the grouped GEMMs, the combine and the whole
+backward (dX, router gradient, weight gradients) on one batch of synthetic
+inputs already resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+Multi-GPU: the path is replicated per GPU (no collective on the data path);
+`value` is the work of all ranks over the slowest rank's time ("weak").
+The reference arm (--impl reference) times the fp64 CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import resource
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd TFLOPS & tokens/s (1 GB300), % of dense BF16 peak"
+PAGE_A100_TFLOPS_C2 = 18 * 4096 * 8 * 2048 * 512 / 13.14e-3 / 1e12  # grouped GEMM on one A100, c2 workload
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def workload_desc(wl):
+    s = f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} n={wl.n} K={wl.K}"
+    if wl.bias != "none":
+        s += f" bias={wl.bias}"
+    if wl.m_tile:
+        s += f" token_rounding M_tile={wl.m_tile}"
+    return s
+
+
+# ------------------------------------------------------------------------ per-kernel algorithmic work
+
+
+def kernel_work(wl, P, dW_bytes=2):
+    """Algorithmic flops and minimum HBM bytes of one launch of each kernel label."""
+    T, d, E, n = wl.T, wl.d, wl.E, wl.n
+    return {
+        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E, "tensor"),
+        "topk_softmax": (0, 4 * T * E + 8 * T * wl.K, "hbm"),
+        "permute": (0, 16 * P + 8 * T * wl.K, "hbm"),
+        "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 6 * P * n, "tensor"),
+        "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d, "tensor"),
+        "combine": (0, 2 * P * d + 2 * T * d, "hbm"),
+        "dact_dswiglu": (2 * P * d * n, 2 * T * d + 2 * E * d * n + 10 * P * n, "tensor"),
+        "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d, "tensor"),
+        "wr_transpose": (0, 4 * d * E, "hbm"),
+        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 6 * T * E, "hbm"),
+        "dwr_gemm": (2 * T * d * E, 2 * T * d + 2 * T * E + 4 * d * E, "tensor"),
+        "dwr_reduce": (0, 8 * d * E, "hbm"),
+        "dw_gate_up": (4 * P * d * n, 2 * T * d + 4 * P * n + 2 * dW_bytes * E * n * d, "tensor"),
+        "dw_down": (2 * P * d * n, 2 * T * d + 2 * P * n + dW_bytes * E * d * n, "tensor"),
+    }
+
+
+# ------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxs.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------------ the oracle as CPU baseline
+
+
+def oracle_sample(wl, budget_s: float, max_experts: int | None = None):
+    """Time the fp64 oracle (forward + backward, loop over experts) on the first experts of the
+    workload until `budget_s` of wall time is spent.  Returns flops done, seconds, experts, cores."""
+    from oracle import moe_oracle as mo
+    X = synth.make_x(wl)
+    W_r = synth.make_router(wl)
+    bias = synth.make_bias(wl)
+    dO = synth.make_dout(wl)
+    ru0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    L = mo.router_logits(X, W_r, bias)
+    routing = mo.route_discrete(L, wl.K, wl.m_tile, scores=mo.softmax(L).astype(np.float32) if wl.m_tile else None)
+    w_full = mo.combine_weights(L, routing.topk_ids)
+    Xf = mo.bf16_bits_to_f64(X)
+    dOf = mo.bf16_bits_to_f64(dO)
+    flops = 2 * wl.T * wl.d * wl.E
+    experts = 0
+    for e in range(wl.E):
+        if max_experts is not None and experts >= max_experts:
+            break
+        if time.perf_counter() - t0 > budget_s and experts > 0:
+            break
+        rows = routing.rows_of(e)
+        experts += 1
+        if len(rows) == 0:
+            continue
+        Wg = synth.make_w_gate(wl, [e])[0]
+        Wu = synth.make_w_up(wl, [e])[0]
+        Wd = synth.make_w_down(wl, [e])[0]
+        mo.expert_block_backward(Xf[rows], dOf[rows], w_full[rows, e], Wg, Wu, Wd)
+        flops += 18 * len(rows) * wl.d * wl.n
+    wall = time.perf_counter() - t0
+    ru1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu = (ru1.ru_utime - ru0.ru_utime) + (ru1.ru_stime - ru0.ru_stime)
+    return dict(flops=flops, seconds=wall, experts=experts, cores=round(cpu / max(wall, 1e-9), 1),
+                host_cpus=os.cpu_count())
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    budget = float(os.environ.get("VGG_REF_STEP_SECONDS", "8"))
+    for _ in range(args.warmup):
+        oracle_sample(wl, budget_s=0.5, max_experts=1)
+    flops, secs, experts, cores = 0, 0.0, 0, 0.0
+    for _ in range(args.steps):
+        r = oracle_sample(wl, budget_s=budget)
+        flops += r["flops"]
+        secs += r["seconds"]
+        experts = r["experts"]
+        cores = r["cores"]
+    value = flops / secs / 1e12
+    sample = (f"fp64 oracle fwd+bwd (loop over experts) on the first {experts} of {wl.E} experts with all their "
+              f"routed tokens, plus the full router, per step ({budget:.0f} s budget)")
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(wl)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "host_cpus": os.cpu_count()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ our arm
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import varlen_grouped_gemm_gb300 as vgg
+    from varlen_grouped_gemm_gb300 import build as lib_build
+
+    torch.cuda.set_device(local_rank)
+    if not os.path.exists(vgg.LIB_PATH):
+        lib_build.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+    wl = synth.WORKLOADS[args.workload]
+    pk = peaks()
+    dev = torch.device("cuda", local_rank)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X_h, dO_h = synth.make_x(wl), synth.make_dout(wl)
+    X = to_dev(X_h)
+    dO = to_dev(dO_h)
+    W_r = to_dev(synth.make_router(wl))
+    bias_h = synth.make_bias(wl)
+    bias = None if bias_h is None else torch.from_numpy(bias_h).to(dev)
+    W_gate = to_dev(synth.make_w_gate(wl))
+    W_up = to_dev(synth.make_w_up(wl))
+    W_down = to_dev(synth.make_w_down(wl))
+    ctx = vgg.Context(local_rank)
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
+                               device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+
+    for _ in range(args.warmup):
+        step()
+    rc, code = vgg.moe_get_error(ctx)
+    if rc != 0:
+        raise RuntimeError(f"device error after warm-up: status {rc}, code {code}")
+    P = int(buf.P.item())
+    counts = buf.counts.cpu().numpy()
+
+    # timed region: K steps, per-step events, L2 flushed between steps outside the events
+    clocks = ClockSampler(local_rank)
+    vgg.moe_profile_enable(ctx, True)
+    vgg.moe_profile_read(ctx)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    prof = vgg.moe_profile_read(ctx)
+    vgg.moe_profile_enable(ctx, False)
+    rc, code = vgg.moe_get_error(ctx)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: status {rc}, code {code}")
+    total_ms = float(sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    flops = wl.flops_fwd_bwd(P)
+    tflops = world * flops / (ms * 1e-3) / 1e12
+    tokens_s = world * wl.T / (ms * 1e-3)
+
+    # dominant kernel and its roofline
+    work = kernel_work(wl, P)
+    dom = max(prof.items(), key=lambda kv: kv[1][0])
+    dname, (dms, dlaunch) = dom
+    fl, by, bound = work[dname]
+    avg_ms = dms / max(dlaunch, 1)
+    if bound == "tensor":
+        achieved = fl / (avg_ms * 1e-3) / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sus"], "traffic": None,
+                "peak_source": f"{pk['source']} sustained bf16",
+                "hbm_gbs_min_bytes": by / (avg_ms * 1e-3) / 1e9, "avg_launch_ms": avg_ms}
+    else:
+        achieved = by / (avg_ms * 1e-3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                "avg_launch_ms": avg_ms}
+    kernels = {}
+    for k, (kms, kl) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
+        f2, b2, bd = work.get(k, (0, 0, "hbm"))
+        a = kms / max(kl, 1)
+        kernels[k] = {"ms_per_step": kms / args.steps, "share": kms / max(sum(v[0] for v in prof.values()), 1e-9),
+                      "tflops": f2 / (a * 1e-3) / 1e12 if f2 else None,
+                      "min_bytes_gbs": b2 / (a * 1e-3) / 1e9}
+    launches_per_label = {"permute": 7 if wl.m_tile else 3}
+    gpu_launches = int(sum(cnt * launches_per_label.get(k, 1) for k, (_, cnt) in prof.items()))
+
+    # end to end through the public API with host buffers: H2D of X and dO, D2H of O and dX per step
+    e2e = None
+    if not args.no_e2e:
+        X_pin = torch.from_numpy(X_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+        dO_pin = torch.from_numpy(dO_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+        O_pin = torch.empty((wl.T, wl.d), dtype=torch.bfloat16).pin_memory()
+        dX_pin = torch.empty((wl.T, wl.d), dtype=torch.bfloat16).pin_memory()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            ee[i][0].record(stream)
+            X.copy_(X_pin, non_blocking=True)
+            dO.copy_(dO_pin, non_blocking=True)
+            step()
+            O_pin.copy_(buf.O, non_blocking=True)
+            dX_pin.copy_(buf.dX, non_blocking=True)
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = float(sum(a.elapsed_time(b) for a, b in ee))
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e_ms /= args.steps
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": 2 * 2 * wl.T * wl.d, "d2h_bytes_per_step": 2 * 2 * wl.T * wl.d}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = oracle_sample(wl, budget_s=float(os.environ.get("VGG_CPU_BASELINE_SECONDS", "15")))
+        cpu = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd on the first {r['experts']} of {wl.E} experts with all their routed "
+                         f"tokens, plus the full router ({r['seconds']:.1f} s)",
+               "host_cpus": r["host_cpus"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": tflops / world / PAGE_A100_TFLOPS_C2 if wl.name == "c2" else None,
+            "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller, shapes of the workload)",
+            "config": {"workload": workload_desc(wl), "pairs": P, "empty_experts": int((counts == 0).sum()),
+                       "max_rows_per_expert": int(counts.max()), "dW_dtype": "bf16",
+                       "l2": "flushed between steps (256 MB write, outside the per-step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": tokens_s, "pct_of_peak_bf16": 100 * tflops / world / pk["bf16_sus"],
+            "peak_bf16_tflops": pk["bf16_sus"], "peak_source": pk["source"] + " sustained",
+            "step_ms_min": min(step_ms), "step_ms_median": float(np.median(step_ms)),
+            "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        }
+        if wl.name == "c2":
+            line["baseline_note"] = ("vs_baseline divides by the pages' grouped-GEMM figure for this workload "
+                                     "(13.14 ms fwd+bwd = 47.1 TFLOP/s on one A100): context, another machine")
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

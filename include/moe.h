@@ -1,0 +1,237 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) MoE expert-layer hot path.
+ *
+ * What the calls compute, with the passages they follow (page title, section):
+ *   [GG]  "DeepSeek 계열 MoE 학습 가속: Python expert loop → grouped GEMM"
+ *   [EP]  "EP: Expert를 나누고 토큰 보내기"
+ *   [SM]  "SonicMoE: IO·타일 인식 최적화로 MoE 학습 가속하기"
+ *   [DEP] "Deep EP"
+ *
+ * Shapes: T tokens, d model width, E experts, n expert width, K experts per token.
+ * Layouts are row-major and contiguous.  Expert weights are the stacked
+ * nn.Linear (out, in) matrices ([GG] "(5) Weight stacking"):
+ *   X[T,d] bf16, W_r[d,E] bf16, bias[E] fp32,
+ *   W_gate[E,n,d] bf16, W_up[E,n,d] bf16, W_down[E,d,n] bf16.
+ * Pairs: one (token, expert) assignment.  P = T*K without token rounding; with
+ * token rounding P is computed on the device and is at most
+ * moe_pair_capacity(T, E, K, m_tile).  Arrays indexed by pair are sized for
+ * that capacity ("cap") and ordered by expert, tokens ascending inside an
+ * expert (the "sorted" order of [GG] "(1)-(3) 토큰 정렬").
+ *
+ * Conventions shared by every call:
+ * - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *   neither allocates nor frees per call.  Scratch memory comes from the
+ *   caller's workspace `ws` of at least moe_workspace_bytes(...) bytes
+ *   (256-byte aligned).  moe_create allocates one small device error word.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and returns a host-side status.  Argument errors
+ *   (NULL pointers, sizes out of range, d or n not multiples of 64,
+ *   misaligned pointers) return MOE_ERR_INVALID_ARG before anything is
+ *   launched; a failed launch returns MOE_ERR_CUDA.
+ * - Errors found on the device (an expert id out of range, corrupt offsets,
+ *   a pair count beyond capacity, a bounded wait that timed out) never trap:
+ *   the kernel records a code in the context's error word and returns early.
+ *   moe_get_error() synchronizes the device and reports it.
+ * - Supported sizes: 1 <= K <= 8, K <= E <= 1024, T <= 65536,
+ *   d and n multiples of 64, m_tile 0 or a multiple of 64.
+ * - No C++ exception crosses this interface.
+ */
+#ifndef VGG_MOE_H
+#define VGG_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx;
+typedef void* moe_stream_t; /* cudaStream_t */
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_DEVICE = 4,         /* a kernel recorded a data error; see moe_get_error */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait gave up */
+};
+
+/* Device-side error codes reported by moe_get_error. */
+enum moe_device_error {
+  MOE_DEV_OK = 0,
+  MOE_DEV_BAD_EXPERT = 1,
+  MOE_DEV_DUP_EXPERT = 2,
+  MOE_DEV_BAD_OFFSETS = 3,
+  MOE_DEV_TIMEOUT = 4,
+  MOE_DEV_CAPACITY = 5,
+};
+
+/* Create a context on `device` (makes it current).  Allocates the 16-byte error word. */
+int moe_create(moe_ctx** out, int device);
+int moe_destroy(moe_ctx* ctx);
+const char* moe_status_str(int status);
+
+/* Synchronize the device, return the first device error code in *device_error
+ * (0 = none) and clear it.  Returns MOE_OK, or MOE_ERR_DEVICE /
+ * MOE_ERR_DEVICE_TIMEOUT when a code was pending, or MOE_ERR_CUDA. */
+int moe_get_error(moe_ctx* ctx, int* device_error);
+
+/* Bound of every device spin-wait, in nanoseconds (default 2 s). */
+int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns);
+
+/* Pair capacity for the pair-indexed arrays: T*K, plus E*m_tile/2 under token rounding. */
+long long moe_pair_capacity(int T, int E, int K, int m_tile);
+
+/* Workspace needed by moe_route / moe_permute / moe_grouped_gemm_fwd / moe_backward for these sizes. */
+size_t moe_workspace_bytes(int T, int d, int E, int n, int K, int m_tile);
+
+/*
+ * moe_route — router logits, top-K token choice and combine weights.
+ * [DEP] "1) Router": scores every expert for each token and returns the top-k
+ * expert indices and scores, [BN, k] each.  [EP] "여러 Expert의 결과도 같은
+ * 토큰으로 돌아오기": the combine weights are kept apart from the selection.
+ *
+ *   logits[t,e] = sum_i X[t,i] W_r[i,e] + bias[e]              (fp32 accumulation)
+ *   topk_ids[t,:] = the K largest logits, largest first, ties to the lower expert
+ *   topk_w[t,k]  = exp(l_k - l_max) / sum_{j in top-K} exp(l_j - l_max)
+ *   scores[t,e]  = softmax over all E experts (only when scores != NULL)
+ *
+ * X[T,d], W_r[d,E] bf16; bias[E] fp32 or NULL; outputs logits[T,E] fp32,
+ * scores[T,E] fp32 (NULL allowed unless token rounding follows),
+ * topk_ids[T,K] int32, topk_w[T,K] fp32.
+ */
+int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, int T, int d, int E, int K,
+              float* logits, float* scores, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+              moe_stream_t stream);
+
+/*
+ * moe_permute — group the (token, expert) pairs by expert.
+ * [GG] "(1)-(3) 토큰 정렬": flatten topk_ids, sort by expert (stable: tokens
+ * ascending inside an expert), bincount per expert.  [DEP] table "Ragged vs
+ * Padding": the ragged layout's offset/index metadata.  [EP] "토큰을 Expert로
+ * 보내고 원래 위치로 돌려받기": every result is tracked back to its token.
+ *
+ * With m_tile > 0 (token rounding, [SM] "5 기여 ③ Token Rounding 라우팅"):
+ * each expert's count c_e becomes r_e = m_tile*floor((c_e + m_tile/2)/m_tile)
+ * (at most m_tile*floor(T/m_tile)); short experts are padded with the tokens
+ * not routed to them in descending scores[t,e] (ties: lower token first),
+ * long ones drop routed tokens in ascending score (ties: higher token first).
+ * A padded pair's weight is exp(l_e - l_max)/sum_{j in top-K} exp(l_j - l_max).
+ * `scores` and `logits` are then required; otherwise they may be NULL.
+ *
+ * Outputs: counts[E], offsets[E+1] (exclusive scan, offsets[E] = P),
+ * sorted_tok[cap] (token of each sorted pair), sorted_w[cap] (its combine
+ * weight), tok_ptr[T+1] and tok_pairs[cap] (per token, the sorted positions
+ * of its pairs in ascending expert), P_out (device int32 scalar).  cap must be
+ * at least moe_pair_capacity(T,E,K,m_tile).
+ */
+int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, const float* logits,
+                const float* scores, int T, int E, int K, int m_tile, long long cap, int32_t* counts,
+                int32_t* offsets, int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
+                int32_t* P_out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_fwd — the expert MLP of every pair, as varlen-M grouped GEMMs.
+ * [GG] "(6) 세 번의 gg.gmm" and "Variable-M batched matmul"; [SM] "MoE 연산 =
+ * Grouped GEMM", "4.1 Gather 융합" (token rows gathered inside the operand
+ * load, the permuted X never written), "4.2 Epilogue 융합" (SwiGLU in the
+ * epilogue).  For sorted pair j of expert e with token t = sorted_tok[j]:
+ *
+ *   H[j] = X[t] W_gate[e]^T,  U[j] = X[t] W_up[e]^T,  A[j] = silu(H[j]) * U[j]
+ *   Yw[j] = sorted_w[j] * (A[j] W_down[e]^T)
+ *
+ * H and U are kept in fp32 (the backward's dSwiGLU reads them); A is computed
+ * from the fp32 accumulators and rounded once to bf16, the operand type of the
+ * down projection.  Outputs H, U [cap,n] fp32, A [cap,n] bf16, Yw [cap,d] bf16.
+ */
+int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const void* W_up, const void* W_down,
+                         int T, int d, int E, int n, long long cap, const int32_t* offsets,
+                         const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine — weighted sum of every token's expert outputs, in original token order.
+ * [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기" (y(A2) = 0.7 u0 + 0.3 u2 in
+ * A2's own slot); [DEP] "3) Combine".  O[t] = sum over t's pairs, in ascending
+ * expert, of Yw[j] (weights already applied); fp32 accumulation in a fixed
+ * order (no atomics, deterministic); O[T,d] bf16.  A token without pairs gets 0.
+ */
+int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
+                long long cap, void* O, moe_stream_t stream);
+
+/*
+ * moe_backward — gradients of the layer for an upstream gradient dO[T,d].
+ * [SM] "3 기여 ① 메모리 효율 알고리즘" (dS from <dA', A> instead of <dO, Y>; no
+ * gathered X or dO materialised), "4.2 Epilogue 융합" (dH, dS, A' in one
+ * epilogue, dSwiGLU fused), "4 기여 ②" (varlen-K grouped GEMM for dW).
+ * With dA'[j] = dO[t] W_down[e] and w = sorted_w[j]:
+ *   dS[j] = <dA'[j], A[j]>           (= <dO[t], Y[j]>, the gradient of w)
+ *   dA = w dA',  dU = dA * silu(H),  dH = dA * U * s(H) (1 + H (1 - s(H)))
+ *   dX[t] = sum_j (dH[j] W_gate[e] + dU[j] W_up[e]) + dlogits[t] W_r^T
+ *   dW_gate[e] = sum_j dH[j]^T X[t], dW_up[e] = sum_j dU[j]^T X[t],
+ *   dW_down[e] = sum_j (w dO[t])^T A[j]    (zero for an expert without pairs)
+ *   dlogits[t,k] = [k in F(t)] w_k dS_k - [k in TopK(t)] w_k sum_{i in F(t)} w_i dS_i
+ *   dW_r = X^T dlogits
+ * (F(t) = the token's final pairs; TopK(t) = its top-K; the bias is not trained.)
+ *
+ * Inputs: dO, X, W_r, W_gate, W_up, W_down, the routing state of moe_route and
+ * moe_permute, and H, U (fp32) from moe_grouped_gemm_fwd.  Outputs: dX[T,d] bf16,
+ * dW_gate/dW_up[E,n,d] and dW_down[E,d,n] (bf16, or fp32 when dW_fp32 != 0),
+ * dS[cap] fp32, dlogits[T,E] fp32, dW_r[d,E] fp32.
+ */
+int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                 const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile, long long cap,
+                 const int32_t* topk_ids, const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok,
+                 const float* sorted_w, const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H,
+                 const void* U, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                 float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Per-kernel timing (tracing).  With profiling enabled, every kernel the
+ * library launches is bracketed by a CUDA event pair on its stream (events
+ * come from a pool created by the first moe_profile_enable).  moe_profile_read
+ * waits for the recorded events, returns per kernel label its accumulated
+ * milliseconds and launch count since the last read (names: max_kernels x 32
+ * chars, NUL-terminated), resets the totals and sets *n_kernels to the number
+ * of labels seen.  A context is not thread-safe while profiling.
+ */
+int moe_profile_enable(moe_ctx* ctx, int enable);
+int moe_profile_read(moe_ctx* ctx, int max_kernels, char* names, double* total_ms, long long* launches,
+                     int* n_kernels);
+
+/*
+ * Test exports: the grouped-GEMM main loops on raw operands, fp32 results.
+ * They exist so that integer-valued operands (exact in fp32 whatever the
+ * summation order) can check the gather, the varlen bookkeeping and the
+ * operand layouts bit for bit.
+ *
+ * moe_test_gemm_varlen_m: for each group e and sorted row j of it,
+ *   D[j, c] = sum_k A[row(j), k] * B[e, c, k]      (B_kmajor = 1: B is [G, N, K])
+ *   D[j, c] = sum_k A[row(j), k] * B[e, k, c]      (B_kmajor = 0: B is [G, K, N])
+ * with row(j) = idx[j] (gathered, idx != NULL) or j.  A[rows_a, K] bf16,
+ * D[cap, N] fp32; offsets[G+1].  A gathered row index outside the source
+ * records MOE_DEV_BAD_OFFSETS and reads zeros instead.
+ *
+ * moe_test_gemm_varlen_k: for each group e,
+ *   D[e, m, c] = sum_{j in group e} A[rowa(j), m] * B[rowb(j), c]
+ * with rowa(j) = idx_a ? idx_a[j] : j (same for b).  A[rows_a, M], B[rows_b, N] bf16,
+ * D[G, M, N] fp32 (zeros for an empty group).
+ */
+int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, const void* B, int B_kmajor,
+                           int G, int rows_a, int K, int N, long long cap, const int32_t* offsets, float* D,
+                           moe_stream_t stream);
+int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, int rows_a, const void* B,
+                           const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
+                           const int32_t* offsets, float* D, moe_stream_t stream);
+
+/* Test export: launch one CTA that waits on an mbarrier nobody arrives on, with
+ * the given bound; the wait gives up, records MOE_DEV_TIMEOUT and returns. */
+int moe_test_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VGG_MOE_H */

@@ -1,0 +1,108 @@
+"""Shared helpers for the GPU tests: synthetic inputs on the device, the whole path, and oracle runs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from oracle import moe_oracle as mo
+
+
+def bits_to_dev(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bits (host) -> bf16 tensor on the device."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def dev_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class Inputs:
+    """Host bits (for the oracle) and device tensors (for the CUDA path) of one workload."""
+
+    def __init__(self, wl: synth.Workload, with_grad: bool = True):
+        self.wl = wl
+        self.X = synth.make_x(wl)
+        self.W_r = synth.make_router(wl)
+        self.bias = synth.make_bias(wl)
+        self.W_gate = synth.make_w_gate(wl)
+        self.W_up = synth.make_w_up(wl)
+        self.W_down = synth.make_w_down(wl)
+        self.dO = synth.make_dout(wl) if with_grad else None
+        self.dev = dict(
+            X=bits_to_dev(self.X), W_r=bits_to_dev(self.W_r),
+            bias=None if self.bias is None else torch.from_numpy(self.bias).cuda(),
+            W_gate=bits_to_dev(self.W_gate), W_up=bits_to_dev(self.W_up), W_down=bits_to_dev(self.W_down),
+            dO=None if self.dO is None else bits_to_dev(self.dO))
+
+
+def run_path(ctx, inp: Inputs, backward=True, dW_dtype=torch.float32):
+    import varlen_grouped_gemm_gb300 as vgg
+    wl, dv = inp.wl, inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=backward, dW_dtype=dW_dtype)
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    if backward:
+        vgg.backward(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    return buf
+
+
+def gpu_routing(buf):
+    """The device's discrete routing state as host arrays, trimmed to P pairs."""
+    P = int(buf.P.item())
+    return dict(
+        P=P, topk_ids=buf.topk_ids.cpu().numpy(), topk_w=buf.topk_w.cpu().numpy(),
+        counts=buf.counts.cpu().numpy(), offsets=buf.offsets.cpu().numpy(),
+        sorted_tok=buf.sorted_tok[:P].cpu().numpy(), sorted_w=buf.sorted_w[:P].cpu().numpy(),
+        tok_ptr=buf.tok_ptr.cpu().numpy(), tok_pairs=buf.tok_pairs[:P].cpu().numpy(),
+        logits=buf.logits.cpu().numpy(), scores=None if buf.scores is None else buf.scores.cpu().numpy())
+
+
+def check_routing_bit_exact(g, K, m_tile):
+    """Contract (i): the oracle's discrete stage on the device's own fp32 logits/scores reproduces
+    every index array bit for bit.  Returns the oracle Routing."""
+    r = mo.route_discrete(g["logits"], K, m_tile, scores=g["scores"])
+    np.testing.assert_array_equal(g["topk_ids"], r.topk_ids)
+    np.testing.assert_array_equal(g["counts"], r.counts)
+    np.testing.assert_array_equal(g["offsets"], r.offsets)
+    assert g["P"] == r.P
+    np.testing.assert_array_equal(g["sorted_tok"], r.sorted_tok)
+    np.testing.assert_array_equal(g["tok_ptr"], r.tok_ptr)
+    np.testing.assert_array_equal(g["tok_pairs"], r.tok_pairs)
+    return r
+
+
+def oracle_layer(inp: Inputs, g=None, backward=True):
+    """fp64 oracle forward (+ backward) with the selection taken from the device's fp32 logits/scores
+    when ``g`` is given (so that routing decisions coincide), else from the oracle's own logits."""
+    wl = inp.wl
+    O, cache = mo.moe_forward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K, wl.m_tile,
+                              logits_for_routing=None if g is None else g["logits"],
+                              scores_for_routing=None if g is None else g["scores"])
+    grads = mo.moe_backward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, inp.dO, cache) \
+        if backward else None
+    return O, cache, grads
+
+
+def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None):
+    """Element-wise comparison of every float output with the fp64 oracle (max/mean metric)."""
+    rep = {} if report is None else report
+    rep["O"] = oracle.compare("O", dev_to_f64(buf.O), O_ref)
+    if grads is None:
+        return rep
+    r: mo.Routing = cache["routing"]
+    E = inp.wl.E
+    rep["dX"] = oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])
+    for name, key in (("dW_gate", "dW_gate"), ("dW_up", "dW_up"), ("dW_down", "dW_down")):
+        got = dev_to_f64(getattr(buf, name))
+        ref = np.stack([grads[key][e] for e in range(E)])
+        rep[name] = oracle.compare(name, got, ref)
+        empty = np.nonzero(r.counts == 0)[0]
+        assert not np.any(got[empty]), f"{name}: experts without pairs must get exactly zero"
+    dS_ref = grads["dw"][r.sorted_tok, r.sorted_exp]
+    rep["dS"] = oracle.compare("dS", dev_to_f64(buf.dS)[:r.P], dS_ref)
+    rep["dlogits"] = oracle.compare("dlogits", dev_to_f64(buf.dlogits), grads["dlogits"])
+    rep["dW_r"] = oracle.compare("dW_r", dev_to_f64(buf.dW_r), grads["dW_r"])
+    return rep

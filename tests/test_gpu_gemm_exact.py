@@ -1,0 +1,103 @@
+"""Grouped-GEMM main loops on integer-valued bf16 operands: every product and partial sum is an
+integer below 2^24, so fp32 accumulation is exact in any order and the device result must equal the
+int64 reference bit for bit.  This pins the gather, the varlen bookkeeping (empty, one-row and
+ragged groups, ragged N), both operand layouts (K-major and MN-major) and the bounded wait."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import varlen_grouped_gemm_gb300 as vgg
+    return vgg.Context(0)
+
+
+def _ints(shape, lo, hi, seed):
+    return np.random.default_rng(seed).integers(lo, hi + 1, size=shape).astype(np.int64)
+
+
+def _bf(a):
+    return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("gathered", [True, False])
+@pytest.mark.parametrize("b_kmajor", [True, False])
+@pytest.mark.parametrize("sizes,K,N", [([0, 1, 130, 257, 64], 192, 200), ([300], 64, 136), ([5, 0, 0, 129], 128, 264)])
+def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
+    import varlen_grouped_gemm_gb300 as vgg
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(offsets[-1])
+    cap = P + 7
+    rows_a = P + 40 if gathered else cap
+    A = _ints((rows_a, K), -2, 2, 1)
+    idx = np.random.default_rng(2).permutation(rows_a)[:cap].astype(np.int32) if gathered else None
+    Bk = _ints((G, N, K), -1, 1, 3)  # [G, N, K]
+    B = Bk if b_kmajor else np.ascontiguousarray(Bk.transpose(0, 2, 1))
+    D = torch.full((cap, N), -7.0, device="cuda")
+    vgg.moe_test_gemm_varlen_m(ctx, _bf(A), None if idx is None else torch.from_numpy(idx).cuda(), _bf(B),
+                               b_kmajor, torch.from_numpy(offsets).cuda(), D)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == 0 and code == 0
+    got = D.cpu().numpy()
+    for e in range(G):
+        for j in range(offsets[e], offsets[e + 1]):
+            row = idx[j] if gathered else j
+            np.testing.assert_array_equal(got[j], (A[row] @ Bk[e].T).astype(np.float32), err_msg=f"e={e} j={j}")
+    assert np.all(got[P:] == -7.0), "rows outside every group must stay untouched"
+
+
+@pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 136), ([1, 0, 333], 128, 256), ([70], 64, 320)])
+@pytest.mark.parametrize("gather_a", [False, True])
+def test_varlen_k_exact(ctx, sizes, M, N, gather_a):
+    import varlen_grouped_gemm_gb300 as vgg
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(offsets[-1])
+    cap = P + 3
+    Tb = P + 17
+    A = _ints((Tb if gather_a else cap, M), -2, 2, 4)
+    Bsrc = _ints((Tb, N), -2, 2, 5)
+    idx_b = np.random.default_rng(6).integers(0, Tb, size=cap).astype(np.int32)
+    idx_a = np.random.default_rng(7).integers(0, Tb, size=cap).astype(np.int32) if gather_a else None
+    D = torch.full((G, M, N), 3.0, device="cuda")
+    vgg.moe_test_gemm_varlen_k(ctx, _bf(A), None if idx_a is None else torch.from_numpy(idx_a).cuda(), _bf(Bsrc),
+                               torch.from_numpy(idx_b).cuda(), torch.from_numpy(offsets).cuda(), D, cap)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == 0 and code == 0
+    got = D.cpu().numpy()
+    for e in range(G):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        ra = idx_a[rows] if gather_a else rows
+        ref = A[ra].T @ Bsrc[idx_b[rows]]
+        np.testing.assert_array_equal(got[e], ref.astype(np.float32), err_msg=f"group {e}")
+
+
+def test_bounded_wait_times_out_and_context_survives(ctx):
+    import varlen_grouped_gemm_gb300 as vgg
+    vgg.moe_test_wait_timeout(ctx, 2_000_000)  # 2 ms
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_ERR_DEVICE_TIMEOUT and code == vgg.DEV_TIMEOUT
+    # the context keeps working afterwards
+    offsets = torch.tensor([0, 3], dtype=torch.int32, device="cuda")
+    A = _bf(np.ones((3, 64)))
+    B = _bf(np.ones((1, 8, 64)))
+    D = torch.zeros((3, 8), device="cuda")
+    vgg.moe_test_gemm_varlen_m(ctx, A, None, B, True, offsets, D)
+    assert vgg.moe_get_error(ctx) == (0, 0)
+    assert torch.all(D == 64.0)
+
+
+def test_corrupt_offsets_are_reported_not_trapped(ctx):
+    import varlen_grouped_gemm_gb300 as vgg
+    offsets = torch.tensor([0, 5, 2], dtype=torch.int32, device="cuda")  # not monotone
+    A = _bf(np.ones((8, 64)))
+    B = _bf(np.ones((2, 8, 64)))
+    D = torch.zeros((8, 8), device="cuda")
+    vgg.moe_test_gemm_varlen_m(ctx, A, None, B, True, offsets, D)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_ERR_DEVICE and code == vgg.DEV_BAD_OFFSETS
+    assert torch.all(D == 0)

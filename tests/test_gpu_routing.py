@@ -1,0 +1,96 @@
+"""Routing and grouping on the device vs the oracle's discrete stage.
+
+(i)  Given the device's own fp32 logits (and scores, under token rounding), the oracle reproduces
+     topk_ids, counts, offsets, the expert-grouped order and the per-token return map bit for bit.
+(ii) Against the oracle's fp64 logits: logits within the float tolerance, and every token whose
+     K-th / (K+1)-th margin exceeds the fp32 summation bound has the same top-K set.
+(iii) Integer-valued inputs make the logits exact, so the device's selection must equal the
+     oracle's own selection with no help from the device's values (ties are frequent and
+     exercise the lower-expert rule)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import moe_oracle as mo
+
+from _helpers import Inputs, check_routing_bit_exact, gpu_routing, run_path
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import varlen_grouped_gemm_gb300 as vgg
+    return vgg.Context(0)
+
+
+CASES = [
+    synth.WORKLOADS["tiny"],
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=600, d=256, n=128),
+    synth.scaled(synth.WORKLOADS["c3"], name="c3_small", T=512, d=512, E=64, n=128),
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small", T=777, d=192, E=128, n=192),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_small", T=2048, d=128, E=64, n=64, m_tile=64),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_tr128", T=4096, d=128, E=32, n=64, m_tile=128),
+]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_routing_bit_exact_given_device_logits(ctx, wl):
+    inp = Inputs(wl, with_grad=False)
+    buf = run_path(ctx, inp, backward=False)
+    g = gpu_routing(buf)
+    r = check_routing_bit_exact(g, wl.K, wl.m_tile)
+    # weights: top-K weights vs fp64 from the device logits' selection
+    L64 = mo.router_logits(inp.X, inp.W_r, inp.bias)
+    oracle.compare("logits", g["logits"], L64)
+    w_ref = mo.combine_weights(L64, r.topk_ids)
+    oracle.compare("topk_w", g["topk_w"], np.take_along_axis(w_ref, r.topk_ids, 1))
+    oracle.compare("sorted_w", g["sorted_w"], w_ref[r.sorted_tok, r.sorted_exp])
+    if wl.m_tile:
+        assert np.all(g["counts"] % wl.m_tile == 0)
+        oracle.compare("scores", g["scores"], mo.softmax(L64))
+
+
+@pytest.mark.parametrize("wl", CASES[:4], ids=lambda w: w.name)
+def test_topk_sets_match_fp64_beyond_margin(ctx, wl):
+    inp = Inputs(wl, with_grad=False)
+    buf = run_path(ctx, inp, backward=False)
+    g = gpu_routing(buf)
+    X = mo.bf16_bits_to_f64(inp.X)
+    Wr = mo.bf16_bits_to_f64(inp.W_r)
+    L64 = mo.router_logits(inp.X, inp.W_r, inp.bias)
+    own = mo.topk_experts(L64, wl.K)
+    srt = -np.sort(-L64, axis=1)
+    margin = srt[:, wl.K - 1] - srt[:, wl.K] if wl.K < wl.E else np.full(wl.T, np.inf)
+    # fp32 summation bound on each logit: gamma_d * sum |x_i w_ie|, times 2 for two logits
+    gamma = wl.d * 2.0 ** -24
+    bound = 2 * gamma * (np.abs(X) @ np.abs(Wr)).max(axis=1) + 1e-6
+    safe = margin > bound
+    same = np.all(np.sort(own, 1) == np.sort(g["topk_ids"], 1), axis=1)
+    assert np.all(same[safe]), np.nonzero(~same & safe)[0][:10]
+    assert safe.mean() > 0.9
+
+
+@pytest.mark.parametrize("wl", [
+    synth.scaled(synth.WORKLOADS["tiny"], name="tiny_int", integer=True),
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_int", T=512, d=128, E=32, n=64, integer=True),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_int_tr", T=1024, d=64, E=16, n=64, m_tile=64, integer=True),
+], ids=lambda w: w.name)
+def test_integer_inputs_routing_fully_independent(ctx, wl):
+    inp = Inputs(wl, with_grad=False)
+    buf = run_path(ctx, inp, backward=False)
+    g = gpu_routing(buf)
+    L64 = mo.router_logits(inp.X, inp.W_r, inp.bias)
+    np.testing.assert_array_equal(g["logits"].astype(np.float64), L64)  # exact integers
+    # the oracle's own selection (its own logits and, under rounding, its own fp64 scores compared
+    # in fp32 as the device does) equals the device's
+    s32 = mo.softmax(L64).astype(np.float32) if wl.m_tile else None
+    r = mo.route_discrete(L64, wl.K, wl.m_tile, scores=g["scores"] if wl.m_tile else None)
+    np.testing.assert_array_equal(g["topk_ids"], r.topk_ids)
+    np.testing.assert_array_equal(g["offsets"], r.offsets)
+    np.testing.assert_array_equal(g["sorted_tok"], r.sorted_tok)
+    np.testing.assert_array_equal(g["tok_pairs"], r.tok_pairs)
+    assert (np.diff(np.sort(L64, 1), axis=1) == 0).any(), "integer logits should contain ties"
+    if s32 is not None:
+        oracle.compare("scores", g["scores"], s32)

@@ -1,0 +1,54 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every symbol include/moe.h declares (CPU only)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from varlen_grouped_gemm_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_five_entry_points():
+    names = _declared()
+    for n in ("moe_route", "moe_permute", "moe_grouped_gemm_fwd", "moe_combine", "moe_backward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    import varlen_grouped_gemm_gb300 as vgg
+    assert set(vgg.EXPORTS) == set(_declared())
+
+
+def test_host_only_queries(libpath):
+    import varlen_grouped_gemm_gb300 as vgg
+    assert vgg.moe_pair_capacity(4096, 128, 8, 0) == 4096 * 8
+    assert vgg.moe_pair_capacity(32768, 512, 8, 128) == 32768 * 8 + 512 * 64
+    assert vgg.moe_workspace_bytes(4096, 2048, 128, 512, 8, 0) > 0
+    assert vgg.moe_workspace_bytes(4096, 2000, 128, 512, 8, 0) == 0  # d not a multiple of 64
+    assert vgg.status_str(vgg.MOE_ERR_INVALID_ARG) == "invalid argument"
+
+
+def test_argument_errors_are_reported_without_a_device(libpath):
+    lib = ctypes.CDLL(libpath)
+    lib.moe_route.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 5 + \
+        [ctypes.c_size_t, ctypes.c_void_p]
+    assert lib.moe_route(None, None, None, None, 1, 64, 8, 2, None, None, None, None, None, 0, None) == 1

@@ -380,8 +380,12 @@ def test_token_rounding_invariants(T, E, K, M):
 
 
 def test_metric_scale():
-    o = np.array([1.0, -2.0, 0.0, 4.0])
+    o = np.array([[1.0, -2.0, 0.0, 4.0], [0.01, 0.0, 0.02, -0.02]])
     assert oracle.rel_error(o, o)["max"] == 0.0
-    r = oracle.rel_error(o + np.array([0.0, 0.0, 0.05, 0.0]), o)
-    # a perturbation of an exact zero is judged against the tensor's rms (sqrt(21/4))
+    r = oracle.rel_error(o + np.array([[0.0, 0.0, 0.05, 0.0], [0.0, 0.0, 0.0, 0.0]]), o)
+    # a perturbation of an exact zero is judged against its row's rms (sqrt(21/4))
     assert abs(r["max"] - 0.05 / math.sqrt(21 / 4)) < 1e-12
+    r = oracle.rel_error(o + np.array([[0.0, 0.0, 0.0, 0.0], [0.0, 0.001, 0.0, 0.0]]), o)
+    # in a small row the floor is that row's rms, not the tensor's
+    assert abs(r["max"] - 0.001 / math.sqrt(0.0009 / 4)) < 1e-9
+    assert r["max_global"] < r["max"]

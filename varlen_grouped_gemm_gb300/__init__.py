@@ -1,0 +1,334 @@
+"""GB300 (sm_103a) MoE expert-layer hot path — Python binding of the C ABI in ``include/moe.h``.
+
+Argument marshalling only: every step of the path (routing, grouping, grouped
+GEMMs, combine, backward) runs in the CUDA library ``lib/libvgg_moe.so``.
+PyTorch supplies device memory and streams.  There is no CPU fallback: when
+the library is missing, every call raises.
+
+The functions carry the C names (``moe_route``, ``moe_permute``,
+``moe_grouped_gemm_fwd``, ``moe_combine``, ``moe_backward``); sizes are taken
+from the tensors' shapes.  ``Buffers`` allocates every tensor the path needs
+for one configuration, and ``forward_backward`` runs the whole path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libvgg_moe.so")
+
+# The symbols declared in include/moe.h.
+EXPORTS = (
+    "moe_create", "moe_destroy", "moe_status_str", "moe_get_error", "moe_set_wait_timeout",
+    "moe_pair_capacity", "moe_workspace_bytes", "moe_route", "moe_permute", "moe_grouped_gemm_fwd",
+    "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
+    "moe_test_gemm_varlen_k", "moe_test_wait_timeout",
+)
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
+DEV_OK, DEV_BAD_EXPERT, DEV_DUP_EXPERT, DEV_BAD_OFFSETS, DEV_TIMEOUT, DEV_CAPACITY = range(6)
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_LL = ctypes.c_longlong
+_SZ = ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run varlen_grouped_gemm_gb300/build.py or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        L.moe_create.argtypes = [ctypes.POINTER(_P), _I]
+        L.moe_destroy.argtypes = [_P]
+        L.moe_status_str.argtypes = [_I]
+        L.moe_status_str.restype = ctypes.c_char_p
+        L.moe_get_error.argtypes = [_P, ctypes.POINTER(_I)]
+        L.moe_set_wait_timeout.argtypes = [_P, ctypes.c_ulonglong]
+        L.moe_pair_capacity.argtypes = [_I, _I, _I, _I]
+        L.moe_pair_capacity.restype = _LL
+        L.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+        L.moe_workspace_bytes.restype = _SZ
+        L.moe_route.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_permute.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.moe_grouped_gemm_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P,
+                                           _P, _SZ, _P]
+        L.moe_combine.argtypes = [_P, _P, _P, _P, _I, _I, _LL, _P, _P]
+        L.moe_backward.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P,
+                                   _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]
+        L.moe_test_gemm_varlen_m.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P]
+        L.moe_test_gemm_varlen_k.argtypes = [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
+        L.moe_test_wait_timeout.argtypes = [_P, ctypes.c_ulonglong, _P]
+        L.moe_profile_enable.argtypes = [_P, _I]
+        L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
+                                       ctypes.POINTER(_LL), ctypes.POINTER(_I)]
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().moe_status_str(code).decode()
+
+
+def _check(name: str, rc: int):
+    if rc != MOE_OK:
+        raise RuntimeError(f"{name} failed: {status_str(rc)} (status {rc})")
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Context:
+    """A library context on one device (owns the device error word)."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        h = _P()
+        _check("moe_create", lib().moe_create(ctypes.byref(h), device))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_wait_timeout(self, ns: int):
+        _check("moe_set_wait_timeout", lib().moe_set_wait_timeout(self.handle, int(ns)))
+
+
+def moe_profile_enable(ctx: Context, enable: bool = True):
+    _check("moe_profile_enable", lib().moe_profile_enable(ctx.handle, 1 if enable else 0))
+
+
+def moe_profile_read(ctx: Context) -> dict[str, tuple[float, int]]:
+    """{kernel label: (total ms, launches)} since the last read (waits for the recorded events)."""
+    nmax = 64
+    names = ctypes.create_string_buffer(32 * nmax)
+    ms = (ctypes.c_double * nmax)()
+    cnt = (_LL * nmax)()
+    n = _I(0)
+    _check("moe_profile_read", lib().moe_profile_read(ctx.handle, nmax, names, ms, cnt, ctypes.byref(n)))
+    out = {}
+    for i in range(min(n.value, nmax)):
+        label = names.raw[32 * i:32 * i + 32].split(b"\0", 1)[0].decode()
+        out[label] = (ms[i], int(cnt[i]))
+    return out
+
+
+def moe_get_error(ctx: Context) -> tuple[int, int]:
+    """(status, device error code); synchronizes the device and clears the code."""
+    code = _I(0)
+    rc = lib().moe_get_error(ctx.handle, ctypes.byref(code))
+    return rc, code.value
+
+
+def moe_pair_capacity(T: int, E: int, K: int, m_tile: int = 0) -> int:
+    return int(lib().moe_pair_capacity(T, E, K, m_tile))
+
+
+def moe_workspace_bytes(T: int, d: int, E: int, n: int, K: int, m_tile: int = 0) -> int:
+    return int(lib().moe_workspace_bytes(T, d, E, n, K, m_tile))
+
+
+def _ws(ws):
+    return (None, 0) if ws is None else (ws.data_ptr(), ws.numel() * ws.element_size())
+
+
+def moe_route(ctx, X, W_r, bias, K, logits, scores, topk_ids, topk_w, ws=None, stream=None):
+    T, d = X.shape
+    E = W_r.shape[1]
+    wp, wb = _ws(ws)
+    _check("moe_route", lib().moe_route(
+        ctx.handle, _ptr(X, torch.bfloat16, "X"), _ptr(W_r, torch.bfloat16, "W_r"),
+        _ptr(bias, torch.float32, "bias"), T, d, E, K, _ptr(logits, torch.float32, "logits"),
+        _ptr(scores, torch.float32, "scores"), _ptr(topk_ids, torch.int32, "topk_ids"),
+        _ptr(topk_w, torch.float32, "topk_w"), wp, wb, _stream(stream)))
+
+
+def moe_permute(ctx, topk_ids, topk_w, logits, scores, E, m_tile, counts, offsets, sorted_tok, sorted_w,
+                tok_ptr, tok_pairs, P_out, ws, stream=None):
+    T, K = topk_ids.shape
+    cap = sorted_tok.numel()
+    wp, wb = _ws(ws)
+    _check("moe_permute", lib().moe_permute(
+        ctx.handle, _ptr(topk_ids, torch.int32), _ptr(topk_w, torch.float32), _ptr(logits, torch.float32),
+        _ptr(scores, torch.float32), T, E, K, m_tile, cap, _ptr(counts, torch.int32),
+        _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32), _ptr(sorted_w, torch.float32),
+        _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32), _ptr(P_out, torch.int32), wp, wb,
+        _stream(stream)))
+
+
+def moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, offsets, sorted_tok, sorted_w, H, U, A, Yw, ws=None,
+                         stream=None):
+    T, d = X.shape
+    E, n, _ = W_gate.shape
+    cap = sorted_tok.numel()
+    wp, wb = _ws(ws)
+    bf = torch.bfloat16
+    _check("moe_grouped_gemm_fwd", lib().moe_grouped_gemm_fwd(
+        ctx.handle, _ptr(X, bf), _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf), T, d, E, n, cap,
+        _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32), _ptr(sorted_w, torch.float32),
+        _ptr(H, torch.float32), _ptr(U, torch.float32), _ptr(A, bf), _ptr(Yw, bf), wp, wb, _stream(stream)))
+
+
+def moe_combine(ctx, Yw, tok_ptr, tok_pairs, O, stream=None):
+    T, d = O.shape
+    _check("moe_combine", lib().moe_combine(
+        ctx.handle, _ptr(Yw, torch.bfloat16), _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32), T, d,
+        tok_pairs.numel(), _ptr(O, torch.bfloat16), _stream(stream)))
+
+
+def moe_backward(ctx, dO, X, W_r, W_gate, W_up, W_down, K, m_tile, topk_ids, topk_w, offsets, sorted_tok,
+                 sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dS, dlogits, dW_r, ws,
+                 stream=None):
+    T, d = X.shape
+    E, n, _ = W_gate.shape
+    cap = sorted_tok.numel()
+    wp, wb = _ws(ws)
+    bf = torch.bfloat16
+    dw_fp32 = 1 if dW_gate.dtype == torch.float32 else 0
+    _check("moe_backward", lib().moe_backward(
+        ctx.handle, _ptr(dO, bf), _ptr(X, bf), _ptr(W_r, bf), _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf),
+        T, d, E, n, K, m_tile, cap, _ptr(topk_ids, torch.int32), _ptr(topk_w, torch.float32),
+        _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32), _ptr(sorted_w, torch.float32),
+        _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32), _ptr(H, torch.float32), _ptr(U, torch.float32),
+        _ptr(dX, bf),
+        _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), dw_fp32, _ptr(dS, torch.float32),
+        _ptr(dlogits, torch.float32), _ptr(dW_r, torch.float32), wp, wb, _stream(stream)))
+
+
+def moe_test_gemm_varlen_m(ctx, A, idx, B, b_kmajor, offsets, D, stream=None):
+    G = B.shape[0]
+    K = A.shape[1]
+    N = B.shape[1] if b_kmajor else B.shape[2]
+    _check("moe_test_gemm_varlen_m", lib().moe_test_gemm_varlen_m(
+        ctx.handle, _ptr(A, torch.bfloat16), _ptr(idx, torch.int32), _ptr(B, torch.bfloat16), int(b_kmajor), G,
+        A.shape[0], K, N, D.shape[0], _ptr(offsets, torch.int32), _ptr(D, torch.float32), _stream(stream)))
+
+
+def moe_test_gemm_varlen_k(ctx, A, idx_a, B, idx_b, offsets, D, cap, stream=None):
+    G, M, N = D.shape
+    _check("moe_test_gemm_varlen_k", lib().moe_test_gemm_varlen_k(
+        ctx.handle, _ptr(A, torch.bfloat16), _ptr(idx_a, torch.int32), A.shape[0], _ptr(B, torch.bfloat16),
+        _ptr(idx_b, torch.int32), B.shape[0], G, M, N, cap, _ptr(offsets, torch.int32), _ptr(D, torch.float32),
+        _stream(stream)))
+
+
+def moe_test_wait_timeout(ctx, timeout_ns: int, stream=None):
+    _check("moe_test_wait_timeout", lib().moe_test_wait_timeout(ctx.handle, int(timeout_ns), _stream(stream)))
+
+
+# ------------------------------------------------------------------ buffers and the whole path
+
+
+@dataclass
+class Buffers:
+    """Every device tensor of one forward + backward for sizes (T, d, E, n, K, m_tile)."""
+
+    T: int
+    d: int
+    E: int
+    n: int
+    K: int
+    m_tile: int
+    cap: int
+    logits: torch.Tensor
+    scores: torch.Tensor | None
+    topk_ids: torch.Tensor
+    topk_w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    sorted_tok: torch.Tensor
+    sorted_w: torch.Tensor
+    tok_ptr: torch.Tensor
+    tok_pairs: torch.Tensor
+    P: torch.Tensor
+    H: torch.Tensor
+    U: torch.Tensor
+    A: torch.Tensor
+    Yw: torch.Tensor
+    O: torch.Tensor
+    dX: torch.Tensor | None
+    dW_gate: torch.Tensor | None
+    dW_up: torch.Tensor | None
+    dW_down: torch.Tensor | None
+    dS: torch.Tensor | None
+    dlogits: torch.Tensor | None
+    dW_r: torch.Tensor | None
+    ws: torch.Tensor
+
+    @staticmethod
+    def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda"):
+        cap = moe_pair_capacity(T, E, K, m_tile)
+        f32, i32, bf = torch.float32, torch.int32, torch.bfloat16
+
+        def z(shape, dt):
+            return torch.zeros(shape, dtype=dt, device=device)
+
+        ws_bytes = moe_workspace_bytes(T, d, E, n, K, m_tile)
+        if ws_bytes == 0:
+            raise ValueError(f"unsupported sizes T={T} d={d} E={E} n={n} K={K}")
+        return Buffers(
+            T, d, E, n, K, m_tile, cap,
+            logits=z((T, E), f32), scores=z((T, E), f32) if m_tile else None,
+            topk_ids=z((T, K), i32), topk_w=z((T, K), f32), counts=z((E,), i32), offsets=z((E + 1,), i32),
+            sorted_tok=z((cap,), i32), sorted_w=z((cap,), f32), tok_ptr=z((T + 1,), i32),
+            tok_pairs=z((cap,), i32), P=z((1,), i32),
+            H=z((cap, n), f32), U=z((cap, n), f32), A=z((cap, n), bf), Yw=z((cap, d), bf), O=z((T, d), bf),
+            dX=z((T, d), bf) if backward else None,
+            dW_gate=z((E, n, d), dW_dtype) if backward else None,
+            dW_up=z((E, n, d), dW_dtype) if backward else None,
+            dW_down=z((E, d, n), dW_dtype) if backward else None,
+            dS=z((cap,), f32) if backward else None, dlogits=z((T, E), f32) if backward else None,
+            dW_r=z((d, E), f32) if backward else None,
+            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device))
+
+
+def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
+    """Routing, grouping, grouped GEMMs and combine; the output is ``buf.O``."""
+    moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
+    moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts, buf.offsets,
+                buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
+    moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w, buf.H, buf.U,
+                         buf.A, buf.Yw, buf.ws, stream)
+    moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
+
+
+def backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf: Buffers, stream=None):
+    moe_backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf.K, buf.m_tile, buf.topk_ids, buf.topk_w, buf.offsets,
+                 buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.H, buf.U, buf.dX, buf.dW_gate,
+                 buf.dW_up, buf.dW_down, buf.dS, buf.dlogits, buf.dW_r, buf.ws, stream)
+
+
+def forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf: Buffers, stream=None):
+    forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf, stream)
+    backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf, stream)

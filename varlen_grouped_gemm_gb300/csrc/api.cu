@@ -1,0 +1,698 @@
+// Host side of the C ABI declared in include/moe.h: argument checks, tensor
+// maps, workspace carving and the launch sequence of every entry point.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "moe.h"
+
+// Per-kernel timing: when enabled, every internal launch is bracketed by a
+// pair of CUDA events on the launching stream; moe_profile_read drains them.
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t beg, end;
+};
+
+struct moe_ctx {
+  int device;
+  int num_sms;
+  int* d_err;
+  unsigned long long timeout_ns;
+  bool prof = false;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_next = 0;
+  std::vector<ProfRecord> pending;
+  std::vector<std::string> names;
+  std::vector<double> total_ms;
+  std::vector<long long> launches;
+};
+
+namespace vgg {
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static bool ensure_encode() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
+                 uint32_t box_rows) {
+  if (!ensure_encode()) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t groups,
+                 uint32_t box_rows) {
+  if (!ensure_encode()) return false;
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t al(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+inline int gemm_bn(int N) { return N > 128 ? 256 : 128; }
+
+constexpr int kMaxSplitK = 16;
+
+struct BwdWs {
+  __nv_bfloat16 *dH, *dU, *Ap, *dXp, *dL, *WrT;
+  float* part;
+  float* wr_part;
+};
+
+size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
+  const int part_ld = ceil_div(n, gemm_bn(n));
+  return 3 * al(sizeof(__nv_bfloat16) * cap * n) + al(sizeof(__nv_bfloat16) * cap * d) +
+         al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E) +
+         al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
+         al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
+}
+
+BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
+  const int part_ld = ceil_div(n, gemm_bn(n));
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  BwdWs w{};
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p;
+    p += al(bytes);
+    return r;
+  };
+  w.dH = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.dU = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.Ap = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.dXp = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
+  w.part = reinterpret_cast<float*>(take(sizeof(float) * cap * part_ld));
+  w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E));
+  w.WrT = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d));
+  w.wr_part = reinterpret_cast<float*>(take(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E));
+  return w;
+}
+
+GemmParams base_params(moe_ctx* ctx) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.split_k = 1;
+  p.a_ksplit = INT_MAX;
+  p.b_ksplit = INT_MAX;
+  p.out_rows_split = INT_MAX;
+  p.ga.split = INT_MAX;
+  p.gb.split = INT_MAX;
+  p.err = ctx->d_err;
+  p.timeout_ns = ctx->timeout_ns;
+  return p;
+}
+
+bool shapes_ok(int T, int d, int E, int n, int K) {
+  return T >= 1 && T <= 65536 && d >= 64 && d % 64 == 0 && n >= 64 && n % 64 == 0 && K >= 1 && K <= 8 && E >= K &&
+         E <= kMaxGroups && E % 8 == 0;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+constexpr size_t kProfPool = 4096;
+
+void prof_drain(moe_ctx* ctx) {
+  for (const ProfRecord& r : ctx->pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.end) == cudaSuccess && cudaEventElapsedTime(&ms, r.beg, r.end) == cudaSuccess) {
+      ctx->total_ms[r.kernel] += ms;
+      ctx->launches[r.kernel] += 1;
+    }
+  }
+  ctx->pending.clear();
+  ctx->pool_next = 0;
+}
+
+int prof_kernel_id(moe_ctx* ctx, const char* name) {
+  for (size_t i = 0; i < ctx->names.size(); ++i)
+    if (ctx->names[i] == name) return static_cast<int>(i);
+  ctx->names.emplace_back(name);
+  ctx->total_ms.push_back(0.0);
+  ctx->launches.push_back(0);
+  return static_cast<int>(ctx->names.size() - 1);
+}
+
+// Brackets one launch with events when profiling is on.
+struct ProfScope {
+  moe_ctx* ctx;
+  cudaStream_t s;
+  ProfRecord rec{};
+  bool on = false;
+  ProfScope(moe_ctx* c, const char* name, cudaStream_t st) : ctx(c), s(st) {
+    if (!ctx->prof) return;
+    if (ctx->pool_next + 2 > ctx->pool.size()) prof_drain(ctx);
+    rec.kernel = prof_kernel_id(ctx, name);
+    rec.beg = ctx->pool[ctx->pool_next++];
+    rec.end = ctx->pool[ctx->pool_next++];
+    on = cudaEventRecord(rec.beg, s) == cudaSuccess;
+  }
+  ~ProfScope() {
+    if (on && cudaEventRecord(rec.end, s) == cudaSuccess) ctx->pending.push_back(rec);
+  }
+};
+
+}  // namespace
+}  // namespace vgg
+
+using namespace vgg;
+
+#define VGG_REQUIRE(cond)                  \
+  do {                                     \
+    if (!(cond)) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+#define VGG_CUDA(call)                          \
+  do {                                          \
+    cudaError_t e_ = (call);                    \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+// A timed launch: `name` is the kernel's label in moe_profile_read.
+#define VGG_LAUNCH(name, call)                    \
+  do {                                            \
+    ProfScope ps_(ctx, name, s);                  \
+    cudaError_t e_ = (call);                      \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;   \
+  } while (0)
+
+extern "C" {
+
+int moe_create(moe_ctx** out, int device) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  if (!ensure_encode()) return MOE_ERR_CUDA;
+  moe_ctx* c = new (std::nothrow) moe_ctx;
+  if (!c) return MOE_ERR_CUDA;
+  c->device = device;
+  c->num_sms = sms;
+  c->timeout_ns = 2000000000ull;
+  if (cudaMalloc(&c->d_err, 16) != cudaSuccess || cudaMemset(c->d_err, 0, 16) != cudaSuccess) {
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+int moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  for (cudaEvent_t e : ctx->pool) cudaEventDestroy(e);
+  cudaFree(ctx->d_err);
+  delete ctx;
+  return MOE_OK;
+}
+
+const char* moe_status_str(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE: return "device-side data error (see moe_get_error)";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_get_error(moe_ctx* ctx, int* device_error) {
+  if (!ctx || !device_error) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  *device_error = 0;
+  VGG_CUDA(cudaDeviceSynchronize());
+  int code = 0;
+  VGG_CUDA(cudaMemcpy(&code, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  VGG_CUDA(cudaMemset(ctx->d_err, 0, 16));
+  *device_error = code;
+  if (code == 0) return MOE_OK;
+  return code == DERR_TIMEOUT ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_DEVICE;
+}
+
+int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns) {
+  if (!ctx || timeout_ns == 0) return MOE_ERR_INVALID_ARG;
+  ctx->timeout_ns = timeout_ns;
+  return MOE_OK;
+}
+
+long long moe_pair_capacity(int T, int E, int K, int m_tile) {
+  long long cap = static_cast<long long>(T) * K;
+  if (m_tile > 0) cap += static_cast<long long>(E) * (m_tile / 2);
+  return cap;
+}
+
+size_t moe_workspace_bytes(int T, int d, int E, int n, int K, int m_tile) {
+  if (!shapes_ok(T, d, E, n, K)) return 0;
+  const long long cap = moe_pair_capacity(T, E, K, m_tile);
+  return std::max(permute_ws_bytes(T, E, K, m_tile), bwd_ws_bytes(T, d, E, n, cap)) + kAlign;
+}
+
+int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, int T, int d, int E, int K,
+              float* logits, float* scores, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+              moe_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  VGG_REQUIRE(ctx && X && W_r && logits && topk_ids && topk_w);
+  VGG_REQUIRE(shapes_ok(T, d, E, 64, K));
+  VGG_REQUIRE(aligned16(X) && aligned16(W_r) && aligned16(logits));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmParams p = base_params(ctx);
+  p.M = T;
+  p.N = E;
+  p.K = d;
+  p.groups = 1;
+  p.out0 = logits;
+  p.ld_out = E;
+  p.out_fp32 = 1;
+  p.col_bias = bias;
+  const int BN = gemm_bn(E);
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof(maps));
+  if (!make_map_2d(&maps[0], X, d, T, d, BM) || !make_map_2d(&maps[2], W_r, E, d, E, 64)) return MOE_ERR_CUDA;
+  maps[1] = maps[0];
+  maps[3] = maps[2];
+  const int tiles = ceil_div(T, BM) * ceil_div(E, BN);
+  VGG_LAUNCH("router_logits", run_router_logits(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  VGG_LAUNCH("topk_softmax", launch_topk_softmax(logits, T, E, K, topk_ids, topk_w, scores, s));
+  return MOE_OK;
+}
+
+int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, const float* logits,
+                const float* scores, int T, int E, int K, int m_tile, long long cap, int32_t* counts,
+                int32_t* offsets, int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
+                int32_t* P_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && topk_ids && topk_w && counts && offsets && sorted_tok && sorted_w && tok_ptr && tok_pairs &&
+              ws);
+  VGG_REQUIRE(shapes_ok(T, 64, E, 64, K));
+  VGG_REQUIRE(m_tile >= 0 && (m_tile == 0 || m_tile % 64 == 0));
+  VGG_REQUIRE(cap >= moe_pair_capacity(T, E, K, m_tile) && cap < INT_MAX);
+  VGG_REQUIRE(ws_bytes >= permute_ws_bytes(T, E, K, m_tile));
+  VGG_REQUIRE((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) == 0);
+  if (m_tile > 0) {
+    VGG_REQUIRE(scores && logits);
+    if (T > 32768) return MOE_ERR_UNSUPPORTED;
+  }
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  PermuteWs w = carve_permute_ws(ws, T, E, K, m_tile);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VGG_LAUNCH("permute", launch_permute(topk_ids, topk_w, logits, scores, T, E, K, m_tile, cap, counts, offsets,
+                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
+  return MOE_OK;
+}
+
+int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const void* W_up, const void* W_down,
+                         int T, int d, int E, int n, long long cap, const int32_t* offsets,
+                         const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  VGG_REQUIRE(ctx && X && W_gate && W_up && W_down && offsets && sorted_tok && sorted_w && H && U && A && Yw);
+  VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
+  VGG_REQUIRE(aligned16(X) && aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(H) &&
+              aligned16(U) && aligned16(A) && aligned16(Yw));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap maps[4];
+  // gate/up + SwiGLU: A = X rows gathered by sorted_tok, B = W_gate / W_up pair
+  {
+    GemmParams p = base_params(ctx);
+    p.N = n;
+    p.K = d;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(X);
+    p.ga.idx = sorted_tok;
+    p.ga.ld = d;
+    p.ga.cols = d;
+    p.ga.rows = T;
+    p.out0 = H;
+    p.out1 = U;
+    p.out2 = A;
+    p.ld_out = n;
+    const int BN = n > 64 ? 256 : 128;
+    std::memset(maps, 0, sizeof(maps));
+    if (!make_map_3d(&maps[2], W_gate, d, n, E, BN / 2) || !make_map_3d(&maps[3], W_up, d, n, E, BN / 2))
+      return MOE_ERR_CUDA;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
+    VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  // down projection, scaled by the combine weight of each row
+  {
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = n;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.out0 = Yw;
+    p.ld_out = d;
+    p.row_scale = sorted_w;
+    const int BN = gemm_bn(d);
+    std::memset(maps, 0, sizeof(maps));
+    if (!make_map_2d(&maps[0], A, n, cap, n, BM) || !make_map_3d(&maps[2], W_down, n, d, E, BN)) return MOE_ERR_CUDA;
+    maps[1] = maps[0];
+    maps[3] = maps[2];
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("down_scale", run_down_scale(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  return MOE_OK;
+}
+
+int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
+                long long cap, void* O, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && Yw && tok_ptr && tok_pairs && O);
+  VGG_REQUIRE(T >= 1 && T <= 65536 && d >= 8 && d % 8 == 0 && cap >= 1);
+  VGG_REQUIRE(aligned16(Yw) && aligned16(O));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VGG_LAUNCH("combine", launch_combine(static_cast<const __nv_bfloat16*>(Yw), tok_ptr, tok_pairs, T, d, cap,
+                                       static_cast<__nv_bfloat16*>(O), ctx->d_err, s));
+  return MOE_OK;
+}
+
+int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                 const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile, long long cap,
+                 const int32_t* topk_ids, const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok,
+                 const float* sorted_w, const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H,
+                 const void* U, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                 float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && dO && X && W_r && W_gate && W_up && W_down && topk_ids && topk_w && offsets && sorted_tok &&
+              sorted_w && tok_ptr && tok_pairs && H && U && dX && dW_gate && dW_up && dW_down && dS && dlogits &&
+              dW_r && ws);
+  VGG_REQUIRE(shapes_ok(T, d, E, n, K));
+  VGG_REQUIRE(m_tile >= 0 && cap >= moe_pair_capacity(T, E, K, m_tile) && cap < INT_MAX);
+  VGG_REQUIRE(ws_bytes >= bwd_ws_bytes(T, d, E, n, cap));
+  VGG_REQUIRE((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) == 0);
+  VGG_REQUIRE(aligned16(dO) && aligned16(X) && aligned16(W_r) && aligned16(W_gate) && aligned16(W_up) &&
+              aligned16(W_down) && aligned16(H) && aligned16(U) && aligned16(dX) && aligned16(dW_gate) &&
+              aligned16(dW_up) && aligned16(dW_down) && aligned16(dW_r));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  BwdWs w = carve_bwd(ws, T, d, E, n, cap);
+  CUtensorMap maps[4];
+  const int bn6 = gemm_bn(n);
+  const int part_ld = ceil_div(n, bn6);
+  // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
+  {
+    GemmParams p = base_params(ctx);
+    p.N = n;
+    p.K = d;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(dO);
+    p.ga.idx = sorted_tok;
+    p.ga.ld = d;
+    p.ga.cols = d;
+    p.ga.rows = T;
+    p.in0 = static_cast<const float*>(H);
+    p.in1 = static_cast<const float*>(U);
+    p.ld_in = n;
+    p.out0 = w.dH;
+    p.out1 = w.dU;
+    p.out2 = w.Ap;
+    p.ld_out = n;
+    p.row_scale = sorted_w;
+    p.part = w.part;
+    p.part_ld = part_ld;
+    std::memset(maps, 0, sizeof(maps));
+    if (!make_map_3d(&maps[2], W_down, n, d, E, 64)) return MOE_ERR_CUDA;
+    maps[3] = maps[2];
+    const int tiles = (ceil_div(cap, BM) + E) * part_ld;
+    VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  // dXp = [dH | dU] [W_gate[e]; W_up[e]]
+  {
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = 2 * n;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.a_ksplit = n;
+    p.b_ksplit = n;
+    p.out0 = w.dXp;
+    p.ld_out = d;
+    const int BN = gemm_bn(d);
+    std::memset(maps, 0, sizeof(maps));
+    if (!make_map_2d(&maps[0], w.dH, n, cap, n, BM) || !make_map_2d(&maps[1], w.dU, n, cap, n, BM) ||
+        !make_map_3d(&maps[2], W_gate, d, n, E, 64) || !make_map_3d(&maps[3], W_up, d, n, E, 64))
+      return MOE_ERR_CUDA;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("dx_gemm", run_dx_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  // per token: dS, router-logit gradient, dX
+  VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
+  VGG_LAUNCH("token_backward", launch_token_backward(w.part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w, topk_ids, topk_w, K,
+                                 w.dXp, w.WrT, T, d, cap, dS, dlogits, w.dL, static_cast<__nv_bfloat16*>(dX),
+                                 ctx->d_err, s));
+  // dW_r = X^T dlogits, split over tokens
+  {
+    GemmParams p = base_params(ctx);
+    p.M = d;
+    p.N = E;
+    p.K = T;
+    p.groups = 1;
+    const int BN = gemm_bn(E);
+    const int tiles = ceil_div(d, BM) * ceil_div(E, BN);
+    int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK));
+    split = std::max(1, std::min(split, ceil_div(T, 8 * BK)));
+    p.split_k = split;
+    p.out0 = split == 1 ? static_cast<void*>(dW_r) : static_cast<void*>(w.wr_part);
+    p.ld_out = E;
+    p.group_stride_out = static_cast<long long>(d) * E;
+    p.out_fp32 = 1;
+    std::memset(maps, 0, sizeof(maps));
+    if (!make_map_2d(&maps[0], X, d, T, d, 64) || !make_map_2d(&maps[2], w.dL, E, T, E, 64)) return MOE_ERR_CUDA;
+    maps[1] = maps[0];
+    maps[3] = maps[2];
+    VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, maps, std::min(tiles * split, ctx->num_sms), s));
+    if (split > 1) VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
+  }
+  // varlen-K weight gradients
+  {
+    GemmParams p = base_params(ctx);
+    p.M = 2 * n;
+    p.N = d;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.ga.ptr0 = w.dH;
+    p.ga.ptr1 = w.dU;
+    p.ga.split = n;
+    p.ga.ld = n;
+    p.ga.cols = 2 * n;
+    p.ga.rows = cap;
+    p.gb.ptr0 = static_cast<const __nv_bfloat16*>(X);
+    p.gb.idx = sorted_tok;
+    p.gb.ld = d;
+    p.gb.cols = d;
+    p.gb.rows = T;
+    p.out0 = dW_gate;
+    p.out1 = dW_up;
+    p.out_rows_split = n;
+    p.ld_out = d;
+    p.group_stride_out = static_cast<long long>(n) * d;
+    p.out_fp32 = dW_fp32 ? 1 : 0;
+    const int BN = gemm_bn(d);
+    std::memset(maps, 0, sizeof(maps));
+    const int tiles = E * ceil_div(2 * n, BM) * ceil_div(d, BN);
+    VGG_LAUNCH("dw_gate_up", run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  {
+    GemmParams p = base_params(ctx);
+    p.M = d;
+    p.N = n;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(dO);
+    p.ga.idx = sorted_tok;
+    p.ga.ld = d;
+    p.ga.cols = d;
+    p.ga.rows = T;
+    p.gb.ptr0 = w.Ap;
+    p.gb.ld = n;
+    p.gb.cols = n;
+    p.gb.rows = cap;
+    p.out0 = dW_down;
+    p.ld_out = n;
+    p.group_stride_out = static_cast<long long>(d) * n;
+    p.out_fp32 = dW_fp32 ? 1 : 0;
+    const int BN = gemm_bn(n);
+    std::memset(maps, 0, sizeof(maps));
+    const int tiles = E * ceil_div(d, BM) * ceil_div(n, BN);
+    VGG_LAUNCH("dw_down", run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  }
+  return MOE_OK;
+}
+
+int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, const void* B, int B_kmajor, int G,
+                           int rows_a, int K, int N, long long cap, const int32_t* offsets, float* D,
+                           moe_stream_t stream) {
+  VGG_REQUIRE(ctx && A && B && offsets && D);
+  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && rows_a >= 1 && K >= 64 && K % 64 == 0 && N >= 8 && N % 8 == 0);
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX && aligned16(A) && aligned16(B) && aligned16(D));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  GemmParams p = base_params(ctx);
+  p.N = N;
+  p.K = K;
+  p.groups = G;
+  p.offsets = offsets;
+  p.rows_cap = static_cast<int>(cap);
+  p.ga.ptr0 = static_cast<const __nv_bfloat16*>(A);
+  p.ga.idx = idx;
+  p.ga.ld = K;
+  p.ga.cols = K;
+  p.ga.rows = rows_a;
+  p.out0 = D;
+  p.ld_out = N;
+  p.out_fp32 = 1;
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof(maps));
+  if (!idx && !make_map_2d(&maps[0], A, K, rows_a, K, BM)) return MOE_ERR_CUDA;
+  maps[1] = maps[0];
+  if (B_kmajor) {
+    if (!make_map_3d(&maps[2], B, K, N, G, 128)) return MOE_ERR_CUDA;
+  } else {
+    if (!make_map_3d(&maps[2], B, N, K, G, 64)) return MOE_ERR_CUDA;
+  }
+  maps[3] = maps[2];
+  const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 128);
+  return cuda_status(run_test_m(idx != nullptr, B_kmajor, p, maps, std::min(tiles, ctx->num_sms),
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, int rows_a, const void* B,
+                           const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
+                           const int32_t* offsets, float* D, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && A && B && offsets && D);
+  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 8 && M % 8 == 0 && N >= 8 && N % 8 == 0 && rows_a >= 1 &&
+              rows_b >= 1);
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX && aligned16(A) && aligned16(B) && aligned16(D));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  GemmParams p = base_params(ctx);
+  p.M = M;
+  p.N = N;
+  p.groups = G;
+  p.offsets = offsets;
+  p.rows_cap = static_cast<int>(cap);
+  p.ga.ptr0 = static_cast<const __nv_bfloat16*>(A);
+  p.ga.idx = idx_a;
+  p.ga.ld = M;
+  p.ga.cols = M;
+  p.ga.rows = rows_a;
+  p.gb.ptr0 = static_cast<const __nv_bfloat16*>(B);
+  p.gb.idx = idx_b;
+  p.gb.ld = N;
+  p.gb.cols = N;
+  p.gb.rows = rows_b;
+  p.out0 = D;
+  p.ld_out = N;
+  p.group_stride_out = static_cast<long long>(M) * N;
+  p.out_fp32 = 1;
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof(maps));
+  const int BN = gemm_bn(N);
+  const int tiles = G * ceil_div(M, BM) * ceil_div(N, BN);
+  return cuda_status(run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), static_cast<cudaStream_t>(stream)));
+}
+
+int moe_profile_enable(moe_ctx* ctx, int enable) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (enable && ctx->pool.empty()) {
+    ctx->pool.resize(kProfPool);
+    for (auto& e : ctx->pool)
+      if (cudaEventCreate(&e) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (!enable) prof_drain(ctx);
+  ctx->prof = enable != 0;
+  return MOE_OK;
+}
+
+int moe_profile_read(moe_ctx* ctx, int max_kernels, char* names, double* total_ms, long long* launches,
+                     int* n_kernels) {
+  if (!ctx || max_kernels < 0 || !n_kernels) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  prof_drain(ctx);
+  const int n = static_cast<int>(ctx->names.size());
+  *n_kernels = n;
+  for (int i = 0; i < n && i < max_kernels; ++i) {
+    if (names) {
+      std::strncpy(names + 32 * i, ctx->names[i].c_str(), 31);
+      names[32 * i + 31] = 0;
+    }
+    if (total_ms) total_ms[i] = ctx->total_ms[i];
+    if (launches) launches[i] = ctx->launches[i];
+    ctx->total_ms[i] = 0.0;
+    ctx->launches[i] = 0;
+  }
+  return MOE_OK;
+}
+
+int moe_test_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && timeout_ns > 0 && timeout_ns <= 10000000000ull);
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  return cuda_status(launch_wait_timeout_probe(ctx->d_err, timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

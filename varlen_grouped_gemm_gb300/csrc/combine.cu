@@ -1,0 +1,280 @@
+// Memory-bound per-token kernels: the weighted combine of the forward, the
+// per-token part of the backward (dS reduction, router-logit gradient, dX
+// K-reduction), and two small helpers (transpose, split-K reduction).
+//
+// [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기": a token's expert outputs are
+// summed back into the token's own slot with the combine weights.
+// [DEP] "3) Combine": weighted sum of the k expert outputs per token.
+// [SM] "7 한계 & 의의": the per-pair output Y is materialised and reduced
+// without float atomics, for determinism and precision.
+//
+// Every token is one CTA; its pairs are visited in ascending expert order
+// (tok_pairs), 16-byte vector loads per thread, fp32 accumulation.
+#include "internal.h"
+
+namespace vgg {
+
+constexpr int kCombineThreads = 128;
+constexpr int kMaxTokPairs = 64;
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], uint4 q) {
+  float2 a = unpack_bf16x2(q.x), b = unpack_bf16x2(q.y), c = unpack_bf16x2(q.z), d = unpack_bf16x2(q.w);
+  acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+  acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  return o;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfloat16* __restrict__ Y,
+                                                                  const int32_t* __restrict__ tok_ptr,
+                                                                  const int32_t* __restrict__ tok_pairs, int T, int d,
+                                                                  long long cap, __nv_bfloat16* __restrict__ O,
+                                                                  int* err) {
+  __shared__ int s_j[kMaxTokPairs];
+  __shared__ int s_cnt;
+  const int t = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const long long p0 = tok_ptr[t], p1 = tok_ptr[t + 1];
+    int cnt = static_cast<int>(p1 - p0);
+    if (p0 < 0 || p1 > cap || cnt < 0 || cnt > kMaxTokPairs) {
+      set_error(err, p1 > cap || p0 < 0 || cnt < 0 ? DERR_BAD_OFFSETS : DERR_CAPACITY);
+      cnt = 0;
+    }
+    s_cnt = cnt;
+  }
+  __syncthreads();
+  const int cnt = s_cnt;
+  const long long p0 = tok_ptr[t];
+  for (int r = threadIdx.x; r < cnt; r += kCombineThreads) {
+    int j = tok_pairs[p0 + r];
+    if (j < 0 || j >= cap) {
+      set_error(err, DERR_BAD_OFFSETS);
+      j = -1;
+    }
+    s_j[r] = j;
+  }
+  __syncthreads();
+  const int nv = d >> 3;
+  for (int c = threadIdx.x; c < nv; c += kCombineThreads) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int r = 0;
+    for (; r + 4 <= cnt; r += 4) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = s_j[r + u];
+        q[u] = j >= 0 ? ldg_nc_v4(Y + static_cast<long long>(j) * d + 8 * c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) add_bf16x8(acc, q[u]);
+    }
+    for (; r < cnt; ++r) {
+      const int j = s_j[r];
+      if (j >= 0) add_bf16x8(acc, ldg_nc_v4(Y + static_cast<long long>(j) * d + 8 * c));
+    }
+    *reinterpret_cast<uint4*>(O + static_cast<long long>(t) * d + 8 * c) = pack8(acc);
+  }
+}
+
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
+                           long long cap, __nv_bfloat16* O, int* err, cudaStream_t s) {
+  if (T > 0) combine_kernel<<<T, kCombineThreads, 0, s>>>(Y, tok_ptr, tok_pairs, T, d, cap, O, err);
+  return cudaGetLastError();
+}
+
+// out[c][r] = in[r][c], bf16, 32x32 tiles through shared memory.
+__global__ void transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in, int rows, int cols,
+                                      __nv_bfloat16* __restrict__ out) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[static_cast<long long>(r) * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[static_cast<long long>(c) * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+cudaError_t launch_transpose_bf16(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out, cudaStream_t s) {
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+  transpose_bf16_kernel<<<grid, block, 0, s>>>(in, rows, cols, out);
+  return cudaGetLastError();
+}
+
+// Expert of sorted pair j: the e with offsets[e] <= j < offsets[e+1].
+__device__ __forceinline__ int expert_of(const int32_t* offsets, int E, int j) {
+  int lo = 0, hi = E;  // invariant: offsets[lo] <= j < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(offsets + mid) <= j) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Per token t (one CTA):
+//   dS[j]       = sum over column tiles of the dSwiGLU epilogue's partial <dA'_j, A_j>
+//   dlogits[t]  = [k in F(t)] w_k dS_k - [k in TopK(t)] w_k * sum_{i in F(t)} w_i dS_i
+//   dX[t]       = sum_j dXp[j] (ascending expert) + sum_e dlogits[t,e] W_r[:,e]
+__global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
+    const float* __restrict__ part, int part_ld, const int32_t* __restrict__ tok_ptr,
+    const int32_t* __restrict__ tok_pairs, const int32_t* __restrict__ offsets, int E,
+    const float* __restrict__ sorted_w, const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w, int K,
+    const __nv_bfloat16* __restrict__ dXp, const __nv_bfloat16* __restrict__ WrT, int T, int d, long long cap,
+    float* __restrict__ dS, float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dL_bf16,
+    __nv_bfloat16* __restrict__ dX, int* err) {
+  __shared__ float s_dl[kMaxGroups];
+  __shared__ int s_j[kMaxTokPairs];
+  __shared__ int s_nz_e[kMaxGroups];
+  __shared__ float s_nz_v[kMaxGroups];
+  __shared__ int s_cnt, s_nnz;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kCombineThreads) s_dl[e] = 0.0f;
+  if (tid == 0) {
+    const long long p0 = tok_ptr[t], p1 = tok_ptr[t + 1];
+    int cnt = static_cast<int>(p1 - p0);
+    if (p0 < 0 || p1 > cap || cnt < 0 || cnt > kMaxTokPairs) {
+      set_error(err, DERR_BAD_OFFSETS);
+      cnt = 0;
+    }
+    s_cnt = cnt;
+  }
+  __syncthreads();
+  const int cnt = s_cnt;
+  const long long p0 = tok_ptr[t];
+  if (warp == 0) {
+    float g = 0.0f;
+    for (int r = lane; r < cnt; r += 32) {
+      int j = tok_pairs[p0 + r];
+      if (j < 0 || j >= cap) {
+        set_error(err, DERR_BAD_OFFSETS);
+        s_j[r] = -1;
+        continue;
+      }
+      s_j[r] = j;
+      float ds = 0.0f;
+      for (int q = 0; q < part_ld; ++q) ds += part[static_cast<long long>(j) * part_ld + q];
+      dS[j] = ds;
+      const int e = expert_of(offsets, E, j);
+      const float c = sorted_w[j] * ds;
+      s_dl[e] += c;  // the experts of one token are distinct
+      g += c;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+    __syncwarp();
+    if (lane < K) {
+      const int e = topk_ids[static_cast<long long>(t) * K + lane];
+      if (e >= 0 && e < E) s_dl[e] -= topk_w[static_cast<long long>(t) * K + lane] * g;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kCombineThreads) {
+    const float v = s_dl[e];
+    dlogits[static_cast<long long>(t) * E + e] = v;
+    dL_bf16[static_cast<long long>(t) * E + e] = __float2bfloat16_rn(v);
+  }
+  if (warp == 0) {
+    int n = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const float v = e < E ? s_dl[e] : 0.0f;
+      const unsigned m = __ballot_sync(0xffffffffu, v != 0.0f);
+      if (v != 0.0f) {
+        const int pos = n + __popc(m & ((1u << lane) - 1u));
+        s_nz_e[pos] = e;
+        s_nz_v[pos] = v;
+      }
+      n += __popc(m);
+    }
+    if (lane == 0) s_nnz = n;
+  }
+  __syncthreads();
+  const int nnz = s_nnz;
+  const int nv = d >> 3;
+  for (int c = tid; c < nv; c += kCombineThreads) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int r = 0; r < cnt; ++r) {
+      const int j = s_j[r];
+      if (j >= 0) add_bf16x8(acc, ldg_nc_v4(dXp + static_cast<long long>(j) * d + 8 * c));
+    }
+    for (int i = 0; i < nnz; ++i) {
+      const float v = s_nz_v[i];
+      const uint4 q = *reinterpret_cast<const uint4*>(WrT + static_cast<long long>(s_nz_e[i]) * d + 8 * c);
+      const float2 a = unpack_bf16x2(q.x), b = unpack_bf16x2(q.y), cc = unpack_bf16x2(q.z), dd = unpack_bf16x2(q.w);
+      acc[0] += v * a.x; acc[1] += v * a.y; acc[2] += v * b.x; acc[3] += v * b.y;
+      acc[4] += v * cc.x; acc[5] += v * cc.y; acc[6] += v * dd.x; acc[7] += v * dd.y;
+    }
+    *reinterpret_cast<uint4*>(dX + static_cast<long long>(t) * d + 8 * c) = pack8(acc);
+  }
+}
+
+cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t* tok_ptr, const int32_t* tok_pairs,
+                                  const int32_t* offsets, int E, const float* sorted_w, const int32_t* topk_ids,
+                                  const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
+                                  int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
+                                  __nv_bfloat16* dX, int* err, cudaStream_t s) {
+  if (T > 0)
+    token_backward_kernel<<<T, kCombineThreads, 0, s>>>(part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
+                                                        topk_ids, topk_w, K, dXp, WrT, T, d, cap, dS, dlogits,
+                                                        dL_bf16, dX, err);
+  return cudaGetLastError();
+}
+
+// out[i] = sum_s part[s][i], s ascending.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long n,
+                                     float* __restrict__ out) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float a = 0.0f;
+    for (int s = 0; s < splits; ++s) a += part[s * n + i];
+    out[i] = a;
+  }
+}
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, long long n, float* out, cudaStream_t s) {
+  const long long want = (n + 255) / 256;
+  const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+  if (n > 0) splitk_reduce_kernel<<<blocks, 256, 0, s>>>(part, splits, n, out);
+  return cudaGetLastError();
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait gives up,
+// records the timeout code and the kernel returns normally.
+__global__ void wait_timeout_probe_kernel(int* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, timeout_ns, err);
+  __syncthreads();
+}
+
+cudaError_t launch_wait_timeout_probe(int* err, unsigned long long timeout_ns, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace vgg

@@ -1,0 +1,72 @@
+// Declarations shared by the translation units of the library (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.cuh"
+
+namespace vgg {
+
+// ---- tensor maps (host) -------------------------------------------------------------------
+// 2-D bf16 view [rows][inner] with a row stride, box {64, box_rows}, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
+                 uint32_t box_rows);
+// 3-D bf16 view [groups][rows][inner], box {64, box_rows, 1}, 128-byte swizzle.
+bool make_map_3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t groups,
+                 uint32_t box_rows);
+
+// ---- grouped GEMM instantiations (BN chosen at run time: 128 or 256) -------------------------
+// forward
+cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_down_scale(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_router_logits(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+// backward
+cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_dx_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_varlen_k_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+// test exports
+cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const CUtensorMap* maps, int grid,
+                       cudaStream_t s);
+
+// ---- routing / permutation -----------------------------------------------------------------
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int K, int32_t* ids, float* w, float* scores,
+                                cudaStream_t s);
+
+struct PermuteWs {
+  int32_t* hist;       // [E * nb]
+  int32_t* tokblk;     // [nb + 1]
+  uint32_t* member;    // [T * ceil(E/32)] final pair bitmap (token rounding)
+  int32_t* plain_off;  // [E + 1]
+  int32_t* plain_cnt;  // [E]
+  int32_t* plain_tok;  // [T * K]
+};
+size_t permute_ws_bytes(int T, int E, int K, int m_tile);
+PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile);
+
+cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const float* logits, const float* scores,
+                           int T, int E, int K, int m_tile, long long cap, int32_t* counts, int32_t* offsets,
+                           int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
+                           int32_t* P_out, const PermuteWs& w, int* err, cudaStream_t s);
+
+// ---- combine / reductions --------------------------------------------------------------------
+cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
+                           long long cap, __nv_bfloat16* O, int* err, cudaStream_t s);
+
+cudaError_t launch_transpose_bf16(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out, cudaStream_t s);
+
+// Per token: dS of its pairs (sum of the per-column-tile partials), the router-logit gradient,
+// and dX = sum of the pairs' dX rows + dlogits W_r^T.
+cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t* tok_ptr, const int32_t* tok_pairs,
+                                  const int32_t* offsets, int E, const float* sorted_w, const int32_t* topk_ids,
+                                  const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
+                                  int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
+                                  __nv_bfloat16* dX, int* err, cudaStream_t s);
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, long long n, float* out, cudaStream_t s);
+
+cudaError_t launch_wait_timeout_probe(int* err, unsigned long long timeout_ns, cudaStream_t s);
+
+}  // namespace vgg
