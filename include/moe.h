@@ -211,13 +211,15 @@ int moe_profile_read(moe_ctx* ctx, int max_kernels, char* names, double* total_m
  *   D[j, c] = sum_k A[row(j), k] * B[e, c, k]      (B_kmajor = 1: B is [G, N, K])
  *   D[j, c] = sum_k A[row(j), k] * B[e, k, c]      (B_kmajor = 0: B is [G, K, N])
  * with row(j) = idx[j] (gathered, idx != NULL) or j.  A[rows_a, K] bf16,
- * D[cap, N] fp32; offsets[G+1].  A gathered row index outside the source
+ * D[cap, N] fp32; offsets[G+1].  With B_kmajor = 0, N must be a multiple of 64.  A gathered row index outside the source
  * records MOE_DEV_BAD_OFFSETS and reads zeros instead.
  *
  * moe_test_gemm_varlen_k: for each group e,
  *   D[e, m, c] = sum_{j in group e} A[rowa(j), m] * B[rowb(j), c]
  * with rowa(j) = idx_a ? idx_a[j] : j (same for b).  A[rows_a, M], B[rows_b, N] bf16,
- * D[G, M, N] fp32 (zeros for an empty group).
+ * D[G, M, N] fp32 (zeros for an empty group).  Exactly one of idx_a, idx_b is
+ * non-NULL (the gathered operand is zero past a group's end); M and N are
+ * multiples of 64.
  */
 int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, const void* B, int B_kmajor,
                            int G, int rows_a, int K, int N, long long cap, const int32_t* offsets, float* D,

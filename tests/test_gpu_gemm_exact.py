@@ -35,6 +35,8 @@ def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
     rows_a = P + 40 if gathered else cap
     A = _ints((rows_a, K), -2, 2, 1)
     idx = np.random.default_rng(2).permutation(rows_a)[:cap].astype(np.int32) if gathered else None
+    if not b_kmajor:
+        N -= N % 64  # the MN-major operand is read in 64-column chunks
     Bk = _ints((G, N, K), -1, 1, 3)  # [G, N, K]
     B = Bk if b_kmajor else np.ascontiguousarray(Bk.transpose(0, 2, 1))
     D = torch.full((cap, N), -7.0, device="cuda")
@@ -50,30 +52,35 @@ def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
     assert np.all(got[P:] == -7.0), "rows outside every group must stay untouched"
 
 
-@pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 136), ([1, 0, 333], 128, 256), ([70], 64, 320)])
-@pytest.mark.parametrize("gather_a", [False, True])
-def test_varlen_k_exact(ctx, sizes, M, N, gather_a):
+@pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 192), ([1, 0, 333], 128, 256), ([70], 64, 320)])
+@pytest.mark.parametrize("gathered", ["a", "b"])
+def test_varlen_k_exact(ctx, sizes, M, N, gathered):
+    """D[e] = sum over the group's rows j of A[rowa(j)]^T B[rowb(j)]; one operand is gathered through an
+    index (zero past the group's end), the other is read by sorted position (it runs into the next
+    group's rows, which the zero-filled gathered rows cancel)."""
     import varlen_grouped_gemm_gb300 as vgg
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     P = int(offsets[-1])
     cap = P + 3
-    Tb = P + 17
-    A = _ints((Tb if gather_a else cap, M), -2, 2, 4)
-    Bsrc = _ints((Tb, N), -2, 2, 5)
-    idx_b = np.random.default_rng(6).integers(0, Tb, size=cap).astype(np.int32)
-    idx_a = np.random.default_rng(7).integers(0, Tb, size=cap).astype(np.int32) if gather_a else None
+    Tsrc = P + 17
+    idx = np.random.default_rng(6).integers(0, Tsrc, size=cap).astype(np.int32)
+    if gathered == "a":
+        A, B = _ints((Tsrc, M), -2, 2, 4), _ints((cap, N), -2, 2, 5)
+        idx_a, idx_b = torch.from_numpy(idx).cuda(), None
+    else:
+        A, B = _ints((cap, M), -2, 2, 4), _ints((Tsrc, N), -2, 2, 5)
+        idx_a, idx_b = None, torch.from_numpy(idx).cuda()
     D = torch.full((G, M, N), 3.0, device="cuda")
-    vgg.moe_test_gemm_varlen_k(ctx, _bf(A), None if idx_a is None else torch.from_numpy(idx_a).cuda(), _bf(Bsrc),
-                               torch.from_numpy(idx_b).cuda(), torch.from_numpy(offsets).cuda(), D, cap)
+    vgg.moe_test_gemm_varlen_k(ctx, _bf(A), idx_a, _bf(B), idx_b, torch.from_numpy(offsets).cuda(), D, cap)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == 0 and code == 0
     got = D.cpu().numpy()
     for e in range(G):
         rows = np.arange(offsets[e], offsets[e + 1])
-        ra = idx_a[rows] if gather_a else rows
-        ref = A[ra].T @ Bsrc[idx_b[rows]]
-        np.testing.assert_array_equal(got[e], ref.astype(np.float32), err_msg=f"group {e}")
+        ra = idx[rows] if gathered == "a" else rows
+        rb = idx[rows] if gathered == "b" else rows
+        np.testing.assert_array_equal(got[e], (A[ra].T @ B[rb]).astype(np.float32), err_msg=f"group {e}")
 
 
 def test_bounded_wait_times_out_and_context_survives(ctx):

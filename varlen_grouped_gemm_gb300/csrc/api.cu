@@ -24,6 +24,7 @@ struct moe_ctx {
   int* d_err;
   unsigned long long timeout_ns;
   bool prof = false;
+  int l2_prefetch = 0;  // L2 prefetch of later stages (measured slower; kept switchable)
   std::vector<cudaEvent_t> pool;
   size_t pool_next = 0;
   std::vector<ProfRecord> pending;
@@ -48,28 +49,61 @@ static bool ensure_encode() {
   return true;
 }
 
+static bool encode(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* ptr, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  if (!ensure_encode()) return false;
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
                  uint32_t box_rows) {
-  if (!ensure_encode()) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride_elems * 2};
   cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool make_map_3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t groups,
                  uint32_t box_rows) {
-  if (!ensure_encode()) return false;
   cuuint64_t dims[3] = {inner, rows, groups};
   cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
   cuuint32_t box[3] = {64, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_chunked_map_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_chunks) {
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, 64, box_chunks};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_chunked_map_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t groups,
+                         uint32_t box_chunks) {
+  cuuint64_t dims[4] = {64, rows, cols / 64, groups};
+  cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
+  cuuint32_t box[4] = {64, 64, box_chunks, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_store_map_2d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_stride_elems) {
+  const uint64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_elems * es};
+  cuuint32_t box[2] = {32, 32};
+  return encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides,
+                box, fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t depth) {
+  const uint64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[3] = {cols, rows, depth};
+  cuuint64_t strides[2] = {cols * es, cols * rows * es};
+  cuuint32_t box[3] = {32, 32, 1};
+  return encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides,
+                box, fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 namespace {
@@ -135,13 +169,19 @@ GemmParams base_params(moe_ctx* ctx) {
   std::memset(&p, 0, sizeof(p));
   p.split_k = 1;
   p.a_ksplit = INT_MAX;
+  p.a_colsplit = INT_MAX;
   p.b_ksplit = INT_MAX;
   p.out_rows_split = INT_MAX;
-  p.ga.split = INT_MAX;
-  p.gb.split = INT_MAX;
   p.err = ctx->d_err;
   p.timeout_ns = ctx->timeout_ns;
+  p.l2_prefetch = ctx->l2_prefetch;
   return p;
+}
+
+Maps zero_maps() {
+  Maps m;
+  std::memset(&m, 0, sizeof(m));
+  return m;
 }
 
 bool shapes_ok(int T, int d, int E, int n, int K) {
@@ -312,16 +352,16 @@ int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, i
   p.groups = 1;
   p.out0 = logits;
   p.ld_out = E;
-  p.out_fp32 = 1;
   p.col_bias = bias;
   const int BN = gemm_bn(E);
-  CUtensorMap maps[4];
-  std::memset(maps, 0, sizeof(maps));
-  if (!make_map_2d(&maps[0], X, d, T, d, BM) || !make_map_2d(&maps[2], W_r, E, d, E, 64)) return MOE_ERR_CUDA;
-  maps[1] = maps[0];
-  maps[3] = maps[2];
+  Maps m = zero_maps();
+  if (!make_map_2d(&m.a0, X, d, T, d, BM) || !make_map_2d(&m.b0, W_r, E, d, E, 64) ||
+      !make_store_map_3d(&m.o0, logits, true, E, T, 1))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
   const int tiles = ceil_div(T, BM) * ceil_div(E, BN);
-  VGG_LAUNCH("router_logits", run_router_logits(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+  VGG_LAUNCH("router_logits", run_router_logits(BN, p, m, std::min(tiles, ctx->num_sms), s));
   VGG_LAUNCH("topk_softmax", launch_topk_softmax(logits, T, E, K, topk_ids, topk_w, scores, s));
   return MOE_OK;
 }
@@ -364,8 +404,7 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap maps[4];
-  // gate/up + SwiGLU: A = X rows gathered by sorted_tok, B = W_gate / W_up pair
+  // gate/up + SwiGLU: A = X rows gathered by sorted_tok, B = the W_gate / W_up pair
   {
     GemmParams p = base_params(ctx);
     p.N = n;
@@ -373,21 +412,22 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(X);
-    p.ga.idx = sorted_tok;
-    p.ga.ld = d;
-    p.ga.cols = d;
-    p.ga.rows = T;
+    p.a_idx = sorted_tok;
+    p.a_rows = T;
+    p.a_src = static_cast<const __nv_bfloat16*>(X);
+    p.a_ld = d;
     p.out0 = H;
     p.out1 = U;
     p.out2 = A;
     p.ld_out = n;
     const int BN = n > 64 ? 256 : 128;
-    std::memset(maps, 0, sizeof(maps));
-    if (!make_map_3d(&maps[2], W_gate, d, n, E, BN / 2) || !make_map_3d(&maps[3], W_up, d, n, E, BN / 2))
+    Maps m = zero_maps();
+    if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) ||
+        !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) || !make_store_map_2d(&m.o0, H, true, n, cap, n) ||
+        !make_store_map_2d(&m.o1, U, true, n, cap, n) || !make_store_map_2d(&m.o2, A, false, n, cap, n))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
-    VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // down projection, scaled by the combine weight of each row
   {
@@ -401,12 +441,14 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     p.ld_out = d;
     p.row_scale = sorted_w;
     const int BN = gemm_bn(d);
-    std::memset(maps, 0, sizeof(maps));
-    if (!make_map_2d(&maps[0], A, n, cap, n, BM) || !make_map_3d(&maps[2], W_down, n, d, E, BN)) return MOE_ERR_CUDA;
-    maps[1] = maps[0];
-    maps[3] = maps[2];
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
+        !make_store_map_2d(&m.o0, Yw, false, d, cap, d))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-    VGG_LAUNCH("down_scale", run_down_scale(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;
 }
@@ -444,9 +486,11 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   BwdWs w = carve_bwd(ws, T, d, E, n, cap);
-  CUtensorMap maps[4];
+  const bool f32 = dW_fp32 != 0;
   const int bn6 = gemm_bn(n);
   const int part_ld = ceil_div(n, bn6);
+  if (cap > static_cast<long long>(T) * K)
+    VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
   {
     GemmParams p = base_params(ctx);
@@ -455,11 +499,10 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(dO);
-    p.ga.idx = sorted_tok;
-    p.ga.ld = d;
-    p.ga.cols = d;
-    p.ga.rows = T;
+    p.a_idx = sorted_tok;
+    p.a_rows = T;
+    p.a_src = static_cast<const __nv_bfloat16*>(dO);
+    p.a_ld = d;
     p.in0 = static_cast<const float*>(H);
     p.in1 = static_cast<const float*>(U);
     p.ld_in = n;
@@ -470,11 +513,14 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.row_scale = sorted_w;
     p.part = w.part;
     p.part_ld = part_ld;
-    std::memset(maps, 0, sizeof(maps));
-    if (!make_map_3d(&maps[2], W_down, n, d, E, 64)) return MOE_ERR_CUDA;
-    maps[3] = maps[2];
+    Maps m = zero_maps();
+    if (!make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
+        !make_store_map_2d(&m.o0, w.dH, false, n, cap, n) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n) ||
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n))
+      return MOE_ERR_CUDA;
+    m.b1 = m.b0;
     const int tiles = (ceil_div(cap, BM) + E) * part_ld;
-    VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // dXp = [dH | dU] [W_gate[e]; W_up[e]]
   {
@@ -489,18 +535,19 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.out0 = w.dXp;
     p.ld_out = d;
     const int BN = gemm_bn(d);
-    std::memset(maps, 0, sizeof(maps));
-    if (!make_map_2d(&maps[0], w.dH, n, cap, n, BM) || !make_map_2d(&maps[1], w.dU, n, cap, n, BM) ||
-        !make_map_3d(&maps[2], W_gate, d, n, E, 64) || !make_map_3d(&maps[3], W_up, d, n, E, 64))
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, w.dH, n, cap, n, BM) || !make_map_2d(&m.a1, w.dU, n, cap, n, BM) ||
+        !make_chunked_map_3d(&m.b0, W_gate, d, n, E, BN / 64) || !make_chunked_map_3d(&m.b1, W_up, d, n, E, BN / 64) ||
+        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-    VGG_LAUNCH("dx_gemm", run_dx_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dx_gemm", run_dx_store(BN, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // per token: dS, router-logit gradient, dX
   VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
-  VGG_LAUNCH("token_backward", launch_token_backward(w.part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w, topk_ids, topk_w, K,
-                                 w.dXp, w.WrT, T, d, cap, dS, dlogits, w.dL, static_cast<__nv_bfloat16*>(dX),
-                                 ctx->d_err, s));
+  VGG_LAUNCH("token_backward", launch_token_backward(w.part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
+                                                     topk_ids, topk_w, K, w.dXp, w.WrT, T, d, cap, dS, dlogits, w.dL,
+                                                     static_cast<__nv_bfloat16*>(dX), ctx->d_err, s));
   // dW_r = X^T dlogits, split over tokens
   {
     GemmParams p = base_params(ctx);
@@ -513,18 +560,19 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK));
     split = std::max(1, std::min(split, ceil_div(T, 8 * BK)));
     p.split_k = split;
-    p.out0 = split == 1 ? static_cast<void*>(dW_r) : static_cast<void*>(w.wr_part);
+    float* dst = split == 1 ? dW_r : w.wr_part;
+    p.out0 = dst;
     p.ld_out = E;
-    p.group_stride_out = static_cast<long long>(d) * E;
-    p.out_fp32 = 1;
-    std::memset(maps, 0, sizeof(maps));
-    if (!make_map_2d(&maps[0], X, d, T, d, 64) || !make_map_2d(&maps[2], w.dL, E, T, E, 64)) return MOE_ERR_CUDA;
-    maps[1] = maps[0];
-    maps[3] = maps[2];
-    VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, maps, std::min(tiles * split, ctx->num_sms), s));
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, X, d, T, d, 64) || !make_map_2d(&m.b0, w.dL, E, T, E, 64) ||
+        !make_store_map_3d(&m.o0, dst, true, E, d, split))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
     if (split > 1) VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
   }
-  // varlen-K weight gradients
+  // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok]
   {
     GemmParams p = base_params(ctx);
     p.M = 2 * n;
@@ -532,28 +580,25 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.ga.ptr0 = w.dH;
-    p.ga.ptr1 = w.dU;
-    p.ga.split = n;
-    p.ga.ld = n;
-    p.ga.cols = 2 * n;
-    p.ga.rows = cap;
-    p.gb.ptr0 = static_cast<const __nv_bfloat16*>(X);
-    p.gb.idx = sorted_tok;
-    p.gb.ld = d;
-    p.gb.cols = d;
-    p.gb.rows = T;
+    p.a_colsplit = n;
+    p.b_idx = sorted_tok;
+    p.b_rows = T;
+    p.b_src = static_cast<const __nv_bfloat16*>(X);
+    p.b_ld = d;
     p.out0 = dW_gate;
     p.out1 = dW_up;
     p.out_rows_split = n;
     p.ld_out = d;
-    p.group_stride_out = static_cast<long long>(n) * d;
-    p.out_fp32 = dW_fp32 ? 1 : 0;
     const int BN = gemm_bn(d);
-    std::memset(maps, 0, sizeof(maps));
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
+        !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E) ||
+        !make_store_map_3d(&m.o1, dW_up, f32, d, n, E))
+      return MOE_ERR_CUDA;
     const int tiles = E * ceil_div(2 * n, BM) * ceil_div(d, BN);
-    VGG_LAUNCH("dw_gate_up", run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_gate_up", run_dw_gate_up(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
   }
+  // dW_down[e] = (w dO[tok])^T A  (the weight is folded into A')
   {
     GemmParams p = base_params(ctx);
     p.M = d;
@@ -561,23 +606,21 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.ga.ptr0 = static_cast<const __nv_bfloat16*>(dO);
-    p.ga.idx = sorted_tok;
-    p.ga.ld = d;
-    p.ga.cols = d;
-    p.ga.rows = T;
-    p.gb.ptr0 = w.Ap;
-    p.gb.ld = n;
-    p.gb.cols = n;
-    p.gb.rows = cap;
+    p.a_idx = sorted_tok;
+    p.a_rows = T;
+    p.a_src = static_cast<const __nv_bfloat16*>(dO);
+    p.a_ld = d;
     p.out0 = dW_down;
     p.ld_out = n;
-    p.group_stride_out = static_cast<long long>(d) * n;
-    p.out_fp32 = dW_fp32 ? 1 : 0;
     const int BN = gemm_bn(n);
-    std::memset(maps, 0, sizeof(maps));
+    Maps m = zero_maps();
+    p.b_chunked = 1;
+    if (!make_chunked_map_2d(&m.b0, w.Ap, n, cap, BN / 64) ||
+        !make_store_map_3d(&m.o0, dW_down, f32, n, d, E))
+      return MOE_ERR_CUDA;
+    m.b1 = m.b0;
     const int tiles = E * ceil_div(d, BM) * ceil_div(n, BN);
-    VGG_LAUNCH("dw_down", run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_down", run_dw_down(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;
 }
@@ -596,26 +639,24 @@ int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, cons
   p.groups = G;
   p.offsets = offsets;
   p.rows_cap = static_cast<int>(cap);
-  p.ga.ptr0 = static_cast<const __nv_bfloat16*>(A);
-  p.ga.idx = idx;
-  p.ga.ld = K;
-  p.ga.cols = K;
-  p.ga.rows = rows_a;
+  p.a_idx = idx;
+  p.a_rows = rows_a;
+  p.a_src = static_cast<const __nv_bfloat16*>(A);
+  p.a_ld = K;
   p.out0 = D;
   p.ld_out = N;
-  p.out_fp32 = 1;
-  CUtensorMap maps[4];
-  std::memset(maps, 0, sizeof(maps));
-  if (!idx && !make_map_2d(&maps[0], A, K, rows_a, K, BM)) return MOE_ERR_CUDA;
-  maps[1] = maps[0];
+  Maps m = zero_maps();
+  if (!idx && !make_map_2d(&m.a0, A, K, rows_a, K, BM)) return MOE_ERR_CUDA;
+  m.a1 = m.a0;
   if (B_kmajor) {
-    if (!make_map_3d(&maps[2], B, K, N, G, 128)) return MOE_ERR_CUDA;
+    if (!make_map_3d(&m.b0, B, K, N, G, 128)) return MOE_ERR_CUDA;
   } else {
-    if (!make_map_3d(&maps[2], B, N, K, G, 64)) return MOE_ERR_CUDA;
+    if (N % 64 || !make_chunked_map_3d(&m.b0, B, N, K, G, 2)) return MOE_ERR_CUDA;
   }
-  maps[3] = maps[2];
+  m.b1 = m.b0;
+  if (!make_store_map_2d(&m.o0, D, true, N, cap, N)) return MOE_ERR_CUDA;
   const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 128);
-  return cuda_status(run_test_m(idx != nullptr, B_kmajor, p, maps, std::min(tiles, ctx->num_sms),
+  return cuda_status(run_test_m(idx != nullptr, B_kmajor, p, m, std::min(tiles, ctx->num_sms),
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -623,7 +664,8 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
                            const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
                            const int32_t* offsets, float* D, moe_stream_t stream) {
   VGG_REQUIRE(ctx && A && B && offsets && D);
-  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 8 && M % 8 == 0 && N >= 8 && N % 8 == 0 && rows_a >= 1 &&
+  VGG_REQUIRE((idx_a == nullptr) != (idx_b == nullptr));  // exactly one operand is gathered
+  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 64 && M % 64 == 0 && N >= 64 && N % 64 == 0 && rows_a >= 1 &&
               rows_b >= 1);
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX && aligned16(A) && aligned16(B) && aligned16(D));
   DeviceGuard g(ctx->device);
@@ -634,25 +676,28 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
   p.groups = G;
   p.offsets = offsets;
   p.rows_cap = static_cast<int>(cap);
-  p.ga.ptr0 = static_cast<const __nv_bfloat16*>(A);
-  p.ga.idx = idx_a;
-  p.ga.ld = M;
-  p.ga.cols = M;
-  p.ga.rows = rows_a;
-  p.gb.ptr0 = static_cast<const __nv_bfloat16*>(B);
-  p.gb.idx = idx_b;
-  p.gb.ld = N;
-  p.gb.cols = N;
-  p.gb.rows = rows_b;
+  p.a_idx = idx_a;
+  p.a_rows = rows_a;
+  p.a_src = static_cast<const __nv_bfloat16*>(A);
+  p.a_ld = M;
+  p.b_idx = idx_b;
+  p.b_rows = rows_b;
+  p.b_chunked = 1;
+  p.b_src = static_cast<const __nv_bfloat16*>(B);
+  p.b_ld = N;
   p.out0 = D;
   p.ld_out = N;
-  p.group_stride_out = static_cast<long long>(M) * N;
-  p.out_fp32 = 1;
-  CUtensorMap maps[4];
-  std::memset(maps, 0, sizeof(maps));
   const int BN = gemm_bn(N);
+  Maps m = zero_maps();
+  if ((!idx_a && !make_map_2d(&m.a0, A, M, rows_a, M, 64)) || (!idx_b && !make_chunked_map_2d(&m.b0, B, N, rows_b, BN / 64)) ||
+      !make_store_map_3d(&m.o0, D, true, N, M, G))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
   const int tiles = G * ceil_div(M, BM) * ceil_div(N, BN);
-  return cuda_status(run_varlen_k_store(BN, p, maps, std::min(tiles, ctx->num_sms), static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = std::min(tiles, ctx->num_sms);
+  return cuda_status(idx_b ? run_dw_gate_up(BN, true, p, m, grid, s) : run_dw_down(BN, true, p, m, grid, s));
 }
 
 int moe_profile_enable(moe_ctx* ctx, int enable) {

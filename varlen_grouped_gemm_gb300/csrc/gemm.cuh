@@ -4,14 +4,17 @@
 //
 // One CTA per SM walks a static round-robin list of output tiles.  Warp roles:
 //   warps 0-3  epilogue: tcgen05.ld of the accumulator (row i of the tile = TMEM lane i),
-//              fused elementwise work, global stores;
-//   warps 4-7  cp.async producers for operands whose rows are gathered through an
-//              index (token gather fused into the operand load) or whose reduction
-//              length varies per group (zero-filled past the group's end);
-//   warp  8    TMA producer (one thread) for dense operands; owns the TMEM allocation;
-//   warp  9    UMMA issuer (one thread).
+//              fused elementwise work, results staged in shared memory per 32-row block
+//              and written by TMA stores;
+//   warp  4    TMA producer (one thread) for dense operands, with an L2 prefetch of the
+//              boxes a few stages ahead; owns the TMEM allocation;
+//   warp  5    UMMA issuer (one thread);
+//   warps 6-9  present when an operand's rows are gathered through a token index: they
+//              copy those rows with cp.async (16 B per thread, zero-filled past the end)
+//              straight into the swizzled stage, so the permuted activations are never
+//              written ([SM] "4.1 Gather 융합"); the index lookups run two stages ahead.
 // Shared memory holds STAGES ring slots of A (128 x 64) and B (BN x 64) in the
-// 128-byte-swizzled layout that both TMA and the UMMA descriptors use.  TMEM
+// 128-byte-swizzled layout that TMA writes and the UMMA descriptors read.  TMEM
 // holds two BN-column accumulators so that the epilogue of tile i overlaps the
 // main loop of tile i+1 ([SM] "4.3 MMA ↔ IO 오버랩": TMEM split in two halves,
 // one accumulating while the other drains).
@@ -20,7 +23,8 @@
 //   VAR_M    groups = experts, rows of group g are sorted rows [off[g], off[g+1]);
 //            K and N fixed ([GG] "Variable-M batched matmul").
 //   VAR_K    groups = experts, the reduction runs over the group's rows; M and N
-//            fixed; an empty group writes zeros ([SM] "4 기여 ②": varlen-K).
+//            fixed; rows past the group's end enter as zeros through the gathered
+//            operand's out-of-range fill; an empty group writes zeros ([SM] "4 기여 ②").
 //   VAR_NONE one dense problem, K optionally split across CTAs (partials per split).
 #pragma once
 
@@ -32,24 +36,17 @@ namespace vgg {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 320;
+constexpr int kMaxThreads = 320;  // 6 warps + 4 gather warps when an operand is gathered
 constexpr int kMaxGroups = 1024;
+constexpr int kStgBuf = 4096;    // one staged store: 32 rows x 128 B
+constexpr int kStgDepth = 1;     // staged stores in flight per epilogue warp
+constexpr int kStgBytes = kStgBuf * kStgDepth;
+constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 this many stages ahead
 
-enum AMode { A_TMA_K = 0, A_CP_K = 1, A_CP_MN = 2, A_TMA_MN = 3 };
-enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_CP_MN = 4 };
+enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
+enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3 };
-
-// A row-gathered (or row-predicated) operand read with cp.async.
-struct GatherSrc {
-  const __nv_bfloat16* ptr0;
-  const __nv_bfloat16* ptr1;  // columns >= split are read from ptr1 at (col - split)
-  const int* idx;             // sorted position -> source row; null = identity
-  long long ld;               // row stride in elements
-  int split;                  // column split between ptr0 and ptr1
-  int cols;                   // valid columns of the operand's MN extent
-  long long rows;             // rows of the source; a gathered row index outside [0, rows) is an error
-};
 
 struct GemmParams {
   int M, N, K;
@@ -57,18 +54,27 @@ struct GemmParams {
   const int* offsets;  // [groups + 1], device
   int rows_cap;        // offsets[groups] must not exceed this
   int split_k;         // VAR_NONE: number of K splits
-  int a_ksplit;        // TMA A: k < a_ksplit from map 0, else map 1 at k - a_ksplit
-  int b_ksplit;        // TMA B: same for B
-  GatherSrc ga, gb;
-  void* out0;
+  int a_ksplit;        // A_TMA_K: k < a_ksplit from map a0, else map a1 at k - a_ksplit
+  int a_colsplit;      // A_TMA_MN: columns < split from map a0, else a1 at col - split
+  int b_ksplit;        // B_TMA_MN3: k < b_ksplit from map b0, else b1 at k - b_ksplit
+  int b_chunked;       // B_TMA_MN2: the map is the chunked 3-D view (one load per stage)
+  int l2_prefetch;     // prefetch the tiled operands of later stages into L2
+  const int* a_idx;    // gathered A: sorted position -> source row
+  int a_rows;          // rows of the gathered A source
+  const __nv_bfloat16* a_src;  // gathered A source [a_rows][a_ld]
+  long long a_ld;
+  const int* b_idx;
+  int b_rows;
+  const __nv_bfloat16* b_src;
+  long long b_ld;
+  // epilogue
+  void* out0;  // direct-store pointers (used for a partially filled 32-row block)
   void* out1;
   void* out2;
   long long ld_out;
-  long long group_stride_out;  // VAR_K: per group; VAR_NONE: per K split
-  int out_rows_split;          // VAR_K: output rows >= split go to out1 at row - split
-  int out_fp32;
+  int out_rows_split;  // VAR_K: output rows >= split go to the second output at row - split
   const float* row_scale;  // VAR_M: per sorted row (combine weight)
-  const float* in0;  // dSwiGLU epilogue: H, U (fp32)
+  const float* in0;        // dSwiGLU epilogue: H, U (fp32)
   const float* in1;
   long long ld_in;
   float* part;  // dSwiGLU epilogue: per-row partial dot products [rows][part_ld]
@@ -78,13 +84,19 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
+// Tensor maps: a0/a1 and b0/b1 feed the operands, o0..o2 are the TMA-store targets.
+struct Maps {
+  CUtensorMap a0, a1, b0, b1, o0, o1, o2;
+};
+
 template <int BN, int STAGES>
 struct SmemLayout {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBarOffset = STAGES * kStageBytes;
-  static constexpr int kNumBars = 3 * STAGES + 5;
+  static constexpr int kStgOffset = STAGES * kStageBytes;
+  static constexpr int kBarOffset = kStgOffset + 4 * kStgBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr size_t bytes(int groups) {
     return 1024 + static_cast<size_t>(kMiscOffset) + 16 + 8 * static_cast<size_t>(groups + 2);
@@ -171,6 +183,36 @@ struct Sched {
   }
 };
 
+// A (tile, k-stage) position of the persistent loop; only tiles with a non-empty reduction have stages.
+struct Pos {
+  int t, ks, nk;
+  Tile tl;
+};
+
+template <class S>
+__device__ __forceinline__ void pos_next(const S& sch, const GemmParams& p, int& gcur, Pos& q) {
+  if (q.ks + 1 < q.nk) {
+    ++q.ks;
+    return;
+  }
+  q.ks = 0;
+  for (q.t += gridDim.x; q.t < sch.total; q.t += gridDim.x) {
+    sch.decode(p, q.t, gcur, q.tl);
+    q.nk = (q.tl.k_len + BK - 1) / BK;
+    if (q.nk > 0) return;
+  }
+}
+
+template <class S>
+__device__ __forceinline__ Pos pos_first(const S& sch, const GemmParams& p, int& gcur) {
+  Pos q;
+  q.t = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+  q.ks = 0;
+  q.nk = 0;
+  pos_next(sch, p, gcur, q);
+  return q;
+}
+
 // Byte offset of the 16-byte piece (row r, piece c16) of a 128-byte-swizzled [rows x 128 B] block.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c16) {
   return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
@@ -178,14 +220,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c16) {
 
 // -------------------------------------------------------------------------- epilogue helpers
 
-__device__ __forceinline__ void store_row_chunk(void* base, long long elem_off, const float (&v)[32], int ncols,
-                                                int fp32) {
+// Direct per-thread store of 32 consecutive columns of one row (used for a partial 32-row block).
+__device__ __forceinline__ void store_row32(void* base, long long elem_off, const float (&v)[32], int ncols, bool fp32) {
   if (fp32) {
     float* o = reinterpret_cast<float*>(base) + elem_off;
     if (ncols >= 32) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -211,7 +252,7 @@ __device__ __forceinline__ void store_row_chunk(void* base, long long elem_off, 
   }
 }
 
-__device__ __forceinline__ void load_f32_chunk(const float* src, float (&v)[32], int ncols) {
+__device__ __forceinline__ void load_f32_row32(const float* src, float (&v)[32], int ncols) {
   if (ncols >= 32) {
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -224,39 +265,53 @@ __device__ __forceinline__ void load_f32_chunk(const float* src, float (&v)[32],
   }
 }
 
-__device__ __forceinline__ void load_bf16_chunk(const __nv_bfloat16* src, float (&v)[32], int ncols) {
-  if (ncols >= 32) {
+// Write this thread's 32 values as row r of the warp's staging block, in the swizzled layout of
+// the store map: fp32 rows of 128 B (128-byte swizzle), bf16 rows of 64 B (64-byte swizzle).
+__device__ __forceinline__ void stage_row32(uint8_t* stg, int r, const float (&v)[32], bool fp32) {
+  if (fp32) {
+    uint8_t* row = stg + r * 128;
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      uint4 q = *reinterpret_cast<const uint4*>(src + i);
-      float2 a = unpack_bf16x2(q.x), b = unpack_bf16x2(q.y), c = unpack_bf16x2(q.z), d = unpack_bf16x2(q.w);
-      v[i] = a.x; v[i + 1] = a.y; v[i + 2] = b.x; v[i + 3] = b.y;
-      v[i + 4] = c.x; v[i + 5] = c.y; v[i + 6] = d.x; v[i + 7] = d.y;
-    }
+    for (int p = 0; p < 8; ++p)
+      *reinterpret_cast<float4*>(row + ((p ^ (r & 7)) << 4)) = make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
   } else {
+    uint8_t* row = stg + r * 64;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = (i < ncols) ? __bfloat162float(src[i]) : 0.0f;
+    for (int p = 0; p < 4; ++p) {
+      uint4 q;
+      q.x = pack_bf16x2(v[8 * p], v[8 * p + 1]);
+      q.y = pack_bf16x2(v[8 * p + 2], v[8 * p + 3]);
+      q.z = pack_bf16x2(v[8 * p + 4], v[8 * p + 5]);
+      q.w = pack_bf16x2(v[8 * p + 6], v[8 * p + 7]);
+      *reinterpret_cast<uint4*>(row + ((p ^ ((r >> 1) & 3)) << 4)) = q;
+    }
   }
 }
 
+// Target of one epilogue store: a TMA map and coordinates for full 32-row blocks, a pointer
+// and row offset for the direct path.
+struct OutRef {
+  const CUtensorMap* map;
+  void* ptr;
+  long long row_off;  // element offset of this thread's row (direct path)
+  int c_row;          // TMA row coordinate of the warp's first row
+  int c_z;            // TMA third coordinate (group / split), -1 = 2-D map
+};
+
 // -------------------------------------------------------------------------- the kernel
 
-template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA0,
-                        const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1) {
+template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
   using L = SmemLayout<BN, STAGES>;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != EPI_SWIGLU || BMODE == B_TMA_K3_GU, "SwiGLU epilogue needs the gate/up pair layout");
-  constexpr bool kACp = (AMODE == A_CP_K || AMODE == A_CP_MN);
-  constexpr bool kBCp = (BMODE == B_CP_MN);
-  constexpr bool kAnyCp = kACp || kBCp;
-  constexpr bool kATma = !kACp;
-  constexpr bool kBTma = !kBCp;
-  constexpr bool kAMn = (AMODE == A_CP_MN || AMODE == A_TMA_MN);
-  constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_CP_MN);
-  constexpr uint32_t kTxBytes = (kATma ? L::kABytes : 0) + (kBTma ? L::kBBytes : 0);
+  constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
+  constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_GATHER_MN);
+  constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
+  constexpr bool kBGather = (BMODE == B_GATHER_MN);
+  constexpr bool kGather = kAGather || kBGather;
+  constexpr int kThreads = kGather ? 320 : 192;
+  constexpr uint32_t kTxBytes = (kAGather ? 0 : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
@@ -280,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], (kAnyCp ? 128u : 0u) + (kATma || kBTma ? 1u : 0u));
+      mbar_init(&full_bar[s], 1 + (kGather ? 128 : 0));
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -292,17 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_bad = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 4) {
     tmem_alloc(s_tmem, kTmemCols);
     if (lane == 0) {
-      if (kATma) {
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmA1);
-      }
-      if (kBTma) {
-        tma_prefetch_desc(&tmB0);
-        tma_prefetch_desc(&tmB1);
-      }
+      if (!kAGather) tma_prefetch_desc(&mp.a0);
+      if (!kBGather) tma_prefetch_desc(&mp.b0);
     }
   }
   // group offsets into shared memory (validated: start at 0, monotone, within capacity)
@@ -353,50 +402,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   sch.init(p, s_off, s_tile);
   if (*s_bad) sch.total = 0;
 
-  if (warp == 8) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && (kATma || kBTma)) {
-      int it = 0, gcur = 0;
-      bool aborted = false;
-      for (int t = blockIdx.x; t < sch.total && !aborted; t += gridDim.x) {
-        Tile tl;
-        sch.decode(p, t, gcur, tl);
-        const int nk = (tl.k_len + BK - 1) / BK;
-        for (int ks = 0; ks < nk; ++ks, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err)) {
-            aborted = true;
-            break;
-          }
-          uint8_t* sa = smem + s * L::kStageBytes;
-          uint8_t* sb = sa + L::kABytes;
-          mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
-          const int kg = tl.k_begin + ks * BK;
-          if (AMODE == A_TMA_K) {
-            const int row = (VAR == VAR_M ? s_off[tl.g] : 0) + tl.m0;
-            if (kg < p.a_ksplit) tma_load_2d(sa, &tmA0, &full_bar[s], kg, row);
-            else tma_load_2d(sa, &tmA1, &full_bar[s], kg - p.a_ksplit, row);
-          } else if (AMODE == A_TMA_MN) {
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer (one thread)
+    if (lane == 0) {
+      // Expert weights are read by the few tiles of one expert and then never again: stream them
+      // through L2 (evict first) so that the gathered activations stay resident.
+      const uint64_t pol_stream = l2_policy_evict_first();
+      // Loads (or, with l2 = true, L2 prefetches) of the tiled operands of one stage.
+      auto tiled = [&](const Tile& x, int kstage, uint8_t* sa, uint8_t* sb, uint64_t* bar, bool l2) {
+        const int kg = x.k_begin + kstage * BK;
+        if (AMODE == A_TMA_K) {
+          const int row = (VAR == VAR_M ? s_off[x.g] : 0) + x.m0;
+          const CUtensorMap* mp_a = kg < p.a_ksplit ? &mp.a0 : &mp.a1;
+          const int kc = kg < p.a_ksplit ? kg : kg - p.a_ksplit;
+          if (l2) tma_prefetch_l2_2d(mp_a, kc, row);
+          else tma_load_2d(sa, mp_a, bar, kc, row);
+        } else if (AMODE == A_TMA_MN) {
 #pragma unroll
-            for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * (BK * 128), &tmA0, &full_bar[s], tl.m0 + 64 * c, kg);
-          }
-          if (BMODE == B_TMA_K3) {
-            tma_load_3d(sb, &tmB0, &full_bar[s], kg, tl.n0, tl.g);
-          } else if (BMODE == B_TMA_K3_GU) {
-            tma_load_3d(sb, &tmB0, &full_bar[s], kg, tl.n0, tl.g);
-            tma_load_3d(sb + (BN / 2) * 128, &tmB1, &full_bar[s], kg, tl.n0, tl.g);
-          } else if (BMODE == B_TMA_MN3) {
-            const bool first = kg < p.b_ksplit;
-            const int kc = first ? kg : kg - p.b_ksplit;
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_3d(sb + c * (BK * 128), first ? &tmB0 : &tmB1, &full_bar[s], tl.n0 + 64 * c, kc, tl.g);
-          } else if (BMODE == B_TMA_MN2) {
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * (BK * 128), &tmB0, &full_bar[s], tl.n0 + 64 * c, kg);
+          for (int c = 0; c < BM / 64; ++c) {
+            const int col = x.m0 + 64 * c;
+            const CUtensorMap* mp_a = col < p.a_colsplit ? &mp.a0 : &mp.a1;
+            const int cc = col < p.a_colsplit ? col : col - p.a_colsplit;
+            if (l2) tma_prefetch_l2_2d(mp_a, cc, kg);
+            else tma_load_2d(sa + c * (BK * 128), mp_a, bar, cc, kg);
           }
         }
+        if (BMODE == B_TMA_K3) {
+          if (l2) tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
+          else tma_load_3d_hint(sb, &mp.b0, bar, kg, x.n0, x.g, pol_stream);
+        } else if (BMODE == B_TMA_K3_GU) {
+          if (l2) {
+            tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
+            tma_prefetch_l2_3d(&mp.b1, kg, x.n0, x.g);
+          } else {
+            tma_load_3d_hint(sb, &mp.b0, bar, kg, x.n0, x.g, pol_stream);
+            tma_load_3d_hint(sb + (BN / 2) * 128, &mp.b1, bar, kg, x.n0, x.g, pol_stream);
+          }
+        } else if (BMODE == B_TMA_MN3) {
+          // 4-D view {64 columns, K rows, N/64 chunks, groups}: every 64-column chunk of the stage in one box
+          const bool first = kg < p.b_ksplit;
+          const int kc = first ? kg : kg - p.b_ksplit;
+          if (l2) tma_prefetch_l2_4d(first ? &mp.b0 : &mp.b1, 0, kc, x.n0 / 64, x.g);
+          else tma_load_4d_hint(sb, first ? &mp.b0 : &mp.b1, bar, 0, kc, x.n0 / 64, x.g, pol_stream);
+        } else if (BMODE == B_TMA_MN2) {
+          if (p.b_chunked) {  // 3-D view {64 columns, rows, N/64 chunks}
+            if (l2) tma_prefetch_l2_3d(&mp.b0, 0, kg, x.n0 / 64);
+            else tma_load_3d(sb, &mp.b0, bar, 0, kg, x.n0 / 64);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) {
+              if (l2) tma_prefetch_l2_2d(&mp.b0, x.n0 + 64 * c, kg);
+              else tma_load_2d(sb + c * (BK * 128), &mp.b0, bar, x.n0 + 64 * c, kg);
+            }
+          }
+        }
+      };
+      int it = 0, gcur = 0;
+      bool aborted = false;
+      Pos q = pos_first(sch, p, gcur);
+      while (q.t < sch.total && !aborted) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err)) {
+          aborted = true;
+          break;
+        }
+        uint8_t* sa = smem + s * L::kStageBytes;
+        uint8_t* sb = sa + L::kABytes;
+        if (kTxBytes > 0) {
+          mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
+          tiled(q.tl, q.ks, sa, sb, &full_bar[s], false);
+          // L2 prefetch of the stages ahead of this one within the tile
+          if (!p.l2_prefetch) {
+          } else if (q.ks == 0) {
+            for (int k2 = 1; k2 <= kPrefetchStages && k2 < q.nk; ++k2) tiled(q.tl, k2, sa, sb, nullptr, true);
+          } else if (q.ks + kPrefetchStages < q.nk) {
+            tiled(q.tl, q.ks + kPrefetchStages, sa, sb, nullptr, true);
+          }
+        } else {
+          mbar_arrive(&full_bar[s]);
+        }
+        ++it;
+        pos_next(sch, p, gcur, q);
       }
       if (aborted) {
         // let copies already in flight land before the CTA goes away
@@ -405,103 +492,117 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------------- cp.async producers
-    if (kAnyCp) {
-      const int ptid = tid - 128;
-      int it = 0, gcur = 0;
-      bool aborted = false;
-      for (int t = blockIdx.x; t < sch.total && !aborted; t += gridDim.x) {
-        Tile tl;
-        sch.decode(p, t, gcur, tl);
-        const int nk = (tl.k_len + BK - 1) / BK;
-        // A gathered along M: the tile's 8 rows handled by this thread are fixed for the whole tile
-        long long arow[8];
-        bool aval[8];
-        if (AMODE == A_CP_K) {
+  } else if (kGather && warp >= 6) {
+    // ---------------------------------------------------------------- cp.async gather producers
+    // Thread ptid owns the 16-byte piece c16 of rows rsub + 16 i of every stage.  The token
+    // indices of a position are loaded two positions ahead of its copies.
+    const int ptid = tid - 192;
+    const int c16 = ptid & 7;
+    const int rsub = ptid >> 3;
+    const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
+    auto fetch = [&](const Pos& x, int (&r)[8], const Pos& prev, const int (&pr)[8]) {
+      if (AMODE == A_GATHER_K) {
+        if (x.t == prev.t) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[i] = pr[i];
+        } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int r = (ptid >> 3) + 16 * i;
-            aval[i] = r < tl.rows;
-            const int srow = s_off[tl.g] + tl.m0 + r;
-            arow[i] = aval[i] ? (p.ga.idx ? __ldg(p.ga.idx + srow) : srow) : 0;
-            if (arow[i] < 0 || arow[i] >= p.ga.rows) {
-              if (aval[i]) set_error(p.err, DERR_BAD_OFFSETS);
-              aval[i] = false;
-              arow[i] = 0;
-            }
+            const int rr = rsub + 16 * i;
+            r[i] = rr < x.tl.rows ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
           }
         }
-        for (int ks = 0; ks < nk; ++ks, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err)) {
-            aborted = true;
-            break;
-          }
-          const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
-          const uint32_t sb = sa + L::kABytes;
-          const int c16 = ptid & 7;
-          if (AMODE == A_CP_K) {
-            const int kc = ks * BK + c16 * 8;
+      } else {
+        const int* idx = kAGather ? p.a_idx : p.b_idx;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = (ptid >> 3) + 16 * i;
-              const __nv_bfloat16* src = p.ga.ptr0 + arow[i] * p.ga.ld + kc;
-              cp_async_16(sa + sw128_offset(r, c16), aval[i] ? src : p.ga.ptr0, aval[i] ? 16u : 0u);
-            }
-          } else if (AMODE == A_CP_MN) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int chunk = i >> 2;
-              const int r = (ptid >> 3) + 16 * (i & 3);
-              const int kr = ks * BK + r;
-              const int col = tl.m0 + 64 * chunk + c16 * 8;
-              bool ok = kr < tl.k_len && col < p.ga.cols;
-              const __nv_bfloat16* src = p.ga.ptr0;
-              if (ok) {
-                const int srow = tl.k_begin + kr;
-                const long long row = p.ga.idx ? __ldg(p.ga.idx + srow) : srow;
-                if (row < 0 || row >= p.ga.rows) {
-                  set_error(p.err, DERR_BAD_OFFSETS);
-                  ok = false;
-                } else {
-                  src = (col < p.ga.split) ? p.ga.ptr0 + row * p.ga.ld + col
-                                           : p.ga.ptr1 + row * p.ga.ld + (col - p.ga.split);
-                }
-              }
-              cp_async_16(sa + chunk * (BK * 128) + sw128_offset(r, c16), src, ok ? 16u : 0u);
-            }
-          }
-          if (BMODE == B_CP_MN) {
-#pragma unroll
-            for (int i = 0; i < 4 * (BN / 64); ++i) {
-              const int chunk = i >> 2;
-              const int r = (ptid >> 3) + 16 * (i & 3);
-              const int kr = ks * BK + r;
-              const int col = tl.n0 + 64 * chunk + c16 * 8;
-              bool ok = kr < tl.k_len && col < p.gb.cols;
-              const __nv_bfloat16* src = p.gb.ptr0;
-              if (ok) {
-                const int srow = tl.k_begin + kr;
-                const long long row = p.gb.idx ? __ldg(p.gb.idx + srow) : srow;
-                if (row < 0 || row >= p.gb.rows) {
-                  set_error(p.err, DERR_BAD_OFFSETS);
-                  ok = false;
-                } else {
-                  src = (col < p.gb.split) ? p.gb.ptr0 + row * p.gb.ld + col
-                                           : p.gb.ptr1 + row * p.gb.ld + (col - p.gb.split);
-                }
-              }
-              cp_async_16(sb + chunk * (BK * 128) + sw128_offset(r, c16), src, ok ? 16u : 0u);
-            }
-          }
-          cp_async_mbar_arrive_noinc(&full_bar[s]);
+        for (int j = 0; j < 4; ++j) {
+          const int kr = x.ks * BK + rsub + 16 * j;
+          r[j] = kr < x.tl.k_len ? __ldg(idx + x.tl.k_begin + kr) : -1;
         }
       }
-      cp_async_wait_all();
+    };
+    int it = 0, gcur = 0;
+    bool aborted = false;
+    int r0[8], r1[8], r2[8];
+    Pos q0 = pos_first(sch, p, gcur), q1 = q0, q2 = q0;
+    Pos none;
+    none.t = -1;
+    if (q0.t < sch.total) fetch(q0, r0, none, r0);
+    pos_next(sch, p, gcur, q1);
+    if (q1.t < sch.total) fetch(q1, r1, q0, r0);
+    q2 = q1;
+    pos_next(sch, p, gcur, q2);
+    if (q2.t < sch.total) fetch(q2, r2, q1, r1);
+    while (q0.t < sch.total && !aborted) {
+      const int s = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      if (!mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err)) {
+        aborted = true;
+        break;
+      }
+      const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
+      const uint32_t sb = sa + L::kABytes;
+      if (AMODE == A_GATHER_K) {
+        const int kc = q0.tl.k_begin + q0.ks * BK + c16 * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const long long row = r0[i];
+          bool ok = row >= 0;
+          if (ok && row >= p.a_rows) {
+            set_error(p.err, DERR_BAD_OFFSETS);
+            ok = false;
+          }
+          cp_async_16_hint(sa + sw128_offset(rsub + 16 * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src, ok ? 16u : 0u,
+                           pol_keep);
+        }
+      } else if (AMODE == A_GATHER_MN) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int chunk = i >> 2, j = i & 3;
+          const int col = q0.tl.m0 + 64 * chunk + c16 * 8;
+          const long long row = r0[j];
+          bool ok = row >= 0 && col < p.M;
+          if (ok && row >= p.a_rows) {
+            set_error(p.err, DERR_BAD_OFFSETS);
+            ok = false;
+          }
+          cp_async_16_hint(sa + chunk * (BK * 128) + sw128_offset(rsub + 16 * j, c16),
+                           ok ? p.a_src + row * p.a_ld + col : p.a_src, ok ? 16u : 0u, pol_keep);
+        }
+      }
+      if (BMODE == B_GATHER_MN) {
+#pragma unroll
+        for (int i = 0; i < 4 * (BN / 64); ++i) {
+          const int chunk = i >> 2, j = i & 3;
+          const int col = q0.tl.n0 + 64 * chunk + c16 * 8;
+          const long long row = r0[j];
+          bool ok = row >= 0 && col < p.N;
+          if (ok && row >= p.b_rows) {
+            set_error(p.err, DERR_BAD_OFFSETS);
+            ok = false;
+          }
+          cp_async_16_hint(sb + chunk * (BK * 128) + sw128_offset(rsub + 16 * j, c16),
+                           ok ? p.b_src + row * p.b_ld + col : p.b_src, ok ? 16u : 0u, pol_keep);
+        }
+      }
+      cp_async_mbar_arrive_noinc(&full_bar[s]);
+      ++it;
+      // rotate the index pipeline
+      q0 = q1;
+      q1 = q2;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        r0[i] = r1[i];
+        r1[i] = r2[i];
+      }
+      if (q2.t < sch.total) {
+        const Pos prev = q2;
+        pos_next(sch, p, gcur, q2);
+        if (q2.t < sch.total) fetch(q2, r2, prev, r1);
+      }
     }
-  } else if (warp == 9) {
+    cp_async_wait_all();
+  } else if (warp == 5) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
       int it = 0, acc = 0, gcur = 0;
@@ -524,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             aborted = true;
             break;
           }
-          if (kAnyCp) fence_proxy_async_smem();
+          if (kGather) fence_proxy_async_smem();  // cp.async writes -> UMMA operand reads
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
           const uint32_t sb = sa + L::kABytes;
@@ -545,10 +646,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
+    uint8_t* stg_base = smem + L::kStgOffset + warp * kStgBytes;
+    int stg_i = 0;  // ring position: a buffer is rewritten only after the store kStgDepth-1 back has read it
     int acc = 0, gcur = 0;
     const int row_local = warp * 32 + lane;
+    // Emit 32 columns of this thread's row to `o`: a staged TMA store when all 32 rows of the
+    // warp belong to the output, else a direct store of each valid row.
+    auto emit = [&](const OutRef& o, const float (&v)[32], int col, int ncols, bool full, bool row_ok, bool fp32) {
+      if (ncols <= 0) return;
+      if (full) {
+        uint8_t* stg = stg_base + (stg_i % kStgDepth) * kStgBuf;
+        ++stg_i;
+        if (lane == 0) bulk_wait_read<kStgDepth - 1>();
+        __syncwarp();
+        stage_row32(stg, lane, v, fp32);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (o.c_z < 0) tma_store_2d(o.map, stg, col, o.c_row);
+          else tma_store_3d(o.map, stg, col, o.c_row, o.c_z);
+          bulk_commit();
+        }
+      } else if (row_ok) {
+        store_row32(o.ptr, o.row_off + col, v, ncols, fp32);
+      }
+    };
     for (int t = blockIdx.x; t < sch.total; t += gridDim.x, ++acc) {
       Tile tl;
       sch.decode(p, t, gcur, tl);
@@ -557,19 +681,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * BN;
       const bool row_ok = row_local < tl.rows;
+      // a 32-row block goes out by TMA when all of its rows belong to this output
+      const bool full = (VAR == VAR_M) ? (warp * 32 + 32 <= tl.rows) : true;
       const bool have_acc = tl.k_len > 0;
 
-      if (EPI == EPI_SWIGLU) {
+      if (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_DSWIGLU) {
         const long long orow = s_off[tl.g] + tl.m0 + row_local;
+        const int crow = s_off[tl.g] + tl.m0 + warp * 32;
+        const long long roff = orow * p.ld_out;
+        const OutRef o0{&mp.o0, p.out0, roff, crow, -1}, o1{&mp.o1, p.out1, roff, crow, -1},
+            o2{&mp.o2, p.out2, roff, crow, -1};
+        if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t rh[32], ru[32];
-          tmem_ld32(tbase + c, rh);
-          tmem_ld32(tbase + BN / 2 + c, ru);
-          tmem_ld_wait();
-          const int col = tl.n0 + c;
-          const int ncols = p.N - col;
-          if (row_ok && ncols > 0) {
+          for (int c = 0; c < BN / 2; c += 32) {
+            uint32_t rh[32], ru[32];
+            tmem_ld32(tbase + c, rh);
+            tmem_ld32(tbase + BN / 2 + c, ru);
+            tmem_ld_wait();
+            const int col = tl.n0 + c;
+            const int ncols = p.N - col;
             float h[32], u[32], a[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -577,44 +707,42 @@ __global__ void __launch_bounds__(kThreads, 1)
               u[i] = __uint_as_float(ru[i]);
               a[i] = h[i] * sigmoidf_(h[i]) * u[i];
             }
-            const long long off = orow * p.ld_out + col;
-            store_row_chunk(p.out0, off, h, ncols, 1);  // H, U stay fp32 for the backward
-            store_row_chunk(p.out1, off, u, ncols, 1);
-            store_row_chunk(p.out2, off, a, ncols, 0);  // A is the bf16 operand of the down projection
+            emit(o0, h, col, ncols, full, row_ok, true);   // H, U stay fp32 for the backward
+            emit(o1, u, col, ncols, full, row_ok, true);
+            emit(o2, a, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
           }
-        }
-      } else if (EPI == EPI_SCALE) {
-        const long long orow = s_off[tl.g] + tl.m0 + row_local;
-        const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
+        } else if (EPI == EPI_SCALE) {
+          const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tbase + c, r);
-          tmem_ld_wait();
-          const int col = tl.n0 + c;
-          const int ncols = p.N - col;
-          if (row_ok && ncols > 0) {
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c, r);
+            tmem_ld_wait();
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = w * __uint_as_float(r[i]);
-            store_row_chunk(p.out0, orow * p.ld_out + col, v, ncols, 0);
+            emit(o0, v, tl.n0 + c, p.N - tl.n0 - c, full, row_ok, false);
           }
-        }
-      } else if (EPI == EPI_DSWIGLU) {
-        const long long orow = s_off[tl.g] + tl.m0 + row_local;
-        const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
-        float ds = 0.0f;
+        } else {  // EPI_DSWIGLU
+          const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
+          float ds = 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tbase + c, r);
-          tmem_ld_wait();
-          const int col = tl.n0 + c;
-          const int ncols = p.N - col;
-          if (row_ok && ncols > 0) {
-            float h[32], u[32], dh[32], du[32], ap[32];
-            load_f32_chunk(p.in0 + orow * p.ld_in + col, h, ncols);
-            load_f32_chunk(p.in1 + orow * p.ld_in + col, u, ncols);
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c, r);
+            tmem_ld_wait();
+            const int col = tl.n0 + c;
+            const int ncols = p.N - col;
+            if (ncols <= 0) continue;
+            float h[32], u[32];
+            if (row_ok) {
+              load_f32_row32(p.in0 + orow * p.ld_in + col, h, ncols);
+              load_f32_row32(p.in1 + orow * p.ld_in + col, u, ncols);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] = u[i] = 0.0f;
+            }
+            float dh[32], du[32], ap[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float dap = __uint_as_float(r[i]);  // dA' = dO . W_down (unweighted)
@@ -627,29 +755,31 @@ __global__ void __launch_bounds__(kThreads, 1)
               dh[i] = da * u[i] * sg * (1.0f + h[i] * (1.0f - sg));
               ap[i] = w * a;
             }
-            const long long off = orow * p.ld_out + col;
-            store_row_chunk(p.out0, off, dh, ncols, 0);
-            store_row_chunk(p.out1, off, du, ncols, 0);
-            store_row_chunk(p.out2, off, ap, ncols, 0);
+            emit(o0, dh, col, ncols, full, row_ok, false);
+            emit(o1, du, col, ncols, full, row_ok, false);
+            emit(o2, ap, col, ncols, full, row_ok, false);
           }
+          if (row_ok) p.part[orow * p.part_ld + tl.nt] = ds;
         }
-        if (row_ok) p.part[orow * p.part_ld + tl.nt] = ds;
       } else {  // EPI_STORE
-        long long obase;
-        void* optr = p.out0;
         const int m = tl.m0 + row_local;
+        const int mw = tl.m0 + warp * 32;
+        OutRef o{&mp.o0, p.out0, 0, 0, -1};
         if (VAR == VAR_M) {
-          obase = (s_off[tl.g] + tl.m0 + row_local) * p.ld_out;
+          o.row_off = (s_off[tl.g] + static_cast<long long>(m)) * p.ld_out;
+          o.c_row = s_off[tl.g] + mw;
         } else if (VAR == VAR_K) {
-          obase = static_cast<long long>(tl.g) * p.group_stride_out;
-          if (m >= p.out_rows_split) {
-            optr = p.out1;
-            obase += static_cast<long long>(m - p.out_rows_split) * p.ld_out;
+          o.c_z = tl.g;
+          if (mw >= p.out_rows_split) {
+            o.map = &mp.o1;
+            o.ptr = p.out1;
+            o.c_row = mw - p.out_rows_split;
           } else {
-            obase += static_cast<long long>(m) * p.ld_out;
+            o.c_row = mw;
           }
         } else {
-          obase = static_cast<long long>(tl.split) * p.group_stride_out + static_cast<long long>(m) * p.ld_out;
+          o.c_z = tl.split;
+          o.c_row = mw;
         }
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -657,37 +787,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + c, r);
           tmem_ld_wait();
           const int col = tl.n0 + c;
-          const int ncols = p.N - col;
-          if (row_ok && ncols > 0) {
-            float v[32];
+          float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[i] = have_acc ? __uint_as_float(r[i]) : 0.0f;
-              if (p.col_bias && i < ncols) v[i] += __ldg(p.col_bias + col + i);
-            }
-            store_row_chunk(optr, obase + col, v, ncols, p.out_fp32);
+          for (int i = 0; i < 32; ++i) {
+            v[i] = have_acc ? __uint_as_float(r[i]) : 0.0f;
+            if (p.col_bias && col + i < p.N) v[i] += __ldg(p.col_bias + col + i);
           }
+          emit(o, v, col, p.N - col, full, row_ok, OUTF32);
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[buf]);
     }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 4) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI>
-cudaError_t launch_grouped_gemm(const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<BN, STAGES, AMODE, BMODE, VAR, EPI>;
+template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<BN, STAGES, AMODE, BMODE, VAR, EPI, OUTF32>;
   const size_t smem = SmemLayout<BN, STAGES>::bytes(p.groups);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, stream>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  constexpr bool kGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN);
+  kern<<<grid, kGather ? 320 : 192, smem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

@@ -6,21 +6,21 @@ namespace vgg {
 // [GG] "(6) 세 번의 gg.gmm" gate and up in one pass: the B tile holds BN/2 rows of W_gate[e]
 // and the same BN/2 rows of W_up[e], so the epilogue sees h and u of the same columns.
 // A = X rows gathered through sorted_tok ([SM] "4.1 Gather 융합").
-cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const CUtensorMap* m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_CP_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_CP_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU>(p, m, grid, s);
+cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) return launch_grouped_gemm<256, 4, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
 }
 
-// Down projection, A = sorted activation rows (TMA), epilogue scales by the combine weight.
-cudaError_t run_down_scale(int BN, const GemmParams& p, const CUtensorMap* m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE>(p, m, grid, s);
+// Down projection, A = sorted activation rows, epilogue scales by the combine weight.
+cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
 }
 
-// Router logits X[T,d] W_r[d,E] (+ bias), W_r read MN-major.
-cudaError_t run_router_logits(int BN, const GemmParams& p, const CUtensorMap* m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE>(p, m, grid, s);
+// Router logits X[T,d] W_r[d,E] (+ bias), W_r read MN-major, fp32 out.
+cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
 }
 
 }  // namespace vgg

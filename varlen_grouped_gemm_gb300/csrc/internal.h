@@ -10,26 +10,38 @@
 namespace vgg {
 
 // ---- tensor maps (host) -------------------------------------------------------------------
-// 2-D bf16 view [rows][inner] with a row stride, box {64, box_rows}, 128-byte swizzle.
+// Operand loads, bf16, 128-byte swizzle: 2-D view [rows][inner] with a row stride, box {64, box_rows};
+// 3-D view [groups][rows][inner], box {64, box_rows, 1}.  box_rows = 1 gives the gather map.
 bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
                  uint32_t box_rows);
-// 3-D bf16 view [groups][rows][inner], box {64, box_rows, 1}, 128-byte swizzle.
 bool make_map_3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t groups,
                  uint32_t box_rows);
+// Epilogue stores: box {32 columns, 32 rows}; fp32 with 128-byte swizzle, bf16 with 64-byte swizzle.
+// MN-major operand as chunks of 64 columns: 3-D view {64, rows, cols/64} of a [rows][cols] matrix and
+// 4-D view {64, rows, cols/64, groups} of a [groups][rows][cols] tensor; box {64, 64, box_chunks(, 1)}.
+bool make_chunked_map_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_chunks);
+bool make_chunked_map_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t groups,
+                         uint32_t box_chunks);
+bool make_store_map_2d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_stride_elems);
+bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t depth);
 
 // ---- grouped GEMM instantiations (BN chosen at run time: 128 or 256) -------------------------
 // forward
-cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
-cudaError_t run_down_scale(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
-cudaError_t run_router_logits(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
-cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
-cudaError_t run_dx_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
-cudaError_t run_varlen_k_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
-cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const CUtensorMap* maps, int grid, cudaStream_t s);
+cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dw_down(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // test exports
-cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const CUtensorMap* maps, int grid,
-                       cudaStream_t s);
+cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+
+// Zero rows [offsets[E], cap) of up to three [cap, cols] bf16 buffers (the tail past the last pair).
+cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols, __nv_bfloat16* a,
+                                  __nv_bfloat16* b, __nv_bfloat16* c, cudaStream_t s);
 
 // ---- routing / permutation -----------------------------------------------------------------
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int K, int32_t* ids, float* w, float* scores,
