@@ -217,9 +217,10 @@ int moe_profile_read(moe_ctx* ctx, int max_kernels, char* names, double* total_m
  * moe_test_gemm_varlen_k: for each group e,
  *   D[e, m, c] = sum_{j in group e} A[rowa(j), m] * B[rowb(j), c]
  * with rowa(j) = idx_a ? idx_a[j] : j (same for b).  A[rows_a, M], B[rows_b, N] bf16,
- * D[G, M, N] fp32 (zeros for an empty group).  Exactly one of idx_a, idx_b is
- * non-NULL (the gathered operand is zero past a group's end); M and N are
- * multiples of 64.
+ * D[G, M, N] fp32 (zeros for an empty group).  At most one of idx_a, idx_b is
+ * non-NULL: a gathered operand is zero past a group's end; with both NULL the
+ * rows of B past the group's end are cleared in shared memory (the weight-
+ * gradient path).  M and N are multiples of 64.
  */
 int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, const void* B, int B_kmajor,
                            int G, int rows_a, int K, int N, long long cap, const int32_t* offsets, float* D,

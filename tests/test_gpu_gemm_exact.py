@@ -53,7 +53,7 @@ def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
 
 
 @pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 192), ([1, 0, 333], 128, 256), ([70], 64, 320)])
-@pytest.mark.parametrize("gathered", ["a", "b"])
+@pytest.mark.parametrize("gathered", ["a", "b", "none"])
 def test_varlen_k_exact(ctx, sizes, M, N, gathered):
     """D[e] = sum over the group's rows j of A[rowa(j)]^T B[rowb(j)]; one operand is gathered through an
     index (zero past the group's end), the other is read by sorted position (it runs into the next
@@ -68,9 +68,12 @@ def test_varlen_k_exact(ctx, sizes, M, N, gathered):
     if gathered == "a":
         A, B = _ints((Tsrc, M), -2, 2, 4), _ints((cap, N), -2, 2, 5)
         idx_a, idx_b = torch.from_numpy(idx).cuda(), None
-    else:
+    elif gathered == "b":
         A, B = _ints((cap, M), -2, 2, 4), _ints((Tsrc, N), -2, 2, 5)
         idx_a, idx_b = None, torch.from_numpy(idx).cuda()
+    else:
+        A, B = _ints((cap, M), -2, 2, 4), _ints((cap, N), -2, 2, 5)
+        idx_a, idx_b = None, None
     D = torch.full((G, M, N), 3.0, device="cuda")
     vgg.moe_test_gemm_varlen_k(ctx, _bf(A), idx_a, _bf(B), idx_b, torch.from_numpy(offsets).cuda(), D, cap)
     rc, code = vgg.moe_get_error(ctx)

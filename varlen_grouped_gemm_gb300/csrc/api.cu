@@ -88,22 +88,30 @@ bool make_chunked_map_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool make_store_map_2d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_stride_elems) {
+// Box rows are 128 bytes (fp32: 32 columns; bf16: 64 columns) with the 128-byte swizzle, or for
+// bf16 with box_cols = 32, 64 bytes with the 64-byte swizzle.
+static CUtensorMapSwizzle store_swizzle(bool fp32, uint32_t box_cols) {
+  return (fp32 || box_cols == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+}
+
+bool make_store_map_2d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_stride_elems,
+                       uint32_t box_cols) {
   const uint64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_stride_elems * es};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {fp32 ? 32u : box_cols, 32};
   return encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides,
-                box, fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                box, store_swizzle(fp32, box_cols));
 }
 
-bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t depth) {
+bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint64_t rows, uint64_t depth,
+                       uint32_t box_cols) {
   const uint64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[3] = {cols, rows, depth};
   cuuint64_t strides[2] = {cols * es, cols * rows * es};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {fp32 ? 32u : box_cols, 32, 1};
   return encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides,
-                box, fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                box, store_swizzle(fp32, box_cols));
 }
 
 namespace {
@@ -131,21 +139,21 @@ inline int gemm_bn(int N) { return N > 128 ? 256 : 128; }
 constexpr int kMaxSplitK = 16;
 
 struct BwdWs {
-  __nv_bfloat16 *dH, *dU, *Ap, *dXp, *dL, *WrT;
+  __nv_bfloat16 *dH, *dU, *Ap, *dXp, *dL, *WrT, *Xs, *dOs;
   float* part;
   float* wr_part;
 };
 
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
-  const int part_ld = ceil_div(n, gemm_bn(n));
-  return 3 * al(sizeof(__nv_bfloat16) * cap * n) + al(sizeof(__nv_bfloat16) * cap * d) +
+  const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
+  return 3 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
          al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E) +
          al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
          al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
 }
 
 BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
-  const int part_ld = ceil_div(n, gemm_bn(n));
+  const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
   uint8_t* p = static_cast<uint8_t*>(ws);
   BwdWs w{};
   auto take = [&](size_t bytes) {
@@ -157,6 +165,8 @@ BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
   w.dU = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.Ap = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.dXp = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
+  w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
+  w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.part = reinterpret_cast<float*>(take(sizeof(float) * cap * part_ld));
   w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E));
   w.WrT = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d));
@@ -356,7 +366,7 @@ int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, i
   const int BN = gemm_bn(E);
   Maps m = zero_maps();
   if (!make_map_2d(&m.a0, X, d, T, d, BM) || !make_map_2d(&m.b0, W_r, E, d, E, 64) ||
-      !make_store_map_3d(&m.o0, logits, true, E, T, 1))
+      !make_store_map_3d(&m.o0, logits, true, E, T, 1, 32))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -423,8 +433,8 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
     if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) ||
-        !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) || !make_store_map_2d(&m.o0, H, true, n, cap, n) ||
-        !make_store_map_2d(&m.o1, U, true, n, cap, n) || !make_store_map_2d(&m.o2, A, false, n, cap, n))
+        !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) || !make_store_map_2d(&m.o0, H, true, n, cap, n, 32) ||
+        !make_store_map_2d(&m.o1, U, true, n, cap, n, 32) || !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
     VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, p, m, std::min(tiles, ctx->num_sms), s));
@@ -443,7 +453,7 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     const int BN = gemm_bn(d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
-        !make_store_map_2d(&m.o0, Yw, false, d, cap, d))
+        !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -488,9 +498,13 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
   BwdWs w = carve_bwd(ws, T, d, E, n, cap);
   const bool f32 = dW_fp32 != 0;
   const int bn6 = gemm_bn(n);
-  const int part_ld = ceil_div(n, bn6);
+  const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
   if (cap > static_cast<long long>(T) * K)
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
+  // expert-sorted copies of X and dO: every backward GEMM then reads whole TMA boxes
+  VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, E, sorted_tok, cap, T, d, static_cast<const __nv_bfloat16*>(X),
+                                               static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs, ctx->d_err,
+                                               ctx->num_sms, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
   {
     GemmParams p = base_params(ctx);
@@ -499,10 +513,6 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.a_idx = sorted_tok;
-    p.a_rows = T;
-    p.a_src = static_cast<const __nv_bfloat16*>(dO);
-    p.a_ld = d;
     p.in0 = static_cast<const float*>(H);
     p.in1 = static_cast<const float*>(U);
     p.ld_in = n;
@@ -514,12 +524,13 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.part = w.part;
     p.part_ld = part_ld;
     Maps m = zero_maps();
-    if (!make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
-        !make_store_map_2d(&m.o0, w.dH, false, n, cap, n) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n))
+    if (!make_map_2d(&m.a0, w.dOs, d, cap, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
+        !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
+    m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * part_ld;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, bn6);
     VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // dXp = [dH | dU] [W_gate[e]; W_up[e]]
@@ -538,7 +549,7 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, BM) || !make_map_2d(&m.a1, w.dU, n, cap, n, BM) ||
         !make_chunked_map_3d(&m.b0, W_gate, d, n, E, BN / 64) || !make_chunked_map_3d(&m.b1, W_up, d, n, E, BN / 64) ||
-        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d))
+        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
     VGG_LAUNCH("dx_gemm", run_dx_store(BN, p, m, std::min(tiles, ctx->num_sms), s));
@@ -565,7 +576,7 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.ld_out = E;
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, X, d, T, d, 64) || !make_map_2d(&m.b0, w.dL, E, T, E, 64) ||
-        !make_store_map_3d(&m.o0, dst, true, E, d, split))
+        !make_store_map_3d(&m.o0, dst, true, E, d, split, 32))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -581,10 +592,7 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
     p.a_colsplit = n;
-    p.b_idx = sorted_tok;
-    p.b_rows = T;
-    p.b_src = static_cast<const __nv_bfloat16*>(X);
-    p.b_ld = d;
+    p.b_chunked = 1;
     p.out0 = dW_gate;
     p.out1 = dW_up;
     p.out_rows_split = n;
@@ -592,11 +600,12 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     const int BN = gemm_bn(d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
-        !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E) ||
-        !make_store_map_3d(&m.o1, dW_up, f32, d, n, E))
+        !make_chunked_map_2d(&m.b0, w.Xs, d, cap, BN / 64) || !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) ||
+        !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
       return MOE_ERR_CUDA;
+    m.b1 = m.b0;
     const int tiles = E * ceil_div(2 * n, BM) * ceil_div(d, BN);
-    VGG_LAUNCH("dw_gate_up", run_dw_gate_up(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_gate_up", run_dw_tiled(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // dW_down[e] = (w dO[tok])^T A  (the weight is folded into A')
   {
@@ -606,21 +615,18 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.a_idx = sorted_tok;
-    p.a_rows = T;
-    p.a_src = static_cast<const __nv_bfloat16*>(dO);
-    p.a_ld = d;
     p.out0 = dW_down;
     p.ld_out = n;
     const int BN = gemm_bn(n);
     Maps m = zero_maps();
     p.b_chunked = 1;
-    if (!make_chunked_map_2d(&m.b0, w.Ap, n, cap, BN / 64) ||
-        !make_store_map_3d(&m.o0, dW_down, f32, n, d, E))
+    if (!make_map_2d(&m.a0, w.dOs, d, cap, d, 64) || !make_chunked_map_2d(&m.b0, w.Ap, n, cap, BN / 64) ||
+        !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 64))
       return MOE_ERR_CUDA;
+    m.a1 = m.a0;
     m.b1 = m.b0;
     const int tiles = E * ceil_div(d, BM) * ceil_div(n, BN);
-    VGG_LAUNCH("dw_down", run_dw_down(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_down", run_dw_tiled(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;
 }
@@ -654,7 +660,7 @@ int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, cons
     if (N % 64 || !make_chunked_map_3d(&m.b0, B, N, K, G, 2)) return MOE_ERR_CUDA;
   }
   m.b1 = m.b0;
-  if (!make_store_map_2d(&m.o0, D, true, N, cap, N)) return MOE_ERR_CUDA;
+  if (!make_store_map_2d(&m.o0, D, true, N, cap, N, 32)) return MOE_ERR_CUDA;
   const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 128);
   return cuda_status(run_test_m(idx != nullptr, B_kmajor, p, m, std::min(tiles, ctx->num_sms),
                                 static_cast<cudaStream_t>(stream)));
@@ -664,7 +670,7 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
                            const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
                            const int32_t* offsets, float* D, moe_stream_t stream) {
   VGG_REQUIRE(ctx && A && B && offsets && D);
-  VGG_REQUIRE((idx_a == nullptr) != (idx_b == nullptr));  // exactly one operand is gathered
+  VGG_REQUIRE(idx_a == nullptr || idx_b == nullptr);  // at most one operand is gathered
   VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 64 && M % 64 == 0 && N >= 64 && N % 64 == 0 && rows_a >= 1 &&
               rows_b >= 1);
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX && aligned16(A) && aligned16(B) && aligned16(D));
@@ -690,14 +696,16 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
   const int BN = gemm_bn(N);
   Maps m = zero_maps();
   if ((!idx_a && !make_map_2d(&m.a0, A, M, rows_a, M, 64)) || (!idx_b && !make_chunked_map_2d(&m.b0, B, N, rows_b, BN / 64)) ||
-      !make_store_map_3d(&m.o0, D, true, N, M, G))
+      !make_store_map_3d(&m.o0, D, true, N, M, G, 32))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
   const int tiles = G * ceil_div(M, BM) * ceil_div(N, BN);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = std::min(tiles, ctx->num_sms);
-  return cuda_status(idx_b ? run_dw_gate_up(BN, true, p, m, grid, s) : run_dw_down(BN, true, p, m, grid, s));
+  if (idx_b) return cuda_status(run_dw_gate_up(BN, true, p, m, grid, s));
+  if (idx_a) return cuda_status(run_dw_down(BN, true, p, m, grid, s));
+  return cuda_status(run_dw_tiled(BN, true, p, m, grid, s));
 }
 
 int moe_profile_enable(moe_ctx* ctx, int enable) {

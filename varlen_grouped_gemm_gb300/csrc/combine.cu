@@ -306,3 +306,50 @@ cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, 
 }
 
 }  // namespace vgg
+
+namespace vgg {
+
+// out_a[j] = a[sorted_tok[j]], out_b[j] = b[sorted_tok[j]] for sorted rows j < P = offsets[E]; rows
+// [P, cap) are zeroed.  One warp per row, 16-byte vectors: the backward's expert-sorted copies of
+// X and dO, read by TMA boxes in the weight-gradient and dA' GEMMs.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets, int E,
+                                                          const int32_t* __restrict__ sorted_tok, long long cap,
+                                                          int T, int d, const __nv_bfloat16* __restrict__ a,
+                                                          const __nv_bfloat16* __restrict__ b,
+                                                          __nv_bfloat16* __restrict__ out_a,
+                                                          __nv_bfloat16* __restrict__ out_b, int* err) {
+  const long long P = offsets[E];
+  const int lane = threadIdx.x & 31;
+  const int nv = d >> 3;
+  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < cap;
+       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    int t = -1;
+    if (j < P) {
+      t = sorted_tok[j];
+      if (t < 0 || t >= T) {
+        if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
+        t = -1;
+      }
+    }
+    for (int c = lane; c < nv; c += 32) {
+      uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+      if (t >= 0) {
+        va = ldg_nc_v4(a + static_cast<long long>(t) * d + 8 * c);
+        vb = ldg_nc_v4(b + static_cast<long long>(t) * d + 8 * c);
+      }
+      *reinterpret_cast<uint4*>(out_a + j * d + 8 * c) = va;
+      *reinterpret_cast<uint4*>(out_b + j * d + 8 * c) = vb;
+    }
+  }
+}
+
+cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, long long cap, int T, int d,
+                               const __nv_bfloat16* a, const __nv_bfloat16* b, __nv_bfloat16* out_a,
+                               __nv_bfloat16* out_b, int* err, int num_sms, cudaStream_t s) {
+  const long long want = (cap + 7) / 8;
+  const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(offsets, E, sorted_tok, cap, T, d, a, b, out_a, out_b, err);
+  return cudaGetLastError();
+}
+
+}  // namespace vgg

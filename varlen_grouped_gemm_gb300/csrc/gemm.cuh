@@ -36,11 +36,9 @@ namespace vgg {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kMaxThreads = 320;  // 6 warps + 4 gather warps when an operand is gathered
+constexpr int kMaxThreads = 384;  // up to 8 epilogue warps + producer + issuer, or 4 + 2 + 4 gather warps
 constexpr int kMaxGroups = 1024;
 constexpr int kStgBuf = 4096;    // one staged store: 32 rows x 128 B
-constexpr int kStgDepth = 1;     // staged stores in flight per epilogue warp
-constexpr int kStgBytes = kStgBuf * kStgDepth;
 constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 this many stages ahead
 
 enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
@@ -89,13 +87,14 @@ struct Maps {
   CUtensorMap a0, a1, b0, b1, o0, o1, o2;
 };
 
-template <int BN, int STAGES>
+// EW epilogue warps with DEPTH staged stores each.
+template <int BN, int STAGES, int EW, int DEPTH>
 struct SmemLayout {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStgOffset = STAGES * kStageBytes;
-  static constexpr int kBarOffset = kStgOffset + 4 * kStgBytes;
+  static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr size_t bytes(int groups) {
@@ -287,6 +286,20 @@ __device__ __forceinline__ void stage_row32(uint8_t* stg, int r, const float (&v
   }
 }
 
+// 64 bf16 values as one 128-byte row (128-byte swizzle).
+__device__ __forceinline__ void stage_row64_bf16(uint8_t* stg, int r, const float (&v)[64]) {
+  uint8_t* row = stg + r * 128;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    uint4 q;
+    q.x = pack_bf16x2(v[8 * p], v[8 * p + 1]);
+    q.y = pack_bf16x2(v[8 * p + 2], v[8 * p + 3]);
+    q.z = pack_bf16x2(v[8 * p + 4], v[8 * p + 5]);
+    q.w = pack_bf16x2(v[8 * p + 6], v[8 * p + 7]);
+    *reinterpret_cast<uint4*>(row + ((p ^ (r & 7)) << 4)) = q;
+  }
+}
+
 // Target of one epilogue store: a TMA map and coordinates for full 32-row blocks, a pointer
 // and row offset for the direct path.
 struct OutRef {
@@ -299,10 +312,11 @@ struct OutRef {
 
 // -------------------------------------------------------------------------- the kernel
 
-template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
-  using L = SmemLayout<BN, STAGES>;
+  using L = SmemLayout<BN, STAGES, EW, DEPTH>;
+  static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != EPI_SWIGLU || BMODE == B_TMA_K3_GU, "SwiGLU epilogue needs the gate/up pair layout");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
@@ -310,7 +324,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
   constexpr bool kBGather = (BMODE == B_GATHER_MN);
   constexpr bool kGather = kAGather || kBGather;
-  constexpr int kThreads = kGather ? 320 : 192;
+  constexpr int kProdWarp = EW;        // TMA producer, owns TMEM
+  constexpr int kMmaWarp = EW + 1;     // UMMA issuer
+  constexpr int kGatherWarp0 = EW + 2; // cp.async gather warps (4) when an operand is gathered
+  constexpr int kThreads = (EW + 2 + (kGather ? 4 : 0)) * 32;
+  static_assert(kThreads <= kMaxThreads, "threads");
   constexpr uint32_t kTxBytes = (kAGather ? 0 : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
@@ -340,14 +358,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 128);
+      mbar_init(&tempty_bar[b], EW * 32);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
     *s_bad = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     tmem_alloc(s_tmem, kTmemCols);
     if (lane == 0) {
       if (!kAGather) tma_prefetch_desc(&mp.a0);
@@ -402,7 +420,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   sch.init(p, s_off, s_tile);
   if (*s_bad) sch.total = 0;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ---------------------------------------------------------------- TMA producer (one thread)
     if (lane == 0) {
       // Expert weights are read by the few tiles of one expert and then never again: stream them
@@ -492,11 +510,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
       }
     }
-  } else if (kGather && warp >= 6) {
+  } else if (kGather && warp >= kGatherWarp0) {
     // ---------------------------------------------------------------- cp.async gather producers
     // Thread ptid owns the 16-byte piece c16 of rows rsub + 16 i of every stage.  The token
     // indices of a position are loaded two positions ahead of its copies.
-    const int ptid = tid - 192;
+    const int ptid = tid - kGatherWarp0 * 32;
     const int c16 = ptid & 7;
     const int rsub = ptid >> 3;
     const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
@@ -602,33 +620,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
     }
     cp_async_wait_all();
-  } else if (warp == 5) {
-    // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
-      int it = 0, acc = 0, gcur = 0;
-      bool aborted = false;
-      for (int t = blockIdx.x; t < sch.total && !aborted; t += gridDim.x, ++acc) {
-        Tile tl;
-        sch.decode(p, t, gcur, tl);
-        const int nk = (tl.k_len + BK - 1) / BK;
-        const int buf = acc & 1;
-        if (!mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)) {
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- UMMA issuer (lane 0)
+    // With both operands tiled in the varlen-K mode, the last stage of a group reads rows of the
+    // next group (or the zeroed tail): the whole warp clears those rows of B in shared memory
+    // before lane 0 issues the stage's UMMAs.
+    constexpr bool kZeroTail = (VAR == VAR_K) && !kGather;
+    int it = 0, acc = 0, gcur = 0;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < sch.total && !aborted; t += gridDim.x, ++acc) {
+      Tile tl;
+      sch.decode(p, t, gcur, tl);
+      const int nk = (tl.k_len + BK - 1) / BK;
+      const int buf = acc & 1;
+      // lane 0 waits, the warp follows its verdict (the other lanes block in the shuffle)
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int ks = 0; ks < nk; ++ks, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        ok = 0;
+        if (lane == 0) ok = mbar_wait(&full_bar[s], ph, s_abort, p.timeout_ns, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
           aborted = true;
           break;
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
-        for (int ks = 0; ks < nk; ++ks, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&full_bar[s], ph, s_abort, p.timeout_ns, p.err)) {
-            aborted = true;
-            break;
+        const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
+        const uint32_t sb = sa + L::kABytes;
+        if (kZeroTail) {
+          const int kv = tl.k_len - ks * BK;  // valid rows of this stage
+          if (kv < BK) {
+            uint8_t* b_gen = smem + s * L::kStageBytes + L::kABytes;
+            const int pieces = (BK - kv) * 8;
+            for (int c = 0; c < BN / 64; ++c)
+              for (int i = lane; i < pieces; i += 32)
+                *reinterpret_cast<uint4*>(b_gen + c * (BK * 128) + (kv + (i >> 3)) * 128 + (i & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
           }
+        }
+        if (lane == 0) {
           if (kGather) fence_proxy_async_smem();  // cp.async writes -> UMMA operand reads
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
-          const uint32_t sb = sa + L::kABytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
@@ -637,40 +677,70 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           }
           umma_commit(&empty_bar[s]);
         }
-        if (aborted) break;
-        umma_commit(&tfull_bar[buf]);
+        __syncwarp();
       }
-      if (aborted) {
-        umma_commit(drain_bar);
-        volatile int never = 0;
-        mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
-      }
+      if (aborted) break;
+      if (lane == 0) umma_commit(&tfull_bar[buf]);
+      __syncwarp();
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- epilogue (warps 0-3)
-    uint8_t* stg_base = smem + L::kStgOffset + warp * kStgBytes;
-    int stg_i = 0;  // ring position: a buffer is rewritten only after the store kStgDepth-1 back has read it
+    if (aborted && lane == 0) {
+      umma_commit(drain_bar);
+      volatile int never = 0;
+      mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
+    }
+  } else if (warp < EW) {
+    // ---------------------------------------------------------------- epilogue (warps 0..EW-1)
+    // Warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32 rows) and, with 8 warps, one half of
+    // the tile's columns (w / 4).  Results leave through a ring of DEPTH staged TMA stores.
+    const int quarter = warp & 3;
+    const int half = (EW == 8) ? (warp >> 2) : 0;
+    uint8_t* stg_base = smem + L::kStgOffset + warp * (DEPTH * kStgBuf);
+    int stg_i = 0;
     int acc = 0, gcur = 0;
-    const int row_local = warp * 32 + lane;
-    // Emit 32 columns of this thread's row to `o`: a staged TMA store when all 32 rows of the
-    // warp belong to the output, else a direct store of each valid row.
-    auto emit = [&](const OutRef& o, const float (&v)[32], int col, int ncols, bool full, bool row_ok, bool fp32) {
+    const int row_local = quarter * 32 + lane;
+    auto next_stage_buf = [&]() -> uint8_t* {
+      uint8_t* stg = stg_base + (stg_i % DEPTH) * kStgBuf;
+      ++stg_i;
+      if (lane == 0) bulk_wait_read<DEPTH - 1>();  // the store that last used this buffer has read it
+      __syncwarp();
+      return stg;
+    };
+    auto issue_store = [&](const OutRef& o, const uint8_t* stg, int col) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (o.c_z < 0) tma_store_2d(o.map, stg, col, o.c_row);
+        else tma_store_3d(o.map, stg, col, o.c_row, o.c_z);
+        bulk_commit();
+      }
+    };
+    // 32 columns (fp32, or bf16 through a 64-byte-swizzled box)
+    auto emit32 = [&](const OutRef& o, const float (&v)[32], int col, int ncols, bool full, bool row_ok, bool fp32) {
       if (ncols <= 0) return;
       if (full) {
-        uint8_t* stg = stg_base + (stg_i % kStgDepth) * kStgBuf;
-        ++stg_i;
-        if (lane == 0) bulk_wait_read<kStgDepth - 1>();
-        __syncwarp();
+        uint8_t* stg = next_stage_buf();
         stage_row32(stg, lane, v, fp32);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (o.c_z < 0) tma_store_2d(o.map, stg, col, o.c_row);
-          else tma_store_3d(o.map, stg, col, o.c_row, o.c_z);
-          bulk_commit();
-        }
+        issue_store(o, stg, col);
       } else if (row_ok) {
         store_row32(o.ptr, o.row_off + col, v, ncols, fp32);
+      }
+    };
+    // 64 bf16 columns through one 128-byte-swizzled box
+    auto emit64 = [&](const OutRef& o, const float (&v)[64], int col, int ncols, bool full, bool row_ok) {
+      if (ncols <= 0) return;
+      if (full) {
+        uint8_t* stg = next_stage_buf();
+        stage_row64_bf16(stg, lane, v);
+        issue_store(o, stg, col);
+      } else if (row_ok) {
+        float lo[32], hi[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          lo[i] = v[i];
+          hi[i] = v[32 + i];
+        }
+        store_row32(o.ptr, o.row_off + col, lo, ncols, false);
+        if (ncols > 32) store_row32(o.ptr, o.row_off + col + 32, hi, ncols - 32, false);
       }
     };
     for (int t = blockIdx.x; t < sch.total; t += gridDim.x, ++acc) {
@@ -679,21 +749,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const int buf = acc & 1;
       if (!mbar_wait(&tfull_bar[buf], (acc >> 1) & 1, s_abort, p.timeout_ns, p.err)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * BN;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
       const bool row_ok = row_local < tl.rows;
       // a 32-row block goes out by TMA when all of its rows belong to this output
-      const bool full = (VAR == VAR_M) ? (warp * 32 + 32 <= tl.rows) : true;
+      const bool full = (VAR == VAR_M) ? (quarter * 32 + 32 <= tl.rows) : true;
       const bool have_acc = tl.k_len > 0;
+      constexpr int kCols = (EW == 8) ? BN / 2 : BN;  // accumulator columns handled by this warp
+      const int c_lo = half * kCols;
 
       if (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_DSWIGLU) {
         const long long orow = s_off[tl.g] + tl.m0 + row_local;
-        const int crow = s_off[tl.g] + tl.m0 + warp * 32;
+        const int crow = s_off[tl.g] + tl.m0 + quarter * 32;
         const long long roff = orow * p.ld_out;
         const OutRef o0{&mp.o0, p.out0, roff, crow, -1}, o1{&mp.o1, p.out1, roff, crow, -1},
             o2{&mp.o2, p.out2, roff, crow, -1};
         if (EPI == EPI_SWIGLU) {
+          // columns [0, BN/2) hold h, [BN/2, BN) hold u of the same output columns
+          constexpr int kHalf = (EW == 8) ? BN / 4 : BN / 2;
 #pragma unroll 1
-          for (int c = 0; c < BN / 2; c += 32) {
+          for (int c = half * kHalf; c < (half + 1) * kHalf; c += 32) {
             uint32_t rh[32], ru[32];
             tmem_ld32(tbase + c, rh);
             tmem_ld32(tbase + BN / 2 + c, ru);
@@ -707,27 +781,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               u[i] = __uint_as_float(ru[i]);
               a[i] = h[i] * sigmoidf_(h[i]) * u[i];
             }
-            emit(o0, h, col, ncols, full, row_ok, true);   // H, U stay fp32 for the backward
-            emit(o1, u, col, ncols, full, row_ok, true);
-            emit(o2, a, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
+            emit32(o0, h, col, ncols, full, row_ok, true);   // H, U stay fp32 for the backward
+            emit32(o1, u, col, ncols, full, row_ok, true);
+            emit32(o2, a, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
           }
         } else if (EPI == EPI_SCALE) {
           const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            uint32_t r[32];
-            tmem_ld32(tbase + c, r);
+          for (int c = c_lo; c < c_lo + kCols; c += 64) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tbase + c, r0);
+            tmem_ld32(tbase + c + 32, r1);
             tmem_ld_wait();
-            float v[32];
+            float v[64];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = w * __uint_as_float(r[i]);
-            emit(o0, v, tl.n0 + c, p.N - tl.n0 - c, full, row_ok, false);
+            for (int i = 0; i < 32; ++i) {
+              v[i] = w * __uint_as_float(r0[i]);
+              v[32 + i] = w * __uint_as_float(r1[i]);
+            }
+            emit64(o0, v, tl.n0 + c, p.N - tl.n0 - c, full, row_ok);
           }
         } else {  // EPI_DSWIGLU
           const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
           float ds = 0.0f;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
+          for (int c = c_lo; c < c_lo + kCols; c += 32) {
             uint32_t r[32];
             tmem_ld32(tbase + c, r);
             tmem_ld_wait();
@@ -755,15 +833,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               dh[i] = da * u[i] * sg * (1.0f + h[i] * (1.0f - sg));
               ap[i] = w * a;
             }
-            emit(o0, dh, col, ncols, full, row_ok, false);
-            emit(o1, du, col, ncols, full, row_ok, false);
-            emit(o2, ap, col, ncols, full, row_ok, false);
+            emit32(o0, dh, col, ncols, full, row_ok, false);
+            emit32(o1, du, col, ncols, full, row_ok, false);
+            emit32(o2, ap, col, ncols, full, row_ok, false);
           }
-          if (row_ok) p.part[orow * p.part_ld + tl.nt] = ds;
+          // one partial per (row, column tile, column half)
+          if (row_ok) p.part[orow * p.part_ld + tl.nt * (EW / 4) + half] = ds;
         }
       } else {  // EPI_STORE
         const int m = tl.m0 + row_local;
-        const int mw = tl.m0 + warp * 32;
+        const int mw = tl.m0 + quarter * 32;
         OutRef o{&mp.o0, p.out0, 0, 0, -1};
         if (VAR == VAR_M) {
           o.row_off = (s_off[tl.g] + static_cast<long long>(m)) * p.ld_out;
@@ -774,26 +853,51 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             o.map = &mp.o1;
             o.ptr = p.out1;
             o.c_row = mw - p.out_rows_split;
+            o.row_off = static_cast<long long>(m - p.out_rows_split) * p.ld_out +
+                        static_cast<long long>(tl.g) * p.out_rows_split * p.ld_out;
           } else {
             o.c_row = mw;
+            o.row_off = static_cast<long long>(m) * p.ld_out;
           }
         } else {
           o.c_z = tl.split;
           o.c_row = mw;
         }
+        if (OUTF32) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tbase + c, r);
-          tmem_ld_wait();
-          const int col = tl.n0 + c;
-          float v[32];
+          for (int c = c_lo; c < c_lo + kCols; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c, r);
+            tmem_ld_wait();
+            const int col = tl.n0 + c;
+            float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = have_acc ? __uint_as_float(r[i]) : 0.0f;
-            if (p.col_bias && col + i < p.N) v[i] += __ldg(p.col_bias + col + i);
+            for (int i = 0; i < 32; ++i) {
+              v[i] = have_acc ? __uint_as_float(r[i]) : 0.0f;
+              if (p.col_bias && col + i < p.N) v[i] += __ldg(p.col_bias + col + i);
+            }
+            emit32(o, v, col, p.N - col, full, row_ok, true);
           }
-          emit(o, v, col, p.N - col, full, row_ok, OUTF32);
+        } else {
+#pragma unroll 1
+          for (int c = c_lo; c < c_lo + kCols; c += 64) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tbase + c, r0);
+            tmem_ld32(tbase + c + 32, r1);
+            tmem_ld_wait();
+            const int col = tl.n0 + c;
+            float v[64];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = have_acc ? __uint_as_float(r0[i]) : 0.0f;
+              v[32 + i] = have_acc ? __uint_as_float(r1[i]) : 0.0f;
+              if (p.col_bias) {
+                if (col + i < p.N) v[i] += __ldg(p.col_bias + col + i);
+                if (col + 32 + i < p.N) v[32 + i] += __ldg(p.col_bias + col + 32 + i);
+              }
+            }
+            emit64(o, v, col, p.N - col, full, row_ok);
+          }
         }
       }
       tc_fence_before();
@@ -806,18 +910,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == kProdWarp) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int BN, int STAGES, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<BN, STAGES, AMODE, BMODE, VAR, EPI, OUTF32>;
-  const size_t smem = SmemLayout<BN, STAGES>::bytes(p.groups);
+  auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32>;
+  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH>::bytes(p.groups);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
   constexpr bool kGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN);
-  kern<<<grid, kGather ? 320 : 192, smem, stream>>>(p, maps);
+  kern<<<grid, (EW + 2 + (kGather ? 4 : 0)) * 32, smem, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

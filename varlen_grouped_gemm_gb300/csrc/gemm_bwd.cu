@@ -1,44 +1,54 @@
-// Backward grouped-GEMM instantiations.
+// Backward grouped-GEMM instantiations.  Template arguments as in gemm_fwd.cu; the kernels whose
+// epilogue writes several outputs per tile use 8 epilogue warps and 2 staged stores per warp,
+// paid for with one pipeline stage.
 #include "internal.h"
 
 namespace vgg {
 
-// dA' = dO[tok] W_down[e] (W_down read MN-major), epilogue: dS partial, dH, dU, A'
+// dA' = dO_sorted W_down[e] (W_down read MN-major), epilogue: dS partial, dH, dU, A'
 // ([SM] "4.2 Epilogue 융합": one epilogue emits dH, dS and A').
 cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_GATHER_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_GATHER_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 3, 8, 2, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 4, 8, 2, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
 }
 
 // dXp = [dH | dU] [W_gate[e]; W_up[e]]  (reduction over 2n, B read MN-major from two maps)
 cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
 }
 
-// dW_gate / dW_up [e] = [dH | dU]^T X[tok] over the expert's rows: A = dH/dU rows (tiled, MN-major),
-// B = X rows gathered (zero past the expert's end).
+// Varlen-K weight gradient with both operands read by TMA from expert-sorted rows; the rows past the
+// group's end in its last stage are cleared in shared memory before the last UMMAs.
+cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256)
+    return f32 ? launch_grouped_gemm<256, 3, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+               : launch_grouped_gemm<256, 3, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<128, 4, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+             : launch_grouped_gemm<128, 4, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+}
+
+// Varlen-K with one operand gathered through a token index (cp.async, zero past the group's end).
 cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256)
-    return f32 ? launch_grouped_gemm<256, 4, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, true>(p, m, grid, s)
-               : launch_grouped_gemm<256, 4, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, false>(p, m, grid, s);
-  return f32 ? launch_grouped_gemm<128, 6, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, true>(p, m, grid, s)
-             : launch_grouped_gemm<128, 6, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, false>(p, m, grid, s);
+    return f32 ? launch_grouped_gemm<256, 4, 4, 1, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, true>(p, m, grid, s)
+               : launch_grouped_gemm<256, 4, 4, 1, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, false>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<128, 6, 4, 1, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, true>(p, m, grid, s)
+             : launch_grouped_gemm<128, 6, 4, 1, A_TMA_MN, B_GATHER_MN, VAR_K, EPI_STORE, false>(p, m, grid, s);
 }
 
-// dW_down[e] = dO[tok]^T A' over the expert's rows: A = dO rows gathered, B = A' rows (tiled).
 cudaError_t run_dw_down(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256)
-    return f32 ? launch_grouped_gemm<256, 4, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
-               : launch_grouped_gemm<256, 4, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
-  return f32 ? launch_grouped_gemm<128, 6, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
-             : launch_grouped_gemm<128, 6, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+    return f32 ? launch_grouped_gemm<256, 4, 4, 1, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+               : launch_grouped_gemm<256, 4, 4, 1, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<128, 6, 4, 1, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+             : launch_grouped_gemm<128, 6, 4, 1, A_GATHER_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
 }
 
 // Dense A^T B with both operands MN-major (router weight gradient X^T dlogits), split K, fp32 out.
 cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_MN, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_MN, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
 }
 
 }  // namespace vgg

@@ -1,4 +1,6 @@
 // Forward grouped-GEMM instantiations: gate/up + SwiGLU, down + combine weight, router logits.
+// Template arguments: BN, pipeline stages, epilogue warps, staged stores per epilogue warp, operand
+// modes, grouping mode, epilogue, fp32 output.
 #include "internal.h"
 
 namespace vgg {
@@ -7,20 +9,21 @@ namespace vgg {
 // and the same BN/2 rows of W_up[e], so the epilogue sees h and u of the same columns.
 // A = X rows gathered through sorted_tok ([SM] "4.1 Gather 융합").
 cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+  if (BN == 256)
+    return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
 }
 
 // Down projection, A = sorted activation rows, epilogue scales by the combine weight.
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
 }
 
 // Router logits X[T,d] W_r[d,E] (+ bias), W_r read MN-major, fp32 out.
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);
 }
 
 }  // namespace vgg
