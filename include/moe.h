@@ -133,6 +133,28 @@ int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, cons
                 int32_t* P_out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_permute_noalloc — moe_permute without a workspace, for callers that cannot
+ * allocate device memory at all (a caller that only receives buffers from a host
+ * runtime that offers no allocator, or a loop that must not allocate once it
+ * runs).  The pages describe no such entry point; it is an addition of this
+ * library.
+ *
+ * Same grouping and outputs as moe_permute with m_tile = 0 (plain top-K), but its
+ * scratch lives in a fixed device array inside the library (257 KiB, held by every
+ * GPU that loads the library until the process exits), so it supports at most
+ * T <= 32768 tokens and E <= 512 experts and returns MOE_ERR_UNSUPPORTED beyond
+ * that.  No cudaMalloc, cudaFree or other allocating call is made.
+ * The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU (two
+ * streams, or two contexts on one device) race and must be serialized by the
+ * caller.  The array needs no clearing: every call rewrites what it reads.
+ */
+int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K,
+                        long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok, float* sorted_w,
+                        int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out, moe_stream_t stream);
+
+/*
  * moe_grouped_gemm_fwd — the expert MLP of every pair, as varlen-M grouped GEMMs.
  * [GG] "(6) 세 번의 gg.gmm" and "Variable-M batched matmul"; [SM] "MoE 연산 =
  * Grouped GEMM", "4.1 Gather 융합" (token rows gathered inside the operand

@@ -26,7 +26,7 @@ EXPORTS = (
     "moe_create", "moe_destroy", "moe_status_str", "moe_get_error", "moe_set_wait_timeout",
     "moe_pair_capacity", "moe_workspace_bytes", "moe_route", "moe_permute", "moe_grouped_gemm_fwd",
     "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
-    "moe_test_gemm_varlen_k", "moe_test_wait_timeout",
+    "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
         L.moe_test_gemm_varlen_m.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_test_gemm_varlen_k.argtypes = [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_test_wait_timeout.argtypes = [_P, ctypes.c_ulonglong, _P]
+        L.moe_permute_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -185,6 +186,18 @@ def moe_permute(ctx, topk_ids, topk_w, logits, scores, E, m_tile, counts, offset
         _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32), _ptr(sorted_w, torch.float32),
         _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32), _ptr(P_out, torch.int32), wp, wb,
         _stream(stream)))
+
+
+def moe_permute_noalloc(ctx, topk_ids, topk_w, E, counts, offsets, sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out,
+                        stream=None):
+    """moe_permute (plain top-K) with its scratch in a fixed array inside the library: for callers
+    that cannot allocate device memory.  At most 32768 tokens and 512 experts."""
+    T, K = topk_ids.shape
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        ctx.handle, _ptr(topk_ids, torch.int32), _ptr(topk_w, torch.float32), T, E, K, sorted_tok.numel(),
+        _ptr(counts, torch.int32), _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32),
+        _ptr(sorted_w, torch.float32), _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32),
+        _ptr(P_out, torch.int32), _stream(stream)))
 
 
 def moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, offsets, sorted_tok, sorted_w, H, U, A, Yw, ws=None,

@@ -35,6 +35,9 @@ struct moe_ctx {
 
 namespace vgg {
 
+int ctx_device(const moe_ctx* ctx) { return ctx->device; }
+int* ctx_error_word(moe_ctx* ctx) { return ctx->d_err; }
+
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 static bool ensure_encode() {

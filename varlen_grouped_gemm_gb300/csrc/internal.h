@@ -88,3 +88,11 @@ cudaError_t launch_splitk_reduce(const float* part, int splits, long long n, flo
 cudaError_t launch_wait_timeout_probe(int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 }  // namespace vgg
+
+struct moe_ctx;
+namespace vgg {
+// Context fields needed outside api.cu.
+int ctx_device(const moe_ctx* ctx);
+int* ctx_error_word(moe_ctx* ctx);
+
+}  // namespace vgg
