@@ -58,24 +58,155 @@ def workload_desc(wl):
 
 
 def kernel_work(wl, P, dW_bytes=2):
-    """Algorithmic flops and minimum HBM bytes of one launch of each kernel label."""
-    T, d, E, n = wl.T, wl.d, wl.E, wl.n
+    """Algorithmic flops and minimum HBM bytes of one launch of each kernel label (bf16 = 2 B; the
+    gate/up pre-activations H, U are cached in fp32).  Weights are read once per launch, every
+    activation tensor is written once and read once."""
+    T, d, E, n, K = wl.T, wl.d, wl.E, wl.n, wl.K
     return {
-        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E, "tensor"),
-        "topk_softmax": (0, 4 * T * E + 8 * T * wl.K, "hbm"),
-        "permute": (0, 16 * P + 8 * T * wl.K, "hbm"),
-        "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 6 * P * n, "tensor"),
-        "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d, "tensor"),
-        "combine": (0, 2 * P * d + 2 * T * d, "hbm"),
-        "dact_dswiglu": (2 * P * d * n, 2 * T * d + 2 * E * d * n + 10 * P * n, "tensor"),
-        "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d, "tensor"),
-        "wr_transpose": (0, 4 * d * E, "hbm"),
-        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 6 * T * E, "hbm"),
-        "dwr_gemm": (2 * T * d * E, 2 * T * d + 2 * T * E + 4 * d * E, "tensor"),
-        "dwr_reduce": (0, 8 * d * E, "hbm"),
-        "dw_gate_up": (4 * P * d * n, 2 * T * d + 4 * P * n + 2 * dW_bytes * E * n * d, "tensor"),
-        "dw_down": (2 * P * d * n, 2 * T * d + 2 * P * n + dW_bytes * E * d * n, "tensor"),
+        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E),
+        "topk_softmax": (0, 4 * T * E + 8 * T * K),
+        "permute": (0, 4 * T * K + 16 * P),
+        "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 10 * P * n),
+        "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
+        "combine": (0, 2 * P * d + 2 * T * d),
+        "gather_rows": (0, 4 * T * d + 4 * P * d),
+        "zero_tail": (0, 0),
+        "dact_dswiglu": (2 * P * d * n, 2 * P * d + 2 * E * d * n + 8 * P * n + 6 * P * n),
+        "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d),
+        "wr_transpose": (0, 4 * d * E),
+        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 6 * T * E),
+        "dwr_gemm": (2 * T * d * E, 2 * T * d + 2 * T * E + 4 * d * E),
+        "dwr_reduce": (0, 8 * d * E),
+        "dw_gate_up": (4 * P * d * n, 2 * P * d + 4 * P * n + 2 * dW_bytes * E * n * d),
+        "dw_down": (2 * P * d * n, 2 * P * d + 2 * P * n + dW_bytes * E * d * n),
     }
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources: a recorded ncu traffic figure is used only while it matches."""
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "varlen_grouped_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from an ncu capture (profiles/dram_traffic_<workload>.json), or None
+    when the kernels have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("bytes_per_launch", {}).get(kernel)
+
+
+# Template arguments of the grouped GEMM (BN, stages, epilogue warps, depth, A mode, B mode, grouping,
+# epilogue, fp32 out) -> the label the library's profiling hook uses.
+_GEMM_LABELS = {
+    (1, 1, 0, 1): "gate_up_swiglu", (0, 0, 0, 2): "down_scale", (0, 3, 2, 0): "router_logits",
+    (0, 2, 0, 3): "dact_dswiglu", (0, 2, 0, 0): "dx_gemm", (2, 3, 1, 0): "dw_tiled (gate/up, down)",
+    (2, 3, 2, 0): "dwr_gemm", (2, 4, 1, 0): "dw_gather_b", (3, 3, 1, 0): "dw_gather_a",
+}
+_OTHER_LABELS = {
+    "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
+    "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "combine_kernel": "combine",
+    "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
+    "splitk_reduce_kernel": "dwr_reduce", "gather_rows_kernel": "gather_rows", "zero_tail_rows_kernel": "zero_tail",
+}
+
+
+def _ncu_rows(csv_path):
+    import csv
+    rows, hdr = [], None
+    with open(csv_path) as f:
+        for r in csv.reader(f):
+            if r and r[0] == "ID":
+                hdr = r
+            elif hdr and len(r) == len(hdr):
+                rows.append(dict(zip(hdr, r)))
+    return rows
+
+
+def _label_of(name: str):
+    import re
+    m = re.search(r"grouped_gemm_kernel<([^>]*)>", name)
+    if m:
+        a = [x.strip() for x in m.group(1).split(",")]
+        return _GEMM_LABELS.get((int(a[4]), int(a[5]), int(a[6]), int(a[7])), "grouped_gemm " + m.group(1))
+    for k, v in _OTHER_LABELS.items():
+        if k in name:
+            return v
+    return None
+
+
+def ncu_traffic(csv_path: str, workload: str) -> dict:
+    """Per-launch DRAM bytes (read + write) of one step's kernels from an ncu metrics capture, keyed by
+    the profiling hook's labels; the two weight-gradient launches come in the order gate/up, down."""
+    per, order = {}, []
+    for r in _ncu_rows(csv_path):
+        key = (r["ID"], r["Kernel Name"])
+        if key not in per:
+            per[key] = {}
+            order.append(key)
+        per[key][r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
+    out, dw_seen = {}, 0
+    for key in order:
+        label = _label_of(key[1])
+        if label is None:
+            continue
+        if label.startswith("dw_tiled"):
+            label = "dw_gate_up" if dw_seen == 0 else "dw_down"
+            dw_seen += 1
+        m = per[key]
+        b = m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0)
+        out[label] = out.get(label, 0.0) + b  # the grouping's kernels add up
+    return {"workload": workload, "source_hash": source_hash(), "bytes_per_launch": out}
+
+
+def ncu_launch_summary(csv_path: str) -> str:
+    """Markdown table of an ncu `--metrics gpu__time_duration.sum --csv` launch list: per kernel of this
+    library, its launches, total device time and share (other kernels, e.g. torch fills, are listed apart)."""
+    import csv
+    import re
+    rows, hdr = [], None
+    with open(csv_path) as f:
+        for r in csv.reader(f):
+            if r and r[0] == "ID":
+                hdr = r
+            elif hdr and len(r) == len(hdr):
+                rows.append(dict(zip(hdr, r)))
+    agg, other = {}, {}
+    for r in rows:
+        name = r["Kernel Name"]
+        ns = float(r["Metric Value"])
+        m = re.search(r"grouped_gemm_kernel<([^>]*)>", name)
+        label = None
+        if m:
+            a = [x.strip() for x in m.group(1).split(",")]
+            label = _GEMM_LABELS.get((int(a[4]), int(a[5]), int(a[6]), int(a[7])), "grouped_gemm " + m.group(1))
+        else:
+            for k, v in _OTHER_LABELS.items():
+                if k in name:
+                    label = v
+        tgt = agg if label else other
+        key = label or name.split("(")[0][:60]
+        c, t = tgt.get(key, (0, 0.0))
+        tgt[key] = (c + 1, t + ns)
+    total = sum(t for _, t in agg.values())
+    out = ["| kernel | launches | total (us) | share of this library's time |", "|---|---|---|---|"]
+    for k, (c, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        out.append(f"| {k} | {c} | {t / 1e3:.1f} | {100 * t / total:.1f}% |")
+    out.append("")
+    out.append("Other kernels in the capture (input setup, L2 flush): " +
+               ", ".join(f"{k} x{c}" for k, (c, t) in sorted(other.items(), key=lambda kv: -kv[1][1])))
+    return "\n".join(out)
 
 
 # ------------------------------------------------------------------------ clocks
@@ -97,7 +228,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -181,7 +312,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     wl = synth.WORKLOADS[args.workload]
-    budget = float(os.environ.get("VGG_REF_STEP_SECONDS", "8"))
+    # each step is a bounded sample so that the whole run stays near two minutes
+    budget = min(8.0, max(0.5, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(wl, budget_s=0.5, max_experts=1)
     flops, secs, experts, cores = 0, 0.0, 0, 0.0
@@ -260,11 +392,16 @@ def run_ours(args, rank, world, local_rank):
     vgg.moe_profile_enable(ctx, True)
     vgg.moe_profile_read(ctx)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # clock samples: a 0.5 s busy pre-roll of the same step right before the timed region, and the region
+    clocks.start()
+    t_end = time.perf_counter() + (0.0 if args.profile_run else 0.5)
+    while time.perf_counter() < t_end:
+        step()
+        torch.cuda.synchronize()
+    vgg.moe_profile_read(ctx)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     for i in range(args.steps):
         flush.zero_()
         evs[i][0].record(stream)
@@ -290,31 +427,37 @@ def run_ours(args, rank, world, local_rank):
     tflops = world * flops / (ms * 1e-3) / 1e12
     tokens_s = world * wl.T / (ms * 1e-3)
 
-    # dominant kernel and its roofline
+    # dominant kernel and its roofline: the binding resource of its algorithmic work
     work = kernel_work(wl, P)
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     dname, (dms, dlaunch) = dom
-    fl, by, bound = work[dname]
+    fl, by = work[dname]
     avg_ms = dms / max(dlaunch, 1)
-    if bound == "tensor":
+    t_tensor = fl / (pk["bf16_sus"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    traffic = recorded_traffic(wl.name, dname)
+    if t_tensor >= t_hbm:
         achieved = fl / (avg_ms * 1e-3) / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sus"], "traffic": None,
-                "peak_source": f"{pk['source']} sustained bf16",
-                "hbm_gbs_min_bytes": by / (avg_ms * 1e-3) / 1e9, "avg_launch_ms": avg_ms}
+        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_sus"], "traffic": traffic,
+                "peak_source": f"{pk['source']} (sustained bf16)", "avg_launch_ms": avg_ms,
+                "hbm_gbs_of_min_bytes": by / (avg_ms * 1e-3) / 1e9}
     else:
         achieved = by / (avg_ms * 1e-3) / 1e9
         roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
-                "avg_launch_ms": avg_ms}
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
+                "avg_launch_ms": avg_ms, "tflops": fl / (avg_ms * 1e-3) / 1e12,
+                "algorithmic_bytes": by}
     kernels = {}
+    tot = max(sum(v[0] for v in prof.values()), 1e-9)
     for k, (kms, kl) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
-        f2, b2, bd = work.get(k, (0, 0, "hbm"))
+        f2, b2 = work.get(k, (0, 0))
         a = kms / max(kl, 1)
-        kernels[k] = {"ms_per_step": kms / args.steps, "share": kms / max(sum(v[0] for v in prof.values()), 1e-9),
+        kernels[k] = {"ms_per_step": kms / args.steps, "share": kms / tot,
                       "tflops": f2 / (a * 1e-3) / 1e12 if f2 else None,
-                      "min_bytes_gbs": b2 / (a * 1e-3) / 1e9}
-    launches_per_label = {"permute": 7 if wl.m_tile else 3}
+                      "gbs_of_min_bytes": b2 / (a * 1e-3) / 1e9 if b2 else None,
+                      "bound": ("tensor" if f2 / (pk["bf16_sus"] * 1e12) >= b2 / (pk["hbm_gbs"] * 1e9) else "hbm")}
+    launches_per_label = {"permute": 7 if wl.m_tile else 3}  # one label covers the grouping's kernels
     gpu_launches = int(sum(cnt * launches_per_label.get(k, 1) for k, (_, cnt) in prof.items()))
 
     # end to end through the public API with host buffers: H2D of X and dO, D2H of O and dX per step
@@ -362,6 +505,7 @@ def run_ours(args, rank, world, local_rank):
             "config": {"workload": workload_desc(wl), "pairs": P, "empty_experts": int((counts == 0).sum()),
                        "max_rows_per_expert": int(counts.max()), "dW_dtype": "bf16",
                        "l2": "flushed between steps (256 MB write, outside the per-step events)",
+                       "clock_samples": "nvidia-smi every 50 ms over a 0.5 s busy pre-roll of the same step and the timed region",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tokens_per_s": tokens_s, "pct_of_peak_bf16": 100 * tflops / world / pk["bf16_sus"],
             "peak_bf16_tflops": pk["bf16_sus"], "peak_source": pk["source"] + " sustained",
@@ -385,7 +529,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
+    ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline")
     args = ap.parse_args()
+    if args.profile_run:
+        args.no_e2e = True
+        args.no_cpu_baseline = True
+    if args.ncu_summary:
+        print(ncu_launch_summary(args.ncu_summary))
+        return 0
+    if args.ncu_traffic:
+        print(json.dumps(ncu_traffic(args.ncu_traffic, args.workload), indent=1))
+        return 0
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
