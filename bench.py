@@ -74,7 +74,7 @@ def kernel_work(wl, P, dW_bytes=2):
         "dact_dswiglu": (2 * P * d * n, 2 * P * d + 2 * E * d * n + 8 * P * n + 6 * P * n),
         "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d),
         "wr_transpose": (0, 4 * d * E),
-        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 6 * T * E),
+        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 8 * T * E),
         "dwr_gemm": (2 * T * d * E, 2 * T * d + 2 * T * E + 4 * d * E),
         "dwr_reduce": (0, 8 * d * E),
         "dw_gate_up": (4 * P * d * n, 2 * P * d + 4 * P * n + 2 * dW_bytes * E * n * d),

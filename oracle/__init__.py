@@ -30,4 +30,4 @@ from .moe_oracle import (  # noqa: F401
     token_rounding,
     topk_experts,
 )
-from .metrics import compare, rel_error  # noqa: F401
+from .metrics import WEIGHT_GRAD, compare, rel_error  # noqa: F401

@@ -389,3 +389,27 @@ def test_metric_scale():
     # in a small row the floor is that row's rms, not the tensor's
     assert abs(r["max"] - 0.001 / math.sqrt(0.0009 / 4)) < 1e-9
     assert r["max_global"] < r["max"]
+
+
+def test_metric_weight_gradient_floor():
+    # [experts, rows, cols]: expert 0 has one tiny row, expert 1 is all zero
+    o = np.zeros((2, 2, 3))
+    o[0] = [[3.0, -4.0, 0.0], [1e-6, 0.0, -1e-6]]
+    g = o.copy()
+    g[0, 1, 0] += 1e-7
+    # per-row floor: the tiny row judges the perturbation against its own scale (|o| = 1e-6 here)
+    r = oracle.rel_error(g, o)
+    assert abs(r["max"] - 1e-7 / 1e-6) < 1e-9
+    # weight gradient: floor max(row rms, 1e-3 * rms of expert 0's matrix, sqrt((25 + 2e-12) / 6))
+    r = oracle.rel_error(g, o, param_axes=oracle.WEIGHT_GRAD)
+    assert abs(r["max"] - 1e-7 / (1e-3 * math.sqrt((25 + 2e-12) / 6))) < 1e-12
+    # a big row keeps its own floor: a perturbation of its exact zero is judged against the row rms
+    g = o.copy()
+    g[0, 0, 2] = 0.05
+    r = oracle.rel_error(g, o, param_axes=oracle.WEIGHT_GRAD)
+    assert abs(r["max"] - 0.05 / math.sqrt(25 / 3)) < 1e-12
+    # an all-zero expert is judged against the tensor's rms
+    g = o.copy()
+    g[1, 0, 2] = 1e-3
+    r = oracle.rel_error(g, o, param_axes=oracle.WEIGHT_GRAD)
+    assert abs(r["max"] - 1e-3 / math.sqrt((25 + 2e-12) / 12)) < 1e-12

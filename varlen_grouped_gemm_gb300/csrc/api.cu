@@ -142,7 +142,8 @@ inline int gemm_bn(int N) { return N > 128 ? 256 : 128; }
 constexpr int kMaxSplitK = 16;
 
 struct BwdWs {
-  __nv_bfloat16 *dH, *dU, *Ap, *dXp, *dL, *WrT, *Xs, *dOs;
+  __nv_bfloat16 *dH, *dU, *Ap, *dXp, *WrT, *Xs, *dOs;
+  __nv_bfloat16* dL;  // [2][T][E]: dlogits split into a bf16 high part and the bf16 rounding of the rest
   float* part;
   float* wr_part;
 };
@@ -150,7 +151,7 @@ struct BwdWs {
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
   const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
   return 3 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
-         al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E) +
+         al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(T) * E) +
          al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
          al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
 }
@@ -171,7 +172,7 @@ BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
   w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.part = reinterpret_cast<float*>(take(sizeof(float) * cap * part_ld));
-  w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(T) * E));
+  w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(T) * E));
   w.WrT = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d));
   w.wr_part = reinterpret_cast<float*>(take(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E));
   return w;
@@ -562,7 +563,10 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
   VGG_LAUNCH("token_backward", launch_token_backward(w.part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
                                                      topk_ids, topk_w, K, w.dXp, w.WrT, T, d, cap, dS, dlogits, w.dL,
                                                      static_cast<__nv_bfloat16*>(dX), ctx->d_err, s));
-  // dW_r = X^T dlogits, split over tokens
+  // dW_r = X^T dlogits, split over tokens.  dlogits enters as two bf16 GEMMs, X^T hi + X^T lo with
+  // hi = bf16(dlogits) and lo = bf16(dlogits - hi), which carries ~16 significant bits: a single bf16
+  // rounding of dlogits costs up to a few percent on the columns of heavily loaded experts, whose
+  // gradient sums thousands of tokens' rounding errors.  Partials of both halves are reduced together.
   {
     GemmParams p = base_params(ctx);
     p.M = d;
@@ -571,20 +575,24 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     p.groups = 1;
     const int BN = gemm_bn(E);
     const int tiles = ceil_div(d, BM) * ceil_div(E, BN);
-    int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK));
+    int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK / 2));
     split = std::max(1, std::min(split, ceil_div(T, 8 * BK)));
     p.split_k = split;
-    float* dst = split == 1 ? dW_r : w.wr_part;
-    p.out0 = dst;
     p.ld_out = E;
-    Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, X, d, T, d, 64) || !make_map_2d(&m.b0, w.dL, E, T, E, 64) ||
-        !make_store_map_3d(&m.o0, dst, true, E, d, split, 32))
-      return MOE_ERR_CUDA;
-    m.a1 = m.a0;
-    m.b1 = m.b0;
-    VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
-    if (split > 1) VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
+    for (int half = 0; half < 2; ++half) {
+      float* dst = w.wr_part + static_cast<size_t>(half) * split * d * E;
+      p.out0 = dst;
+      Maps m = zero_maps();
+      if (!make_map_2d(&m.a0, X, d, T, d, 64) ||
+          !make_map_2d(&m.b0, w.dL + static_cast<size_t>(half) * T * E, E, T, E, 64) ||
+          !make_store_map_3d(&m.o0, dst, true, E, d, split, 32))
+        return MOE_ERR_CUDA;
+      m.a1 = m.a0;
+      m.b1 = m.b0;
+      VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
+    }
+    VGG_LAUNCH("dwr_reduce",
+               launch_splitk_reduce(w.wr_part, 2 * split, static_cast<long long>(d) * E, dW_r, s));
   }
   // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok]
   {

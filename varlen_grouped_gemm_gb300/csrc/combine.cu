@@ -190,7 +190,9 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
   for (int e = tid; e < E; e += kCombineThreads) {
     const float v = s_dl[e];
     dlogits[static_cast<long long>(t) * E + e] = v;
-    dL_bf16[static_cast<long long>(t) * E + e] = __float2bfloat16_rn(v);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    dL_bf16[static_cast<long long>(t) * E + e] = hi;
+    dL_bf16[static_cast<long long>(T + t) * E + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
   }
   if (warp == 0) {
     int n = 0;

@@ -75,8 +75,9 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const
 
 cudaError_t launch_transpose_bf16(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out, cudaStream_t s);
 
-// Per token: dS of its pairs (sum of the per-column-tile partials), the router-logit gradient,
-// and dX = sum of the pairs' dX rows + dlogits W_r^T.
+// Per token: dS of its pairs (sum of the per-column-tile partials), the router-logit gradient
+// (fp32, and as bf16 high and low parts in dL_bf16[2][T][E]), and dX = sum of the pairs' dX rows
+// + dlogits W_r^T.
 cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t* tok_ptr, const int32_t* tok_pairs,
                                   const int32_t* offsets, int E, const float* sorted_w, const int32_t* topk_ids,
                                   const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
