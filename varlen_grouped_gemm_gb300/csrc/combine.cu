@@ -214,7 +214,18 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
   const int nv = d >> 3;
   for (int c = tid; c < nv; c += kCombineThreads) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int r = 0; r < cnt; ++r) {
+    int r = 0;
+    for (; r + 4 <= cnt; r += 4) {  // four rows in flight per thread
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = s_j[r + u];
+        q[u] = j >= 0 ? ldg_nc_v4(dXp + static_cast<long long>(j) * d + 8 * c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) add_bf16x8(acc, q[u]);
+    }
+    for (; r < cnt; ++r) {
       const int j = s_j[r];
       if (j >= 0) add_bf16x8(acc, ldg_nc_v4(dXp + static_cast<long long>(j) * d + 8 * c));
     }

@@ -41,7 +41,7 @@ constexpr int kMaxGroups = 1024;
 constexpr int kStgBuf = 4096;    // one staged store: 32 rows x 128 B
 constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 this many stages ahead
 
-enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
+enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3, A_GATHER4_K = 4 };
 enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3 };
@@ -97,8 +97,11 @@ struct SmemLayout {
   static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
-  static constexpr size_t bytes(int groups) {
-    return 1024 + static_cast<size_t>(kMiscOffset) + 16 + 8 * static_cast<size_t>(groups + 2);
+  // Varlen-M keeps the group offsets and tile starts in shared memory; varlen-K reads the offsets
+  // from global memory (a few loads per tile), which leaves room for one more pipeline stage.
+  static constexpr size_t bytes(int groups, int var) {
+    return 1024 + static_cast<size_t>(kMiscOffset) + 16 +
+           (var == VAR_M ? 8 * static_cast<size_t>(groups + 2) : var == VAR_NONE ? 8 : 0);
   }
 };
 
@@ -344,8 +347,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
   int* s_bad = reinterpret_cast<int*>(smem + L::kMiscOffset + 8);
-  int* s_off = reinterpret_cast<int*>(smem + L::kMiscOffset + 16);
-  int* s_tile = s_off + (p.groups + 1);
+  int* s_off_sm = reinterpret_cast<int*>(smem + L::kMiscOffset + 16);
+  const int* s_off = (VAR == VAR_K) ? p.offsets : s_off_sm;
+  int* s_tile = s_off_sm + (p.groups + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -373,11 +377,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   }
   // group offsets into shared memory (validated: start at 0, monotone, within capacity)
-  if (VAR != VAR_NONE) {
-    for (int g = tid; g <= p.groups; g += kThreads) s_off[g] = __ldg(p.offsets + g);
-  } else if (tid == 0) {
-    s_off[0] = 0;
-    s_off[1] = p.M;
+  if (VAR == VAR_M) {
+    for (int g = tid; g <= p.groups; g += kThreads) s_off_sm[g] = __ldg(p.offsets + g);
+  } else if (VAR == VAR_NONE && tid == 0) {
+    s_off_sm[0] = 0;
+    s_off_sm[1] = p.M;
   }
   __syncthreads();
   if (VAR != VAR_NONE && warp == 0) {
@@ -398,13 +402,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (g < p.groups) s_tile[g] = running + incl - cnt;
+      if (VAR == VAR_M && g < p.groups) s_tile[g] = running + incl - cnt;
       running += __shfl_sync(0xffffffffu, incl, 31);
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
       if (s_off[0] != 0 || s_off[p.groups] > p.rows_cap) bad = 1;
-      s_tile[p.groups] = bad ? 0 : running;
+      if (VAR == VAR_M) s_tile[p.groups] = bad ? 0 : running;
       if (bad) {
         *s_bad = 1;
         set_error(p.err, DERR_BAD_OFFSETS);
@@ -420,7 +424,64 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   sch.init(p, s_off, s_tile);
   if (*s_bad) sch.total = 0;
 
-  if (warp == kProdWarp) {
+  if (warp == kProdWarp && AMODE == A_GATHER4_K) {
+    // ---------------------------------------------------------------- TMA producer, gathered A
+    // Lane 0 waits for the stage and loads B; every lane then copies 4 of the tile's 128 A rows
+    // with one tile::gather4 (rows 4 lane .. 4 lane + 3, 128 bytes of K each).  A tile's row
+    // indices are read once per tile; rows past the group's end repeat the tile's first row
+    // (finite data whose results the epilogue never stores).
+    const uint64_t pol_stream = l2_policy_evict_first();
+    int it = 0, gcur = 0, cur_t = -1;
+    int r4[4] = {0, 0, 0, 0};
+    bool aborted = false;
+    Pos q = pos_first(sch, p, gcur);
+    while (q.t < sch.total) {
+      const int s = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        aborted = true;
+        break;
+      }
+      if (q.t != cur_t) {
+        cur_t = q.t;
+        const int* idx = p.a_idx + s_off[q.tl.g] + q.tl.m0;
+        const int first = __ldg(idx);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * lane + i;
+          int row = rr < q.tl.rows ? __ldg(idx + rr) : first;
+          if (row < 0 || row >= p.a_rows) {
+            set_error(p.err, DERR_BAD_OFFSETS);
+            row = 0;
+          }
+          r4[i] = row;
+        }
+      }
+      uint8_t* sa = smem + s * L::kStageBytes;
+      uint8_t* sb = sa + L::kABytes;
+      const int kg = q.tl.k_begin + q.ks * BK;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
+        if (BMODE == B_TMA_K3_GU) {
+          tma_load_3d_hint(sb, &mp.b0, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
+          tma_load_3d_hint(sb + (BN / 2) * 128, &mp.b1, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
+        } else if (BMODE == B_TMA_K3) {
+          tma_load_3d_hint(sb, &mp.b0, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
+        }
+      }
+      __syncwarp();
+      tma_gather4(sa + lane * 512, &mp.a0, &full_bar[s], kg, r4[0], r4[1], r4[2], r4[3]);
+      ++it;
+      pos_next(sch, p, gcur, q);
+    }
+    if (aborted && lane == 0) {
+      volatile int never = 0;
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
+    }
+  } else if (warp == kProdWarp) {
     // ---------------------------------------------------------------- TMA producer (one thread)
     if (lane == 0) {
       // Expert weights are read by the few tiles of one expert and then never again: stream them
@@ -916,7 +977,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32>;
-  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH>::bytes(p.groups);
+  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH>::bytes(p.groups, VAR);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;

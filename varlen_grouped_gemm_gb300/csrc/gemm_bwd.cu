@@ -1,5 +1,5 @@
-// Backward grouped-GEMM instantiations.  Template arguments as in gemm_fwd.cu; the kernels whose
-// epilogue writes several outputs per tile use 8 epilogue warps and 2 staged stores per warp,
+// Backward grouped-GEMM instantiations.  Template arguments as in gemm_fwd.cu; the dSwiGLU kernel,
+// whose epilogue writes three outputs per tile, uses 8 epilogue warps and 2 staged stores per warp,
 // paid for with one pipeline stage.
 #include "internal.h"
 
@@ -19,13 +19,15 @@ cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, c
 }
 
 // Varlen-K weight gradient with both operands read by TMA from expert-sorted rows; the rows past the
-// group's end in its last stage are cleared in shared memory before the last UMMAs.
+// group's end in its last stage are cleared in shared memory before the last UMMAs.  A tile reduces
+// over one expert's rows only (a few stages), so the ring's depth sets the bytes in flight: 4 stages
+// and one staged store per epilogue warp measured faster than 3 stages with two.
 cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256)
-    return f32 ? launch_grouped_gemm<256, 3, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
-               : launch_grouped_gemm<256, 3, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
-  return f32 ? launch_grouped_gemm<128, 4, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
-             : launch_grouped_gemm<128, 4, 8, 2, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+    return f32 ? launch_grouped_gemm<256, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+               : launch_grouped_gemm<256, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
+             : launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
 }
 
 // Varlen-K with one operand gathered through a token index (cp.async, zero past the group's end).

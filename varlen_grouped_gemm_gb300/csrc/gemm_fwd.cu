@@ -14,6 +14,13 @@ cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int g
   return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
 }
 
+// The same with A's rows copied by TMA tile::gather4 (map box {64 columns, 1 row}).
+cudaError_t run_gate_up_swiglu_g4(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256)
+    return launch_grouped_gemm<256, 4, 4, 1, A_GATHER4_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_GATHER4_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+}
+
 // Down projection, A = sorted activation rows, epilogue scales by the combine weight.
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);

@@ -28,6 +28,7 @@ bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint
 // ---- grouped GEMM instantiations (BN chosen at run time: 128 or 256) -------------------------
 // forward
 cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_gate_up_swiglu_g4(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
@@ -60,6 +61,7 @@ struct PermuteWs {
   int32_t* plain_off;  // [E + 1]
   int32_t* plain_cnt;  // [E]
   int32_t* plain_tok;  // [T * K]
+  float* scoresT;      // [E * T] scores transposed (token rounding)
 };
 size_t permute_ws_bytes(int T, int E, int K, int m_tile);
 PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile);

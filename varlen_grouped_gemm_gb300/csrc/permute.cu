@@ -161,49 +161,66 @@ __global__ void __launch_bounds__(kTokBlock) perm_hist_kernel(const int32_t* __r
 
 // One block of 1024 threads: exclusive scan of hist (expert-major) in place,
 // offsets/counts, and the exclusive scan of the per-block token pair counts.
+// hist is scanned in tiles of 8192 staged in shared memory (coalesced loads and
+// stores; each thread scans 8 consecutive entries), with a carry between tiles.
+constexpr int kScanTile = 8192;
+
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int E, int nb,
                                                          int32_t* __restrict__ tokblk, int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ P_out,
                                                          long long cap, int* err) {
   __shared__ int s_warp[33];
   __shared__ int s_tok[33];
+  __shared__ int tile[kScanTile];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long N = static_cast<long long>(E) * nb;
-  const long long chunk = (N + 1023) / 1024;
-  const long long lo = tid * chunk, hi = min(N, lo + chunk);
-  int local = 0;
-  for (long long i = lo; i < hi; ++i) local += hist[i];
-  // block exclusive scan of `local`
-  int incl = local;
+  int carry = 0;
+  for (long long base = 0; base < N; base += kScanTile) {
+    for (int i = tid; i < kScanTile; i += 1024) tile[i] = (base + i < N) ? hist[base + i] : 0;
+    __syncthreads();
+    int v[8];
+    int local = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = s_warp[lane];
-    int wi = w;
+    for (int q = 0; q < 8; ++q) {
+      v[q] = tile[8 * tid + q];
+      local += v[q];
+    }
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    s_warp[lane] = wi - w;
-    if (lane == 31) s_warp[32] = wi;
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = s_warp[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      s_warp[lane] = wi - w;
+      if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    int run = carry + s_warp[warp] + incl - local;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      tile[8 * tid + q] = run;
+      run += v[q];
+    }
+    carry += s_warp[32];
+    __syncthreads();
+    for (int i = tid; i < kScanTile; i += 1024)
+      if (base + i < N) hist[base + i] = tile[i];
+    __syncthreads();
   }
-  __syncthreads();
-  int run = s_warp[warp] + incl - local;
-  for (long long i = lo; i < hi; ++i) {
-    const int v = hist[i];
-    hist[i] = run;
-    run += v;
-  }
-  const int total = s_warp[32];
+  const int total = carry;
   // per-block token pair bases (nb <= 256 -> a few warps)
   if (warp == 0) {
-    int carry = 0;
+    int tcarry = 0;
     for (int base = 0; base < nb; base += 32) {
       const int i = base + lane;
       const int v = (i < nb) ? tokblk[i] : 0;
@@ -213,12 +230,12 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      if (i < nb) tokblk[i] = carry + x - v;
-      carry += __shfl_sync(0xffffffffu, x, 31);
+      if (i < nb) tokblk[i] = tcarry + x - v;
+      tcarry += __shfl_sync(0xffffffffu, x, 31);
     }
     if (lane == 0) {
-      tokblk[nb] = carry;
-      s_tok[0] = carry;
+      tokblk[nb] = tcarry;
+      s_tok[0] = tcarry;
     }
   }
   __syncthreads();
@@ -281,43 +298,96 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
   }
 }
 
+// out[c][r] = in[r][c] for fp32 [rows x cols], 32x32 tiles through shared memory: the token
+// rounding select reads one expert's scores for all tokens, a column of the [T x E] scores.
+__global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[static_cast<long long>(r) * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[static_cast<long long>(c) * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
 // Token rounding, one CTA per expert: choose the final token set of expert e
 // and mark it in the membership bitmap.  Priority of a token for e is
 // (score descending, token ascending); the selection is a radix select of the
 // need-th largest score among the candidates, ties at the threshold resolved
-// by ascending token.  Keys (score bits) are staged in shared memory.
+// by ascending token.  Keys (score bits; positive floats order as integers)
+// are staged in shared memory.  The first digit (bits 31..21) is histogrammed
+// over all candidates; the keys of the bin holding the threshold are then
+// compacted into a short list that the two remaining digits (20..10, 9..0)
+// scan, so only one pass touches every token.
 constexpr int kTrThreads = 1024;
 constexpr int kTrMaxT = 32768;
+constexpr int kTrListCap = 8192;  // compacted keys of the threshold bin; a larger bin rescans all keys
 
-__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_warp[warp] = incl;
+// Histogram of digit (k >> shift) & (NB - 1) over keys matching `prefix` on `mask` (0xFFFFFFFF = not a
+// candidate), then the digit of the remaining-th largest: lane l of warp 0 owns NB/32 bins, a suffix
+// scan over lanes finds the owner of the bin, which walks its bins downwards.  Updates prefix, mask,
+// remaining; returns the count of the chosen bin.  Lanes with the same digit add once per warp.
+template <int NB>
+__device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& mask, int shift, int& remaining,
+                        int* hist, int* s_res) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i < NB; i += kTrThreads) hist[i] = 0;
   __syncthreads();
-  if (warp == 0) {
-    const int w = s_warp[lane];
-    int wi = w;
+  for (int i0 = 0; i0 < n; i0 += kTrThreads) {
+    const int i = i0 + tid;
+    uint32_t dg = NB;
+    if (i < n) {
+      const uint32_t k = a[i];
+      if (k != 0xFFFFFFFFu && (k & mask) == prefix) dg = (k >> shift) & (NB - 1);
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, dg);
+    if (dg != static_cast<uint32_t>(NB) && lane == __ffs(grp) - 1) atomicAdd(&hist[dg], __popc(grp));
+  }
+  __syncthreads();
+  if (tid < 32) {
+    constexpr int PER = NB / 32;
+    int sl = 0;
+    for (int i = 0; i < PER; ++i) sl += hist[PER * lane + i];
+    int suf = sl;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
+      const int y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
     }
-    s_warp[lane] = wi - w;
-    if (lane == 31) s_warp[32] = wi;
+    const unsigned reach = __ballot_sync(0xffffffffu, suf >= remaining);
+    const int owner = reach ? 31 - __clz(reach) : 0;
+    if (lane == owner) {
+      int cum = suf - sl;
+      int digit = PER * lane, cnt = 0;
+      for (int i = PER - 1; i >= 0; --i) {
+        const int h = hist[PER * lane + i];
+        if (cum + h >= remaining) {
+          digit = PER * lane + i;
+          cnt = h;
+          break;
+        }
+        cum += h;
+      }
+      s_res[0] = digit;
+      s_res[1] = remaining - cum;
+      s_res[2] = cnt;
+    }
   }
   __syncthreads();
-  const int res = s_warp[warp] + incl - v;
-  total = s_warp[32];
+  prefix |= static_cast<uint32_t>(s_res[0]) << shift;
+  mask |= static_cast<uint32_t>(NB - 1) << shift;
+  remaining = s_res[1];
+  const int cnt = s_res[2];
   __syncthreads();
-  return res;
+  return cnt;
 }
 
-__global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __restrict__ scores, int T, int E,
+
+__global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __restrict__ scoresT, int T, int E,
                                                               int m_tile, const int32_t* __restrict__ plain_off,
                                                               const int32_t* __restrict__ plain_tok,
                                                               long long plain_cap, uint32_t* __restrict__ member,
@@ -325,9 +395,9 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
   extern __shared__ uint32_t tr_smem[];
   uint32_t* keys = tr_smem;               // [T]; 0xFFFFFFFF = not a candidate
   uint32_t* routed = tr_smem + T;         // [ceil(T/32)]
-  __shared__ int hist[256];
-  __shared__ int s_warp[33];
-  __shared__ int s_digit, s_remaining;
+  uint32_t* list = routed + ((T + 31) >> 5);  // [kTrListCap] keys of the threshold bin
+  __shared__ int hist[2048];
+  __shared__ int s_res[4];
   const int e = blockIdx.x, tid = threadIdx.x;
   const int W = (E + 31) >> 5;
   const int TW = (T + 31) >> 5;
@@ -357,54 +427,73 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
   }
   const int need = drop ? r : r - c;
   if (need == 0) return;
+  const float* col = scoresT + static_cast<long long>(e) * T;  // this expert's scores, token-contiguous
+#pragma unroll 4
   for (int t = tid; t < T; t += kTrThreads) {
     const bool is_routed = (routed[t >> 5] >> (t & 31)) & 1u;
     const bool cand = drop ? is_routed : !is_routed;
-    keys[t] = cand ? __float_as_uint(scores[static_cast<long long>(t) * E + e]) : 0xFFFFFFFFu;
+    keys[t] = cand ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
   }
   __syncthreads();
   uint32_t prefix = 0, mask = 0;
   int remaining = need;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kTrThreads) hist[i] = 0;
-    __syncthreads();
-    for (int t = tid; t < T; t += kTrThreads) {
-      const uint32_t k = keys[t];
-      if (k != 0xFFFFFFFFu && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int cum = 0, digit = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        if (cum + hist[dgt] >= remaining) {
-          digit = dgt;
-          break;
-        }
-        cum += hist[dgt];
-      }
-      s_digit = digit;
-      s_remaining = remaining - cum;
-    }
-    __syncthreads();
-    prefix |= static_cast<uint32_t>(s_digit) << shift;
-    mask |= 255u << shift;
-    remaining = s_remaining;
-    __syncthreads();
+  const int lane = tid & 31;
+  tr_digit<2048>(keys, T, prefix, mask, 21, remaining, hist, s_res);
+  // compact the keys of the threshold bin (warp-aggregated appends; order is irrelevant here)
+  if (tid == 0) s_res[3] = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += kTrThreads) {
+    const int t = t0 + tid;
+    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
+    const bool in = k != 0xFFFFFFFFu && (k & mask) == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, in);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_res[3], __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (in && pos < kTrListCap) list[pos] = k;
+  }
+  __syncthreads();
+  const int nlist = s_res[3];
+  int ties;
+  if (nlist <= kTrListCap) {
+    tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
+  } else {
+    tr_digit<2048>(keys, T, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(keys, T, prefix, mask, 0, remaining, hist, s_res);
   }
   // keys above the threshold are all taken; at the threshold the `remaining` lowest tokens.
-  const int per = (T + kTrThreads - 1) / kTrThreads;
-  const int t0 = tid * per, t1 = min(T, t0 + per);
-  int ties = 0;
-  for (int t = t0; t < t1; ++t) ties += (keys[t] == prefix);
-  int tot;
-  int before = block_exclusive_scan_1024(ties, s_warp, tot);
-  for (int t = t0; t < t1; ++t) {
-    const uint32_t k = keys[t];
-    if (k == 0xFFFFFFFFu) continue;
-    bool take = k > prefix;
-    if (k == prefix) take = (before++ < remaining);
-    if (take) atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
+  if (ties == remaining) {  // every tie is taken: no order needed
+    for (int t = tid; t < T; t += kTrThreads) {
+      const uint32_t k = keys[t];
+      if (k != 0xFFFFFFFFu && k >= prefix) atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
+    }
+    return;
+  }
+  // Equal scores beyond the need: tokens in chunks of 1024 consecutive ones; a tie's rank in token
+  // order is the ties of earlier chunks, of earlier warps of this chunk and of lower lanes.
+  __shared__ int s_wties[kTrThreads / 32];
+  const int warp_id = tid >> 5;
+  int tie_base = 0;
+  for (int base = 0; base < T; base += kTrThreads) {
+    const int t = base + tid;
+    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
+    const bool cand = k != 0xFFFFFFFFu;
+    const bool tie = cand && k == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    if (lane == 0) s_wties[warp_id] = __popc(bal);
+    __syncthreads();
+    int before = tie_base + __popc(bal & ((1u << lane) - 1u)), chunk_ties = 0;
+    for (int w = 0; w < kTrThreads / 32; ++w) {
+      const int cw = s_wties[w];
+      if (w < warp_id) before += cw;
+      chunk_ties += cw;
+    }
+    if (cand && (k > prefix || (tie && before < remaining)))
+      atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
+    tie_base += chunk_ties;
+    __syncthreads();
   }
 }
 
@@ -415,6 +504,7 @@ size_t permute_ws_bytes(int T, int E, int K, int m_tile) {
   if (m_tile > 0) {
     b += al(sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32));
     b += al(sizeof(int32_t) * (E + 1)) + al(sizeof(int32_t) * E) + al(sizeof(int32_t) * static_cast<size_t>(T) * K);
+    b += al(sizeof(float) * static_cast<size_t>(T) * E);
   }
   return b;
 }
@@ -436,6 +526,8 @@ PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile) {
     w.plain_cnt = reinterpret_cast<int32_t*>(p);
     p += al(sizeof(int32_t) * E);
     w.plain_tok = reinterpret_cast<int32_t*>(p);
+    p += al(sizeof(int32_t) * static_cast<size_t>(T) * K);
+    w.scoresT = reinterpret_cast<float*>(p);
   }
   return w;
 }
@@ -466,11 +558,12 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   // final token sets
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
-  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + (T + 31) / 32);
+  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + (T + 31) / 32 + kTrListCap);
   st = cudaFuncSetAttribute(tr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrMaxT / 32)));
+                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrMaxT / 32 + kTrListCap)));
   if (st != cudaSuccess) return st;
-  tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(scores, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
+  transpose_f32_kernel<<<dim3((E + 31) / 32, (T + 31) / 32), dim3(32, 8), 0, s>>>(scores, T, E, w.scoresT);
+  tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(w.scoresT, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
                                                  w.member, err);
   // group the final pairs
   perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);

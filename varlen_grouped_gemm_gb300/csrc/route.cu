@@ -66,21 +66,24 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
     w[static_cast<long long>(t) * K + lane] = my_ex / sum;
   }
   if (scores) {
+    // full softmax for token rounding's priorities: the fast exponential and one reciprocal (the
+    // selection compares these values among themselves; relative error ~1e-6)
     float z = 0.0f;
     float ex[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      ex[i] = (e < E) ? expf(v[i] - vmax) : 0.0f;
+      ex[i] = (e < E) ? __expf(v[i] - vmax) : 0.0f;
       z += ex[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv = 1.0f / z;
     float* srow = scores + static_cast<long long>(t) * E;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) srow[e] = ex[i] / z;
+      if (e < E) srow[e] = ex[i] * inv;
     }
   }
 }
