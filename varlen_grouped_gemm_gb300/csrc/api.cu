@@ -4,7 +4,6 @@
 
 #include <algorithm>
 #include <climits>
-#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -26,7 +25,7 @@ struct moe_ctx {
   unsigned long long timeout_ns;
   bool prof = false;
   int l2_prefetch = 0;  // L2 prefetch of later stages (measured slower; kept switchable)
-  int gather_tma = 0;   // gate/up A rows by TMA gather4 instead of cp.async
+
   std::vector<cudaEvent_t> pool;
   size_t pool_next = 0;
   std::vector<ProfRecord> pending;
@@ -290,7 +289,6 @@ int moe_create(moe_ctx** out, int device) {
   c->device = device;
   c->num_sms = sms;
   c->timeout_ns = 2000000000ull;
-  if (const char* g4 = std::getenv("VGG_GATHER_TMA")) c->gather_tma = std::atoi(g4);
   if (cudaMalloc(&c->d_err, 16) != cudaSuccess || cudaMemset(c->d_err, 0, 16) != cudaSuccess) {
     delete c;
     return MOE_ERR_CUDA;
@@ -439,16 +437,14 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     p.ld_out = n;
     const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
-    if (ctx->gather_tma && !make_map_2d(&m.a0, X, d, T, d, 1)) return MOE_ERR_CUDA;
     if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) ||
         !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) || !make_store_map_2d(&m.o0, H, true, n, cap, n, 32) ||
         !make_store_map_2d(&m.o1, U, true, n, cap, n, 32) || !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
-    if (ctx->gather_tma)
-      VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu_g4(BN, p, m, std::min(tiles, ctx->num_sms), s));
-    else
-      VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, p, m, std::min(tiles, ctx->num_sms), s));
+    // pairs of CTAs on neighbouring column tiles share the gathered X rows (each gathers half)
+    const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
+    VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // down projection, scaled by the combine weight of each row
   {

@@ -3,16 +3,21 @@
 //   D[128 x BN] (+)= A[128 x K] * B[K x BN]    bf16 operands, fp32 accumulation in TMEM
 //
 // One CTA per SM walks a static round-robin list of output tiles.  Warp roles:
-//   warps 0-3  epilogue: tcgen05.ld of the accumulator (row i of the tile = TMEM lane i),
-//              fused elementwise work, results staged in shared memory per 32-row block
-//              and written by TMA stores;
-//   warp  4    TMA producer (one thread) for dense operands, with an L2 prefetch of the
-//              boxes a few stages ahead; owns the TMEM allocation;
-//   warp  5    UMMA issuer (one thread);
-//   warps 6-9  present when an operand's rows are gathered through a token index: they
+//   warps 0..EW-1  epilogue (4 or 8): tcgen05.ld of the accumulator (row i of the tile = TMEM
+//              lane i), fused elementwise work, results staged in shared memory per 32-row
+//              block and written by TMA stores;
+//   warp  EW   TMA producer (lane 0) for the tiled operands; owns the TMEM allocation.  Loads
+//              issued by one thread complete one after another, so the ring's stages are dealt
+//              round-robin to up to 4 producer threads (this one and extra warps placed last);
+//   warp  EW+1 UMMA issuer (lane 0);
+//   warps EW+2..EW+5  present when an operand's rows are gathered through a token index: they
 //              copy those rows with cp.async (16 B per thread, zero-filled past the end)
 //              straight into the swizzled stage, so the permuted activations are never
-//              written ([SM] "4.1 Gather 융합"); the index lookups run two stages ahead.
+//              written ([SM] "4.1 Gather 융합"); the index lookups run two stages ahead;
+//   relay warp present with clusters of CN CTAs on neighbouring column tiles of one row tile:
+//              each CTA gathers 128/CN of the rows and the relay copies its slice into the
+//              peers' shared memory (distributed shared memory), so the gathered activations
+//              are read from L2 once per cluster instead of once per CTA.
 // Shared memory holds STAGES ring slots of A (128 x 64) and B (BN x 64) in the
 // 128-byte-swizzled layout that TMA writes and the UMMA descriptors read.  TMEM
 // holds two BN-column accumulators so that the epilogue of tile i overlaps the
@@ -41,7 +46,7 @@ constexpr int kMaxGroups = 1024;
 constexpr int kStgBuf = 4096;    // one staged store: 32 rows x 128 B
 constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 this many stages ahead
 
-enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3, A_GATHER4_K = 4 };
+enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3 };
@@ -95,7 +100,7 @@ struct SmemLayout {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStgOffset = STAGES * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kNumBars = 3 * STAGES + 5;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   // Varlen-M keeps the group offsets and tile starts in shared memory; varlen-K reads the offsets
   // from global memory (a few loads per tile), which leaves room for one more pipeline stage.
@@ -116,16 +121,24 @@ struct Tile {
   int split;    // VAR_NONE: K split index
 };
 
-template <int BN, int BMODE, int VAR>
+// With CN > 1 (varlen-M only) the CN CTAs of a cluster take the same (group, row tile) with
+// consecutive column tiles: a work unit is (group, row tile, group of CN column tiles) and the CTA
+// of cluster rank r computes column tile CN * unit_col + r (past the last one it computes nothing
+// that is stored, but still takes part in loading the shared operand).
+template <int BN, int BMODE, int VAR, int CN = 1>
 struct Sched {
   static constexpr int kColsPerTile = (BMODE == B_TMA_K3_GU) ? BN / 2 : BN;
   int ntiles, mtiles, per_group, total, ks_len;
+  int first, stride, rank;  // this CTA's first unit, the unit stride, its rank in the cluster
   const int* s_off;
   const int* s_tile;
 
   __device__ void init(const GemmParams& p, const int* off, const int* tile) {
     s_off = off;
     s_tile = tile;
+    rank = (CN > 1) ? static_cast<int>(blockIdx.x % CN) : 0;
+    first = static_cast<int>(blockIdx.x / CN);
+    stride = static_cast<int>(gridDim.x / CN);
     ntiles = (p.N + kColsPerTile - 1) / kColsPerTile;
     mtiles = (p.M + BM - 1) / BM;
     if (VAR == VAR_M) {
@@ -148,7 +161,7 @@ struct Sched {
       const int rows_g = s_off[g + 1] - s_off[g];
       const int mt_g = (rows_g + BM - 1) / BM;
       const int l = t - s_tile[g];
-      const int mt = l % mt_g, nt = l / mt_g;
+      const int mt = l % mt_g, nt = (l / mt_g) * CN + rank;
       tl.g = g;
       tl.m0 = mt * BM;
       tl.nt = nt;
@@ -198,7 +211,7 @@ __device__ __forceinline__ void pos_next(const S& sch, const GemmParams& p, int&
     return;
   }
   q.ks = 0;
-  for (q.t += gridDim.x; q.t < sch.total; q.t += gridDim.x) {
+  for (q.t += sch.stride; q.t < sch.total; q.t += sch.stride) {
     sch.decode(p, q.t, gcur, q.tl);
     q.nk = (q.tl.k_len + BK - 1) / BK;
     if (q.nk > 0) return;
@@ -208,7 +221,7 @@ __device__ __forceinline__ void pos_next(const S& sch, const GemmParams& p, int&
 template <class S>
 __device__ __forceinline__ Pos pos_first(const S& sch, const GemmParams& p, int& gcur) {
   Pos q;
-  q.t = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+  q.t = sch.first - sch.stride;
   q.ks = 0;
   q.nk = 0;
   pos_next(sch, p, gcur, q);
@@ -315,7 +328,16 @@ struct OutRef {
 
 // -------------------------------------------------------------------------- the kernel
 
-template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+// Producer threads for a ring of `stages` with `spare` warps left: the largest of 4, 3, 2 that
+// divides the stage count and fits, else 1.
+__host__ __device__ constexpr int gemm_producers(int stages, int spare) {
+  return (stages % 4 == 0 && spare >= 3)   ? 4
+         : (stages % 3 == 0 && spare >= 2) ? 3
+         : (stages % 2 == 0 && spare >= 1) ? 2
+                                           : 1;
+}
+
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
   using L = SmemLayout<BN, STAGES, EW, DEPTH>;
@@ -330,9 +352,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   constexpr int kProdWarp = EW;        // TMA producer, owns TMEM
   constexpr int kMmaWarp = EW + 1;     // UMMA issuer
   constexpr int kGatherWarp0 = EW + 2; // cp.async gather warps (4) when an operand is gathered
-  constexpr int kThreads = (EW + 2 + (kGather ? 4 : 0)) * 32;
+  // Clusters of CN CTAs along N share the gathered A tile: each CTA gathers rows
+  // [rank * kSlice, (rank + 1) * kSlice) and a relay thread copies them to the peers.
+  static_assert(CN == 1 || (CN == 2 || CN == 4), "cluster of 1, 2 or 4");
+  static_assert(CN == 1 || (AMODE == A_GATHER_K && VAR == VAR_M && !kBGather), "clusters share a gathered A");
+  constexpr bool kRelay = (CN > 1);
+  constexpr int kSlice = BM / CN;               // A rows gathered by each CTA of a cluster
+  constexpr uint32_t kSliceBytes = kSlice * 128;
+  constexpr int kRelayWarp = EW + 2 + 4;
+  // TMA loads issued by one thread complete one after another; stages are spread round-robin over
+  // kNP producer threads (lane 0 of the producer warp and of kNP - 1 extra warps placed last), so
+  // that several stages are in flight at once.  kNP divides STAGES: a stage always has the same
+  // producer.
+  constexpr int kBaseWarps = EW + 2 + (kGather ? 4 : 0) + (kRelay ? 1 : 0);
+  constexpr int kNP = gemm_producers(STAGES, kMaxThreads / 32 - kBaseWarps);
+  constexpr int kXProdWarp0 = kBaseWarps;  // extra producer warps
+  constexpr int kThreads = (kBaseWarps + kNP - 1) * 32;
   static_assert(kThreads <= kMaxThreads, "threads");
-  constexpr uint32_t kTxBytes = (kAGather ? 0 : L::kABytes) + (kBGather ? 0 : L::kBBytes);
+  constexpr uint32_t kTxBytes =
+      (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
@@ -344,6 +382,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint64_t* tfull_bar = bars + 2 * STAGES;
   uint64_t* tempty_bar = bars + 2 * STAGES + 2;
   uint64_t* drain_bar = bars + 2 * STAGES + 4;
+  uint64_t* gath_bar = bars + 2 * STAGES + 5;  // [STAGES] own A slice gathered (relay mode)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
   int* s_bad = reinterpret_cast<int*>(smem + L::kMiscOffset + 8);
@@ -357,8 +396,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1 + (kGather ? 128 : 0));
-      mbar_init(&empty_bar[s], 1);
+      // relay mode: the producer's expect_tx and the relay's arrival; else the producer and,
+      // with a gathered operand, the 128 gather threads
+      mbar_init(&full_bar[s], kRelay ? 2 : 1 + (kGather ? 128 : 0));
+      mbar_init(&empty_bar[s], CN);  // every CTA of the cluster releases the stage
+      if (kRelay) mbar_init(&gath_bar[s], 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -393,8 +435,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int rows_g = s_off[g + 1] - s_off[g];
         if (rows_g < 0) bad = 1;
         if (VAR == VAR_M)
-          cnt = max(0, (rows_g + BM - 1) / BM) * ((p.N + Sched<BN, BMODE, VAR>::kColsPerTile - 1) /
-                                                  Sched<BN, BMODE, VAR>::kColsPerTile);
+          cnt = max(0, (rows_g + BM - 1) / BM) *
+                (((p.N + Sched<BN, BMODE, VAR>::kColsPerTile - 1) / Sched<BN, BMODE, VAR>::kColsPerTile + CN - 1) /
+                 CN);
       }
       int incl = cnt;
 #pragma unroll
@@ -418,75 +461,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CN > 1) cluster_sync();  // the peers' barriers are initialised before anything targets them
   const uint32_t tmem_base = *s_tmem;
 
-  Sched<BN, BMODE, VAR> sch;
+  Sched<BN, BMODE, VAR, CN> sch;
   sch.init(p, s_off, s_tile);
   if (*s_bad) sch.total = 0;
 
-  if (warp == kProdWarp && AMODE == A_GATHER4_K) {
-    // ---------------------------------------------------------------- TMA producer, gathered A
-    // Lane 0 waits for the stage and loads B; every lane then copies 4 of the tile's 128 A rows
-    // with one tile::gather4 (rows 4 lane .. 4 lane + 3, 128 bytes of K each).  A tile's row
-    // indices are read once per tile; rows past the group's end repeat the tile's first row
-    // (finite data whose results the epilogue never stores).
-    const uint64_t pol_stream = l2_policy_evict_first();
-    int it = 0, gcur = 0, cur_t = -1;
-    int r4[4] = {0, 0, 0, 0};
-    bool aborted = false;
-    Pos q = pos_first(sch, p, gcur);
-    while (q.t < sch.total) {
-      const int s = it % STAGES;
-      const uint32_t ph = (it / STAGES) & 1;
-      int ok = 0;
-      if (lane == 0) ok = mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        aborted = true;
-        break;
-      }
-      if (q.t != cur_t) {
-        cur_t = q.t;
-        const int* idx = p.a_idx + s_off[q.tl.g] + q.tl.m0;
-        const int first = __ldg(idx);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = 4 * lane + i;
-          int row = rr < q.tl.rows ? __ldg(idx + rr) : first;
-          if (row < 0 || row >= p.a_rows) {
-            set_error(p.err, DERR_BAD_OFFSETS);
-            row = 0;
-          }
-          r4[i] = row;
-        }
-      }
-      uint8_t* sa = smem + s * L::kStageBytes;
-      uint8_t* sb = sa + L::kABytes;
-      const int kg = q.tl.k_begin + q.ks * BK;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
-        if (BMODE == B_TMA_K3_GU) {
-          tma_load_3d_hint(sb, &mp.b0, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
-          tma_load_3d_hint(sb + (BN / 2) * 128, &mp.b1, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
-        } else if (BMODE == B_TMA_K3) {
-          tma_load_3d_hint(sb, &mp.b0, &full_bar[s], kg, q.tl.n0, q.tl.g, pol_stream);
-        }
-      }
-      __syncwarp();
-      tma_gather4(sa + lane * 512, &mp.a0, &full_bar[s], kg, r4[0], r4[1], r4[2], r4[3]);
-      ++it;
-      pos_next(sch, p, gcur, q);
-    }
-    if (aborted && lane == 0) {
-      volatile int never = 0;
-      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-        mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
-    }
-  } else if (warp == kProdWarp) {
-    // ---------------------------------------------------------------- TMA producer (one thread)
+  if (warp == kProdWarp || (warp >= kXProdWarp0 && warp < kXProdWarp0 + kNP - 1)) {
+    // ---------------------------------------------------------------- TMA producers (lane 0 each)
+    const int pj = (warp == kProdWarp) ? 0 : warp - kXProdWarp0 + 1;  // this thread's stages: it % kNP == pj
     if (lane == 0) {
-      // Expert weights are read by the few tiles of one expert and then never again: stream them
-      // through L2 (evict first) so that the gathered activations stay resident.
-      const uint64_t pol_stream = l2_policy_evict_first();
+      // An expert's weight tile is read by the CTAs on the expert's row tiles at about the same
+      // time: normal L2 priority lets the later ones hit (evict-first measured up to 25% slower).
+      const uint64_t pol_stream = l2_policy_evict_normal();
       // Loads (or, with l2 = true, L2 prefetches) of the tiled operands of one stage.
       auto tiled = [&](const Tile& x, int kstage, uint8_t* sa, uint8_t* sb, uint64_t* bar, bool l2) {
         const int kg = x.k_begin + kstage * BK;
@@ -540,6 +528,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       bool aborted = false;
       Pos q = pos_first(sch, p, gcur);
       while (q.t < sch.total && !aborted) {
+        if (it % kNP != pj) {  // another producer's stage
+          ++it;
+          pos_next(sch, p, gcur, q);
+          continue;
+        }
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!mbar_wait(&empty_bar[s], ph ^ 1, s_abort, p.timeout_ns, p.err)) {
@@ -565,29 +558,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         pos_next(sch, p, gcur, q);
       }
       if (aborted) {
-        // let copies already in flight land before the CTA goes away
+        // let this thread's copies already in flight land before the CTA goes away
         volatile int never = 0;
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
+          if (j % kNP == pj) mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
+      } else if (CN > 1) {
+        // every CTA's release of this thread's last stages has arrived here, so no peer still
+        // targets this CTA's barriers when it leaves
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          if (j % kNP == pj) mbar_wait(&empty_bar[j % STAGES], (j / STAGES) & 1, s_abort, p.timeout_ns, p.err);
       }
     }
-  } else if (kGather && warp >= kGatherWarp0) {
+  } else if (kGather && warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
     // ---------------------------------------------------------------- cp.async gather producers
     // Thread ptid owns the 16-byte piece c16 of rows rsub + 16 i of every stage.  The token
     // indices of a position are loaded two positions ahead of its copies.
     const int ptid = tid - kGatherWarp0 * 32;
     const int c16 = ptid & 7;
     const int rsub = ptid >> 3;
+    constexpr int kRowsPer = kSlice / 16;   // A rows per thread and stage (8 without a cluster)
+    const int slice0 = sch.rank * kSlice;  // first tile row gathered by this CTA
     const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
     auto fetch = [&](const Pos& x, int (&r)[8], const Pos& prev, const int (&pr)[8]) {
       if (AMODE == A_GATHER_K) {
         if (x.t == prev.t) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) r[i] = pr[i];
+          for (int i = 0; i < kRowsPer; ++i) r[i] = pr[i];
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = rsub + 16 * i;
+          for (int i = 0; i < kRowsPer; ++i) {
+            const int rr = slice0 + rsub + 16 * i;
             r[i] = rr < x.tl.rows ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
           }
         }
@@ -624,15 +624,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       if (AMODE == A_GATHER_K) {
         const int kc = q0.tl.k_begin + q0.ks * BK + c16 * 8;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kRowsPer; ++i) {
           const long long row = r0[i];
           bool ok = row >= 0;
           if (ok && row >= p.a_rows) {
             set_error(p.err, DERR_BAD_OFFSETS);
             ok = false;
           }
-          cp_async_16_hint(sa + sw128_offset(rsub + 16 * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src, ok ? 16u : 0u,
-                           pol_keep);
+          cp_async_16_hint(sa + sw128_offset(slice0 + rsub + 16 * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src,
+                           ok ? 16u : 0u, pol_keep);
         }
       } else if (AMODE == A_GATHER_MN) {
 #pragma unroll
@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                            ok ? p.b_src + row * p.b_ld + col : p.b_src, ok ? 16u : 0u, pol_keep);
         }
       }
-      cp_async_mbar_arrive_noinc(&full_bar[s]);
+      cp_async_mbar_arrive_noinc(kRelay ? &gath_bar[s] : &full_bar[s]);
       ++it;
       // rotate the index pipeline
       q0 = q1;
@@ -681,6 +681,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
     }
     cp_async_wait_all();
+  } else if (kRelay && warp == kRelayWarp) {
+    // ---------------------------------------------------------------- relay (one thread)
+    // Once this CTA's slice of a stage has landed, make it visible to the async proxy, copy it
+    // into the same stage of every peer (completing bytes on the peer's full barrier) and mark
+    // it ready here.  The peers' stage is free: this CTA's gather warps waited on the stage's
+    // empty barrier, which every CTA of the cluster releases.
+    if (lane == 0) {
+      const uint32_t me = cluster_ctarank();
+      int it = 0, gcur = 0;
+      Pos q = pos_first(sch, p, gcur);
+      while (q.t < sch.total) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(&gath_bar[s], ph, s_abort, p.timeout_ns, p.err)) break;
+        fence_proxy_async_smem();
+        const uint32_t src = smem_u32(smem + s * L::kStageBytes) + me * kSliceBytes;
+        const uint32_t fb = smem_u32(&full_bar[s]);
+#pragma unroll
+        for (int r = 1; r < CN; ++r) {
+          const uint32_t peer = (me + r) % CN;
+          bulk_copy_to_peer(mapa_shared(src, peer), src, kSliceBytes, mapa_shared(fb, peer));
+        }
+        mbar_arrive(&full_bar[s]);
+        ++it;
+        pos_next(sch, p, gcur, q);
+      }
+    }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- UMMA issuer (lane 0)
     // With both operands tiled in the varlen-K mode, the last stage of a group reads rows of the
@@ -689,7 +716,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     constexpr bool kZeroTail = (VAR == VAR_K) && !kGather;
     int it = 0, acc = 0, gcur = 0;
     bool aborted = false;
-    for (int t = blockIdx.x; t < sch.total && !aborted; t += gridDim.x, ++acc) {
+    for (int t = sch.first; t < sch.total && !aborted; t += sch.stride, ++acc) {
       Tile tl;
       sch.decode(p, t, gcur, tl);
       const int nk = (tl.k_len + BK - 1) / BK;
@@ -736,7 +763,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const uint64_t bd = kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty_bar[s]);
+          if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
+          else umma_commit(&empty_bar[s]);
         }
         __syncwarp();
       }
@@ -804,7 +832,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (ncols > 32) store_row32(o.ptr, o.row_off + col + 32, hi, ncols - 32, false);
       }
     };
-    for (int t = blockIdx.x; t < sch.total; t += gridDim.x, ++acc) {
+    for (int t = sch.first; t < sch.total; t += sch.stride, ++acc) {
       Tile tl;
       sch.decode(p, t, gcur, tl);
       const int buf = acc & 1;
@@ -971,19 +999,45 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CN > 1) cluster_sync();  // peers finished with this CTA's shared memory
   if (warp == kProdWarp) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32>
+// grid: CTAs wanted (at most one per SM); with CN > 1 it is rounded to whole clusters and capped
+// at the clusters that can be resident at once.
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32, CN>;
   const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH>::bytes(p.groups, VAR);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
   constexpr bool kGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN);
-  kern<<<grid, (EW + 2 + (kGather ? 4 : 0)) * 32, smem, stream>>>(p, maps);
-  return cudaGetLastError();
+  constexpr int kBase = EW + 2 + (kGather ? 4 : 0) + (CN > 1 ? 1 : 0);
+  const int threads = (kBase + gemm_producers(STAGES, kMaxThreads / 32 - kBase) - 1) * 32;
+  if (CN == 1) {
+    kern<<<grid, threads, smem, stream>>>(p, maps);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CN;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(CN, 1, 1);
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  int clusters = (grid + CN - 1) / CN;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
+  cfg.gridDim = dim3(clusters * CN, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
 }  // namespace vgg

@@ -8,17 +8,17 @@ namespace vgg {
 // [GG] "(6) 세 번의 gg.gmm" gate and up in one pass: the B tile holds BN/2 rows of W_gate[e]
 // and the same BN/2 rows of W_up[e], so the epilogue sees h and u of the same columns.
 // A = X rows gathered through sorted_tok ([SM] "4.1 Gather 융합").
-cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256)
+// cn > 1: clusters of cn CTAs on consecutive column tiles of one row tile gather a cn-th of the
+// A rows each and pass them to one another through distributed shared memory.
+cudaError_t run_gate_up_swiglu(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) {
+    if (cn == 4)
+      return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 4>(p, m, grid, s);
+    if (cn == 2)
+      return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 2>(p, m, grid, s);
     return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
+  }
   return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
-}
-
-// The same with A's rows copied by TMA tile::gather4 (map box {64 columns, 1 row}).
-cudaError_t run_gate_up_swiglu_g4(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256)
-    return launch_grouped_gemm<256, 4, 4, 1, A_GATHER4_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, 4, 1, A_GATHER4_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false>(p, m, grid, s);
 }
 
 // Down projection, A = sorted activation rows, epilogue scales by the combine weight.

@@ -27,8 +27,7 @@ bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint
 
 // ---- grouped GEMM instantiations (BN chosen at run time: 128 or 256) -------------------------
 // forward
-cudaError_t run_gate_up_swiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_gate_up_swiglu_g4(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_gate_up_swiglu(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
