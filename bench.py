@@ -157,7 +157,7 @@ def ncu_traffic(csv_path: str, workload: str) -> dict:
             per[key] = {}
             order.append(key)
         per[key][r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
-    out, dw_seen = {}, 0
+    out, launches, dw_seen = {}, {}, 0
     for key in order:
         label = _label_of(key[1])
         if label is None:
@@ -167,7 +167,12 @@ def ncu_traffic(csv_path: str, workload: str) -> dict:
             dw_seen += 1
         m = per[key]
         b = m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0)
-        out[label] = out.get(label, 0.0) + b  # the grouping's kernels add up
+        out[label] = out.get(label, 0.0) + b
+        if "grouped_gemm_kernel" in key[1]:
+            launches[label] = launches.get(label, 0) + 1
+    # the grouping's kernels add up to one entry-point launch; a GEMM label launched twice per step
+    # (the router weight gradient's two halves) is averaged per launch
+    out = {k: v / launches.get(k, 1) for k, v in out.items()}
     return {"workload": workload, "source_hash": source_hash(), "bytes_per_launch": out}
 
 
