@@ -43,6 +43,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxThreads = 384;  // up to 8 epilogue warps + producer + issuer, or 4 + 2 + 4 gather warps
 constexpr int kMaxGroups = 1024;
+constexpr size_t kMaxSmem = 232448;  // dynamic shared memory per CTA (227 KB)
 constexpr int kStgBuf = 4096;    // one staged store: 32 rows x 128 B
 constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 this many stages ahead
 
@@ -102,11 +103,11 @@ struct SmemLayout {
   static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
   static constexpr int kNumBars = 3 * STAGES + 5;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
-  // Varlen-M keeps the group offsets and tile starts in shared memory; varlen-K reads the offsets
-  // from global memory (a few loads per tile), which leaves room for one more pipeline stage.
+  // The grouped modes read the group offsets from global memory (a few cached loads per tile);
+  // varlen-M keeps its per-group tile starts in shared memory.
   static constexpr size_t bytes(int groups, int var) {
     return 1024 + static_cast<size_t>(kMiscOffset) + 16 +
-           (var == VAR_M ? 8 * static_cast<size_t>(groups + 2) : var == VAR_NONE ? 8 : 0);
+           (var == VAR_M ? 4 * static_cast<size_t>(groups + 1) : var == VAR_NONE ? 8 : 0);
   }
 };
 
@@ -386,9 +387,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
   int* s_bad = reinterpret_cast<int*>(smem + L::kMiscOffset + 8);
-  int* s_off_sm = reinterpret_cast<int*>(smem + L::kMiscOffset + 16);
-  const int* s_off = (VAR == VAR_K) ? p.offsets : s_off_sm;
-  int* s_tile = s_off_sm + (p.groups + 1);
+  int* s_off_sm = reinterpret_cast<int*>(smem + L::kMiscOffset + 16);  // dense mode: {0, M}
+  const int* s_off = (VAR == VAR_NONE) ? s_off_sm : p.offsets;
+  int* s_tile = s_off_sm;  // varlen-M: first tile of every group, [groups + 1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -419,9 +420,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   }
   // group offsets into shared memory (validated: start at 0, monotone, within capacity)
-  if (VAR == VAR_M) {
-    for (int g = tid; g <= p.groups; g += kThreads) s_off_sm[g] = __ldg(p.offsets + g);
-  } else if (VAR == VAR_NONE && tid == 0) {
+  if (VAR == VAR_NONE && tid == 0) {
     s_off_sm[0] = 0;
     s_off_sm[1] = p.M;
   }
