@@ -338,9 +338,24 @@ __host__ __device__ constexpr int gemm_producers(int stages, int spare) {
                                            : 1;
 }
 
+// Warp roles of one instantiation.  The gate/up GEMM gathers its A rows with 8 cp.async warps (the
+// copy rate grows with the number of issuing warps: about 16, 25 and 33 B/ns per SM with 4, 8 and 16
+// warps) and runs 512 threads, so its roles stay within 128 registers per thread.
+template <int STAGES, int EW, int AMODE, int BMODE, int CN>
+struct WarpPlan {
+  static constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
+  static constexpr bool kGather = kAGather || BMODE == B_GATHER_MN;
+  static constexpr int kGW = (AMODE == A_GATHER_K) ? 8 : (kGather ? 4 : 0);  // gather warps
+  static constexpr int kMaxWarps = (AMODE == A_GATHER_K) ? 16 : kMaxThreads / 32;
+  static constexpr int kBase = EW + 2 + kGW + (CN > 1 ? 1 : 0);
+  static constexpr int kNP = gemm_producers(STAGES, kMaxWarps - kBase);
+  static constexpr int kThreads = (kBase + kNP - 1) * 32;
+};
+
 template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
+  using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN>;
   using L = SmemLayout<BN, STAGES, EW, DEPTH>;
   static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
@@ -352,7 +367,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   constexpr bool kGather = kAGather || kBGather;
   constexpr int kProdWarp = EW;        // TMA producer, owns TMEM
   constexpr int kMmaWarp = EW + 1;     // UMMA issuer
-  constexpr int kGatherWarp0 = EW + 2; // cp.async gather warps (4) when an operand is gathered
+  constexpr int kGatherWarp0 = EW + 2; // cp.async gather warps when an operand is gathered
+  constexpr int kGW = WP::kGW;
+  constexpr int kRStep = kGW * 4;      // row stride between a gather thread's rows
   // Clusters of CN CTAs along N share the gathered A tile: each CTA gathers rows
   // [rank * kSlice, (rank + 1) * kSlice) and a relay thread copies them to the peers.
   static_assert(CN == 1 || (CN == 2 || CN == 4), "cluster of 1, 2 or 4");
@@ -360,16 +377,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   constexpr bool kRelay = (CN > 1);
   constexpr int kSlice = BM / CN;               // A rows gathered by each CTA of a cluster
   constexpr uint32_t kSliceBytes = kSlice * 128;
-  constexpr int kRelayWarp = EW + 2 + 4;
+  constexpr int kRelayWarp = EW + 2 + kGW;
   // TMA loads issued by one thread complete one after another; stages are spread round-robin over
   // kNP producer threads (lane 0 of the producer warp and of kNP - 1 extra warps placed last), so
   // that several stages are in flight at once.  kNP divides STAGES: a stage always has the same
   // producer.
-  constexpr int kBaseWarps = EW + 2 + (kGather ? 4 : 0) + (kRelay ? 1 : 0);
-  constexpr int kNP = gemm_producers(STAGES, kMaxThreads / 32 - kBaseWarps);
-  constexpr int kXProdWarp0 = kBaseWarps;  // extra producer warps
-  constexpr int kThreads = (kBaseWarps + kNP - 1) * 32;
-  static_assert(kThreads <= kMaxThreads, "threads");
+  constexpr int kNP = WP::kNP;
+  constexpr int kXProdWarp0 = WP::kBase;  // extra producer warps
+  constexpr int kThreads = WP::kThreads;
+  static_assert(kThreads <= 512 && (kGW == 0 || kSlice % (kRStep > 0 ? kRStep : 1) == 0), "threads / gather rows");
   constexpr uint32_t kTxBytes =
       (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
@@ -399,9 +415,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       // relay mode: the producer's expect_tx and the relay's arrival; else the producer and,
       // with a gathered operand, the 128 gather threads
-      mbar_init(&full_bar[s], kRelay ? 2 : 1 + (kGather ? 128 : 0));
+      mbar_init(&full_bar[s], kRelay ? 2 : 1 + (kGather ? kGW * 32 : 0));
       mbar_init(&empty_bar[s], CN);  // every CTA of the cluster releases the stage
-      if (kRelay) mbar_init(&gath_bar[s], 128);
+      if (kRelay) mbar_init(&gath_bar[s], kGW * 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -568,14 +584,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           if (j % kNP == pj) mbar_wait(&empty_bar[j % STAGES], (j / STAGES) & 1, s_abort, p.timeout_ns, p.err);
       }
     }
-  } else if (kGather && warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
+  } else if (kGather && warp >= kGatherWarp0 && warp < kGatherWarp0 + kGW) {
     // ---------------------------------------------------------------- cp.async gather producers
-    // Thread ptid owns the 16-byte piece c16 of rows rsub + 16 i of every stage.  The token
+    // Thread ptid owns the 16-byte piece c16 of rows rsub + kRStep i of every stage.  The token
     // indices of a position are loaded two positions ahead of its copies.
     const int ptid = tid - kGatherWarp0 * 32;
     const int c16 = ptid & 7;
     const int rsub = ptid >> 3;
-    constexpr int kRowsPer = kSlice / 16;   // A rows per thread and stage (8 without a cluster)
+    constexpr int kRowsPer = kSlice / (kRStep > 0 ? kRStep : 1);  // A rows per thread and stage
     const int slice0 = sch.rank * kSlice;  // first tile row gathered by this CTA
     const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
     auto fetch = [&](const Pos& x, int (&r)[8], const Pos& prev, const int (&pr)[8]) {
@@ -586,7 +602,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < kRowsPer; ++i) {
-            const int rr = slice0 + rsub + 16 * i;
+            const int rr = slice0 + rsub + kRStep * i;
             r[i] = rr < x.tl.rows ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
           }
         }
@@ -630,7 +646,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             set_error(p.err, DERR_BAD_OFFSETS);
             ok = false;
           }
-          cp_async_16_hint(sa + sw128_offset(slice0 + rsub + 16 * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src,
+          cp_async_16_hint(sa + sw128_offset(slice0 + rsub + kRStep * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src,
                            ok ? 16u : 0u, pol_keep);
         }
       } else if (AMODE == A_GATHER_MN) {
@@ -862,16 +878,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             tmem_ld_wait();
             const int col = tl.n0 + c;
             const int ncols = p.N - col;
-            float h[32], u[32], a[32];
+            float h[32], u[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               h[i] = __uint_as_float(rh[i]);
               u[i] = __uint_as_float(ru[i]);
-              a[i] = h[i] * sigmoidf_(h[i]) * u[i];
             }
-            emit32(o0, h, col, ncols, full, row_ok, true);   // H, U stay fp32 for the backward
+            emit32(o0, h, col, ncols, full, row_ok, true);  // H, U stay fp32 for the backward
             emit32(o1, u, col, ncols, full, row_ok, true);
-            emit32(o2, a, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = h[i] * sigmoidf_(h[i]) * u[i];  // A, in place of h
+            emit32(o2, h, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
           }
         } else if (EPI == EPI_SCALE) {
           const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
@@ -1012,8 +1029,7 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid,
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
   constexpr bool kGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN);
-  constexpr int kBase = EW + 2 + (kGather ? 4 : 0) + (CN > 1 ? 1 : 0);
-  const int threads = (kBase + gemm_producers(STAGES, kMaxThreads / 32 - kBase) - 1) * 32;
+  const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads;
   if (CN == 1) {
     kern<<<grid, threads, smem, stream>>>(p, maps);
     return cudaGetLastError();
