@@ -323,14 +323,20 @@ cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, 
 namespace vgg {
 
 // out_a[j] = a[sorted_tok[j]], out_b[j] = b[sorted_tok[j]] for sorted rows j < P = offsets[E]; rows
-// [P, cap) are zeroed.  One warp per row, 16-byte vectors: the backward's expert-sorted copies of
-// X and dO, read by TMA boxes in the weight-gradient and dA' GEMMs.
+// [P, cap) are zeroed.  One warp per row, 16-byte vectors, all loads of a batch issued before its
+// stores, streaming stores: the backward's expert-sorted copies of X and dO, read by TMA boxes in
+// the weight-gradient and dA' GEMMs.
+__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets, int E,
                                                           const int32_t* __restrict__ sorted_tok, long long cap,
                                                           int T, int d, const __nv_bfloat16* __restrict__ a,
                                                           const __nv_bfloat16* __restrict__ b,
                                                           __nv_bfloat16* __restrict__ out_a,
                                                           __nv_bfloat16* __restrict__ out_b, int* err) {
+  constexpr int kU = 4;  // 16-byte vectors per lane and operand in flight
   const long long P = offsets[E];
   const int lane = threadIdx.x & 31;
   const int nv = d >> 3;
@@ -344,14 +350,25 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
         t = -1;
       }
     }
-    for (int c = lane; c < nv; c += 32) {
-      uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-      if (t >= 0) {
-        va = ldg_nc_v4(a + static_cast<long long>(t) * d + 8 * c);
-        vb = ldg_nc_v4(b + static_cast<long long>(t) * d + 8 * c);
+    for (int c0 = 0; c0 < nv; c0 += 32 * kU) {
+      uint4 va[kU], vb[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u + lane;
+        va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+        if (t >= 0 && c < nv) {
+          va[u] = ldg_nc_v4(a + static_cast<long long>(t) * d + 8 * c);
+          vb[u] = ldg_nc_v4(b + static_cast<long long>(t) * d + 8 * c);
+        }
       }
-      *reinterpret_cast<uint4*>(out_a + j * d + 8 * c) = va;
-      *reinterpret_cast<uint4*>(out_b + j * d + 8 * c) = vb;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < nv) {
+          st_cs_v4(out_a + j * d + 8 * c, va[u]);
+          st_cs_v4(out_b + j * d + 8 * c, vb[u]);
+        }
+      }
     }
   }
 }
