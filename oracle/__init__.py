@@ -17,9 +17,11 @@ pin checks the oracle against that reading, not against the pages' own
 from .moe_oracle import (  # noqa: F401
     Routing,
     bf16_bits_to_f64,
+    capacity_drop,
     combine,
     combine_weights,
     expert_block_backward,
+    expert_capacity,
     expert_ffn,
     group_by_expert,
     moe_backward,

@@ -11,6 +11,7 @@ Sources (page title, then the section a function follows):
 [EP]  "EP: Expert를 나누고 토큰 보내기"
 [SM]  "SonicMoE: IO·타일 인식 최적화로 MoE 학습 가속하기"
 [DEP] "Deep EP"
+[DEP] "Drop/Padding 방식" (same page): the capacity-based dispatch variant
 
 Readings where the pages are silent (listed again in the design notes):
 * top-K order: descending logit, ties to the lower expert index;
@@ -21,12 +22,17 @@ Readings where the pages are silent (listed again in the design notes):
   padding adds the highest-priority unrouted tokens, dropping removes the
   lowest-priority routed ones; every final pair (t,e) has weight
   s[t,e] / sum_{j in TopK(t)} s[t,j] (the same denominator as top-K);
-* the router bias is added to the logits and is not trained.
+* the router bias is added to the logits and is not trained;
+* capacity dispatch: C = ceil(cf * T * K / E); the "position" policy keeps an
+  expert's first C routed tokens in token order, the "probs" policy the C with
+  the largest routing probability (the top-K renormalised weight), ties to the
+  lower token; kept pairs keep their top-K weight (no re-normalisation).
 
 All floating point here is fp64; bf16 inputs are widened exactly.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 
 import numpy as np
@@ -146,6 +152,42 @@ def token_rounding(scores, topk_ids, m_tile: int):
     return member, r.astype(np.int64)
 
 
+def expert_capacity(T: int, E: int, K: int, capacity_factor: float) -> int:
+    """Capacity C of every expert: the capacity factor times the mean load T*K/E, rounded up.
+
+    [DEP] "Drop/Padding 방식": the [BN, H] tokens are rearranged per expert into [E, C, H],
+    C being the most tokens one expert can hold; the pages give no formula for C, the
+    capacity factor is named for the variant's switch.
+    """
+    return int(math.ceil(capacity_factor * T * K / E))
+
+
+def capacity_drop(topk_ids, keys, E: int, C: int, policy: str = "position") -> np.ndarray:
+    """The pairs an expert keeps under capacity C: member[T,E].
+
+    [DEP] "Drop/Padding 방식": line up each expert's tokens, cut at C and drop the rest;
+    tokens over capacity go by the "position" policy (the first C in token order stay)
+    or the "probs" policy (the C with the largest routing probability stay, ties to the
+    lower token).  ``keys[T,K]`` are the routing probabilities of the top-K pairs (the
+    combine weights), compared in their own dtype.
+    """
+    topk_ids = np.asarray(topk_ids)
+    keys = np.asarray(keys)
+    T, K = topk_ids.shape
+    member = np.zeros((T, E), dtype=bool)
+    for e in range(E):
+        tt, kk = np.nonzero(topk_ids == e)  # tokens ascending
+        if policy == "position":
+            keep = tt[:C]
+        elif policy == "probs":
+            order = np.lexsort((tt, -keys[tt, kk]))
+            keep = tt[order][:C]
+        else:
+            raise ValueError(policy)
+        member[keep, e] = True
+    return member
+
+
 @dataclass
 class Routing:
     """Discrete routing state: which (token, expert) pairs exist and in which order.
@@ -174,8 +216,13 @@ class Routing:
         return self.sorted_tok[self.offsets[e]:self.offsets[e + 1]]
 
 
-def route_discrete(logits, K: int, m_tile: int = 0, scores=None) -> Routing:
+def route_discrete(logits, K: int, m_tile: int = 0, scores=None, capacity: int = 0, policy: str = "position",
+                   drop_keys=None) -> Routing:
     """The discrete stage of routing from a given set of logits (and scores for rounding).
+
+    With ``capacity`` > 0 the pairs over an expert's capacity are dropped (``capacity_drop``);
+    ``drop_keys[T,K]`` are the routing probabilities the "probs" policy compares (default:
+    the oracle's own combine weights of the top-K pairs).
 
     Builds the expert-grouped order ([GG] steps (1)-(3)) and the per-token
     return map ([EP] "토큰을 Expert로 보내고 원래 위치로 돌려받기": each result has to
@@ -188,6 +235,10 @@ def route_discrete(logits, K: int, m_tile: int = 0, scores=None) -> Routing:
         if scores is None:
             scores = softmax(logits)
         member, _ = token_rounding(scores, topk, m_tile)
+    elif capacity:
+        if drop_keys is None:
+            drop_keys = np.take_along_axis(combine_weights(logits, topk), topk, axis=1)
+        member = capacity_drop(topk, drop_keys, E, capacity, policy)
     else:
         member = np.zeros((T, E), dtype=bool)
         member[np.arange(T)[:, None], topk] = True
@@ -196,7 +247,7 @@ def route_discrete(logits, K: int, m_tile: int = 0, scores=None) -> Routing:
     # expert-major, token-ascending order of the pairs
     e_idx, t_idx = np.nonzero(member.T)
     sorted_exp, sorted_tok = e_idx.astype(np.int64), t_idx.astype(np.int64)
-    if not m_tile:
+    if not m_tile and not capacity:
         # cross-check with the flatten + stable-sort description
         c2, o2, _, st2 = group_by_expert(topk, E)
         assert np.array_equal(c2, counts) and np.array_equal(st2, sorted_tok)
@@ -247,8 +298,10 @@ def combine(y_sorted, routing: Routing, w_full, T: int) -> np.ndarray:
 
 
 def moe_forward(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,
-                scores_for_routing=None):
+                scores_for_routing=None, capacity: int = 0, policy: str = "position", drop_keys=None):
     """Forward of the layer.  Returns (O[T,d], cache).
+
+    ``capacity`` > 0 selects the capacity (drop/pad) dispatch of ``route_discrete``.
 
     The selection comes from ``logits_for_routing`` (and ``scores_for_routing``
     under token rounding) when given — e.g. a device's fp32 logits, so that the
@@ -259,7 +312,8 @@ def moe_forward(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, log
     T, d = X.shape
     L = router_logits(X, W_r, bias)
     sel = L if logits_for_routing is None else logits_for_routing
-    routing = route_discrete(sel, K, m_tile, scores=scores_for_routing)
+    routing = route_discrete(sel, K, m_tile, scores=scores_for_routing, capacity=capacity, policy=policy,
+                             drop_keys=drop_keys)
     w_full = combine_weights(L, routing.topk_ids)
     E = L.shape[1]
     y_sorted = np.zeros((routing.P, d))

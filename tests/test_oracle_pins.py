@@ -376,6 +376,78 @@ def test_token_rounding_invariants(T, E, K, M):
         assert np.all(np.diff(rt.rows_of(e)) > 0)
 
 
+# ---------------------------------------------------------------- capacity (drop/pad) dispatch
+
+
+def test_capacity_closed_values():
+    # C = ceil(cf * T * K / E)
+    assert mo.expert_capacity(4096, 128, 8, 1.0) == 256
+    assert mo.expert_capacity(4096, 128, 8, 1.25) == 320
+    assert mo.expert_capacity(10, 3, 2, 1.0) == 7
+    assert mo.expert_capacity(5, 4, 1, 0.5) == 1
+
+
+def test_capacity_probs_worked_values():
+    # expert 0 receives tokens 0, 1, 3, 4 with probabilities .9, .5, .5, .8; expert 1 token 2
+    ids = np.array([[0], [0], [1], [0], [0]])
+    keys = np.array([[0.9], [0.5], [0.7], [0.5], [0.8]])
+    m = mo.capacity_drop(ids, keys, 2, 2, "probs")
+    assert sorted(np.nonzero(m[:, 0])[0].tolist()) == [0, 4] and np.nonzero(m[:, 1])[0].tolist() == [2]
+    m = mo.capacity_drop(ids, keys, 2, 3, "probs")  # the tie at .5 goes to the lower token
+    assert sorted(np.nonzero(m[:, 0])[0].tolist()) == [0, 1, 4]
+    m = mo.capacity_drop(ids, keys, 2, 2, "position")  # first two in token order
+    assert sorted(np.nonzero(m[:, 0])[0].tolist()) == [0, 1]
+
+
+@pytest.mark.parametrize("policy", ["position", "probs"])
+def test_capacity_brute_force_and_invariants(policy):
+    rng = np.random.default_rng(7)
+    T, E, K = 60, 6, 3
+    L = rng.standard_normal((T, E))
+    topk = mo.topk_experts(L, K)
+    keys = np.take_along_axis(mo.combine_weights(L, topk), topk, axis=1)
+    for C in (1, 5, 30, T):
+        m = mo.capacity_drop(topk, keys, E, C, policy)
+        # streaming reference: visit pairs in priority order, keep while the expert has room
+        pairs = [(t, int(topk[t, k]), keys[t, k]) for t in range(T) for k in range(K)]
+        if policy == "probs":
+            pairs.sort(key=lambda x: (-x[2], x[0]))
+        ref = np.zeros((T, E), dtype=bool)
+        room = np.full(E, C)
+        for t, e, _ in pairs:
+            if room[e] > 0:
+                ref[t, e] = True
+                room[e] -= 1
+        np.testing.assert_array_equal(m, ref)
+        c = np.bincount(topk.reshape(-1), minlength=E)
+        np.testing.assert_array_equal(m.sum(0), np.minimum(c, C))
+    # capacity above every count keeps the plain top-K routing
+    r0 = mo.route_discrete(L, K)
+    r1 = mo.route_discrete(L, K, capacity=T, policy=policy)
+    for f in ("member", "counts", "offsets", "sorted_tok", "tok_ptr", "tok_pairs"):
+        np.testing.assert_array_equal(getattr(r0, f), getattr(r1, f))
+
+
+@pytest.mark.parametrize("policy", ["position", "probs"])
+def test_capacity_backward_matches_autograd(policy):
+    T, d, E, n, K = 12, 8, 4, 5, 2
+    X, W_r, b = _rand((T, d), 50), _rand((d, E), 51, 0.5), _rand((E,), 52, 0.5)
+    Wg, Wu, Wd = _rand((E, n, d), 53, 0.4), _rand((E, n, d), 54, 0.4), _rand((E, d, n), 55, 0.4)
+    dO = _rand((T, d), 56)
+    O, cache = mo.moe_forward(X, W_r, b, Wg, Wu, Wd, K, capacity=4, policy=policy)
+    r = cache["routing"]
+    assert r.member.sum() < T * K, "capacity 4 should drop pairs"
+    g = mo.moe_backward(X, W_r, b, Wg, Wu, Wd, dO, cache)
+    ref = _dense_loss_torch(X, W_r, b, Wg, Wu, Wd, dO, r.member, r.topk_ids)
+    np.testing.assert_allclose(O, ref["O"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dX"], ref["dX"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dW_r"], ref["dW_r"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dlogits"], ref["dlogits"], rtol=1e-10, atol=1e-12)
+    for e in range(E):
+        np.testing.assert_allclose(g["dW_gate"][e], ref["dWg"][e], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dW_down"][e], ref["dWd"][e], rtol=1e-10, atol=1e-12)
+
+
 # ---------------------------------------------------------------- the metric
 
 
