@@ -51,6 +51,8 @@ def workload_desc(wl):
         s += f" bias={wl.bias}"
     if wl.m_tile:
         s += f" token_rounding M_tile={wl.m_tile}"
+    if wl.capacity_factor:
+        s += f" capacity_dispatch factor={wl.capacity_factor} policy={wl.drop_policy}"
     return s
 
 
@@ -287,7 +289,9 @@ def oracle_sample(wl, budget_s: float, max_experts: int | None = None):
     ru0 = resource.getrusage(resource.RUSAGE_SELF)
     t0 = time.perf_counter()
     L = mo.router_logits(X, W_r, bias)
-    routing = mo.route_discrete(L, wl.K, wl.m_tile, scores=mo.softmax(L).astype(np.float32) if wl.m_tile else None)
+    cap_c = mo.expert_capacity(wl.T, wl.E, wl.K, wl.capacity_factor) if wl.capacity_factor else 0
+    routing = mo.route_discrete(L, wl.K, wl.m_tile, scores=mo.softmax(L).astype(np.float32) if wl.m_tile else None,
+                                capacity=cap_c, policy=wl.drop_policy)
     w_full = mo.combine_weights(L, routing.topk_ids)
     Xf = mo.bf16_bits_to_f64(X)
     dOf = mo.bf16_bits_to_f64(dO)
@@ -378,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
     W_down = to_dev(synth.make_w_down(wl))
     ctx = vgg.Context(local_rank)
     buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
-                               device=dev)
+                               device=dev, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -508,7 +512,8 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": tflops / world / PAGE_A100_TFLOPS_C2 if wl.name == "c2" else None,
             "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller, shapes of the workload)",
-            "config": {"workload": workload_desc(wl), "pairs": P, "empty_experts": int((counts == 0).sum()),
+            "config": {"workload": workload_desc(wl), "pairs": P, "kept_pairs": int(counts.sum()),
+                       "empty_experts": int((counts == 0).sum()),
                        "max_rows_per_expert": int(counts.max()), "dW_dtype": "bf16",
                        "l2": "flushed between steps (256 MB write, outside the per-step events)",
                        "clock_samples": "nvidia-smi every 50 ms over a 0.5 s busy pre-roll of the same step and the timed region",

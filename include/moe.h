@@ -133,6 +133,31 @@ int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, cons
                 int32_t* P_out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_permute_capacity — the capacity (drop/pad) dispatch variant of moe_permute.
+ * [DEP] "Drop/Padding 방식": the pairs are laid out per expert as [E, C] slots;
+ * each expert keeps at most C of its routed tokens and the rest are dropped,
+ * an expert with fewer is padded to C.  policy 0 ("position") keeps the first
+ * C routed tokens in token order, policy 1 ("probs") the C with the largest
+ * routing probability topk_w (ties: lower token first).  Kept pairs keep their
+ * top-K weight.  C is the caller's (e.g. ceil(capacity_factor * T*K/E)).
+ *
+ * Outputs: counts[E] (kept pairs per expert), offsets[E+1] = e*C,
+ * sorted_tok[cap] (token of every slot, -1 for an empty slot), sorted_w[cap]
+ * (its weight, 0 for an empty slot), tok_ptr[T+1] and tok_pairs[cap] (per
+ * token, the slots of its kept pairs in ascending expert), P_out = E*C.
+ * cap >= E*C; T <= 32768; ws of at least moe_capacity_workspace_bytes(...).
+ * The slots feed moe_grouped_gemm_fwd / moe_combine / moe_backward unchanged
+ * (every slot is a GEMM row; an empty slot is a zero row with weight 0).
+ */
+int moe_permute_capacity(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
+                         int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                         float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* Workspace of the whole path under the capacity dispatch (pair capacity E*C). */
+size_t moe_capacity_workspace_bytes(int T, int d, int E, int n, int K, int C);
+
+/*
  * moe_permute_noalloc — moe_permute without a workspace, for callers that cannot
  * allocate device memory at all (a caller that only receives buffers from a host
  * runtime that offers no allocator, or a loop that must not allocate once it

@@ -16,6 +16,7 @@ Workloads follow the five configurations of the benchmark description:
 * ``c3``     T=8192,  d=7168, E=256, n=2048, K=8  router bias ~N(0, 0.5)
 * ``c4``     T=8192,  d=2880, E=128, n=2880, K=4  log-Zipf(s=1.2) prior b_e = -1.2 ln(e+1)
 * ``c5``     T=32768, d=1536, E=512, n=256,  K=8  token rounding to M_tile=128 (``c5_plain`` without)
+* ``c2_cap``, ``c2_cap_probs``  the c2 shape under the capacity (drop/pad) dispatch, capacity factor 1
 
 Layouts (row-major, the pages' ``(E, out, in)`` stacking of nn.Linear weights):
 X[T,d], W_r[d,E], W_gate[E,n,d], W_up[E,n,d], W_down[E,d,n], bias[E] fp32, dO[T,d].
@@ -134,6 +135,8 @@ class Workload:
     fwd_only: bool = False
     integer: bool = False     # integer-valued inputs (exact GEMMs and router logits)
     seed: int = 0
+    capacity_factor: float = 0.0  # capacity (drop/pad) dispatch; 0 = ragged
+    drop_policy: str = "position"
 
     @property
     def pairs(self) -> int:
@@ -153,6 +156,9 @@ WORKLOADS = {
     "c4": Workload("c4", 8192, 2880, 128, 2880, 4, bias="zipf"),
     "c5": Workload("c5", 32768, 1536, 512, 256, 8, m_tile=128),
     "c5_plain": Workload("c5_plain", 32768, 1536, 512, 256, 8),
+    # the capacity (drop/pad) dispatch variant on the c2 shape
+    "c2_cap": Workload("c2_cap", 4096, 2048, 128, 512, 8, capacity_factor=1.0),
+    "c2_cap_probs": Workload("c2_cap_probs", 4096, 2048, 128, 512, 8, capacity_factor=1.0, drop_policy="probs"),
 }
 
 

@@ -40,7 +40,8 @@ class Inputs:
 def run_path(ctx, inp: Inputs, backward=True, dW_dtype=torch.float32):
     import varlen_grouped_gemm_gb300 as vgg
     wl, dv = inp.wl, inp.dev
-    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=backward, dW_dtype=dW_dtype)
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=backward, dW_dtype=dW_dtype,
+                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy)
     vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
     if backward:
         vgg.backward(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)

@@ -26,7 +26,8 @@ EXPORTS = (
     "moe_create", "moe_destroy", "moe_status_str", "moe_get_error", "moe_set_wait_timeout",
     "moe_pair_capacity", "moe_workspace_bytes", "moe_route", "moe_permute", "moe_grouped_gemm_fwd",
     "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
-    "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc",
+    "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc", "moe_permute_capacity",
+    "moe_capacity_workspace_bytes",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -68,6 +69,10 @@ def lib() -> ctypes.CDLL:
         L.moe_test_gemm_varlen_k.argtypes = [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_test_wait_timeout.argtypes = [_P, ctypes.c_ulonglong, _P]
         L.moe_permute_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P]
+        L.moe_permute_capacity.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                           _P]
+        L.moe_capacity_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+        L.moe_capacity_workspace_bytes.restype = _SZ
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -200,6 +205,31 @@ def moe_permute_noalloc(ctx, topk_ids, topk_w, E, counts, offsets, sorted_tok, s
         _ptr(P_out, torch.int32), _stream(stream)))
 
 
+POLICIES = {"position": 0, "probs": 1}
+
+
+def expert_capacity(T: int, E: int, K: int, capacity_factor: float) -> int:
+    """Slots per expert of the capacity dispatch: ceil(capacity_factor * T * K / E)."""
+    import math
+    return int(math.ceil(capacity_factor * T * K / E))
+
+
+def moe_permute_capacity(ctx, topk_ids, topk_w, E, C, policy, counts, offsets, sorted_tok, sorted_w, tok_ptr,
+                         tok_pairs, P_out, ws, stream=None):
+    """Capacity (drop/pad) dispatch: expert e keeps at most C pairs in slots [e C, (e+1) C)."""
+    T, K = topk_ids.shape
+    wp, wb = _ws(ws)
+    _check("moe_permute_capacity", lib().moe_permute_capacity(
+        ctx.handle, _ptr(topk_ids, torch.int32), _ptr(topk_w, torch.float32), T, E, K, C, POLICIES[policy],
+        sorted_tok.numel(), _ptr(counts, torch.int32), _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32),
+        _ptr(sorted_w, torch.float32), _ptr(tok_ptr, torch.int32), _ptr(tok_pairs, torch.int32),
+        _ptr(P_out, torch.int32), wp, wb, _stream(stream)))
+
+
+def moe_capacity_workspace_bytes(T: int, d: int, E: int, n: int, K: int, C: int) -> int:
+    return int(lib().moe_capacity_workspace_bytes(T, d, E, n, K, C))
+
+
 def moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, offsets, sorted_tok, sorted_w, H, U, A, Yw, ws=None,
                          stream=None):
     T, d = X.shape
@@ -298,16 +328,27 @@ class Buffers:
     dlogits: torch.Tensor | None
     dW_r: torch.Tensor | None
     ws: torch.Tensor
+    capacity: int = 0          # capacity dispatch: slots per expert (0 = ragged)
+    drop_policy: str = "position"
 
     @staticmethod
-    def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda"):
-        cap = moe_pair_capacity(T, E, K, m_tile)
+    def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
+                 drop_policy="position", capacity_factor=0.0):
+        """Buffers for one configuration; capacity > 0 (or capacity_factor > 0, giving
+        ceil(capacity_factor * T * K / E)) selects the capacity (drop/pad) dispatch with that many slots per
+        expert (pair-indexed arrays sized E * capacity)."""
+        if capacity_factor and not capacity:
+            capacity = expert_capacity(T, E, K, capacity_factor)
+        if capacity and m_tile:
+            raise ValueError("token rounding and the capacity dispatch are exclusive")
+        cap = E * capacity if capacity else moe_pair_capacity(T, E, K, m_tile)
         f32, i32, bf = torch.float32, torch.int32, torch.bfloat16
 
         def z(shape, dt):
             return torch.zeros(shape, dtype=dt, device=device)
 
-        ws_bytes = moe_workspace_bytes(T, d, E, n, K, m_tile)
+        ws_bytes = moe_capacity_workspace_bytes(T, d, E, n, K, capacity) if capacity else \
+            moe_workspace_bytes(T, d, E, n, K, m_tile)
         if ws_bytes == 0:
             raise ValueError(f"unsupported sizes T={T} d={d} E={E} n={n} K={K}")
         return Buffers(
@@ -323,14 +364,19 @@ class Buffers:
             dW_down=z((E, d, n), dW_dtype) if backward else None,
             dS=z((cap,), f32) if backward else None, dlogits=z((T, E), f32) if backward else None,
             dW_r=z((d, E), f32) if backward else None,
-            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device))
+            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device), capacity=capacity, drop_policy=drop_policy)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
     """Routing, grouping, grouped GEMMs and combine; the output is ``buf.O``."""
     moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
-    moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts, buf.offsets,
-                buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
+    if buf.capacity:
+        moe_permute_capacity(ctx, buf.topk_ids, buf.topk_w, buf.E, buf.capacity, buf.drop_policy, buf.counts,
+                             buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws,
+                             stream)
+    else:
+        moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts,
+                    buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
     moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w, buf.H, buf.U,
                          buf.A, buf.Yw, buf.ws, stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)

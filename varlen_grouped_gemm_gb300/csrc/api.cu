@@ -405,6 +405,33 @@ int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, cons
   return MOE_OK;
 }
 
+int moe_permute_capacity(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
+                         int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                         float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && topk_ids && topk_w && counts && offsets && sorted_tok && sorted_w && tok_ptr && tok_pairs &&
+              P_out && ws);
+  VGG_REQUIRE(shapes_ok(T, 64, E, 64, K));
+  VGG_REQUIRE(C >= 1 && (policy == 0 || policy == 1));
+  VGG_REQUIRE(cap >= static_cast<long long>(E) * C && cap < INT_MAX);
+  VGG_REQUIRE(ws_bytes >= permute_ws_bytes(T, E, K, 1));
+  VGG_REQUIRE((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) == 0);
+  if (T > 32768) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  PermuteWs w = carve_permute_ws(ws, T, E, K, 1);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VGG_LAUNCH("permute", launch_permute_capacity(topk_ids, topk_w, T, E, K, C, policy, cap, counts, offsets,
+                                                sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
+  return MOE_OK;
+}
+
+size_t moe_capacity_workspace_bytes(int T, int d, int E, int n, int K, int C) {
+  if (!shapes_ok(T, d, E, n, K) || C < 1) return 0;
+  const long long cap = static_cast<long long>(E) * C;
+  return std::max(permute_ws_bytes(T, E, K, 1), bwd_ws_bytes(T, d, E, n, cap)) + kAlign;
+}
+
 int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const void* W_up, const void* W_down,
                          int T, int d, int E, int n, long long cap, const int32_t* offsets,
                          const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
@@ -493,7 +520,9 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
               sorted_w && tok_ptr && tok_pairs && H && U && dX && dW_gate && dW_up && dW_down && dS && dlogits &&
               dW_r && ws);
   VGG_REQUIRE(shapes_ok(T, d, E, n, K));
-  VGG_REQUIRE(m_tile >= 0 && cap >= moe_pair_capacity(T, E, K, m_tile) && cap < INT_MAX);
+  // cap: the pair arrays' length (moe_pair_capacity, or E*C for the capacity dispatch); the device checks
+  // offsets[E] <= cap
+  VGG_REQUIRE(m_tile >= 0 && cap >= 1 && cap < INT_MAX);
   VGG_REQUIRE(ws_bytes >= bwd_ws_bytes(T, d, E, n, cap));
   VGG_REQUIRE((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) == 0);
   VGG_REQUIRE(aligned16(dO) && aligned16(X) && aligned16(W_r) && aligned16(W_gate) && aligned16(W_up) &&

@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
        j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
     int t = -1;
     if (j < P) {
-      t = sorted_tok[j];
-      if (t < 0 || t >= T) {
+      t = sorted_tok[j];  // -1: an empty slot of the capacity layout (a zero row)
+      if (t < -1 || t >= T) {
         if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
         t = -1;
       }

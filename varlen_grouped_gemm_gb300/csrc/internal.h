@@ -70,6 +70,13 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
                            int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
                            int32_t* P_out, const PermuteWs& w, int* err, cudaStream_t s);
 
+// Capacity (drop/pad) dispatch: the kept pairs of expert e in slots [e C, (e + 1) C), offsets e C.
+// Uses the token-rounding workspace layout (m_tile > 0).
+cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
+                                    int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                                    float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
+                                    const PermuteWs& w, int* err, cudaStream_t s);
+
 // ---- combine / reductions --------------------------------------------------------------------
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
                            long long cap, __nv_bfloat16* O, int* err, cudaStream_t s);

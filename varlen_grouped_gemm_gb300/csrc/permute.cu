@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ topk_w, const uint32_t* __restrict__ member,
     const float* __restrict__ logits, int T, int E, int K, int nb, const int32_t* __restrict__ base,
     const int32_t* __restrict__ tokbase, long long cap, int32_t* __restrict__ sorted_tok,
-    float* __restrict__ sorted_w, int32_t* __restrict__ tok_ptr, int32_t* __restrict__ tok_pairs, int* err) {
+    float* __restrict__ sorted_w, int32_t* __restrict__ tok_ptr, int32_t* __restrict__ tok_pairs, int* err,
+    int slot_stride) {
   extern __shared__ uint32_t bits[];  // [E][8]
   __shared__ int s_warp[33];
   // pairs per token: K without rounding; rounding may pad a token into more experts
@@ -287,7 +288,9 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
     const int e = es[q];
     int rank = __popc(bits[e * 8 + w_self] & lt_mask);
     for (int w = 0; w < w_self; ++w) rank += __popc(bits[e * 8 + w]);
-    const long long j = static_cast<long long>(base[static_cast<long long>(e) * nb + b]) + rank;
+    long long j = static_cast<long long>(base[static_cast<long long>(e) * nb + b]) + rank;
+    // capacity layout: expert e's kept pairs fill slots [e * slot_stride, ...) in token order
+    if (slot_stride > 0) j = static_cast<long long>(e) * slot_stride + (j - base[static_cast<long long>(e) * nb]);
     if (j >= cap || tp + q >= cap) {
       set_error(err, DERR_CAPACITY);
       continue;
@@ -387,6 +390,74 @@ __device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& ma
 }
 
 
+// The `need` largest keys of keys[0, n) (0xFFFFFFFF = not a candidate), ties at the threshold going
+// to the lowest indices: a radix select (one 11-bit digit over all keys, the threshold bin compacted
+// into `list` for the two remaining digits), then take(i) for every selected index i.  Block-wide;
+// 1 <= need <= the number of candidates.
+template <class Take>
+__device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* list, int* hist, int* s_res, Take take) {
+  __shared__ int s_wties[kTrThreads / 32];
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = need;
+  const int lane = tid & 31;
+  tr_digit<2048>(keys, n, prefix, mask, 21, remaining, hist, s_res);
+  // compact the keys of the threshold bin (warp-aggregated appends; order is irrelevant here)
+  if (tid == 0) s_res[3] = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < n; t0 += kTrThreads) {
+    const int t = t0 + tid;
+    const uint32_t k = t < n ? keys[t] : 0xFFFFFFFFu;
+    const bool in = k != 0xFFFFFFFFu && (k & mask) == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, in);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_res[3], __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (in && pos < kTrListCap) list[pos] = k;
+  }
+  __syncthreads();
+  const int nlist = s_res[3];
+  int ties;
+  if (nlist <= kTrListCap) {
+    tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
+  } else {
+    tr_digit<2048>(keys, n, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(keys, n, prefix, mask, 0, remaining, hist, s_res);
+  }
+  // keys above the threshold are all taken; at the threshold the `remaining` lowest indices.
+  if (ties == remaining) {  // every tie is taken: no order needed
+    for (int t = tid; t < n; t += kTrThreads) {
+      const uint32_t k = keys[t];
+      if (k != 0xFFFFFFFFu && k >= prefix) take(t);
+    }
+    return;
+  }
+  // Equal keys beyond the need: indices in chunks of kTrThreads; a tie's rank in index order is the
+  // ties of earlier chunks, of earlier warps of this chunk and of lower lanes.
+  const int warp_id = tid >> 5;
+  int tie_base = 0;
+  for (int base = 0; base < n; base += kTrThreads) {
+    const int t = base + tid;
+    const uint32_t k = t < n ? keys[t] : 0xFFFFFFFFu;
+    const bool cand = k != 0xFFFFFFFFu;
+    const bool tie = cand && k == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    if (lane == 0) s_wties[warp_id] = __popc(bal);
+    __syncthreads();
+    int before = tie_base + __popc(bal & ((1u << lane) - 1u)), chunk_ties = 0;
+    for (int w = 0; w < kTrThreads / 32; ++w) {
+      const int cw = s_wties[w];
+      if (w < warp_id) before += cw;
+      chunk_ties += cw;
+    }
+    if (cand && (k > prefix || (tie && before < remaining))) take(t);
+    tie_base += chunk_ties;
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __restrict__ scoresT, int T, int E,
                                                               int m_tile, const int32_t* __restrict__ plain_off,
                                                               const int32_t* __restrict__ plain_tok,
@@ -435,66 +506,52 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
     keys[t] = cand ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
   }
   __syncthreads();
-  uint32_t prefix = 0, mask = 0;
-  int remaining = need;
-  const int lane = tid & 31;
-  tr_digit<2048>(keys, T, prefix, mask, 21, remaining, hist, s_res);
-  // compact the keys of the threshold bin (warp-aggregated appends; order is irrelevant here)
-  if (tid == 0) s_res[3] = 0;
-  __syncthreads();
-  for (int t0 = 0; t0 < T; t0 += kTrThreads) {
-    const int t = t0 + tid;
-    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
-    const bool in = k != 0xFFFFFFFFu && (k & mask) == prefix;
-    const unsigned bal = __ballot_sync(0xffffffffu, in);
-    int base = 0;
-    if (lane == 0 && bal) base = atomicAdd(&s_res[3], __popc(bal));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const int pos = base + __popc(bal & ((1u << lane) - 1u));
-    if (in && pos < kTrListCap) list[pos] = k;
-  }
-  __syncthreads();
-  const int nlist = s_res[3];
-  int ties;
-  if (nlist <= kTrListCap) {
-    tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
-    ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
-  } else {
-    tr_digit<2048>(keys, T, prefix, mask, 10, remaining, hist, s_res);
-    ties = tr_digit<1024>(keys, T, prefix, mask, 0, remaining, hist, s_res);
-  }
-  // keys above the threshold are all taken; at the threshold the `remaining` lowest tokens.
-  if (ties == remaining) {  // every tie is taken: no order needed
-    for (int t = tid; t < T; t += kTrThreads) {
-      const uint32_t k = keys[t];
-      if (k != 0xFFFFFFFFu && k >= prefix) atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
-    }
+  select_take(keys, T, need, list, hist, s_res, [&](int t) {
+    atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
+  });
+}
+
+// Capacity dispatch ([DEP] "Drop/Padding 방식"), one CTA per expert: of the expert's routed pairs
+// (token order) keep the first C ("position") or the C with the largest routing probability, ties
+// to the lower token ("probs"), and mark them in the membership bitmap.
+__global__ void __launch_bounds__(kTrThreads) cap_select_kernel(const int32_t* __restrict__ plain_off,
+                                                               const int32_t* __restrict__ plain_tok,
+                                                               const float* __restrict__ plain_w, long long plain_cap,
+                                                               int T, int E, int C, int policy,
+                                                               uint32_t* __restrict__ member, int* err) {
+  extern __shared__ uint32_t cs_smem[];
+  uint32_t* keys = cs_smem;      // [T] probabilities of the expert's routed pairs, in token order
+  uint32_t* list = cs_smem + T;  // [kTrListCap]
+  __shared__ int hist[2048];
+  __shared__ int s_res[4];
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int W = (E + 31) >> 5;
+  const int off = plain_off[e];
+  const int c = plain_off[e + 1] - off;
+  if (off < 0 || c < 0 || off + c > plain_cap || c > T) {
+    if (tid == 0) set_error(err, DERR_BAD_OFFSETS);
     return;
   }
-  // Equal scores beyond the need: tokens in chunks of 1024 consecutive ones; a tie's rank in token
-  // order is the ties of earlier chunks, of earlier warps of this chunk and of lower lanes.
-  __shared__ int s_wties[kTrThreads / 32];
-  const int warp_id = tid >> 5;
-  int tie_base = 0;
-  for (int base = 0; base < T; base += kTrThreads) {
-    const int t = base + tid;
-    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
-    const bool cand = k != 0xFFFFFFFFu;
-    const bool tie = cand && k == prefix;
-    const unsigned bal = __ballot_sync(0xffffffffu, tie);
-    if (lane == 0) s_wties[warp_id] = __popc(bal);
-    __syncthreads();
-    int before = tie_base + __popc(bal & ((1u << lane) - 1u)), chunk_ties = 0;
-    for (int w = 0; w < kTrThreads / 32; ++w) {
-      const int cw = s_wties[w];
-      if (w < warp_id) before += cw;
-      chunk_ties += cw;
-    }
-    if (cand && (k > prefix || (tie && before < remaining)))
-      atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
-    tie_base += chunk_ties;
-    __syncthreads();
+  const uint32_t ebit = 1u << (e & 31);
+  const int ew = e >> 5;
+  auto keep = [&](int i) {
+    const int t = plain_tok[off + i];
+    if (t >= 0 && t < T) atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
+  };
+  if (c <= C || policy == 0) {  // everything fits, or the first C in token order
+    const int nk = min(c, C);
+    for (int i = tid; i < nk; i += kTrThreads) keep(i);
+    return;
   }
+  for (int i = tid; i < c; i += kTrThreads) keys[i] = __float_as_uint(plain_w[off + i]);  // positive floats
+  __syncthreads();
+  select_take(keys, c, C, list, hist, s_res, keep);
+}
+
+// offsets of the capacity layout: expert e owns slots [e C, (e + 1) C); every slot is a row of the GEMMs.
+__global__ void slot_offsets_kernel(int32_t* offsets, int E, int C, int32_t* P_out) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = e * C;
+  if (threadIdx.x == 0 && P_out) *P_out = E * C;
 }
 
 size_t permute_ws_bytes(int T, int E, int K, int m_tile) {
@@ -544,7 +601,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
     perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err);
     perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
                                                                 w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
-                                                                tok_pairs, err);
+                                                                tok_pairs, err, 0);
     return cudaGetLastError();
   }
   // plain grouping into the workspace (only the expert-grouped tokens are needed)
@@ -553,7 +610,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err);
   perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, nullptr, nullptr, T, E, K, nb,
                                                               w.hist, w.tokblk, plain_cap, w.plain_tok, nullptr,
-                                                              nullptr, nullptr, err);
+                                                              nullptr, nullptr, err, 0);
   if ((st = cudaGetLastError()) != cudaSuccess) return st;
   // final token sets
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
@@ -570,7 +627,44 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err);
   perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, logits, T, E, K, nb,
                                                              w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
-                                                             tok_pairs, err);
+                                                             tok_pairs, err, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
+                                    int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                                    float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
+                                    const PermuteWs& w, int* err, cudaStream_t s) {
+  const int nb = (T + kTokBlock - 1) / kTokBlock;
+  const size_t bits_smem = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
+  const long long plain_cap = static_cast<long long>(T) * K;
+  cudaError_t st;
+  // plain grouping of the top-K pairs with their probabilities (into the workspace)
+  perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err);
+  perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
+                                                              w.hist, w.tokblk, plain_cap, w.plain_tok, w.scoresT,
+                                                              nullptr, nullptr, err, 0);
+  if ((st = cudaGetLastError()) != cudaSuccess) return st;
+  // kept pairs
+  const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
+  if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
+  const size_t sel_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + kTrListCap);
+  st = cudaFuncSetAttribute(cap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrListCap)));
+  if (st != cudaSuccess) return st;
+  cap_select_kernel<<<E, kTrThreads, sel_smem, s>>>(w.plain_off, w.plain_tok, w.scoresT, plain_cap, T, E, C, policy,
+                                                    w.member, err);
+  // group the kept pairs into slots e C + (rank in token order); empty slots hold token -1, weight 0
+  const size_t slots = static_cast<size_t>(E) * C;
+  if ((st = cudaMemsetAsync(sorted_tok, 0xFF, sizeof(int32_t) * slots, s)) != cudaSuccess) return st;
+  if ((st = cudaMemsetAsync(sorted_w, 0, sizeof(float) * slots, s)) != cudaSuccess) return st;
+  perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, nullptr, cap, err);
+  perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, nullptr, T, E, K, nb,
+                                                             w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
+                                                             tok_pairs, err, C);
+  slot_offsets_kernel<<<1, 256, 0, s>>>(offsets, E, C, P_out);
   return cudaGetLastError();
 }
 
