@@ -65,7 +65,7 @@ def kernel_work(wl, P, dW_bytes=2):
     activation tensor is written once and read once."""
     T, d, E, n, K = wl.T, wl.d, wl.E, wl.n, wl.K
     return {
-        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E),
+        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E),  # (split: + partials, read by top-K)
         "topk_softmax": (0, 4 * T * E + 8 * T * K),
         "permute": (0, 4 * T * K + 16 * P + (4 * T * E if wl.m_tile else 0)),
         "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 10 * P * n),
@@ -77,7 +77,7 @@ def kernel_work(wl, P, dW_bytes=2):
         "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d),
         "wr_transpose": (0, 4 * d * E),
         "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 8 * T * E),
-        "dwr_gemm": (2 * T * d * E, 2 * T * d + 2 * T * E + 4 * d * E),
+        "dwr_gemm": (4 * T * d * E, 2 * T * d + 4 * T * E + 4 * d * E),  # dlogits as two bf16 parts
         "dwr_reduce": (0, 8 * d * E),
         "dw_gate_up": (4 * P * d * n, 2 * P * d + 4 * P * n + 2 * dW_bytes * E * n * d),
         "dw_down": (2 * P * d * n, 2 * P * d + 2 * P * n + dW_bytes * E * d * n),
@@ -119,6 +119,7 @@ _GEMM_LABELS = {
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
     "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "transpose_f32_kernel": "permute",
+    "perm_escan_kernel": "permute", "cap_select_kernel": "permute", "slot_offsets_kernel": "permute",
     "combine_kernel": "combine",
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_kernel": "gather_rows", "zero_tail_rows_kernel": "zero_tail",
@@ -467,7 +468,7 @@ def run_ours(args, rank, world, local_rank):
                       "tflops": f2 / (a * 1e-3) / 1e12 if f2 else None,
                       "gbs_of_min_bytes": b2 / (a * 1e-3) / 1e9 if b2 else None,
                       "bound": ("tensor" if f2 / (pk["bf16_sus"] * 1e12) >= b2 / (pk["hbm_gbs"] * 1e9) else "hbm")}
-    launches_per_label = {"permute": 8 if wl.m_tile else 3}  # one label covers the grouping's kernels
+    launches_per_label = {"permute": (10 if (wl.m_tile or wl.capacity_factor) else 4)}  # the grouping's kernels
     gpu_launches = int(sum(cnt * launches_per_label.get(k, 1) for k, (_, cnt) in prof.items()))
 
     # end to end through the public API with host buffers: H2D of X and dO, D2H of O and dX per step

@@ -144,7 +144,8 @@ constexpr int kMaxSplitK = 16;
 
 struct BwdWs {
   __nv_bfloat16 *dH, *dU, *Ap, *dXp, *WrT, *Xs, *dOs;
-  __nv_bfloat16* dL;  // [2][T][E]: dlogits split into a bf16 high part and the bf16 rounding of the rest
+  __nv_bfloat16* dL;  // [2][Tp][E], Tp = T rounded up to 64: dlogits as a bf16 high part and the bf16
+                      // rounding of the rest; rows [T, Tp) of both halves are zero
   float* part;
   float* wr_part;
 };
@@ -152,7 +153,7 @@ struct BwdWs {
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
   const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
   return 3 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
-         al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(T) * E) +
+         al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(ceil_div(T, 64)) * 64 * E) +
          al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
          al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
 }
@@ -173,7 +174,7 @@ BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
   w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.part = reinterpret_cast<float*>(take(sizeof(float) * cap * part_ld));
-  w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(T) * E));
+  w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(ceil_div(T, 64)) * 64 * E));
   w.WrT = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d));
   w.wr_part = reinterpret_cast<float*>(take(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E));
   return w;
@@ -185,6 +186,7 @@ GemmParams base_params(moe_ctx* ctx) {
   p.split_k = 1;
   p.a_ksplit = INT_MAX;
   p.a_colsplit = INT_MAX;
+  p.a_kwrap = INT_MAX;
   p.b_ksplit = INT_MAX;
   p.out_rows_split = INT_MAX;
   p.err = ctx->d_err;
@@ -337,6 +339,20 @@ int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns) {
   return MOE_OK;
 }
 
+constexpr int kMaxRouteSplit = 4;
+
+// Split of the router GEMM's reduction over d when it has fewer tiles than SMs (the partials
+// are summed, with the bias, by the top-K kernel).
+static int route_split(int T, int d, int E, int num_sms) {
+  const int tiles = ceil_div(T, BM) * ceil_div(E, gemm_bn(E));
+  int split = std::min(kMaxRouteSplit, std::max(1, num_sms / std::max(tiles, 1)));
+  return std::max(1, std::min(split, d / (8 * BK)));
+}
+
+static size_t route_ws_bytes(int T, int E) {
+  return sizeof(float) * static_cast<size_t>(kMaxRouteSplit) * T * E;
+}
+
 long long moe_pair_capacity(int T, int E, int K, int m_tile) {
   long long cap = static_cast<long long>(T) * K;
   if (m_tile > 0) cap += static_cast<long long>(E) * (m_tile / 2);
@@ -346,38 +362,43 @@ long long moe_pair_capacity(int T, int E, int K, int m_tile) {
 size_t moe_workspace_bytes(int T, int d, int E, int n, int K, int m_tile) {
   if (!shapes_ok(T, d, E, n, K)) return 0;
   const long long cap = moe_pair_capacity(T, E, K, m_tile);
-  return std::max(permute_ws_bytes(T, E, K, m_tile), bwd_ws_bytes(T, d, E, n, cap)) + kAlign;
+  return std::max({permute_ws_bytes(T, E, K, m_tile), bwd_ws_bytes(T, d, E, n, cap), route_ws_bytes(T, E)}) + kAlign;
 }
 
 int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, int T, int d, int E, int K,
               float* logits, float* scores, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
               moe_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   VGG_REQUIRE(ctx && X && W_r && logits && topk_ids && topk_w);
   VGG_REQUIRE(shapes_ok(T, d, E, 64, K));
   VGG_REQUIRE(aligned16(X) && aligned16(W_r) && aligned16(logits));
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int split = route_split(T, d, E, ctx->num_sms);
+  // without room in the caller's workspace the GEMM writes the logits (plus bias) itself
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < sizeof(float) * static_cast<size_t>(split) * T * E)
+    split = 1;
+  float* part = split > 1 ? static_cast<float*>(ws) : nullptr;
   GemmParams p = base_params(ctx);
   p.M = T;
   p.N = E;
   p.K = d;
   p.groups = 1;
-  p.out0 = logits;
+  p.split_k = split;
+  p.out0 = split > 1 ? part : logits;
   p.ld_out = E;
-  p.col_bias = bias;
+  p.col_bias = split > 1 ? nullptr : bias;
   const int BN = gemm_bn(E);
   Maps m = zero_maps();
   if (!make_map_2d(&m.a0, X, d, T, d, BM) || !make_map_2d(&m.b0, W_r, E, d, E, 64) ||
-      !make_store_map_3d(&m.o0, logits, true, E, T, 1, 32))
+      !make_store_map_3d(&m.o0, split > 1 ? part : logits, true, E, T, split, 32))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
   const int tiles = ceil_div(T, BM) * ceil_div(E, BN);
-  VGG_LAUNCH("router_logits", run_router_logits(BN, p, m, std::min(tiles, ctx->num_sms), s));
-  VGG_LAUNCH("topk_softmax", launch_topk_softmax(logits, T, E, K, topk_ids, topk_w, scores, s));
+  VGG_LAUNCH("router_logits", run_router_logits(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
+  VGG_LAUNCH("topk_softmax", launch_topk_softmax(logits, part, split, bias, T, E, K, topk_ids, topk_w, scores, s));
   return MOE_OK;
 }
 
@@ -429,7 +450,7 @@ int moe_permute_capacity(moe_ctx* ctx, const int32_t* topk_ids, const float* top
 size_t moe_capacity_workspace_bytes(int T, int d, int E, int n, int K, int C) {
   if (!shapes_ok(T, d, E, n, K) || C < 1) return 0;
   const long long cap = static_cast<long long>(E) * C;
-  return std::max(permute_ws_bytes(T, E, K, 1), bwd_ws_bytes(T, d, E, n, cap)) + kAlign;
+  return std::max({permute_ws_bytes(T, E, K, 1), bwd_ws_bytes(T, d, E, n, cap), route_ws_bytes(T, E)}) + kAlign;
 }
 
 int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const void* W_up, const void* W_down,
@@ -592,39 +613,42 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
   }
   // per token: dS, router-logit gradient, dX
   VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
+  const int Tp = ceil_div(T, 64) * 64;
+  __nv_bfloat16* dL_lo = w.dL + static_cast<size_t>(Tp) * E;
+  if (Tp > T) {  // zero rows past the last token in both halves
+    if (cudaMemsetAsync(w.dL + static_cast<size_t>(T) * E, 0, sizeof(__nv_bfloat16) * (Tp - T) * E, s) != cudaSuccess ||
+        cudaMemsetAsync(dL_lo + static_cast<size_t>(T) * E, 0, sizeof(__nv_bfloat16) * (Tp - T) * E, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   VGG_LAUNCH("token_backward", launch_token_backward(w.part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
                                                      topk_ids, topk_w, K, w.dXp, w.WrT, T, d, cap, dS, dlogits, w.dL,
-                                                     static_cast<__nv_bfloat16*>(dX), ctx->d_err, s));
-  // dW_r = X^T dlogits, split over tokens.  dlogits enters as two bf16 GEMMs, X^T hi + X^T lo with
-  // hi = bf16(dlogits) and lo = bf16(dlogits - hi), which carries ~16 significant bits: a single bf16
-  // rounding of dlogits costs up to a few percent on the columns of heavily loaded experts, whose
-  // gradient sums thousands of tokens' rounding errors.  Partials of both halves are reduced together.
+                                                     dL_lo, static_cast<__nv_bfloat16*>(dX), ctx->d_err, s));
+  // dW_r = X^T dlogits, split over tokens.  dlogits enters as X^T hi + X^T lo with hi = bf16(dlogits) and
+  // lo = bf16(dlogits - hi), about 16 significant bits: a single bf16 rounding of dlogits costs up to a few
+  // percent on the columns of heavily loaded experts, whose gradient sums thousands of tokens' rounding
+  // errors.  One launch reduces over 2 Tp rows: [hi; lo] against X read twice (rows k >= Tp wrap to k - Tp).
   {
     GemmParams p = base_params(ctx);
     p.M = d;
     p.N = E;
-    p.K = T;
+    p.K = 2 * Tp;
     p.groups = 1;
+    p.a_kwrap = Tp;
     const int BN = gemm_bn(E);
     const int tiles = ceil_div(d, BM) * ceil_div(E, BN);
-    int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK / 2));
-    split = std::max(1, std::min(split, ceil_div(T, 8 * BK)));
+    int split = std::max(1, std::min(ctx->num_sms / std::max(tiles, 1), kMaxSplitK));
+    split = std::max(1, std::min(split, ceil_div(2 * Tp, 8 * BK)));
     p.split_k = split;
     p.ld_out = E;
-    for (int half = 0; half < 2; ++half) {
-      float* dst = w.wr_part + static_cast<size_t>(half) * split * d * E;
-      p.out0 = dst;
-      Maps m = zero_maps();
-      if (!make_map_2d(&m.a0, X, d, T, d, 64) ||
-          !make_map_2d(&m.b0, w.dL + static_cast<size_t>(half) * T * E, E, T, E, 64) ||
-          !make_store_map_3d(&m.o0, dst, true, E, d, split, 32))
-        return MOE_ERR_CUDA;
-      m.a1 = m.a0;
-      m.b1 = m.b0;
-      VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
-    }
-    VGG_LAUNCH("dwr_reduce",
-               launch_splitk_reduce(w.wr_part, 2 * split, static_cast<long long>(d) * E, dW_r, s));
+    p.out0 = w.wr_part;
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, X, d, T, d, 64) || !make_map_2d(&m.b0, w.dL, E, 2 * static_cast<uint64_t>(Tp), E, 64) ||
+        !make_store_map_3d(&m.o0, w.wr_part, true, E, d, split, 32))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
+    VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
   }
   // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok]
   {

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
     const float* __restrict__ sorted_w, const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w, int K,
     const __nv_bfloat16* __restrict__ dXp, const __nv_bfloat16* __restrict__ WrT, int T, int d, long long cap,
     float* __restrict__ dS, float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dL_bf16,
-    __nv_bfloat16* __restrict__ dX, int* err) {
+    __nv_bfloat16* __restrict__ dL_lo, __nv_bfloat16* __restrict__ dX, int* err) {
   __shared__ float s_dl[kMaxGroups];
   __shared__ int s_j[kMaxTokPairs];
   __shared__ int s_nz_e[kMaxGroups];
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
     dlogits[static_cast<long long>(t) * E + e] = v;
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
     dL_bf16[static_cast<long long>(t) * E + e] = hi;
-    dL_bf16[static_cast<long long>(T + t) * E + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    dL_lo[static_cast<long long>(t) * E + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
   }
   if (warp == 0) {
     int n = 0;
@@ -244,11 +244,11 @@ cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t*
                                   const int32_t* offsets, int E, const float* sorted_w, const int32_t* topk_ids,
                                   const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
                                   int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
-                                  __nv_bfloat16* dX, int* err, cudaStream_t s) {
+                                  __nv_bfloat16* dL_lo, __nv_bfloat16* dX, int* err, cudaStream_t s) {
   if (T > 0)
     token_backward_kernel<<<T, kCombineThreads, 0, s>>>(part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
                                                         topk_ids, topk_w, K, dXp, WrT, T, d, cap, dS, dlogits,
-                                                        dL_bf16, dX, err);
+                                                        dL_bf16, dL_lo, dX, err);
   return cudaGetLastError();
 }
 

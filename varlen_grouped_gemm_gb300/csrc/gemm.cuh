@@ -60,6 +60,7 @@ struct GemmParams {
   int split_k;         // VAR_NONE: number of K splits
   int a_ksplit;        // A_TMA_K: k < a_ksplit from map a0, else map a1 at k - a_ksplit
   int a_colsplit;      // A_TMA_MN: columns < split from map a0, else a1 at col - split
+  int a_kwrap;         // A_TMA_MN: reduction rows k >= a_kwrap are read at k - a_kwrap (A repeated along K)
   int b_ksplit;        // B_TMA_MN3: k < b_ksplit from map b0, else b1 at k - b_ksplit
   int b_chunked;       // B_TMA_MN2: the map is the chunked 3-D view (one load per stage)
   int l2_prefetch;     // prefetch the tiled operands of later stages into L2
@@ -505,8 +506,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             const int col = x.m0 + 64 * c;
             const CUtensorMap* mp_a = col < p.a_colsplit ? &mp.a0 : &mp.a1;
             const int cc = col < p.a_colsplit ? col : col - p.a_colsplit;
-            if (l2) tma_prefetch_l2_2d(mp_a, cc, kg);
-            else tma_load_2d(sa + c * (BK * 128), mp_a, bar, cc, kg);
+            const int ka = kg >= p.a_kwrap ? kg - p.a_kwrap : kg;
+            if (l2) tma_prefetch_l2_2d(mp_a, cc, ka);
+            else tma_load_2d(sa + c * (BK * 128), mp_a, bar, cc, ka);
           }
         }
         if (BMODE == B_TMA_K3) {

@@ -50,8 +50,10 @@ cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, 
                                   __nv_bfloat16* b, __nv_bfloat16* c, cudaStream_t s);
 
 // ---- routing / permutation -----------------------------------------------------------------
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int K, int32_t* ids, float* w, float* scores,
-                                cudaStream_t s);
+// Top-K and combine weights; with part != nullptr the logits are first summed from `split` partials
+// (plus bias) and written.
+cudaError_t launch_topk_softmax(float* logits, const float* part, int split, const float* bias, int T, int E, int K,
+                                int32_t* ids, float* w, float* scores, cudaStream_t s);
 
 struct PermuteWs {
   int32_t* hist;       // [E * nb]
@@ -84,13 +86,13 @@ cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const
 cudaError_t launch_transpose_bf16(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out, cudaStream_t s);
 
 // Per token: dS of its pairs (sum of the per-column-tile partials), the router-logit gradient
-// (fp32, and as bf16 high and low parts in dL_bf16[2][T][E]), and dX = sum of the pairs' dX rows
-// + dlogits W_r^T.
+// (fp32, and as bf16 high and low parts dL_bf16[T][E], dL_lo[T][E]), and dX = sum of the pairs' dX
+// rows + dlogits W_r^T.
 cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t* tok_ptr, const int32_t* tok_pairs,
                                   const int32_t* offsets, int E, const float* sorted_w, const int32_t* topk_ids,
                                   const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
                                   int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
-                                  __nv_bfloat16* dX, int* err, cudaStream_t s);
+                                  __nv_bfloat16* dL_lo, __nv_bfloat16* dX, int* err, cudaStream_t s);
 
 cudaError_t launch_splitk_reduce(const float* part, int splits, long long n, float* out, cudaStream_t s);
 

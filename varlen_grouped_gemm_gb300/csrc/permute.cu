@@ -12,13 +12,15 @@
 // the earlier tokens of its block that chose e is a popcount over that bitmap,
 // so no atomics decide any position and the result is the same on every run:
 //   1. hist:    per (expert, block) counts            -> hist[e][b]
-//   2. scan:    one exclusive scan over hist in expert-major order gives the
-//               first sorted position of every (e, b) block, the offsets and
-//               the per-token pair base of every block
-//   3. scatter: sorted position = base[e][b] + in-block rank.
+//   2. scan:    one warp per expert scans its blocks in place (the expert's
+//               pairs before each block) and totals them; one block scans the
+//               totals into the offsets and the per-block token pair bases
+//   3. scatter: sorted position = offsets[e] + hist[e][b] + in-block rank.
 // Token rounding ([SM] "5 기여 ③ Token Rounding 라우팅") runs the plain grouping
 // first, then per expert selects the final token set (tr_select_kernel) into a
-// [T x E] membership bitmap, and groups again from that bitmap.
+// [T x E] membership bitmap, and groups again from that bitmap.  The capacity
+// dispatch ([DEP] "Drop/Padding 방식") does the same with cap_select_kernel and
+// scatters the kept pairs into slots e*C + (rank in token order).
 #include <climits>
 
 #include "internal.h"
@@ -159,70 +161,79 @@ __global__ void __launch_bounds__(kTokBlock) perm_hist_kernel(const int32_t* __r
   if (tid == 0) tokblk[b] = total;
 }
 
-// One block of 1024 threads: exclusive scan of hist (expert-major) in place,
-// offsets/counts, and the exclusive scan of the per-block token pair counts.
-// hist is scanned in tiles of 8192 staged in shared memory (coalesced loads and
-// stores; each thread scans 8 consecutive entries), with a carry between tiles.
-constexpr int kScanTile = 8192;
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    s_warp[lane] = wi - w;
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  const int res = s_warp[warp] + incl - v;
+  total = s_warp[32];
+  __syncthreads();
+  return res;
+}
 
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int E, int nb,
-                                                         int32_t* __restrict__ tokblk, int32_t* __restrict__ counts,
+// Scan, level 1: one warp per expert turns its per-block counts hist[e][*] into in-expert exclusive
+// prefixes (block order = token order) and writes the expert's total.
+__global__ void __launch_bounds__(256) perm_escan_kernel(int32_t* __restrict__ hist, int E, int nb,
+                                                         int32_t* __restrict__ counts) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  int32_t* h = hist + static_cast<long long>(e) * nb;
+  int carry = 0;
+  for (int b0 = 0; b0 < nb; b0 += 32) {
+    const int b = b0 + lane;
+    const int v = b < nb ? h[b] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (b < nb) h[b] = carry + x - v;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) counts[e] = carry;
+}
+
+// Scan, level 2 (one block): offsets = exclusive scan of the expert totals, offsets[E] = P, and the
+// exclusive scan of the per-block token pair counts.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t* __restrict__ counts, int E,
+                                                         int32_t* __restrict__ tokblk, int nb,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ P_out,
                                                          long long cap, int* err) {
   __shared__ int s_warp[33];
-  __shared__ int s_tok[33];
-  __shared__ int tile[kScanTile];
+  __shared__ int s_tok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long N = static_cast<long long>(E) * nb;
   int carry = 0;
-  for (long long base = 0; base < N; base += kScanTile) {
-    for (int i = tid; i < kScanTile; i += 1024) tile[i] = (base + i < N) ? hist[base + i] : 0;
-    __syncthreads();
-    int v[8];
-    int local = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      v[q] = tile[8 * tid + q];
-      local += v[q];
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int w = s_warp[lane];
-      int wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += y;
-      }
-      s_warp[lane] = wi - w;
-      if (lane == 31) s_warp[32] = wi;
-    }
-    __syncthreads();
-    int run = carry + s_warp[warp] + incl - local;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      tile[8 * tid + q] = run;
-      run += v[q];
-    }
-    carry += s_warp[32];
-    __syncthreads();
-    for (int i = tid; i < kScanTile; i += 1024)
-      if (base + i < N) hist[base + i] = tile[i];
-    __syncthreads();
+  for (int base = 0; base < E; base += 1024) {  // E <= 1024: one pass
+    const int e = base + tid;
+    const int v = e < E ? counts[e] : 0;
+    int total;
+    const int ex = block_exclusive_scan_1024(v, s_warp, total);
+    if (e < E) offsets[e] = carry + ex;
+    carry += total;
   }
-  const int total = carry;
-  // per-block token pair bases (nb <= 256 -> a few warps)
   if (warp == 0) {
     int tcarry = 0;
-    for (int base = 0; base < nb; base += 32) {
-      const int i = base + lane;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int i = b0 + lane;
       const int v = (i < nb) ? tokblk[i] : 0;
       int x = v;
 #pragma unroll
@@ -235,25 +246,28 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
     }
     if (lane == 0) {
       tokblk[nb] = tcarry;
-      s_tok[0] = tcarry;
+      s_tok = tcarry;
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += 1024) offsets[e] = hist[static_cast<long long>(e) * nb];
   if (tid == 0) {
-    offsets[E] = total;
-    if (P_out) *P_out = total;
-    if (total > cap || s_tok[0] != total) set_error(err, DERR_CAPACITY);
+    offsets[E] = carry;
+    if (P_out) *P_out = carry;
+    if (carry > cap || s_tok != carry) set_error(err, DERR_CAPACITY);
   }
-  __syncthreads();
-  if (counts)
-    for (int e = tid; e < E; e += 1024) counts[e] = (e + 1 < E ? hist[static_cast<long long>(e + 1) * nb] : total) - hist[static_cast<long long>(e) * nb];
+}
+
+void launch_scan(int32_t* hist, int E, int nb, int32_t* tokblk, int32_t* counts, int32_t* offsets, int32_t* P_out,
+                 long long cap, int* err, cudaStream_t s) {
+  perm_escan_kernel<<<(E + 7) / 8, 256, 0, s>>>(hist, E, nb, counts);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(counts, E, tokblk, nb, offsets, P_out, cap, err);
 }
 
 template <bool FROM_MEMBER>
 __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ topk_w, const uint32_t* __restrict__ member,
     const float* __restrict__ logits, int T, int E, int K, int nb, const int32_t* __restrict__ base,
+    const int32_t* __restrict__ eoff,
     const int32_t* __restrict__ tokbase, long long cap, int32_t* __restrict__ sorted_tok,
     float* __restrict__ sorted_w, int32_t* __restrict__ tok_ptr, int32_t* __restrict__ tok_pairs, int* err,
     int slot_stride) {
@@ -288,9 +302,10 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
     const int e = es[q];
     int rank = __popc(bits[e * 8 + w_self] & lt_mask);
     for (int w = 0; w < w_self; ++w) rank += __popc(bits[e * 8 + w]);
-    long long j = static_cast<long long>(base[static_cast<long long>(e) * nb + b]) + rank;
-    // capacity layout: expert e's kept pairs fill slots [e * slot_stride, ...) in token order
-    if (slot_stride > 0) j = static_cast<long long>(e) * slot_stride + (j - base[static_cast<long long>(e) * nb]);
+    // base: the pair's rank among its expert's pairs before this token block; eoff: the expert's first
+    // position (capacity layout: expert e's kept pairs fill slots [e * slot_stride, ...) in token order)
+    const long long in_e = static_cast<long long>(base[static_cast<long long>(e) * nb + b]) + rank;
+    const long long j = (slot_stride > 0 ? static_cast<long long>(e) * slot_stride : eoff[e]) + in_e;
     if (j >= cap || tp + q >= cap) {
       set_error(err, DERR_CAPACITY);
       continue;
@@ -598,18 +613,20 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   cudaError_t st;
   if (m_tile <= 0) {
     perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-    perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err);
+    launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
     perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
-                                                                w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
+                                                                w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
+                                                                tok_ptr,
                                                                 tok_pairs, err, 0);
     return cudaGetLastError();
   }
   // plain grouping into the workspace (only the expert-grouped tokens are needed)
   const long long plain_cap = static_cast<long long>(T) * K;
   perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err);
+  launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
   perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, nullptr, nullptr, T, E, K, nb,
-                                                              w.hist, w.tokblk, plain_cap, w.plain_tok, nullptr,
+                                                              w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
+                                                              nullptr,
                                                               nullptr, nullptr, err, 0);
   if ((st = cudaGetLastError()) != cudaSuccess) return st;
   // final token sets
@@ -624,9 +641,10 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
                                                  w.member, err);
   // group the final pairs
   perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err);
+  launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
   perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, logits, T, E, K, nb,
-                                                             w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
+                                                             w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
+                                                             tok_ptr,
                                                              tok_pairs, err, 0);
   return cudaGetLastError();
 }
@@ -641,9 +659,10 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
   cudaError_t st;
   // plain grouping of the top-K pairs with their probabilities (into the workspace)
   perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err);
+  launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
   perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
-                                                              w.hist, w.tokblk, plain_cap, w.plain_tok, w.scoresT,
+                                                              w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
+                                                              w.scoresT,
                                                               nullptr, nullptr, err, 0);
   if ((st = cudaGetLastError()) != cudaSuccess) return st;
   // kept pairs
@@ -660,9 +679,10 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
   if ((st = cudaMemsetAsync(sorted_tok, 0xFF, sizeof(int32_t) * slots, s)) != cudaSuccess) return st;
   if ((st = cudaMemsetAsync(sorted_w, 0, sizeof(float) * slots, s)) != cudaSuccess) return st;
   perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(w.hist, E, nb, w.tokblk, counts, offsets, nullptr, cap, err);
+  launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, nullptr, cap, err, s);
   perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, nullptr, T, E, K, nb,
-                                                             w.hist, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr,
+                                                             w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
+                                                             tok_ptr,
                                                              tok_pairs, err, C);
   slot_offsets_kernel<<<1, 256, 0, s>>>(offsets, E, C, P_out);
   return cudaGetLastError();

@@ -15,19 +15,39 @@
 
 namespace vgg {
 
+// With split > 1 the router GEMM left `split` partial sums of the logits in part[split][T][E]: they are
+// added in split order with the bias and the result is written to logits first.
 template <int VPL>
-__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                           int32_t* __restrict__ ids, float* __restrict__ w,
+__global__ void __launch_bounds__(256) topk_softmax_kernel(float* __restrict__ logits, const float* __restrict__ part,
+                                                           int split, const float* __restrict__ bias, int T, int E,
+                                                           int K, int32_t* __restrict__ ids, float* __restrict__ w,
                                                            float* __restrict__ scores) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const float* row = logits + static_cast<long long>(t) * E;
+  float* row = logits + static_cast<long long>(t) * E;
   float v[VPL];
+  if (part) {
+    const long long plane = static_cast<long long>(T) * E;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldg(row + e) : -FLT_MAX;
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float a = __ldg(part + static_cast<long long>(t) * E + e);
+        for (int sp = 1; sp < split; ++sp) a += __ldg(part + sp * plane + static_cast<long long>(t) * E + e);
+        if (bias) a += __ldg(bias + e);
+        v[i] = a;
+        row[e] = a;
+      } else {
+        v[i] = -FLT_MAX;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? __ldg(row + e) : -FLT_MAX;
+    }
   }
   uint32_t taken = 0;
   float vmax = 0.0f, my_ex = 0.0f, sum = 0.0f;
@@ -88,15 +108,17 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
   }
 }
 
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int K, int32_t* ids, float* w, float* scores,
-                                cudaStream_t s) {
+cudaError_t launch_topk_softmax(float* logits, const float* part, int split, const float* bias, int T, int E, int K,
+                                int32_t* ids, float* w, float* scores, cudaStream_t s) {
   const int blocks = (T + 7) / 8;
-  if (E <= 32) topk_softmax_kernel<1><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
-  else if (E <= 64) topk_softmax_kernel<2><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
-  else if (E <= 128) topk_softmax_kernel<4><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
-  else if (E <= 256) topk_softmax_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
-  else if (E <= 512) topk_softmax_kernel<16><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
-  else topk_softmax_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, K, ids, w, scores);
+#define VGG_TOPK(V) topk_softmax_kernel<V><<<blocks, 256, 0, s>>>(logits, part, split, bias, T, E, K, ids, w, scores)
+  if (E <= 32) VGG_TOPK(1);
+  else if (E <= 64) VGG_TOPK(2);
+  else if (E <= 128) VGG_TOPK(4);
+  else if (E <= 256) VGG_TOPK(8);
+  else if (E <= 512) VGG_TOPK(16);
+  else VGG_TOPK(32);
+#undef VGG_TOPK
   return cudaGetLastError();
 }
 
