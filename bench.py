@@ -122,7 +122,8 @@ _OTHER_LABELS = {
     "perm_escan_kernel": "permute", "cap_select_kernel": "permute", "slot_offsets_kernel": "permute",
     "combine_kernel": "combine",
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
-    "splitk_reduce_kernel": "dwr_reduce", "gather_rows_kernel": "gather_rows", "zero_tail_rows_kernel": "zero_tail",
+    "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
+    "zero_tail_rows_kernel": "zero_tail",
 }
 
 

@@ -559,9 +559,10 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
   if (cap > static_cast<long long>(T) * K)
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
   // expert-sorted copies of X and dO: every backward GEMM then reads whole TMA boxes
-  VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, E, sorted_tok, cap, T, d, static_cast<const __nv_bfloat16*>(X),
+  VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
+                                               static_cast<const __nv_bfloat16*>(X),
                                                static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs, ctx->d_err,
-                                               ctx->num_sms, s));
+                                               ctx->num_sms, ctx->timeout_ns, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
   {
     GemmParams p = base_params(ctx);

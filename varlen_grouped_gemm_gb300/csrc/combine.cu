@@ -322,63 +322,115 @@ cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, 
 
 namespace vgg {
 
-// out_a[j] = a[sorted_tok[j]], out_b[j] = b[sorted_tok[j]] for sorted rows j < P = offsets[E]; rows
-// [P, cap) are zeroed.  One warp per row, 16-byte vectors, all loads of a batch issued before its
-// stores, streaming stores: the backward's expert-sorted copies of X and dO, read by TMA boxes in
-// the weight-gradient and dA' GEMMs.
-__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+// out_a[j] = a[sorted_tok[j]], out_b[j] = b[sorted_tok[j]] for the sorted positions j of the pairs, zero
+// rows elsewhere in [0, cap): the backward's expert-sorted copies of X and dO, read by TMA boxes in the
+// weight-gradient and dA' GEMMs.  Token-major with bulk (TMA) transfers: lane 0 of each warp reads
+// token t's rows of a and b once (chunks of up to 4 KB, global -> shared) and writes them to the sorted
+// positions of all of t's pairs (tok_pairs), so a and b stream from memory once instead of once per
+// pair (row-major gathers re-read them from DRAM when they do not fit in L2).  Positions that hold no
+// pair (the tail [P, cap) and the empty slots of the capacity layout) are then written from a zeroed
+// chunk.  One token in flight per warp, three CTAs per SM.
+constexpr int kGrWarps = 8;
+constexpr int kGrChunk = 2048;  // bf16 elements per bulk copy
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
-__global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets, int E,
-                                                          const int32_t* __restrict__ sorted_tok, long long cap,
-                                                          int T, int d, const __nv_bfloat16* __restrict__ a,
-                                                          const __nv_bfloat16* __restrict__ b,
-                                                          __nv_bfloat16* __restrict__ out_a,
-                                                          __nv_bfloat16* __restrict__ out_b, int* err) {
-  constexpr int kU = 4;  // 16-byte vectors per lane and operand in flight
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
+    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ sorted_tok,
+    const int32_t* __restrict__ tok_ptr, const int32_t* __restrict__ tok_pairs, long long cap, int T, int d,
+    const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b, __nv_bfloat16* __restrict__ out_a,
+    __nv_bfloat16* __restrict__ out_b, int* err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t gr_smem[];  // zero chunk, then per warp two chunks
+  __shared__ uint64_t bars[kGrWarps];
+  __shared__ int abort_flag;
+  constexpr uint32_t kChunkBytes = kGrChunk * 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < static_cast<int>(kChunkBytes / 16); i += blockDim.x)
+    reinterpret_cast<uint4*>(gr_smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kGrWarps; ++w) mbar_init(&bars[w], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();  // the zero chunk is read by bulk stores
+  __syncthreads();
+  if (lane != 0) return;
+  const uint32_t zero = smem_u32(gr_smem);
+  const uint32_t buf = zero + kChunkBytes * (1 + 2 * warp);
   const long long P = offsets[E];
-  const int lane = threadIdx.x & 31;
-  const int nv = d >> 3;
-  for (long long j = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; j < cap;
-       j += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-    int t = -1;
-    if (j < P) {
-      t = sorted_tok[j];  // -1: an empty slot of the capacity layout (a zero row)
-      if (t < -1 || t >= T) {
-        if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
-        t = -1;
-      }
+  const long long gw = static_cast<long long>(blockIdx.x) * kGrWarps + warp;
+  const long long nw = static_cast<long long>(gridDim.x) * kGrWarps;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (long long t = gw; t < T && ok; t += nw) {
+    const long long q0 = tok_ptr[t], q1 = tok_ptr[t + 1];
+    if (q0 < 0 || q1 > cap || q1 < q0) {
+      set_error(err, DERR_BAD_OFFSETS);
+      continue;
     }
-    for (int c0 = 0; c0 < nv; c0 += 32 * kU) {
-      uint4 va[kU], vb[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int c = c0 + 32 * u + lane;
-        va[u] = vb[u] = make_uint4(0, 0, 0, 0);
-        if (t >= 0 && c < nv) {
-          va[u] = ldg_nc_v4(a + static_cast<long long>(t) * d + 8 * c);
-          vb[u] = ldg_nc_v4(b + static_cast<long long>(t) * d + 8 * c);
-        }
+    if (q1 == q0) continue;
+    for (int c0 = 0; c0 < d; c0 += kGrChunk) {
+      const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
+      bulk_wait_read<0>();  // the previous stores have read this warp's buffer
+      mbar_arrive_expect_tx(&bars[warp], 2 * bytes);
+      bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
+      bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+      if (!mbar_wait(&bars[warp], phase, &abort_flag, timeout_ns, err)) {
+        ok = false;
+        break;
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int c = c0 + 32 * u + lane;
-        if (c < nv) {
-          st_cs_v4(out_a + j * d + 8 * c, va[u]);
-          st_cs_v4(out_b + j * d + 8 * c, vb[u]);
+      phase ^= 1u;
+      for (long long q = q0; q < q1; ++q) {
+        const long long j = tok_pairs[q];
+        if (j < 0 || j >= cap) {
+          set_error(err, DERR_BAD_OFFSETS);
+          continue;
         }
+        bulk_s2g(out_a + j * d + c0, buf, bytes);
+        bulk_s2g(out_b + j * d + c0, buf + kChunkBytes, bytes);
       }
+      bulk_commit();
     }
   }
+  // positions without a pair: the tail and the empty slots of the capacity layout
+  for (long long j = gw; j < cap && ok; j += nw) {
+    if (j < P && sorted_tok[j] >= 0) continue;
+    for (int c0 = 0; c0 < d; c0 += kGrChunk) {
+      const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
+      bulk_s2g(out_a + j * d + c0, zero, bytes);
+      bulk_s2g(out_b + j * d + c0, zero, bytes);
+    }
+    bulk_commit();
+  }
+  if (!ok) {  // a load that never completed: let copies in flight land before leaving
+    volatile int never = 0;
+    mbar_wait(&bars[warp], phase, &never, 20000000ull, nullptr);
+  }
+  bulk_wait0();
 }
 
-cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, long long cap, int T, int d,
-                               const __nv_bfloat16* a, const __nv_bfloat16* b, __nv_bfloat16* out_a,
-                               __nv_bfloat16* out_b, int* err, int num_sms, cudaStream_t s) {
-  const long long want = (cap + 7) / 8;
-  const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(offsets, E, sorted_tok, cap, T, d, a, b, out_a, out_b, err);
+cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, const int32_t* tok_ptr,
+                               const int32_t* tok_pairs, long long cap, int T, int d, const __nv_bfloat16* a,
+                               const __nv_bfloat16* b, __nv_bfloat16* out_a, __nv_bfloat16* out_b, int* err,
+                               int num_sms, unsigned long long timeout_ns, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kGrChunk) * 2 * (1 + 2 * kGrWarps);
+  cudaError_t st =
+      cudaFuncSetAttribute(gather_rows_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (st != cudaSuccess) return st;
+  const long long want = (T + kGrWarps - 1) / kGrWarps;
+  const int blocks = static_cast<int>(want < 3LL * num_sms ? want : 3LL * num_sms);
+  if (blocks > 0)
+    gather_rows_bulk_kernel<<<blocks, kGrWarps * 32, smem, s>>>(offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
+                                                               a, b, out_a, out_b, err, timeout_ns);
   return cudaGetLastError();
 }
 
