@@ -134,7 +134,7 @@ __device__ __forceinline__ int expert_of(const int32_t* offsets, int E, int j) {
 //   dS[j]       = sum over column tiles of the dSwiGLU epilogue's partial <dA'_j, A_j>
 //   dlogits[t]  = [k in F(t)] w_k dS_k - [k in TopK(t)] w_k * sum_{i in F(t)} w_i dS_i
 //   dX[t]       = sum_j dXp[j] (ascending expert) + sum_e dlogits[t,e] W_r[:,e]
-__global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
+__global__ void __launch_bounds__(256) token_backward_kernel(
     const float* __restrict__ part, int part_ld, const int32_t* __restrict__ tok_ptr,
     const int32_t* __restrict__ tok_pairs, const int32_t* __restrict__ offsets, int E,
     const float* __restrict__ sorted_w, const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w, int K,
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
   __shared__ float s_nz_v[kMaxGroups];
   __shared__ int s_cnt, s_nnz;
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += kCombineThreads) s_dl[e] = 0.0f;
+  for (int e = tid; e < E; e += blockDim.x) s_dl[e] = 0.0f;
   if (tid == 0) {
     const long long p0 = tok_ptr[t], p1 = tok_ptr[t + 1];
     int cnt = static_cast<int>(p1 - p0);
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kCombineThreads) {
+  for (int e = tid; e < E; e += blockDim.x) {
     const float v = s_dl[e];
     dlogits[static_cast<long long>(t) * E + e] = v;
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kCombineThreads) token_backward_kernel(
   __syncthreads();
   const int nnz = s_nnz;
   const int nv = d >> 3;
-  for (int c = tid; c < nv; c += kCombineThreads) {
+  for (int c = tid; c < nv; c += blockDim.x) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     int r = 0;
     for (; r + 4 <= cnt; r += 4) {  // four rows in flight per thread
@@ -245,8 +245,10 @@ cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t*
                                   const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
                                   int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
                                   __nv_bfloat16* dL_lo, __nv_bfloat16* dX, int* err, cudaStream_t s) {
+  // one thread per 16-byte column vector of a row (at least 64, at most 256 threads)
+  const int threads = d / 8 <= 64 ? 64 : (d / 8 >= 256 ? 256 : (d / 8 + 31) / 32 * 32);
   if (T > 0)
-    token_backward_kernel<<<T, kCombineThreads, 0, s>>>(part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
+    token_backward_kernel<<<T, threads, 0, s>>>(part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
                                                         topk_ids, topk_w, K, dXp, WrT, T, d, cap, dS, dlogits,
                                                         dL_bf16, dL_lo, dX, err);
   return cudaGetLastError();
