@@ -84,6 +84,19 @@ def kernel_work(wl, P, dW_bytes=2):
     }
 
 
+def activation_memory(buf) -> dict:
+    """Device bytes of the layer's state between forward and backward: what the forward keeps for the
+    backward (routing state, the fp32 H and U from which the backward recomputes A), the forward-only
+    temporaries (A for the down projection, Yw for the combine), the workspace and the peak torch
+    allocation of the process (inputs, weights and gradients included)."""
+    import torch
+    nb = lambda *ts: int(sum(t.numel() * t.element_size() for t in ts if t is not None))
+    return {"kept_for_backward_bytes": nb(buf.H, buf.U, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.offsets,
+                                          buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs),
+            "forward_temporaries_bytes": nb(buf.A, buf.Yw), "workspace_bytes": nb(buf.ws),
+            "peak_allocated_bytes": int(torch.cuda.max_memory_allocated())}
+
+
 def source_hash() -> str:
     """Hash of the CUDA sources: a recorded ncu traffic figure is used only while it matches."""
     import hashlib
@@ -524,6 +537,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_bf16_tflops": pk["bf16_sus"], "peak_source": pk["source"] + " sustained",
             "step_ms_min": min(step_ms), "step_ms_median": float(np.median(step_ms)),
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
+            "activation_memory": activation_memory(buf),
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         }
         if wl.name == "c2":

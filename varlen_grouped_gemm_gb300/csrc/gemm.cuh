@@ -731,6 +731,51 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
     // next group (or the zeroed tail): the whole warp clears those rows of B in shared memory
     // before lane 0 issues the stage's UMMAs.
     constexpr bool kZeroTail = (VAR == VAR_K) && !kGather;
+    if (!kZeroTail) {
+      // lane 0 alone: no warp-wide step between a stage's arrival and its UMMAs
+      if (lane == 0) {
+        int it = 0, acc = 0, gcur = 0;
+        bool aborted = false;
+        for (int t = sch.first; t < sch.total && !aborted; t += sch.stride, ++acc) {
+          Tile tl;
+          sch.decode(p, t, gcur, tl);
+          const int nk = (tl.k_len + BK - 1) / BK;
+          const int buf = acc & 1;
+          if (!mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int ks = 0; ks < nk; ++ks, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            if (!mbar_wait(&full_bar[s], ph, s_abort, p.timeout_ns, p.err)) {
+              aborted = true;
+              break;
+            }
+            const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
+            const uint32_t sb = sa + L::kABytes;
+            if (kGather) fence_proxy_async_smem();  // cp.async writes -> UMMA operand reads
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad =
+                  kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd =
+                  kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_bf16(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+            }
+            if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
+            else umma_commit(&empty_bar[s]);
+          }
+          if (aborted) break;
+          umma_commit(&tfull_bar[buf]);
+        }
+        if (*s_abort) {
+          umma_commit(drain_bar);
+          volatile int never = 0;
+          mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
+        }
+      }
+    } else {
     int it = 0, acc = 0, gcur = 0;
     bool aborted = false;
     for (int t = sch.first; t < sch.total && !aborted; t += sch.stride, ++acc) {
@@ -793,6 +838,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       umma_commit(drain_bar);
       volatile int never = 0;
       mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
+    }
     }
   } else if (warp < EW) {
     // ---------------------------------------------------------------- epilogue (warps 0..EW-1)
