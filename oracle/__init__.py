@@ -20,14 +20,20 @@ from .moe_oracle import (  # noqa: F401
     capacity_drop,
     combine,
     combine_weights,
+    dequantize_rows_e4m3,
+    e4m3_decode,
+    e4m3_encode,
+    e4m3_round,
     expert_block_backward,
     expert_capacity,
     expert_ffn,
     group_by_expert,
     moe_backward,
     moe_forward,
+    moe_forward_fp8,
     route_discrete,
     router_logits,
+    quantize_rows_e4m3,
     softmax,
     token_rounding,
     topk_experts,

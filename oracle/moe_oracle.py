@@ -393,3 +393,105 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None):
     dX += dL @ Wr.T
     dWr = X.T @ dL
     return dict(dX=dX, dW_gate=dWg, dW_up=dWu, dW_down=dWd, dw=dw_full, dlogits=dL, dW_r=dWr)
+
+
+# ---------------------------------------------------------------- FP8 variant of the gate/up GEMM
+#
+# [GG] "FP8" (DeepGEMM is named for FP8 grouped GEMMs): the variant computes the gate/up
+# projections from e4m3 operands.  The pages give no scaling recipe; reading: one fp32 scale per
+# row of X (per token) and per row of W_gate / W_up (per output channel), s = amax / 448 computed in
+# fp32, codes e4m3(x / s) with x / s in fp32, round to nearest even, saturating at +-448.  The
+# product of two dequantized rows is then exact in fp64.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest e4m3 value of each element (ties to even), saturating at +-448, as fp64.
+
+    e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; normal values 2^(e-7) (1 + m/8) for
+    e = 1..15 (all but e = 15, m = 7, which is NaN), subnormals 2^-6 m/8.  The spacing of the values
+    in [2^k, 2^(k+1)) is 2^(k-3) for k >= -6, and 2^-9 below 2^-6.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    k = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    step = np.where(a >= 2.0 ** -6, 2.0 ** (k - 3), 2.0 ** -9)
+    q = np.round(a / step) * step  # np.round: half to even; a / step is exact (power-of-two step)
+    q = np.minimum(q, E4M3_MAX)
+    return np.copysign(q, v)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """The e4m3 bit patterns (uint8) of values already on the e4m3 grid."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = (np.signbit(v)).astype(np.uint8) << 7
+    k = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    normal = a >= 2.0 ** -6
+    e = np.where(normal, k + 7, 0).astype(np.int64)
+    m = np.where(normal, a / 2.0 ** k - 1.0, a / 2.0 ** -6) * 8
+    code = (e << 3) | np.round(m).astype(np.int64)
+    return (sign | np.where(a > 0, code, 0).astype(np.uint8)).astype(np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of e4m3 bit patterns (uint8; NaN patterns are not produced here)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e > 0, 2.0 ** (e - 7) * (1.0 + m / 8.0), 2.0 ** -6 * (m / 8.0))
+    return s * mag
+
+
+def quantize_rows_e4m3(M):
+    """Per-row e4m3 quantization: (codes uint8 [R, C], scales fp32 [R]); row r dequantizes to
+    e4m3_decode(codes[r]) * scales[r].  The scale and the divided values are computed in fp32."""
+    A = np.asarray(M)
+    if A.dtype == np.uint16:
+        A = bf16_bits_to_f64(A).astype(np.float32)
+    A = A.astype(np.float32)
+    amax = np.max(np.abs(A), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    y = (A / scale[..., None]).astype(np.float32)
+    return e4m3_encode(e4m3_round(y)), scale
+
+
+def dequantize_rows_e4m3(codes, scales) -> np.ndarray:
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, logits_for_routing=None):
+    """Forward of the layer with the gate/up projections from e4m3 operands (per-token scales on X,
+    per-output-channel scales on W_gate and W_up, ``quantize_rows_e4m3``); routing, SwiGLU, the down
+    projection and the combine as in ``moe_forward``.  Returns (O, cache) with the cache's
+    ``h``, ``u``, ``a`` per sorted pair (fp64) and the quantized operands."""
+    X64 = _f64(X)
+    T, d = X64.shape
+    E, n, _ = np.shape(W_gate)
+    xq, xs = quantize_rows_e4m3(X)
+    Xd = dequantize_rows_e4m3(xq, xs)
+    gq, gs = quantize_rows_e4m3(np.asarray(W_gate).reshape(E * n, d))
+    uq, us = quantize_rows_e4m3(np.asarray(W_up).reshape(E * n, d))
+    Wg_d = dequantize_rows_e4m3(gq, gs).reshape(E, n, d)
+    Wu_d = dequantize_rows_e4m3(uq, us).reshape(E, n, d)
+    L = router_logits(X64, W_r, bias)
+    sel = L if logits_for_routing is None else logits_for_routing
+    routing = route_discrete(sel, K)
+    w_full = combine_weights(L, routing.topk_ids)
+    P = routing.P
+    h = np.zeros((P, n))
+    u = np.zeros((P, n))
+    y_sorted = np.zeros((P, d))
+    for e in range(E):
+        lo, hi = routing.offsets[e], routing.offsets[e + 1]
+        if hi == lo:
+            continue
+        rows = routing.sorted_tok[lo:hi]
+        h[lo:hi] = Xd[rows] @ Wg_d[e].T
+        u[lo:hi] = Xd[rows] @ Wu_d[e].T
+        y_sorted[lo:hi] = (silu(h[lo:hi]) * u[lo:hi]) @ _f64(W_down[e]).T
+    O = combine(y_sorted, routing, w_full, T)
+    return O, dict(logits=L, routing=routing, w_full=w_full, h=h, u=u, a=silu(h) * u, y_sorted=y_sorted,
+                   xq=xq, xs=xs, gq=gq, gs=gs, uq=uq, us=us)

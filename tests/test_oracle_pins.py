@@ -448,6 +448,103 @@ def test_capacity_backward_matches_autograd(policy):
         np.testing.assert_allclose(g["dW_down"][e], ref["dWd"][e], rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------- FP8 (e4m3) gate/up variant
+
+
+def test_e4m3_rounding_matches_torch():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(50000) * 100, rng.standard_normal(50000) * 1e-3,
+                        rng.uniform(-463, 463, 20000)]).astype(np.float32)
+    # exact ties between neighbours of the e4m3 grid at several binades
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ties = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, ties, -ties])
+    # torch's conversion does not saturate (|x| >= 464 gives NaN); the satfinite clamp is pinned separately
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(mo.e4m3_round(x), ref.to(torch.float64).numpy())
+    np.testing.assert_array_equal(mo.e4m3_encode(mo.e4m3_round(x)), ref.view(torch.uint8).numpy())
+    codes = np.arange(0, 256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]  # no NaN patterns
+    np.testing.assert_array_equal(mo.e4m3_decode(codes),
+                                  torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy())
+
+
+def test_e4m3_closed_values():
+    v = np.array([448.0, 1.0, 2.0 ** -9, 1.0625, 1.1875, 2.0 ** -10, 460.0, -3.3])
+    np.testing.assert_array_equal(mo.e4m3_round(v), [448.0, 1.0, 2.0 ** -9, 1.0, 1.25, 0.0, 448.0, -3.25])
+    np.testing.assert_array_equal(mo.e4m3_encode(mo.e4m3_round(v[:3])), [0x7E, 0x38, 0x01])
+    # satfinite: anything beyond the largest finite value clamps to +-448
+    np.testing.assert_array_equal(mo.e4m3_round(np.array([1e6, -500.0, 464.0])), [448.0, -448.0, 448.0])
+
+
+def test_quantize_rows_scale_and_error():
+    rng = np.random.default_rng(12)
+    M = rng.standard_normal((40, 96)).astype(np.float32)
+    q, s = mo.quantize_rows_e4m3(M)
+    D = mo.dequantize_rows_e4m3(q, s)
+    # the largest element of every row lands on +-448 times the scale
+    np.testing.assert_array_equal(np.max(np.abs(mo.e4m3_decode(q)), axis=1), 448.0)
+    np.testing.assert_array_equal(s, (np.max(np.abs(M), axis=1) / np.float32(448)).astype(np.float32))
+    # relative error of normal-range values at most half a unit of the 3-bit mantissa
+    big = np.abs(M) >= (2.0 ** -6) * s[:, None]
+    assert np.max(np.abs(D - M)[big] / np.abs(M)[big]) <= 2.0 ** -4 + 1e-7
+
+
+def test_fp8_forward_reduces_to_bf16_on_representable_inputs():
+    # rows whose largest magnitude is 448 * 2^-k get a power-of-two scale, and elements that are e4m3 values
+    # times that scale quantize without error, so the e4m3 forward equals the plain forward: X rows reach
+    # 3.5 (scale 2^-7, elements in {-3..3}), weight rows reach 0.875 (scale 2^-9, elements in {-0.5, 0, 0.5})
+    rng = np.random.default_rng(13)
+    T, d, E, n, K = 24, 16, 4, 8, 2
+    X = rng.integers(-3, 4, (T, d)).astype(np.float64)
+    X[:, 0] = 3.5
+    W_r = rng.standard_normal((d, E)) * 0.3
+    Wg = rng.integers(-1, 2, (E, n, d)).astype(np.float64) * 0.5
+    Wu = rng.integers(-1, 2, (E, n, d)).astype(np.float64) * 0.5
+    Wg[:, :, 0] = 0.875
+    Wu[:, :, 0] = -0.875
+    Wd = rng.standard_normal((E, d, n)) * 0.2
+    O8, c8 = mo.moe_forward_fp8(X, W_r, None, Wg, Wu, Wd, K)
+    O, c = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    np.testing.assert_allclose(O8, O, rtol=1e-12, atol=1e-12)
+    for e in range(E):
+        lo, hi = c["routing"].offsets[e], c["routing"].offsets[e + 1]
+        h, u, _, _ = mo.expert_ffn(X[c["routing"].rows_of(e)], Wg[e], Wu[e], Wd[e])
+        np.testing.assert_allclose(c8["h"][lo:hi], h, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(c8["u"][lo:hi], u, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_gate_up_within_quantization_bound():
+    # |x_i - xq_i| <= max(2^-4 |x_i|, 2^-10 s) (half a step of the 3-bit mantissa, or of the subnormal
+    # spacing 2^-9 s), likewise for the weights; h from the quantized operands stays within the
+    # resulting bound of the exact h, element by element, and differs from it (the quantization is real)
+    rng = np.random.default_rng(14)
+    T, d, E, n, K = 32, 64, 4, 16, 2
+    X = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (rng.standard_normal((E, n, d)) * 0.05).astype(np.float32)
+    Wu = (rng.standard_normal((E, n, d)) * 0.05).astype(np.float32)
+    W_r = rng.standard_normal((d, E)) * 0.3
+    Wd = rng.standard_normal((E, d, n)) * 0.05
+    O8, c8 = mo.moe_forward_fp8(X, W_r, None, Wg, Wu, Wd, K)
+    r = c8["routing"]
+    xs = c8["xs"].astype(np.float64)
+    dx = np.maximum(2.0 ** -4 * np.abs(X), 2.0 ** -10 * xs[:, None])
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        rows = r.rows_of(e)
+        for W, key, skey in ((Wg[e], "h", "gs"), (Wu[e], "u", "us")):
+            ws = c8[skey][e * n:(e + 1) * n].astype(np.float64)
+            dw = np.maximum(2.0 ** -4 * np.abs(W), 2.0 ** -10 * ws[:, None])
+            exact = X[rows].astype(np.float64) @ W.astype(np.float64).T
+            bound = np.abs(X[rows]) @ dw.T + dx[rows] @ np.abs(W).T + dx[rows] @ dw.T
+            err = np.abs(c8[key][lo:hi] - exact)
+            assert np.all(err <= bound * (1 + 1e-9) + 1e-300)
+            assert np.max(err) > 0
+    O, _ = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    assert 0 < np.max(np.abs(O8 - O)) < 0.2 * np.max(np.abs(O))
+
+
 # ---------------------------------------------------------------- the metric
 
 
