@@ -128,6 +128,7 @@ _GEMM_LABELS = {
     (1, 1, 0, 1): "gate_up_swiglu", (0, 0, 0, 2): "down_scale", (0, 3, 2, 0): "router_logits",
     (0, 2, 0, 3): "dact_dswiglu", (0, 2, 0, 0): "dx_gemm", (2, 3, 1, 0): "dw_tiled (gate/up, down)",
     (2, 3, 2, 0): "dwr_gemm", (2, 4, 1, 0): "dw_gather_b", (3, 3, 1, 0): "dw_gather_a",
+    (1, 1, 0, 4): "gate_up_swiglu_e4m3",
 }
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
@@ -136,7 +137,7 @@ _OTHER_LABELS = {
     "combine_kernel": "combine",
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
-    "zero_tail_rows_kernel": "zero_tail",
+    "zero_tail_rows_kernel": "zero_tail", "quantize_rows_e4m3_kernel": "quantize_e4m3",
 }
 
 
@@ -367,6 +368,53 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------------ our arm
 
 
+def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, stream, steps, warmup, pk):
+    """Forward only: the e4m3 gate/up path against the bf16 forward on the same inputs (weights quantized
+    once, outside the timed region; X quantized inside every step).  Per-kernel times from the library's
+    own events."""
+    import torch
+    b8 = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False, device=X.device,
+                              capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
+    w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
+    runs = {"bf16": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf),
+            "e4m3": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8)}
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        vgg.moe_profile_enable(ctx, True)
+        vgg.moe_profile_read(ctx)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        prof = vgg.moe_profile_read(ctx)
+        vgg.moe_profile_enable(ctx, False)
+        out[name] = (float(np.mean([a.elapsed_time(b) for a, b in evs])), prof)
+    rc, code = vgg.moe_get_error(ctx)
+    if rc != 0:
+        raise RuntimeError(f"device error in the e4m3 forward: status {rc}, code {code}")
+    P = int(b8.P.item())
+    fl = 4 * P * wl.d * wl.n
+    gu8 = out["e4m3"][1]["gate_up_swiglu_e4m3"]
+    gu16 = out["bf16"][1]["gate_up_swiglu"]
+    t8, t16 = gu8[0] / gu8[1], gu16[0] / gu16[1]
+    q = out["e4m3"][1].get("quantize_e4m3", (0.0, 1))
+    peak8 = 2 * pk["bf16"]
+    del b8, w8
+    return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
+            "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": q[0] / max(q[1], 1),
+            "gate_up_tflops": fl / (t8 * 1e-3) / 1e12, "bf16_gate_up_tflops": fl / (t16 * 1e-3) / 1e12,
+            "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
+            "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
+            "recipe": "e4m3 X (per token) and W_gate/W_up (per output channel), fp32 scales, fp32 accumulation",
+            "steps": steps, "l2": "flushed between steps"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import varlen_grouped_gemm_gb300 as vgg
@@ -513,6 +561,11 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": 2 * 2 * wl.T * wl.d, "d2h_bytes_per_step": 2 * 2 * wl.T * wl.d}
 
+    e4m3 = None
+    if not args.no_e4m3 and wl.d % 128 == 0:
+        e4m3 = measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, stream,
+                            max(3, min(args.steps, 20)), max(3, args.warmup), pk)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample(wl, budget_s=float(os.environ.get("VGG_CPU_BASELINE_SECONDS", "15")))
@@ -538,7 +591,7 @@ def run_ours(args, rank, world, local_rank):
             "step_ms_min": min(step_ms), "step_ms_median": float(np.median(step_ms)),
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
             "activation_memory": activation_memory(buf),
-            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "e4m3_forward": e4m3,
         }
         if wl.name == "c2":
             line["baseline_note"] = ("vs_baseline divides by the pages' grouped-GEMM figure for this workload "
@@ -556,6 +609,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e4m3", action="store_true", help="skip the e4m3 gate/up forward measurement")
     ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
     ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
     ap.add_argument("--profile-run", action="store_true",

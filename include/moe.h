@@ -199,6 +199,46 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_quantize_rows_e4m3 — per-row e4m3 quantization for the FP8 gate/up GEMM.
+ * [GG] "한계" (a fine-grained FP8 grouped GEMM as the next 2x over bf16; the page
+ * gives no recipe, the per-row one here is this library's reading).
+ *
+ * M [rows, cols] bf16 (device), row-major.  For every row r:
+ *   scales[r] = max_i |M[r,i]| / 448 in fp32 (1 when the row is all zeros),
+ *   q[r,i]    = e4m3(M[r,i] / scales[r]), the division in fp32, rounded to
+ *               nearest even and saturated at +-448 (e4m3: 4 exponent bits,
+ *               bias 7, 3 mantissa bits; q holds the bit patterns, one byte each).
+ * Outputs q [rows, cols] uint8 and scales [rows] fp32 (device, caller-owned).
+ * Use it on X (one scale per token) and on the rows of W_gate / W_up viewed as
+ * [E*n, d] (one scale per output channel).  cols % 16 == 0; M and q 16-byte
+ * aligned; else MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, float* scales,
+                           moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_fwd_e4m3 — moe_grouped_gemm_fwd with e4m3 gate/up operands.
+ * [GG] "한계" and "(6) 세 번의 gg.gmm"; [SM] "4.1 Gather 융합", "4.2 Epilogue 융합".
+ * Xq [T,d] and x_scale [T]: moe_quantize_rows_e4m3 of X; Wg_q, Wu_q [E,n,d] and
+ * wg_scale, wu_scale [E,n]: moe_quantize_rows_e4m3 of W_gate, W_up as [E*n, d].
+ * For sorted pair j of expert e with token t = sorted_tok[j] and column c:
+ *
+ *   H[j,c] = x_scale[t] * wg_scale[e,c] * sum_i e4m3(Xq[t,i]) e4m3(Wg_q[e,c,i])
+ *   U[j,c] likewise with Wu_q, wu_scale;  A[j] = silu(H[j]) * U[j] (bf16)
+ *   Yw[j]  = sorted_w[j] * (A[j] W_down[e]^T)   (bf16 operands, as moe_grouped_gemm_fwd)
+ *
+ * The code products are accumulated in fp32 on the tensor cores (kind::f8f6f4).
+ * A slot with sorted_tok = -1 (capacity dispatch) gives zero rows.  Requires
+ * d % 128 == 0 besides moe_grouped_gemm_fwd's shape rules; outputs and
+ * ownership as moe_grouped_gemm_fwd; no workspace.
+ */
+int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale, const void* Wg_q,
+                              const float* wg_scale, const void* Wu_q, const float* wu_scale, const void* W_down,
+                              int T, int d, int E, int n, long long cap, const int32_t* offsets,
+                              const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
+                              moe_stream_t stream);
+
+/*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.
  * [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기" (y(A2) = 0.7 u0 + 0.3 u2 in
  * A2's own slot); [DEP] "3) Combine".  O[t] = sum over t's pairs, in ascending

@@ -462,11 +462,13 @@ def dequantize_rows_e4m3(codes, scales) -> np.ndarray:
     return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
 
 
-def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, logits_for_routing=None):
+def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,
+                    scores_for_routing=None, capacity: int = 0, policy: str = "position", drop_keys=None):
     """Forward of the layer with the gate/up projections from e4m3 operands (per-token scales on X,
-    per-output-channel scales on W_gate and W_up, ``quantize_rows_e4m3``); routing, SwiGLU, the down
-    projection and the combine as in ``moe_forward``.  Returns (O, cache) with the cache's
-    ``h``, ``u``, ``a`` per sorted pair (fp64) and the quantized operands."""
+    per-output-channel scales on W_gate and W_up, ``quantize_rows_e4m3``); routing (with the same
+    token rounding / capacity options), SwiGLU, the down projection and the combine as in
+    ``moe_forward``.  Returns (O, cache) with the cache's ``h``, ``u``, ``a`` per sorted pair (fp64)
+    and the quantized operands."""
     X64 = _f64(X)
     T, d = X64.shape
     E, n, _ = np.shape(W_gate)
@@ -478,7 +480,8 @@ def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, logits_for_routi
     Wu_d = dequantize_rows_e4m3(uq, us).reshape(E, n, d)
     L = router_logits(X64, W_r, bias)
     sel = L if logits_for_routing is None else logits_for_routing
-    routing = route_discrete(sel, K)
+    routing = route_discrete(sel, K, m_tile, scores=scores_for_routing, capacity=capacity, policy=policy,
+                             drop_keys=drop_keys)
     w_full = combine_weights(L, routing.topk_ids)
     P = routing.P
     h = np.zeros((P, n))

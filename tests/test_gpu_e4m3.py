@@ -1,0 +1,157 @@
+"""The e4m3 gate/up forward on the device vs the oracle's e4m3 forward.
+
+[GG] "한계": a fine-grained FP8 grouped GEMM as the next step after bf16; the recipe (per-row scales,
+s = max|row| / 448 in fp32, codes rounded to nearest even and saturated) is the library's reading.
+Checked: the quantized operands (codes and scales of X and of W_gate / W_up) bit for bit against the
+oracle's quantization of the same bf16 inputs; the routing bit for bit (as in the bf16 path); H, U, A
+per sorted pair and O within the usual tolerance against the oracle's fp64 forward from the same
+e4m3 operands (the device accumulates the code products in fp32).  Cases: ragged tails, empty experts
+(skewed prior), token rounding, the capacity dispatch with empty slots, and the benchmark's c2 shape at
+full size on sampled tokens.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import moe_oracle as mo
+
+from _helpers import Inputs, bits_to_dev, check_routing_bit_exact, dev_to_f64, gpu_routing
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import varlen_grouped_gemm_gb300 as vgg
+    return vgg.Context(0)
+
+
+def _bf16_bits(M: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(M).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_rows_bit_exact(ctx):
+    import varlen_grouped_gemm_gb300 as vgg
+    rng = np.random.default_rng(21)
+    rows, cols = 300, 272
+    # row magnitudes over many binades, so that codes land in the subnormal range too
+    M = rng.standard_normal((rows, cols)) * np.exp2(rng.uniform(-40, 20, (rows, 1)))
+    M[3] = 0.0
+    M[4] = 0.0
+    M[4, 17] = -3.0
+    M[5, ::7] *= 1e-6
+    bits = _bf16_bits(M)
+    for shape in ((rows, cols), (3, 100, cols)):
+        b = np.concatenate([bits, bits])[:int(np.prod(shape[:-1]))].reshape(shape)
+        Md = bits_to_dev(b)
+        q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+        s = torch.empty(shape[:-1], dtype=torch.float32, device="cuda")
+        vgg.moe_quantize_rows_e4m3(ctx, Md, q, s)
+        qo, so = mo.quantize_rows_e4m3(b.reshape(-1, cols))
+        np.testing.assert_array_equal(q.cpu().numpy().reshape(-1, cols), qo)
+        np.testing.assert_array_equal(s.cpu().numpy().reshape(-1), so)
+    assert so[3] == 1.0 and np.all(qo[3] == 0), "a zero row: scale 1, zero codes"
+
+
+CASES = [
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=512, d=256, E=16, n=192, K=4),
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small", T=640, d=384, E=32, n=320, K=4),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
+    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f05", T=512, d=256, E=16, n=192, K=4, capacity_factor=0.5),
+]
+
+
+def _run(ctx, wl, dev):
+    import varlen_grouped_gemm_gb300 as vgg
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False,
+                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
+    w8 = vgg.E4m3Weights.quantize(ctx, dev["W_gate"], dev["W_up"])
+    vgg.forward_e4m3(ctx, dev["X"], dev["W_r"], dev["bias"], w8, dev["W_down"], buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    return buf, w8
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_e4m3_forward_matches_oracle(ctx, wl):
+    inp = Inputs(wl, with_grad=False)
+    buf, w8 = _run(ctx, wl, inp.dev)
+    E, n, d = wl.E, wl.n, wl.d
+    xq, xs = mo.quantize_rows_e4m3(inp.X)
+    np.testing.assert_array_equal(buf.xq.cpu().numpy(), xq)
+    np.testing.assert_array_equal(buf.xs.cpu().numpy(), xs)
+    for got_q, got_s, Wb in ((w8.Wg_q, w8.wg_scale, inp.W_gate), (w8.Wu_q, w8.wu_scale, inp.W_up)):
+        q, s = mo.quantize_rows_e4m3(Wb.reshape(E * n, d))
+        np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * n, d), q)
+        np.testing.assert_array_equal(got_s.cpu().numpy().reshape(-1), s)
+
+    g = gpu_routing(buf)
+    C = buf.capacity
+    O_ref, cache = mo.moe_forward_fp8(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K, wl.m_tile,
+                                      logits_for_routing=g["logits"], scores_for_routing=g["scores"], capacity=C,
+                                      policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None)
+    r = cache["routing"]
+    rep = {"O": oracle.compare("O", dev_to_f64(buf.O), O_ref)}
+    if C:
+        # slots e*C + rank hold the kept pairs; the rest are empty (zero rows)
+        slot_of = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(E)]).astype(np.int64)
+        empty = np.setdiff1d(np.arange(E * C), slot_of)
+        assert r.P < wl.T * wl.K and len(empty) > 0
+        assert not torch.any(buf.H[torch.from_numpy(empty).cuda()] != 0).item(), "empty slots give zero rows"
+        sel = torch.from_numpy(slot_of).cuda()
+        H, U, A = buf.H[sel], buf.U[sel], buf.A[sel]
+    else:
+        check_routing_bit_exact(g, wl.K, wl.m_tile)
+        H, U, A = buf.H[:r.P], buf.U[:r.P], buf.A[:r.P]
+    rep["H"] = oracle.compare("H", dev_to_f64(H), cache["h"])
+    rep["U"] = oracle.compare("U", dev_to_f64(U), cache["u"])
+    rep["A"] = oracle.compare("A", dev_to_f64(A), cache["a"])
+    if wl.bias == "zipf":
+        assert (r.counts == 0).any(), "the skewed prior should leave some experts empty"
+    print(wl.name, {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
+
+
+def test_e4m3_fullsize_c2(ctx):
+    """The c2 shape at full size (the configuration the benchmark's e4m3 line times), on sampled tokens:
+    every expert contribution of a token depends only on its own row and the experts' weights."""
+    wl = synth.WORKLOADS["c2"]
+    dev = {name: bits_to_dev(make(wl)) for name, make in (
+        ("X", synth.make_x), ("W_r", synth.make_router), ("W_gate", synth.make_w_gate), ("W_up", synth.make_w_up),
+        ("W_down", synth.make_w_down))}
+    dev["bias"] = None
+    buf, w8 = _run(ctx, wl, dev)
+    try:
+        g = gpu_routing(buf)
+        r = check_routing_bit_exact(g, wl.K, 0)
+        rng = np.random.default_rng(77)
+        toks = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, 6, replace=False)])).astype(np.int64)
+        X = synth.make_x(wl, rows=toks)
+        xq, xs = mo.quantize_rows_e4m3(X)
+        tsel = torch.from_numpy(toks).cuda()
+        np.testing.assert_array_equal(buf.xq[tsel].cpu().numpy(), xq)
+        np.testing.assert_array_equal(buf.xs[tsel].cpu().numpy(), xs)
+        Xd = mo.dequantize_rows_e4m3(xq, xs)
+        L = mo.router_logits(X, synth.make_router(wl), None)
+        w = mo.combine_weights(L, r.topk_ids[toks])
+        O = np.zeros((len(toks), wl.d))
+        member = r.member[toks]
+        for e in sorted(set(np.nonzero(member)[1].tolist())):
+            rows = np.nonzero(member[:, e])[0]
+            gq, gs = mo.quantize_rows_e4m3(synth.make_w_gate(wl, [e])[0])
+            uq, us = mo.quantize_rows_e4m3(synth.make_w_up(wl, [e])[0])
+            np.testing.assert_array_equal(w8.Wg_q[e].cpu().numpy(), gq)
+            np.testing.assert_array_equal(w8.wu_scale[e].cpu().numpy(), us)
+            h = Xd[rows] @ mo.dequantize_rows_e4m3(gq, gs).T
+            u = Xd[rows] @ mo.dequantize_rows_e4m3(uq, us).T
+            y = (mo.silu(h) * u) @ mo.bf16_bits_to_f64(synth.make_w_down(wl, [e])[0]).T
+            O[rows] += w[rows, e][:, None] * y
+        rep = oracle.compare("O (sampled tokens)", dev_to_f64(buf.O[tsel]), O)
+        print("c2 e4m3", len(toks), "tokens", (rep["max"], rep["mean"]))
+    finally:
+        del buf, dev, w8
+        gc.collect()
+        torch.cuda.empty_cache()

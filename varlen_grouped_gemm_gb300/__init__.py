@@ -27,7 +27,7 @@ EXPORTS = (
     "moe_pair_capacity", "moe_workspace_bytes", "moe_route", "moe_permute", "moe_grouped_gemm_fwd",
     "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
     "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc", "moe_permute_capacity",
-    "moe_capacity_workspace_bytes",
+    "moe_capacity_workspace_bytes", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
                                            _P]
         L.moe_capacity_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
         L.moe_capacity_workspace_bytes.restype = _SZ
+        L.moe_quantize_rows_e4m3.argtypes = [_P, _P, _LL, _I, _P, _P, _P]
+        L.moe_grouped_gemm_fwd_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P,
+                                                _P, _P, _P, _P, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -243,6 +246,30 @@ def moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, offsets, sorted_tok, sort
         _ptr(H, torch.float32), _ptr(U, torch.float32), _ptr(A, bf), _ptr(Yw, bf), wp, wb, _stream(stream)))
 
 
+def moe_quantize_rows_e4m3(ctx, M, q, scales, stream=None):
+    """Per-row e4m3 codes (uint8, shaped like M) and fp32 scales (one per row of M's last axis)."""
+    cols = M.shape[-1]
+    rows = M.numel() // cols
+    if q.shape != M.shape or scales.numel() != rows:
+        raise ValueError("q must be shaped like M and scales hold one value per row")
+    _check("moe_quantize_rows_e4m3", lib().moe_quantize_rows_e4m3(
+        ctx.handle, _ptr(M, torch.bfloat16), rows, cols, _ptr(q, torch.uint8), _ptr(scales, torch.float32),
+        _stream(stream)))
+
+
+def moe_grouped_gemm_fwd_e4m3(ctx, Xq, x_scale, Wg_q, wg_scale, Wu_q, wu_scale, W_down, offsets, sorted_tok,
+                              sorted_w, H, U, A, Yw, stream=None):
+    T, d = Xq.shape
+    E, n, _ = Wg_q.shape
+    cap = sorted_tok.numel()
+    u8, f32 = torch.uint8, torch.float32
+    _check("moe_grouped_gemm_fwd_e4m3", lib().moe_grouped_gemm_fwd_e4m3(
+        ctx.handle, _ptr(Xq, u8), _ptr(x_scale, f32), _ptr(Wg_q, u8), _ptr(wg_scale, f32), _ptr(Wu_q, u8),
+        _ptr(wu_scale, f32), _ptr(W_down, torch.bfloat16), T, d, E, n, cap, _ptr(offsets, torch.int32),
+        _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32), _ptr(A, torch.bfloat16),
+        _ptr(Yw, torch.bfloat16), _stream(stream)))
+
+
 def moe_combine(ctx, Yw, tok_ptr, tok_pairs, O, stream=None):
     T, d = O.shape
     _check("moe_combine", lib().moe_combine(
@@ -330,10 +357,12 @@ class Buffers:
     ws: torch.Tensor
     capacity: int = 0          # capacity dispatch: slots per expert (0 = ragged)
     drop_policy: str = "position"
+    xq: torch.Tensor | None = None  # e4m3 forward: X's codes [T, d] and per-token scales [T]
+    xs: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
-                 drop_policy="position", capacity_factor=0.0):
+                 drop_policy="position", capacity_factor=0.0, e4m3=False):
         """Buffers for one configuration; capacity > 0 (or capacity_factor > 0, giving
         ceil(capacity_factor * T * K / E)) selects the capacity (drop/pad) dispatch with that many slots per
         expert (pair-indexed arrays sized E * capacity)."""
@@ -364,7 +393,8 @@ class Buffers:
             dW_down=z((E, d, n), dW_dtype) if backward else None,
             dS=z((cap,), f32) if backward else None, dlogits=z((T, E), f32) if backward else None,
             dW_r=z((d, E), f32) if backward else None,
-            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device), capacity=capacity, drop_policy=drop_policy)
+            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device), capacity=capacity, drop_policy=drop_policy,
+            xq=z((T, d), torch.uint8) if e4m3 else None, xs=z((T,), f32) if e4m3 else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
@@ -379,6 +409,47 @@ def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
                     buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
     moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w, buf.H, buf.U,
                          buf.A, buf.Yw, buf.ws, stream)
+    moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
+
+
+@dataclass
+class E4m3Weights:
+    """W_gate and W_up as e4m3 codes [E, n, d] (uint8) with one fp32 scale per output channel [E, n]."""
+
+    Wg_q: torch.Tensor
+    wg_scale: torch.Tensor
+    Wu_q: torch.Tensor
+    wu_scale: torch.Tensor
+
+    @staticmethod
+    def quantize(ctx, W_gate, W_up, stream=None) -> "E4m3Weights":
+        E, n, d = W_gate.shape
+        dev = W_gate.device
+        w = E4m3Weights(torch.empty((E, n, d), dtype=torch.uint8, device=dev),
+                        torch.empty((E, n), dtype=torch.float32, device=dev),
+                        torch.empty((E, n, d), dtype=torch.uint8, device=dev),
+                        torch.empty((E, n), dtype=torch.float32, device=dev))
+        moe_quantize_rows_e4m3(ctx, W_gate, w.Wg_q, w.wg_scale, stream)
+        moe_quantize_rows_e4m3(ctx, W_up, w.Wu_q, w.wu_scale, stream)
+        return w
+
+
+def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, stream=None):
+    """The forward with the gate/up GEMM on e4m3 operands (``buf`` allocated with ``e4m3=True``): routing and
+    grouping as ``forward``, X quantized per token, then the e4m3 grouped GEMMs and the combine."""
+    if buf.xq is None:
+        raise ValueError("buffers were allocated without e4m3=True")
+    moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
+    if buf.capacity:
+        moe_permute_capacity(ctx, buf.topk_ids, buf.topk_w, buf.E, buf.capacity, buf.drop_policy, buf.counts,
+                             buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws,
+                             stream)
+    else:
+        moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts,
+                    buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
+    moe_quantize_rows_e4m3(ctx, X, buf.xq, buf.xs, stream)
+    moe_grouped_gemm_fwd_e4m3(ctx, buf.xq, buf.xs, w8.Wg_q, w8.wg_scale, w8.Wu_q, w8.wu_scale, W_down, buf.offsets,
+                              buf.sorted_tok, buf.sorted_w, buf.H, buf.U, buf.A, buf.Yw, stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 

@@ -272,6 +272,30 @@ using namespace vgg;
     if (e_ != cudaSuccess) return MOE_ERR_CUDA;   \
   } while (0)
 
+// Down projection of the sorted activation rows A, each row scaled by its combine weight (Yw).
+static int down_projection(moe_ctx* ctx, const void* A, const void* W_down, int d, int E, int n, long long cap,
+                           const int32_t* offsets, const float* sorted_w, void* Yw, cudaStream_t s) {
+  GemmParams p = base_params(ctx);
+  p.N = d;
+  p.K = n;
+  p.groups = E;
+  p.offsets = offsets;
+  p.rows_cap = static_cast<int>(cap);
+  p.out0 = Yw;
+  p.ld_out = d;
+  p.row_scale = sorted_w;
+  const int BN = gemm_bn(d);
+  Maps m = zero_maps();
+  if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
+      !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+  VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  return MOE_OK;
+}
+
 extern "C" {
 
 int moe_create(moe_ctx** out, int device) {
@@ -494,28 +518,69 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
     VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  // down projection, scaled by the combine weight of each row
+  return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
+}
+
+int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, float* scales,
+                           moe_stream_t stream) {
+  VGG_REQUIRE(ctx && M && q && scales);
+  VGG_REQUIRE(rows >= 0 && rows <= (1ll << 31) && cols >= 16 && cols % 16 == 0);
+  VGG_REQUIRE(aligned16(M) && aligned16(q));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VGG_LAUNCH("quantize_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(M), rows, cols,
+                                                        static_cast<uint8_t*>(q), scales, s));
+  return MOE_OK;
+}
+
+int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale, const void* Wg_q,
+                              const float* wg_scale, const void* Wu_q, const float* wu_scale, const void* W_down,
+                              int T, int d, int E, int n, long long cap, const int32_t* offsets,
+                              const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
+                              moe_stream_t stream) {
+  VGG_REQUIRE(ctx && Xq && x_scale && Wg_q && wg_scale && Wu_q && wu_scale && W_down && offsets && sorted_tok &&
+              sorted_w && H && U && A && Yw);
+  VGG_REQUIRE(shapes_ok(T, d, E, n, 1) && d % 128 == 0);
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
+  VGG_REQUIRE(aligned16(Xq) && aligned16(Wg_q) && aligned16(Wu_q) && aligned16(W_down) && aligned16(H) &&
+              aligned16(U) && aligned16(A) && aligned16(Yw));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
+    // e4m3 rows are handed to TMA and to the gather as rows of d / 2 16-bit units (code pairs): the
+    // 128-byte stage rows, swizzle and coordinates are those of the bf16 form
+    const int dk = d / 2;
     GemmParams p = base_params(ctx);
-    p.N = d;
-    p.K = n;
+    p.N = n;
+    p.K = dk;
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
-    p.out0 = Yw;
-    p.ld_out = d;
-    p.row_scale = sorted_w;
-    const int BN = gemm_bn(d);
+    p.a_idx = sorted_tok;
+    p.a_rows = T;
+    p.a_src = static_cast<const __nv_bfloat16*>(Xq);
+    p.a_ld = dk;
+    p.out0 = H;
+    p.out1 = U;
+    p.out2 = A;
+    p.ld_out = n;
+    p.row_scale = x_scale;
+    p.in0 = wg_scale;
+    p.in1 = wu_scale;
+    p.ld_in = n;
+    const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
-        !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
+    if (!make_map_3d(&m.b0, Wg_q, dk, n, E, BN / 2) || !make_map_3d(&m.b1, Wu_q, dk, n, E, BN / 2) ||
+        !make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32) ||
+        !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
-    m.a1 = m.a0;
-    m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-    VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
+    const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
+    VGG_LAUNCH("gate_up_swiglu_e4m3", run_gate_up_swiglu_e4m3(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  return MOE_OK;
+  return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
 }
 
 int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,

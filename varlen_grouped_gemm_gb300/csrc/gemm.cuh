@@ -50,7 +50,9 @@ constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 thi
 enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
-enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3 };
+// EPI_SWIGLU_Q: the SwiGLU epilogue of the e4m3 form (operands are e4m3 codes of per-row-scaled
+// rows; the accumulator is multiplied by the token's scale and the output channel's scale first).
+enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4 };
 
 struct GemmParams {
   int M, N, K;
@@ -78,8 +80,8 @@ struct GemmParams {
   void* out2;
   long long ld_out;
   int out_rows_split;  // VAR_K: output rows >= split go to the second output at row - split
-  const float* row_scale;  // VAR_M: per sorted row (combine weight)
-  const float* in0;        // dSwiGLU epilogue: H, U (fp32)
+  const float* row_scale;  // VAR_M: per sorted row (combine weight); e4m3 SwiGLU: per source row of A
+  const float* in0;        // dSwiGLU epilogue: H, U (fp32); e4m3 SwiGLU: W_gate, W_up scales [groups][ld_in]
   const float* in1;
   long long ld_in;
   float* part;  // dSwiGLU epilogue: per-row partial dot products [rows][part_ld]
@@ -88,6 +90,15 @@ struct GemmParams {
   int* err;
   unsigned long long timeout_ns;
 };
+
+// One UMMA of the stage's K step: bf16 operands (K = 16) or e4m3 operands (K = 32); either way the
+// step covers 32 bytes of every 128-byte operand row.
+template <bool F8>
+__device__ __forceinline__ void umma_step(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (F8) umma_e4m3(d_tmem, adesc, bdesc, idesc, accumulate);
+  else umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+}
 
 // Tensor maps: a0/a1 and b0/b1 feed the operands, o0..o2 are the TMA-store targets.
 struct Maps {
@@ -360,7 +371,13 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   using L = SmemLayout<BN, STAGES, EW, DEPTH>;
   static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(EPI != EPI_SWIGLU || BMODE == B_TMA_K3_GU, "SwiGLU epilogue needs the gate/up pair layout");
+  static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_Q) || BMODE == B_TMA_K3_GU,
+                "SwiGLU epilogue needs the gate/up pair layout");
+  // The e4m3 form moves 128-byte operand rows like the bf16 form: the host describes e4m3 rows to TMA
+  // and to the gather as 16-bit units (two codes each), so K, the coordinates and the swizzled layout
+  // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
+  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q);
+  static_assert(!kF8 || (AMODE == A_GATHER_K && VAR == VAR_M), "e4m3 form: gathered K-major A, varlen-M");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
   constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_GATHER_MN);
   constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
@@ -390,7 +407,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   constexpr uint32_t kTxBytes =
       (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
-  constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
+  constexpr uint32_t kIdesc =
+      kF8 ? idesc_e4m3(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0) : idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -761,7 +779,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
                   kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
               const uint64_t bd =
                   kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+              umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
             }
             if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
             else umma_commit(&empty_bar[s]);
@@ -823,7 +841,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+            umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
           }
           if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
           else umma_commit(&empty_bar[s]);
@@ -909,15 +927,20 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       constexpr int kCols = (EW == 8) ? BN / 2 : BN;  // accumulator columns handled by this warp
       const int c_lo = half * kCols;
 
-      if (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_DSWIGLU) {
+      if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE || EPI == EPI_DSWIGLU) {
         const long long orow = s_off[tl.g] + tl.m0 + row_local;
         const int crow = s_off[tl.g] + tl.m0 + quarter * 32;
         const long long roff = orow * p.ld_out;
         const OutRef o0{&mp.o0, p.out0, roff, crow, -1}, o1{&mp.o1, p.out1, roff, crow, -1},
             o2{&mp.o2, p.out2, roff, crow, -1};
-        if (EPI == EPI_SWIGLU) {
+        if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q) {
           // columns [0, BN/2) hold h, [BN/2, BN) hold u of the same output columns
           constexpr int kHalf = (EW == 8) ? BN / 4 : BN / 2;
+          float sx = 1.0f;  // e4m3 form: the scale of the row's token (an empty slot's row gets 0)
+          if (EPI == EPI_SWIGLU_Q && row_ok) {
+            const int tok = __ldg(p.a_idx + orow);
+            sx = (tok >= 0 && tok < p.a_rows) ? __ldg(p.row_scale + tok) : 0.0f;
+          }
 #pragma unroll 1
           for (int c = half * kHalf; c < (half + 1) * kHalf; c += 32) {
             uint32_t rh[32], ru[32];
@@ -931,6 +954,17 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             for (int i = 0; i < 32; ++i) {
               h[i] = __uint_as_float(rh[i]);
               u[i] = __uint_as_float(ru[i]);
+            }
+            if (EPI == EPI_SWIGLU_Q) {
+              // lane i holds the scales of column col + i; the warp's rows share them by shuffle
+              const long long so = static_cast<long long>(tl.g) * p.ld_in + col + lane;
+              const float gl = lane < ncols ? __ldg(p.in0 + so) : 0.0f;
+              const float ul = lane < ncols ? __ldg(p.in1 + so) : 0.0f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                h[i] *= sx * __shfl_sync(0xffffffffu, gl, i);
+                u[i] *= sx * __shfl_sync(0xffffffffu, ul, i);
+              }
             }
             emit32(o0, h, col, ncols, full, row_ok, true);  // H, U stay fp32 for the backward
             emit32(o1, u, col, ncols, full, row_ok, true);

@@ -1,0 +1,72 @@
+// Gate/up + SwiGLU grouped GEMM with e4m3 operands: the gathered token rows of X and the W_gate /
+// W_up pair are e4m3 codes of per-row-scaled rows, accumulated in fp32 by the kind::f8f6f4 UMMA; the
+// epilogue multiplies by the token's and the output channel's scale before SwiGLU.
+// [GG] "한계": the fine-grained FP8 grouped GEMM named there as the next 2x after bf16.
+#include <cuda_fp8.h>
+
+#include "internal.h"
+
+namespace vgg {
+
+cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) {
+    if (cn == 2)
+      return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU_Q, false, 2>(p, m, grid, s);
+    return launch_grouped_gemm<256, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU_Q, false>(p, m, grid, s);
+  }
+  return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU_Q, false>(p, m, grid, s);
+}
+
+// Per-row e4m3 quantization: s = max|row| / 448 (1 for a zero row), codes = e4m3(x / s), the division
+// in fp32 and the conversion rounding to nearest even and saturating at +-448.  One warp per row,
+// 8 elements (16 bytes) per lane and step; the second pass re-reads the row from L1/L2.
+__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ M, long long rows,
+                                                                 int cols, uint8_t* __restrict__ q,
+                                                                 float* __restrict__ scales) {
+  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(M + r * cols);
+  const int vecs = cols / 8;
+  float amax = 0.0f;
+  for (int v = lane; v < vecs; v += 32) {
+    const uint4 x = __ldg(src + v);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (lane == 0) scales[r] = s;
+  uint2* dst = reinterpret_cast<uint2*>(q + r * cols);
+  for (int v = lane; v < vecs; v += 32) {
+    const uint4 x = __ldg(src + v);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+    uint32_t w[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 a = __bfloat1622float2(h[2 * j]);
+      const float2 b = __bfloat1622float2(h[2 * j + 1]);
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)), __NV_SATFINITE, __NV_E4M3);
+      w[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    dst[v] = make_uint2(w[0], w[1]);
+  }
+}
+
+cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, int cols, uint8_t* q, float* scales,
+                                      cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  quantize_rows_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(M, rows, cols, q, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace vgg
