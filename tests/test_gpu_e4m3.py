@@ -61,7 +61,8 @@ CASES = [
     synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=512, d=256, E=16, n=192, K=4),
     synth.scaled(synth.WORKLOADS["c4"], name="c4_small", T=640, d=384, E=32, n=320, K=4),
     synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
-    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f05", T=512, d=256, E=16, n=192, K=4, capacity_factor=0.5),
+    # capacity factor 1 under a skewed load: some experts drop pairs, others leave slots empty
+    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias", T=512, d=256, E=16, n=192, K=4, bias="normal"),
 ]
 
 
