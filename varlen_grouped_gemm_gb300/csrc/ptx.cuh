@@ -262,7 +262,10 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
   return __bfloat1622float2(v);
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Logistic sigmoid from the fast exponential and the fast division intrinsics: relative error of a few
+// ulp of fp32 (far below the bf16 rounding of the activations it feeds); the correctly rounded division
+// made the SwiGLU epilogue the bottleneck of the gate/up GEMM.  For x below about -87 the result is 0.
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 }  // namespace vgg
 
