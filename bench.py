@@ -69,6 +69,8 @@ def kernel_work(wl, P, dW_bytes=2):
         "topk_softmax": (0, 4 * T * E + 8 * T * K),
         "permute": (0, 4 * T * K + 16 * P + (4 * T * E if wl.m_tile else 0)),
         "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 10 * P * n),
+        "gate_up_swiglu_e4m3": (4 * P * d * n, T * d + 4 * T + 2 * E * n * d + 8 * E * n + 10 * P * n),
+        "quantize_e4m3": (0, 3 * T * d + 4 * T),
         "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
         "combine": (0, 2 * P * d + 2 * T * d),
         "gather_rows": (0, 4 * T * d + 4 * P * d),
