@@ -4,16 +4,27 @@
 // [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기": the combine weights are the
 // softmax renormalised over the chosen experts, kept apart from the selection.
 //
-// One warp per token.  Lane l holds experts l, l+32, ... in registers; each of
-// the K rounds is a warp arg-max with the order (value descending, expert
-// ascending), so equal logits go to the lower expert.  The full softmax over E
-// (needed by token rounding) is written only when asked for.
+// One warp per token.  Lane l holds experts l, l+32, ... in registers as order-preserving unsigned keys
+// of the logits (-0 folded into +0 first, so that equal logits have equal keys); each of the K rounds is
+// a warp arg-max with the order (key descending, expert ascending), so equal logits go to the lower
+// expert.  Within a lane the slots are in ascending expert order, so a strict comparison keeps the
+// lowest expert among equal keys; a taken slot (and a slot past E) holds key 0, below every logit.
+// The full softmax over E (needed by token rounding) is written only when asked for.
 #include <cfloat>
 #include <climits>
 
 #include "internal.h"
 
 namespace vgg {
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t b = __float_as_uint(x + 0.0f);  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 // With split > 1 the router GEMM left `split` partial sums of the logits in part[split][T][E]: they are
 // added in split order with the bias and the result is written to logits first.
@@ -49,30 +60,36 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(float* __restrict__ l
       v[i] = (e < E) ? __ldg(row + e) : -FLT_MAX;
     }
   }
-  uint32_t taken = 0;
+  uint32_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) key[i] = (lane + 32 * i < E) ? order_key(v[i]) : 0u;
   float vmax = 0.0f, my_ex = 0.0f, sum = 0.0f;
   int my_id = 0;
   for (int k = 0; k < K; ++k) {
-    float bv = -FLT_MAX;
-    int be = INT_MAX;
+    uint32_t bk = 0u;
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
-      }
+      const bool better = key[i] > bk;
+      bk = better ? key[i] : bk;
+      bi = better ? i : bi;
     }
+    int be = bk ? lane + 32 * bi : INT_MAX;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
       const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
+      if (ok > bk || (ok == bk && oe < be)) {
+        bk = ok;
         be = oe;
       }
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (i == (be >> 5)) key[i] = 0u;
+    }
+    const float bv = key_value(bk);
     if (k == 0) vmax = bv;
     const float ex = expf(bv - vmax);
     sum += ex;  // same order in every lane: k ascending
