@@ -119,21 +119,32 @@ cudaError_t launch_transpose_bf16(const __nv_bfloat16* in, int rows, int cols, _
   return cudaGetLastError();
 }
 
-// Expert of sorted pair j: the e with offsets[e] <= j < offsets[e+1].
-__device__ __forceinline__ int expert_of(const int32_t* offsets, int E, int j) {
-  int lo = 0, hi = E;  // invariant: offsets[lo] <= j < offsets[hi]
+// Per token t (one warp; 8 tokens per CTA):
+//   dS[j]       = sum over column tiles of the dSwiGLU epilogue's partial <dA'_j, A_j>
+//   dlogits[t]  = [k in F(t)] w_k dS_k - [k in TopK(t)] w_k * sum_{i in F(t)} w_i dS_i
+//   dX[t]       = sum_j dXp[j] (ascending expert) + sum_e dlogits[t,e] W_r[:,e]
+// The CTA stages the group offsets in shared memory once (the expert of a pair is a binary search
+// there); each warp keeps its token's dlogits row in shared memory, so the only CTA-wide barrier is the
+// one after the offsets.
+constexpr int kTbWarps = 8;
+constexpr int kTbNz = kMaxTokPairs + 8;  // nonzero dlogits of a token: its pairs' experts and its top-K
+
+// Expert of sorted pair j: the e with off[e] <= j < off[e+1].
+__device__ __forceinline__ int expert_of_smem(const int* off, int E, int j) {
+  int lo = 0, hi = E;  // invariant: off[lo] <= j < off[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(offsets + mid) <= j) lo = mid;
+    if (off[mid] <= j) lo = mid;
     else hi = mid;
   }
   return lo;
 }
 
-// Per token t (one CTA):
-//   dS[j]       = sum over column tiles of the dSwiGLU epilogue's partial <dA'_j, A_j>
-//   dlogits[t]  = [k in F(t)] w_k dS_k - [k in TopK(t)] w_k * sum_{i in F(t)} w_i dS_i
-//   dX[t]       = sum_j dXp[j] (ascending expert) + sum_e dlogits[t,e] W_r[:,e]
+size_t token_backward_smem(int E) {
+  return sizeof(float) * kTbWarps * E + sizeof(int) * (E + 1) +
+         kTbWarps * (sizeof(int) * kMaxTokPairs + (sizeof(int) + sizeof(float)) * kTbNz);
+}
+
 __global__ void __launch_bounds__(256) token_backward_kernel(
     const float* __restrict__ part, int part_ld, const int32_t* __restrict__ tok_ptr,
     const int32_t* __restrict__ tok_pairs, const int32_t* __restrict__ offsets, int E,
@@ -141,78 +152,77 @@ __global__ void __launch_bounds__(256) token_backward_kernel(
     const __nv_bfloat16* __restrict__ dXp, const __nv_bfloat16* __restrict__ WrT, int T, int d, long long cap,
     float* __restrict__ dS, float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dL_bf16,
     __nv_bfloat16* __restrict__ dL_lo, __nv_bfloat16* __restrict__ dX, int* err) {
-  __shared__ float s_dl[kMaxGroups];
-  __shared__ int s_j[kMaxTokPairs];
-  __shared__ int s_nz_e[kMaxGroups];
-  __shared__ float s_nz_v[kMaxGroups];
-  __shared__ int s_cnt, s_nnz;
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += blockDim.x) s_dl[e] = 0.0f;
-  if (tid == 0) {
-    const long long p0 = tok_ptr[t], p1 = tok_ptr[t + 1];
-    int cnt = static_cast<int>(p1 - p0);
-    if (p0 < 0 || p1 > cap || cnt < 0 || cnt > kMaxTokPairs) {
+  extern __shared__ __align__(16) uint8_t tb_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* s_dl = reinterpret_cast<float*>(tb_smem) + warp * E;
+  int* s_off = reinterpret_cast<int*>(tb_smem + sizeof(float) * kTbWarps * E);
+  int* s_j = s_off + (E + 1) + warp * kMaxTokPairs;
+  int* s_nz_e = s_off + (E + 1) + kTbWarps * kMaxTokPairs + warp * kTbNz;
+  float* s_nz_v = reinterpret_cast<float*>(s_off + (E + 1) + kTbWarps * (kMaxTokPairs + kTbNz)) + warp * kTbNz;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldg(offsets + i);
+  __syncthreads();
+  const int t = blockIdx.x * kTbWarps + warp;
+  if (t >= T) return;
+  const long long p0 = __ldg(tok_ptr + t), p1 = __ldg(tok_ptr + t + 1);
+  int cnt = static_cast<int>(p1 - p0);
+  if (p0 < 0 || p1 > cap || cnt < 0 || cnt > kMaxTokPairs) {
+    if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
+    cnt = 0;
+  }
+  for (int e = lane; e < E; e += 32) s_dl[e] = 0.0f;
+  __syncwarp();
+  float g = 0.0f;
+  for (int r = lane; r < cnt; r += 32) {
+    const int j = __ldg(tok_pairs + p0 + r);
+    if (j < 0 || j >= cap) {
       set_error(err, DERR_BAD_OFFSETS);
-      cnt = 0;
+      s_j[r] = -1;
+      continue;
     }
-    s_cnt = cnt;
+    s_j[r] = j;
+    float ds = 0.0f;
+    for (int q = 0; q < part_ld; ++q) ds += __ldg(part + static_cast<long long>(j) * part_ld + q);
+    dS[j] = ds;
+    const float c = __ldg(sorted_w + j) * ds;
+    s_dl[expert_of_smem(s_off, E, j)] += c;  // the experts of one token are distinct
+    g += c;
   }
-  __syncthreads();
-  const int cnt = s_cnt;
-  const long long p0 = tok_ptr[t];
-  if (warp == 0) {
-    float g = 0.0f;
-    for (int r = lane; r < cnt; r += 32) {
-      int j = tok_pairs[p0 + r];
-      if (j < 0 || j >= cap) {
-        set_error(err, DERR_BAD_OFFSETS);
-        s_j[r] = -1;
-        continue;
-      }
-      s_j[r] = j;
-      float ds = 0.0f;
-      for (int q = 0; q < part_ld; ++q) ds += part[static_cast<long long>(j) * part_ld + q];
-      dS[j] = ds;
-      const int e = expert_of(offsets, E, j);
-      const float c = sorted_w[j] * ds;
-      s_dl[e] += c;  // the experts of one token are distinct
-      g += c;
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
-    __syncwarp();
-    if (lane < K) {
-      const int e = topk_ids[static_cast<long long>(t) * K + lane];
-      if (e >= 0 && e < E) s_dl[e] -= topk_w[static_cast<long long>(t) * K + lane] * g;
+  for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+  __syncwarp();
+  if (lane < K) {
+    const int e = __ldg(topk_ids + static_cast<long long>(t) * K + lane);
+    if (e >= 0 && e < E) s_dl[e] -= __ldg(topk_w + static_cast<long long>(t) * K + lane) * g;
+  }
+  __syncwarp();
+  int nnz = 0;
+  const long long rowE = static_cast<long long>(t) * E;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const float v = e < E ? s_dl[e] : 0.0f;
+    if (e < E) {
+      dlogits[rowE + e] = v;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      dL_bf16[rowE + e] = hi;
+      dL_lo[rowE + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
     }
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    const float v = s_dl[e];
-    dlogits[static_cast<long long>(t) * E + e] = v;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    dL_bf16[static_cast<long long>(t) * E + e] = hi;
-    dL_lo[static_cast<long long>(t) * E + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  }
-  if (warp == 0) {
-    int n = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const float v = e < E ? s_dl[e] : 0.0f;
-      const unsigned m = __ballot_sync(0xffffffffu, v != 0.0f);
-      if (v != 0.0f) {
-        const int pos = n + __popc(m & ((1u << lane) - 1u));
+    const unsigned m = __ballot_sync(0xffffffffu, v != 0.0f);
+    if (v != 0.0f) {
+      const int pos = nnz + __popc(m & ((1u << lane) - 1u));
+      if (pos < kTbNz) {
         s_nz_e[pos] = e;
         s_nz_v[pos] = v;
       }
-      n += __popc(m);
     }
-    if (lane == 0) s_nnz = n;
+    nnz += __popc(m);
   }
-  __syncthreads();
-  const int nnz = s_nnz;
+  if (nnz > kTbNz) {  // cannot happen: the nonzeros are the token's pair experts and its top-K
+    if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
+    nnz = kTbNz;
+  }
+  __syncwarp();
   const int nv = d >> 3;
-  for (int c = tid; c < nv; c += blockDim.x) {
+  for (int c = lane; c < nv; c += 32) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     int r = 0;
     for (; r + 4 <= cnt; r += 4) {  // four rows in flight per thread
@@ -245,12 +255,14 @@ cudaError_t launch_token_backward(const float* part, int part_ld, const int32_t*
                                   const float* topk_w, int K, const __nv_bfloat16* dXp, const __nv_bfloat16* WrT,
                                   int T, int d, long long cap, float* dS, float* dlogits, __nv_bfloat16* dL_bf16,
                                   __nv_bfloat16* dL_lo, __nv_bfloat16* dX, int* err, cudaStream_t s) {
-  // one thread per 16-byte column vector of a row (at least 64, at most 256 threads)
-  const int threads = d / 8 <= 64 ? 64 : (d / 8 >= 256 ? 256 : (d / 8 + 31) / 32 * 32);
-  if (T > 0)
-    token_backward_kernel<<<T, threads, 0, s>>>(part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w,
-                                                        topk_ids, topk_w, K, dXp, WrT, T, d, cap, dS, dlogits,
-                                                        dL_bf16, dL_lo, dX, err);
+  if (T <= 0) return cudaSuccess;
+  const size_t smem = token_backward_smem(E);
+  cudaError_t e = cudaFuncSetAttribute(token_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  token_backward_kernel<<<(T + kTbWarps - 1) / kTbWarps, 32 * kTbWarps, smem, s>>>(
+      part, part_ld, tok_ptr, tok_pairs, offsets, E, sorted_w, topk_ids, topk_w, K, dXp, WrT, T, d, cap, dS, dlogits,
+      dL_bf16, dL_lo, dX, err);
   return cudaGetLastError();
 }
 
