@@ -615,11 +615,12 @@ def main():
     ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
     ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
     ap.add_argument("--profile-run", action="store_true",
-                    help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline")
+                    help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline, no e4m3 forward")
     args = ap.parse_args()
     if args.profile_run:
         args.no_e2e = True
         args.no_cpu_baseline = True
+        args.no_e4m3 = True
     if args.ncu_summary:
         print(ncu_launch_summary(args.ncu_summary))
         return 0
