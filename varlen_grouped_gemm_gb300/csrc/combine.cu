@@ -345,6 +345,7 @@ namespace vgg {
 // pair (the tail [P, cap) and the empty slots of the capacity layout) are then written from a zeroed
 // chunk.  One token in flight per warp, three CTAs per SM.
 constexpr int kGrWarps = 8;
+static_assert(kMaxTokPairs <= 64, "gather_rows: at most two pair positions per lane");
 constexpr int kGrChunk = 2048;  // bf16 elements per bulk copy
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -377,7 +378,9 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   }
   fence_proxy_async_smem();  // the zero chunk is read by bulk stores
   __syncthreads();
-  if (lane != 0) return;
+  // A warp takes one token at a time: lane 0 loads the token's rows (one bulk copy per tensor and chunk)
+  // and every lane stores them to one (or two) of the token's pair positions, so the stores of a token
+  // are issued in parallel and the position lookups overlap the load.
   const uint32_t zero = smem_u32(gr_smem);
   const uint32_t buf = zero + kChunkBytes * (1 + 2 * warp);
   const long long P = offsets[E];
@@ -386,37 +389,50 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   uint32_t phase = 0;
   bool ok = true;
   for (long long t = gw; t < T && ok; t += nw) {
-    const long long q0 = tok_ptr[t], q1 = tok_ptr[t + 1];
-    if (q0 < 0 || q1 > cap || q1 < q0) {
-      set_error(err, DERR_BAD_OFFSETS);
+    const long long q0 = __ldg(tok_ptr + t), q1 = __ldg(tok_ptr + t + 1);
+    if (q0 < 0 || q1 > cap || q1 < q0 || q1 - q0 > kMaxTokPairs) {
+      if (lane == 0) set_error(err, DERR_BAD_OFFSETS);
       continue;
     }
-    if (q1 == q0) continue;
+    const int cnt = static_cast<int>(q1 - q0);
+    if (cnt == 0) continue;
+    long long jl[2] = {-1, -1};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lane + 32 * h;
+      if (r < cnt) {
+        const long long j = __ldg(tok_pairs + q0 + r);
+        if (j < 0 || j >= cap) set_error(err, DERR_BAD_OFFSETS);
+        else jl[h] = j;
+      }
+    }
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
-      bulk_wait_read<0>();  // the previous stores have read this warp's buffer
-      mbar_arrive_expect_tx(&bars[warp], 2 * bytes);
-      bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
-      bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
-      if (!mbar_wait(&bars[warp], phase, &abort_flag, timeout_ns, err)) {
+      bulk_wait_read<0>();  // this lane's previous stores have read the warp's buffer
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp], 2 * bytes);
+        bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
+        bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+      }
+      const int landed = mbar_wait(&bars[warp], phase, &abort_flag, timeout_ns, err) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, landed)) {
         ok = false;
         break;
       }
       phase ^= 1u;
-      for (long long q = q0; q < q1; ++q) {
-        const long long j = tok_pairs[q];
-        if (j < 0 || j >= cap) {
-          set_error(err, DERR_BAD_OFFSETS);
-          continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (jl[h] >= 0) {
+          bulk_s2g(out_a + jl[h] * d + c0, buf, bytes);
+          bulk_s2g(out_b + jl[h] * d + c0, buf + kChunkBytes, bytes);
         }
-        bulk_s2g(out_a + j * d + c0, buf, bytes);
-        bulk_s2g(out_b + j * d + c0, buf + kChunkBytes, bytes);
       }
       bulk_commit();
     }
   }
   // positions without a pair: the tail and the empty slots of the capacity layout
-  for (long long j = gw; j < cap && ok; j += nw) {
+  for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32) {
     if (j < P && sorted_tok[j] >= 0) continue;
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
     }
     bulk_commit();
   }
-  if (!ok) {  // a load that never completed: let copies in flight land before leaving
+  if (!ok && lane == 0) {  // a load that never completed: let copies in flight land before leaving
     volatile int never = 0;
     mbar_wait(&bars[warp], phase, &never, 20000000ull, nullptr);
   }
