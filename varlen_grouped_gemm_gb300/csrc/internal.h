@@ -68,6 +68,14 @@ struct PermuteWs {
   int32_t* plain_tok;  // [T * K]
   float* scoresT;      // [E * T] scores transposed (token rounding)
 };
+// Tokens per grouping block: the smallest of 32, 64, 128, 256 whose [E x blocks] histogram and block
+// bases stay within 65536 counts ((E + 1) x blocks), else 256.  Small token counts get more, smaller
+// blocks; for T <= 32768 and E <= 512 everything fits the fixed scratch of moe_permute_noalloc.
+inline int perm_tok_block(int T, int E) {
+  for (int tb = 32; tb < 256; tb *= 2)
+    if (static_cast<long long>(E + 1) * ((T + tb - 1) / tb) <= 65536) return tb;
+  return 256;
+}
 size_t permute_ws_bytes(int T, int E, int K, int m_tile);
 PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile);
 

@@ -3,8 +3,8 @@
 // Examples: code that only receives buffers handed to it by a host runtime with no allocator
 // interface, or a loop that must not call into an allocator once it is running.
 //
-// The grouping's scratch (per-expert, per-256-token-block counts and their scan, plus the
-// per-block pair bases) lives in a file-scope device array of fixed size, which every GPU that
+// The grouping's scratch (per-expert, per-token-block counts and their scan, plus the per-block
+// pair bases; perm_tok_block keeps them within the array for T <= 32768, E <= 512) lives in a file-scope device array of fixed size, which every GPU that
 // loads this library keeps until the process exits.  Host code cannot pass that array's name to
 // a kernel (in host code it names a host-side stand-in, not device memory), so the first call on
 // each device looks up the array's device address with cudaGetSymbolAddress and caches it.
@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kNoAllocMaxT = 32768;                // tokens
 constexpr int kNoAllocMaxE = 512;                  // experts
-constexpr int kNoAllocBlocks = kNoAllocMaxT / 256;  // 256-token blocks of the grouping
+constexpr int kNoAllocBlocks = kNoAllocMaxT / 256;  // the array holds (E + 1) x 128 + 1 counts
 constexpr int kNoAllocScratchInts = kNoAllocMaxE * kNoAllocBlocks + kNoAllocBlocks + 1;  // hist + block bases
 
 // 65,665 ints = 257 KiB; contents are fully rewritten by every call before they are read.
@@ -62,14 +62,19 @@ extern "C" int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const 
   if (!scratch) {
     status = MOE_ERR_CUDA;
   } else {
-    const int nb = (T + 255) / 256;
-    PermuteWs w{};
-    w.hist = scratch;
-    w.tokblk = scratch + static_cast<long long>(E) * nb;
-    if (launch_permute(topk_ids, topk_w, nullptr, nullptr, T, E, K, 0, cap, counts, offsets, sorted_tok, sorted_w,
-                       tok_ptr, tok_pairs, P_out, w, ctx_error_word(ctx), static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-      status = MOE_ERR_CUDA;
+    const int tb = perm_tok_block(T, E);
+    const int nb = (T + tb - 1) / tb;
+    if (static_cast<long long>(E + 1) * nb + 1 > kNoAllocScratchInts) {
+      status = MOE_ERR_UNSUPPORTED;
+    } else {
+      PermuteWs w{};
+      w.hist = scratch;
+      w.tokblk = scratch + static_cast<long long>(E) * nb;
+      if (launch_permute(topk_ids, topk_w, nullptr, nullptr, T, E, K, 0, cap, counts, offsets, sorted_tok, sorted_w,
+                         tok_ptr, tok_pairs, P_out, w, ctx_error_word(ctx), static_cast<cudaStream_t>(stream)) !=
+          cudaSuccess)
+        status = MOE_ERR_CUDA;
+    }
   }
   if (prev != device) cudaSetDevice(prev);
   return status;

@@ -27,7 +27,6 @@
 
 namespace vgg {
 
-constexpr int kTokBlock = 256;
 
 __device__ __forceinline__ int block_exclusive_scan_256(int v, int* s_warp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -65,9 +64,19 @@ __device__ __forceinline__ int token_experts(int t, const int32_t* ids, const fl
                                              int max_out, int* err) {
   int cnt = 0;
   if (!FROM_MEMBER) {
-    for (int k = 0; k < K; ++k) {
-      const int e = ids[static_cast<long long>(t) * K + k];
-      const float w = topk_w ? topk_w[static_cast<long long>(t) * K + k] : 0.0f;
+    // the token's K choices (K <= 8) loaded together, then inserted in ascending expert order
+    int ek[8];
+    float wk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      ek[k] = k < K ? __ldg(ids + static_cast<long long>(t) * K + k) : 0;
+      wk[k] = (k < K && topk_w) ? __ldg(topk_w + static_cast<long long>(t) * K + k) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k >= K) break;
+      const int e = ek[k];
+      const float w = wk[k];
       if (e < 0 || e >= E) {
         set_error(err, DERR_BAD_EXPERT);
         continue;
@@ -118,24 +127,25 @@ __device__ __forceinline__ int token_experts(int t, const int32_t* ids, const fl
   return cnt;
 }
 
-template <bool FROM_MEMBER>
-__global__ void __launch_bounds__(kTokBlock) perm_hist_kernel(const int32_t* __restrict__ ids,
-                                                             const uint32_t* __restrict__ member, int T, int E,
-                                                             int K, int nb, int32_t* __restrict__ hist,
-                                                             int32_t* __restrict__ tokblk, int* err) {
-  extern __shared__ uint32_t bits[];  // [E][8]
+template <bool FROM_MEMBER, int TB>
+__global__ void __launch_bounds__(TB) perm_hist_kernel(const int32_t* __restrict__ ids,
+                                                      const uint32_t* __restrict__ member, int T, int E, int K,
+                                                      int nb, int32_t* __restrict__ hist,
+                                                      int32_t* __restrict__ tokblk, int* err) {
+  constexpr int NW = TB / 32;  // membership words per expert
+  extern __shared__ uint32_t bits[];  // [E][NW]
   __shared__ int s_warp[33];
   const int b = blockIdx.x, tid = threadIdx.x;
-  for (int i = tid; i < E * 8; i += kTokBlock) bits[i] = 0;
+  for (int i = tid; i < E * NW; i += TB) bits[i] = 0;
   __syncthreads();
-  const int t = b * kTokBlock + tid;
+  const int t = b * TB + tid;
   int cnt = 0;
   if (t < T) {
     if (!FROM_MEMBER) {
       int es[8];
       float ws[8];
       cnt = token_experts<false>(t, ids, nullptr, nullptr, nullptr, E, K, es, ws, 8, err);
-      for (int q = 0; q < cnt; ++q) atomicOr(&bits[es[q] * 8 + (tid >> 5)], 1u << (tid & 31));
+      for (int q = 0; q < cnt; ++q) atomicOr(&bits[es[q] * NW + (tid >> 5)], 1u << (tid & 31));
     } else {
       const int W = (E + 31) >> 5;
       for (int wi = 0; wi < W; ++wi) {
@@ -143,17 +153,17 @@ __global__ void __launch_bounds__(kTokBlock) perm_hist_kernel(const int32_t* __r
         while (word) {
           const int bit = __ffs(word) - 1;
           word &= word - 1;
-          atomicOr(&bits[(wi * 32 + bit) * 8 + (tid >> 5)], 1u << (tid & 31));
+          atomicOr(&bits[(wi * 32 + bit) * NW + (tid >> 5)], 1u << (tid & 31));
           ++cnt;
         }
       }
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kTokBlock) {
+  for (int e = tid; e < E; e += TB) {
     int s = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) s += __popc(bits[e * 8 + w]);
+    for (int w = 0; w < NW; ++w) s += __popc(bits[e * NW + w]);
     hist[static_cast<long long>(e) * nb + b] = s;
   }
   int total;
@@ -263,22 +273,23 @@ void launch_scan(int32_t* hist, int E, int nb, int32_t* tokblk, int32_t* counts,
   perm_scan_kernel<<<1, 1024, 0, s>>>(counts, E, tokblk, nb, offsets, P_out, cap, err);
 }
 
-template <bool FROM_MEMBER>
-__global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
+template <bool FROM_MEMBER, int TB>
+__global__ void __launch_bounds__(TB) perm_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ topk_w, const uint32_t* __restrict__ member,
     const float* __restrict__ logits, int T, int E, int K, int nb, const int32_t* __restrict__ base,
     const int32_t* __restrict__ eoff,
     const int32_t* __restrict__ tokbase, long long cap, int32_t* __restrict__ sorted_tok,
     float* __restrict__ sorted_w, int32_t* __restrict__ tok_ptr, int32_t* __restrict__ tok_pairs, int* err,
     int slot_stride) {
-  extern __shared__ uint32_t bits[];  // [E][8]
+  constexpr int NW = TB / 32;
+  extern __shared__ uint32_t bits[];  // [E][NW]
   __shared__ int s_warp[33];
   // pairs per token: K without rounding; rounding may pad a token into more experts
   constexpr int kMaxPairs = FROM_MEMBER ? 32 : 8;
   const int b = blockIdx.x, tid = threadIdx.x;
-  for (int i = tid; i < E * 8; i += kTokBlock) bits[i] = 0;
+  for (int i = tid; i < E * NW; i += TB) bits[i] = 0;
   __syncthreads();
-  const int t = b * kTokBlock + tid;
+  const int t = b * TB + tid;
   int es[kMaxPairs];
   float ws[kMaxPairs];
   int cnt = 0;
@@ -288,7 +299,7 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
       set_error(err, DERR_CAPACITY);
       cnt = kMaxPairs;
     }
-    for (int q = 0; q < cnt; ++q) atomicOr(&bits[es[q] * 8 + (tid >> 5)], 1u << (tid & 31));
+    for (int q = 0; q < cnt; ++q) atomicOr(&bits[es[q] * NW + (tid >> 5)], 1u << (tid & 31));
   }
   __syncthreads();
   int total;
@@ -298,14 +309,25 @@ __global__ void __launch_bounds__(kTokBlock) perm_scatter_kernel(
   if (t == T - 1 && tok_ptr) tok_ptr[T] = static_cast<int32_t>(tp + cnt);
   const int w_self = tid >> 5;
   const uint32_t lt_mask = (1u << (tid & 31)) - 1u;
-  for (int q = 0; q < cnt; ++q) {
+  // base: the pair's rank among its expert's pairs before this token block; eoff: the expert's first
+  // position (capacity layout: expert e's kept pairs fill slots [e * slot_stride, ...) in token order).
+  // The lookups of a token's pairs are issued together before any is used.
+  long long first[kMaxPairs];
+#pragma unroll
+  for (int q = 0; q < kMaxPairs; ++q) {
+    if (q < cnt) {
+      const int e = es[q];
+      first[q] = static_cast<long long>(__ldg(base + static_cast<long long>(e) * nb + b)) +
+                 (slot_stride > 0 ? static_cast<long long>(e) * slot_stride : __ldg(eoff + e));
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxPairs; ++q) {
+    if (q >= cnt) break;
     const int e = es[q];
-    int rank = __popc(bits[e * 8 + w_self] & lt_mask);
-    for (int w = 0; w < w_self; ++w) rank += __popc(bits[e * 8 + w]);
-    // base: the pair's rank among its expert's pairs before this token block; eoff: the expert's first
-    // position (capacity layout: expert e's kept pairs fill slots [e * slot_stride, ...) in token order)
-    const long long in_e = static_cast<long long>(base[static_cast<long long>(e) * nb + b]) + rank;
-    const long long j = (slot_stride > 0 ? static_cast<long long>(e) * slot_stride : eoff[e]) + in_e;
+    int rank = __popc(bits[e * NW + w_self] & lt_mask);
+    for (int w = 0; w < w_self; ++w) rank += __popc(bits[e * NW + w]);
+    const long long j = first[q] + rank;
     if (j >= cap || tp + q >= cap) {
       set_error(err, DERR_CAPACITY);
       continue;
@@ -570,7 +592,8 @@ __global__ void slot_offsets_kernel(int32_t* offsets, int E, int C, int32_t* P_o
 }
 
 size_t permute_ws_bytes(int T, int E, int K, int m_tile) {
-  const long long nb = (T + kTokBlock - 1) / kTokBlock;
+  const int tb = perm_tok_block(T, E);
+  const long long nb = (T + tb - 1) / tb;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t b = al(sizeof(int32_t) * E * nb) + al(sizeof(int32_t) * (nb + 1));
   if (m_tile > 0) {
@@ -582,7 +605,8 @@ size_t permute_ws_bytes(int T, int E, int K, int m_tile) {
 }
 
 PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile) {
-  const long long nb = (T + kTokBlock - 1) / kTokBlock;
+  const int tb = perm_tok_block(T, E);
+  const long long nb = (T + tb - 1) / tb;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   uint8_t* p = static_cast<uint8_t*>(ws);
   PermuteWs w{};
@@ -604,17 +628,29 @@ PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile) {
   return w;
 }
 
+// Launch a grouping kernel (template <bool FROM_MEMBER, int TB>) with TB threads per block.
+#define VGG_PERM_LAUNCH(KERNEL, FM, tb, nb, smem, s, ...)                        \
+  do {                                                                           \
+    switch (tb) {                                                                \
+      case 32: KERNEL<FM, 32><<<nb, 32, smem, s>>>(__VA_ARGS__); break;          \
+      case 64: KERNEL<FM, 64><<<nb, 64, smem, s>>>(__VA_ARGS__); break;          \
+      case 128: KERNEL<FM, 128><<<nb, 128, smem, s>>>(__VA_ARGS__); break;       \
+      default: KERNEL<FM, 256><<<nb, 256, smem, s>>>(__VA_ARGS__); break;        \
+    }                                                                            \
+  } while (0)
+
 cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const float* logits, const float* scores,
                            int T, int E, int K, int m_tile, long long cap, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
                            int32_t* P_out, const PermuteWs& w, int* err, cudaStream_t s) {
-  const int nb = (T + kTokBlock - 1) / kTokBlock;
-  const size_t bits_smem = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
+  const int tb = perm_tok_block(T, E);
+  const int nb = (T + tb - 1) / tb;
+  const size_t bits_smem = static_cast<size_t>(E) * (tb / 32) * sizeof(uint32_t);
   cudaError_t st;
   if (m_tile <= 0) {
-    perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
+    VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
     launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
-    perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
+    VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
                                                                 w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
                                                                 tok_ptr,
                                                                 tok_pairs, err, 0);
@@ -622,9 +658,9 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   }
   // plain grouping into the workspace (only the expert-grouped tokens are needed)
   const long long plain_cap = static_cast<long long>(T) * K;
-  perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
+  VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
   launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
-  perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, nullptr, nullptr, T, E, K, nb,
+  VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, nullptr, nullptr, T, E, K, nb,
                                                               w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
                                                               nullptr,
                                                               nullptr, nullptr, err, 0);
@@ -640,9 +676,9 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(w.scoresT, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
                                                  w.member, err);
   // group the final pairs
-  perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
+  VGG_PERM_LAUNCH(perm_hist_kernel, true, tb, nb, bits_smem, s, topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
   launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
-  perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, logits, T, E, K, nb,
+  VGG_PERM_LAUNCH(perm_scatter_kernel, true, tb, nb, bits_smem, s, topk_ids, topk_w, w.member, logits, T, E, K, nb,
                                                              w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
                                                              tok_ptr,
                                                              tok_pairs, err, 0);
@@ -653,14 +689,15 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
                                     int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
                                     float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
                                     const PermuteWs& w, int* err, cudaStream_t s) {
-  const int nb = (T + kTokBlock - 1) / kTokBlock;
-  const size_t bits_smem = static_cast<size_t>(E) * 8 * sizeof(uint32_t);
+  const int tb = perm_tok_block(T, E);
+  const int nb = (T + tb - 1) / tb;
+  const size_t bits_smem = static_cast<size_t>(E) * (tb / 32) * sizeof(uint32_t);
   const long long plain_cap = static_cast<long long>(T) * K;
   cudaError_t st;
   // plain grouping of the top-K pairs with their probabilities (into the workspace)
-  perm_hist_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
+  VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
   launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
-  perm_scatter_kernel<false><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
+  VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
                                                               w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
                                                               w.scoresT,
                                                               nullptr, nullptr, err, 0);
@@ -678,9 +715,9 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
   const size_t slots = static_cast<size_t>(E) * C;
   if ((st = cudaMemsetAsync(sorted_tok, 0xFF, sizeof(int32_t) * slots, s)) != cudaSuccess) return st;
   if ((st = cudaMemsetAsync(sorted_w, 0, sizeof(float) * slots, s)) != cudaSuccess) return st;
-  perm_hist_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
+  VGG_PERM_LAUNCH(perm_hist_kernel, true, tb, nb, bits_smem, s, topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
   launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, nullptr, cap, err, s);
-  perm_scatter_kernel<true><<<nb, kTokBlock, bits_smem, s>>>(topk_ids, topk_w, w.member, nullptr, T, E, K, nb,
+  VGG_PERM_LAUNCH(perm_scatter_kernel, true, tb, nb, bits_smem, s, topk_ids, topk_w, w.member, nullptr, T, E, K, nb,
                                                              w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
                                                              tok_ptr,
                                                              tok_pairs, err, C);
