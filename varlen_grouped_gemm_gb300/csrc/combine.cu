@@ -8,8 +8,8 @@
 // [SM] "7 한계 & 의의": the per-pair output Y is materialised and reduced
 // without float atomics, for determinism and precision.
 //
-// Every token is one CTA; its pairs are visited in ascending expert order
-// (tok_pairs), 16-byte vector loads per thread, fp32 accumulation.
+// The combine is one CTA per token, the per-token backward one warp per token; a token's pairs are
+// visited in ascending expert order (tok_pairs), 16-byte vector loads per thread, fp32 accumulation.
 #include "internal.h"
 
 namespace vgg {
