@@ -536,11 +536,22 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
   const int need = drop ? r : r - c;
   if (need == 0) return;
   const float* col = scoresT + static_cast<long long>(e) * T;  // this expert's scores, token-contiguous
+  if (drop) {
+    // the candidates are the c routed tokens, in token order: select among them alone
+    for (int i = tid; i < c; i += kTrThreads) {
+      const int t = plain_tok[off + i];
+      keys[i] = (t >= 0 && t < T) ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
+    }
+    __syncthreads();
+    select_take(keys, c, need, list, hist, s_res, [&](int i) {
+      atomicOr(&member[static_cast<long long>(plain_tok[off + i]) * W + ew], ebit);
+    });
+    return;
+  }
 #pragma unroll 4
   for (int t = tid; t < T; t += kTrThreads) {
     const bool is_routed = (routed[t >> 5] >> (t & 31)) & 1u;
-    const bool cand = drop ? is_routed : !is_routed;
-    keys[t] = cand ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
+    keys[t] = is_routed ? 0xFFFFFFFFu : __float_as_uint(__ldg(col + t));
   }
   __syncthreads();
   select_take(keys, T, need, list, hist, s_res, [&](int t) {
