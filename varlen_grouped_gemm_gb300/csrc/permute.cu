@@ -367,27 +367,12 @@ constexpr int kTrThreads = 1024;
 constexpr int kTrMaxT = 32768;
 constexpr int kTrListCap = 8192;  // compacted keys of the threshold bin; a larger bin rescans all keys
 
-// Histogram of digit (k >> shift) & (NB - 1) over keys matching `prefix` on `mask` (0xFFFFFFFF = not a
-// candidate), then the digit of the remaining-th largest: lane l of warp 0 owns NB/32 bins, a suffix
-// scan over lanes finds the owner of the bin, which walks its bins downwards.  Updates prefix, mask,
-// remaining; returns the count of the chosen bin.  Lanes with the same digit add once per warp.
+// The digit of the remaining-th largest from a filled histogram of digit (k >> shift) & (NB - 1): lane l
+// of warp 0 owns NB/32 bins, a suffix scan over lanes finds the owner of the bin, which walks its bins
+// downwards.  Updates prefix, mask, remaining; returns the count of the chosen bin.
 template <int NB>
-__device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& mask, int shift, int& remaining,
-                        int* hist, int* s_res) {
+__device__ int tr_pick(const int* hist, uint32_t& prefix, uint32_t& mask, int shift, int& remaining, int* s_res) {
   const int tid = threadIdx.x, lane = tid & 31;
-  for (int i = tid; i < NB; i += kTrThreads) hist[i] = 0;
-  __syncthreads();
-  for (int i0 = 0; i0 < n; i0 += kTrThreads) {
-    const int i = i0 + tid;
-    uint32_t dg = NB;
-    if (i < n) {
-      const uint32_t k = a[i];
-      if (k != 0xFFFFFFFFu && (k & mask) == prefix) dg = (k >> shift) & (NB - 1);
-    }
-    const unsigned grp = __match_any_sync(0xffffffffu, dg);
-    if (dg != static_cast<uint32_t>(NB) && lane == __ffs(grp) - 1) atomicAdd(&hist[dg], __popc(grp));
-  }
-  __syncthreads();
   if (tid < 32) {
     constexpr int PER = NB / 32;
     int sl = 0;
@@ -424,6 +409,34 @@ __device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& ma
   const int cnt = s_res[2];
   __syncthreads();
   return cnt;
+}
+
+// Add digit dg (NB = not counted) of each thread's key to hist, once per group of equal digits in the warp.
+template <int NB>
+__device__ __forceinline__ void tr_count(int* hist, uint32_t dg) {
+  const unsigned grp = __match_any_sync(0xffffffffu, dg);
+  if (dg != static_cast<uint32_t>(NB) && (threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&hist[dg], __popc(grp));
+}
+
+// Histogram of digit (k >> shift) & (NB - 1) over keys matching `prefix` on `mask` (0xFFFFFFFF = not a
+// candidate), then tr_pick.
+template <int NB>
+__device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& mask, int shift, int& remaining,
+                        int* hist, int* s_res) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < NB; i += kTrThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < n; i0 += kTrThreads) {
+    const int i = i0 + tid;
+    uint32_t dg = NB;
+    if (i < n) {
+      const uint32_t k = a[i];
+      if (k != 0xFFFFFFFFu && (k & mask) == prefix) dg = (k >> shift) & (NB - 1);
+    }
+    tr_count<NB>(hist, dg);
+  }
+  __syncthreads();
+  return tr_pick<NB>(hist, prefix, mask, shift, remaining, s_res);
 }
 
 
@@ -495,6 +508,99 @@ __device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* lis
   }
 }
 
+// Token rounding's padding: the `need` largest scores among the tokens not routed to the expert (col:
+// the expert's scores, token-contiguous; routed: bitmap of its routed tokens), ties to the lower token;
+// take(t) for each.  The candidates' keys are staged in keys[T] while their first digit is counted
+// (one pass over global memory); when the threshold bin fits the list, one pass over the keys takes
+// every key above that bin and compacts the bin's keys with their tokens, and the rest runs on the
+// list.  Otherwise select_take runs on the staged keys.
+template <class Take>
+__device__ void select_take_unrouted(const float* col, const uint32_t* routed, int T, int need, uint32_t* keys,
+                                     uint32_t* list, int* list_tok, int* hist, int* s_res, Take take) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int i = tid; i < 2048; i += kTrThreads) hist[i] = 0;
+  __syncthreads();
+#pragma unroll 4
+  for (int t0 = 0; t0 < T; t0 += kTrThreads) {
+    const int t = t0 + tid;
+    uint32_t dg = 2048;
+    if (t < T) {
+      const bool is_routed = (routed[t >> 5] >> (t & 31)) & 1u;
+      const uint32_t k = is_routed ? 0xFFFFFFFFu : __float_as_uint(__ldg(col + t));
+      keys[t] = k;
+      if (!is_routed) dg = k >> 21;
+    }
+    tr_count<2048>(hist, dg);
+  }
+  __syncthreads();
+  uint32_t prefix = 0, mask = 0;
+  int remaining = need;
+  const int bin_cnt = tr_pick<2048>(hist, prefix, mask, 21, remaining, s_res);
+  if (bin_cnt > kTrListCap) {  // a crowded bin: the general select on the staged keys
+    select_take(keys, T, need, list, hist, s_res, take);
+    return;
+  }
+  const uint32_t bin = prefix >> 21;
+  if (tid == 0) s_res[3] = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += kTrThreads) {
+    const int t = t0 + tid;
+    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
+    const bool cand = k != 0xFFFFFFFFu;
+    if (cand && (k >> 21) > bin) take(t);  // above the threshold bin: always in
+    const bool in = cand && (k >> 21) == bin;
+    const unsigned bal = __ballot_sync(0xffffffffu, in);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_res[3], __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (in && pos < kTrListCap) {
+      list[pos] = k;
+      list_tok[pos] = t;
+    }
+  }
+  __syncthreads();
+  const int nlist = min(s_res[3], kTrListCap);
+  tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
+  const int ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
+  // prefix is now the threshold key: the list's keys above it are in, and `remaining` of its ties,
+  // the lowest tokens first
+  for (int i = tid; i < nlist; i += kTrThreads) {
+    const uint32_t k = list[i];
+    if (k > prefix) {
+      take(list_tok[i]);
+    } else if (k == prefix && ties == remaining) {
+      take(list_tok[i]);
+    } else if (k == prefix && ties <= 256) {
+      int rank = 0;
+      const int ti = list_tok[i];
+      for (int q = 0; q < nlist; ++q) rank += (list[q] == prefix && list_tok[q] < ti) ? 1 : 0;
+      if (rank < remaining) take(ti);
+    }
+  }
+  if (ties == remaining || ties <= 256) return;
+  // many equal keys at the threshold: rank the ties in token order over the staged keys
+  __shared__ int s_wt[kTrThreads / 32];
+  const int warp_id = tid >> 5;
+  int tie_base = 0;
+  for (int base = 0; base < T; base += kTrThreads) {
+    const int t = base + tid;
+    const bool tie = t < T && keys[t] == prefix;
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    if (lane == 0) s_wt[warp_id] = __popc(bal);
+    __syncthreads();
+    int before = tie_base + __popc(bal & ((1u << lane) - 1u)), chunk_ties = 0;
+    for (int w = 0; w < kTrThreads / 32; ++w) {
+      const int cw = s_wt[w];
+      if (w < warp_id) before += cw;
+      chunk_ties += cw;
+    }
+    if (tie && before < remaining) take(t);
+    tie_base += chunk_ties;
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __restrict__ scoresT, int T, int E,
                                                               int m_tile, const int32_t* __restrict__ plain_off,
                                                               const int32_t* __restrict__ plain_tok,
@@ -504,6 +610,7 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
   uint32_t* keys = tr_smem;               // [T]; 0xFFFFFFFF = not a candidate
   uint32_t* routed = tr_smem + T;         // [ceil(T/32)]
   uint32_t* list = routed + ((T + 31) >> 5);  // [kTrListCap] keys of the threshold bin
+  int* list_tok = reinterpret_cast<int*>(list + kTrListCap);  // [kTrListCap] their tokens
   __shared__ int hist[2048];
   __shared__ int s_res[4];
   const int e = blockIdx.x, tid = threadIdx.x;
@@ -548,13 +655,7 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
     });
     return;
   }
-#pragma unroll 4
-  for (int t = tid; t < T; t += kTrThreads) {
-    const bool is_routed = (routed[t >> 5] >> (t & 31)) & 1u;
-    keys[t] = is_routed ? 0xFFFFFFFFu : __float_as_uint(__ldg(col + t));
-  }
-  __syncthreads();
-  select_take(keys, T, need, list, hist, s_res, [&](int t) {
+  select_take_unrouted(col, routed, T, need, keys, list, list_tok, hist, s_res, [&](int t) {
     atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
   });
 }
@@ -679,9 +780,9 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   // final token sets
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
-  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + (T + 31) / 32 + kTrListCap);
+  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + (T + 31) / 32 + 2 * kTrListCap);
   st = cudaFuncSetAttribute(tr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrMaxT / 32 + kTrListCap)));
+                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrMaxT / 32 + 2 * kTrListCap)));
   if (st != cudaSuccess) return st;
   transpose_f32_kernel<<<dim3((E + 31) / 32, (T + 31) / 32), dim3(32, 8), 0, s>>>(scores, T, E, w.scoresT);
   tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(w.scoresT, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
