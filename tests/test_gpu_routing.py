@@ -9,6 +9,7 @@
      exercise the lower-expert rule)."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import synth
@@ -76,6 +77,9 @@ def test_topk_sets_match_fp64_beyond_margin(ctx, wl):
     synth.scaled(synth.WORKLOADS["tiny"], name="tiny_int", integer=True),
     synth.scaled(synth.WORKLOADS["c2"], name="c2_int", T=512, d=128, E=32, n=64, integer=True),
     synth.scaled(synth.WORKLOADS["c5"], name="c5_int_tr", T=1024, d=64, E=16, n=64, m_tile=64, integer=True),
+    # thousands of candidates per expert with few distinct scores: the padding's threshold falls among
+    # hundreds of equal scores, taken in token order
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_int_tr_ties", T=8192, d=64, E=16, n=64, m_tile=128, integer=True),
 ], ids=lambda w: w.name)
 def test_integer_inputs_routing_fully_independent(ctx, wl):
     inp = Inputs(wl, with_grad=False)
@@ -94,3 +98,28 @@ def test_integer_inputs_routing_fully_independent(ctx, wl):
     assert (np.diff(np.sort(L64, 1), axis=1) == 0).any(), "integer logits should contain ties"
     if s32 is not None:
         oracle.compare("scores", g["scores"], s32)
+
+
+@pytest.mark.parametrize("reps", [3000, 100])
+def test_token_rounding_repeated_tokens(ctx, reps):
+    """Token rounding when tokens repeat (groups of `reps` identical rows): every expert's candidates come
+    in groups of equal scores, so the threshold of both the drop and the padding selection falls inside
+    a group and its equal scores are taken in token order (thousands of ties for reps=3000, tens for 100)."""
+    import varlen_grouped_gemm_gb300 as vgg
+    T, d, E, K, m_tile = 8192, 64, 16, 4, 128
+    rng = np.random.default_rng(reps)
+    X = np.repeat(rng.integers(-2, 3, (T // reps + 1, d)), reps, axis=0)[:T]
+    W_r = rng.integers(-2, 3, (d, E))
+    Xd = torch.tensor(X, dtype=torch.bfloat16, device="cuda")
+    Wd = torch.tensor(W_r, dtype=torch.bfloat16, device="cuda")
+    buf = vgg.Buffers.allocate(T, d, E, 64, K, m_tile, backward=False)
+    vgg.moe_route(ctx, Xd, Wd, None, K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws)
+    vgg.moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, E, m_tile, buf.counts, buf.offsets,
+                    buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    g = gpu_routing(buf)
+    r = check_routing_bit_exact(g, K, m_tile)
+    assert np.all(r.counts % m_tile == 0)
+    c = np.bincount(r.topk_ids.reshape(-1), minlength=E)
+    assert (r.counts < c).any() and (r.counts > c).any(), "both dropping and padding experts"
