@@ -31,6 +31,7 @@ from .moe_oracle import (  # noqa: F401
     moe_backward,
     moe_forward,
     moe_forward_fp8,
+    round_bf16,
     route_discrete,
     router_logits,
     quantize_rows_e4m3,

@@ -462,13 +462,23 @@ def dequantize_rows_e4m3(codes, scales) -> np.ndarray:
     return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
 
 
+def round_bf16(v) -> np.ndarray:
+    """Nearest bf16 value (8 significant bits, ties to even) of each element, as fp64 (normal range)."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)  # v = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
 def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,
-                    scores_for_routing=None, capacity: int = 0, policy: str = "position", drop_keys=None):
+                    scores_for_routing=None, capacity: int = 0, policy: str = "position", drop_keys=None,
+                    fp8_down: bool = False):
     """Forward of the layer with the gate/up projections from e4m3 operands (per-token scales on X,
     per-output-channel scales on W_gate and W_up, ``quantize_rows_e4m3``); routing (with the same
     token rounding / capacity options), SwiGLU, the down projection and the combine as in
-    ``moe_forward``.  Returns (O, cache) with the cache's ``h``, ``u``, ``a`` per sorted pair (fp64)
-    and the quantized operands."""
+    ``moe_forward``.  With ``fp8_down`` the down projection takes e4m3 operands as well: the
+    activation rows A (the bf16 operand of the down projection, ``round_bf16``) quantized per row and
+    W_down per output channel.  Returns (O, cache) with the cache's ``h``, ``u``, ``a`` per sorted
+    pair (fp64) and the quantized operands."""
     X64 = _f64(X)
     T, d = X64.shape
     E, n, _ = np.shape(W_gate)
@@ -486,7 +496,6 @@ def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0,
     P = routing.P
     h = np.zeros((P, n))
     u = np.zeros((P, n))
-    y_sorted = np.zeros((P, d))
     for e in range(E):
         lo, hi = routing.offsets[e], routing.offsets[e + 1]
         if hi == lo:
@@ -494,7 +503,22 @@ def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0,
         rows = routing.sorted_tok[lo:hi]
         h[lo:hi] = Xd[rows] @ Wg_d[e].T
         u[lo:hi] = Xd[rows] @ Wu_d[e].T
-        y_sorted[lo:hi] = (silu(h[lo:hi]) * u[lo:hi]) @ _f64(W_down[e]).T
+    a = silu(h) * u
+    extra = {}
+    if fp8_down:
+        aq, as_ = quantize_rows_e4m3(round_bf16(a).astype(np.float32))
+        dq, ds = quantize_rows_e4m3(np.asarray(W_down).reshape(E * d, n))
+        a_op = dequantize_rows_e4m3(aq, as_)
+        Wd_op = dequantize_rows_e4m3(dq, ds).reshape(E, d, n)
+        extra = dict(aq=aq, as_=as_, dq=dq, ds=ds)
+    else:
+        a_op, Wd_op = a, None
+    y_sorted = np.zeros((P, d))
+    for e in range(E):
+        lo, hi = routing.offsets[e], routing.offsets[e + 1]
+        if hi == lo:
+            continue
+        y_sorted[lo:hi] = a_op[lo:hi] @ (Wd_op[e] if fp8_down else _f64(W_down[e])).T
     O = combine(y_sorted, routing, w_full, T)
-    return O, dict(logits=L, routing=routing, w_full=w_full, h=h, u=u, a=silu(h) * u, y_sorted=y_sorted,
-                   xq=xq, xs=xs, gq=gq, gs=gs, uq=uq, us=us)
+    return O, dict(logits=L, routing=routing, w_full=w_full, h=h, u=u, a=a, y_sorted=y_sorted,
+                   xq=xq, xs=xs, gq=gq, gs=gs, uq=uq, us=us, **extra)

@@ -545,6 +545,45 @@ def test_fp8_gate_up_within_quantization_bound():
     assert 0 < np.max(np.abs(O8 - O)) < 0.2 * np.max(np.abs(O))
 
 
+def test_round_bf16_matches_torch_and_ties():
+    rng = np.random.default_rng(15)
+    # values with at most 24 significant bits, where torch's conversion (through fp32) is exact RNE
+    x = rng.standard_normal(20000).astype(np.float32).astype(np.float64) * np.exp2(rng.integers(-20, 20, 20000))
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(mo.round_bf16(x), ref)
+    # halfway cases round to the even neighbour
+    np.testing.assert_array_equal(mo.round_bf16([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0]),
+                                  [1.0, 1 + 2.0 ** -6, -1.0, 3.0])
+
+
+def test_fp8_down_within_quantization_bound():
+    # with e4m3 down-projection operands, y differs from (bf16 A) W_down^T by at most the element-wise
+    # quantization bound of A's rows and W_down's rows, and does differ
+    rng = np.random.default_rng(16)
+    T, d, E, n, K = 32, 64, 4, 32, 2
+    X = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wu = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wd = (rng.standard_normal((E, d, n)) * 0.1).astype(np.float32)
+    W_r = rng.standard_normal((d, E)) * 0.3
+    O8, c8 = mo.moe_forward_fp8(X, W_r, None, Wg, Wu, Wd, K, fp8_down=True)
+    O8g, c8g = mo.moe_forward_fp8(X, W_r, None, Wg, Wu, Wd, K)
+    r = c8["routing"]
+    np.testing.assert_array_equal(c8["h"], c8g["h"])  # the gate/up part is unchanged
+    a = mo.round_bf16(c8["a"])
+    da = np.maximum(2.0 ** -4 * np.abs(a), 2.0 ** -10 * c8["as_"].astype(np.float64)[:, None])
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        W = Wd[e].astype(np.float64)
+        dw = np.maximum(2.0 ** -4 * np.abs(W), 2.0 ** -10 * c8["ds"][e * d:(e + 1) * d].astype(np.float64)[:, None])
+        exact = a[lo:hi] @ W.T
+        bound = np.abs(a[lo:hi]) @ dw.T + da[lo:hi] @ np.abs(W).T + da[lo:hi] @ dw.T
+        err = np.abs(c8["y_sorted"][lo:hi] - exact)
+        assert np.all(err <= bound * (1 + 1e-9) + 1e-300)
+        assert np.max(err) > 0
+    assert 0 < np.max(np.abs(O8 - O8g)) < 0.2 * np.max(np.abs(O8g))
+
+
 # ---------------------------------------------------------------- the metric
 
 
