@@ -217,7 +217,8 @@ int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols
                            moe_stream_t stream);
 
 /*
- * moe_grouped_gemm_fwd_e4m3 — moe_grouped_gemm_fwd with e4m3 gate/up operands.
+ * moe_grouped_gemm_fwd_e4m3 — moe_grouped_gemm_fwd with e4m3 gate/up operands and,
+ * optionally, an e4m3 down projection.
  * [GG] "한계" and "(6) 세 번의 gg.gmm"; [SM] "4.1 Gather 융합", "4.2 Epilogue 융합".
  * Xq [T,d] and x_scale [T]: moe_quantize_rows_e4m3 of X; Wg_q, Wu_q [E,n,d] and
  * wg_scale, wu_scale [E,n]: moe_quantize_rows_e4m3 of W_gate, W_up as [E*n, d].
@@ -225,18 +226,25 @@ int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols
  *
  *   H[j,c] = x_scale[t] * wg_scale[e,c] * sum_i e4m3(Xq[t,i]) e4m3(Wg_q[e,c,i])
  *   U[j,c] likewise with Wu_q, wu_scale;  A[j] = silu(H[j]) * U[j] (bf16)
- *   Yw[j]  = sorted_w[j] * (A[j] W_down[e]^T)   (bf16 operands, as moe_grouped_gemm_fwd)
  *
- * The code products are accumulated in fp32 on the tensor cores (kind::f8f6f4).
- * A slot with sorted_tok = -1 (capacity dispatch) gives zero rows.  Requires
- * d % 128 == 0 besides moe_grouped_gemm_fwd's shape rules; outputs and
- * ownership as moe_grouped_gemm_fwd; no workspace.
+ * Down projection, bf16 (Wd_q == NULL): Yw[j] = sorted_w[j] * (A[j] W_down[e]^T) as in
+ * moe_grouped_gemm_fwd.  e4m3 (Wd_q != NULL; W_down may be NULL): Wd_q [E,d,n] and wd_scale
+ * [E,d] are moe_quantize_rows_e4m3 of W_down as [E*d, n]; the rows of A below offsets[E] are
+ * quantized the same way into Aq [cap,n] (uint8 codes) and a_scale [cap] (caller-owned device
+ * buffers), and
+ *
+ *   Yw[j,c] = sorted_w[j] * a_scale[j] * wd_scale[e,c] * sum_i e4m3(Aq[j,i]) e4m3(Wd_q[e,c,i])
+ *
+ * Code products are accumulated in fp32 on the tensor cores (kind::f8f6f4).  A slot with
+ * sorted_tok = -1 (capacity dispatch) gives zero rows.  Requires d % 128 == 0 (and n % 128 == 0 for
+ * the e4m3 down projection) besides moe_grouped_gemm_fwd's shape rules; outputs H, U, A, Yw and
+ * ownership as moe_grouped_gemm_fwd; no workspace.  MOE_ERR_INVALID_ARG on a violated rule.
  */
 int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale, const void* Wg_q,
                               const float* wg_scale, const void* Wu_q, const float* wu_scale, const void* W_down,
-                              int T, int d, int E, int n, long long cap, const int32_t* offsets,
-                              const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
-                              moe_stream_t stream);
+                              const void* Wd_q, const float* wd_scale, int T, int d, int E, int n, long long cap,
+                              const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w, void* H,
+                              void* U, void* A, void* Aq, float* a_scale, void* Yw, moe_stream_t stream);
 
 /*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.

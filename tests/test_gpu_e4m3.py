@@ -66,21 +66,30 @@ CASES = [
 ]
 
 
-def _run(ctx, wl, dev):
+def _run(ctx, wl, dev, fp8_down=False):
     import varlen_grouped_gemm_gb300 as vgg
     buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False,
                                capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
-    w8 = vgg.E4m3Weights.quantize(ctx, dev["W_gate"], dev["W_up"])
+    w8 = vgg.E4m3Weights.quantize(ctx, dev["W_gate"], dev["W_up"], dev["W_down"] if fp8_down else None)
     vgg.forward_e4m3(ctx, dev["X"], dev["W_r"], dev["bias"], w8, dev["W_down"], buf)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == vgg.MOE_OK and code == 0, (rc, code)
     return buf, w8
 
 
-@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
-def test_e4m3_forward_matches_oracle(ctx, wl):
+DOWN8_CASES = [
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_small_n256", T=512, d=256, E=16, n=256, K=4),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
+    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias_n256", T=512, d=256, E=16, n=256, K=4, bias="normal"),
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small_zipf_n384", T=640, d=384, E=32, n=384, K=4),
+]
+
+
+@pytest.mark.parametrize("wl,fp8_down", [(w, False) for w in CASES] + [(w, True) for w in DOWN8_CASES],
+                         ids=lambda x: x.name if hasattr(x, "name") else ("down8" if x else "down16"))
+def test_e4m3_forward_matches_oracle(ctx, wl, fp8_down):
     inp = Inputs(wl, with_grad=False)
-    buf, w8 = _run(ctx, wl, inp.dev)
+    buf, w8 = _run(ctx, wl, inp.dev, fp8_down)
     E, n, d = wl.E, wl.n, wl.d
     xq, xs = mo.quantize_rows_e4m3(inp.X)
     np.testing.assert_array_equal(buf.xq.cpu().numpy(), xq)
@@ -94,7 +103,18 @@ def test_e4m3_forward_matches_oracle(ctx, wl):
     C = buf.capacity
     O_ref, cache = mo.moe_forward_fp8(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K, wl.m_tile,
                                       logits_for_routing=g["logits"], scores_for_routing=g["scores"], capacity=C,
-                                      policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None)
+                                      policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None,
+                                      fp8_down=fp8_down)
+    if fp8_down:
+        # W_down's codes, and A's codes against the oracle's quantization of the device's own bf16 A rows
+        q, s = mo.quantize_rows_e4m3(inp.W_down.reshape(E * d, n))
+        np.testing.assert_array_equal(w8.Wd_q.cpu().numpy().reshape(E * d, n), q)
+        np.testing.assert_array_equal(w8.wd_scale.cpu().numpy().reshape(-1), s)
+        rows = int(buf.offsets[E].item())
+        A_bits = buf.A[:rows].view(torch.int16).cpu().numpy().view(np.uint16)
+        qa, sa = mo.quantize_rows_e4m3(A_bits)
+        np.testing.assert_array_equal(buf.aq[:rows].cpu().numpy(), qa)
+        np.testing.assert_array_equal(buf.as_[:rows].cpu().numpy(), sa)
     r = cache["routing"]
     rep = {"O": oracle.compare("O", dev_to_f64(buf.O), O_ref)}
     if C:

@@ -74,8 +74,8 @@ def lib() -> ctypes.CDLL:
         L.moe_capacity_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
         L.moe_capacity_workspace_bytes.restype = _SZ
         L.moe_quantize_rows_e4m3.argtypes = [_P, _P, _LL, _I, _P, _P, _P]
-        L.moe_grouped_gemm_fwd_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P,
-                                                _P, _P, _P, _P, _P]
+        L.moe_grouped_gemm_fwd_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P,
+                                                _P, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -258,16 +258,18 @@ def moe_quantize_rows_e4m3(ctx, M, q, scales, stream=None):
 
 
 def moe_grouped_gemm_fwd_e4m3(ctx, Xq, x_scale, Wg_q, wg_scale, Wu_q, wu_scale, W_down, offsets, sorted_tok,
-                              sorted_w, H, U, A, Yw, stream=None):
+                              sorted_w, H, U, A, Yw, Wd_q=None, wd_scale=None, Aq=None, a_scale=None, stream=None):
+    """e4m3 gate/up; the down projection in bf16 (W_down) or, given Wd_q / wd_scale and the Aq / a_scale
+    buffers, in e4m3."""
     T, d = Xq.shape
     E, n, _ = Wg_q.shape
     cap = sorted_tok.numel()
     u8, f32 = torch.uint8, torch.float32
     _check("moe_grouped_gemm_fwd_e4m3", lib().moe_grouped_gemm_fwd_e4m3(
         ctx.handle, _ptr(Xq, u8), _ptr(x_scale, f32), _ptr(Wg_q, u8), _ptr(wg_scale, f32), _ptr(Wu_q, u8),
-        _ptr(wu_scale, f32), _ptr(W_down, torch.bfloat16), T, d, E, n, cap, _ptr(offsets, torch.int32),
-        _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32), _ptr(A, torch.bfloat16),
-        _ptr(Yw, torch.bfloat16), _stream(stream)))
+        _ptr(wu_scale, f32), _ptr(W_down, torch.bfloat16), _ptr(Wd_q, u8), _ptr(wd_scale, f32), T, d, E, n, cap,
+        _ptr(offsets, torch.int32), _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32),
+        _ptr(A, torch.bfloat16), _ptr(Aq, u8), _ptr(a_scale, f32), _ptr(Yw, torch.bfloat16), _stream(stream)))
 
 
 def moe_combine(ctx, Yw, tok_ptr, tok_pairs, O, stream=None):
@@ -359,6 +361,8 @@ class Buffers:
     drop_policy: str = "position"
     xq: torch.Tensor | None = None  # e4m3 forward: X's codes [T, d] and per-token scales [T]
     xs: torch.Tensor | None = None
+    aq: torch.Tensor | None = None  # e4m3 down projection: A's codes [cap, n] and per-row scales [cap]
+    as_: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
@@ -394,7 +398,8 @@ class Buffers:
             dS=z((cap,), f32) if backward else None, dlogits=z((T, E), f32) if backward else None,
             dW_r=z((d, E), f32) if backward else None,
             ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device), capacity=capacity, drop_policy=drop_policy,
-            xq=z((T, d), torch.uint8) if e4m3 else None, xs=z((T,), f32) if e4m3 else None)
+            xq=z((T, d), torch.uint8) if e4m3 else None, xs=z((T,), f32) if e4m3 else None,
+            aq=z((cap, n), torch.uint8) if e4m3 else None, as_=z((cap,), f32) if e4m3 else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
@@ -414,15 +419,18 @@ def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
 
 @dataclass
 class E4m3Weights:
-    """W_gate and W_up as e4m3 codes [E, n, d] (uint8) with one fp32 scale per output channel [E, n]."""
+    """W_gate and W_up as e4m3 codes [E, n, d] (uint8) with one fp32 scale per output channel [E, n]; with
+    W_down given, W_down as codes [E, d, n] with scales [E, d] too (the e4m3 down projection)."""
 
     Wg_q: torch.Tensor
     wg_scale: torch.Tensor
     Wu_q: torch.Tensor
     wu_scale: torch.Tensor
+    Wd_q: torch.Tensor | None = None
+    wd_scale: torch.Tensor | None = None
 
     @staticmethod
-    def quantize(ctx, W_gate, W_up, stream=None) -> "E4m3Weights":
+    def quantize(ctx, W_gate, W_up, W_down=None, stream=None) -> "E4m3Weights":
         E, n, d = W_gate.shape
         dev = W_gate.device
         w = E4m3Weights(torch.empty((E, n, d), dtype=torch.uint8, device=dev),
@@ -431,12 +439,17 @@ class E4m3Weights:
                         torch.empty((E, n), dtype=torch.float32, device=dev))
         moe_quantize_rows_e4m3(ctx, W_gate, w.Wg_q, w.wg_scale, stream)
         moe_quantize_rows_e4m3(ctx, W_up, w.Wu_q, w.wu_scale, stream)
+        if W_down is not None:
+            w.Wd_q = torch.empty((E, d, n), dtype=torch.uint8, device=dev)
+            w.wd_scale = torch.empty((E, d), dtype=torch.float32, device=dev)
+            moe_quantize_rows_e4m3(ctx, W_down, w.Wd_q, w.wd_scale, stream)
         return w
 
 
 def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, stream=None):
     """The forward with the gate/up GEMM on e4m3 operands (``buf`` allocated with ``e4m3=True``): routing and
-    grouping as ``forward``, X quantized per token, then the e4m3 grouped GEMMs and the combine."""
+    grouping as ``forward``, X quantized per token, then the e4m3 grouped GEMMs and the combine.  When ``w8``
+    holds W_down's codes the down projection runs on e4m3 operands too (``W_down`` may then be None)."""
     if buf.xq is None:
         raise ValueError("buffers were allocated without e4m3=True")
     moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
@@ -448,8 +461,11 @@ def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, strea
         moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts,
                     buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
     moe_quantize_rows_e4m3(ctx, X, buf.xq, buf.xs, stream)
-    moe_grouped_gemm_fwd_e4m3(ctx, buf.xq, buf.xs, w8.Wg_q, w8.wg_scale, w8.Wu_q, w8.wu_scale, W_down, buf.offsets,
-                              buf.sorted_tok, buf.sorted_w, buf.H, buf.U, buf.A, buf.Yw, stream)
+    moe_grouped_gemm_fwd_e4m3(ctx, buf.xq, buf.xs, w8.Wg_q, w8.wg_scale, w8.Wu_q, w8.wu_scale,
+                              None if w8.Wd_q is not None else W_down, buf.offsets, buf.sorted_tok, buf.sorted_w,
+                              buf.H, buf.U, buf.A, buf.Yw, Wd_q=w8.Wd_q, wd_scale=w8.wd_scale,
+                              Aq=buf.aq if w8.Wd_q is not None else None,
+                              a_scale=buf.as_ if w8.Wd_q is not None else None, stream=stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 

@@ -529,19 +529,22 @@ int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  VGG_LAUNCH("quantize_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(M), rows, cols,
+  VGG_LAUNCH("quantize_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(M), rows, nullptr, cols,
                                                         static_cast<uint8_t*>(q), scales, s));
   return MOE_OK;
 }
 
 int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale, const void* Wg_q,
                               const float* wg_scale, const void* Wu_q, const float* wu_scale, const void* W_down,
-                              int T, int d, int E, int n, long long cap, const int32_t* offsets,
-                              const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
-                              moe_stream_t stream) {
-  VGG_REQUIRE(ctx && Xq && x_scale && Wg_q && wg_scale && Wu_q && wu_scale && W_down && offsets && sorted_tok &&
-              sorted_w && H && U && A && Yw);
+                              const void* Wd_q, const float* wd_scale, int T, int d, int E, int n, long long cap,
+                              const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w, void* H,
+                              void* U, void* A, void* Aq, float* a_scale, void* Yw, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && Xq && x_scale && Wg_q && wg_scale && Wu_q && wu_scale && offsets && sorted_tok && sorted_w &&
+              H && U && A && Yw);
   VGG_REQUIRE(shapes_ok(T, d, E, n, 1) && d % 128 == 0);
+  // the down projection: bf16 (W_down) or e4m3 (Wd_q, wd_scale with the Aq, a_scale buffers)
+  const bool down8 = Wd_q != nullptr;
+  VGG_REQUIRE(down8 ? (wd_scale && Aq && a_scale && n % 128 == 0 && aligned16(Wd_q) && aligned16(Aq)) : W_down != nullptr);
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
   VGG_REQUIRE(aligned16(Xq) && aligned16(Wg_q) && aligned16(Wu_q) && aligned16(W_down) && aligned16(H) &&
               aligned16(U) && aligned16(A) && aligned16(Yw));
@@ -580,7 +583,35 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
     const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
     VGG_LAUNCH("gate_up_swiglu_e4m3", run_gate_up_swiglu_e4m3(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
+  if (!down8) return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
+  // A's rows (those below offsets[E]) to e4m3, then the e4m3 down projection
+  VGG_LAUNCH("quantize_a_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(A), cap, offsets + E, n,
+                                                          static_cast<uint8_t*>(Aq), a_scale, s));
+  {
+    const int nk = n / 2;  // code pairs, as in the gate/up form
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = nk;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.out0 = Yw;
+    p.ld_out = d;
+    p.row_scale = sorted_w;
+    p.in0 = a_scale;
+    p.in1 = wd_scale;
+    p.ld_in = d;
+    const int BN = gemm_bn(d);
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, BN) ||
+        !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("down_scale_e4m3", run_down_scale_e4m3(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  }
+  return MOE_OK;
 }
 
 int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,

@@ -50,9 +50,10 @@ constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 thi
 enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
-// EPI_SWIGLU_Q: the SwiGLU epilogue of the e4m3 form (operands are e4m3 codes of per-row-scaled
-// rows; the accumulator is multiplied by the token's scale and the output channel's scale first).
-enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4 };
+// EPI_SWIGLU_Q, EPI_SCALE_Q: the SwiGLU and the combine-weight epilogues of the e4m3 form (operands are
+// e4m3 codes of per-row-scaled rows; the accumulator is multiplied by the A row's scale and the
+// output channel's scale first).
+enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5 };
 
 struct GemmParams {
   int M, N, K;
@@ -81,8 +82,8 @@ struct GemmParams {
   long long ld_out;
   int out_rows_split;  // VAR_K: output rows >= split go to the second output at row - split
   const float* row_scale;  // VAR_M: per sorted row (combine weight); e4m3 SwiGLU: per source row of A
-  const float* in0;        // dSwiGLU epilogue: H, U (fp32); e4m3 SwiGLU: W_gate, W_up scales [groups][ld_in]
-  const float* in1;
+  const float* in0;        // dSwiGLU: H, U (fp32); e4m3 SwiGLU: W_gate, W_up scales [groups][ld_in];
+  const float* in1;        // e4m3 combine-weight epilogue: A row scales [rows], W scales [groups][ld_in]
   long long ld_in;
   float* part;  // dSwiGLU epilogue: per-row partial dot products [rows][part_ld]
   int part_ld;
@@ -376,8 +377,10 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   // The e4m3 form moves 128-byte operand rows like the bf16 form: the host describes e4m3 rows to TMA
   // and to the gather as 16-bit units (two codes each), so K, the coordinates and the swizzled layout
   // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
-  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q);
-  static_assert(!kF8 || (AMODE == A_GATHER_K && VAR == VAR_M), "e4m3 form: gathered K-major A, varlen-M");
+  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q);
+  static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
+                         VAR == VAR_M),
+                "e4m3 form: K-major operands, varlen-M");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
   constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_GATHER_MN);
   constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
@@ -927,7 +930,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       constexpr int kCols = (EW == 8) ? BN / 2 : BN;  // accumulator columns handled by this warp
       const int c_lo = half * kCols;
 
-      if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE || EPI == EPI_DSWIGLU) {
+      if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE || EPI == EPI_SCALE_Q || EPI == EPI_DSWIGLU) {
         const long long orow = s_off[tl.g] + tl.m0 + row_local;
         const int crow = s_off[tl.g] + tl.m0 + quarter * 32;
         const long long roff = orow * p.ld_out;
@@ -972,8 +975,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             for (int i = 0; i < 32; ++i) h[i] = h[i] * sigmoidf_(h[i]) * u[i];  // A, in place of h
             emit32(o2, h, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
           }
-        } else if (EPI == EPI_SCALE) {
-          const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
+        } else if (EPI == EPI_SCALE || EPI == EPI_SCALE_Q) {
+          float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
+          if (EPI == EPI_SCALE_Q && row_ok) w *= __ldg(p.in0 + orow);  // the A row's e4m3 scale
 #pragma unroll 1
           for (int c = c_lo; c < c_lo + kCols; c += 64) {
             uint32_t r0[32], r1[32];
@@ -981,10 +985,23 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             tmem_ld32(tbase + c + 32, r1);
             tmem_ld_wait();
             float v[64];
+            if (EPI == EPI_SCALE_Q) {
+              // lane i holds the scales of columns c + i and c + 32 + i; the warp's rows share them
+              const int col = tl.n0 + c + lane;
+              const long long so = static_cast<long long>(tl.g) * p.ld_in + col;
+              const float s0 = col < p.N ? __ldg(p.in1 + so) : 0.0f;
+              const float s1 = col + 32 < p.N ? __ldg(p.in1 + so + 32) : 0.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[i] = w * __uint_as_float(r0[i]);
-              v[32 + i] = w * __uint_as_float(r1[i]);
+              for (int i = 0; i < 32; ++i) {
+                v[i] = w * __shfl_sync(0xffffffffu, s0, i) * __uint_as_float(r0[i]);
+                v[32 + i] = w * __shfl_sync(0xffffffffu, s1, i) * __uint_as_float(r1[i]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] = w * __uint_as_float(r0[i]);
+                v[32 + i] = w * __uint_as_float(r1[i]);
+              }
             }
             emit64(o0, v, tl.n0 + c, p.N - tl.n0 - c, full, row_ok);
           }

@@ -17,15 +17,23 @@ cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const M
   return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU_Q, false>(p, m, grid, s);
 }
 
+// Down projection with e4m3 operands (A rows and W_down rows quantized per row); the epilogue multiplies
+// by the A row's scale, the output channel's scale and the combine weight.
+cudaError_t run_down_scale_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
+}
+
 // Per-row e4m3 quantization: s = max|row| / 448 (1 for a zero row), codes = e4m3(x / s), the division
 // in fp32 and the conversion rounding to nearest even and saturating at +-448.  One warp per row,
 // 8 elements (16 bytes) per lane and step; the second pass re-reads the row from L1/L2.
 __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ M, long long rows,
-                                                                 int cols, uint8_t* __restrict__ q,
+                                                                 const int32_t* __restrict__ rows_limit, int cols,
+                                                                 uint8_t* __restrict__ q,
                                                                  float* __restrict__ scales) {
   const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+  if (r >= rows || (rows_limit && r >= __ldg(rows_limit))) return;
   const uint4* src = reinterpret_cast<const uint4*>(M + r * cols);
   const int vecs = cols / 8;
   float amax = 0.0f;
@@ -61,11 +69,12 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bflo
   }
 }
 
-cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, int cols, uint8_t* q, float* scales,
-                                      cudaStream_t s) {
+// rows_limit (device, optional): only rows below *rows_limit are quantized.
+cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
+                                      uint8_t* q, float* scales, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;
-  quantize_rows_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(M, rows, cols, q, scales);
+  quantize_rows_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
   return cudaGetLastError();
 }
 

@@ -29,8 +29,9 @@ bool make_store_map_3d(CUtensorMap* m, void* ptr, bool fp32, uint64_t cols, uint
 // forward
 cudaError_t run_gate_up_swiglu(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, int cols, uint8_t* q, float* scales,
-                                      cudaStream_t s);
+cudaError_t run_down_scale_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
+                                      uint8_t* q, float* scales, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
