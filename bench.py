@@ -72,6 +72,8 @@ def kernel_work(wl, P, dW_bytes=2):
         "gate_up_swiglu_e4m3": (4 * P * d * n, T * d + 4 * T + 2 * E * n * d + 8 * E * n + 10 * P * n),
         "quantize_e4m3": (0, 3 * T * d + 4 * T),
         "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
+        "down_scale_e4m3": (2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
+        "quantize_a_e4m3": (0, 3 * P * n + 4 * P),
         "combine": (0, 2 * P * d + 2 * T * d),
         "gather_rows": (0, 4 * T * d + 4 * P * d),
         "zero_tail": (0, 0),
@@ -130,7 +132,7 @@ _GEMM_LABELS = {
     (1, 1, 0, 1): "gate_up_swiglu", (0, 0, 0, 2): "down_scale", (0, 3, 2, 0): "router_logits",
     (0, 2, 0, 3): "dact_dswiglu", (0, 2, 0, 0): "dx_gemm", (2, 3, 1, 0): "dw_tiled (gate/up, down)",
     (2, 3, 2, 0): "dwr_gemm", (2, 4, 1, 0): "dw_gather_b", (3, 3, 1, 0): "dw_gather_a",
-    (1, 1, 0, 4): "gate_up_swiglu_e4m3",
+    (1, 1, 0, 4): "gate_up_swiglu_e4m3", (0, 0, 0, 5): "down_scale_e4m3",
 }
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
@@ -380,6 +382,10 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
     runs = {"bf16": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf),
             "e4m3": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8)}
+    w8d = None
+    if wl.n % 128 == 0:  # the e4m3 down projection as well
+        w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down)
+        runs["e4m3_down8"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
     out = {}
     for name, fn in runs.items():
         for _ in range(warmup):
@@ -407,8 +413,18 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
     t8, t16 = gu8[0] / gu8[1], gu16[0] / gu16[1]
     q = out["e4m3"][1].get("quantize_e4m3", (0.0, 1))
     peak8 = 2 * pk["bf16"]
-    del b8, w8
-    return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
+    full = {}
+    if "e4m3_down8" in out:
+        pr = out["e4m3_down8"][1]
+        dn = pr["down_scale_e4m3"]
+        dn16 = out["bf16"][1]["down_scale"]
+        qa = pr.get("quantize_a_e4m3", (0.0, 1))
+        fl_dn = 2 * P * wl.d * wl.n
+        full = {"forward_e4m3_down_ms": out["e4m3_down8"][0], "down_ms": dn[0] / dn[1],
+                "bf16_down_ms": dn16[0] / dn16[1], "quantize_a_ms": qa[0] / max(qa[1], 1),
+                "down_tflops": fl_dn / (dn[0] / dn[1] * 1e-3) / 1e12}
+    del b8, w8, w8d
+    return {**full, "forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
             "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": q[0] / max(q[1], 1),
             "gate_up_tflops": fl / (t8 * 1e-3) / 1e12, "bf16_gate_up_tflops": fl / (t16 * 1e-3) / 1e12,
             "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
