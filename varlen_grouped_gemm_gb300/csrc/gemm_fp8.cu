@@ -20,13 +20,43 @@ cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const M
 // Down projection with e4m3 operands (A rows and W_down rows quantized per row); the epilogue multiplies
 // by the A row's scale, the output channel's scale and the combine weight.
 cudaError_t run_down_scale_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
+  // 8 epilogue warps: with half as many stages per tile as the bf16 form the epilogue sets the pace
+  // (4 warps: 91 us at c2, 8: 67 us)
+  if (BN == 256) return launch_grouped_gemm<256, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
   return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
 }
 
 // Per-row e4m3 quantization: s = max|row| / 448 (1 for a zero row), codes = e4m3(x / s), the division
-// in fp32 and the conversion rounding to nearest even and saturating at +-448.  One warp per row,
-// 8 elements (16 bytes) per lane and step; the second pass re-reads the row from L1/L2.
+// in fp32 and the conversion rounding to nearest even and saturating at +-448.  One warp per row, 8
+// elements (16 bytes) per lane and step.  Rows of up to 32 x 8 x VR columns stay in registers between the
+// two passes; longer rows (VR = 0) are read twice (the second time from L1/L2).
+__device__ __forceinline__ uint2 e4m3x8(const uint4 x, float s) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+  uint32_t w[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float2 a = __bfloat1622float2(h[2 * j]);
+    const float2 b = __bfloat1622float2(h[2 * j + 1]);
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)), __NV_SATFINITE, __NV_E4M3);
+    w[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ float amax8(const uint4 x, float m) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __bfloat1622float2(h[j]);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
+template <int VR>
 __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ M, long long rows,
                                                                  const int32_t* __restrict__ rows_limit, int cols,
                                                                  uint8_t* __restrict__ q,
@@ -35,37 +65,33 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const __nv_bflo
   const int lane = threadIdx.x & 31;
   if (r >= rows || (rows_limit && r >= __ldg(rows_limit))) return;
   const uint4* src = reinterpret_cast<const uint4*>(M + r * cols);
+  uint2* dst = reinterpret_cast<uint2*>(q + r * cols);
   const int vecs = cols / 8;
   float amax = 0.0f;
-  for (int v = lane; v < vecs; v += 32) {
-    const uint4 x = __ldg(src + v);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+  uint4 x[VR > 0 ? VR : 1];
+  if (VR > 0) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(h[j]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int i = 0; i < VR; ++i) {
+      const int v = lane + 32 * i;
+      x[i] = v < vecs ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int i = 0; i < VR; ++i) amax = amax8(x[i], amax);
+  } else {
+    for (int v = lane; v < vecs; v += 32) amax = amax8(__ldg(src + v), amax);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (lane == 0) scales[r] = s;
-  uint2* dst = reinterpret_cast<uint2*>(q + r * cols);
-  for (int v = lane; v < vecs; v += 32) {
-    const uint4 x = __ldg(src + v);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-    uint32_t w[2];
+  if (VR > 0) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float2 a = __bfloat1622float2(h[2 * j]);
-      const float2 b = __bfloat1622float2(h[2 * j + 1]);
-      const __nv_fp8x2_storage_t lo =
-          __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s)), __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi =
-          __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s)), __NV_SATFINITE, __NV_E4M3);
-      w[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    for (int i = 0; i < VR; ++i) {
+      const int v = lane + 32 * i;
+      if (v < vecs) dst[v] = e4m3x8(x[i], s);
     }
-    dst[v] = make_uint2(w[0], w[1]);
+  } else {
+    for (int v = lane; v < vecs; v += 32) dst[v] = e4m3x8(__ldg(src + v), s);
   }
 }
 
@@ -74,7 +100,12 @@ cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, co
                                       uint8_t* q, float* scales, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;
-  quantize_rows_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (cols <= 256) quantize_rows_e4m3_kernel<1><<<g, 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
+  else if (cols <= 512) quantize_rows_e4m3_kernel<2><<<g, 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
+  else if (cols <= 1024) quantize_rows_e4m3_kernel<4><<<g, 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
+  else if (cols <= 2048) quantize_rows_e4m3_kernel<8><<<g, 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
+  else quantize_rows_e4m3_kernel<0><<<g, 256, 0, s>>>(M, rows, rows_limit, cols, q, scales);
   return cudaGetLastError();
 }
 
