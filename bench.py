@@ -338,6 +338,26 @@ def oracle_sample(wl, budget_s: float, max_experts: int | None = None):
                 host_cpus=os.cpu_count())
 
 
+# ------------------------------------------------------------------------ replicas (N > 1)
+# One process per GPU, each a full replica of the layer on its own batch (no data-path collective):
+# the job's time is the slowest rank's and its throughput all ranks' work over that time.
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, ms_per_step: float) -> float:
+    """Units per second of the whole job: every rank processed units_per_rank in the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -508,15 +528,11 @@ def run_ours(args, rank, world, local_rank):
     rc, code = vgg.moe_get_error(ctx)
     if rc != 0:
         raise RuntimeError(f"device error in timed region: status {rc}, code {code}")
-    total_ms = float(sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
     ms = total_ms / args.steps
     flops = wl.flops_fwd_bwd(P)
-    tflops = world * flops / (ms * 1e-3) / 1e12
-    tokens_s = world * wl.T / (ms * 1e-3)
+    tflops = whole_job_rate(world, flops, ms) / 1e12
+    tokens_s = whole_job_rate(world, wl.T, ms)
 
     # dominant kernel and its roofline: the binding resource of its algorithmic work
     work = kernel_work(wl, P)
@@ -570,13 +586,8 @@ def run_ours(args, rank, world, local_rank):
             dX_pin.copy_(buf.dX, non_blocking=True)
             ee[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = float(sum(a.elapsed_time(b) for a, b in ee))
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e_ms /= args.steps
-        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+        e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in ee)), dist, dev) / args.steps
+        e2e = {"value": whole_job_rate(world, flops, e_ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": 2 * 2 * wl.T * wl.d, "d2h_bytes_per_step": 2 * 2 * wl.T * wl.d}
 
     e4m3 = None
