@@ -401,11 +401,15 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
     runs = {"bf16": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf),
-            "e4m3": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8)}
+            "e4m3": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8),
+            # forward only (inference): H and U, kept for the backward, are not written
+            "bf16_infer": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf, cache=False),
+            "e4m3_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8, cache=False)}
     w8d = None
     if wl.n % 128 == 0:  # the e4m3 down projection as well
         w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down)
         runs["e4m3_down8"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
+        runs["e4m3_down8_infer"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False)
     out = {}
     for name, fn in runs.items():
         for _ in range(warmup):
@@ -443,8 +447,11 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
         full = {"forward_e4m3_down_ms": out["e4m3_down8"][0], "down_ms": dn[0] / dn[1],
                 "bf16_down_ms": dn16[0] / dn16[1], "quantize_a_ms": qa[0] / max(qa[1], 1),
                 "down_tflops": fl_dn / (dn[0] / dn[1] * 1e-3) / 1e12}
+    infer = {"bf16_forward_infer_ms": out["bf16_infer"][0], "forward_infer_ms": out["e4m3_infer"][0]}
+    if "e4m3_down8_infer" in out:
+        infer["forward_e4m3_down_infer_ms"] = out["e4m3_down8_infer"][0]
     del b8, w8, w8d
-    return {**full, "forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
+    return {**full, **infer, "forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
             "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": q[0] / max(q[1], 1),
             "gate_up_tflops": fl / (t8 * 1e-3) / 1e12, "bf16_gate_up_tflops": fl / (t16 * 1e-3) / 1e12,
             "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,

@@ -189,7 +189,8 @@ int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const float* topk
  *   H[j] = X[t] W_gate[e]^T,  U[j] = X[t] W_up[e]^T,  A[j] = silu(H[j]) * U[j]
  *   Yw[j] = sorted_w[j] * (A[j] W_down[e]^T)
  *
- * H and U are kept in fp32 (the backward's dSwiGLU reads them); A is computed
+ * H and U are kept in fp32 (the backward's dSwiGLU reads them; both may be NULL for a
+ * forward-only call, which then writes neither); A is computed
  * from the fp32 accumulators and rounded once to bf16, the operand type of the
  * down projection.  Outputs H, U [cap,n] fp32, A [cap,n] bf16, Yw [cap,d] bf16.
  */
@@ -237,8 +238,9 @@ int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols
  *
  * Code products are accumulated in fp32 on the tensor cores (kind::f8f6f4).  A slot with
  * sorted_tok = -1 (capacity dispatch) gives zero rows.  Requires d % 128 == 0 (and n % 128 == 0 for
- * the e4m3 down projection) besides moe_grouped_gemm_fwd's shape rules; outputs H, U, A, Yw and
- * ownership as moe_grouped_gemm_fwd; no workspace.  MOE_ERR_INVALID_ARG on a violated rule.
+ * the e4m3 down projection) besides moe_grouped_gemm_fwd's shape rules; outputs H, U (both may be
+ * NULL: forward only), A, Yw and ownership as moe_grouped_gemm_fwd; no workspace.
+ * MOE_ERR_INVALID_ARG on a violated rule.
  */
 int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale, const void* Wg_q,
                               const float* wg_scale, const void* Wu_q, const float* wu_scale, const void* W_down,

@@ -176,3 +176,23 @@ def test_e4m3_fullsize_c2(ctx):
         del buf, dev, w8
         gc.collect()
         torch.cuda.empty_cache()
+
+
+def test_e4m3_forward_only(ctx):
+    """cache=False with the e4m3 down projection: the same O bit for bit, H and U left untouched."""
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.scaled(synth.WORKLOADS["c2"], name="c2_small_n256", T=512, d=256, E=16, n=256, K=4)
+    inp = Inputs(wl, with_grad=False)
+    dv = inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=False, e4m3=True)
+    w8 = vgg.E4m3Weights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"])
+    vgg.forward_e4m3(ctx, dv["X"], dv["W_r"], dv["bias"], w8, None, buf)
+    O_cached = buf.O.clone()
+    buf.H.fill_(7.0)
+    buf.U.fill_(7.0)
+    buf.O.zero_()
+    vgg.forward_e4m3(ctx, dv["X"], dv["W_r"], dv["bias"], w8, None, buf, cache=False)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    assert torch.equal(buf.O, O_cached)
+    assert bool((buf.H == 7.0).all()) and bool((buf.U == 7.0).all())

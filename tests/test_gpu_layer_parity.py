@@ -63,3 +63,22 @@ def test_deterministic(ctx):
     b = run_path(ctx, inp, backward=True)
     for name in ("O", "dX", "dW_gate", "dW_up", "dW_down", "dS", "dlogits", "dW_r", "sorted_tok", "tok_pairs"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_forward_only_skips_the_backward_cache(ctx):
+    """cache=False (H = U = NULL at the C ABI): the same O bit for bit, and H, U left untouched."""
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.scaled(synth.WORKLOADS["c2"], name="c2_fwd_only", T=512, d=256, E=16, n=192, K=4)
+    inp = Inputs(wl, with_grad=False)
+    dv = inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=False)
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    O_cached = buf.O.clone()
+    buf.H.fill_(7.0)
+    buf.U.fill_(7.0)
+    buf.O.zero_()
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf, cache=False)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    assert torch.equal(buf.O, O_cached)
+    assert bool((buf.H == 7.0).all()) and bool((buf.U == 7.0).all())

@@ -402,8 +402,9 @@ class Buffers:
             aq=z((cap, n), torch.uint8) if e4m3 else None, as_=z((cap,), f32) if e4m3 else None)
 
 
-def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
-    """Routing, grouping, grouped GEMMs and combine; the output is ``buf.O``."""
+def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, cache=True):
+    """Routing, grouping, grouped GEMMs and combine; the output is ``buf.O``.  ``cache=False``: forward only,
+    the pre-activations H, U the backward needs are not written."""
     moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
     if buf.capacity:
         moe_permute_capacity(ctx, buf.topk_ids, buf.topk_w, buf.E, buf.capacity, buf.drop_policy, buf.counts,
@@ -412,8 +413,8 @@ def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None):
     else:
         moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts,
                     buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
-    moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w, buf.H, buf.U,
-                         buf.A, buf.Yw, buf.ws, stream)
+    moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w,
+                         buf.H if cache else None, buf.U if cache else None, buf.A, buf.Yw, buf.ws, stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 
@@ -446,10 +447,11 @@ class E4m3Weights:
         return w
 
 
-def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, stream=None):
+def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, stream=None, cache=True):
     """The forward with the gate/up GEMM on e4m3 operands (``buf`` allocated with ``e4m3=True``): routing and
     grouping as ``forward``, X quantized per token, then the e4m3 grouped GEMMs and the combine.  When ``w8``
-    holds W_down's codes the down projection runs on e4m3 operands too (``W_down`` may then be None)."""
+    holds W_down's codes the down projection runs on e4m3 operands too (``W_down`` may then be None).
+    ``cache=False``: forward only (H, U not written)."""
     if buf.xq is None:
         raise ValueError("buffers were allocated without e4m3=True")
     moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
@@ -463,7 +465,8 @@ def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, strea
     moe_quantize_rows_e4m3(ctx, X, buf.xq, buf.xs, stream)
     moe_grouped_gemm_fwd_e4m3(ctx, buf.xq, buf.xs, w8.Wg_q, w8.wg_scale, w8.Wu_q, w8.wu_scale,
                               None if w8.Wd_q is not None else W_down, buf.offsets, buf.sorted_tok, buf.sorted_w,
-                              buf.H, buf.U, buf.A, buf.Yw, Wd_q=w8.Wd_q, wd_scale=w8.wd_scale,
+                              buf.H if cache else None, buf.U if cache else None, buf.A, buf.Yw, Wd_q=w8.Wd_q,
+                              wd_scale=w8.wd_scale,
                               Aq=buf.aq if w8.Wd_q is not None else None,
                               a_scale=buf.as_ if w8.Wd_q is not None else None, stream=stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)

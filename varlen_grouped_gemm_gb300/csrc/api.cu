@@ -483,7 +483,8 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
   (void)ws;
   (void)ws_bytes;
-  VGG_REQUIRE(ctx && X && W_gate && W_up && W_down && offsets && sorted_tok && sorted_w && H && U && A && Yw);
+  VGG_REQUIRE(ctx && X && W_gate && W_up && W_down && offsets && sorted_tok && sorted_w && A && Yw);
+  VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
   VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
   VGG_REQUIRE(aligned16(X) && aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(H) &&
@@ -509,9 +510,9 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     p.ld_out = n;
     const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
-    if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) ||
-        !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) || !make_store_map_2d(&m.o0, H, true, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o1, U, true, n, cap, n, 32) || !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
+    if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) || !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) ||
+        (H && (!make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32))) ||
+        !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
     // pairs of CTAs on neighbouring column tiles share the gathered X rows (each gathers half)
@@ -540,7 +541,8 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
                               const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w, void* H,
                               void* U, void* A, void* Aq, float* a_scale, void* Yw, moe_stream_t stream) {
   VGG_REQUIRE(ctx && Xq && x_scale && Wg_q && wg_scale && Wu_q && wu_scale && offsets && sorted_tok && sorted_w &&
-              H && U && A && Yw);
+              A && Yw);
+  VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
   VGG_REQUIRE(shapes_ok(T, d, E, n, 1) && d % 128 == 0);
   // the down projection: bf16 (W_down) or e4m3 (Wd_q, wd_scale with the Aq, a_scale buffers)
   const bool down8 = Wd_q != nullptr;
@@ -576,7 +578,7 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
     const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
     if (!make_map_3d(&m.b0, Wg_q, dk, n, E, BN / 2) || !make_map_3d(&m.b1, Wu_q, dk, n, E, BN / 2) ||
-        !make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32) ||
+        (H && (!make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32))) ||
         !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);

@@ -969,8 +969,10 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
                 u[i] *= sx * __shfl_sync(0xffffffffu, ul, i);
               }
             }
-            emit32(o0, h, col, ncols, full, row_ok, true);  // H, U stay fp32 for the backward
-            emit32(o1, u, col, ncols, full, row_ok, true);
+            if (p.out0) {  // H, U stay fp32 for the backward; a forward-only call passes neither
+              emit32(o0, h, col, ncols, full, row_ok, true);
+              emit32(o1, u, col, ncols, full, row_ok, true);
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = h[i] * sigmoidf_(h[i]) * u[i];  // A, in place of h
             emit32(o2, h, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
