@@ -82,6 +82,8 @@ DOWN8_CASES = [
     synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
     synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias_n256", T=512, d=256, E=16, n=256, K=4, bias="normal"),
     synth.scaled(synth.WORKLOADS["c4"], name="c4_small_zipf_n384", T=640, d=384, E=32, n=384, K=4),
+    # 512 experts: the group table leaves no room for a fourth stage (the three-stage form)
+    synth.scaled(synth.WORKLOADS["c5_plain"], name="c5_small_e512", T=2048, d=256, E=512, n=128, K=8),
 ]
 
 

@@ -21,8 +21,10 @@ cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const M
 // by the A row's scale, the output channel's scale and the combine weight.
 cudaError_t run_down_scale_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   // 8 epilogue warps: with half as many stages per tile as the bf16 form the epilogue sets the pace
-  // (4 warps: 91 us at c2, 8: 67 us)
-  if (BN == 256) return launch_grouped_gemm<256, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
+  // (4 warps: 91 us at c2, 8: 67 us); three stages when the group table leaves no room for four
+  if (BN == 256 && SmemLayout<256, 4, 8, 1>::bytes(p.groups, VAR_M) <= kMaxSmem)
+    return launch_grouped_gemm<256, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 3, 8, 2, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
   return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE_Q, false>(p, m, grid, s);
 }
 
