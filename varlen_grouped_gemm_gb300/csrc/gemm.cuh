@@ -1,6 +1,7 @@
 // Persistent grouped GEMM for sm_103a on the 5th-generation tensor cores.
 //
-//   D[128 x BN] (+)= A[128 x K] * B[K x BN]    bf16 operands, fp32 accumulation in TMEM
+//   D[128 x BN] (+)= A[128 x K] * B[K x BN]    bf16 operands (kind::f16) or, for the e4m3 epilogues,
+//                                              e4m3 operands (kind::f8f6f4); fp32 accumulation in TMEM
 //
 // One CTA per SM walks a static round-robin list of output tiles.  Warp roles:
 //   warps 0..EW-1  epilogue (4 or 8): tcgen05.ld of the accumulator (row i of the tile = TMEM
@@ -10,26 +11,28 @@
 //              issued by one thread complete one after another, so the ring's stages are dealt
 //              round-robin to up to 4 producer threads (this one and extra warps placed last);
 //   warp  EW+1 UMMA issuer (lane 0);
-//   warps EW+2..EW+5  present when an operand's rows are gathered through a token index: they
-//              copy those rows with cp.async (16 B per thread, zero-filled past the end)
-//              straight into the swizzled stage, so the permuted activations are never
-//              written ([SM] "4.1 Gather 융합"); the index lookups run two stages ahead;
+//   gather warps (8 for a gathered K-major A, else 4) present when an operand's rows are gathered
+//              through a token index: they copy those rows with cp.async (16 B per thread,
+//              zero-filled past the end) straight into the swizzled stage, so the permuted
+//              activations are never written ([SM] "4.1 Gather 융합"); the index lookups run two
+//              stages ahead;
 //   relay warp present with clusters of CN CTAs on neighbouring column tiles of one row tile:
 //              each CTA gathers 128/CN of the rows and the relay copies its slice into the
 //              peers' shared memory (distributed shared memory), so the gathered activations
 //              are read from L2 once per cluster instead of once per CTA.
-// Shared memory holds STAGES ring slots of A (128 x 64) and B (BN x 64) in the
-// 128-byte-swizzled layout that TMA writes and the UMMA descriptors read.  TMEM
-// holds two BN-column accumulators so that the epilogue of tile i overlaps the
-// main loop of tile i+1 ([SM] "4.3 MMA ↔ IO 오버랩": TMEM split in two halves,
-// one accumulating while the other drains).
+// Shared memory holds STAGES ring slots of A (128 rows x 128 bytes) and B (BN rows x 128 bytes: 64
+// bf16 or 128 e4m3 values of K) in the 128-byte-swizzled layout that TMA writes and the UMMA
+// descriptors read.  TMEM holds two BN-column accumulators so that the epilogue of tile i overlaps
+// the main loop of tile i+1 ([SM] "4.3 MMA ↔ IO 오버랩": TMEM split in two halves, one accumulating
+// while the other drains).
 //
 // Grouping ("varlen") modes:
 //   VAR_M    groups = experts, rows of group g are sorted rows [off[g], off[g+1]);
 //            K and N fixed ([GG] "Variable-M batched matmul").
 //   VAR_K    groups = experts, the reduction runs over the group's rows; M and N
-//            fixed; rows past the group's end enter as zeros through the gathered
-//            operand's out-of-range fill; an empty group writes zeros ([SM] "4 기여 ②").
+//            fixed; rows past the group's end enter as zeros (the gathered operand's
+//            out-of-range fill, or cleared in shared memory when both operands are tiled);
+//            an empty group writes zeros ([SM] "4 기여 ②").
 //   VAR_NONE one dense problem, K optionally split across CTAs (partials per split).
 #pragma once
 
