@@ -405,11 +405,10 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
             # forward only (inference): H and U, kept for the backward, are not written
             "bf16_infer": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf, cache=False),
             "e4m3_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8, cache=False)}
-    w8d = None
-    if wl.n % 128 == 0:  # the e4m3 down projection as well
-        w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down)
-        runs["e4m3_down8"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
-        runs["e4m3_down8_infer"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False)
+    # the e4m3 down projection as well
+    w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down)
+    runs["e4m3_down8"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
+    runs["e4m3_down8_infer"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False)
     out = {}
     for name, fn in runs.items():
         for _ in range(warmup):
@@ -642,7 +641,7 @@ def run_ours(args, rank, world, local_rank):
                "serial_value": whole_job_rate(world, flops, serial_ms) / 1e12}
 
     e4m3 = None
-    if not args.no_e4m3 and wl.d % 128 == 0:
+    if not args.no_e4m3:
         e4m3 = measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, stream,
                             max(3, min(args.steps, 20)), max(3, args.warmup), pk)
 

@@ -237,8 +237,8 @@ int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols
  *   Yw[j,c] = sorted_w[j] * a_scale[j] * wd_scale[e,c] * sum_i e4m3(Aq[j,i]) e4m3(Wd_q[e,c,i])
  *
  * Code products are accumulated in fp32 on the tensor cores (kind::f8f6f4).  A slot with
- * sorted_tok = -1 (capacity dispatch) gives zero rows.  Requires d % 128 == 0 (and n % 128 == 0 for
- * the e4m3 down projection) besides moe_grouped_gemm_fwd's shape rules; outputs H, U (both may be
+ * sorted_tok = -1 (capacity dispatch) gives zero rows.  Shape rules as moe_grouped_gemm_fwd (d and n
+ * multiples of 64: a last stage of 128 codes may be half past K and reads zeros there); outputs H, U (both may be
  * NULL: forward only), A, Yw and ownership as moe_grouped_gemm_fwd; no workspace.
  * MOE_ERR_INVALID_ARG on a violated rule.
  */

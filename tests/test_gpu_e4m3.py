@@ -60,6 +60,8 @@ def test_quantize_rows_bit_exact(ctx):
 CASES = [
     synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=512, d=256, E=16, n=192, K=4),
     synth.scaled(synth.WORKLOADS["c4"], name="c4_small", T=640, d=384, E=32, n=320, K=4),
+    # d = 320: the last K stage holds 64 of its 128 codes (zeros past K)
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small_d320", T=640, d=320, E=32, n=320, K=4),
     synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
     # capacity factor 1 under a skewed load: some experts drop pairs, others leave slots empty
     synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias", T=512, d=256, E=16, n=192, K=4, bias="normal"),
@@ -84,6 +86,8 @@ DOWN8_CASES = [
     synth.scaled(synth.WORKLOADS["c4"], name="c4_small_zipf_n384", T=640, d=384, E=32, n=384, K=4),
     # 512 experts: the group table leaves no room for a fourth stage (the three-stage form)
     synth.scaled(synth.WORKLOADS["c5_plain"], name="c5_small_e512", T=2048, d=256, E=512, n=128, K=8),
+    # d = n = 320: both e4m3 GEMMs end on a half stage
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small_320", T=640, d=320, E=32, n=320, K=4),
 ]
 
 

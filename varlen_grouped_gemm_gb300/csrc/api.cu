@@ -543,10 +543,10 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
   VGG_REQUIRE(ctx && Xq && x_scale && Wg_q && wg_scale && Wu_q && wu_scale && offsets && sorted_tok && sorted_w &&
               A && Yw);
   VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
-  VGG_REQUIRE(shapes_ok(T, d, E, n, 1) && d % 128 == 0);
+  VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
   // the down projection: bf16 (W_down) or e4m3 (Wd_q, wd_scale with the Aq, a_scale buffers)
   const bool down8 = Wd_q != nullptr;
-  VGG_REQUIRE(down8 ? (wd_scale && Aq && a_scale && n % 128 == 0 && aligned16(Wd_q) && aligned16(Aq)) : W_down != nullptr);
+  VGG_REQUIRE(down8 ? (wd_scale && Aq && a_scale && aligned16(Wd_q) && aligned16(Aq)) : W_down != nullptr);
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
   VGG_REQUIRE(aligned16(Xq) && aligned16(Wg_q) && aligned16(Wu_q) && aligned16(W_down) && aligned16(H) &&
               aligned16(U) && aligned16(A) && aligned16(Yw));

@@ -664,10 +664,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       const uint32_t sb = sa + L::kABytes;
       if (AMODE == A_GATHER_K) {
         const int kc = q0.tl.k_begin + q0.ks * BK + c16 * 8;
+        const bool k_in = kc < p.K;  // a last stage past K (K a multiple of 8 units) reads zeros
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           const long long row = r0[i];
-          bool ok = row >= 0;
+          bool ok = row >= 0 && k_in;
           if (ok && row >= p.a_rows) {
             set_error(p.err, DERR_BAD_OFFSETS);
             ok = false;
