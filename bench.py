@@ -493,21 +493,22 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def eager_step():
         vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
 
     for _ in range(args.warmup):
-        step()
+        eager_step()
     rc, code = vgg.moe_get_error(ctx)
     if rc != 0:
         raise RuntimeError(f"device error after warm-up: status {rc}, code {code}")
     P = int(buf.P.item())
     counts = buf.counts.cpu().numpy()
+    # the step as a CUDA graph (the library's host work done once, at capture), unless --no-graph
+    graph = None if args.no_graph else vgg.StepGraph(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+    step = graph.replay if graph is not None else eager_step
 
     # timed region: K steps, per-step events, L2 flushed between steps outside the events
     clocks = ClockSampler(local_rank)
-    vgg.moe_profile_enable(ctx, True)
-    vgg.moe_profile_read(ctx)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     # clock samples: a 0.5 s busy pre-roll of the same step right before the timed region, and the region
     clocks.start()
@@ -515,7 +516,6 @@ def run_ours(args, rank, world, local_rank):
     while time.perf_counter() < t_end:
         step()
         torch.cuda.synchronize()
-    vgg.moe_profile_read(ctx)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -529,11 +529,18 @@ def run_ours(args, rank, world, local_rank):
     if dist is not None:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    prof = vgg.moe_profile_read(ctx)
-    vgg.moe_profile_enable(ctx, False)
     rc, code = vgg.moe_get_error(ctx)
     if rc != 0:
         raise RuntimeError(f"device error in timed region: status {rc}, code {code}")
+    # per-kernel times: the same K steps again, eager, with the library's per-launch events
+    vgg.moe_profile_enable(ctx, True)
+    vgg.moe_profile_read(ctx)
+    for i in range(args.steps):
+        flush.zero_()
+        eager_step()
+    torch.cuda.synchronize()
+    prof = vgg.moe_profile_read(ctx)
+    vgg.moe_profile_enable(ctx, False)
     total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
     ms = total_ms / args.steps
     flops = wl.flops_fwd_bwd(P)
@@ -607,6 +614,12 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(2):  # warm-up of the second buffer set
             vgg.forward_backward(ctx, slots[1][0], W_r, bias, W_gate, W_up, W_down, slots[1][1], buf2, stream)
         torch.cuda.synchronize()
+        if graph is not None:
+            graph2 = vgg.StepGraph(ctx, slots[1][0], W_r, bias, W_gate, W_up, W_down, slots[1][1], buf2)
+            runs = [graph.replay, graph2.replay]
+        else:
+            runs = [lambda i=i: vgg.forward_backward(ctx, slots[i][0], W_r, bias, W_gate, W_up, W_down, slots[i][1],
+                                                     slots[i][2], stream) for i in range(2)]
         if dist is not None:
             dist.barrier()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -618,7 +631,7 @@ def run_ours(args, rank, world, local_rank):
         for i in range(args.steps):
             Xi, dOi, bi = slots[i % 2]
             stream.wait_event(h2d[i % 2])
-            vgg.forward_backward(ctx, Xi, W_r, bias, W_gate, W_up, W_down, dOi, bi, stream)
+            runs[i % 2]()
             done[i % 2].record(stream)
             with torch.cuda.stream(cs):
                 if i + 1 < args.steps:
@@ -632,7 +645,7 @@ def run_ours(args, rank, world, local_rank):
         t1.record(cs)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(t0.elapsed_time(t1), dist, dev) / args.steps
-        del buf2, slots
+        del buf2, slots, runs
         e2e = {"value": whole_job_rate(world, flops, e_ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": 2 * 2 * wl.T * wl.d, "d2h_bytes_per_step": 2 * 2 * wl.T * wl.d,
                "mode": "pipelined: step i+1's H2D and step i's D2H on a copy stream during step i "
@@ -663,6 +676,7 @@ def run_ours(args, rank, world, local_rank):
                        "empty_experts": int((counts == 0).sum()),
                        "max_rows_per_expert": int(counts.max()), "dW_dtype": "bf16",
                        "l2": "flushed between steps (256 MB write, outside the per-step events)",
+                       "launch": "eager calls" if graph is None else "the step's 18 launches as one CUDA graph",
                        "clock_samples": "nvidia-smi every 50 ms over a 0.5 s busy pre-roll of the same step and the timed region",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tokens_per_s": tokens_s, "pct_of_peak_bf16": 100 * tflops / world / pk["bf16_sus"],
@@ -689,15 +703,18 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e4m3", action="store_true", help="skip the e4m3 gate/up forward measurement")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of the captured step graph")
     ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
     ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
     ap.add_argument("--profile-run", action="store_true",
-                    help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline, no e4m3 forward")
+                    help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline, no e4m3 forward, "
+                         "eager launches")
     args = ap.parse_args()
     if args.profile_run:
         args.no_e2e = True
         args.no_cpu_baseline = True
         args.no_e4m3 = True
+        args.no_graph = True
     if args.ncu_summary:
         print(ncu_launch_summary(args.ncu_summary))
         return 0

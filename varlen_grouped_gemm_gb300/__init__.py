@@ -478,6 +478,33 @@ def backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf: Buffers, stream=None):
                  buf.dW_up, buf.dW_down, buf.dS, buf.dlogits, buf.dW_r, buf.ws, stream)
 
 
+class StepGraph:
+    """One forward + backward (``backward=False``: the forward) captured as a CUDA graph for fixed tensors and
+    buffers.  The library's host work (argument checks, tensor-map encoding, launch configuration) runs once, at
+    capture; ``replay()`` launches the whole step at once on the current stream.  New inputs are copied into the
+    captured tensors (same addresses) before a replay; outputs land in ``buf`` as with the eager calls."""
+
+    def __init__(self, ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf: Buffers, backward=True):
+        def run():
+            if backward:
+                forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+            else:
+                forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf)
+        side = torch.cuda.Stream(device=X.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # one eager pass outside the capture (first-use configuration)
+            run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize(X.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            run()
+        torch.cuda.synchronize(X.device)
+
+    def replay(self):
+        self.graph.replay()
+
+
 def forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf: Buffers, stream=None):
     forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf, stream)
     backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf, stream)
