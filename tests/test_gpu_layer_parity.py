@@ -82,3 +82,26 @@ def test_forward_only_skips_the_backward_cache(ctx):
     assert rc == vgg.MOE_OK and code == 0, (rc, code)
     assert torch.equal(buf.O, O_cached)
     assert bool((buf.H == 7.0).all()) and bool((buf.U == 7.0).all())
+
+
+def test_step_graph_replays_the_eager_step(ctx):
+    """StepGraph: a captured forward + backward replays to the eager results, also after new inputs were
+    copied into the captured tensors."""
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.scaled(synth.WORKLOADS["c2"], name="c2_graph", T=512, d=256, E=16, n=192, K=4)
+    inp = Inputs(wl)
+    dv = inp.dev
+    X, dO = dv["X"].clone(), dv["dO"].clone()
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=True)
+    g = vgg.StepGraph(ctx, X, dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], dO, buf)
+    X.copy_(dv["X"].flip(0))  # other tokens in the same tensor
+    dO.copy_(dv["dO"] * 0.5)
+    g.replay()
+    torch.cuda.synchronize()
+    got = {k: getattr(buf, k).clone() for k in ("O", "dX", "dW_gate", "dW_up", "dW_down", "dW_r", "dlogits")}
+    ref = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=True)
+    vgg.forward_backward(ctx, X, dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], dO, ref)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    for k, v in got.items():
+        assert torch.equal(v, getattr(ref, k)), k
