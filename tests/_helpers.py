@@ -87,8 +87,9 @@ def oracle_layer(inp: Inputs, g=None, backward=True):
     return O, cache, grads
 
 
-def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None):
-    """Element-wise comparison of every float output with the fp64 oracle (max/mean metric)."""
+def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None, refs=None):
+    """Element-wise comparison of every float output with the fp64 oracle (max/mean metric).  ``refs`` may
+    replace the reference of a weight gradient (by name)."""
     rep = {} if report is None else report
     rep["O"] = oracle.compare("O", dev_to_f64(buf.O), O_ref)
     if grads is None:
@@ -98,7 +99,7 @@ def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None):
     rep["dX"] = oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])
     for name, key in (("dW_gate", "dW_gate"), ("dW_up", "dW_up"), ("dW_down", "dW_down")):
         got = dev_to_f64(getattr(buf, name))
-        ref = np.stack([grads[key][e] for e in range(E)])
+        ref = refs[name] if refs and name in refs else np.stack([grads[key][e] for e in range(E)])
         rep[name] = oracle.compare(name, got, ref, param_axes=oracle.WEIGHT_GRAD)
         empty = np.nonzero(r.counts == 0)[0]
         assert not np.any(got[empty]), f"{name}: experts without pairs must get exactly zero"
