@@ -361,11 +361,15 @@ def router_grad_rows(member, topk_ids, w_full, dw_full):
     return np.where(member, w_full * dw_full, 0.0) - np.where(topk_mask, w_full * G, 0.0)
 
 
-def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None):
+def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp8_dx: bool = False):
     """Backward of the layer given the forward cache.
 
     Returns dX, dW_gate, dW_up, dW_down (fp64, all experts or the listed ones),
     dw[T,E] (d loss / d combine weight, zero off the pair set), dlogits[T,E], dW_r[d,E].
+
+    With ``fp8_dx`` the expert part of dX takes e4m3 operands: each pair's row [dH | dU] (bf16, the
+    dSwiGLU epilogue's output type, ``round_bf16``) quantized per row, and [W_gate; W_up]^T (d rows of
+    2n) quantized per row (per input channel of the layer), ``quantize_rows_e4m3``.
     """
     X, dO = _f64(X), _f64(dO)
     T, d = X.shape
@@ -385,7 +389,13 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None):
             continue
         g = expert_block_backward(X[rows], dO[rows], w_full[rows, e], W_gate[e], W_up[e], W_down[e])
         dw_full[rows, e] = g["dw"]
-        np.add.at(dX, rows, g["dx"])
+        if fp8_dx:
+            hq, hs = quantize_rows_e4m3(round_bf16(np.concatenate([g["dh"], g["du"]], axis=1)).astype(np.float32))
+            B = np.concatenate([_f64(W_gate[e]), _f64(W_up[e])], axis=0).T  # [d, 2n]
+            bq, bs = quantize_rows_e4m3(B.astype(np.float32))
+            np.add.at(dX, rows, dequantize_rows_e4m3(hq, hs) @ dequantize_rows_e4m3(bq, bs).T)
+        else:
+            np.add.at(dX, rows, g["dx"])
         if e in dWg:
             dWg[e], dWu[e], dWd[e] = g["dWg"], g["dWu"], g["dWd"]
     dL = router_grad_rows(routing.member, routing.topk_ids, w_full, dw_full)

@@ -584,6 +584,44 @@ def test_fp8_down_within_quantization_bound():
     assert 0 < np.max(np.abs(O8 - O8g)) < 0.2 * np.max(np.abs(O8g))
 
 
+def test_fp8_dx_within_quantization_bound():
+    # with e4m3 dX operands, each pair's dX contribution differs from (bf16 [dH|dU]) [W_gate; W_up] by at
+    # most the element-wise quantization bound of the two rows, and does differ; the rest is unchanged
+    rng = np.random.default_rng(17)
+    T, d, E, n, K = 24, 64, 4, 32, 2
+    X = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wu = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wd = (rng.standard_normal((E, d, n)) * 0.1).astype(np.float32)
+    W_r = rng.standard_normal((d, E)) * 0.3
+    dO = rng.standard_normal((T, d)).astype(np.float32)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    g16 = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache)
+    g8 = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache, fp8_dx=True)
+    for k in ("dW_r", "dlogits", "dw"):
+        np.testing.assert_array_equal(g8[k], g16[k])
+    r = cache["routing"]
+    w = cache["w_full"]
+    bound = np.zeros((T, d))
+    for e in range(E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        blk = mo.expert_block_backward(X[rows], dO[rows], w[rows, e], Wg[e], Wu[e], Wd[e])
+        hu = mo.round_bf16(np.concatenate([blk["dh"], blk["du"]], axis=1))
+        _, hs = mo.quantize_rows_e4m3(hu.astype(np.float32))
+        B = np.concatenate([Wg[e], Wu[e]], axis=0).T.astype(np.float64)
+        _, bs = mo.quantize_rows_e4m3(B.astype(np.float32))
+        dh = np.maximum(2.0 ** -4 * np.abs(hu), 2.0 ** -10 * hs.astype(np.float64)[:, None])
+        db = np.maximum(2.0 ** -4 * np.abs(B), 2.0 ** -10 * bs.astype(np.float64)[:, None])
+        bound[rows] += np.abs(hu) @ db.T + dh @ np.abs(B).T + dh @ db.T
+        # reference with the bf16 [dH|dU] rows and exact weights
+        g16["dX"][rows] += hu @ B.T - blk["dx"]
+    err = np.abs(g8["dX"] - g16["dX"])
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-12)
+    assert np.max(err) > 0
+
+
 # ---------------------------------------------------------------- the metric
 
 
