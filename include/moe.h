@@ -286,6 +286,36 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
                  float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_quantize_dx_weights_e4m3 — the B operand of the e4m3 dX GEMM: for every expert e the matrix
+ * [W_gate[e]; W_up[e]]^T (d rows of 2n: row c holds W_gate[e][:, c] then W_up[e][:, c]) quantized
+ * per row as moe_quantize_rows_e4m3 does.  [GG] "한계"; [SM] "4 기여 ②" (the dX GEMM).
+ * W_gate, W_up [E,n,d] bf16; tmp [E,d,2n] bf16 device scratch (caller-owned, overwritten);
+ * outputs Wgu_q [E,d,2n] uint8 codes and wgu_scale [E,d] fp32.  Shape rules as moe_backward;
+ * 16-byte aligned pointers; else MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_dx_weights_e4m3(moe_ctx* ctx, const void* W_gate, const void* W_up, int E, int n, int d, void* tmp,
+                                 void* Wgu_q, float* wgu_scale, moe_stream_t stream);
+
+/*
+ * moe_backward_e4m3 — moe_backward with the dX GEMM on e4m3 operands.
+ * [GG] "한계" (the FP8 grouped GEMM); [SM] "4 기여 ②".  Arguments as moe_backward, plus
+ * Wgu_q / wgu_scale from moe_quantize_dx_weights_e4m3 and the caller-owned buffers HUq [cap, 2n]
+ * (uint8) and hu_scale [cap] (fp32): the rows [dH[j] | dU[j]] below offsets[E] are quantized per
+ * row into them (one scale over both halves), and
+ *
+ *   dXp[j,c] = hu_scale[j] * wgu_scale[e,c] * sum_k e4m3(HUq[j,k]) e4m3(Wgu_q[e,c,k])
+ *
+ * accumulated in fp32 (kind::f8f6f4); everything else as moe_backward (bf16 weight gradients).
+ */
+int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale, int T, int d,
+                      int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids, const float* topk_w,
+                      const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                      const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* HUq,
+                      float* hu_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                      float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Per-kernel timing (tracing).  With profiling enabled, every kernel the
  * library launches is bracketed by a CUDA event pair on its stream (events
  * come from a pool created by the first moe_profile_enable).  moe_profile_read

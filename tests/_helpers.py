@@ -96,7 +96,7 @@ def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None, refs=None)
         return rep
     r: mo.Routing = cache["routing"]
     E = inp.wl.E
-    rep["dX"] = oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])
+    rep["dX"] = oracle.compare("dX", dev_to_f64(buf.dX), refs["dX"] if refs and "dX" in refs else grads["dX"])
     for name, key in (("dW_gate", "dW_gate"), ("dW_up", "dW_up"), ("dW_down", "dW_down")):
         got = dev_to_f64(getattr(buf, name))
         ref = refs[name] if refs and name in refs else np.stack([grads[key][e] for e in range(E)])

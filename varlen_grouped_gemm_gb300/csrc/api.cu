@@ -629,12 +629,15 @@ int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int3
   return MOE_OK;
 }
 
-int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
-                 const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile, long long cap,
-                 const int32_t* topk_ids, const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok,
-                 const float* sorted_w, const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H,
-                 const void* U, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
-                 float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
+// The backward; with Wgu_q the dX GEMM runs on e4m3 operands (moe_backward_e4m3).
+static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                         const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile,
+                         long long cap, const int32_t* topk_ids, const float* topk_w, const int32_t* offsets,
+                         const int32_t* sorted_tok, const float* sorted_w, const int32_t* tok_ptr,
+                         const int32_t* tok_pairs, const void* H, const void* U, void* dX, void* dW_gate,
+                         void* dW_up, void* dW_down, int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws,
+                         size_t ws_bytes, moe_stream_t stream, const void* Wgu_q, const float* wgu_scale, void* HUq,
+                         float* hu_scale) {
   VGG_REQUIRE(ctx && dO && X && W_r && W_gate && W_up && W_down && topk_ids && topk_w && offsets && sorted_tok &&
               sorted_w && tok_ptr && tok_pairs && H && U && dX && dW_gate && dW_up && dW_down && dS && dlogits &&
               dW_r && ws);
@@ -690,7 +693,32 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, m, std::min(tiles, ctx->num_sms), s));
   }
   // dXp = [dH | dU] [W_gate[e]; W_up[e]]
-  {
+  if (Wgu_q) {
+    // e4m3: each pair's row [dH | dU] quantized (the rows below offsets[E]), B = [W_gate; W_up]^T quantized per
+    // row by moe_quantize_dx_weights_e4m3; rows are handed to TMA as 16-bit units (code pairs)
+    VGG_LAUNCH("quantize_hu_e4m3", launch_quantize_rows_pair_e4m3(w.dH, w.dU, cap, offsets + E, n,
+                                                                  static_cast<uint8_t*>(HUq), hu_scale, s));
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = n;  // 2n codes
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.out0 = w.dXp;
+    p.ld_out = d;
+    p.row_scale = hu_scale;
+    p.in1 = wgu_scale;
+    p.ld_in = d;
+    const int BN = gemm_bn(d);
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, HUq, n, cap, n, BM) || !make_map_3d(&m.b0, Wgu_q, n, d, E, BN) ||
+        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("dx_gemm_e4m3", run_dx_store_e4m3(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  } else {
     GemmParams p = base_params(ctx);
     p.N = d;
     p.K = 2 * n;
@@ -794,6 +822,48 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
     const int tiles = E * ceil_div(d, BM) * ceil_div(n, BN);
     VGG_LAUNCH("dw_down", run_dw_tiled(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
   }
+  return MOE_OK;
+}
+
+int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                 const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile, long long cap,
+                 const int32_t* topk_ids, const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok,
+                 const float* sorted_w, const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H,
+                 const void* U, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                 float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
+                       sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
+                       dlogits, dW_r, ws, ws_bytes, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
+                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale, int T, int d,
+                      int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids, const float* topk_w,
+                      const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                      const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* HUq,
+                      float* hu_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                      float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  VGG_REQUIRE(Wgu_q && wgu_scale && HUq && hu_scale && aligned16(Wgu_q) && aligned16(HUq));
+  return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
+                       sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
+                       dlogits, dW_r, ws, ws_bytes, stream, Wgu_q, wgu_scale, HUq, hu_scale);
+}
+
+int moe_quantize_dx_weights_e4m3(moe_ctx* ctx, const void* W_gate, const void* W_up, int E, int n, int d, void* tmp,
+                                 void* Wgu_q, float* wgu_scale, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && W_gate && W_up && tmp && Wgu_q && wgu_scale);
+  VGG_REQUIRE(shapes_ok(1, d, E, n, 1));
+  VGG_REQUIRE(aligned16(W_gate) && aligned16(W_up) && aligned16(tmp) && aligned16(Wgu_q));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16* t = static_cast<__nv_bfloat16*>(tmp);
+  VGG_LAUNCH("quantize_e4m3", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_gate), E, n, d, t, 2 * n,
+                                                         0, s));
+  VGG_LAUNCH("quantize_e4m3", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_up), E, n, d, t, 2 * n, n,
+                                                         s));
+  VGG_LAUNCH("quantize_e4m3", launch_quantize_rows_e4m3(t, static_cast<long long>(E) * d, nullptr, 2 * n,
+                                                        static_cast<uint8_t*>(Wgu_q), wgu_scale, s));
   return MOE_OK;
 }
 

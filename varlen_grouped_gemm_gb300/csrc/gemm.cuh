@@ -53,10 +53,12 @@ constexpr int kPrefetchStages = 4;  // tiled operands are prefetched into L2 thi
 enum AMode { A_TMA_K = 0, A_GATHER_K = 1, A_TMA_MN = 2, A_GATHER_MN = 3 };
 enum BMode { B_TMA_K3 = 0, B_TMA_K3_GU = 1, B_TMA_MN3 = 2, B_TMA_MN2 = 3, B_GATHER_MN = 4 };
 enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
-// EPI_SWIGLU_Q, EPI_SCALE_Q: the SwiGLU and the combine-weight epilogues of the e4m3 form (operands are
-// e4m3 codes of per-row-scaled rows; the accumulator is multiplied by the A row's scale and the
-// output channel's scale first).
-enum EpiKind { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5 };
+// EPI_SWIGLU_Q, EPI_SCALE_Q, EPI_STORE_Q: the SwiGLU, the combine-weight and the plain (varlen-M, bf16)
+// epilogues of the e4m3 form (operands are e4m3 codes of per-row-scaled rows; the accumulator is
+// multiplied by the A row's scale and the output channel's scale first).
+enum EpiKind {
+  EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6
+};
 
 struct GemmParams {
   int M, N, K;
@@ -380,7 +382,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   // The e4m3 form moves 128-byte operand rows like the bf16 form: the host describes e4m3 rows to TMA
   // and to the gather as 16-bit units (two codes each), so K, the coordinates and the swizzled layout
   // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
-  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q);
+  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q);
+  static_assert(EPI != EPI_STORE_Q || !OUTF32, "the e4m3 plain epilogue stores bf16");
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
                          VAR == VAR_M),
                 "e4m3 form: K-major operands, varlen-M");
@@ -1089,6 +1092,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             emit32(o, v, col, p.N - col, full, row_ok, true);
           }
         } else {
+          // e4m3 form: the A row's scale (per sorted row of the group) times the output channel's scale
+          float sr = 1.0f;
+          if (EPI == EPI_STORE_Q && VAR == VAR_M && row_ok) sr = __ldg(p.row_scale + s_off[tl.g] + m);
 #pragma unroll 1
           for (int c = c_lo; c < c_lo + kCols; c += 64) {
             uint32_t r0[32], r1[32];
@@ -1104,6 +1110,17 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
               if (p.col_bias) {
                 if (col + i < p.N) v[i] += __ldg(p.col_bias + col + i);
                 if (col + 32 + i < p.N) v[32 + i] += __ldg(p.col_bias + col + 32 + i);
+              }
+            }
+            if (EPI == EPI_STORE_Q) {
+              // lane i holds the scales of columns col + i and col + 32 + i; the warp's rows share them
+              const long long so = static_cast<long long>(tl.g) * p.ld_in + col + lane;
+              const float s0 = col + lane < p.N ? __ldg(p.in1 + so) : 0.0f;
+              const float s1 = col + 32 + lane < p.N ? __ldg(p.in1 + so + 32) : 0.0f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] *= sr * __shfl_sync(0xffffffffu, s0, i);
+                v[32 + i] *= sr * __shfl_sync(0xffffffffu, s1, i);
               }
             }
             emit64(o, v, col, p.N - col, full, row_ok);
