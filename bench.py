@@ -74,6 +74,8 @@ def kernel_work(wl, P, dW_bytes=2):
         "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
         "down_scale_e4m3": (2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
         "quantize_a_e4m3": (0, 3 * P * n + 4 * P),
+        "quantize_hu_e4m3": (0, 6 * P * n + 4 * P),
+        "dx_gemm_e4m3": (4 * P * d * n, 2 * P * n + 4 * P + 2 * E * n * d + 4 * E * d + 2 * P * d),
         "combine": (0, 2 * P * d + 2 * T * d),
         "gather_rows": (0, 4 * T * d + 4 * P * d),
         "zero_tail": (0, 0),
@@ -132,7 +134,7 @@ _GEMM_LABELS = {
     (1, 1, 0, 1): "gate_up_swiglu", (0, 0, 0, 2): "down_scale", (0, 3, 2, 0): "router_logits",
     (0, 2, 0, 3): "dact_dswiglu", (0, 2, 0, 0): "dx_gemm", (2, 3, 1, 0): "dw_tiled (gate/up, down)",
     (2, 3, 2, 0): "dwr_gemm", (2, 4, 1, 0): "dw_gather_b", (3, 3, 1, 0): "dw_gather_a",
-    (1, 1, 0, 4): "gate_up_swiglu_e4m3", (0, 0, 0, 5): "down_scale_e4m3",
+    (1, 1, 0, 4): "gate_up_swiglu_e4m3", (0, 0, 0, 5): "down_scale_e4m3", (0, 0, 0, 6): "dx_gemm_e4m3",
 }
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
@@ -392,30 +394,39 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------------ our arm
 
 
-def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, stream, steps, warmup, pk):
-    """Forward only: the e4m3 gate/up path against the bf16 forward on the same inputs (weights quantized
-    once, outside the timed region; X quantized inside every step).  Per-kernel times from the library's
-    own events."""
+def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flush, stream, steps, warmup, pk):
+    """The e4m3 forms against bf16 on the same inputs, eager calls: the forward (e4m3 gate/up; also the e4m3
+    down projection; also forward only), and a training step (e4m3 forward GEMMs and the e4m3 dX GEMM in the
+    backward).  Weights are quantized once, outside the timed steps; activations inside every step.  Each
+    arm is timed with CUDA events (L2 flushed between steps), then run again with the library's per-launch
+    events for the per-kernel times."""
     import torch
-    b8 = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False, device=X.device,
-                              capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
+    b8 = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
+                              device=X.device, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy,
+                              e4m3=True)
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
+    w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down, dx=True)
+
+    def e4m3_step():
+        vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
+        vgg.backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8d, b8)
+
     runs = {"bf16": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf),
             "e4m3": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8),
             # forward only (inference): H and U, kept for the backward, are not written
             "bf16_infer": lambda: vgg.forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf, cache=False),
-            "e4m3_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8, cache=False)}
-    # the e4m3 down projection as well
-    w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down)
-    runs["e4m3_down8"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
-    runs["e4m3_down8_infer"] = lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False)
+            "e4m3_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8, W_down, b8, cache=False),
+            # the e4m3 down projection as well
+            "e4m3_down8": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8),
+            "e4m3_down8_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False),
+            # training steps
+            "bf16_step": lambda: vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf),
+            "e4m3_step": e4m3_step}
     out = {}
     for name, fn in runs.items():
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
-        vgg.moe_profile_enable(ctx, True)
-        vgg.moe_profile_read(ctx)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i in range(steps):
             flush.zero_()
@@ -423,40 +434,48 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, s
             fn()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        vgg.moe_profile_enable(ctx, True)
+        vgg.moe_profile_read(ctx)
+        for i in range(steps):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
         prof = vgg.moe_profile_read(ctx)
         vgg.moe_profile_enable(ctx, False)
-        out[name] = (float(np.mean([a.elapsed_time(b) for a, b in evs])), prof)
+        out[name] = (ms, prof)
     rc, code = vgg.moe_get_error(ctx)
     if rc != 0:
-        raise RuntimeError(f"device error in the e4m3 forward: status {rc}, code {code}")
+        raise RuntimeError(f"device error in the e4m3 arms: status {rc}, code {code}")
     P = int(b8.P.item())
     fl = 4 * P * wl.d * wl.n
-    gu8 = out["e4m3"][1]["gate_up_swiglu_e4m3"]
-    gu16 = out["bf16"][1]["gate_up_swiglu"]
-    t8, t16 = gu8[0] / gu8[1], gu16[0] / gu16[1]
-    q = out["e4m3"][1].get("quantize_e4m3", (0.0, 1))
+    per = lambda name, k: out[name][1][k][0] / out[name][1][k][1]
+    t8, t16 = per("e4m3", "gate_up_swiglu_e4m3"), per("bf16", "gate_up_swiglu")
+    qx = out["e4m3"][1].get("quantize_e4m3", (0.0, 1))
     peak8 = 2 * pk["bf16"]
-    full = {}
-    if "e4m3_down8" in out:
-        pr = out["e4m3_down8"][1]
-        dn = pr["down_scale_e4m3"]
-        dn16 = out["bf16"][1]["down_scale"]
-        qa = pr.get("quantize_a_e4m3", (0.0, 1))
-        fl_dn = 2 * P * wl.d * wl.n
-        full = {"forward_e4m3_down_ms": out["e4m3_down8"][0], "down_ms": dn[0] / dn[1],
-                "bf16_down_ms": dn16[0] / dn16[1], "quantize_a_ms": qa[0] / max(qa[1], 1),
-                "down_tflops": fl_dn / (dn[0] / dn[1] * 1e-3) / 1e12}
-    infer = {"bf16_forward_infer_ms": out["bf16_infer"][0], "forward_infer_ms": out["e4m3_infer"][0]}
-    if "e4m3_down8_infer" in out:
-        infer["forward_e4m3_down_infer_ms"] = out["e4m3_down8_infer"][0]
+    dn, dn16 = per("e4m3_down8", "down_scale_e4m3"), per("bf16", "down_scale")
+    dx8, dx16 = per("e4m3_step", "dx_gemm_e4m3"), per("bf16_step", "dx_gemm")
+    qa = out["e4m3_down8"][1].get("quantize_a_e4m3", (0.0, 1))
+    qh = out["e4m3_step"][1].get("quantize_hu_e4m3", (0.0, 1))
+    fl_dn = 2 * P * wl.d * wl.n
+    step_fl = wl.flops_fwd_bwd(P)
     del b8, w8, w8d
-    return {**full, **infer, "forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
-            "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": q[0] / max(q[1], 1),
+    return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
+            "forward_e4m3_down_ms": out["e4m3_down8"][0],
+            "bf16_forward_infer_ms": out["bf16_infer"][0], "forward_infer_ms": out["e4m3_infer"][0],
+            "forward_e4m3_down_infer_ms": out["e4m3_down8_infer"][0],
+            "train_step_ms": out["e4m3_step"][0], "bf16_train_step_ms": out["bf16_step"][0],
+            "train_step_tflops": step_fl / (out["e4m3_step"][0] * 1e-3) / 1e12,
+            "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": qx[0] / max(qx[1], 1),
+            "down_ms": dn, "bf16_down_ms": dn16, "quantize_a_ms": qa[0] / max(qa[1], 1),
+            "dx_ms": dx8, "bf16_dx_ms": dx16, "quantize_hu_ms": qh[0] / max(qh[1], 1),
             "gate_up_tflops": fl / (t8 * 1e-3) / 1e12, "bf16_gate_up_tflops": fl / (t16 * 1e-3) / 1e12,
+            "down_tflops": fl_dn / (dn * 1e-3) / 1e12, "dx_tflops": fl / (dx8 * 1e-3) / 1e12,
             "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
-            "recipe": "e4m3 X (per token) and W_gate/W_up (per output channel), fp32 scales, fp32 accumulation",
-            "steps": steps, "l2": "flushed between steps"}
+            "recipe": "e4m3 operands with one fp32 scale per row: X per token, A and [dH|dU] per pair, weights per "
+                      "output channel of each GEMM; fp32 accumulation; dW, dact and the router stay bf16",
+            "steps": steps, "l2": "flushed between steps", "launch": "eager calls"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -655,7 +674,7 @@ def run_ours(args, rank, world, local_rank):
 
     e4m3 = None
     if not args.no_e4m3:
-        e4m3 = measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, buf, flush, stream,
+        e4m3 = measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flush, stream,
                             max(3, min(args.steps, 20)), max(3, args.warmup), pk)
 
     cpu = None
