@@ -328,18 +328,24 @@ def moe_forward(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, log
     return O, dict(logits=L, routing=routing, w_full=w_full, y_sorted=y_sorted)
 
 
-def expert_block_backward(x, dO, w, Wg, Wu, Wd):
+def expert_block_backward(x, dO, w, Wg, Wu, Wd, dap=None):
     """Backward of one expert on the rows routed to it, by the chain rule on its definition.
 
     O_t = sum_e w[t,e] y_e(x_t), y = a Wd^T, a = silu(h) * u, h = x Wg^T, u = x Wu^T.
     Returns dict with y, dw (= <dO_t, y_t>), dx contribution, dWg, dWu, dWd.
+    ``dap`` replaces dA' = dO Wd (the unweighted gradient of a) when given (the e4m3 dSwiGLU GEMM);
+    dw is then <dA', a>, the identity the fused epilogue uses.
     """
     x, dO, w = _f64(x), _f64(dO), _f64(w)
     Wg, Wu, Wd = _f64(Wg), _f64(Wu), _f64(Wd)
     h, u, a, y = expert_ffn(x, Wg, Wu, Wd)
-    dw = np.sum(dO * y, axis=1)
     dy = w[:, None] * dO
-    da = dy @ Wd
+    if dap is None:
+        dw = np.sum(dO * y, axis=1)
+        da = dy @ Wd
+    else:
+        dw = np.sum(dap * a, axis=1)
+        da = w[:, None] * dap
     sig = 1.0 / (1.0 + np.exp(-h))
     du = da * (h * sig)
     dh = da * u * (sig * (1.0 + h * (1.0 - sig)))
@@ -361,7 +367,8 @@ def router_grad_rows(member, topk_ids, w_full, dw_full):
     return np.where(member, w_full * dw_full, 0.0) - np.where(topk_mask, w_full * G, 0.0)
 
 
-def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp8_dx: bool = False):
+def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp8_dx: bool = False,
+                 fp8_dact: bool = False):
     """Backward of the layer given the forward cache.
 
     Returns dX, dW_gate, dW_up, dW_down (fp64, all experts or the listed ones),
@@ -370,6 +377,8 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
     With ``fp8_dx`` the expert part of dX takes e4m3 operands: each pair's row [dH | dU] (bf16, the
     dSwiGLU epilogue's output type, ``round_bf16``) quantized per row, and [W_gate; W_up]^T (d rows of
     2n) quantized per row (per input channel of the layer), ``quantize_rows_e4m3``.
+    With ``fp8_dact`` the dSwiGLU GEMM dA' = dO W_down takes e4m3 operands: dO per token (row) and
+    W_down^T (n rows of d) per row; dS = <dA', A> then comes from that dA' (the epilogue's identity).
     """
     X, dO = _f64(X), _f64(dO)
     T, d = X.shape
@@ -387,7 +396,12 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
         rows = routing.rows_of(e)
         if len(rows) == 0:
             continue
-        g = expert_block_backward(X[rows], dO[rows], w_full[rows, e], W_gate[e], W_up[e], W_down[e])
+        dap = None
+        if fp8_dact:
+            oq, os_ = quantize_rows_e4m3(dO[rows].astype(np.float32))
+            wq, ws_ = quantize_rows_e4m3(_f64(W_down[e]).T.astype(np.float32))  # [n, d]
+            dap = dequantize_rows_e4m3(oq, os_) @ dequantize_rows_e4m3(wq, ws_).T
+        g = expert_block_backward(X[rows], dO[rows], w_full[rows, e], W_gate[e], W_up[e], W_down[e], dap=dap)
         dw_full[rows, e] = g["dw"]
         if fp8_dx:
             hq, hs = quantize_rows_e4m3(round_bf16(np.concatenate([g["dh"], g["du"]], axis=1)).astype(np.float32))

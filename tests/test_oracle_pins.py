@@ -622,6 +622,44 @@ def test_fp8_dx_within_quantization_bound():
     assert np.max(err) > 0
 
 
+def test_fp8_dact_within_quantization_bound():
+    # with e4m3 dA' operands (dO per token, W_down^T per row): dA' within the element-wise quantization bound
+    # of the exact dO W_down, dS = <dA', A> exactly, and the weight gradients of W_down unchanged
+    rng = np.random.default_rng(18)
+    T, d, E, n, K = 24, 64, 4, 32, 2
+    X = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wu = (rng.standard_normal((E, n, d)) * 0.1).astype(np.float32)
+    Wd = (rng.standard_normal((E, d, n)) * 0.1).astype(np.float32)
+    W_r = rng.standard_normal((d, E)) * 0.3
+    dO = rng.standard_normal((T, d)).astype(np.float32)
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    g16 = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache)
+    g8 = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache, fp8_dact=True)
+    r = cache["routing"]
+    w = cache["w_full"]
+    for e in range(E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        np.testing.assert_allclose(g8["dW_down"][e], g16["dW_down"][e], rtol=1e-12, atol=1e-12)
+        D = dO[rows].astype(np.float64)
+        Bt = Wd[e].T.astype(np.float64)  # [n, d]
+        _, os_ = mo.quantize_rows_e4m3(D.astype(np.float32))
+        _, ws_ = mo.quantize_rows_e4m3(Bt.astype(np.float32))
+        dd = np.maximum(2.0 ** -4 * np.abs(D), 2.0 ** -10 * os_.astype(np.float64)[:, None])
+        db = np.maximum(2.0 ** -4 * np.abs(Bt), 2.0 ** -10 * ws_.astype(np.float64)[:, None])
+        bound = np.abs(D) @ db.T + dd @ np.abs(Bt).T + dd @ db.T
+        blk = mo.expert_block_backward(X[rows], dO[rows], w[rows, e], Wg[e], Wu[e], Wd[e])
+        exact = D @ Bt.T
+        oq, _ = mo.quantize_rows_e4m3(D.astype(np.float32))
+        wq, _ = mo.quantize_rows_e4m3(Bt.astype(np.float32))
+        dap = mo.dequantize_rows_e4m3(oq, os_) @ mo.dequantize_rows_e4m3(wq, ws_).T
+        assert np.all(np.abs(dap - exact) <= bound * (1 + 1e-9) + 1e-12) and np.max(np.abs(dap - exact)) > 0
+        np.testing.assert_allclose(g8["dw"][rows, e], np.sum(dap * blk["a"], axis=1), rtol=1e-12, atol=1e-12)
+    assert 0 < np.max(np.abs(g8["dX"] - g16["dX"])) < 0.2 * np.max(np.abs(g16["dX"]))
+
+
 # ---------------------------------------------------------------- the metric
 
 
