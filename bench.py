@@ -405,7 +405,7 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                               device=X.device, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy,
                               e4m3=True)
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
-    w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down, dx=True)
+    w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down, backward=True)
 
     def e4m3_step():
         vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)

@@ -297,22 +297,37 @@ int moe_quantize_dx_weights_e4m3(moe_ctx* ctx, const void* W_gate, const void* W
                                  void* Wgu_q, float* wgu_scale, moe_stream_t stream);
 
 /*
- * moe_backward_e4m3 — moe_backward with the dX GEMM on e4m3 operands.
- * [GG] "한계" (the FP8 grouped GEMM); [SM] "4 기여 ②".  Arguments as moe_backward, plus
- * Wgu_q / wgu_scale from moe_quantize_dx_weights_e4m3 and the caller-owned buffers HUq [cap, 2n]
- * (uint8) and hu_scale [cap] (fp32): the rows [dH[j] | dU[j]] below offsets[E] are quantized per
- * row into them (one scale over both halves), and
- *
- *   dXp[j,c] = hu_scale[j] * wgu_scale[e,c] * sum_k e4m3(HUq[j,k]) e4m3(Wgu_q[e,c,k])
- *
- * accumulated in fp32 (kind::f8f6f4); everything else as moe_backward (bf16 weight gradients).
+ * moe_quantize_dact_weights_e4m3 — the B operand of the e4m3 dSwiGLU GEMM: W_down[e]^T (n rows of d)
+ * quantized per row as moe_quantize_rows_e4m3 does.  [SM] "3 기여 ①" (dA' = dO W_down).
+ * W_down [E,d,n] bf16; tmp [E,n,d] bf16 device scratch (caller-owned, overwritten); outputs
+ * Wdt_q [E,n,d] uint8 codes and wdt_scale [E,n] fp32.  Shape rules as moe_backward; 16-byte
+ * aligned pointers; else MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_dact_weights_e4m3(moe_ctx* ctx, const void* W_down, int E, int n, int d, void* tmp, void* Wdt_q,
+                                   float* wdt_scale, moe_stream_t stream);
+
+/*
+ * moe_backward_e4m3 — moe_backward with the dX GEMM and/or the dSwiGLU GEMM on e4m3 operands.
+ * [GG] "한계" (the FP8 grouped GEMM); [SM] "3 기여 ①", "4 기여 ②".  Arguments as moe_backward, plus:
+ *   Wgu_q / wgu_scale (moe_quantize_dx_weights_e4m3; NULL: bf16 dX GEMM) with the caller-owned
+ *   buffers HUq [cap, 2n] uint8 and hu_scale [cap] fp32: the rows [dH[j] | dU[j]] below offsets[E]
+ *   are quantized per row into them (one scale over both halves), and
+ *     dXp[j,c] = hu_scale[j] * wgu_scale[e,c] * sum_k e4m3(HUq[j,k]) e4m3(Wgu_q[e,c,k]);
+ *   Wdt_q / wdt_scale (moe_quantize_dact_weights_e4m3; NULL: bf16 dSwiGLU GEMM) with dOq [cap, d]
+ *   uint8 and do_scale [cap] fp32: the expert-sorted dO rows below offsets[E] are quantized per row
+ *   into them, and
+ *     dA'[j,c] = do_scale[j] * wdt_scale[e,c] * sum_i e4m3(dOq[j,i]) e4m3(Wdt_q[e,c,i]),
+ *   the dSwiGLU epilogue (dS = <dA', A>, dH, dU, A') running on that dA'.
+ * Code products accumulate in fp32 (kind::f8f6f4); everything else as moe_backward (bf16 weight
+ * gradients).  MOE_ERR_INVALID_ARG on a missing or misaligned buffer.
  */
 int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
-                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale, int T, int d,
-                      int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids, const float* topk_w,
-                      const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
-                      const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* HUq,
-                      float* hu_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale,
+                      const void* Wdt_q, const float* wdt_scale, int T, int d, int E, int n, int K, int m_tile,
+                      long long cap, const int32_t* topk_ids, const float* topk_w, const int32_t* offsets,
+                      const int32_t* sorted_tok, const float* sorted_w, const int32_t* tok_ptr,
+                      const int32_t* tok_pairs, const void* H, const void* U, void* HUq, float* hu_scale, void* dOq,
+                      float* do_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
                       float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*

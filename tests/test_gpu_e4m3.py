@@ -211,18 +211,20 @@ BWD8_CASES = [
 ]
 
 
+@pytest.mark.parametrize("dx,dact", [(True, False), (False, True), (True, True)], ids=["dx", "dact", "dx_dact"])
 @pytest.mark.parametrize("wl", BWD8_CASES, ids=lambda w: w.name)
-def test_e4m3_dx_backward_matches_oracle(ctx, wl):
-    """moe_backward_e4m3 against the oracle:
-    * the B codes ([W_gate; W_up]^T per row) bit for bit;
-    * the [dH | dU] codes against the oracle's quantization of its own bf16 [dH | dU]: the decision is taken
-      on values that differ by bf16 rounding, so a code may sit on the other side of an e4m3 rounding
-      boundary: at most 1% of them, each by one e4m3 step;
+def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
+    """moe_backward_e4m3 against the oracle's e4m3 backward:
+    * the weight codes ([W_gate; W_up]^T and W_down^T per row) bit for bit;
+    * the dSwiGLU GEMM's dO codes bit for bit (they are decided on the exact bf16 dO);
+    * the dX GEMM's [dH | dU] codes against the oracle's quantization of its own bf16 [dH | dU]: the decision
+      is taken on values that differ by bf16 rounding, so a code may sit on the other side of an e4m3
+      rounding boundary: at most 1% of them, each by one e4m3 step;
     * dX against the oracle's sum of the device's [dH | dU] codes times the B codes (plus the router part),
       within the usual tolerance: the GEMM and the per-token reduction exactly;
-    * dX against the oracle's own e4m3 backward: mean within the usual tolerance, max within 0.15 (one
-      e4m3 step of a code is up to 12.5% of that element);
-    * every other gradient as in the bf16 backward."""
+    * dX against the oracle's own e4m3 backward: mean within the usual tolerance, max within 0.15 (one e4m3
+      step of a code is up to 12.5% of that element) -- the variant's own tolerance;
+    * every other gradient within the usual tolerance of the oracle's e4m3 backward."""
     import varlen_grouped_gemm_gb300 as vgg
     import oracle
     from _helpers import compare_layer
@@ -230,47 +232,63 @@ def test_e4m3_dx_backward_matches_oracle(ctx, wl):
     dv = inp.dev
     E, n, d = wl.E, wl.n, wl.d
     buf = vgg.Buffers.allocate(wl.T, d, E, n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.float32, e4m3=True)
-    w8 = vgg.E4m3Weights.quantize(ctx, dv["W_gate"], dv["W_up"], dx=True)
+    w8 = vgg.E4m3Weights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"], backward=True)
     vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
-    vgg.backward_e4m3(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], w8, buf)
+    vgg.backward_e4m3(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], w8, buf, dx=dx,
+                      dact=dact)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == vgg.MOE_OK and code == 0, (rc, code)
-    Wg = mo.bf16_bits_to_f64(inp.W_gate)
-    Wu = mo.bf16_bits_to_f64(inp.W_up)
+    Wg, Wu = mo.bf16_bits_to_f64(inp.W_gate), mo.bf16_bits_to_f64(inp.W_up)
+    Wd = mo.bf16_bits_to_f64(inp.W_down)
     B = np.concatenate([Wg, Wu], axis=1).transpose(0, 2, 1).reshape(E * d, 2 * n)  # [E*d, 2n]
     bq, bs = mo.quantize_rows_e4m3(B.astype(np.float32))
     np.testing.assert_array_equal(w8.Wgu_q.cpu().numpy().reshape(E * d, 2 * n), bq)
     np.testing.assert_array_equal(w8.wgu_scale.cpu().numpy().reshape(-1), bs)
     Bd = mo.dequantize_rows_e4m3(bq, bs).reshape(E, d, 2 * n)
+    tq, ts = mo.quantize_rows_e4m3(Wd.transpose(0, 2, 1).reshape(E * n, d).astype(np.float32))
+    np.testing.assert_array_equal(w8.Wdt_q.cpu().numpy().reshape(E * n, d), tq)
+    np.testing.assert_array_equal(w8.wdt_scale.cpu().numpy().reshape(-1), ts)
+    Wdt = mo.dequantize_rows_e4m3(tq, ts).reshape(E, n, d)
 
     g = gpu_routing(buf)
     O_ref, cache = mo.moe_forward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K, wl.m_tile,
                                   logits_for_routing=g["logits"], scores_for_routing=g["scores"])
     grads = mo.moe_backward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, inp.dO, cache,
-                            fp8_dx=True)
+                            fp8_dx=dx, fp8_dact=dact)
     r = cache["routing"]
     X64, dO64 = mo.bf16_bits_to_f64(inp.X), mo.bf16_bits_to_f64(inp.dO)
-    huq = buf.huq[:r.P].cpu().numpy()
-    hus = buf.hus[:r.P].cpu().numpy()
-    dX_codes = grads["dlogits"] @ mo.bf16_bits_to_f64(inp.W_r).T
+    if dact:  # dO codes of every sorted pair, bit for bit
+        oq, os_ = mo.quantize_rows_e4m3(inp.dO[r.sorted_tok])
+        np.testing.assert_array_equal(buf.doq[:r.P].cpu().numpy(), oq)
+        np.testing.assert_array_equal(buf.dos[:r.P].cpu().numpy(), os_)
+    refs = None
     flips = 0
-    for e in range(E):
-        lo, hi = r.offsets[e], r.offsets[e + 1]
-        if hi == lo:
-            continue
-        rows = r.sorted_tok[lo:hi]
-        blk = mo.expert_block_backward(X64[rows], dO64[rows], cache["w_full"][rows, e], inp.W_gate[e], inp.W_up[e],
-                                       inp.W_down[e])
-        oq, _ = mo.quantize_rows_e4m3(mo.round_bf16(np.concatenate([blk["dh"], blk["du"]], axis=1)).astype(np.float32))
-        diff = huq[lo:hi] != oq
-        flips += int(diff.sum())
-        if diff.any():  # a differing code is a neighbour on the e4m3 grid (same sign, adjacent magnitude)
-            a, b = huq[lo:hi][diff].astype(np.int64), oq[diff].astype(np.int64)
-            assert np.all(np.abs(a - b) == 1) or np.all(np.abs((a & 0x7F) - (b & 0x7F)) <= 1)
-        np.add.at(dX_codes, rows, mo.dequantize_rows_e4m3(huq[lo:hi], hus[lo:hi]) @ Bd[e].T)
-    assert flips <= 0.01 * huq.size, flips
-    rep = compare_layer(buf, inp, O_ref, cache, grads, refs={"dX": dX_codes})
+    if dx:
+        huq = buf.huq[:r.P].cpu().numpy()
+        hus = buf.hus[:r.P].cpu().numpy()
+        dX_codes = grads["dlogits"] @ mo.bf16_bits_to_f64(inp.W_r).T
+        for e in range(E):
+            lo, hi = r.offsets[e], r.offsets[e + 1]
+            if hi == lo:
+                continue
+            rows = r.sorted_tok[lo:hi]
+            dap = None
+            if dact:
+                dq, ds_ = mo.quantize_rows_e4m3(inp.dO[rows])
+                dap = mo.dequantize_rows_e4m3(dq, ds_) @ Wdt[e].T
+            blk = mo.expert_block_backward(X64[rows], dO64[rows], cache["w_full"][rows, e], inp.W_gate[e],
+                                           inp.W_up[e], inp.W_down[e], dap=dap)
+            hq, _ = mo.quantize_rows_e4m3(mo.round_bf16(np.concatenate([blk["dh"], blk["du"]], axis=1)).astype(np.float32))
+            diff = huq[lo:hi] != hq
+            flips += int(diff.sum())
+            if diff.any():  # a differing code is a neighbour on the e4m3 grid
+                a, b = huq[lo:hi][diff].astype(np.int64), hq[diff].astype(np.int64)
+                assert np.all((a & 0x80) == (b & 0x80)) and np.all(np.abs((a & 0x7F) - (b & 0x7F)) <= 1)
+            np.add.at(dX_codes, rows, mo.dequantize_rows_e4m3(huq[lo:hi], hus[lo:hi]) @ Bd[e].T)
+        assert flips <= 0.01 * huq.size, flips
+        refs = {"dX": dX_codes}
+    rep = compare_layer(buf, inp, O_ref, cache, grads, refs=refs)
     end = oracle.metrics.rel_error(buf.dX.double().cpu().numpy(), grads["dX"])
     assert end["mean"] <= 3e-3 and end["max"] <= 0.15, end
-    print(wl.name, "code flips", flips, "of", huq.size, "dX vs oracle e4m3", (round(end["max"], 4), round(end["mean"], 6)),
-          {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
+    print(wl.name, "dx", dx, "dact", dact, "code flips", flips, "dX vs oracle e4m3",
+          (round(end["max"], 4), round(end["mean"], 6)), {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})

@@ -28,7 +28,7 @@ EXPORTS = (
     "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
     "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc", "moe_permute_capacity",
     "moe_capacity_workspace_bytes", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
-    "moe_quantize_dx_weights_e4m3", "moe_backward_e4m3",
+    "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -78,9 +78,10 @@ def lib() -> ctypes.CDLL:
         L.moe_grouped_gemm_fwd_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P,
                                                 _P, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_quantize_dx_weights_e4m3.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P]
-        L.moe_backward_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL, _P, _P,
-                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
-                                        _SZ, _P]
+        L.moe_quantize_dact_weights_e4m3.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P]
+        L.moe_backward_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL,
+                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I,
+                                        _P, _P, _P, _P, _SZ, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -313,9 +314,19 @@ def moe_quantize_dx_weights_e4m3(ctx, W_gate, W_up, Wgu_q, wgu_scale, stream=Non
     return tmp  # the caller keeps it alive until the stream has run the call
 
 
-def moe_backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, Wgu_q, wgu_scale, K, m_tile, topk_ids, topk_w, offsets,
-                      sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, HUq, hu_scale, dX, dW_gate, dW_up, dW_down,
-                      dS, dlogits, dW_r, ws, stream=None):
+def moe_quantize_dact_weights_e4m3(ctx, W_down, Wdt_q, wdt_scale, stream=None):
+    """W_down^T per expert ([E, n, d]) as e4m3 codes with one scale per row (the dSwiGLU GEMM's B)."""
+    E, d, n = W_down.shape
+    tmp = torch.empty((E, n, d), dtype=torch.bfloat16, device=W_down.device)
+    _check("moe_quantize_dact_weights_e4m3", lib().moe_quantize_dact_weights_e4m3(
+        ctx.handle, _ptr(W_down, torch.bfloat16), E, n, d, _ptr(tmp, torch.bfloat16), _ptr(Wdt_q, torch.uint8),
+        _ptr(wdt_scale, torch.float32), _stream(stream)))
+    return tmp  # the caller keeps it alive until the stream has run the call
+
+
+def moe_backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, Wgu_q, wgu_scale, Wdt_q, wdt_scale, K, m_tile, topk_ids,
+                      topk_w, offsets, sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, HUq, hu_scale, dOq, do_scale,
+                      dX, dW_gate, dW_up, dW_down, dS, dlogits, dW_r, ws, stream=None):
     T, d = X.shape
     E, n, _ = W_gate.shape
     cap = sorted_tok.numel()
@@ -324,9 +335,10 @@ def moe_backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, Wgu_q, wgu_scale, K
     dw_fp32 = 1 if dW_gate.dtype == torch.float32 else 0
     _check("moe_backward_e4m3", lib().moe_backward_e4m3(
         ctx.handle, _ptr(dO, bf), _ptr(X, bf), _ptr(W_r, bf), _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf),
-        _ptr(Wgu_q, torch.uint8), _ptr(wgu_scale, f32), T, d, E, n, K, m_tile, cap, _ptr(topk_ids, i32),
-        _ptr(topk_w, f32), _ptr(offsets, i32), _ptr(sorted_tok, i32), _ptr(sorted_w, f32), _ptr(tok_ptr, i32),
-        _ptr(tok_pairs, i32), _ptr(H, f32), _ptr(U, f32), _ptr(HUq, torch.uint8), _ptr(hu_scale, f32), _ptr(dX, bf),
+        _ptr(Wgu_q, torch.uint8), _ptr(wgu_scale, f32), _ptr(Wdt_q, torch.uint8), _ptr(wdt_scale, f32), T, d, E, n,
+        K, m_tile, cap, _ptr(topk_ids, i32), _ptr(topk_w, f32), _ptr(offsets, i32), _ptr(sorted_tok, i32),
+        _ptr(sorted_w, f32), _ptr(tok_ptr, i32), _ptr(tok_pairs, i32), _ptr(H, f32), _ptr(U, f32),
+        _ptr(HUq, torch.uint8), _ptr(hu_scale, f32), _ptr(dOq, torch.uint8), _ptr(do_scale, f32), _ptr(dX, bf),
         _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), dw_fp32, _ptr(dS, f32), _ptr(dlogits, f32), _ptr(dW_r, f32), wp,
         wb, _stream(stream)))
 
@@ -398,6 +410,8 @@ class Buffers:
     as_: torch.Tensor | None = None
     huq: torch.Tensor | None = None  # e4m3 dX GEMM: [dH | dU] codes [cap, 2n] and per-row scales [cap]
     hus: torch.Tensor | None = None
+    doq: torch.Tensor | None = None  # e4m3 dSwiGLU GEMM: sorted dO codes [cap, d] and per-row scales [cap]
+    dos: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
@@ -436,7 +450,9 @@ class Buffers:
             xq=z((T, d), torch.uint8) if e4m3 else None, xs=z((T,), f32) if e4m3 else None,
             aq=z((cap, n), torch.uint8) if e4m3 else None, as_=z((cap,), f32) if e4m3 else None,
             huq=z((cap, 2 * n), torch.uint8) if (e4m3 and backward) else None,
-            hus=z((cap,), f32) if (e4m3 and backward) else None)
+            hus=z((cap,), f32) if (e4m3 and backward) else None,
+            doq=z((cap, d), torch.uint8) if (e4m3 and backward) else None,
+            dos=z((cap,), f32) if (e4m3 and backward) else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, cache=True):
@@ -468,9 +484,13 @@ class E4m3Weights:
     wd_scale: torch.Tensor | None = None
     Wgu_q: torch.Tensor | None = None  # the e4m3 dX GEMM: [W_gate; W_up]^T codes [E, d, 2n], scales [E, d]
     wgu_scale: torch.Tensor | None = None
+    Wdt_q: torch.Tensor | None = None  # the e4m3 dSwiGLU GEMM: W_down^T codes [E, n, d], scales [E, n]
+    wdt_scale: torch.Tensor | None = None
 
     @staticmethod
-    def quantize(ctx, W_gate, W_up, W_down=None, stream=None, dx=False) -> "E4m3Weights":
+    def quantize(ctx, W_gate, W_up, W_down=None, stream=None, backward=False) -> "E4m3Weights":
+        """The forward's codes (W_down's too when given); with ``backward`` also the two backward copies
+        ([W_gate; W_up]^T for the dX GEMM, W_down^T for the dSwiGLU GEMM; W_down required)."""
         E, n, d = W_gate.shape
         dev = W_gate.device
         w = E4m3Weights(torch.empty((E, n, d), dtype=torch.uint8, device=dev),
@@ -483,12 +503,17 @@ class E4m3Weights:
             w.Wd_q = torch.empty((E, d, n), dtype=torch.uint8, device=dev)
             w.wd_scale = torch.empty((E, d), dtype=torch.float32, device=dev)
             moe_quantize_rows_e4m3(ctx, W_down, w.Wd_q, w.wd_scale, stream)
-        if dx:
+        if backward:
+            if W_down is None:
+                raise ValueError("the backward codes need W_down")
             w.Wgu_q = torch.empty((E, d, 2 * n), dtype=torch.uint8, device=dev)
             w.wgu_scale = torch.empty((E, d), dtype=torch.float32, device=dev)
             tmp = moe_quantize_dx_weights_e4m3(ctx, W_gate, W_up, w.Wgu_q, w.wgu_scale, stream)
-            torch.cuda.synchronize(dev)  # the scratch copy may go once the call has run
-            del tmp
+            w.Wdt_q = torch.empty((E, n, d), dtype=torch.uint8, device=dev)
+            w.wdt_scale = torch.empty((E, n), dtype=torch.float32, device=dev)
+            tmp2 = moe_quantize_dact_weights_e4m3(ctx, W_down, w.Wdt_q, w.wdt_scale, stream)
+            torch.cuda.synchronize(dev)  # the scratch copies may go once the calls have run
+            del tmp, tmp2
         return w
 
 
@@ -517,15 +542,18 @@ def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, strea
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 
-def backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8: E4m3Weights, buf: Buffers, stream=None):
-    """The backward with the dX GEMM on e4m3 operands (``w8`` quantized with ``dx=True``, ``buf`` allocated
-    with ``e4m3=True``); the weight gradients stay bf16."""
+def backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8: E4m3Weights, buf: Buffers, stream=None, dx=True,
+                  dact=True):
+    """The backward with the dX GEMM (``dx``) and the dSwiGLU GEMM (``dact``) on e4m3 operands (``w8`` quantized
+    with ``backward=True``, ``buf`` allocated with ``e4m3=True``); the weight gradients stay bf16."""
     if w8.Wgu_q is None or buf.huq is None:
-        raise ValueError("e4m3 backward needs E4m3Weights.quantize(..., dx=True) and Buffers(e4m3=True)")
-    moe_backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8.Wgu_q, w8.wgu_scale, buf.K, buf.m_tile, buf.topk_ids,
+        raise ValueError("e4m3 backward needs E4m3Weights.quantize(..., backward=True) and Buffers(e4m3=True)")
+    moe_backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8.Wgu_q if dx else None, w8.wgu_scale if dx else None,
+                      w8.Wdt_q if dact else None, w8.wdt_scale if dact else None, buf.K, buf.m_tile, buf.topk_ids,
                       buf.topk_w, buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.H, buf.U,
-                      buf.huq, buf.hus, buf.dX, buf.dW_gate, buf.dW_up, buf.dW_down, buf.dS, buf.dlogits, buf.dW_r,
-                      buf.ws, stream)
+                      buf.huq if dx else None, buf.hus if dx else None, buf.doq if dact else None,
+                      buf.dos if dact else None, buf.dX, buf.dW_gate, buf.dW_up, buf.dW_down, buf.dS, buf.dlogits,
+                      buf.dW_r, buf.ws, stream)
 
 
 def backward(ctx, dO, X, W_r, W_gate, W_up, W_down, buf: Buffers, stream=None):

@@ -637,7 +637,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
                          const int32_t* tok_pairs, const void* H, const void* U, void* dX, void* dW_gate,
                          void* dW_up, void* dW_down, int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws,
                          size_t ws_bytes, moe_stream_t stream, const void* Wgu_q, const float* wgu_scale, void* HUq,
-                         float* hu_scale) {
+                         float* hu_scale, const void* Wdt_q, const float* wdt_scale, void* dOq, float* do_scale) {
   VGG_REQUIRE(ctx && dO && X && W_r && W_gate && W_up && W_down && topk_ids && topk_w && offsets && sorted_tok &&
               sorted_w && tok_ptr && tok_pairs && H && U && dX && dW_gate && dW_up && dW_down && dS && dlogits &&
               dW_r && ws);
@@ -665,7 +665,40 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
                                                static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs, ctx->d_err,
                                                ctx->num_sms, ctx->timeout_ns, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
-  {
+  if (Wdt_q) {
+    // e4m3: the sorted dO rows (below offsets[E]) quantized per row, B = W_down^T quantized per row by
+    // moe_quantize_dact_weights_e4m3; rows handed to TMA as 16-bit units (code pairs)
+    VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(w.dOs, cap, offsets + E, d, static_cast<uint8_t*>(dOq),
+                                                            do_scale, s));
+    GemmParams p = base_params(ctx);
+    p.N = n;
+    p.K = d / 2;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.in0 = static_cast<const float*>(H);
+    p.in1 = static_cast<const float*>(U);
+    p.ld_in = n;
+    p.out0 = w.dH;
+    p.out1 = w.dU;
+    p.out2 = w.Ap;
+    p.ld_out = n;
+    p.row_scale = sorted_w;
+    p.part = w.part;
+    p.part_ld = part_ld;
+    p.q_row = do_scale;
+    p.q_col = wdt_scale;
+    p.q_ld = n;
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, Wdt_q, d / 2, n, E, bn6) ||
+        !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, bn6);
+    VGG_LAUNCH("dact_dswiglu_e4m3", run_dact_dswiglu_e4m3(bn6, p, m, std::min(tiles, ctx->num_sms), s));
+  } else {
     GemmParams p = base_params(ctx);
     p.N = n;
     p.K = d;
@@ -833,20 +866,41 @@ int moe_backward(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, c
                  float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
   return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
                        sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
-                       dlogits, dW_r, ws, ws_bytes, stream, nullptr, nullptr, nullptr, nullptr);
+                       dlogits, dW_r, ws, ws_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, nullptr);
 }
 
 int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
-                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale, int T, int d,
-                      int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids, const float* topk_w,
-                      const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
-                      const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* HUq,
-                      float* hu_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
+                      const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale,
+                      const void* Wdt_q, const float* wdt_scale, int T, int d, int E, int n, int K, int m_tile,
+                      long long cap, const int32_t* topk_ids, const float* topk_w, const int32_t* offsets,
+                      const int32_t* sorted_tok, const float* sorted_w, const int32_t* tok_ptr,
+                      const int32_t* tok_pairs, const void* H, const void* U, void* HUq, float* hu_scale, void* dOq,
+                      float* do_scale, void* dX, void* dW_gate, void* dW_up, void* dW_down, int dW_fp32, float* dS,
                       float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
-  VGG_REQUIRE(Wgu_q && wgu_scale && HUq && hu_scale && aligned16(Wgu_q) && aligned16(HUq));
+  // each e4m3 GEMM is optional: a NULL weight code array keeps that GEMM in bf16
+  VGG_REQUIRE(!Wgu_q || (wgu_scale && HUq && hu_scale && aligned16(Wgu_q) && aligned16(HUq)));
+  VGG_REQUIRE(!Wdt_q || (wdt_scale && dOq && do_scale && aligned16(Wdt_q) && aligned16(dOq)));
   return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
                        sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
-                       dlogits, dW_r, ws, ws_bytes, stream, Wgu_q, wgu_scale, HUq, hu_scale);
+                       dlogits, dW_r, ws, ws_bytes, stream, Wgu_q, wgu_scale, HUq, hu_scale, Wdt_q, wdt_scale, dOq,
+                       do_scale);
+}
+
+int moe_quantize_dact_weights_e4m3(moe_ctx* ctx, const void* W_down, int E, int n, int d, void* tmp, void* Wdt_q,
+                                   float* wdt_scale, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && W_down && tmp && Wdt_q && wdt_scale);
+  VGG_REQUIRE(shapes_ok(1, d, E, n, 1));
+  VGG_REQUIRE(aligned16(W_down) && aligned16(tmp) && aligned16(Wdt_q));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16* t = static_cast<__nv_bfloat16*>(tmp);
+  VGG_LAUNCH("quantize_e4m3", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_down), E, d, n, t, d, 0,
+                                                         s));
+  VGG_LAUNCH("quantize_e4m3", launch_quantize_rows_e4m3(t, static_cast<long long>(E) * n, nullptr, d,
+                                                        static_cast<uint8_t*>(Wdt_q), wdt_scale, s));
+  return MOE_OK;
 }
 
 int moe_quantize_dx_weights_e4m3(moe_ctx* ctx, const void* W_gate, const void* W_up, int E, int n, int d, void* tmp,

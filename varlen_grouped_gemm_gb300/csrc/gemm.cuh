@@ -56,8 +56,10 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 // EPI_SWIGLU_Q, EPI_SCALE_Q, EPI_STORE_Q: the SwiGLU, the combine-weight and the plain (varlen-M, bf16)
 // epilogues of the e4m3 form (operands are e4m3 codes of per-row-scaled rows; the accumulator is
 // multiplied by the A row's scale and the output channel's scale first).
+// EPI_DSWIGLU_Q: the dSwiGLU epilogue of the e4m3 form (the accumulator times q_row[row] q_col[column]).
 enum EpiKind {
-  EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6
+  EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
+  EPI_DSWIGLU_Q = 7
 };
 
 struct GemmParams {
@@ -93,6 +95,9 @@ struct GemmParams {
   float* part;  // dSwiGLU epilogue: per-row partial dot products [rows][part_ld]
   int part_ld;
   const float* col_bias;
+  const float* q_row;  // e4m3 dSwiGLU: A row scales [rows], B row scales [groups][q_ld]
+  const float* q_col;
+  int q_ld;
   int* err;
   unsigned long long timeout_ns;
 };
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   // The e4m3 form moves 128-byte operand rows like the bf16 form: the host describes e4m3 rows to TMA
   // and to the gather as 16-bit units (two codes each), so K, the coordinates and the swizzled layout
   // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
-  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q);
+  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q || EPI == EPI_DSWIGLU_Q);
   static_assert(EPI != EPI_STORE_Q || !OUTF32, "the e4m3 plain epilogue stores bf16");
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
                          VAR == VAR_M),
@@ -937,7 +942,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       constexpr int kCols = (EW == 8) ? BN / 2 : BN;  // accumulator columns handled by this warp
       const int c_lo = half * kCols;
 
-      if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE || EPI == EPI_SCALE_Q || EPI == EPI_DSWIGLU) {
+      if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE || EPI == EPI_SCALE_Q || EPI == EPI_DSWIGLU ||
+          EPI == EPI_DSWIGLU_Q) {
         const long long orow = s_off[tl.g] + tl.m0 + row_local;
         const int crow = s_off[tl.g] + tl.m0 + quarter * 32;
         const long long roff = orow * p.ld_out;
@@ -1014,8 +1020,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             }
             emit64(o0, v, tl.n0 + c, p.N - tl.n0 - c, full, row_ok);
           }
-        } else {  // EPI_DSWIGLU
+        } else {  // EPI_DSWIGLU, EPI_DSWIGLU_Q
           const float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
+          const float sq = (EPI == EPI_DSWIGLU_Q && row_ok) ? __ldg(p.q_row + orow) : 1.0f;  // e4m3: A row scale
           float ds = 0.0f;
 #pragma unroll 1
           for (int c = c_lo; c < c_lo + kCols; c += 32) {
@@ -1025,6 +1032,13 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             const int col = tl.n0 + c;
             const int ncols = p.N - col;
             if (ncols <= 0) continue;
+            if (EPI == EPI_DSWIGLU_Q) {
+              // lane i holds column col + i's B scale; the warp's rows share it
+              const float cs = lane < ncols ? __ldg(p.q_col + static_cast<long long>(tl.g) * p.q_ld + col + lane) : 0.0f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                r[i] = __float_as_uint(__uint_as_float(r[i]) * sq * __shfl_sync(0xffffffffu, cs, i));
+            }
             float h[32], u[32];
             if (row_ok) {
               load_f32_row32(p.in0 + orow * p.ld_in + col, h, ncols);

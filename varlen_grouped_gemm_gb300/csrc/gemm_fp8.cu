@@ -147,6 +147,15 @@ cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, co
   return cudaGetLastError();
 }
 
+// The backward's dSwiGLU GEMM with e4m3 operands: A = dO's rows (sorted), B = W_down^T (n rows of d), both
+// quantized per row; the epilogue applies both scales to dA' and runs the dSwiGLU epilogue.
+cudaError_t run_dact_dswiglu_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256 && SmemLayout<256, 4, 8, 1>::bytes(p.groups, VAR_M) <= kMaxSmem)
+    return launch_grouped_gemm<256, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU_Q, false>(p, m, grid, s);
+  if (BN == 256) return launch_grouped_gemm<256, 3, 8, 2, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU_Q, false>(p, m, grid, s);
+  return launch_grouped_gemm<128, 4, 8, 2, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU_Q, false>(p, m, grid, s);
+}
+
 // Per-row e4m3 quantization of the rows [M0[r] | M1[r]] (two bf16 matrices of `cols` columns each, side by
 // side), the rows below *rows_limit: one scale per row over both halves, codes [rows, 2 cols].  One warp
 // per row; the row is read twice (the second time from L1/L2).

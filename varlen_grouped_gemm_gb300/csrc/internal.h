@@ -31,6 +31,7 @@ cudaError_t run_gate_up_swiglu(int BN, int cn, const GemmParams& p, const Maps& 
 cudaError_t run_gate_up_swiglu_e4m3(int BN, int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dx_store_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dact_dswiglu_e4m3(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rows_pair_e4m3(const __nv_bfloat16* M0, const __nv_bfloat16* M1, long long rows,
                                            const int32_t* rows_limit, int cols, uint8_t* q, float* scales,
                                            cudaStream_t s);
