@@ -76,6 +76,8 @@ def kernel_work(wl, P, dW_bytes=2):
         "quantize_a_e4m3": (0, 3 * P * n + 4 * P),
         "quantize_hu_e4m3": (0, 6 * P * n + 4 * P),
         "dx_gemm_e4m3": (4 * P * d * n, 2 * P * n + 4 * P + 2 * E * n * d + 4 * E * d + 2 * P * d),
+        "quantize_do_e4m3": (0, 3 * P * d + 4 * P),
+        "dact_dswiglu_e4m3": (2 * P * d * n, P * d + 4 * P + E * d * n + 4 * E * n + 8 * P * n + 6 * P * n),
         "combine": (0, 2 * P * d + 2 * T * d),
         "gather_rows": (0, 4 * T * d + 4 * P * d),
         "zero_tail": (0, 0),
@@ -135,6 +137,7 @@ _GEMM_LABELS = {
     (0, 2, 0, 3): "dact_dswiglu", (0, 2, 0, 0): "dx_gemm", (2, 3, 1, 0): "dw_tiled (gate/up, down)",
     (2, 3, 2, 0): "dwr_gemm", (2, 4, 1, 0): "dw_gather_b", (3, 3, 1, 0): "dw_gather_a",
     (1, 1, 0, 4): "gate_up_swiglu_e4m3", (0, 0, 0, 5): "down_scale_e4m3", (0, 0, 0, 6): "dx_gemm_e4m3",
+    (0, 0, 0, 7): "dact_dswiglu_e4m3",
 }
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
@@ -396,8 +399,8 @@ def run_reference(args, rank, world):
 
 def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flush, stream, steps, warmup, pk):
     """The e4m3 forms against bf16 on the same inputs, eager calls: the forward (e4m3 gate/up; also the e4m3
-    down projection; also forward only), and a training step (e4m3 forward GEMMs and the e4m3 dX GEMM in the
-    backward).  Weights are quantized once, outside the timed steps; activations inside every step.  Each
+    down projection; also forward only), and a training step (e4m3 forward GEMMs, and the e4m3 dSwiGLU and dX GEMMs
+    in the backward).  Weights are quantized once, outside the timed steps; activations inside every step.  Each
     arm is timed with CUDA events (L2 flushed between steps), then run again with the library's per-launch
     events for the per-kernel times."""
     import torch
@@ -457,6 +460,8 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
     dx8, dx16 = per("e4m3_step", "dx_gemm_e4m3"), per("bf16_step", "dx_gemm")
     qa = out["e4m3_down8"][1].get("quantize_a_e4m3", (0.0, 1))
     qh = out["e4m3_step"][1].get("quantize_hu_e4m3", (0.0, 1))
+    da8, da16 = per("e4m3_step", "dact_dswiglu_e4m3"), per("bf16_step", "dact_dswiglu")
+    qd = out["e4m3_step"][1].get("quantize_do_e4m3", (0.0, 1))
     fl_dn = 2 * P * wl.d * wl.n
     step_fl = wl.flops_fwd_bwd(P)
     del b8, w8, w8d
@@ -469,12 +474,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             "gate_up_ms": t8, "bf16_gate_up_ms": t16, "quantize_x_ms": qx[0] / max(qx[1], 1),
             "down_ms": dn, "bf16_down_ms": dn16, "quantize_a_ms": qa[0] / max(qa[1], 1),
             "dx_ms": dx8, "bf16_dx_ms": dx16, "quantize_hu_ms": qh[0] / max(qh[1], 1),
+            "dact_ms": da8, "bf16_dact_ms": da16, "quantize_do_ms": qd[0] / max(qd[1], 1),
             "gate_up_tflops": fl / (t8 * 1e-3) / 1e12, "bf16_gate_up_tflops": fl / (t16 * 1e-3) / 1e12,
             "down_tflops": fl_dn / (dn * 1e-3) / 1e12, "dx_tflops": fl / (dx8 * 1e-3) / 1e12,
+            "dact_tflops": fl_dn / (da8 * 1e-3) / 1e12,
             "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
-            "recipe": "e4m3 operands with one fp32 scale per row: X per token, A and [dH|dU] per pair, weights per "
-                      "output channel of each GEMM; fp32 accumulation; dW, dact and the router stay bf16",
+            "recipe": "e4m3 operands with one fp32 scale per row: X per token, A, dO and [dH|dU] per pair, weights per "
+                      "output channel of each GEMM; fp32 accumulation; dW and the router stay bf16",
             "steps": steps, "l2": "flushed between steps", "launch": "eager calls"}
 
 
