@@ -314,8 +314,10 @@ int moe_quantize_dact_weights_e4m3(moe_ctx* ctx, const void* W_down, int E, int 
  *   are quantized per row into them (one scale over both halves), and
  *     dXp[j,c] = hu_scale[j] * wgu_scale[e,c] * sum_k e4m3(HUq[j,k]) e4m3(Wgu_q[e,c,k]);
  *   Wdt_q / wdt_scale (moe_quantize_dact_weights_e4m3; NULL: bf16 dSwiGLU GEMM) with dOq [cap, d]
- *   uint8 and do_scale [cap] fp32: the expert-sorted dO rows below offsets[E] are quantized per row
- *   into them, and
+ *   uint8 and do_scale [cap] fp32: they receive the per-row quantization of the expert-sorted dO rows
+ *   (dO is quantized once per token when the workspace's dX-partials region holds T*d + 4T bytes, i.e.
+ *   whenever cap >= T, and the codes gathered with dO; else the sorted rows below offsets[E] are
+ *   quantized; the codes are the same either way), and
  *     dA'[j,c] = do_scale[j] * wdt_scale[e,c] * sum_i e4m3(dOq[j,i]) e4m3(Wdt_q[e,c,i]),
  *   the dSwiGLU epilogue (dS = <dA', A>, dH, dU, A') running on that dA'.
  * Code products accumulate in fp32 (kind::f8f6f4); everything else as moe_backward (bf16 weight

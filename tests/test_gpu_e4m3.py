@@ -261,6 +261,8 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
         oq, os_ = mo.quantize_rows_e4m3(inp.dO[r.sorted_tok])
         np.testing.assert_array_equal(buf.doq[:r.P].cpu().numpy(), oq)
         np.testing.assert_array_equal(buf.dos[:r.P].cpu().numpy(), os_)
+    if dact and buf.sorted_tok.numel() >= wl.T:  # dO quantized per token and gathered: empty rows zero, scale 1
+        assert not buf.doq[r.P:].any().item() and bool((buf.dos[r.P:] == 1).all().item())
     refs = None
     flips = 0
     if dx:
@@ -292,3 +294,55 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
     assert end["mean"] <= 3e-3 and end["max"] <= 0.15, end
     print(wl.name, "dx", dx, "dact", dact, "code flips", flips, "dX vs oracle e4m3",
           (round(end["max"], 4), round(end["mean"], 6)), {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
+
+
+@pytest.mark.parametrize("dx", [False, True], ids=["dact", "dx_dact"])
+def test_e4m3_backward_capacity_layout(ctx, dx):
+    """The e4m3 dSwiGLU GEMM on the capacity layout ([E, C] slots) with fewer slots than tokens: dO is then
+    quantized on its sorted rows rather than once per token.  The slots' dO codes and scales bit for bit (empty
+    slots: zero codes, scale 1); every gradient against the oracle's e4m3 backward on the same kept pairs
+    (dX with the variant's own tolerance when the dX GEMM is e4m3 too, else the usual one)."""
+    import varlen_grouped_gemm_gb300 as vgg
+    import oracle
+    wl = synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_e4m3", T=512, d=256, E=16, n=192, K=2,
+                      capacity_factor=0.25)
+    inp = Inputs(wl)
+    dv = inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.float32,
+                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, e4m3=True)
+    assert buf.sorted_tok.numel() < wl.T
+    w8 = vgg.E4m3Weights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"], backward=True)
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    vgg.backward_e4m3(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], w8, buf, dx=dx,
+                      dact=True)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    C = mo.expert_capacity(wl.T, wl.E, wl.K, wl.capacity_factor)
+    O_ref, cache = mo.moe_forward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K,
+                                  logits_for_routing=buf.logits.cpu().numpy(), capacity=C, policy=wl.drop_policy,
+                                  drop_keys=buf.topk_w.cpu().numpy())
+    r = cache["routing"]
+    assert r.P < wl.T * wl.K
+    st = buf.sorted_tok.cpu().numpy()
+    kept = st >= 0
+    q, sc = mo.quantize_rows_e4m3(inp.dO[st[kept]])
+    doq, dos = buf.doq.cpu().numpy(), buf.dos.cpu().numpy()
+    np.testing.assert_array_equal(doq[kept], q)
+    np.testing.assert_array_equal(dos[kept], sc)
+    assert not doq[~kept].any() and np.all(dos[~kept] == 1)
+    g = mo.moe_backward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, inp.dO, cache, fp8_dx=dx,
+                        fp8_dact=True)
+    oracle.compare("O", dev_to_f64(buf.O), O_ref)
+    dX = dev_to_f64(buf.dX)
+    if dx:
+        end = oracle.metrics.rel_error(dX, g["dX"])
+        assert end["mean"] <= 3e-3 and end["max"] <= 0.15, end
+    else:
+        oracle.compare("dX", dX, g["dX"])
+    for name in ("dW_gate", "dW_up", "dW_down"):
+        oracle.compare(name, dev_to_f64(getattr(buf, name)), np.stack([g[name][e] for e in range(wl.E)]),
+                       param_axes=oracle.WEIGHT_GRAD)
+    slot_of = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(wl.E)]).astype(np.int64)
+    oracle.compare("dS", dev_to_f64(buf.dS)[slot_of], g["dw"][r.sorted_tok, r.sorted_exp])
+    oracle.compare("dlogits", dev_to_f64(buf.dlogits), g["dlogits"])
+    oracle.compare("dW_r", dev_to_f64(buf.dW_r), g["dW_r"])

@@ -659,17 +659,31 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
   if (cap > static_cast<long long>(T) * K)
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
-  // expert-sorted copies of X and dO: every backward GEMM then reads whole TMA boxes
+  // e4m3 dSwiGLU GEMM: dO quantized once per token (a token's pairs share its row, so its codes are those of
+  // every pair) into the dX partials' region, which is free until the dX GEMM; the gather below copies the
+  // code rows and scales to the sorted positions.  When that region is too small (a capacity layout with
+  // cap < T) the sorted rows are quantized instead.
+  const size_t tok_codes = al(static_cast<size_t>(T) * d);
+  const bool dact_tok = Wdt_q && tok_codes + sizeof(float) * T <= sizeof(__nv_bfloat16) * cap * d;
+  uint8_t* tq = reinterpret_cast<uint8_t*>(w.dXp);
+  float* ts = reinterpret_cast<float*>(tq + tok_codes);
+  if (dact_tok)
+    VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(dO), T, nullptr, d, tq,
+                                                            ts, s));
+  // expert-sorted copies of X and dO (and of dO's codes): every backward GEMM then reads whole TMA boxes
   VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
                                                static_cast<const __nv_bfloat16*>(X),
-                                               static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs, ctx->d_err,
-                                               ctx->num_sms, ctx->timeout_ns, s));
+                                               static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs,
+                                               dact_tok ? tq : nullptr, dact_tok ? ts : nullptr,
+                                               static_cast<uint8_t*>(dOq), do_scale, ctx->d_err, ctx->num_sms,
+                                               ctx->timeout_ns, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
   if (Wdt_q) {
-    // e4m3: the sorted dO rows (below offsets[E]) quantized per row, B = W_down^T quantized per row by
-    // moe_quantize_dact_weights_e4m3; rows handed to TMA as 16-bit units (code pairs)
-    VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(w.dOs, cap, offsets + E, d, static_cast<uint8_t*>(dOq),
-                                                            do_scale, s));
+    // e4m3: the sorted dO code rows (gathered above, else the sorted rows below offsets[E] quantized here),
+    // B = W_down^T quantized per row by moe_quantize_dact_weights_e4m3; rows handed to TMA as 16-bit units
+    if (!dact_tok)
+      VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(w.dOs, cap, offsets + E, d,
+                                                              static_cast<uint8_t*>(dOq), do_scale, s));
     GemmParams p = base_params(ctx);
     p.N = n;
     p.K = d / 2;

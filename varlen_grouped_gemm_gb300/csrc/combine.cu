@@ -344,6 +344,10 @@ namespace vgg {
 // pair (row-major gathers re-read them from DRAM when they do not fit in L2).  Positions that hold no
 // pair (the tail [P, cap) and the empty slots of the capacity layout) are then written from a zeroed
 // chunk.  One token in flight per warp, three CTAs per SM.
+//
+// CODES: a third source travels with b, the tokens' e4m3 code rows c ([T, d] bytes) and their scales cs
+// ([T]): out_c[j] = c[sorted_tok[j]], out_cs[j] = cs[sorted_tok[j]]; positions without a pair get zero
+// codes and scale 1 (a zero row's quantization).  A third buffer per warp: two CTAs per SM.
 constexpr int kGrWarps = 8;
 static_assert(kMaxTokPairs <= 64, "gather_rows: at most two pair positions per lane");
 constexpr int kGrChunk = 2048;  // bf16 elements per bulk copy
@@ -359,12 +363,14 @@ __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes
                : "memory");
 }
 
+template <bool CODES>
 __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
     const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ sorted_tok,
     const int32_t* __restrict__ tok_ptr, const int32_t* __restrict__ tok_pairs, long long cap, int T, int d,
     const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b, __nv_bfloat16* __restrict__ out_a,
-    __nv_bfloat16* __restrict__ out_b, int* err, unsigned long long timeout_ns) {
-  extern __shared__ __align__(128) uint8_t gr_smem[];  // zero chunk, then per warp two chunks
+    __nv_bfloat16* __restrict__ out_b, const uint8_t* __restrict__ c, const float* __restrict__ cs,
+    uint8_t* __restrict__ out_c, float* __restrict__ out_cs, int* err, unsigned long long timeout_ns) {
+  extern __shared__ __align__(128) uint8_t gr_smem[];  // zero chunk, then per warp two chunks (+ a code chunk)
   __shared__ uint64_t bars[kGrWarps];
   __shared__ int abort_flag;
   constexpr uint32_t kChunkBytes = kGrChunk * 2;
@@ -381,8 +387,9 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   // A warp takes one token at a time: lane 0 loads the token's rows (one bulk copy per tensor and chunk)
   // and every lane stores them to one (or two) of the token's pair positions, so the stores of a token
   // are issued in parallel and the position lookups overlap the load.
+  constexpr uint32_t kWarpBytes = 2 * kChunkBytes + (CODES ? kGrChunk : 0);
   const uint32_t zero = smem_u32(gr_smem);
-  const uint32_t buf = zero + kChunkBytes * (1 + 2 * warp);
+  const uint32_t buf = zero + kChunkBytes + kWarpBytes * warp;
   const long long P = offsets[E];
   const long long gw = static_cast<long long>(blockIdx.x) * kGrWarps + warp;
   const long long nw = static_cast<long long>(gridDim.x) * kGrWarps;
@@ -406,14 +413,21 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
         else jl[h] = j;
       }
     }
+    if (CODES) {
+      const float sc = __ldg(cs + t);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (jl[h] >= 0) out_cs[jl[h]] = sc;
+    }
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
       bulk_wait_read<0>();  // this lane's previous stores have read the warp's buffer
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[warp], 2 * bytes);
+        mbar_arrive_expect_tx(&bars[warp], 2 * bytes + (CODES ? bytes / 2 : 0));
         bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
         bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+        if (CODES) bulk_g2s(buf + 2 * kChunkBytes, c + t * d + c0, bytes / 2, &bars[warp]);
       }
       const int landed = mbar_wait(&bars[warp], phase, &abort_flag, timeout_ns, err) ? 1 : 0;
       if (!__all_sync(0xffffffffu, landed)) {
@@ -426,6 +440,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
         if (jl[h] >= 0) {
           bulk_s2g(out_a + jl[h] * d + c0, buf, bytes);
           bulk_s2g(out_b + jl[h] * d + c0, buf + kChunkBytes, bytes);
+          if (CODES) bulk_s2g(out_c + jl[h] * d + c0, buf + 2 * kChunkBytes, bytes / 2);
         }
       }
       bulk_commit();
@@ -434,10 +449,12 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   // positions without a pair: the tail and the empty slots of the capacity layout
   for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32) {
     if (j < P && sorted_tok[j] >= 0) continue;
+    if (CODES) out_cs[j] = 1.0f;
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
       bulk_s2g(out_a + j * d + c0, zero, bytes);
       bulk_s2g(out_b + j * d + c0, zero, bytes);
+      if (CODES) bulk_s2g(out_c + j * d + c0, zero, bytes / 2);
     }
     bulk_commit();
   }
@@ -450,17 +467,28 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
 
 cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, const int32_t* tok_ptr,
                                const int32_t* tok_pairs, long long cap, int T, int d, const __nv_bfloat16* a,
-                               const __nv_bfloat16* b, __nv_bfloat16* out_a, __nv_bfloat16* out_b, int* err,
+                               const __nv_bfloat16* b, __nv_bfloat16* out_a, __nv_bfloat16* out_b,
+                               const uint8_t* c, const float* cs, uint8_t* out_c, float* out_cs, int* err,
                                int num_sms, unsigned long long timeout_ns, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(kGrChunk) * 2 * (1 + 2 * kGrWarps);
-  cudaError_t st =
-      cudaFuncSetAttribute(gather_rows_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const bool codes = c != nullptr;
+  const size_t smem = static_cast<size_t>(kGrChunk) * (2 + kGrWarps * (codes ? 5 : 4));
+  const void* fn = codes ? reinterpret_cast<const void*>(gather_rows_bulk_kernel<true>)
+                         : reinterpret_cast<const void*>(gather_rows_bulk_kernel<false>);
+  cudaError_t st = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (st != cudaSuccess) return st;
   const long long want = (T + kGrWarps - 1) / kGrWarps;
-  const int blocks = static_cast<int>(want < 3LL * num_sms ? want : 3LL * num_sms);
-  if (blocks > 0)
-    gather_rows_bulk_kernel<<<blocks, kGrWarps * 32, smem, s>>>(offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
-                                                               a, b, out_a, out_b, err, timeout_ns);
+  const long long per_sm = codes ? 2 : 3;
+  const int blocks = static_cast<int>(want < per_sm * num_sms ? want : per_sm * num_sms);
+  if (blocks > 0) {
+    if (codes)
+      gather_rows_bulk_kernel<true><<<blocks, kGrWarps * 32, smem, s>>>(
+          offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, c, cs, out_c, out_cs, err,
+          timeout_ns);
+    else
+      gather_rows_bulk_kernel<false><<<blocks, kGrWarps * 32, smem, s>>>(
+          offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, nullptr, nullptr, nullptr,
+          nullptr, err, timeout_ns);
+  }
   return cudaGetLastError();
 }
 
