@@ -222,29 +222,38 @@ __global__ void __launch_bounds__(256) token_backward_kernel(
   }
   __syncwarp();
   const int nv = d >> 3;
+  // Per 8 columns: the pair rows in batches of eight loads in flight (one memory round trip for a token
+  // of up to eight pairs), added in pair order; then the router part, eight W_r^T rows (L2-resident) per
+  // round trip, in nonzero order.
+  constexpr int kB = 8;
   for (int c = lane; c < nv; c += 32) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    int r = 0;
-    for (; r + 4 <= cnt; r += 4) {  // four rows in flight per thread
-      uint4 q[4];
+    for (int r0 = 0; r0 < cnt; r0 += kB) {
+      uint4 q[kB];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = s_j[r + u];
+      for (int u = 0; u < kB; ++u) {
+        const int j = r0 + u < cnt ? s_j[r0 + u] : -1;
         q[u] = j >= 0 ? ldg_nc_v4(dXp + static_cast<long long>(j) * d + 8 * c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) add_bf16x8(acc, q[u]);
+      for (int u = 0; u < kB; ++u)
+        if (r0 + u < cnt && s_j[r0 + u] >= 0) add_bf16x8(acc, q[u]);
     }
-    for (; r < cnt; ++r) {
-      const int j = s_j[r];
-      if (j >= 0) add_bf16x8(acc, ldg_nc_v4(dXp + static_cast<long long>(j) * d + 8 * c));
-    }
-    for (int i = 0; i < nnz; ++i) {
-      const float v = s_nz_v[i];
-      const uint4 q = *reinterpret_cast<const uint4*>(WrT + static_cast<long long>(s_nz_e[i]) * d + 8 * c);
-      const float2 a = unpack_bf16x2(q.x), b = unpack_bf16x2(q.y), cc = unpack_bf16x2(q.z), dd = unpack_bf16x2(q.w);
-      acc[0] += v * a.x; acc[1] += v * a.y; acc[2] += v * b.x; acc[3] += v * b.y;
-      acc[4] += v * cc.x; acc[5] += v * cc.y; acc[6] += v * dd.x; acc[7] += v * dd.y;
+    for (int i0 = 0; i0 < nnz; i0 += kB) {
+      uint4 q[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        q[u] = i0 + u < nnz ? *reinterpret_cast<const uint4*>(WrT + static_cast<long long>(s_nz_e[i0 + u]) * d + 8 * c)
+                            : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        if (i0 + u >= nnz) break;
+        const float v = s_nz_v[i0 + u];
+        const float2 a = unpack_bf16x2(q[u].x), b = unpack_bf16x2(q[u].y), cc = unpack_bf16x2(q[u].z),
+                     dd = unpack_bf16x2(q[u].w);
+        acc[0] += v * a.x; acc[1] += v * a.y; acc[2] += v * b.x; acc[3] += v * b.y;
+        acc[4] += v * cc.x; acc[5] += v * cc.y; acc[6] += v * dd.x; acc[7] += v * dd.y;
+      }
     }
     *reinterpret_cast<uint4*>(dX + static_cast<long long>(t) * d + 8 * c) = pack8(acc);
   }
