@@ -52,3 +52,20 @@ def test_argument_errors_are_reported_without_a_device(libpath):
     lib.moe_route.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 5 + \
         [ctypes.c_size_t, ctypes.c_void_p]
     assert lib.moe_route(None, None, None, None, 1, 64, 8, 2, None, None, None, None, None, 0, None) == 1
+
+
+# Every entry point that takes a context checks its arguments before any device work: a NULL context (all
+# other arguments zero) is MOE_ERR_INVALID_ARG, with or without a GPU.
+_CTX_ENTRIES = ["moe_route", "moe_permute", "moe_grouped_gemm_fwd", "moe_combine", "moe_backward",
+                "moe_permute_noalloc", "moe_permute_capacity", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
+                "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
+                "moe_test_gemm_varlen_m", "moe_test_gemm_varlen_k"]
+
+
+@pytest.mark.parametrize("name", _CTX_ENTRIES)
+def test_null_context_is_an_argument_error(libpath, name):
+    import varlen_grouped_gemm_gb300 as vgg
+    fn = getattr(vgg.lib(), name)
+    args = [None if t in (ctypes.c_void_p, ctypes.c_char_p) else 0 for t in fn.argtypes]
+    assert fn.argtypes[0] is ctypes.c_void_p
+    assert fn(*args) == vgg.MOE_ERR_INVALID_ARG
