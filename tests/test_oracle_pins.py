@@ -697,3 +697,62 @@ def test_metric_weight_gradient_floor():
     g[1, 0, 2] = 1e-3
     r = oracle.rel_error(g, o, param_axes=oracle.WEIGHT_GRAD)
     assert abs(r["max"] - 1e-3 / math.sqrt((25 + 2e-12) / 12)) < 1e-12
+
+
+def test_bf16_widening_matches_torch_and_special_values():
+    """bf16 bits -> fp64 against torch's own bf16 conversion on random non-NaN bit patterns, and exact values:
+    1.0, -2.0, the smallest subnormal 2^-133, the largest finite bf16 and +inf."""
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 1 << 16, 4096, dtype=np.uint32).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # drop inf/NaN exponents
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(mo.bf16_bits_to_f64(bits), ref)
+    special = np.array([0x3F80, 0xC000, 0x0001, 0x7F7F, 0x7F80], dtype=np.uint16)
+    got = mo.bf16_bits_to_f64(special)
+    assert got[0] == 1.0 and got[1] == -2.0 and got[2] == 2.0 ** -133
+    assert got[3] == (2 - 2 ** -7) * 2.0 ** 127 and np.isinf(got[4]) and got[4] > 0
+
+
+def test_router_logits_of_one_hot_tokens_are_router_rows():
+    """A token whose row is the unit vector e_i scores every expert with row i of W_r (plus the bias): the
+    orientation of the router product (X W_r, not its transpose) and the bias broadcast over experts."""
+    d, E = 6, 4
+    rng = np.random.default_rng(3)
+    W_r = rng.standard_normal((d, E))
+    bias = rng.standard_normal(E)
+    X = np.eye(d)[[2, 0, 5]]
+    L = mo.router_logits(X, W_r, bias)
+    np.testing.assert_array_equal(L, W_r[[2, 0, 5]] + bias[None, :])
+    np.testing.assert_array_equal(mo.router_logits(X, W_r), W_r[[2, 0, 5]])
+
+
+@pytest.mark.parametrize("K,pad", [(1, False), (2, False), (3, True)])
+def test_router_grad_rows_is_the_derivative_of_the_combine_weights(K, pad):
+    """router_grad_rows against central differences of f(l) = sum over the token's final pairs of
+    w_e(l) dw_e, with w = combine_weights(l, TopK) and the top-K set held fixed.  With ``pad`` the final set
+    also holds an expert outside the top-K (a token rounding pad), whose weight still normalises over the
+    top-K.  With K = 1 and no pad the weight is identically 1, so the gradient is zero."""
+    rng = np.random.default_rng(11 + K)
+    T, E = 5, 6
+    L = rng.standard_normal((T, E))
+    topk = mo.topk_experts(L, K)
+    member = np.zeros((T, E), dtype=bool)
+    member[np.arange(T)[:, None], topk] = True
+    if pad:
+        for t in range(T):
+            member[t, [e for e in range(E) if not member[t, e]][0]] = True
+    dw = rng.standard_normal((T, E))
+    got = mo.router_grad_rows(member, topk, mo.combine_weights(L, topk), dw)
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            lp, lm = L.copy(), L.copy()
+            lp[t, e] += h
+            lm[t, e] -= h
+            fp = np.sum(np.where(member, mo.combine_weights(lp, topk) * dw, 0.0)[t])
+            fm = np.sum(np.where(member, mo.combine_weights(lm, topk) * dw, 0.0)[t])
+            assert abs(got[t, e] - (fp - fm) / (2 * h)) < 1e-7, (t, e)
+    if K == 1 and not pad:
+        np.testing.assert_allclose(got, 0.0, atol=1e-15)
+    if not pad:  # the weights on the top-K set sum to one, so their logit gradient sums to zero
+        np.testing.assert_allclose(got.sum(axis=1), 0.0, atol=1e-12)
