@@ -76,7 +76,7 @@ def kernel_work(wl, P, dW_bytes=2):
         "quantize_a_e4m3": (0, 3 * P * n + 4 * P),
         "quantize_hu_e4m3": (0, 6 * P * n + 4 * P),
         "dx_gemm_e4m3": (4 * P * d * n, 2 * P * n + 4 * P + 2 * E * n * d + 4 * E * d + 2 * P * d),
-        "quantize_do_e4m3": (0, 3 * P * d + 4 * P),
+        "quantize_do_e4m3": (0, 3 * T * d + 4 * T),  # dO per token (the sorted-row form, cap < T: 3Pd + 4P)
         "dact_dswiglu_e4m3": (2 * P * d * n, P * d + 4 * P + E * d * n + 4 * E * n + 8 * P * n + 6 * P * n),
         "combine": (0, 2 * P * d + 2 * T * d),
         "gather_rows": (0, 4 * T * d + 4 * P * d),
