@@ -60,49 +60,102 @@ def workload_desc(wl):
 
 
 def kernel_work(wl, P, dW_bytes=2):
-    """Algorithmic flops and minimum HBM bytes of one launch of each kernel label (bf16 = 2 B; the
-    gate/up pre-activations H, U are cached in fp32).  Weights are read once per launch, every
-    activation tensor is written once and read once."""
+    """Per kernel label: (flops, algorithmic bytes, bytes this design moves) of one launch (bf16 = 2 B).
+
+    Algorithmic bytes follow the hot path's byte model: weights read once per launch, a gathered operand
+    counted once per unique token row (2Td), every cached activation (H, U, A, Yw, dH, dU, A', dXp) in bf16,
+    written once and read once.  The moved bytes count what this design stores and reads instead: H and U in
+    fp32 (8Pn instead of 4Pn), the expert-sorted copies of X and dO that the backward GEMMs read (2Pd each
+    instead of 2Td) and the bf16 low parts of dH, dU and A' that the weight-gradient GEMMs read.  The grouping
+    and the sorted copies (gather_rows) have no place in the byte model (the gathers belong inside the GEMMs'
+    loads): their algorithmic bytes are the ones they would move if they were the whole job."""
     T, d, E, n, K = wl.T, wl.d, wl.E, wl.n, wl.K
+    same = lambda f, b: (f, b, b)
+    dWb = dW_bytes
     return {
-        "router_logits": (2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E),  # (split: + partials, read by top-K)
-        "topk_softmax": (0, 4 * T * E + 8 * T * K),
-        "permute": (0, 4 * T * K + 16 * P + (4 * T * E if wl.m_tile else 0)),
-        "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 10 * P * n),
-        "gate_up_swiglu_e4m3": (4 * P * d * n, T * d + 4 * T + 2 * E * n * d + 8 * E * n + 10 * P * n),
-        "quantize_e4m3": (0, 3 * T * d + 4 * T),
-        "down_scale": (2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
-        "down_scale_e4m3": (2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
-        "quantize_a_e4m3": (0, 3 * P * n + 4 * P),
-        "quantize_hu_e4m3": (0, 6 * P * n + 4 * P),
-        "dx_gemm_e4m3": (4 * P * d * n, 2 * P * n + 4 * P + 2 * E * n * d + 4 * E * d + 2 * P * d),
-        "quantize_do_e4m3": (0, 3 * T * d + 4 * T),  # dO per token (the sorted-row form, cap < T: 3Pd + 4P)
-        "dact_dswiglu_e4m3": (2 * P * d * n, P * d + 4 * P + E * d * n + 4 * E * n + 8 * P * n + 6 * P * n),
-        "combine": (0, 2 * P * d + 2 * T * d),
-        "gather_rows": (0, 4 * T * d + 4 * P * d),
-        "zero_tail": (0, 0),
-        "dact_dswiglu": (2 * P * d * n, 2 * P * d + 2 * E * d * n + 8 * P * n + 6 * P * n),
-        "dx_gemm": (4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d),
-        "wr_transpose": (0, 4 * d * E),
-        "token_backward": (2 * P * d, 2 * P * d + 2 * T * d + 8 * T * E),
-        "dwr_gemm": (4 * T * d * E, 2 * T * d + 4 * T * E + 4 * d * E),  # dlogits as two bf16 parts
-        "dwr_reduce": (0, 8 * d * E),
-        "dw_gate_up": (4 * P * d * n, 2 * P * d + 4 * P * n + 2 * dW_bytes * E * n * d),
-        "dw_down": (2 * P * d * n, 2 * P * d + 2 * P * n + dW_bytes * E * d * n),
+        "router_logits": same(2 * T * d * E, 2 * T * d + 2 * d * E + 4 * T * E),
+        "topk_softmax": same(0, 4 * T * E + 8 * T * K),
+        "permute": same(0, 4 * T * K + 16 * P + (4 * T * E if wl.m_tile else 0)),
+        "gate_up_swiglu": (4 * P * d * n, 2 * T * d + 4 * E * n * d + 6 * P * n, 2 * T * d + 4 * E * n * d + 10 * P * n),
+        "gate_up_swiglu_e4m3": (4 * P * d * n, T * d + 4 * T + 2 * E * n * d + 8 * E * n + 6 * P * n,
+                                T * d + 4 * T + 2 * E * n * d + 8 * E * n + 10 * P * n),
+        "quantize_e4m3": same(0, 3 * T * d + 4 * T),
+        "down_scale": same(2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
+        "down_scale_e4m3": same(2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
+        "quantize_a_e4m3": same(0, 3 * P * n + 4 * P),
+        "quantize_hu_e4m3": same(0, 6 * P * n + 4 * P),
+        "dx_gemm_e4m3": same(4 * P * d * n, 2 * P * n + 4 * P + 2 * E * n * d + 4 * E * d + 2 * P * d),
+        "quantize_do_e4m3": same(0, 3 * T * d + 4 * T),  # dO per token (the sorted-row form, cap < T: 3Pd + 4P)
+        "dact_dswiglu_e4m3": (2 * P * d * n, T * d + 4 * T + E * d * n + 4 * E * n + 10 * P * n,
+                              P * d + 4 * P + E * d * n + 4 * E * n + 8 * P * n + 12 * P * n),
+        "combine": same(0, 2 * P * d + 2 * T * d),
+        "gather_rows": same(0, 4 * T * d + 4 * P * d),
+        "zero_tail": same(0, 0),
+        "dact_dswiglu": (2 * P * d * n, 2 * T * d + 2 * E * d * n + 10 * P * n,
+                         2 * P * d + 2 * E * d * n + 8 * P * n + 12 * P * n),
+        "dx_gemm": same(4 * P * d * n, 4 * P * n + 4 * E * n * d + 2 * P * d),
+        "wr_transpose": same(0, 4 * d * E),
+        "token_backward": same(2 * P * d, 2 * P * d + 2 * T * d + 8 * T * E),
+        "dwr_gemm": same(4 * T * d * E, 2 * T * d + 4 * T * E + 4 * d * E),  # dlogits as two bf16 parts
+        "dwr_reduce": same(0, 8 * d * E),
+        "dw_gate_up": (4 * P * d * n, 2 * T * d + 4 * P * n + 2 * dWb * E * n * d,
+                       2 * P * d + 8 * P * n + 2 * dWb * E * n * d),
+        "dw_down": (2 * P * d * n, 2 * T * d + 2 * P * n + dWb * E * d * n, 2 * P * d + 4 * P * n + dWb * E * d * n),
     }
 
 
-def activation_memory(buf) -> dict:
-    """Device bytes of the layer's state between forward and backward: what the forward keeps for the
-    backward (routing state, the fp32 H and U from which the backward recomputes A), the forward-only
-    temporaries (A for the down projection, Yw for the combine), the workspace and the peak torch
-    allocation of the process (inputs, weights and gradients included)."""
+def roofline(name, work, ms_total, launches, pk, traffic=None):
+    """The kernel against its binding resource: algorithmic flops or bytes per launch over its average
+    launch time, as a fraction of the measured peak (sustained bf16 for a kernel timed inside the step)."""
+    fl, by, mv = work[name]
+    avg_ms = ms_total / max(launches, 1)
+    t_tensor = fl / (pk["bf16_sus"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = fl / (avg_ms * 1e-3) / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_sus"], "traffic": traffic,
+                "peak_source": f"{pk['source']} (sustained bf16)", "avg_launch_ms": avg_ms,
+                "hbm_gbs_of_algorithmic_bytes": by / (avg_ms * 1e-3) / 1e9, "algorithmic_bytes": by,
+                "moved_bytes": mv}
+    achieved = by / (avg_ms * 1e-3) / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
+            "avg_launch_ms": avg_ms, "tflops": fl / (avg_ms * 1e-3) / 1e12, "tensor_frac": fl / (avg_ms * 1e-3) / 1e12
+            / pk["bf16_sus"], "algorithmic_bytes": by, "moved_bytes": mv,
+            "moved_gbs": mv / (avg_ms * 1e-3) / 1e9}
+
+
+def kernel_table(prof, work, steps, pk):
+    """Per kernel label: time per step, share, TFLOP/s, GB/s of algorithmic and of moved bytes, bound."""
+    kernels = {}
+    tot = max(sum(v[0] for v in prof.values()), 1e-9)
+    for k, (kms, kl) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
+        f2, b2, m2 = work.get(k, (0, 0, 0))
+        a = max(kms / max(kl, 1), 1e-9)
+        kernels[k] = {"ms_per_step": kms / steps, "share": kms / tot,
+                      "tflops": f2 / (a * 1e-3) / 1e12 if f2 else None,
+                      "gbs_of_algorithmic_bytes": b2 / (a * 1e-3) / 1e9 if b2 else None,
+                      "gbs_of_moved_bytes": m2 / (a * 1e-3) / 1e9 if m2 else None,
+                      "bound": ("tensor" if f2 / (pk["bf16_sus"] * 1e12) >= b2 / (pk["hbm_gbs"] * 1e9) else "hbm")}
+    return kernels
+
+
+def activation_memory(buf, base=0) -> dict:
+    """Device bytes of the layer's state between forward and backward, under the caching rule of the
+    SonicMoE page (cache only what the backward needs, no O(T K d) tensor such as Y or the gathered X): what
+    the forward keeps for the backward (routing state and the fp32 H and U from which the backward recomputes
+    A), the forward-only temporaries (A for the down projection, Yw for the combine), the workspace (the
+    backward's scratch, including its expert-sorted copies of X and dO) and the peak allocation of this
+    workload (inputs, weights and gradients included; bytes allocated before `base` excluded)."""
     import torch
     nb = lambda *ts: int(sum(t.numel() * t.element_size() for t in ts if t is not None))
-    return {"kept_for_backward_bytes": nb(buf.H, buf.U, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.offsets,
-                                          buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs),
+    kept = nb(buf.H, buf.U, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.offsets, buf.sorted_tok,
+              buf.sorted_w, buf.tok_ptr, buf.tok_pairs)
+    T = buf.topk_ids.shape[0]
+    return {"kept_for_backward_bytes": kept, "kept_bytes_per_token": kept / T, "cached_o_tkd_tensors": [],
             "forward_temporaries_bytes": nb(buf.A, buf.Yw), "workspace_bytes": nb(buf.ws),
-            "peak_allocated_bytes": int(torch.cuda.max_memory_allocated())}
+            "peak_allocated_bytes": int(torch.cuda.max_memory_allocated()) - int(base)}
 
 
 def source_hash() -> str:
@@ -485,6 +538,73 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             "steps": steps, "l2": "flushed between steps", "launch": "eager calls"}
 
 
+def measure_workload(vgg, ctx, name, steps, warmup, pk, dev, flush, stream):
+    """One more workload's step on its own inputs: ms, TFLOP/s, tokens/s, the dominant kernel against its
+    roofline, per-kernel shares and activation memory.  X, W_r, the bias and dO come from the seeded
+    generator (they decide the routing); the expert weights are drawn on the device (torch's generator,
+    seed 0, standard deviation 1/sqrt(fan_in)), which keeps the set-up of the largest workloads short: the
+    step's time does not depend on their values.  The step runs as one CUDA graph, L2 flushed between steps."""
+    import torch
+    wl = synth.WORKLOADS[name]
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X, dO, W_r = to_dev(synth.make_x(wl)), to_dev(synth.make_dout(wl)), to_dev(synth.make_router(wl))
+    bias_h = synth.make_bias(wl)
+    bias = None if bias_h is None else torch.from_numpy(bias_h).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    draw = lambda shape, fan_in: torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16).mul_(fan_in ** -0.5)
+    W_gate = draw((wl.E, wl.n, wl.d), wl.d)
+    W_up = draw((wl.E, wl.n, wl.d), wl.d)
+    W_down = draw((wl.E, wl.d, wl.n), wl.n)
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
+                               device=dev, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy)
+    for _ in range(warmup):
+        vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+    graph = vgg.StepGraph(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+    graph.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        graph.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    vgg.moe_profile_enable(ctx, True)
+    vgg.moe_profile_read(ctx)
+    for i in range(steps):
+        flush.zero_()
+        vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf)
+    torch.cuda.synchronize()
+    prof = vgg.moe_profile_read(ctx)
+    vgg.moe_profile_enable(ctx, False)
+    rc, code = vgg.moe_get_error(ctx)
+    if rc != 0:
+        raise RuntimeError(f"device error in workload {name}: status {rc}, code {code}")
+    P = int(buf.P.item())
+    counts = buf.counts.cpu().numpy()
+    work = kernel_work(wl, P)
+    dname, (dms, dl) = max(prof.items(), key=lambda kv: kv[1][0])
+    flops = wl.flops_fwd_bwd(P)
+    out = {"workload": workload_desc(wl), "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+           "pct_of_peak_bf16": 100 * flops / (ms * 1e-3) / 1e12 / pk["bf16_sus"], "tokens_per_s": wl.T / (ms * 1e-3),
+           "pairs": P, "empty_experts": int((counts == 0).sum()), "max_rows_per_expert": int(counts.max()),
+           "roofline": roofline(dname, work, dms, dl, pk, recorded_traffic(wl.name, dname)),
+           "kernels": {k: {"ms_per_step": v["ms_per_step"], "share": round(v["share"], 4)}
+                       for k, v in kernel_table(prof, work, steps, pk).items()},
+           "activation_memory": activation_memory(buf, base), "steps": steps,
+           "expert_weights": "drawn on the device (torch generator, seed 0)"}
+    del graph, buf, X, dO, W_r, bias, W_gate, W_up, W_down
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import varlen_grouped_gemm_gb300 as vgg
@@ -575,34 +695,9 @@ def run_ours(args, rank, world, local_rank):
 
     # dominant kernel and its roofline: the binding resource of its algorithmic work
     work = kernel_work(wl, P)
-    dom = max(prof.items(), key=lambda kv: kv[1][0])
-    dname, (dms, dlaunch) = dom
-    fl, by = work[dname]
-    avg_ms = dms / max(dlaunch, 1)
-    t_tensor = fl / (pk["bf16_sus"] * 1e12)
-    t_hbm = by / (pk["hbm_gbs"] * 1e9)
-    traffic = recorded_traffic(wl.name, dname)
-    if t_tensor >= t_hbm:
-        achieved = fl / (avg_ms * 1e-3) / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_sus"], "traffic": traffic,
-                "peak_source": f"{pk['source']} (sustained bf16)", "avg_launch_ms": avg_ms,
-                "hbm_gbs_of_min_bytes": by / (avg_ms * 1e-3) / 1e9}
-    else:
-        achieved = by / (avg_ms * 1e-3) / 1e9
-        roof = {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
-                "avg_launch_ms": avg_ms, "tflops": fl / (avg_ms * 1e-3) / 1e12,
-                "algorithmic_bytes": by}
-    kernels = {}
-    tot = max(sum(v[0] for v in prof.values()), 1e-9)
-    for k, (kms, kl) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
-        f2, b2 = work.get(k, (0, 0))
-        a = kms / max(kl, 1)
-        kernels[k] = {"ms_per_step": kms / args.steps, "share": kms / tot,
-                      "tflops": f2 / (a * 1e-3) / 1e12 if f2 else None,
-                      "gbs_of_min_bytes": b2 / (a * 1e-3) / 1e9 if b2 else None,
-                      "bound": ("tensor" if f2 / (pk["bf16_sus"] * 1e12) >= b2 / (pk["hbm_gbs"] * 1e9) else "hbm")}
+    dname, (dms, dlaunch) = max(prof.items(), key=lambda kv: kv[1][0])
+    roof = roofline(dname, work, dms, dlaunch, pk, recorded_traffic(wl.name, dname))
+    kernels = kernel_table(prof, work, args.steps, pk)
     launches_per_label = {"permute": (10 if (wl.m_tile or wl.capacity_factor) else 4)}  # the grouping's kernels
     gpu_launches = int(sum(cnt * launches_per_label.get(k, 1) for k, (_, cnt) in prof.items()))
 
@@ -684,6 +779,13 @@ def run_ours(args, rank, world, local_rank):
         e4m3 = measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flush, stream,
                             max(3, min(args.steps, 20)), max(3, args.warmup), pk)
 
+    per_workload = None
+    if world == 1 and args.per_workload:
+        per_workload = {}
+        for name in [w for w in args.per_workload.split(",") if w and w != wl.name]:
+            per_workload[name] = measure_workload(vgg, ctx, name, max(3, min(args.steps, 10)), 3, pk, dev, flush,
+                                                  stream)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample(wl, budget_s=float(os.environ.get("VGG_CPU_BASELINE_SECONDS", "15")))
@@ -711,6 +813,7 @@ def run_ours(args, rank, world, local_rank):
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
             "activation_memory": activation_memory(buf),
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "e4m3_forward": e4m3,
+            "per_workload": per_workload,
         }
         if wl.name == "c2":
             line["baseline_note"] = ("vs_baseline divides by the pages' grouped-GEMM figure for this workload "
@@ -730,6 +833,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e4m3", action="store_true", help="skip the e4m3 gate/up forward measurement")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of the captured step graph")
+    ap.add_argument("--per-workload", default="c3,c4,c5,c5_plain",
+                    help="comma-separated further workloads timed after the main one (empty: none)")
     ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
     ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
     ap.add_argument("--profile-run", action="store_true",
@@ -741,6 +846,7 @@ def main():
         args.no_cpu_baseline = True
         args.no_e4m3 = True
         args.no_graph = True
+        args.per_workload = ""
     if args.ncu_summary:
         print(ncu_launch_summary(args.ncu_summary))
         return 0

@@ -84,6 +84,14 @@ int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns);
 /* Pair capacity for the pair-indexed arrays: T*K, plus E*m_tile/2 under token rounding. */
 long long moe_pair_capacity(int T, int E, int K, int m_tile);
 
+/*
+ * Slots per expert of the capacity dispatch (moe_permute_capacity):
+ * C = ceil(capacity_factor * T * K / E), the factor times the mean load, evaluated left to right in
+ * double precision.  [DEP] "Drop/Padding 방식" names the capacity factor but gives no formula; this
+ * is the library's reading.  Returns 0 for T, E or K below 1 or a factor that is not in (0, 1e6].
+ */
+long long moe_expert_capacity(int T, int E, int K, double capacity_factor);
+
 /* Workspace needed by moe_route / moe_permute / moe_grouped_gemm_fwd / moe_backward for these sizes. */
 size_t moe_workspace_bytes(int T, int d, int E, int n, int K, int m_tile);
 
@@ -139,7 +147,7 @@ int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, cons
  * an expert with fewer is padded to C.  policy 0 ("position") keeps the first
  * C routed tokens in token order, policy 1 ("probs") the C with the largest
  * routing probability topk_w (ties: lower token first).  Kept pairs keep their
- * top-K weight.  C is the caller's (e.g. ceil(capacity_factor * T*K/E)).
+ * top-K weight.  C is the caller's (moe_expert_capacity gives ceil(capacity_factor * T*K/E)).
  *
  * Outputs: counts[E] (kept pairs per expert), offsets[E+1] = e*C,
  * sorted_tok[cap] (token of every slot, -1 for an empty slot), sorted_w[cap]
@@ -174,6 +182,9 @@ size_t moe_capacity_workspace_bytes(int T, int d, int E, int n, int K, int C);
  * capture.  All calls share the one array: calls that overlap on the GPU (two
  * streams, or two contexts on one device) race and must be serialized by the
  * caller.  The array needs no clearing: every call rewrites what it reads.
+ * The cached address belongs to the device's primary context: a process that
+ * resets a device (cudaDeviceReset) must not call this entry point on that
+ * device afterwards.
  */
 int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K,
                         long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok, float* sorted_w,
@@ -190,9 +201,12 @@ int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const float* topk
  *   Yw[j] = sorted_w[j] * (A[j] W_down[e]^T)
  *
  * H and U are kept in fp32 (the backward's dSwiGLU reads them; both may be NULL for a
- * forward-only call, which then writes neither); A is computed
- * from the fp32 accumulators and rounded once to bf16, the operand type of the
- * down projection.  Outputs H, U [cap,n] fp32, A [cap,n] bf16, Yw [cap,d] bf16.
+ * forward-only call, which then writes neither); A is computed from the fp32
+ * accumulators and stored rounded to bf16.  The down projection takes A as that
+ * bf16 value plus the bf16 rounding of the rest (about 16 significant bits, two
+ * UMMAs per K step); the low part lives in the workspace `ws` between the two
+ * GEMMs (at least 2*cap*n bytes, 256-byte aligned; moe_workspace_bytes covers it).
+ * Outputs H, U [cap,n] fp32, A [cap,n] bf16, Yw [cap,d] bf16.
  */
 int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const void* W_up, const void* W_down,
                          int T, int d, int E, int n, long long cap, const int32_t* offsets,
@@ -260,9 +274,13 @@ int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int3
 
 /*
  * moe_backward — gradients of the layer for an upstream gradient dO[T,d].
- * [SM] "3 기여 ① 메모리 효율 알고리즘" (dS from <dA', A> instead of <dO, Y>; no
- * gathered X or dO materialised), "4.2 Epilogue 융합" (dH, dS, A' in one
- * epilogue, dSwiGLU fused), "4 기여 ②" (varlen-K grouped GEMM for dW).
+ * [SM] "3 기여 ① 메모리 효율 알고리즘" (dS from <dA', A> instead of <dO, Y>),
+ * "4.2 Epilogue 융합" (dH, dS, A' in one epilogue, dSwiGLU fused), "4 기여 ②"
+ * (varlen-K grouped GEMM for dW).  Unlike [SM] "4.1 Gather 융합", the backward
+ * writes expert-sorted copies of X and dO into the workspace once (every
+ * backward GEMM then reads whole TMA boxes); the weight-gradient GEMMs take
+ * dH, dU and A' as a bf16 high part plus the bf16 rounding of the rest (about
+ * 16 significant bits of the epilogue's fp32 values), also in the workspace.
  * With dA'[j] = dO[t] W_down[e] and w = sorted_w[j]:
  *   dS[j] = <dA'[j], A[j]>           (= <dO[t], Y[j]>, the gradient of w)
  *   dA = w dA',  dU = dA * silu(H),  dH = dA * U * s(H) (1 + H (1 - s(H)))
@@ -372,6 +390,28 @@ int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, cons
 int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, int rows_a, const void* B,
                            const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
                            const int32_t* offsets, float* D, moe_stream_t stream);
+
+/*
+ * moe_test_gemm_varlen_m_dual: the down projection's main loop with a two-part A, for each group e and
+ * sorted row j of it,
+ *   D[j, c] = sum_k (A_hi[j, k] + A_lo[j, k]) * B[e, c, k]       (B is [G, N, K], K-major)
+ * (two UMMAs per K step into one fp32 accumulator).  A_hi, A_lo [rows_a, K] bf16 with rows_a >= cap,
+ * D[cap, N] fp32; rows outside every group are left untouched.  K a multiple of 64, N of 8.
+ */
+int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, const void* B, int G, int rows_a,
+                                int K, int N, long long cap, const int32_t* offsets, float* D, moe_stream_t stream);
+
+/*
+ * moe_test_gemm_varlen_k_dual: the weight-gradient form with a two-part A, for each group e,
+ *   S[e, m, c] = sum_{j in group e} (A_hi[j, m] + A_lo[j, m]) * B[j, c]
+ * (two UMMAs per K step into one fp32 accumulator).  A_hi, A_lo [rows_a, M], B [rows_b, N] bf16;
+ * rows of B past a group's end are cleared in shared memory.  trans = 0: D[G, M, N] = S;
+ * trans = 1: D[G, N, M] with D[e, c, m] = S[e, m, c] (the transposed store of dW_down).  fp32
+ * out, zeros for an empty group; M and N multiples of 64.
+ */
+int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, int rows_a, const void* B, int rows_b,
+                                int G, int M, int N, long long cap, const int32_t* offsets, int trans, float* D,
+                                moe_stream_t stream);
 
 /* Test export: launch one CTA that waits on an mbarrier nobody arrives on, with
  * the given bound; the wait gives up, records MOE_DEV_TIMEOUT and returns. */

@@ -56,5 +56,20 @@ def test_every_profiled_label_has_work_figures(wl):
     missing = sorted(names - set(work))
     assert not missing, missing
     for k in names:
-        flops, nbytes = work[k]
-        assert flops >= 0 and (nbytes > 0 or k == "zero_tail"), k
+        flops, nbytes, moved = work[k]
+        assert flops >= 0 and (nbytes > 0 or k == "zero_tail") and moved >= nbytes, k
+
+
+def test_roofline_follows_the_byte_model():
+    """The roofline of the dominant kernel divides the byte model's algorithmic bytes (gathered rows counted
+    once per token, bf16 activations) by the launch time: dW gate/up at c2 moves 2Td + 4Pn + 4End."""
+    import bench
+    w = synth.WORKLOADS["c2"]
+    P = w.T * w.K
+    work = bench.kernel_work(w, P)
+    alg = 2 * w.T * w.d + 4 * P * w.n + 4 * w.E * w.n * w.d
+    assert work["dw_gate_up"][1] == alg
+    pk = {"hbm_gbs": 6682.8, "bf16_sus": 1737.5, "source": "measured"}
+    r = bench.roofline("dw_gate_up", work, 0.1832 * 10, 10, pk)
+    assert r["bound"] == "hbm" and abs(r["frac"] - alg / 0.1832e-3 / 1e9 / 6682.8) < 1e-12
+    assert abs(r["frac"] - 0.507) < 0.002

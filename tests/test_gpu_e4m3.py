@@ -263,7 +263,6 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
         np.testing.assert_array_equal(buf.dos[:r.P].cpu().numpy(), os_)
     if dact and buf.sorted_tok.numel() >= wl.T:  # dO quantized per token and gathered: empty rows zero, scale 1
         assert not buf.doq[r.P:].any().item() and bool((buf.dos[r.P:] == 1).all().item())
-    refs = None
     flips = 0
     if dx:
         huq = buf.huq[:r.P].cpu().numpy()
@@ -288,10 +287,12 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
                 assert np.all((a & 0x80) == (b & 0x80)) and np.all(np.abs((a & 0x7F) - (b & 0x7F)) <= 1)
             np.add.at(dX_codes, rows, mo.dequantize_rows_e4m3(huq[lo:hi], hus[lo:hi]) @ Bd[e].T)
         assert flips <= 0.01 * huq.size, flips
-        refs = {"dX": dX_codes}
-    rep = compare_layer(buf, inp, O_ref, cache, grads, refs=refs)
-    end = oracle.metrics.rel_error(buf.dX.double().cpu().numpy(), grads["dX"])
-    assert end["mean"] <= 3e-3 and end["max"] <= 0.15, end
+        # the e4m3 GEMM and the token reduction on the device's own codes: the usual bf16 tolerance
+        oracle.compare("dX (from the device's codes)", dev_to_f64(buf.dX), dX_codes)
+    rep = compare_layer(buf, inp, O_ref, cache, grads, skip=("dX",) if dx else ())
+    # against the oracle's own e4m3 backward: the variant's tolerance (one e4m3 step of a code is up to 12.5%
+    # of that element), both floors
+    end = oracle.compare("dX (e4m3 variant)", dev_to_f64(buf.dX), grads["dX"], max_rel=0.15)
     print(wl.name, "dx", dx, "dact", dact, "code flips", flips, "dX vs oracle e4m3",
           (round(end["max"], 4), round(end["mean"], 6)), {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
 
@@ -335,8 +336,7 @@ def test_e4m3_backward_capacity_layout(ctx, dx):
     oracle.compare("O", dev_to_f64(buf.O), O_ref)
     dX = dev_to_f64(buf.dX)
     if dx:
-        end = oracle.metrics.rel_error(dX, g["dX"])
-        assert end["mean"] <= 3e-3 and end["max"] <= 0.15, end
+        oracle.compare("dX (e4m3 variant)", dX, g["dX"], max_rel=0.15)
     else:
         oracle.compare("dX", dX, g["dX"])
     for name in ("dW_gate", "dW_up", "dW_down"):

@@ -55,32 +55,9 @@ def test_edge_case_layer(ctx, wl):
         return
     check_routing_bit_exact(g, wl.K, wl.m_tile)
     O_ref, cache, grads = oracle_layer(inp, g)
-    refs = None
-    if wl.name == "e1024":
-        # about 16 rows per expert: dW_down's worst rows reach 2.8e-2 against the exact gradient because its
-        # operand A' = w A is bf16 (a precision point of the method); the device is held to the same sum with
-        # A' rounded to bf16 in fp64, and to the exact gradient on average
-        from oracle import moe_oracle as mo
-        import oracle
-        r = cache["routing"]
-        dO64 = mo.bf16_bits_to_f64(inp.dO)
-        X64 = mo.bf16_bits_to_f64(inp.X)
-        emu = np.zeros((wl.E, wl.d, wl.n))
-        for e in range(wl.E):
-            lo, hi = r.offsets[e], r.offsets[e + 1]
-            if hi == lo:
-                continue
-            rows = r.sorted_tok[lo:hi]
-            _, _, a, _ = mo.expert_ffn(X64[rows], inp.W_gate[e], inp.W_up[e], inp.W_down[e])
-            emu[e] = dO64[rows].T @ mo.round_bf16(cache["w_full"][rows, e][:, None] * a)
-        exact = np.stack([grads["dW_down"][e] for e in range(wl.E)])
-        rep_exact = oracle.metrics.rel_error(buf.dW_down.double().cpu().numpy(), exact, oracle.WEIGHT_GRAD)
-        assert rep_exact["mean"] <= 3e-3, rep_exact
-        refs = {"dW_down": emu}
-    rep = compare_layer(buf, inp, O_ref, cache, grads, refs=refs)
-    if refs:
-        # the device computes that sum: equal up to A' elements that round to the other bf16 neighbour
-        assert rep["dW_down"]["max"] <= 1e-2 and rep["dW_down"]["mean"] <= 1e-5, rep["dW_down"]
+    # e1024: about 16 rows per expert, where a single bf16 rounding of the weight-gradient operands would cost
+    # up to 2.8e-2 on dW_down; the two-part operands keep every tensor within the bound of the exact gradient
+    rep = compare_layer(buf, inp, O_ref, cache, grads)
     if wl.m_tile:
         assert np.all(g["counts"] % wl.m_tile == 0)
     print(wl.name, "P", g["P"], {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})

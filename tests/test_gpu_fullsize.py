@@ -12,11 +12,13 @@ sampled outputs it computes one by one, and the rest through properties that hol
   weights regenerated from the seeded generator; sampled tokens are the first and last token, two
   tokens of the heaviest expert and 16 random ones;
 * dW of whole experts: the heaviest and the lightest non-empty expert, all of their rows;
-* dW_r = X^T dlogits, evaluated in fp64 from the device's own dlogits;
+* whole columns of dW_r = X^T dlogits (the lightest non-empty expert's and a random one), from the
+  oracle's own dlogits of every token that has a nonzero entry in the column;
 * experts that receive no pair get exactly zero weight gradients.
 
-Tolerance: the one the small parity tests use (max relative error <= 2e-2, mean <= 3e-3 against
-max(|ref|, rms of the token's row, or of the expert's whole matrix for a weight gradient)).
+Tolerance: the one the small parity tests use (max relative error <= 2e-2, mean <= 3e-3, under both the
+row floor and the tensor-wide floor of the compared set).
+The complete element-by-element comparison at c2 is in test_gpu_full_c2.py.
 """
 import gc
 
@@ -135,9 +137,22 @@ def test_fullsize_parity(ctx, name):
                 ref.append(dw_ref[i, r.sorted_exp[j]])
         rep["dS"] = oracle.compare("dS (sampled pairs)", np.array(got)[None, :], np.array(ref)[None, :])
 
-        # dW_r = X^T dlogits from the device's own dlogits, in fp64
-        ref_wr = (dev["X"].double().t() @ buf.dlogits.double()).cpu().numpy()
-        rep["dW_r"] = oracle.compare("dW_r (= X^T dlogits)", dev_to_f64(buf.dW_r), ref_wr)
+        # whole columns of dW_r = X^T dlogits, from the oracle's own dlogits of every token whose row of dlogits
+        # is nonzero in that column (the tokens routed to the expert or holding it in their top-K): the
+        # lightest non-empty expert and one drawn at random
+        routed = np.zeros((wl.T, wl.E), dtype=bool)
+        routed[np.arange(wl.T)[:, None], r.topk_ids] = True
+        cols = sorted({lightest, int(rng.integers(wl.E))})
+        ref_cols = []
+        for e in cols:
+            tk = np.nonzero(r.member[:, e] | routed[:, e])[0].astype(np.int64)
+            if len(tk) == 0:
+                ref_cols.append(np.zeros(wl.d))
+                continue
+            _, _, dL_e, _ = _token_oracle(wl, r, tk, W_r_bits, bias)
+            ref_cols.append(mo.bf16_bits_to_f64(synth.make_x(wl, rows=tk)).T @ dL_e[:, e])
+        got_cols = dev_to_f64(buf.dW_r[:, torch.tensor(cols, device="cuda")]).T
+        rep["dW_r"] = oracle.compare(f"dW_r columns {cols}", got_cols, np.stack(ref_cols))
 
         for e in sorted({heavy, lightest}):
             dWg, dWu, dWd = _expert_dw_oracle(wl, r, e, W_r_bits, bias)

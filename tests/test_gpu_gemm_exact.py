@@ -1,7 +1,8 @@
 """Grouped-GEMM main loops on integer-valued bf16 operands: every product and partial sum is an
 integer below 2^24, so fp32 accumulation is exact in any order and the device result must equal the
 int64 reference bit for bit.  This pins the gather, the varlen bookkeeping (empty, one-row and
-ragged groups, ragged N), both operand layouts (K-major and MN-major) and the bounded wait."""
+ragged groups, ragged N), both operand layouts (K-major and MN-major), the two-part A operand and
+transposed store of the weight-gradient GEMMs, and the bounded wait."""
 import numpy as np
 import pytest
 import torch
@@ -84,6 +85,59 @@ def test_varlen_k_exact(ctx, sizes, M, N, gathered):
         ra = idx[rows] if gathered == "a" else rows
         rb = idx[rows] if gathered == "b" else rows
         np.testing.assert_array_equal(got[e], (A[ra].T @ B[rb]).astype(np.float32), err_msg=f"group {e}")
+
+
+@pytest.mark.parametrize("sizes,K,N", [([0, 1, 130, 257, 64], 192, 200), ([300], 64, 512), ([5, 0, 0, 129], 128, 264)])
+def test_varlen_m_dual_exact(ctx, sizes, K, N):
+    """The down projection's form: per sorted row, (A_hi + A_lo) B[e]^T with two UMMAs per K step into one
+    accumulator; A_lo holds small integers times 2^-8 so that a dropped or misplaced low-part product shows."""
+    import varlen_grouped_gemm_gb300 as vgg
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(offsets[-1])
+    cap = P + 7
+    A_hi = _ints((cap, K), -2, 2, 11).astype(np.float64)
+    A_lo = _ints((cap, K), -3, 3, 12).astype(np.float64) / 256.0
+    B = _ints((G, N, K), -1, 1, 13).astype(np.float64)
+    D = torch.full((cap, N), -7.0, device="cuda")
+    vgg.moe_test_gemm_varlen_m_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(B), torch.from_numpy(offsets).cuda(), D)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == 0 and code == 0
+    got = D.cpu().numpy()
+    for e in range(G):
+        lo, hi = offsets[e], offsets[e + 1]
+        ref = ((A_hi[lo:hi] + A_lo[lo:hi]) @ B[e].T).astype(np.float32)
+        np.testing.assert_array_equal(got[lo:hi], ref, err_msg=f"group {e}")
+    assert np.all(got[P:] == -7.0), "rows outside every group must stay untouched"
+
+
+@pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 192), ([1, 0, 333], 128, 256), ([70], 64, 320),
+                                         ([17] * 9 + [0, 130], 320, 512)])
+@pytest.mark.parametrize("trans", [False, True])
+def test_varlen_k_dual_exact(ctx, sizes, M, N, trans):
+    """The weight-gradient form: per group, (A_hi + A_lo)^T B over the group's rows, two UMMAs per K step into
+    one accumulator; B's rows past a group's end are cleared in shared memory.  A_lo holds small integers
+    times 2^-8 (exact in bf16) so that a dropped or misplaced low-part product changes the result.  With
+    trans the tile leaves through transposed 32 x 32 blocks: D[e] is the transpose."""
+    import varlen_grouped_gemm_gb300 as vgg
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(offsets[-1])
+    cap = P + 3
+    A_hi = _ints((cap, M), -2, 2, 7).astype(np.float64)
+    A_lo = _ints((cap, M), -3, 3, 8).astype(np.float64) / 256.0
+    B = _ints((cap, N), -2, 2, 9).astype(np.float64)
+    shape = (G, N, M) if trans else (G, M, N)
+    D = torch.full(shape, 3.0, device="cuda")
+    vgg.moe_test_gemm_varlen_k_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(B), torch.from_numpy(offsets).cuda(), D, cap,
+                                    trans=trans)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == 0 and code == 0
+    got = D.cpu().numpy()
+    for e in range(G):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        ref = ((A_hi[rows] + A_lo[rows]).T @ B[rows]).astype(np.float32)  # multiples of 2^-8 below 2^15: exact
+        np.testing.assert_array_equal(got[e], ref.T if trans else ref, err_msg=f"group {e}")
 
 
 def test_bounded_wait_times_out_and_context_survives(ctx):

@@ -47,6 +47,22 @@ def test_host_only_queries(libpath):
     assert vgg.status_str(vgg.MOE_ERR_INVALID_ARG) == "invalid argument"
 
 
+def test_expert_capacity_matches_the_oracle(libpath):
+    """The capacity dispatch's slot count C = ceil(cf T K / E) comes from the library (the binding does no
+    arithmetic); it equals the oracle's reading on a grid that includes exact multiples and fractions."""
+    import varlen_grouped_gemm_gb300 as vgg
+    from oracle import moe_oracle as mo
+    for T in (1, 5, 10, 4096, 8192, 65536):
+        for E in (3, 4, 8, 128, 512):
+            for K in (1, 2, 8):
+                for cf in (0.5, 1.0, 1.25, 2.0, 1.0 / 3.0, 0.1):
+                    assert vgg.expert_capacity(T, E, K, cf) == mo.expert_capacity(T, E, K, cf), (T, E, K, cf)
+    assert vgg.lib().moe_expert_capacity(4096, 128, 8, 1.0) == 256
+    for bad in ((0, 8, 2, 1.0), (16, 0, 2, 1.0), (16, 8, 0, 1.0), (16, 8, 2, 0.0), (16, 8, 2, -1.0),
+                (16, 8, 2, float("nan"))):
+        assert vgg.lib().moe_expert_capacity(*bad) == 0, bad
+
+
 def test_argument_errors_are_reported_without_a_device(libpath):
     lib = ctypes.CDLL(libpath)
     lib.moe_route.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 5 + \
@@ -59,7 +75,8 @@ def test_argument_errors_are_reported_without_a_device(libpath):
 _CTX_ENTRIES = ["moe_route", "moe_permute", "moe_grouped_gemm_fwd", "moe_combine", "moe_backward",
                 "moe_permute_noalloc", "moe_permute_capacity", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
                 "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
-                "moe_test_gemm_varlen_m", "moe_test_gemm_varlen_k"]
+                "moe_test_gemm_varlen_m", "moe_test_gemm_varlen_k", "moe_test_gemm_varlen_k_dual",
+                "moe_test_gemm_varlen_m_dual"]
 
 
 @pytest.mark.parametrize("name", _CTX_ENTRIES)

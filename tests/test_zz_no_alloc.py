@@ -50,6 +50,45 @@ def test_noalloc_permute_matches_permute(wl):
             assert torch.equal(got[k], ref[k]), (call, k)
 
 
+def _route(vgg, ctx, wl, permute_experts=None):
+    X = torch.from_numpy(synth.make_x(wl).view(np.int16)).view(torch.bfloat16).cuda()
+    W_r = torch.from_numpy(synth.make_router(wl).view(np.int16)).view(torch.bfloat16).cuda()
+    if permute_experts is not None:  # a different routing of the same shape: the router's columns shuffled
+        W_r = W_r[:, torch.from_numpy(permute_experts).cuda()].contiguous()
+    logits = torch.empty((wl.T, wl.E), device="cuda")
+    ids = torch.empty((wl.T, wl.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.T, wl.K), device="cuda")
+    vgg.moe_route(ctx, X, W_r, None, wl.K, logits, None, ids, w)
+    return ids, w
+
+
+def test_noalloc_after_a_larger_call():
+    """The array keeps the previous call's contents: a call at the largest size (T = 32768, E = 512) leaves
+    every count slot written, then smaller, differently routed calls must still equal moe_permute."""
+    import varlen_grouped_gemm_gb300 as vgg
+    ctx = vgg.Context(0)
+    big = synth.scaled(synth.WORKLOADS["c5_plain"], name="noalloc_big", T=32768, d=128, n=64)
+    ids, w = _route(vgg, ctx, big)
+    st = _state(vgg, big.T, big.E, big.K)
+    vgg.moe_permute_noalloc(ctx, ids, w, big.E, st["counts"], st["offsets"], st["sorted_tok"], st["sorted_w"],
+                            st["tok_ptr"], st["tok_pairs"], st["P"])
+    assert vgg.moe_get_error(ctx) == (0, 0)
+    small = synth.scaled(synth.WORKLOADS["c2"], name="noalloc_small", T=777, d=128, E=64, K=4)
+    for perm_seed in (1, 2):
+        ids, w = _route(vgg, ctx, small, np.random.default_rng(perm_seed).permutation(small.E))
+        ref = _state(vgg, small.T, small.E, small.K)
+        ws = torch.empty(vgg.moe_workspace_bytes(small.T, small.d, small.E, small.n, small.K, 0), dtype=torch.uint8,
+                         device="cuda")
+        vgg.moe_permute(ctx, ids, w, None, None, small.E, 0, ref["counts"], ref["offsets"], ref["sorted_tok"],
+                        ref["sorted_w"], ref["tok_ptr"], ref["tok_pairs"], ref["P"], ws)
+        got = _state(vgg, small.T, small.E, small.K)
+        vgg.moe_permute_noalloc(ctx, ids, w, small.E, got["counts"], got["offsets"], got["sorted_tok"],
+                                got["sorted_w"], got["tok_ptr"], got["tok_pairs"], got["P"])
+        assert vgg.moe_get_error(ctx) == (0, 0)
+        for k in ref:
+            assert torch.equal(got[k], ref[k]), (perm_seed, k)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     import varlen_grouped_gemm_gb300 as vgg
     ctx = vgg.Context(0)

@@ -29,6 +29,7 @@ EXPORTS = (
     "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc", "moe_permute_capacity",
     "moe_capacity_workspace_bytes", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
     "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
+    "moe_expert_capacity", "moe_test_gemm_varlen_k_dual", "moe_test_gemm_varlen_m_dual",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -69,6 +70,10 @@ def lib() -> ctypes.CDLL:
         L.moe_test_gemm_varlen_m.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_test_gemm_varlen_k.argtypes = [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_test_wait_timeout.argtypes = [_P, ctypes.c_ulonglong, _P]
+        L.moe_expert_capacity.argtypes = [_I, _I, _I, ctypes.c_double]
+        L.moe_expert_capacity.restype = _LL
+        L.moe_test_gemm_varlen_k_dual.argtypes = [_P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _P, _I, _P, _P]
+        L.moe_test_gemm_varlen_m_dual.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_permute_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_permute_capacity.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                            _P]
@@ -218,9 +223,11 @@ POLICIES = {"position": 0, "probs": 1}
 
 
 def expert_capacity(T: int, E: int, K: int, capacity_factor: float) -> int:
-    """Slots per expert of the capacity dispatch: ceil(capacity_factor * T * K / E)."""
-    import math
-    return int(math.ceil(capacity_factor * T * K / E))
+    """Slots per expert of the capacity dispatch (the library's moe_expert_capacity)."""
+    C = int(lib().moe_expert_capacity(T, E, K, float(capacity_factor)))
+    if C < 1:
+        raise ValueError(f"moe_expert_capacity: invalid arguments T={T} E={E} K={K} cf={capacity_factor}")
+    return C
 
 
 def moe_permute_capacity(ctx, topk_ids, topk_w, E, C, policy, counts, offsets, sorted_tok, sorted_w, tok_ptr,
@@ -357,6 +364,25 @@ def moe_test_gemm_varlen_k(ctx, A, idx_a, B, idx_b, offsets, D, cap, stream=None
     _check("moe_test_gemm_varlen_k", lib().moe_test_gemm_varlen_k(
         ctx.handle, _ptr(A, torch.bfloat16), _ptr(idx_a, torch.int32), A.shape[0], _ptr(B, torch.bfloat16),
         _ptr(idx_b, torch.int32), B.shape[0], G, M, N, cap, _ptr(offsets, torch.int32), _ptr(D, torch.float32),
+        _stream(stream)))
+
+
+def moe_test_gemm_varlen_m_dual(ctx, A_hi, A_lo, B, offsets, D, stream=None):
+    """Test export: per group and sorted row, (A_hi + A_lo) B[e]^T (B is [G, N, K]); D is [cap, N] fp32."""
+    G, N, K = B.shape
+    _check("moe_test_gemm_varlen_m_dual", lib().moe_test_gemm_varlen_m_dual(
+        ctx.handle, _ptr(A_hi, torch.bfloat16), _ptr(A_lo, torch.bfloat16), _ptr(B, torch.bfloat16), G,
+        A_hi.shape[0], K, N, D.shape[0], _ptr(offsets, torch.int32), _ptr(D, torch.float32), _stream(stream)))
+
+
+def moe_test_gemm_varlen_k_dual(ctx, A_hi, A_lo, B, offsets, D, cap, trans=False, stream=None):
+    """Test export: per group, (A_hi + A_lo)^T B over the group's rows (D [G, M, N], or [G, N, M] with trans)."""
+    G = D.shape[0]
+    M = A_hi.shape[1]
+    N = B.shape[1]
+    _check("moe_test_gemm_varlen_k_dual", lib().moe_test_gemm_varlen_k_dual(
+        ctx.handle, _ptr(A_hi, torch.bfloat16), _ptr(A_lo, torch.bfloat16), A_hi.shape[0], _ptr(B, torch.bfloat16),
+        B.shape[0], G, M, N, cap, _ptr(offsets, torch.int32), int(bool(trans)), _ptr(D, torch.float32),
         _stream(stream)))
 
 

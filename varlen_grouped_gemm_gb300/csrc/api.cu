@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -144,6 +145,7 @@ constexpr int kMaxSplitK = 16;
 
 struct BwdWs {
   __nv_bfloat16 *dH, *dU, *Ap, *dXp, *WrT, *Xs, *dOs;
+  __nv_bfloat16 *dH_lo, *dU_lo, *Ap_lo;  // bf16 rounding of what dH, dU, A' leave of the fp32 values
   __nv_bfloat16* dL;  // [2][Tp][E], Tp = T rounded up to 64: dlogits as a bf16 high part and the bf16
                       // rounding of the rest; rows [T, Tp) of both halves are zero
   float* part;
@@ -152,10 +154,16 @@ struct BwdWs {
 
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
   const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
-  return 3 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
+  return 6 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
          al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(ceil_div(T, 64)) * 64 * E) +
          al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
          al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
+}
+
+// Store maps of the dSwiGLU epilogue's low parts (o3..o5), like those of dH, dU, A'.
+bool make_lo_maps(Maps& m, const BwdWs& w, int n, long long cap) {
+  return make_store_map_2d(&m.o3, w.dH_lo, false, n, cap, n, 32) && make_store_map_2d(&m.o4, w.dU_lo, false, n, cap, n, 32) &&
+         make_store_map_2d(&m.o5, w.Ap_lo, false, n, cap, n, 32);
 }
 
 BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
@@ -170,6 +178,9 @@ BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
   w.dH = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.dU = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.Ap = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.dH_lo = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.dU_lo = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
+  w.Ap_lo = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.dXp = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
   w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
@@ -272,9 +283,10 @@ using namespace vgg;
     if (e_ != cudaSuccess) return MOE_ERR_CUDA;   \
   } while (0)
 
-// Down projection of the sorted activation rows A, each row scaled by its combine weight (Yw).
-static int down_projection(moe_ctx* ctx, const void* A, const void* W_down, int d, int E, int n, long long cap,
-                           const int32_t* offsets, const float* sorted_w, void* Yw, cudaStream_t s) {
+// Down projection of the sorted activation rows A, each row scaled by its combine weight (Yw).  With A_lo
+// (the bf16 rounding of what A's bf16 value leaves of the fp32 activation) the GEMM takes A as two parts.
+static int down_projection(moe_ctx* ctx, const void* A, const void* A_lo, const void* W_down, int d, int E, int n,
+                           long long cap, const int32_t* offsets, const float* sorted_w, void* Yw, cudaStream_t s) {
   GemmParams p = base_params(ctx);
   p.N = d;
   p.K = n;
@@ -287,12 +299,37 @@ static int down_projection(moe_ctx* ctx, const void* A, const void* W_down, int 
   const int BN = gemm_bn(d);
   Maps m = zero_maps();
   if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
-      !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
+      !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64) || (A_lo && !make_map_2d(&m.a2, A_lo, n, cap, n, BM)))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
+  m.a3 = m.a2;
   m.b1 = m.b0;
   const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-  VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  if (A_lo) VGG_LAUNCH("down_scale", run_down_scale_dual(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  else VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  return MOE_OK;
+}
+
+// The plain grouping of moe_permute (m_tile = 0) with its hist / block-base scratch taken from `scratch`
+// (scratch_ints ints) instead of a workspace: the same argument checks and launch as moe_permute.
+int vgg::permute_plain_with_scratch(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K,
+                                    long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
+                                    float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
+                                    int32_t* scratch, long long scratch_ints, cudaStream_t s) {
+  VGG_REQUIRE(ctx && topk_ids && topk_w && counts && offsets && sorted_tok && sorted_w && tok_ptr && tok_pairs &&
+              scratch);
+  VGG_REQUIRE(shapes_ok(T, 64, E, 64, K));
+  VGG_REQUIRE(cap >= moe_pair_capacity(T, E, K, 0) && cap < INT_MAX);
+  const int tb = perm_tok_block(T, E);
+  const int nb = (T + tb - 1) / tb;
+  if (static_cast<long long>(E + 1) * nb + 1 > scratch_ints) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  PermuteWs w{};
+  w.hist = scratch;
+  w.tokblk = scratch + static_cast<long long>(E) * nb;
+  VGG_LAUNCH("permute", launch_permute(topk_ids, topk_w, nullptr, nullptr, T, E, K, 0, cap, counts, offsets,
+                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
   return MOE_OK;
 }
 
@@ -381,6 +418,12 @@ long long moe_pair_capacity(int T, int E, int K, int m_tile) {
   long long cap = static_cast<long long>(T) * K;
   if (m_tile > 0) cap += static_cast<long long>(E) * (m_tile / 2);
   return cap;
+}
+
+long long moe_expert_capacity(int T, int E, int K, double capacity_factor) {
+  if (T < 1 || E < 1 || K < 1 || !(capacity_factor > 0.0) || capacity_factor > 1e6) return 0;
+  // the factor times the mean load T K / E, evaluated left to right in double, rounded up
+  return static_cast<long long>(std::ceil(capacity_factor * T * K / E));
 }
 
 size_t moe_workspace_bytes(int T, int d, int E, int n, int K, int m_tile) {
@@ -481,17 +524,19 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
                          int T, int d, int E, int n, long long cap, const int32_t* offsets,
                          const int32_t* sorted_tok, const float* sorted_w, void* H, void* U, void* A, void* Yw,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
-  VGG_REQUIRE(ctx && X && W_gate && W_up && W_down && offsets && sorted_tok && sorted_w && A && Yw);
+  VGG_REQUIRE(ctx && X && W_gate && W_up && W_down && offsets && sorted_tok && sorted_w && A && Yw && ws);
   VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
   VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
+  // the workspace holds A's low part between the two GEMMs
+  VGG_REQUIRE(ws_bytes >= sizeof(__nv_bfloat16) * static_cast<size_t>(cap) * n);
+  VGG_REQUIRE((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) == 0);
   VGG_REQUIRE(aligned16(X) && aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(H) &&
               aligned16(U) && aligned16(A) && aligned16(Yw));
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* A_lo = ws;
   // gate/up + SwiGLU: A = X rows gathered by sorted_tok, B = the W_gate / W_up pair
   {
     GemmParams p = base_params(ctx);
@@ -507,19 +552,20 @@ int moe_grouped_gemm_fwd(moe_ctx* ctx, const void* X, const void* W_gate, const 
     p.out0 = H;
     p.out1 = U;
     p.out2 = A;
+    p.out3 = A_lo;
     p.ld_out = n;
     const int BN = n > 64 ? 256 : 128;
     Maps m = zero_maps();
     if (!make_map_3d(&m.b0, W_gate, d, n, E, BN / 2) || !make_map_3d(&m.b1, W_up, d, n, E, BN / 2) ||
         (H && (!make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32))) ||
-        !make_store_map_2d(&m.o2, A, false, n, cap, n, 32))
+        !make_store_map_2d(&m.o2, A, false, n, cap, n, 32) || !make_store_map_2d(&m.o3, A_lo, false, n, cap, n, 32))
       return MOE_ERR_CUDA;
     const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN / 2);
     // pairs of CTAs on neighbouring column tiles share the gathered X rows (each gathers half)
     const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
     VGG_LAUNCH("gate_up_swiglu", run_gate_up_swiglu(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
+  return down_projection(ctx, A, A_lo, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
 }
 
 int moe_quantize_rows_e4m3(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, float* scales,
@@ -585,7 +631,7 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
     const int cn = ceil_div(n, BN / 2) >= 2 ? 2 : 1;
     VGG_LAUNCH("gate_up_swiglu_e4m3", run_gate_up_swiglu_e4m3(BN, cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  if (!down8) return down_projection(ctx, A, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
+  if (!down8) return down_projection(ctx, A, nullptr, W_down, d, E, n, cap, offsets, sorted_w, Yw, s);
   // A's rows (those below offsets[E]) to e4m3, then the e4m3 down projection
   VGG_LAUNCH("quantize_a_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(A), cap, offsets + E, n,
                                                           static_cast<uint8_t*>(Aq), a_scale, s));
@@ -657,8 +703,10 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   const bool f32 = dW_fp32 != 0;
   const int bn6 = gemm_bn(n);
   const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
-  if (cap > static_cast<long long>(T) * K)
+  if (cap > static_cast<long long>(T) * K) {
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
+    VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH_lo, w.dU_lo, w.Ap_lo, s));
+  }
   // e4m3 dSwiGLU GEMM: dO quantized once per token (a token's pairs share its row, so its codes are those of
   // every pair) into the dX partials' region, which is free until the dX GEMM; the gather below copies the
   // code rows and scales to the sorted positions.  When that region is too small (a capacity layout with
@@ -696,6 +744,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dH;
     p.out1 = w.dU;
     p.out2 = w.Ap;
+    p.out3 = w.dH_lo;
+    p.out4 = w.dU_lo;
+    p.out5 = w.Ap_lo;
     p.ld_out = n;
     p.row_scale = sorted_w;
     p.part = w.part;
@@ -706,7 +757,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, Wdt_q, d / 2, n, E, bn6) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32))
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -725,6 +776,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dH;
     p.out1 = w.dU;
     p.out2 = w.Ap;
+    p.out3 = w.dH_lo;
+    p.out4 = w.dU_lo;
+    p.out5 = w.Ap_lo;
     p.ld_out = n;
     p.row_scale = sorted_w;
     p.part = w.part;
@@ -732,7 +786,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dOs, d, cap, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32))
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -824,7 +878,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
     VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
   }
-  // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok]
+  // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok], with [dH | dU] as high and low
+  // bf16 parts (about 16 significant bits of the fp32 gradients)
   {
     GemmParams p = base_params(ctx);
     p.M = 2 * n;
@@ -841,33 +896,37 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     const int BN = gemm_bn(d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
+        !make_map_2d(&m.a2, w.dH_lo, n, cap, n, 64) || !make_map_2d(&m.a3, w.dU_lo, n, cap, n, 64) ||
         !make_chunked_map_2d(&m.b0, w.Xs, d, cap, BN / 64) || !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) ||
         !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
       return MOE_ERR_CUDA;
     m.b1 = m.b0;
     const int tiles = E * ceil_div(2 * n, BM) * ceil_div(d, BN);
-    VGG_LAUNCH("dw_gate_up", run_dw_tiled(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_gate_up", run_dw_dual(BN, f32, false, p, m, std::min(tiles, ctx->num_sms), s));
   }
-  // dW_down[e] = (w dO[tok])^T A  (the weight is folded into A')
+  // dW_down[e] = dO[tok]^T A' (the combine weight is folded into A' = w A), computed as its transpose
+  // A'^T dO[tok] with A' as high and low bf16 parts (tile rows = columns of dW_down) and stored through
+  // transposed blocks
   {
     GemmParams p = base_params(ctx);
-    p.M = d;
-    p.N = n;
+    p.M = n;
+    p.N = d;
     p.groups = E;
     p.offsets = offsets;
     p.rows_cap = static_cast<int>(cap);
     p.out0 = dW_down;
     p.ld_out = n;
-    const int BN = gemm_bn(n);
+    const int BN = gemm_bn(d);
     Maps m = zero_maps();
     p.b_chunked = 1;
-    if (!make_map_2d(&m.a0, w.dOs, d, cap, d, 64) || !make_chunked_map_2d(&m.b0, w.Ap, n, cap, BN / 64) ||
-        !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 64))
+    if (!make_map_2d(&m.a0, w.Ap, n, cap, n, 64) || !make_map_2d(&m.a2, w.Ap_lo, n, cap, n, 64) ||
+        !make_chunked_map_2d(&m.b0, w.dOs, d, cap, BN / 64) || !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
+    m.a3 = m.a2;
     m.b1 = m.b0;
-    const int tiles = E * ceil_div(d, BM) * ceil_div(n, BN);
-    VGG_LAUNCH("dw_down", run_dw_tiled(BN, f32, p, m, std::min(tiles, ctx->num_sms), s));
+    const int tiles = E * ceil_div(n, BM) * ceil_div(d, BN);
+    VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;
 }
@@ -970,6 +1029,33 @@ int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, cons
                                 static_cast<cudaStream_t>(stream)));
 }
 
+int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, const void* B, int G, int rows_a,
+                                int K, int N, long long cap, const int32_t* offsets, float* D, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && A_hi && A_lo && B && offsets && D);
+  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && rows_a >= 1 && K >= 64 && K % 64 == 0 && N >= 8 && N % 8 == 0);
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX && rows_a >= cap && aligned16(A_hi) && aligned16(A_lo) && aligned16(B) &&
+              aligned16(D));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  GemmParams p = base_params(ctx);
+  p.N = N;
+  p.K = K;
+  p.groups = G;
+  p.offsets = offsets;
+  p.rows_cap = static_cast<int>(cap);
+  p.out0 = D;
+  p.ld_out = N;
+  Maps m = zero_maps();
+  if (!make_map_2d(&m.a0, A_hi, K, rows_a, K, BM) || !make_map_2d(&m.a2, A_lo, K, rows_a, K, BM) ||
+      !make_map_3d(&m.b0, B, K, N, G, 256) || !make_store_map_2d(&m.o0, D, true, N, cap, N, 32))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.a3 = m.a2;
+  m.b1 = m.b0;
+  const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 256);
+  return cuda_status(run_test_m_dual(p, m, std::min(tiles, ctx->num_sms), static_cast<cudaStream_t>(stream)));
+}
+
 int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, int rows_a, const void* B,
                            const int32_t* idx_b, int rows_b, int G, int M, int N, long long cap,
                            const int32_t* offsets, float* D, moe_stream_t stream) {
@@ -1010,6 +1096,38 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
   if (idx_b) return cuda_status(run_dw_gate_up(BN, true, p, m, grid, s));
   if (idx_a) return cuda_status(run_dw_down(BN, true, p, m, grid, s));
   return cuda_status(run_dw_tiled(BN, true, p, m, grid, s));
+}
+
+int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, int rows_a, const void* B, int rows_b,
+                                int G, int M, int N, long long cap, const int32_t* offsets, int trans, float* D,
+                                moe_stream_t stream) {
+  VGG_REQUIRE(ctx && A_hi && A_lo && B && offsets && D);
+  VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 64 && M % 64 == 0 && N >= 64 && N % 64 == 0 && rows_a >= 1 &&
+              rows_b >= 1);
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX && aligned16(A_hi) && aligned16(A_lo) && aligned16(B) && aligned16(D));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  GemmParams p = base_params(ctx);
+  p.M = M;
+  p.N = N;
+  p.groups = G;
+  p.offsets = offsets;
+  p.rows_cap = static_cast<int>(cap);
+  p.b_chunked = 1;
+  p.out0 = D;
+  p.ld_out = N;
+  const int BN = gemm_bn(N);
+  Maps m = zero_maps();
+  if (!make_map_2d(&m.a0, A_hi, M, rows_a, M, 64) || !make_map_2d(&m.a2, A_lo, M, rows_a, M, 64) ||
+      !make_chunked_map_2d(&m.b0, B, N, rows_b, BN / 64) ||
+      !(trans ? make_store_map_3d(&m.o0, D, true, M, N, G, 32) : make_store_map_3d(&m.o0, D, true, N, M, G, 32)))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.a3 = m.a2;
+  m.b1 = m.b0;
+  const int tiles = G * ceil_div(M, BM) * ceil_div(N, BN);
+  return cuda_status(run_dw_dual(BN, true, trans != 0, p, m, std::min(tiles, ctx->num_sms),
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 int moe_profile_enable(moe_ctx* ctx, int enable) {

@@ -57,6 +57,16 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 // epilogues of the e4m3 form (operands are e4m3 codes of per-row-scaled rows; the accumulator is
 // multiplied by the A row's scale and the output channel's scale first).
 // EPI_DSWIGLU_Q: the dSwiGLU epilogue of the e4m3 form (the accumulator times q_row[row] q_col[column]).
+// Extra forms (bit flags):
+//   X_DUAL_A  the A operand arrives as a bf16 high part (maps a0/a1) and the bf16 rounding of the rest
+//             (maps a2/a3, the same coordinates); every K step issues two UMMAs into one accumulator, so
+//             the product carries about 16 significant bits of A.  The weight-gradient GEMMs take the
+//             per-pair gradients (fp32 in the dSwiGLU epilogue) this way, the down projection the
+//             activations A (fp32 in the SwiGLU epilogue).
+//   X_TRANS   varlen-K plain store of the transposed tile: the tile's rows (TMEM lanes) are output
+//             columns, its accumulator columns output rows; each 32 x 32 block is transposed while it is
+//             staged for the TMA store.
+enum XFlags { X_DUAL_A = 1, X_TRANS = 2 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
   EPI_DSWIGLU_Q = 7
@@ -86,6 +96,9 @@ struct GemmParams {
   void* out0;  // direct-store pointers (used for a partially filled 32-row block)
   void* out1;
   void* out2;
+  void* out3;  // dSwiGLU: bf16 low parts of dH, dU, A' (NULL: not written)
+  void* out4;
+  void* out5;
   long long ld_out;
   int out_rows_split;  // VAR_K: output rows >= split go to the second output at row - split
   const float* row_scale;  // VAR_M: per sorted row (combine weight); e4m3 SwiGLU: per source row of A
@@ -111,15 +124,17 @@ __device__ __forceinline__ void umma_step(uint32_t d_tmem, uint64_t adesc, uint6
   else umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
 }
 
-// Tensor maps: a0/a1 and b0/b1 feed the operands, o0..o2 are the TMA-store targets.
+// Tensor maps: a0/a1 and b0/b1 feed the operands (a2/a3: the low parts of a dual A), o0..o5 are the
+// TMA-store targets.
 struct Maps {
-  CUtensorMap a0, a1, b0, b1, o0, o1, o2;
+  CUtensorMap a0, a1, a2, a3, b0, b1, o0, o1, o2, o3, o4, o5;
 };
 
-// EW epilogue warps with DEPTH staged stores each.
-template <int BN, int STAGES, int EW, int DEPTH>
+// EW epilogue warps with DEPTH staged stores each; NA A tiles per stage (2: high and low parts).
+template <int BN, int STAGES, int EW, int DEPTH, int NA = 1>
 struct SmemLayout {
-  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kA1Bytes = BM * BK * 2;
+  static constexpr int kABytes = NA * kA1Bytes;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStgOffset = STAGES * kStageBytes;
@@ -375,11 +390,14 @@ struct WarpPlan {
   static constexpr int kThreads = (kBase + kNP - 1) * 32;
 };
 
-template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1>
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1,
+          int XF = 0>
 __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
   using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN>;
-  using L = SmemLayout<BN, STAGES, EW, DEPTH>;
+  constexpr bool kDual = (XF & X_DUAL_A) != 0;
+  constexpr bool kTrans = (XF & X_TRANS) != 0;
+  using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1>;
   static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_Q) || BMODE == B_TMA_K3_GU,
@@ -392,6 +410,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
                          VAR == VAR_M),
                 "e4m3 form: K-major operands, varlen-M");
+  static_assert(!kDual || ((AMODE == A_TMA_MN || AMODE == A_TMA_K) && !kF8), "dual A: a tiled bf16 A");
+  static_assert(!kTrans || (VAR == VAR_K && EPI == EPI_STORE), "transposed store: varlen-K plain epilogue");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
   constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_GATHER_MN);
   constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
@@ -532,15 +552,26 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           const int kc = kg < p.a_ksplit ? kg : kg - p.a_ksplit;
           if (l2) tma_prefetch_l2_2d(mp_a, kc, row);
           else tma_load_2d(sa, mp_a, bar, kc, row);
+          if (kDual) {  // the low part, same coordinates, into the stage's second A tile
+            const CUtensorMap* mp_l = kg < p.a_ksplit ? &mp.a2 : &mp.a3;
+            if (l2) tma_prefetch_l2_2d(mp_l, kc, row);
+            else tma_load_2d(sa + L::kA1Bytes, mp_l, bar, kc, row);
+          }
         } else if (AMODE == A_TMA_MN) {
 #pragma unroll
           for (int c = 0; c < BM / 64; ++c) {
             const int col = x.m0 + 64 * c;
-            const CUtensorMap* mp_a = col < p.a_colsplit ? &mp.a0 : &mp.a1;
-            const int cc = col < p.a_colsplit ? col : col - p.a_colsplit;
+            const bool first = col < p.a_colsplit;
+            const CUtensorMap* mp_a = first ? &mp.a0 : &mp.a1;
+            const int cc = first ? col : col - p.a_colsplit;
             const int ka = kg >= p.a_kwrap ? kg - p.a_kwrap : kg;
             if (l2) tma_prefetch_l2_2d(mp_a, cc, ka);
             else tma_load_2d(sa + c * (BK * 128), mp_a, bar, cc, ka);
+            if (kDual) {  // the low part, same coordinates, into the stage's second A tile
+              const CUtensorMap* mp_l = first ? &mp.a2 : &mp.a3;
+              if (l2) tma_prefetch_l2_2d(mp_l, cc, ka);
+              else tma_load_2d(sa + L::kA1Bytes + c * (BK * 128), mp_l, bar, cc, ka);
+            }
           }
         }
         if (BMODE == B_TMA_K3) {
@@ -795,6 +826,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
               const uint64_t bd =
                   kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
               umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+              if (kDual)  // the low part of A times the same B, into the same accumulator
+                umma_step<kF8>(d_tmem,
+                               kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
+                                    : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024),
+                               bd, kIdesc, 1u);
             }
             if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
             else umma_commit(&empty_bar[s]);
@@ -857,6 +893,12 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             const uint64_t ad = kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+            // dual A: the low part times the same B, into the same accumulator
+            if (kDual)
+              umma_step<kF8>(d_tmem,
+                             kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
+                                  : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024),
+                             bd, kIdesc, 1u);
           }
           if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
           else umma_commit(&empty_bar[s]);
@@ -949,6 +991,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
         const long long roff = orow * p.ld_out;
         const OutRef o0{&mp.o0, p.out0, roff, crow, -1}, o1{&mp.o1, p.out1, roff, crow, -1},
             o2{&mp.o2, p.out2, roff, crow, -1};
+        const OutRef o3{&mp.o3, p.out3, roff, crow, -1}, o4{&mp.o4, p.out4, roff, crow, -1},
+            o5{&mp.o5, p.out5, roff, crow, -1};
         if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_Q) {
           // columns [0, BN/2) hold h, [BN/2, BN) hold u of the same output columns
           constexpr int kHalf = (EW == 8) ? BN / 4 : BN / 2;
@@ -989,6 +1033,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = h[i] * sigmoidf_(h[i]) * u[i];  // A, in place of h
             emit32(o2, h, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
+            if (p.out3) {  // and the bf16 rounding of what A's bf16 value leaves (the down projection's low part)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] -= bf16_round(h[i]);
+              emit32(o3, h, col, ncols, full, row_ok, false);
+            }
           }
         } else if (EPI == EPI_SCALE || EPI == EPI_SCALE_Q) {
           float w = row_ok ? __ldg(p.row_scale + orow) : 0.0f;
@@ -1063,6 +1112,18 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             emit32(o0, dh, col, ncols, full, row_ok, false);
             emit32(o1, du, col, ncols, full, row_ok, false);
             emit32(o2, ap, col, ncols, full, row_ok, false);
+            if (p.out3) {
+              // the bf16 rounding of what the high parts left (the weight-gradient GEMMs' low operands)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                dh[i] -= bf16_round(dh[i]);
+                du[i] -= bf16_round(du[i]);
+                ap[i] -= bf16_round(ap[i]);
+              }
+              emit32(o3, dh, col, ncols, full, row_ok, false);
+              emit32(o4, du, col, ncols, full, row_ok, false);
+              emit32(o5, ap, col, ncols, full, row_ok, false);
+            }
           }
           // one partial per (row, column tile, column half)
           if (row_ok) p.part[orow * p.part_ld + tl.nt * (EW / 4) + half] = ds;
@@ -1090,7 +1151,33 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           o.c_z = tl.split;
           o.c_row = mw;
         }
-        if (OUTF32) {
+        if (kTrans) {
+          // Each 32 x 32 block leaves transposed: block row i = accumulator column col + i (an output
+          // row), block column = this thread's tile row (output column mw + lane).  Staged in the swizzled
+          // layout of the store map (fp32 rows of 128 B, bf16 rows of 64 B); the TMA store clips rows and
+          // columns past the output's extent.
+#pragma unroll 1
+          for (int c = c_lo; c < c_lo + kCols; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c, r);
+            tmem_ld_wait();
+            const int col = tl.n0 + c;
+            if (col >= p.N || mw >= p.M) continue;  // a block wholly past the output (M, N multiples of 64)
+            uint8_t* stg = next_stage_buf();
+            if (OUTF32) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<float*>(stg + i * 128 + ((((lane >> 2) ^ (i & 7)) << 4) | ((lane & 3) << 2))) =
+                    have_acc ? __uint_as_float(r[i]) : 0.0f;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<__nv_bfloat16*>(stg + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3)) << 4) | ((lane & 7) << 1))) =
+                    __float2bfloat16_rn(have_acc ? __uint_as_float(r[i]) : 0.0f);
+            }
+            issue_store(OutRef{&mp.o0, nullptr, 0, col, tl.g}, stg, mw);
+          }
+        } else if (OUTF32) {
 #pragma unroll 1
           for (int c = c_lo; c < c_lo + kCols; c += 32) {
             uint32_t r[32];
@@ -1157,14 +1244,14 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
 
 // grid: CTAs wanted (at most one per SM); with CN > 1 it is rounded to whole clusters and capped
 // at the clusters that can be resident at once.
-template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1>
+template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1,
+          int XF = 0>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32, CN>;
-  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH>::bytes(p.groups, VAR);
+  auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32, CN, XF>;
+  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH, (XF & X_DUAL_A) ? 2 : 1>::bytes(p.groups, VAR);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
-  constexpr bool kGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN || BMODE == B_GATHER_MN);
   const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads;
   if (CN == 1) {
     kern<<<grid, threads, smem, stream>>>(p, maps);

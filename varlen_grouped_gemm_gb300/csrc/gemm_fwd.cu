@@ -27,6 +27,14 @@ cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid,
   return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false>(p, m, grid, s);
 }
 
+// The down projection with A as a bf16 high part and the bf16 rounding of the rest (two UMMAs per K step
+// into one accumulator); a stage holds both A tiles and B (BN = 256: 64 KB, three stages).
+cudaError_t run_down_scale_dual(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256)
+    return launch_grouped_gemm<256, 3, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_DUAL_A>(p, m, grid, s);
+  return launch_grouped_gemm<128, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_DUAL_A>(p, m, grid, s);
+}
+
 // Router logits X[T,d] W_r[d,E] (+ bias), W_r read MN-major, fp32 out.
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_MN2, VAR_NONE, EPI_STORE, true>(p, m, grid, s);

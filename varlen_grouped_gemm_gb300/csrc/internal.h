@@ -40,6 +40,7 @@ cudaError_t launch_transpose_into_bf16(const __nv_bfloat16* in, int E, int R, in
 cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                       uint8_t* q, float* scales, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_down_scale_dual(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
 cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
@@ -47,9 +48,11 @@ cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, c
 cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_down(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dw_dual(int BN, bool f32, bool trans, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // test exports
 cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_test_m_dual(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 
 // Expert-sorted copies of two [T, d] bf16 tensors (rows without a pair zeroed), and optionally of per-token
 // e4m3 code rows c with their scales cs (rows without a pair: zero codes, scale 1).
@@ -127,5 +130,13 @@ namespace vgg {
 // Context fields needed outside api.cu.
 int ctx_device(const moe_ctx* ctx);
 int* ctx_error_word(moe_ctx* ctx);
+
+// moe_permute's plain grouping (m_tile = 0) with the scratch taken from `scratch` (scratch_ints ints) rather
+// than a workspace; returns a moe_status (the checks and the launch of moe_permute, MOE_ERR_UNSUPPORTED when
+// the scratch is too small for T and E).
+int permute_plain_with_scratch(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, int T, int E, int K,
+                               long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok, float* sorted_w,
+                               int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out, int32_t* scratch,
+                               long long scratch_ints, cudaStream_t s);
 
 }  // namespace vgg

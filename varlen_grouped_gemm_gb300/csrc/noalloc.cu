@@ -4,8 +4,9 @@
 // interface, or a loop that must not call into an allocator once it is running.
 //
 // The grouping's scratch (per-expert, per-token-block counts and their scan, plus the per-block
-// pair bases; perm_tok_block keeps them within the array for T <= 32768, E <= 512) lives in a file-scope device array of fixed size, which every GPU that
-// loads this library keeps until the process exits.  Host code cannot pass that array's name to
+// pair bases; perm_tok_block keeps them within the array for T <= 32768, E <= 512) lives in a
+// file-scope device array of fixed size, which every GPU that loads this library keeps until the
+// process exits.  Host code cannot pass that array's name to
 // a kernel (in host code it names a host-side stand-in, not device memory), so the first call on
 // each device looks up the array's device address with cudaGetSymbolAddress and caches it.
 #include <mutex>
@@ -28,7 +29,8 @@ constexpr int kMaxDevices = 64;
 int32_t* g_scratch_dev[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device (looked up once per device).  The address
+// belongs to the device's primary context, so it stays valid unless the process resets the device.
 int32_t* scratch_for(int device) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_dev[device]) {
@@ -47,35 +49,19 @@ extern "C" int moe_permute_noalloc(moe_ctx* ctx, const int32_t* topk_ids, const 
                                    float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
                                    moe_stream_t stream) {
   using namespace vgg;
-  if (!ctx || !topk_ids || !topk_w || !counts || !offsets || !sorted_tok || !sorted_w || !tok_ptr || !tok_pairs)
-    return MOE_ERR_INVALID_ARG;
-  if (T < 1 || K < 1 || K > 8 || E < K || E % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (!ctx) return MOE_ERR_INVALID_ARG;
   if (T > kNoAllocMaxT || E > kNoAllocMaxE) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
-  if (cap < static_cast<long long>(T) * K) return MOE_ERR_INVALID_ARG;
   const int device = ctx_device(ctx);
-  int prev = -1;
   if (device < 0 || device >= kMaxDevices) return MOE_ERR_INVALID_ARG;
+  // the array's address is looked up with the context's device current
+  int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess) return MOE_ERR_CUDA;
   if (prev != device && cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
-  int status = MOE_OK;
   int32_t* scratch = scratch_for(device);
-  if (!scratch) {
-    status = MOE_ERR_CUDA;
-  } else {
-    const int tb = perm_tok_block(T, E);
-    const int nb = (T + tb - 1) / tb;
-    if (static_cast<long long>(E + 1) * nb + 1 > kNoAllocScratchInts) {
-      status = MOE_ERR_UNSUPPORTED;
-    } else {
-      PermuteWs w{};
-      w.hist = scratch;
-      w.tokblk = scratch + static_cast<long long>(E) * nb;
-      if (launch_permute(topk_ids, topk_w, nullptr, nullptr, T, E, K, 0, cap, counts, offsets, sorted_tok, sorted_w,
-                         tok_ptr, tok_pairs, P_out, w, ctx_error_word(ctx), static_cast<cudaStream_t>(stream)) !=
-          cudaSuccess)
-        status = MOE_ERR_CUDA;
-    }
-  }
   if (prev != device) cudaSetDevice(prev);
-  return status;
+  if (!scratch) return MOE_ERR_CUDA;
+  // the checks and the launch of moe_permute's plain grouping, on the fixed array
+  return permute_plain_with_scratch(ctx, topk_ids, topk_w, T, E, K, cap, counts, offsets, sorted_tok, sorted_w,
+                                    tok_ptr, tok_pairs, P_out, scratch, kNoAllocScratchInts,
+                                    static_cast<cudaStream_t>(stream));
 }
