@@ -131,6 +131,8 @@ def kernel_table(prof, work, steps, pk):
     kernels = {}
     tot = max(sum(v[0] for v in prof.values()), 1e-9)
     for k, (kms, kl) in sorted(prof.items(), key=lambda kv: -kv[1][0]):
+        if kl == 0:  # a label of the context that this pass did not launch
+            continue
         f2, b2, m2 = work.get(k, (0, 0, 0))
         a = max(kms / max(kl, 1), 1e-9)
         kernels[k] = {"ms_per_step": kms / steps, "share": kms / tot,

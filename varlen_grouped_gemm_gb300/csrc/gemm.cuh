@@ -66,10 +66,7 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //   X_TRANS   varlen-K plain store of the transposed tile: the tile's rows (TMEM lanes) are output
 //             columns, its accumulator columns output rows; each 32 x 32 block is transposed while it is
 //             staged for the TMA store.
-//   X_SPLIT   every stage's loads are dealt to four producer threads (one per warp), 8 KB boxes each, each
-//             thread with its own expect_tx on the stage's full barrier: one thread's TMA loads complete one
-//             after another, so a stage arrives four boxes at a time instead of one.
-enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_SPLIT = 4 };
+enum XFlags { X_DUAL_A = 1, X_TRANS = 2 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
   EPI_DSWIGLU_Q = 7
@@ -382,23 +379,22 @@ __host__ __device__ constexpr int gemm_producers(int stages, int spare) {
 // Warp roles of one instantiation.  The gate/up GEMM gathers its A rows with 8 cp.async warps (the
 // copy rate grows with the number of issuing warps: about 16, 25 and 33 B/ns per SM with 4, 8 and 16
 // warps) and runs 512 threads, so its roles stay within 128 registers per thread.
-template <int STAGES, int EW, int AMODE, int BMODE, int CN, int XF = 0>
+template <int STAGES, int EW, int AMODE, int BMODE, int CN>
 struct WarpPlan {
   static constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
   static constexpr bool kGather = kAGather || BMODE == B_GATHER_MN;
-  static constexpr bool kSplit = (XF & X_SPLIT) != 0;
   static constexpr int kGW = (AMODE == A_GATHER_K) ? 8 : (kGather ? 4 : 0);  // gather warps
-  static constexpr int kMaxWarps = (AMODE == A_GATHER_K || kSplit) ? 16 : kMaxThreads / 32;
+  static constexpr int kMaxWarps = (AMODE == A_GATHER_K) ? 16 : kMaxThreads / 32;
   static constexpr int kBase = EW + 2 + kGW + (CN > 1 ? 1 : 0);
-  static constexpr int kNP = kSplit ? 4 : gemm_producers(STAGES, kMaxWarps - kBase);
+  static constexpr int kNP = gemm_producers(STAGES, kMaxWarps - kBase);
   static constexpr int kThreads = (kBase + kNP - 1) * 32;
 };
 
 template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1,
           int XF = 0>
-__global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kThreads, 1)
+__global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
-  using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>;
+  using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN>;
   constexpr bool kDual = (XF & X_DUAL_A) != 0;
   constexpr bool kTrans = (XF & X_TRANS) != 0;
   using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1>;
@@ -416,9 +412,6 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
                 "e4m3 form: K-major operands, varlen-M");
   static_assert(!kDual || ((AMODE == A_TMA_MN || AMODE == A_TMA_K) && !kF8), "dual A: a tiled bf16 A");
   static_assert(!kTrans || (VAR == VAR_K && EPI == EPI_STORE), "transposed store: varlen-K plain epilogue");
-  constexpr bool kSplit = (XF & X_SPLIT) != 0;
-  static_assert(!kSplit || (AMODE == A_TMA_MN && BMODE == B_TMA_MN2 && CN == 1),
-                "split loads: MN-major tiled A and B in 64-column chunks");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
   constexpr bool kBMn = (BMODE == B_TMA_MN3 || BMODE == B_TMA_MN2 || BMODE == B_GATHER_MN);
   constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
@@ -475,7 +468,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
     for (int s = 0; s < STAGES; ++s) {
       // relay mode: the producer's expect_tx and the relay's arrival; else the producer and,
       // with a gathered operand, the 128 gather threads
-      mbar_init(&full_bar[s], kRelay ? 2 : (kSplit ? kNP : 1) + (kGather ? kGW * 32 : 0));
+      mbar_init(&full_bar[s], kRelay ? 2 : 1 + (kGather ? kGW * 32 : 0));
       mbar_init(&empty_bar[s], CN);  // every CTA of the cluster releases the stage
       if (kRelay) mbar_init(&gath_bar[s], kGW * 32);
     }
@@ -611,29 +604,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
           }
         }
       };
-      // Split loads: a stage is NA * BM / 64 A chunks and BN / 64 B chunks of 8 KB each (64 rows of K x 128 B);
-      // chunk u goes to producer u % kNP.
-      constexpr int kAChunks = (kDual ? 2 : 1) * (BM / 64);
-      constexpr int kUnits = kAChunks + BN / 64;
-      auto split_unit = [&](const Tile& x, int kstage, uint8_t* sa, uint8_t* sb, uint64_t* bar, int u) {
-        const int kg = x.k_begin + kstage * BK;
-        if (u < kAChunks) {
-          const int part = u / (BM / 64), c = u % (BM / 64);
-          const int col = x.m0 + 64 * c;
-          const bool first = col < p.a_colsplit;
-          const CUtensorMap* mp_a = part ? (first ? &mp.a2 : &mp.a3) : (first ? &mp.a0 : &mp.a1);
-          const int ka = kg >= p.a_kwrap ? kg - p.a_kwrap : kg;
-          tma_load_2d(sa + part * L::kA1Bytes + c * (BK * 128), mp_a, bar, first ? col : col - p.a_colsplit, ka);
-        } else {
-          const int c = u - kAChunks;  // one 64-column chunk of B (the map's box holds one chunk)
-          tma_load_3d_hint(sb + c * (BK * 128), &mp.b0, bar, 0, kg, x.n0 / 64 + c, pol_stream);
-        }
-      };
       int it = 0, gcur = 0;
       bool aborted = false;
       Pos q = pos_first(sch, p, gcur);
       while (q.t < sch.total && !aborted) {
-        if (!kSplit && it % kNP != pj) {  // another producer's stage
+        if (it % kNP != pj) {  // another producer's stage
           ++it;
           pos_next(sch, p, gcur, q);
           continue;
@@ -646,16 +621,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
         }
         uint8_t* sa = smem + s * L::kStageBytes;
         uint8_t* sb = sa + L::kABytes;
-        if (kSplit) {
-          constexpr uint32_t kUnitBytes = BK * 128;
-          const uint32_t mine = static_cast<uint32_t>((kUnits - pj + kNP - 1) / kNP) * kUnitBytes;
-          if (mine > 0) {
-            mbar_arrive_expect_tx(&full_bar[s], mine);
-            for (int u = pj; u < kUnits; u += kNP) split_unit(q.tl, q.ks, sa, sb, &full_bar[s], u);
-          } else {
-            mbar_arrive(&full_bar[s]);
-          }
-        } else if (kTxBytes > 0) {
+        if (kTxBytes > 0) {
           mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
           tiled(q.tl, q.ks, sa, sb, &full_bar[s], false);
           // L2 prefetch of the stages ahead of this one within the tile
@@ -675,7 +641,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
         // let this thread's copies already in flight land before the CTA goes away
         volatile int never = 0;
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          if (kSplit || j % kNP == pj) mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
+          if (j % kNP == pj) mbar_wait(&full_bar[j % STAGES], (j / STAGES) & 1, &never, 20000000ull, nullptr);
       } else if (CN > 1) {
         // every CTA's release of this thread's last stages has arrived here, so no peer still
         // targets this CTA's barriers when it leaves
@@ -1296,7 +1262,7 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
-  const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kThreads;
+  const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads;
   if (CN == 1) {
     kern<<<grid, threads, smem, stream>>>(p, maps);
     return cudaGetLastError();
