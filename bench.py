@@ -89,7 +89,8 @@ def kernel_work(wl, P, dW_bytes=2):
         "dact_dswiglu_e4m3": (2 * P * d * n, T * d + 4 * T + E * d * n + 4 * E * n + 10 * P * n,
                               P * d + 4 * P + E * d * n + 4 * E * n + 8 * P * n + 12 * P * n),
         "combine": same(0, 2 * P * d + 2 * T * d),
-        "gather_rows": same(0, 4 * T * d + 4 * P * d),
+        "gather_rows": same(0, 4 * T * d + 4 * P * d),  # (+ the padding's zero rows, at most 15 per expert)
+        "pad_offsets": same(0, 8 * E),
         "zero_tail": same(0, 0),
         "dact_dswiglu": (2 * P * d * n, 2 * T * d + 2 * E * d * n + 10 * P * n,
                          2 * P * d + 2 * E * d * n + 8 * P * n + 12 * P * n),
@@ -202,6 +203,7 @@ _OTHER_LABELS = {
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
     "zero_tail_rows_kernel": "zero_tail", "quantize_rows_e4m3_kernel": "quantize_e4m3",
+    "pad_offsets_kernel": "pad_offsets",
 }
 
 

@@ -403,15 +403,17 @@ int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo
 
 /*
  * moe_test_gemm_varlen_k_dual: the weight-gradient form with a two-part A, for each group e,
- *   S[e, m, c] = sum_{j in group e} (A_hi[j, m] + A_lo[j, m]) * B[j, c]
- * (two UMMAs per K step into one fp32 accumulator).  A_hi, A_lo [rows_a, M], B [rows_b, N] bf16;
- * rows of B past a group's end are cleared in shared memory.  trans = 0: D[G, M, N] = S;
+ *   S[e, m, c] = sum_{i < M_e} (A_hi[off[e] + i, m] + A_lo[off[e] + i, m]) * B[boff[e] + i, c]
+ * (two UMMAs per K step into one fp32 accumulator), M_e = off[e+1] - off[e].  A_hi, A_lo [rows_a, M],
+ * B [rows_b, N] bf16.  b_offsets = NULL: boff = off, and the rows of B past a group's end are cleared in
+ * shared memory; else boff = b_offsets[G+1], the padded layout of the backward's sorted copies (each group's
+ * rows followed by zero rows up to the next multiple of 16, which the caller provides).  trans = 0: D[G, M, N] = S;
  * trans = 1: D[G, N, M] with D[e, c, m] = S[e, m, c] (the transposed store of dW_down).  fp32
  * out, zeros for an empty group; M and N multiples of 64.
  */
 int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, int rows_a, const void* B, int rows_b,
-                                int G, int M, int N, long long cap, const int32_t* offsets, int trans, float* D,
-                                moe_stream_t stream);
+                                int G, int M, int N, long long cap, const int32_t* offsets, const int32_t* b_offsets,
+                                int trans, float* D, moe_stream_t stream);
 
 /* Test export: launch one CTA that waits on an mbarrier nobody arrives on, with
  * the given bound; the wait gives up, records MOE_DEV_TIMEOUT and returns. */

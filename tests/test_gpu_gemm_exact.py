@@ -114,11 +114,13 @@ def test_varlen_m_dual_exact(ctx, sizes, K, N):
 @pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 192), ([1, 0, 333], 128, 256), ([70], 64, 320),
                                          ([17] * 9 + [0, 130], 320, 512)])
 @pytest.mark.parametrize("trans", [False, True])
-def test_varlen_k_dual_exact(ctx, sizes, M, N, trans):
+@pytest.mark.parametrize("padded", [False, True])
+def test_varlen_k_dual_exact(ctx, sizes, M, N, trans, padded):
     """The weight-gradient form: per group, (A_hi + A_lo)^T B over the group's rows, two UMMAs per K step into
     one accumulator; B's rows past a group's end are cleared in shared memory.  A_lo holds small integers
     times 2^-8 (exact in bf16) so that a dropped or misplaced low-part product changes the result.  With
-    trans the tile leaves through transposed 32 x 32 blocks: D[e] is the transpose."""
+    trans the tile leaves through transposed 32 x 32 blocks: D[e] is the transpose.  padded: B in the layout of
+    the backward's sorted copies, every group followed by zero rows up to a multiple of 16 (no clearing)."""
     import varlen_grouped_gemm_gb300 as vgg
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
@@ -129,8 +131,16 @@ def test_varlen_k_dual_exact(ctx, sizes, M, N, trans):
     B = _ints((cap, N), -2, 2, 9).astype(np.float64)
     shape = (G, N, M) if trans else (G, M, N)
     D = torch.full(shape, 3.0, device="cuda")
-    vgg.moe_test_gemm_varlen_k_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(B), torch.from_numpy(offsets).cuda(), D, cap,
-                                    trans=trans)
+    b_off = None
+    Bdev = B
+    if padded:
+        poff = np.concatenate([[0], np.cumsum((np.array(sizes) + 15) // 16 * 16)]).astype(np.int32)
+        Bdev = np.zeros((int(poff[-1]) + 64, N))  # a few rows past the last group stay zero too
+        for e in range(G):
+            Bdev[poff[e]:poff[e] + sizes[e]] = B[offsets[e]:offsets[e + 1]]
+        b_off = torch.from_numpy(poff).cuda()
+    vgg.moe_test_gemm_varlen_k_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(Bdev), torch.from_numpy(offsets).cuda(), D, cap,
+                                    trans=trans, b_offsets=b_off)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == 0 and code == 0
     got = D.cpu().numpy()

@@ -72,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.moe_test_wait_timeout.argtypes = [_P, ctypes.c_ulonglong, _P]
         L.moe_expert_capacity.argtypes = [_I, _I, _I, ctypes.c_double]
         L.moe_expert_capacity.restype = _LL
-        L.moe_test_gemm_varlen_k_dual.argtypes = [_P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _P, _I, _P, _P]
+        L.moe_test_gemm_varlen_k_dual.argtypes = [_P, _P, _P, _I, _P, _I, _I, _I, _I, _LL, _P, _P, _I, _P, _P]
         L.moe_test_gemm_varlen_m_dual.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P]
         L.moe_permute_noalloc.argtypes = [_P, _P, _P, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P]
         L.moe_permute_capacity.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _LL, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -375,15 +375,16 @@ def moe_test_gemm_varlen_m_dual(ctx, A_hi, A_lo, B, offsets, D, stream=None):
         A_hi.shape[0], K, N, D.shape[0], _ptr(offsets, torch.int32), _ptr(D, torch.float32), _stream(stream)))
 
 
-def moe_test_gemm_varlen_k_dual(ctx, A_hi, A_lo, B, offsets, D, cap, trans=False, stream=None):
-    """Test export: per group, (A_hi + A_lo)^T B over the group's rows (D [G, M, N], or [G, N, M] with trans)."""
+def moe_test_gemm_varlen_k_dual(ctx, A_hi, A_lo, B, offsets, D, cap, trans=False, b_offsets=None, stream=None):
+    """Test export: per group, (A_hi + A_lo)^T B over the group's rows (D [G, M, N], or [G, N, M] with trans);
+    b_offsets: B's rows in the padded layout (groups rounded up to 16 rows, zero rows in between)."""
     G = D.shape[0]
     M = A_hi.shape[1]
     N = B.shape[1]
     _check("moe_test_gemm_varlen_k_dual", lib().moe_test_gemm_varlen_k_dual(
         ctx.handle, _ptr(A_hi, torch.bfloat16), _ptr(A_lo, torch.bfloat16), A_hi.shape[0], _ptr(B, torch.bfloat16),
-        B.shape[0], G, M, N, cap, _ptr(offsets, torch.int32), int(bool(trans)), _ptr(D, torch.float32),
-        _stream(stream)))
+        B.shape[0], G, M, N, cap, _ptr(offsets, torch.int32), _ptr(b_offsets, torch.int32), int(bool(trans)),
+        _ptr(D, torch.float32), _stream(stream)))
 
 
 def moe_test_wait_timeout(ctx, timeout_ns: int, stream=None):

@@ -146,15 +146,21 @@ constexpr int kMaxSplitK = 16;
 struct BwdWs {
   __nv_bfloat16 *dH, *dU, *Ap, *dXp, *WrT, *Xs, *dOs;
   __nv_bfloat16 *dH_lo, *dU_lo, *Ap_lo;  // bf16 rounding of what dH, dU, A' leave of the fp32 values
+  int32_t* poff;  // [E + 1] group offsets of the padded sorted copies Xs, dOs (groups rounded up to 16 rows)
   __nv_bfloat16* dL;  // [2][Tp][E], Tp = T rounded up to 64: dlogits as a bf16 high part and the bf16
                       // rounding of the rest; rows [T, Tp) of both halves are zero
   float* part;
   float* wr_part;
 };
 
+// Rows of the padded sorted copies: every group rounded up to a multiple of 16 rows.
+inline long long padded_rows(long long cap, int E) { return cap + 15ll * E; }
+
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
   const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
-  return 6 * al(sizeof(__nv_bfloat16) * cap * n) + 3 * al(sizeof(__nv_bfloat16) * cap * d) +
+  const long long cp = padded_rows(cap, E);
+  return 6 * al(sizeof(__nv_bfloat16) * cap * n) + al(sizeof(__nv_bfloat16) * cap * d) +
+         2 * al(sizeof(__nv_bfloat16) * cp * d) + al(sizeof(int32_t) * (E + 1)) +
          al(sizeof(float) * cap * part_ld) + al(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(ceil_div(T, 64)) * 64 * E) +
          al(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d) +
          al(sizeof(float) * static_cast<size_t>(kMaxSplitK) * d * E);
@@ -182,8 +188,9 @@ BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
   w.dU_lo = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.Ap_lo = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * n));
   w.dXp = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
-  w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
-  w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * cap * d));
+  w.Xs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * padded_rows(cap, E) * d));
+  w.dOs = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * padded_rows(cap, E) * d));
+  w.poff = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
   w.part = reinterpret_cast<float*>(take(sizeof(float) * cap * part_ld));
   w.dL = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * 2 * static_cast<size_t>(ceil_div(T, 64)) * 64 * E));
   w.WrT = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * static_cast<size_t>(E) * d));
@@ -718,8 +725,14 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   if (dact_tok)
     VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(dO), T, nullptr, d, tq,
                                                             ts, s));
-  // expert-sorted copies of X and dO (and of dO's codes): every backward GEMM then reads whole TMA boxes
-  VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
+  // expert-sorted copies of X and dO (and of dO's codes): every backward GEMM then reads whole TMA boxes.  The
+  // bf16 copies are padded per expert to multiples of 16 rows (zero rows), except when the e4m3 dSwiGLU GEMM
+  // quantizes the sorted dO rows themselves (a capacity layout with fewer slots than tokens).
+  const bool padded = !(Wdt_q && !dact_tok);
+  const long long cap_pad = padded ? padded_rows(cap, E) : cap;
+  const int32_t* poff = padded ? w.poff : nullptr;
+  if (padded) VGG_LAUNCH("pad_offsets", launch_pad_offsets(offsets, E, w.poff, ctx->d_err, s));
+  VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, poff, cap_pad, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
                                                static_cast<const __nv_bfloat16*>(X),
                                                static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs,
                                                dact_tok ? tq : nullptr, dact_tok ? ts : nullptr,
@@ -783,8 +796,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.row_scale = sorted_w;
     p.part = w.part;
     p.part_ld = part_ld;
+    p.a_offsets = poff;  // dO's sorted copy may be padded per expert
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, w.dOs, d, cap, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
+    if (!make_map_2d(&m.a0, w.dOs, d, cap_pad, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
         !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
       return MOE_ERR_CUDA;
@@ -889,6 +903,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.rows_cap = static_cast<int>(cap);
     p.a_colsplit = n;
     p.b_chunked = 1;
+    p.b_offsets = poff;
     p.out0 = dW_gate;
     p.out1 = dW_up;
     p.out_rows_split = n;
@@ -897,7 +912,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
         !make_map_2d(&m.a2, w.dH_lo, n, cap, n, 64) || !make_map_2d(&m.a3, w.dU_lo, n, cap, n, 64) ||
-        !make_chunked_map_2d(&m.b0, w.Xs, d, cap, BN / 64) || !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) ||
+        !make_chunked_map_2d(&m.b0, w.Xs, d, cap_pad, BN / 64) || !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) ||
         !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
       return MOE_ERR_CUDA;
     m.b1 = m.b0;
@@ -919,8 +934,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     const int BN = gemm_bn(d);
     Maps m = zero_maps();
     p.b_chunked = 1;
+    p.b_offsets = poff;
     if (!make_map_2d(&m.a0, w.Ap, n, cap, n, 64) || !make_map_2d(&m.a2, w.Ap_lo, n, cap, n, 64) ||
-        !make_chunked_map_2d(&m.b0, w.dOs, d, cap, BN / 64) || !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
+        !make_chunked_map_2d(&m.b0, w.dOs, d, cap_pad, BN / 64) || !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.a3 = m.a2;
@@ -1099,8 +1115,8 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
 }
 
 int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, int rows_a, const void* B, int rows_b,
-                                int G, int M, int N, long long cap, const int32_t* offsets, int trans, float* D,
-                                moe_stream_t stream) {
+                                int G, int M, int N, long long cap, const int32_t* offsets, const int32_t* b_offsets,
+                                int trans, float* D, moe_stream_t stream) {
   VGG_REQUIRE(ctx && A_hi && A_lo && B && offsets && D);
   VGG_REQUIRE(G >= 1 && G <= kMaxGroups && M >= 64 && M % 64 == 0 && N >= 64 && N % 64 == 0 && rows_a >= 1 &&
               rows_b >= 1);
@@ -1114,6 +1130,7 @@ int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo
   p.offsets = offsets;
   p.rows_cap = static_cast<int>(cap);
   p.b_chunked = 1;
+  p.b_offsets = b_offsets;
   p.out0 = D;
   p.ld_out = N;
   const int BN = gemm_bn(N);

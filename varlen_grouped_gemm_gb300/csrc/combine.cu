@@ -345,9 +345,11 @@ cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, 
 
 namespace vgg {
 
-// out_a[j] = a[sorted_tok[j]], out_b[j] = b[sorted_tok[j]] for the sorted positions j of the pairs, zero
-// rows elsewhere in [0, cap): the backward's expert-sorted copies of X and dO, read by TMA boxes in the
-// weight-gradient and dA' GEMMs.  Token-major with bulk (TMA) transfers: lane 0 of each warp reads
+// out_a[j'] = a[sorted_tok[j]], out_b[j'] = b[sorted_tok[j]] for the sorted positions j of the pairs, zero
+// rows elsewhere: the backward's expert-sorted copies of X and dO, read by TMA boxes in the weight-gradient
+// and dA' GEMMs.  With poff the copies are padded per group (j' = j + poff[g] - offsets[g], cap_pad rows):
+// every group's rows are followed by zero rows up to a multiple of 16, so a varlen-K GEMM's last UMMA K step
+// reads zeros past the group's end; rows past poff[E] are left unwritten.  Without poff j' = j (cap rows).  Token-major with bulk (TMA) transfers: lane 0 of each warp reads
 // token t's rows of a and b once (chunks of up to 4 KB, global -> shared) and writes them to the sorted
 // positions of all of t's pairs (tok_pairs), so a and b stream from memory once instead of once per
 // pair (row-major gathers re-read them from DRAM when they do not fit in L2).  Positions that hold no
@@ -372,9 +374,73 @@ __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes
                : "memory");
 }
 
+// The group of sorted position j: the largest g with off[g] <= j (empty groups skipped), 0 <= g < E.
+__device__ __forceinline__ int group_of(const int32_t* __restrict__ off, int E, long long j) {
+  int lo = 0, hi = E;  // off[lo] <= j < off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(off + mid) <= j) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Padded group offsets: poff[g] = sum over earlier groups of their row counts rounded up to 16 (poff[E] =
+// the padded total).  One block.
+__global__ void __launch_bounds__(1024) pad_offsets_kernel(const int32_t* __restrict__ off, int E,
+                                                           int32_t* __restrict__ poff, int* err) {
+  __shared__ int wsum[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < E; base += 1024) {
+    const int g = base + tid;
+    int r = 0;
+    if (g < E) {
+      r = __ldg(off + g + 1) - __ldg(off + g);
+      if (r < 0) {
+        set_error(err, DERR_BAD_OFFSETS);
+        r = 0;
+      }
+      r = (r + 15) & ~15;
+    }
+    int incl = r;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = wsum[lane], wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      wsum[lane] = wi - w;  // exclusive prefix of the warps
+    }
+    __syncthreads();
+    const int excl = carry + wsum[warp] + incl - r;
+    if (g < E) poff[g] = excl;
+    __syncthreads();
+    if (tid == 1023 || g == E - 1) carry = excl + r;
+    __syncthreads();
+  }
+  if (tid == 0) poff[E] = carry;
+}
+
+cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, int* err, cudaStream_t s) {
+  pad_offsets_kernel<<<1, 1024, 0, s>>>(offsets, E, poff, err);
+  return cudaGetLastError();
+}
+
 template <bool CODES>
 __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
-    const int32_t* __restrict__ offsets, int E, const int32_t* __restrict__ sorted_tok,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff, long long cap_pad, int E,
+    const int32_t* __restrict__ sorted_tok,
     const int32_t* __restrict__ tok_ptr, const int32_t* __restrict__ tok_pairs, long long cap, int T, int d,
     const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b, __nv_bfloat16* __restrict__ out_a,
     __nv_bfloat16* __restrict__ out_b, const uint8_t* __restrict__ c, const float* __restrict__ cs,
@@ -412,14 +478,37 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
     }
     const int cnt = static_cast<int>(q1 - q0);
     if (cnt == 0) continue;
-    long long jl[2] = {-1, -1};
+    // lane 0 issues chunk c0's loads of the token's rows into the warp's buffer
+    auto load_chunk = [&](int c0) {
+      const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
+      bulk_wait_read<0>();  // this lane's previous stores have read the warp's buffer
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp], 2 * bytes + (CODES ? bytes / 2 : 0));
+        bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
+        bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+        if (CODES) bulk_g2s(buf + 2 * kChunkBytes, c + t * d + c0, bytes / 2, &bars[warp]);
+      }
+    };
+    load_chunk(0);
+    // the pair positions (and their rows in the padded copies) are looked up while the first chunk loads
+    long long jl[2] = {-1, -1}, jp[2] = {-1, -1};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int r = lane + 32 * h;
       if (r < cnt) {
         const long long j = __ldg(tok_pairs + q0 + r);
-        if (j < 0 || j >= cap) set_error(err, DERR_BAD_OFFSETS);
-        else jl[h] = j;
+        if (j < 0 || j >= cap || (poff && j >= P)) {
+          set_error(err, DERR_BAD_OFFSETS);
+        } else {
+          jl[h] = j;
+          if (poff) {
+            const int g = group_of(offsets, E, j);
+            jp[h] = j + (__ldg(poff + g) - __ldg(offsets + g));
+          } else {
+            jp[h] = j;
+          }
+        }
       }
     }
     if (CODES) {
@@ -430,14 +519,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
     }
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
-      bulk_wait_read<0>();  // this lane's previous stores have read the warp's buffer
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[warp], 2 * bytes + (CODES ? bytes / 2 : 0));
-        bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
-        bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
-        if (CODES) bulk_g2s(buf + 2 * kChunkBytes, c + t * d + c0, bytes / 2, &bars[warp]);
-      }
+      if (c0 > 0) load_chunk(c0);
       const int landed = mbar_wait(&bars[warp], phase, &abort_flag, timeout_ns, err) ? 1 : 0;
       if (!__all_sync(0xffffffffu, landed)) {
         ok = false;
@@ -447,25 +529,54 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (jl[h] >= 0) {
-          bulk_s2g(out_a + jl[h] * d + c0, buf, bytes);
-          bulk_s2g(out_b + jl[h] * d + c0, buf + kChunkBytes, bytes);
+          bulk_s2g(out_a + jp[h] * d + c0, buf, bytes);
+          bulk_s2g(out_b + jp[h] * d + c0, buf + kChunkBytes, bytes);
           if (CODES) bulk_s2g(out_c + jl[h] * d + c0, buf + 2 * kChunkBytes, bytes / 2);
         }
       }
       bulk_commit();
     }
   }
-  // positions without a pair: the tail and the empty slots of the capacity layout
-  for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32) {
-    if (j < P && sorted_tok[j] >= 0) continue;
-    if (CODES) out_cs[j] = 1.0f;
+  // rows without a pair: the tail and the empty slots of the capacity layout, and with the padded layout the
+  // rows that round every group up to a multiple of 16
+  auto zero_row = [&](long long q) {
     for (int c0 = 0; c0 < d; c0 += kGrChunk) {
       const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
-      bulk_s2g(out_a + j * d + c0, zero, bytes);
-      bulk_s2g(out_b + j * d + c0, zero, bytes);
-      if (CODES) bulk_s2g(out_c + j * d + c0, zero, bytes / 2);
+      bulk_s2g(out_a + q * d + c0, zero, bytes);
+      bulk_s2g(out_b + q * d + c0, zero, bytes);
     }
     bulk_commit();
+  };
+  if (poff) {
+    // empty slots of the capacity layout (rare), then the padding rows of every group: at most 15 per group,
+    // one per thread.  Rows past the padded total are never read (a group's last UMMA K step ends on its
+    // padded boundary) and stay unwritten.
+    const long long tid = gw * 32 + lane, nt = nw * 32;
+    for (long long j = tid; j < P && ok; j += nt) {
+      if (sorted_tok[j] >= 0) continue;
+      const int g = group_of(offsets, E, j);
+      zero_row(j + (__ldg(poff + g) - __ldg(offsets + g)));
+    }
+    for (long long k = tid; k < 15ll * E && ok; k += nt) {
+      const int g = static_cast<int>(k / 15), i = static_cast<int>(k % 15);
+      const long long row = __ldg(poff + g) + (__ldg(offsets + g + 1) - __ldg(offsets + g)) + i;
+      if (row < __ldg(poff + g + 1)) zero_row(row);
+    }
+  } else {
+    for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32)
+      if (j >= P || sorted_tok[j] < 0) zero_row(j);
+  }
+  // the code rows keep the unpadded layout
+  if (CODES) {
+    for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32) {
+      if (j < P && sorted_tok[j] >= 0) continue;
+      out_cs[j] = 1.0f;
+      for (int c0 = 0; c0 < d; c0 += kGrChunk) {
+        const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
+        bulk_s2g(out_c + j * d + c0, zero, bytes / 2);
+      }
+      bulk_commit();
+    }
   }
   if (!ok && lane == 0) {  // a load that never completed: let copies in flight land before leaving
     volatile int never = 0;
@@ -474,7 +585,8 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   bulk_wait0();
 }
 
-cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, const int32_t* tok_ptr,
+cudaError_t launch_gather_rows(const int32_t* offsets, const int32_t* poff, long long cap_pad, int E,
+                               const int32_t* sorted_tok, const int32_t* tok_ptr,
                                const int32_t* tok_pairs, long long cap, int T, int d, const __nv_bfloat16* a,
                                const __nv_bfloat16* b, __nv_bfloat16* out_a, __nv_bfloat16* out_b,
                                const uint8_t* c, const float* cs, uint8_t* out_c, float* out_cs, int* err,
@@ -491,11 +603,11 @@ cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sor
   if (blocks > 0) {
     if (codes)
       gather_rows_bulk_kernel<true><<<blocks, kGrWarps * 32, smem, s>>>(
-          offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, c, cs, out_c, out_cs, err,
+          offsets, poff, cap_pad, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, c, cs, out_c, out_cs, err,
           timeout_ns);
     else
       gather_rows_bulk_kernel<false><<<blocks, kGrWarps * 32, smem, s>>>(
-          offsets, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, nullptr, nullptr, nullptr,
+          offsets, poff, cap_pad, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d, a, b, out_a, out_b, nullptr, nullptr, nullptr,
           nullptr, err, timeout_ns);
   }
   return cudaGetLastError();

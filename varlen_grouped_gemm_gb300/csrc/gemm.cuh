@@ -90,6 +90,11 @@ struct GemmParams {
   long long a_ld;
   const int* b_idx;
   int b_rows;
+  // Optional row bases of the tiled operands (device, [groups + 1]): VAR_M A rows of group g start at
+  // a_offsets[g], VAR_K B rows (the reduction) at b_offsets[g], instead of offsets[g].  The backward's
+  // expert-sorted copies use them: every expert padded to a multiple of 16 rows with zero rows.
+  const int* a_offsets;
+  const int* b_offsets;
   const __nv_bfloat16* b_src;
   long long b_ld;
   // epilogue
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       auto tiled = [&](const Tile& x, int kstage, uint8_t* sa, uint8_t* sb, uint64_t* bar, bool l2) {
         const int kg = x.k_begin + kstage * BK;
         if (AMODE == A_TMA_K) {
-          const int row = (VAR == VAR_M ? s_off[x.g] : 0) + x.m0;
+          const int row = (VAR == VAR_M ? (p.a_offsets ? __ldg(p.a_offsets + x.g) : s_off[x.g]) : 0) + x.m0;
           const CUtensorMap* mp_a = kg < p.a_ksplit ? &mp.a0 : &mp.a1;
           const int kc = kg < p.a_ksplit ? kg : kg - p.a_ksplit;
           if (l2) tma_prefetch_l2_2d(mp_a, kc, row);
@@ -592,14 +597,16 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           if (l2) tma_prefetch_l2_4d(first ? &mp.b0 : &mp.b1, 0, kc, x.n0 / 64, x.g);
           else tma_load_4d_hint(sb, first ? &mp.b0 : &mp.b1, bar, 0, kc, x.n0 / 64, x.g, pol_stream);
         } else if (BMODE == B_TMA_MN2) {
+          // varlen-K with padded B rows: the group's reduction rows start at b_offsets[g] in B
+          const int kgb = (VAR == VAR_K && p.b_offsets) ? __ldg(p.b_offsets + x.g) + kstage * BK : kg;
           if (p.b_chunked) {  // 3-D view {64 columns, rows, N/64 chunks}
-            if (l2) tma_prefetch_l2_3d(&mp.b0, 0, kg, x.n0 / 64);
-            else tma_load_3d(sb, &mp.b0, bar, 0, kg, x.n0 / 64);
+            if (l2) tma_prefetch_l2_3d(&mp.b0, 0, kgb, x.n0 / 64);
+            else tma_load_3d(sb, &mp.b0, bar, 0, kgb, x.n0 / 64);
           } else {
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c) {
-              if (l2) tma_prefetch_l2_2d(&mp.b0, x.n0 + 64 * c, kg);
-              else tma_load_2d(sb + c * (BK * 128), &mp.b0, bar, x.n0 + 64 * c, kg);
+              if (l2) tma_prefetch_l2_2d(&mp.b0, x.n0 + 64 * c, kgb);
+              else tma_load_2d(sb + c * (BK * 128), &mp.b0, bar, x.n0 + 64 * c, kgb);
             }
           }
         }
@@ -881,7 +888,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             // step past the group's end are cleared
             nkk = (kv + 15) / 16;
             const int kend = nkk * 16;
-            if (kv < kend) {
+            if (kv < kend && !p.b_offsets) {  // padded B rows are zero there already
               uint8_t* b_gen = smem + s * L::kStageBytes + L::kABytes;
               const int pieces = (kend - kv) * 8;
               for (int c = 0; c < BN / 64; ++c)

@@ -55,12 +55,17 @@ cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const Ma
 cudaError_t run_test_m_dual(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 
 // Expert-sorted copies of two [T, d] bf16 tensors (rows without a pair zeroed), and optionally of per-token
-// e4m3 code rows c with their scales cs (rows without a pair: zero codes, scale 1).
-cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* sorted_tok, const int32_t* tok_ptr,
+// e4m3 code rows c with their scales cs (rows without a pair: zero codes, scale 1).  With poff the two bf16
+// copies are padded per group to multiples of 16 rows (cap_pad rows); the code rows are not.
+cudaError_t launch_gather_rows(const int32_t* offsets, const int32_t* poff, long long cap_pad, int E,
+                               const int32_t* sorted_tok, const int32_t* tok_ptr,
                                const int32_t* tok_pairs, long long cap, int T, int d, const __nv_bfloat16* a,
                                const __nv_bfloat16* b, __nv_bfloat16* out_a, __nv_bfloat16* out_b,
                                const uint8_t* c, const float* cs, uint8_t* out_c, float* out_cs, int* err,
                                int num_sms, unsigned long long timeout_ns, cudaStream_t s);
+
+// poff[g] = sum over the groups before g of their row counts rounded up to 16; poff[E] the total.
+cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, int* err, cudaStream_t s);
 
 // Zero rows [offsets[E], cap) of up to three [cap, cols] bf16 buffers (the tail past the last pair).
 cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols, __nv_bfloat16* a,
