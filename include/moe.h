@@ -81,6 +81,18 @@ int moe_get_error(moe_ctx* ctx, int* device_error);
 /* Bound of every device spin-wait, in nanoseconds (default 2 s). */
 int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns);
 
+/*
+ * CTA pairs (tcgen05 cta_group::2): a cluster of two CTAs computes each 256-row tile with M = 256
+ * UMMAs issued by the even CTA, each CTA holding its 128 rows of A and half of B's 256 columns.
+ * varlen_m (0/1): the tiled varlen-M GEMMs with 256-column tiles (dX, dA' with the dSwiGLU epilogue, the
+ * two-part down projection); varlen_k (0/1): the two-part weight-gradient GEMMs on padded sorted rows.
+ * Both default to 0: on GB300 they measured slower than one CTA per 128-row tile (the varlen-K tiles
+ * are bound by their epilogue, the varlen-M ones gain nothing from halving each SM's B bytes).  Results
+ * are identical either way up to fp32 summation order.  Returns MOE_ERR_INVALID_ARG for a NULL ctx or a
+ * flag other than 0 or 1.
+ */
+int moe_set_cta_pairs(moe_ctx* ctx, int varlen_m, int varlen_k);
+
 /* Pair capacity for the pair-indexed arrays: T*K, plus E*m_tile/2 under token rounding. */
 long long moe_pair_capacity(int T, int E, int K, int m_tile);
 
@@ -374,7 +386,8 @@ int moe_profile_read(moe_ctx* ctx, int max_kernels, char* names, double* total_m
  *   D[j, c] = sum_k A[row(j), k] * B[e, k, c]      (B_kmajor = 0: B is [G, K, N])
  * with row(j) = idx[j] (gathered, idx != NULL) or j.  A[rows_a, K] bf16,
  * D[cap, N] fp32; offsets[G+1].  With B_kmajor = 0, N must be a multiple of 64.  A gathered row index outside the source
- * records MOE_DEV_BAD_OFFSETS and reads zeros instead.
+ * records MOE_DEV_BAD_OFFSETS and reads zeros instead.  Tiles of 128 x 128; without idx and with
+ * moe_set_cta_pairs(ctx, 1, .) CTA pairs on 256 x 256 tiles.
  *
  * moe_test_gemm_varlen_k: for each group e,
  *   D[e, m, c] = sum_{j in group e} A[rowa(j), m] * B[rowb(j), c]
@@ -396,7 +409,8 @@ int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, in
  * sorted row j of it,
  *   D[j, c] = sum_k (A_hi[j, k] + A_lo[j, k]) * B[e, c, k]       (B is [G, N, K], K-major)
  * (two UMMAs per K step into one fp32 accumulator).  A_hi, A_lo [rows_a, K] bf16 with rows_a >= cap,
- * D[cap, N] fp32; rows outside every group are left untouched.  K a multiple of 64, N of 8.
+ * D[cap, N] fp32; rows outside every group are left untouched.  K a multiple of 64, N of 8.  Tiles of
+ * 128 x 256 (CTA pairs on 256 x 256 with moe_set_cta_pairs(ctx, 1, .)).
  */
 int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, const void* B, int G, int rows_a,
                                 int K, int N, long long cap, const int32_t* offsets, float* D, moe_stream_t stream);
@@ -409,7 +423,8 @@ int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo
  * shared memory; else boff = b_offsets[G+1], the padded layout of the backward's sorted copies (each group's
  * rows followed by zero rows up to the next multiple of 16, which the caller provides).  trans = 0: D[G, M, N] = S;
  * trans = 1: D[G, N, M] with D[e, c, m] = S[e, m, c] (the transposed store of dW_down).  fp32
- * out, zeros for an empty group; M and N multiples of 64.
+ * out, zeros for an empty group; M and N multiples of 64.  The kernel configuration is the backward's for
+ * the same N (CTA pairs with b_offsets, N > 128 and moe_set_cta_pairs(ctx, ., 1)).
  */
 int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, int rows_a, const void* B, int rows_b,
                                 int G, int M, int N, long long cap, const int32_t* offsets, const int32_t* b_offsets,

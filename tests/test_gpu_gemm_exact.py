@@ -2,7 +2,10 @@
 integer below 2^24, so fp32 accumulation is exact in any order and the device result must equal the
 int64 reference bit for bit.  This pins the gather, the varlen bookkeeping (empty, one-row and
 ragged groups, ragged N), both operand layouts (K-major and MN-major), the two-part A operand and
-transposed store of the weight-gradient GEMMs, and the bounded wait."""
+transposed store of the weight-gradient GEMMs, the CTA-pair form of the tiled GEMMs (two CTAs per
+256-row tile, M = 256 UMMAs), and the bounded wait."""
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -24,10 +27,22 @@ def _bf(a):
     return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).cuda()
 
 
-@pytest.mark.parametrize("gathered", [True, False])
+@contextlib.contextmanager
+def _cta_pairs(ctx, on):
+    """CTA pairs for both GEMM families while the block runs (off is the default)."""
+    ctx.set_cta_pairs(on, on)
+    try:
+        yield
+    finally:
+        ctx.set_cta_pairs(False, False)
+
+
+@pytest.mark.parametrize("gathered,pairs", [(True, False), (False, False), (False, True)])
 @pytest.mark.parametrize("b_kmajor", [True, False])
 @pytest.mark.parametrize("sizes,K,N", [([0, 1, 130, 257, 64], 192, 200), ([300], 64, 136), ([5, 0, 0, 129], 128, 264)])
-def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
+def test_varlen_m_exact(ctx, gathered, pairs, b_kmajor, sizes, K, N):
+    """pairs: CTA pairs on 256 x 256 tiles; a group's odd CTA may hold rows past the group (or no rows at
+    all), which it must neither store nor let into the even CTA's rows."""
     import varlen_grouped_gemm_gb300 as vgg
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
@@ -41,8 +56,9 @@ def test_varlen_m_exact(ctx, gathered, b_kmajor, sizes, K, N):
     Bk = _ints((G, N, K), -1, 1, 3)  # [G, N, K]
     B = Bk if b_kmajor else np.ascontiguousarray(Bk.transpose(0, 2, 1))
     D = torch.full((cap, N), -7.0, device="cuda")
-    vgg.moe_test_gemm_varlen_m(ctx, _bf(A), None if idx is None else torch.from_numpy(idx).cuda(), _bf(B),
-                               b_kmajor, torch.from_numpy(offsets).cuda(), D)
+    with _cta_pairs(ctx, pairs):
+        vgg.moe_test_gemm_varlen_m(ctx, _bf(A), None if idx is None else torch.from_numpy(idx).cuda(), _bf(B),
+                                   b_kmajor, torch.from_numpy(offsets).cuda(), D)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == 0 and code == 0
     got = D.cpu().numpy()
@@ -87,8 +103,9 @@ def test_varlen_k_exact(ctx, sizes, M, N, gathered):
         np.testing.assert_array_equal(got[e], (A[ra].T @ B[rb]).astype(np.float32), err_msg=f"group {e}")
 
 
+@pytest.mark.parametrize("pairs", [False, True])
 @pytest.mark.parametrize("sizes,K,N", [([0, 1, 130, 257, 64], 192, 200), ([300], 64, 512), ([5, 0, 0, 129], 128, 264)])
-def test_varlen_m_dual_exact(ctx, sizes, K, N):
+def test_varlen_m_dual_exact(ctx, pairs, sizes, K, N):
     """The down projection's form: per sorted row, (A_hi + A_lo) B[e]^T with two UMMAs per K step into one
     accumulator; A_lo holds small integers times 2^-8 so that a dropped or misplaced low-part product shows."""
     import varlen_grouped_gemm_gb300 as vgg
@@ -100,7 +117,8 @@ def test_varlen_m_dual_exact(ctx, sizes, K, N):
     A_lo = _ints((cap, K), -3, 3, 12).astype(np.float64) / 256.0
     B = _ints((G, N, K), -1, 1, 13).astype(np.float64)
     D = torch.full((cap, N), -7.0, device="cuda")
-    vgg.moe_test_gemm_varlen_m_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(B), torch.from_numpy(offsets).cuda(), D)
+    with _cta_pairs(ctx, pairs):
+        vgg.moe_test_gemm_varlen_m_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(B), torch.from_numpy(offsets).cuda(), D)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == 0 and code == 0
     got = D.cpu().numpy()
@@ -112,10 +130,10 @@ def test_varlen_m_dual_exact(ctx, sizes, K, N):
 
 
 @pytest.mark.parametrize("sizes,M,N", [([0, 5, 64, 200], 192, 192), ([1, 0, 333], 128, 256), ([70], 64, 320),
-                                         ([17] * 9 + [0, 130], 320, 512)])
+                                         ([17] * 9 + [0, 130], 320, 512), ([300, 0, 17], 128, 4096)])
 @pytest.mark.parametrize("trans", [False, True])
-@pytest.mark.parametrize("padded", [False, True])
-def test_varlen_k_dual_exact(ctx, sizes, M, N, trans, padded):
+@pytest.mark.parametrize("padded,pairs", [(False, False), (True, False), (True, True)])
+def test_varlen_k_dual_exact(ctx, sizes, M, N, trans, padded, pairs):
     """The weight-gradient form: per group, (A_hi + A_lo)^T B over the group's rows, two UMMAs per K step into
     one accumulator; B's rows past a group's end are cleared in shared memory.  A_lo holds small integers
     times 2^-8 (exact in bf16) so that a dropped or misplaced low-part product changes the result.  With
@@ -139,8 +157,9 @@ def test_varlen_k_dual_exact(ctx, sizes, M, N, trans, padded):
         for e in range(G):
             Bdev[poff[e]:poff[e] + sizes[e]] = B[offsets[e]:offsets[e + 1]]
         b_off = torch.from_numpy(poff).cuda()
-    vgg.moe_test_gemm_varlen_k_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(Bdev), torch.from_numpy(offsets).cuda(), D, cap,
-                                    trans=trans, b_offsets=b_off)
+    with _cta_pairs(ctx, pairs):
+        vgg.moe_test_gemm_varlen_k_dual(ctx, _bf(A_hi), _bf(A_lo), _bf(Bdev), torch.from_numpy(offsets).cuda(), D,
+                                        cap, trans=trans, b_offsets=b_off)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == 0 and code == 0
     got = D.cpu().numpy()

@@ -47,6 +47,21 @@ def test_layer_matches_oracle(ctx, wl):
     print(wl.name, {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
 
 
+@pytest.mark.parametrize("wl", [CASES[1], CASES[2]], ids=lambda w: w.name)
+def test_layer_with_cta_pairs(ctx, wl):
+    """The same layer with the tiled varlen-M GEMMs and the weight-gradient GEMMs on CTA pairs (two CTAs per
+    256-row tile): the same tolerance against the oracle."""
+    inp = Inputs(wl)
+    ctx.set_cta_pairs(True, True)
+    try:
+        buf = run_path(ctx, inp, backward=True, dW_dtype=torch.float32)
+    finally:
+        ctx.set_cta_pairs(False, False)
+    g = gpu_routing(buf)
+    O_ref, cache, grads = oracle_layer(inp, g)
+    compare_layer(buf, inp, O_ref, cache, grads)
+
+
 def test_dW_bf16_storage(ctx):
     wl = synth.scaled(synth.WORKLOADS["c2"], name="c2_bf16dw", T=256, d=128, E=8, n=128, K=2)
     inp = Inputs(wl)

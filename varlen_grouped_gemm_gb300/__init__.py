@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libvgg_moe.so")
 
 # The symbols declared in include/moe.h.
 EXPORTS = (
-    "moe_create", "moe_destroy", "moe_status_str", "moe_get_error", "moe_set_wait_timeout",
+    "moe_create", "moe_destroy", "moe_status_str", "moe_get_error", "moe_set_wait_timeout", "moe_set_cta_pairs",
     "moe_pair_capacity", "moe_workspace_bytes", "moe_route", "moe_permute", "moe_grouped_gemm_fwd",
     "moe_combine", "moe_backward", "moe_profile_enable", "moe_profile_read", "moe_test_gemm_varlen_m",
     "moe_test_gemm_varlen_k", "moe_test_wait_timeout", "moe_permute_noalloc", "moe_permute_capacity",
@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.moe_status_str.restype = ctypes.c_char_p
         L.moe_get_error.argtypes = [_P, ctypes.POINTER(_I)]
         L.moe_set_wait_timeout.argtypes = [_P, ctypes.c_ulonglong]
+        L.moe_set_cta_pairs.argtypes = [_P, _I, _I]
         L.moe_pair_capacity.argtypes = [_I, _I, _I, _I]
         L.moe_pair_capacity.restype = _LL
         L.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
@@ -143,6 +144,10 @@ class Context:
 
     def set_wait_timeout(self, ns: int):
         _check("moe_set_wait_timeout", lib().moe_set_wait_timeout(self.handle, int(ns)))
+
+    def set_cta_pairs(self, varlen_m: bool, varlen_k: bool):
+        """CTA pairs (two CTAs per 256-row tile) for the tiled varlen-M and the weight-gradient GEMMs."""
+        _check("moe_set_cta_pairs", lib().moe_set_cta_pairs(self.handle, int(varlen_m), int(varlen_k)))
 
 
 def moe_profile_enable(ctx: Context, enable: bool = True):

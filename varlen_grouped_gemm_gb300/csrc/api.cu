@@ -26,6 +26,8 @@ struct moe_ctx {
   unsigned long long timeout_ns;
   bool prof = false;
   int l2_prefetch = 0;  // L2 prefetch of later stages (measured slower; kept switchable)
+  int cta_pair = 0;     // CTA pairs on the 256-row tiles of the tiled varlen-M GEMMs (dX, dA', two-part down)
+  int cta_pair_dw = 0;  // CTA pairs on the varlen-K weight-gradient GEMMs (both measured slower; switchable)
 
   std::vector<cudaEvent_t> pool;
   size_t pool_next = 0;
@@ -140,6 +142,41 @@ struct DeviceGuard {
 };
 
 inline int gemm_bn(int N) { return N > 128 ? 256 : 128; }
+
+// Launch shape of a varlen-M GEMM over cap sorted rows in E groups with N output columns.  With BN = 256
+// (and pairs allowed) a CTA pair computes each 256-row tile, each CTA loading BN / 2 of B's columns.
+struct VmShape {
+  bool pair;
+  int b_cols;  // columns of B per TMA box
+  int grid;    // CTAs
+};
+inline VmShape vm_shape(const moe_ctx* ctx, int BN, bool allow, long long cap, int E, int N) {
+  VmShape sh;
+  sh.pair = allow && ctx->cta_pair && BN == 256;
+  sh.b_cols = sh.pair ? BN / 2 : BN;
+  const long long tiles = static_cast<long long>(ceil_div(cap, sh.pair ? 2 * BM : BM) + E) * ceil_div(N, BN);
+  sh.grid = static_cast<int>(sh.pair ? std::min<long long>(2 * tiles, ctx->num_sms / 2 * 2)
+                                     : std::min<long long>(tiles, ctx->num_sms));
+  return sh;
+}
+
+// Launch shape of a two-part varlen-K weight-gradient GEMM ([G][M][N] output).  With padded B rows
+// and BN = 256 a CTA pair computes each 256-row tile (each CTA loads BN / 2 of B's columns);
+// otherwise one CTA per 128-row tile.
+struct DwShape {
+  bool pair;
+  int b_chunks;  // 64-column chunks of B per TMA box
+  int grid;      // CTAs
+};
+inline DwShape dw_shape(const moe_ctx* ctx, int BN, bool padded, int G, int M, int N) {
+  DwShape sh;
+  sh.pair = padded && BN == 256 && ctx->cta_pair_dw;
+  sh.b_chunks = (sh.pair ? BN / 2 : BN) / 64;
+  const long long tiles = static_cast<long long>(G) * ceil_div(M, sh.pair ? 2 * BM : BM) * ceil_div(N, BN);
+  const long long ctas = sh.pair ? 2 * tiles : tiles;
+  sh.grid = static_cast<int>(std::min<long long>(ctas, sh.pair ? ctx->num_sms / 2 * 2 : ctx->num_sms));
+  return sh;
+}
 
 constexpr int kMaxSplitK = 16;
 
@@ -304,16 +341,16 @@ static int down_projection(moe_ctx* ctx, const void* A, const void* A_lo, const 
   p.ld_out = d;
   p.row_scale = sorted_w;
   const int BN = gemm_bn(d);
+  const VmShape sh = vm_shape(ctx, BN, A_lo != nullptr, cap, E, d);
   Maps m = zero_maps();
-  if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, BN) ||
+  if (!make_map_2d(&m.a0, A, n, cap, n, BM) || !make_map_3d(&m.b0, W_down, n, d, E, sh.b_cols) ||
       !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64) || (A_lo && !make_map_2d(&m.a2, A_lo, n, cap, n, BM)))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.a3 = m.a2;
   m.b1 = m.b0;
-  const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-  if (A_lo) VGG_LAUNCH("down_scale", run_down_scale_dual(BN, p, m, std::min(tiles, ctx->num_sms), s));
-  else VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, std::min(tiles, ctx->num_sms), s));
+  if (A_lo) VGG_LAUNCH("down_scale", run_down_scale_dual(BN, sh.pair, p, m, sh.grid, s));
+  else VGG_LAUNCH("down_scale", run_down_scale(BN, p, m, sh.grid, s));
   return MOE_OK;
 }
 
@@ -404,6 +441,13 @@ int moe_get_error(moe_ctx* ctx, int* device_error) {
 int moe_set_wait_timeout(moe_ctx* ctx, unsigned long long timeout_ns) {
   if (!ctx || timeout_ns == 0) return MOE_ERR_INVALID_ARG;
   ctx->timeout_ns = timeout_ns;
+  return MOE_OK;
+}
+
+int moe_set_cta_pairs(moe_ctx* ctx, int varlen_m, int varlen_k) {
+  if (!ctx || (varlen_m != 0 && varlen_m != 1) || (varlen_k != 0 && varlen_k != 1)) return MOE_ERR_INVALID_ARG;
+  ctx->cta_pair = varlen_m;
+  ctx->cta_pair_dw = varlen_k;
   return MOE_OK;
 }
 
@@ -797,15 +841,15 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.part = w.part;
     p.part_ld = part_ld;
     p.a_offsets = poff;  // dO's sorted copy may be padded per expert
+    const VmShape sh = vm_shape(ctx, bn6, true, cap, E, n);
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, w.dOs, d, cap_pad, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, bn6 / 64) ||
+    if (!make_map_2d(&m.a0, w.dOs, d, cap_pad, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, sh.b_cols / 64) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
         !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, bn6);
-    VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, sh.pair, p, m, sh.grid, s));
   }
   // dXp = [dH | dU] [W_gate[e]; W_up[e]]
   if (Wgu_q) {
@@ -845,13 +889,13 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dXp;
     p.ld_out = d;
     const int BN = gemm_bn(d);
+    const VmShape sh = vm_shape(ctx, BN, true, cap, E, d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, BM) || !make_map_2d(&m.a1, w.dU, n, cap, n, BM) ||
-        !make_chunked_map_3d(&m.b0, W_gate, d, n, E, BN / 64) || !make_chunked_map_3d(&m.b1, W_up, d, n, E, BN / 64) ||
-        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
+        !make_chunked_map_3d(&m.b0, W_gate, d, n, E, sh.b_cols / 64) ||
+        !make_chunked_map_3d(&m.b1, W_up, d, n, E, sh.b_cols / 64) || !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
-    VGG_LAUNCH("dx_gemm", run_dx_store(BN, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dx_gemm", run_dx_store(BN, sh.pair, p, m, sh.grid, s));
   }
   // per token: dS, router-logit gradient, dX
   VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
@@ -909,15 +953,15 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out_rows_split = n;
     p.ld_out = d;
     const int BN = gemm_bn(d);
+    const DwShape sh = dw_shape(ctx, BN, poff != nullptr, E, 2 * n, d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
         !make_map_2d(&m.a2, w.dH_lo, n, cap, n, 64) || !make_map_2d(&m.a3, w.dU_lo, n, cap, n, 64) ||
-        !make_chunked_map_2d(&m.b0, w.Xs, d, cap_pad, BN / 64) || !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) ||
-        !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
+        !make_chunked_map_2d(&m.b0, w.Xs, d, cap_pad, sh.b_chunks) ||
+        !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) || !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
       return MOE_ERR_CUDA;
     m.b1 = m.b0;
-    const int tiles = E * ceil_div(2 * n, BM) * ceil_div(d, BN);
-    VGG_LAUNCH("dw_gate_up", run_dw_dual(BN, f32, false, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_gate_up", run_dw_dual(BN, f32, false, sh.pair, p, m, sh.grid, s));
   }
   // dW_down[e] = dO[tok]^T A' (the combine weight is folded into A' = w A), computed as its transpose
   // A'^T dO[tok] with A' as high and low bf16 parts (tile rows = columns of dW_down) and stored through
@@ -932,17 +976,18 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = dW_down;
     p.ld_out = n;
     const int BN = gemm_bn(d);
+    const DwShape sh = dw_shape(ctx, BN, poff != nullptr, E, n, d);
     Maps m = zero_maps();
     p.b_chunked = 1;
     p.b_offsets = poff;
     if (!make_map_2d(&m.a0, w.Ap, n, cap, n, 64) || !make_map_2d(&m.a2, w.Ap_lo, n, cap, n, 64) ||
-        !make_chunked_map_2d(&m.b0, w.dOs, d, cap_pad, BN / 64) || !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
+        !make_chunked_map_2d(&m.b0, w.dOs, d, cap_pad, sh.b_chunks) ||
+        !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.a3 = m.a2;
     m.b1 = m.b0;
-    const int tiles = E * ceil_div(n, BM) * ceil_div(d, BN);
-    VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, p, m, std::min(tiles, ctx->num_sms), s));
+    VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, sh.pair, p, m, sh.grid, s));
   }
   return MOE_OK;
 }
@@ -1040,9 +1085,11 @@ int moe_test_gemm_varlen_m(moe_ctx* ctx, const void* A, const int32_t* idx, cons
   }
   m.b1 = m.b0;
   if (!make_store_map_2d(&m.o0, D, true, N, cap, N, 32)) return MOE_ERR_CUDA;
+  // 128-column tiles, or CTA pairs on 256-column tiles (each CTA loads the same 128-column B boxes)
+  const VmShape sh = vm_shape(ctx, idx ? 128 : 256, true, cap, G, N);
   const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 128);
-  return cuda_status(run_test_m(idx != nullptr, B_kmajor, p, m, std::min(tiles, ctx->num_sms),
-                                static_cast<cudaStream_t>(stream)));
+  return cuda_status(run_test_m(idx != nullptr, B_kmajor, sh.pair, p, m,
+                                sh.pair ? sh.grid : std::min(tiles, ctx->num_sms), static_cast<cudaStream_t>(stream)));
 }
 
 int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo, const void* B, int G, int rows_a,
@@ -1061,15 +1108,15 @@ int moe_test_gemm_varlen_m_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo
   p.rows_cap = static_cast<int>(cap);
   p.out0 = D;
   p.ld_out = N;
+  const VmShape sh = vm_shape(ctx, 256, true, cap, G, N);
   Maps m = zero_maps();
   if (!make_map_2d(&m.a0, A_hi, K, rows_a, K, BM) || !make_map_2d(&m.a2, A_lo, K, rows_a, K, BM) ||
-      !make_map_3d(&m.b0, B, K, N, G, 256) || !make_store_map_2d(&m.o0, D, true, N, cap, N, 32))
+      !make_map_3d(&m.b0, B, K, N, G, sh.b_cols) || !make_store_map_2d(&m.o0, D, true, N, cap, N, 32))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.a3 = m.a2;
   m.b1 = m.b0;
-  const int tiles = (ceil_div(cap, BM) + G) * ceil_div(N, 256);
-  return cuda_status(run_test_m_dual(p, m, std::min(tiles, ctx->num_sms), static_cast<cudaStream_t>(stream)));
+  return cuda_status(run_test_m_dual(sh.pair, p, m, sh.grid, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_test_gemm_varlen_k(moe_ctx* ctx, const void* A, const int32_t* idx_a, int rows_a, const void* B,
@@ -1134,17 +1181,16 @@ int moe_test_gemm_varlen_k_dual(moe_ctx* ctx, const void* A_hi, const void* A_lo
   p.out0 = D;
   p.ld_out = N;
   const int BN = gemm_bn(N);
+  const DwShape sh = dw_shape(ctx, BN, b_offsets != nullptr, G, M, N);
   Maps m = zero_maps();
   if (!make_map_2d(&m.a0, A_hi, M, rows_a, M, 64) || !make_map_2d(&m.a2, A_lo, M, rows_a, M, 64) ||
-      !make_chunked_map_2d(&m.b0, B, N, rows_b, BN / 64) ||
+      !make_chunked_map_2d(&m.b0, B, N, rows_b, sh.b_chunks) ||
       !(trans ? make_store_map_3d(&m.o0, D, true, M, N, G, 32) : make_store_map_3d(&m.o0, D, true, N, M, G, 32)))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.a3 = m.a2;
   m.b1 = m.b0;
-  const int tiles = G * ceil_div(M, BM) * ceil_div(N, BN);
-  return cuda_status(run_dw_dual(BN, true, trans != 0, p, m, std::min(tiles, ctx->num_sms),
-                                 static_cast<cudaStream_t>(stream)));
+  return cuda_status(run_dw_dual(BN, true, trans != 0, sh.pair, p, m, sh.grid, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_profile_enable(moe_ctx* ctx, int enable) {

@@ -66,7 +66,10 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //   X_TRANS   varlen-K plain store of the transposed tile: the tile's rows (TMEM lanes) are output
 //             columns, its accumulator columns output rows; each 32 x 32 block is transposed while it is
 //             staged for the TMA store.
-enum XFlags { X_DUAL_A = 1, X_TRANS = 2 };
+//   X_PAIR    a CTA pair (cluster of 2, cta_group::2) computes a 256-row tile: each CTA loads its 128 rows of A
+//             and half of B's columns, both CTAs' TMA loads complete on the even CTA's barriers, the even CTA
+//             issues the M = 256 UMMAs, and each CTA drains its own 128 TMEM rows (varlen-K with padded B).
+enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
   EPI_DSWIGLU_Q = 7
@@ -135,12 +138,13 @@ struct Maps {
   CUtensorMap a0, a1, a2, a3, b0, b1, o0, o1, o2, o3, o4, o5;
 };
 
-// EW epilogue warps with DEPTH staged stores each; NA A tiles per stage (2: high and low parts).
-template <int BN, int STAGES, int EW, int DEPTH, int NA = 1>
+// EW epilogue warps with DEPTH staged stores each; NA A tiles per stage (2: high and low parts); BNL rows of
+// B per stage in this CTA (half of BN for a CTA pair).
+template <int BN, int STAGES, int EW, int DEPTH, int NA = 1, int BNL = BN>
 struct SmemLayout {
   static constexpr int kA1Bytes = BM * BK * 2;
   static constexpr int kABytes = NA * kA1Bytes;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBBytes = BNL * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStgOffset = STAGES * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
@@ -169,9 +173,11 @@ struct Tile {
 // consecutive column tiles: a work unit is (group, row tile, group of CN column tiles) and the CTA
 // of cluster rank r computes column tile CN * unit_col + r (past the last one it computes nothing
 // that is stored, but still takes part in loading the shared operand).
-template <int BN, int BMODE, int VAR, int CN = 1>
+// With PAIR (varlen-K) the two CTAs of a cluster take the same tile of 256 rows, rank r rows 128 r ..
+template <int BN, int BMODE, int VAR, int CN = 1, bool PAIR = false>
 struct Sched {
   static constexpr int kColsPerTile = (BMODE == B_TMA_K3_GU) ? BN / 2 : BN;
+  static constexpr int kRowsPerTile = PAIR ? 2 * BM : BM;  // a CTA pair computes 256-row tiles
   int ntiles, mtiles, per_group, total, ks_len;
   int first, stride, rank;  // this CTA's first unit, the unit stride, its rank in the cluster
   const int* s_off;
@@ -184,7 +190,7 @@ struct Sched {
     first = static_cast<int>(blockIdx.x / CN);
     stride = static_cast<int>(gridDim.x / CN);
     ntiles = (p.N + kColsPerTile - 1) / kColsPerTile;
-    mtiles = (p.M + BM - 1) / BM;
+    mtiles = PAIR ? (p.M + 2 * BM - 1) / (2 * BM) : (p.M + BM - 1) / BM;
     if (VAR == VAR_M) {
       total = tile[p.groups];
     } else if (VAR == VAR_K) {
@@ -203,11 +209,11 @@ struct Sched {
       while (s_tile[gcur + 1] <= t) ++gcur;
       const int g = gcur;
       const int rows_g = s_off[g + 1] - s_off[g];
-      const int mt_g = (rows_g + BM - 1) / BM;
+      const int mt_g = (rows_g + kRowsPerTile - 1) / kRowsPerTile;
       const int l = t - s_tile[g];
-      const int mt = l % mt_g, nt = (l / mt_g) * CN + rank;
+      const int mt = l % mt_g, nt = PAIR ? l / mt_g : (l / mt_g) * CN + rank;
       tl.g = g;
-      tl.m0 = mt * BM;
+      tl.m0 = PAIR ? mt * 2 * BM + BM * rank : mt * BM;  // a pair: rows past the group read as absent
       tl.nt = nt;
       tl.n0 = nt * kColsPerTile;
       tl.rows = min(BM, rows_g - tl.m0);
@@ -219,7 +225,7 @@ struct Sched {
       const int l = t - g * per_group;
       const int mt = l % mtiles, nt = l / mtiles;
       tl.g = g;
-      tl.m0 = mt * BM;
+      tl.m0 = PAIR ? mt * 2 * BM + BM * rank : mt * BM;
       tl.nt = nt;
       tl.n0 = nt * kColsPerTile;
       tl.rows = min(BM, p.M - tl.m0);
@@ -384,25 +390,26 @@ __host__ __device__ constexpr int gemm_producers(int stages, int spare) {
 // Warp roles of one instantiation.  The gate/up GEMM gathers its A rows with 8 cp.async warps (the
 // copy rate grows with the number of issuing warps: about 16, 25 and 33 B/ns per SM with 4, 8 and 16
 // warps) and runs 512 threads, so its roles stay within 128 registers per thread.
-template <int STAGES, int EW, int AMODE, int BMODE, int CN>
+template <int STAGES, int EW, int AMODE, int BMODE, int CN, int XF = 0>
 struct WarpPlan {
   static constexpr bool kAGather = (AMODE == A_GATHER_K || AMODE == A_GATHER_MN);
   static constexpr bool kGather = kAGather || BMODE == B_GATHER_MN;
   static constexpr int kGW = (AMODE == A_GATHER_K) ? 8 : (kGather ? 4 : 0);  // gather warps
   static constexpr int kMaxWarps = (AMODE == A_GATHER_K) ? 16 : kMaxThreads / 32;
-  static constexpr int kBase = EW + 2 + kGW + (CN > 1 ? 1 : 0);
+  static constexpr int kBase = EW + 2 + kGW + ((CN > 1 && !(XF & X_PAIR)) ? 1 : 0);  // + the relay warp
   static constexpr int kNP = gemm_producers(STAGES, kMaxWarps - kBase);
   static constexpr int kThreads = (kBase + kNP - 1) * 32;
 };
 
 template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, int EPI, bool OUTF32, int CN = 1,
           int XF = 0>
-__global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads, 1)
+__global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ Maps mp) {
-  using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN>;
+  using WP = WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>;
   constexpr bool kDual = (XF & X_DUAL_A) != 0;
   constexpr bool kTrans = (XF & X_TRANS) != 0;
-  using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1>;
+  constexpr bool kPair = (XF & X_PAIR) != 0;
+  using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1, kPair ? BN / 2 : BN>;
   static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_Q) || BMODE == B_TMA_K3_GU,
@@ -430,8 +437,12 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   // Clusters of CN CTAs along N share the gathered A tile: each CTA gathers rows
   // [rank * kSlice, (rank + 1) * kSlice) and a relay thread copies them to the peers.
   static_assert(CN == 1 || (CN == 2 || CN == 4), "cluster of 1, 2 or 4");
-  static_assert(CN == 1 || (AMODE == A_GATHER_K && VAR == VAR_M && !kBGather), "clusters share a gathered A");
-  constexpr bool kRelay = (CN > 1);
+  static_assert(CN == 1 || kPair || (AMODE == A_GATHER_K && VAR == VAR_M && !kBGather), "clusters share a gathered A");
+  static_assert(!kPair || (CN == 2 && !kF8 && BN == 256 &&
+                            ((VAR == VAR_K && AMODE == A_TMA_MN && BMODE == B_TMA_MN2) ||
+                             (VAR == VAR_M && AMODE == A_TMA_K && (BMODE == B_TMA_K3 || BMODE == B_TMA_MN3)))),
+                "CTA pair: BN = 256, tiled bf16 operands (varlen-K: MN-major A, chunked B; varlen-M: K-major A)");
+  constexpr bool kRelay = (CN > 1) && !kPair;
   constexpr int kSlice = BM / CN;               // A rows gathered by each CTA of a cluster
   constexpr uint32_t kSliceBytes = kSlice * 128;
   constexpr int kRelayWarp = EW + 2 + kGW;
@@ -443,11 +454,12 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   constexpr int kXProdWarp0 = WP::kBase;  // extra producer warps
   constexpr int kThreads = WP::kThreads;
   static_assert(kThreads <= 512 && (kGW == 0 || kSlice % (kRStep > 0 ? kRStep : 1) == 0), "threads / gather rows");
+  // a pair's even CTA expects both CTAs' loads on its barrier
   constexpr uint32_t kTxBytes =
-      (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
+      kPair ? 2 * (L::kABytes + L::kBBytes) : (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
   constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc =
-      kF8 ? idesc_e4m3(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0) : idesc_bf16(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
+      kF8 ? idesc_e4m3(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0) : idesc_bf16(kPair ? 2 * BM : BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -474,12 +486,12 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       // relay mode: the producer's expect_tx and the relay's arrival; else the producer and,
       // with a gathered operand, the 128 gather threads
       mbar_init(&full_bar[s], kRelay ? 2 : 1 + (kGather ? kGW * 32 : 0));
-      mbar_init(&empty_bar[s], CN);  // every CTA of the cluster releases the stage
+      mbar_init(&empty_bar[s], kPair ? 1 : CN);  // every CTA of the cluster releases the stage (a pair: one UMMA commit)
       if (kRelay) mbar_init(&gath_bar[s], kGW * 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], EW * 32);
+      mbar_init(&tempty_bar[b], (kPair ? 2 : 1) * EW * 32);  // a pair: both CTAs' epilogues drain the tile
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -487,7 +499,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
     fence_mbar_init();
   }
   if (warp == kProdWarp) {
-    tmem_alloc(s_tmem, kTmemCols);
+    if (!kPair) tmem_alloc(s_tmem, kTmemCols);  // a pair allocates collectively once both CTAs are up
     if (lane == 0) {
       if (!kAGather) tma_prefetch_desc(&mp.a0);
       if (!kBGather) tma_prefetch_desc(&mp.b0);
@@ -507,10 +519,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       if (g < p.groups) {
         const int rows_g = s_off[g + 1] - s_off[g];
         if (rows_g < 0) bad = 1;
-        if (VAR == VAR_M)
-          cnt = max(0, (rows_g + BM - 1) / BM) *
-                (((p.N + Sched<BN, BMODE, VAR>::kColsPerTile - 1) / Sched<BN, BMODE, VAR>::kColsPerTile + CN - 1) /
-                 CN);
+        if (VAR == VAR_M) {
+          // a pair: 256-row tiles, every column tile; clusters along N: CN column tiles per unit
+          constexpr int kCpt = Sched<BN, BMODE, VAR>::kColsPerTile, kRpt = kPair ? 2 * BM : BM, kCn = kPair ? 1 : CN;
+          cnt = max(0, (rows_g + kRpt - 1) / kRpt) * (((p.N + kCpt - 1) / kCpt + kCn - 1) / kCn);
+        }
       }
       int incl = cnt;
 #pragma unroll
@@ -535,11 +548,23 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   __syncthreads();
   tc_fence_after();
   if (CN > 1) cluster_sync();  // the peers' barriers are initialised before anything targets them
+  if (kPair) {
+    if (warp == kProdWarp) tmem_alloc_pair(s_tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();
+  }
   const uint32_t tmem_base = *s_tmem;
+  const uint32_t cta_rank = kPair ? cluster_ctarank() : 0;
 
-  Sched<BN, BMODE, VAR, CN> sch;
+  Sched<BN, BMODE, VAR, CN, kPair> sch;
   sch.init(p, s_off, s_tile);
   if (*s_bad) sch.total = 0;
+  if (kPair && VAR == VAR_K && !p.b_offsets) {  // the varlen-K pair reads padded B rows only
+    if (threadIdx.x == 0) set_error(p.err, DERR_BAD_OFFSETS);
+    sch.total = 0;
+  }
 
   if (warp == kProdWarp || (warp >= kXProdWarp0 && warp < kXProdWarp0 + kNP - 1)) {
     // ---------------------------------------------------------------- TMA producers (lane 0 each)
@@ -551,6 +576,58 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       // Loads (or, with l2 = true, L2 prefetches) of the tiled operands of one stage.
       auto tiled = [&](const Tile& x, int kstage, uint8_t* sa, uint8_t* sb, uint64_t* bar, bool l2) {
         const int kg = x.k_begin + kstage * BK;
+        if (kPair) {
+          // this CTA's 128 rows of the pair's M = 256 tile (x.m0 carries the rank) and its half of B's
+          // columns (the host's B boxes are half as wide); every copy completes on the even CTA's full barrier
+          const uint32_t lb = l2 ? 0u : pair_leader_addr(bar);
+          const int rk = static_cast<int>(cta_rank);
+          if (AMODE == A_TMA_K) {
+            const int row = (p.a_offsets ? __ldg(p.a_offsets + x.g) : s_off[x.g]) + x.m0;
+            const bool first = kg < p.a_ksplit;
+            const int kc = first ? kg : kg - p.a_ksplit;
+            if (l2) {
+              tma_prefetch_l2_2d(first ? &mp.a0 : &mp.a1, kc, row);
+              if (kDual) tma_prefetch_l2_2d(first ? &mp.a2 : &mp.a3, kc, row);
+            } else {
+              tma_load_2d_pair(sa, first ? &mp.a0 : &mp.a1, lb, kc, row);
+              if (kDual) tma_load_2d_pair(sa + L::kA1Bytes, first ? &mp.a2 : &mp.a3, lb, kc, row);
+            }
+          } else {
+            const int ka = kg >= p.a_kwrap ? kg - p.a_kwrap : kg;
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c) {
+              const int col = x.m0 + 64 * c;
+              const bool first = col < p.a_colsplit;
+              const int cc = first ? col : col - p.a_colsplit;
+              if (l2) {
+                tma_prefetch_l2_2d(first ? &mp.a0 : &mp.a1, cc, ka);
+                if (kDual) tma_prefetch_l2_2d(first ? &mp.a2 : &mp.a3, cc, ka);
+              } else {
+                tma_load_2d_pair(sa + c * (BK * 128), first ? &mp.a0 : &mp.a1, lb, cc, ka);
+                if (kDual) tma_load_2d_pair(sa + L::kA1Bytes + c * (BK * 128), first ? &mp.a2 : &mp.a3, lb, cc, ka);
+              }
+            }
+          }
+          if (BMODE == B_TMA_K3) {  // 3-D weights {K, N, groups}: BN / 2 rows of N
+            const int n = x.n0 + (BN / 2) * rk;
+            if (l2) tma_prefetch_l2_3d(&mp.b0, kg, n, x.g);
+            else tma_load_3d_pair(sb, &mp.b0, lb, kg, n, x.g);
+          } else if (BMODE == B_TMA_MN3) {  // 4-D view {64 columns, K rows, N/64 chunks, groups}: BN / 128 chunks
+            const bool first = kg < p.b_ksplit;
+            const int kc = first ? kg : kg - p.b_ksplit;
+            const int chunk = x.n0 / 64 + (BN / 128) * rk;
+            if (l2) tma_prefetch_l2_4d(first ? &mp.b0 : &mp.b1, 0, kc, chunk, x.g);
+            else tma_load_4d_pair(sb, first ? &mp.b0 : &mp.b1, lb, 0, kc, chunk, x.g);
+          } else {
+            // padded B rows: the group's reduction rows start at b_offsets[g]; 3-D view {64 columns, rows,
+            // N/64 chunks} with boxes of BN/128 chunks
+            const int kgb = __ldg(p.b_offsets + x.g) + kstage * BK;
+            const int chunk = x.n0 / 64 + (BN / 128) * rk;
+            if (l2) tma_prefetch_l2_3d(&mp.b0, 0, kgb, chunk);
+            else tma_load_3d_pair(sb, &mp.b0, lb, 0, kgb, chunk);
+          }
+          return;
+        }
         if (AMODE == A_TMA_K) {
           const int row = (VAR == VAR_M ? (p.a_offsets ? __ldg(p.a_offsets + x.g) : s_off[x.g]) : 0) + x.m0;
           const CUtensorMap* mp_a = kg < p.a_ksplit ? &mp.a0 : &mp.a1;
@@ -629,7 +706,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
         uint8_t* sa = smem + s * L::kStageBytes;
         uint8_t* sb = sa + L::kABytes;
         if (kTxBytes > 0) {
-          mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
+          if (!kPair || cta_rank == 0) mbar_arrive_expect_tx(&full_bar[s], kTxBytes);
           tiled(q.tl, q.ks, sa, sb, &full_bar[s], false);
           // L2 prefetch of the stages ahead of this one within the tile
           if (!p.l2_prefetch) {
@@ -644,7 +721,12 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
         ++it;
         pos_next(sch, p, gcur, q);
       }
-      if (aborted) {
+      if (aborted && kPair) {
+        // the copies count on the even CTA's barriers: give those in flight 20 ms to land
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 20000000ull) {
+        }
+      } else if (aborted) {
         // let this thread's copies already in flight land before the CTA goes away
         volatile int never = 0;
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
@@ -796,8 +878,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
         pos_next(sch, p, gcur, q);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp && (!kPair || cta_rank == 0)) {
     // ---------------------------------------------------------------- UMMA issuer (lane 0)
+    // (a pair: the even CTA's, for both CTAs)
     // With both operands tiled in the varlen-K mode, the last stage of a group reads rows of the
     // next group (or the zeroed tail): its UMMAs stop at the K step (16 rows) that holds the group's
     // last row, and the whole warp clears the rows of that step past the group's end in B before
@@ -813,7 +896,10 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           sch.decode(p, t, gcur, tl);
           const int nk = (tl.k_len + BK - 1) / BK;
           const int buf = acc & 1;
-          if (!mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)) break;
+          // a pair: the odd CTA's epilogue released the accumulator with cluster-scope arrivals
+          if (!(kPair ? mbar_wait_cluster(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)
+                      : mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)))
+            break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
           for (int ks = 0; ks < nk; ++ks, ++it) {
@@ -833,21 +919,28 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
                   kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
               const uint64_t bd =
                   kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-              umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
-              if (kDual)  // the low part of A times the same B, into the same accumulator
-                umma_step<kF8>(d_tmem,
-                               kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
-                                    : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024),
-                               bd, kIdesc, 1u);
+              // dual A: the low part of A times the same B, into the same accumulator
+              const uint64_t adl = kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
+                                        : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024);
+              if (kPair) {  // same offsets in both CTAs: each holds its rows of A and its columns of B
+                umma_bf16_pair(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                if (kDual) umma_bf16_pair(d_tmem, adl, bd, kIdesc, 1u);
+              } else {
+                umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                if (kDual) umma_step<kF8>(d_tmem, adl, bd, kIdesc, 1u);
+              }
             }
-            if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
+            if (kPair) umma_commit_pair_mc(&empty_bar[s], 3);  // both CTAs' stage s is free
+            else if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
             else umma_commit(&empty_bar[s]);
           }
           if (aborted) break;
-          umma_commit(&tfull_bar[buf]);
+          if (kPair) umma_commit_pair_mc(&tfull_bar[buf], 3);  // both CTAs' halves of the accumulator are ready
+          else umma_commit(&tfull_bar[buf]);
         }
         if (*s_abort) {
-          umma_commit(drain_bar);
+          if (kPair) umma_commit_pair_mc(drain_bar, 1);
+          else umma_commit(drain_bar);
           volatile int never = 0;
           mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
         }
@@ -862,7 +955,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
       const int buf = acc & 1;
       // lane 0 waits, the warp follows its verdict (the other lanes block in the shuffle)
       int ok = 0;
-      if (lane == 0) ok = mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err);
+      if (lane == 0)  // a pair: the odd CTA's epilogue released it with cluster-scope arrivals
+        ok = kPair ? mbar_wait_cluster(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err)
+                   : mbar_wait(&tempty_bar[buf], ((acc >> 1) & 1) ^ 1, s_abort, p.timeout_ns, p.err);
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
         aborted = true;
         break;
@@ -908,25 +1003,33 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             if (kk >= nkk) break;
             const uint64_t ad = kAMn ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = kBMn ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
             // dual A: the low part times the same B, into the same accumulator
-            if (kDual)
-              umma_step<kF8>(d_tmem,
-                             kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
-                                  : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024),
-                             bd, kIdesc, 1u);
+            const uint64_t adl = kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
+                                      : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024);
+            if (kPair) {  // same offsets in both CTAs' shared memory: each holds its rows of A, its columns of B
+              umma_bf16_pair(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+              if (kDual) umma_bf16_pair(d_tmem, adl, bd, kIdesc, 1u);
+            } else {
+              umma_step<kF8>(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+              if (kDual) umma_step<kF8>(d_tmem, adl, bd, kIdesc, 1u);
+            }
           }
-          if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
+          if (kPair) umma_commit_pair_mc(&empty_bar[s], 3);  // both CTAs' stage s is free
+          else if (CN > 1) umma_commit_mc(&empty_bar[s], static_cast<uint16_t>((1u << CN) - 1u));
           else umma_commit(&empty_bar[s]);
         }
         __syncwarp();
       }
       if (aborted) break;
-      if (lane == 0) umma_commit(&tfull_bar[buf]);
+      if (lane == 0) {
+        if (kPair) umma_commit_pair_mc(&tfull_bar[buf], 3);  // both CTAs' halves of the accumulator are ready
+        else umma_commit(&tfull_bar[buf]);
+      }
       __syncwarp();
     }
     if (aborted && lane == 0) {
-      umma_commit(drain_bar);
+      if (kPair) umma_commit_pair_mc(drain_bar, 1);
+      else umma_commit(drain_bar);
       volatile int never = 0;
       mbar_wait(drain_bar, 0, &never, 20000000ull, nullptr);
     }
@@ -1168,7 +1271,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
           o.c_z = tl.split;
           o.c_row = mw;
         }
-        if (kTrans) {
+        if (VAR == VAR_K && mw >= p.M) {
+          // rows past the output (the odd CTA of a pair on the last row tile): nothing to store
+        } else if (kTrans) {
           // Each 32 x 32 block leaves transposed: block row i = accumulator column col + i (an output
           // row), block column = this thread's tile row (output column mw + lane).  Staged in the swizzled
           // layout of the store map (fp32 rows of 128 B, bf16 rows of 64 B); the TMA store clips rows and
@@ -1179,7 +1284,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
             tmem_ld32(tbase + c, r);
             tmem_ld_wait();
             const int col = tl.n0 + c;
-            if (col >= p.N || mw >= p.M) continue;  // a block wholly past the output (M, N multiples of 64)
+            if (col >= p.N) continue;  // a block wholly past the output (N a multiple of 64)
             uint8_t* stg = next_stage_buf();
             if (OUTF32) {
 #pragma unroll
@@ -1246,7 +1351,8 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty_bar[buf]);
+      if (kPair && cta_rank != 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
+      else mbar_arrive(&tempty_bar[buf]);
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -1256,7 +1362,10 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThrea
   __syncthreads();
   tc_fence_after();
   if (CN > 1) cluster_sync();  // peers finished with this CTA's shared memory
-  if (warp == kProdWarp) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == kProdWarp) {
+    if (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // grid: CTAs wanted (at most one per SM); with CN > 1 it is rounded to whole clusters and capped
@@ -1265,11 +1374,12 @@ template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, 
           int XF = 0>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32, CN, XF>;
-  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH, (XF & X_DUAL_A) ? 2 : 1>::bytes(p.groups, VAR);
+  const size_t smem =
+      SmemLayout<BN, STAGES, EW, DEPTH, (XF & X_DUAL_A) ? 2 : 1, (XF & X_PAIR) ? BN / 2 : BN>::bytes(p.groups, VAR);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
-  const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN>::kThreads;
+  const int threads = WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kThreads;
   if (CN == 1) {
     kern<<<grid, threads, smem, stream>>>(p, maps);
     return cudaGetLastError();

@@ -9,7 +9,12 @@ namespace vgg {
 // ([SM] "4.2 Epilogue 융합": one epilogue emits dH, dS and A').
 // Four stages with one staged store per epilogue warp when the group table leaves room (measured
 // 5-7% faster than three stages with two).
-cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+// A CTA pair (pair: each CTA loads 128 of the 256 columns of B) takes 32 KB stages, so six fit.
+cudaError_t run_dact_dswiglu(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (pair && BN == 256 && SmemLayout<256, 6, 8, 1, 1, 128>::bytes(p.groups, VAR_M) <= kMaxSmem)
+    return launch_grouped_gemm<256, 6, 8, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false, 2, X_PAIR>(p, m, grid, s);
+  if (pair && BN == 256)
+    return launch_grouped_gemm<256, 5, 8, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false, 2, X_PAIR>(p, m, grid, s);
   if (BN == 256 && SmemLayout<256, 4, 8, 1>::bytes(p.groups, VAR_M) <= kMaxSmem)
     return launch_grouped_gemm<256, 4, 8, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
   if (BN == 256) return launch_grouped_gemm<256, 3, 8, 2, A_TMA_K, B_TMA_MN3, VAR_M, EPI_DSWIGLU, false>(p, m, grid, s);
@@ -17,7 +22,9 @@ cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int gri
 }
 
 // dXp = [dH | dU] [W_gate[e]; W_up[e]]  (reduction over 2n, B read MN-major from two maps)
-cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+cudaError_t run_dx_store(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (pair && BN == 256)
+    return launch_grouped_gemm<256, 6, 4, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false, 2, X_PAIR>(p, m, grid, s);
   if (BN == 256) return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
   return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_MN3, VAR_M, EPI_STORE, false>(p, m, grid, s);
 }
@@ -32,28 +39,6 @@ cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, i
                : launch_grouped_gemm<256, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
   return f32 ? launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true>(p, m, grid, s)
              : launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
-}
-
-// Varlen-K weight gradient with a two-part A: the per-pair gradients as a bf16 high part and the bf16
-// rounding of the rest (two UMMAs per K step into one accumulator), B the expert-sorted input rows.  A
-// stage holds both A tiles and B (BN = 256: 64 KB, so three stages); four epilogue warps measured faster
-// than eight (c2: dW gate/up 254 -> 231 us, dW down 131 -> 128 us).  trans: the tile is D^T of the
-// stored output (dW_down[e] = dO^T A' computed as A'^T dO: M = n, N = d), written through transposed
-// 32 x 32 blocks.
-cudaError_t run_dw_dual(int BN, bool f32, bool trans, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  constexpr int D = X_DUAL_A, DT = X_DUAL_A | X_TRANS;
-  if (BN == 256) {
-    if (trans)
-      return f32 ? launch_grouped_gemm<256, 3, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, DT>(p, m, grid, s)
-                 : launch_grouped_gemm<256, 3, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, DT>(p, m, grid, s);
-    return f32 ? launch_grouped_gemm<256, 3, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, D>(p, m, grid, s)
-               : launch_grouped_gemm<256, 3, 4, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, D>(p, m, grid, s);
-  }
-  if (trans)
-    return f32 ? launch_grouped_gemm<128, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, DT>(p, m, grid, s)
-               : launch_grouped_gemm<128, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, DT>(p, m, grid, s);
-  return f32 ? launch_grouped_gemm<128, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, D>(p, m, grid, s)
-             : launch_grouped_gemm<128, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, D>(p, m, grid, s);
 }
 
 // Varlen-K with one operand gathered through a token index (cp.async, zero past the group's end).

@@ -29,7 +29,11 @@ cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid,
 
 // The down projection with A as a bf16 high part and the bf16 rounding of the rest (two UMMAs per K step
 // into one accumulator); a stage holds both A tiles and B (BN = 256: 64 KB, three stages).
-cudaError_t run_down_scale_dual(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+// A CTA pair (pair: each CTA loads 128 of the 256 columns of B) takes 48 KB stages, four of them.
+cudaError_t run_down_scale_dual(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (pair && BN == 256)
+    return launch_grouped_gemm<256, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 2, X_DUAL_A | X_PAIR>(p, m,
+                                                                                                          grid, s);
   if (BN == 256)
     return launch_grouped_gemm<256, 3, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_DUAL_A>(p, m, grid, s);
   return launch_grouped_gemm<128, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_DUAL_A>(p, m, grid, s);

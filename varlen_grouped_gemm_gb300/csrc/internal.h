@@ -40,19 +40,21 @@ cudaError_t launch_transpose_into_bf16(const __nv_bfloat16* in, int E, int R, in
 cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                       uint8_t* q, float* scales, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_down_scale_dual(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_down_scale_dual(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
-cudaError_t run_dact_dswiglu(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_dx_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dact_dswiglu(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dx_store(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_down(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_dw_dual(int BN, bool f32, bool trans, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dw_dual(int BN, bool f32, bool trans, bool pair, const GemmParams& p, const Maps& m, int grid,
+                        cudaStream_t s);
 cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // test exports
-cudaError_t run_test_m(int gathered, int b_kmajor, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_test_m_dual(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_test_m(int gathered, int b_kmajor, bool pair, const GemmParams& p, const Maps& m, int grid,
+                       cudaStream_t s);
+cudaError_t run_test_m_dual(bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 
 // Expert-sorted copies of two [T, d] bf16 tensors (rows without a pair zeroed), and optionally of per-token
 // e4m3 code rows c with their scales cs (rows without a pair: zero codes, scale 1).  With poff the two bf16
