@@ -808,7 +808,8 @@ def run_ours(args, rank, world, local_rank):
                        "empty_experts": int((counts == 0).sum()),
                        "max_rows_per_expert": int(counts.max()), "dW_dtype": "bf16",
                        "l2": "flushed between steps (256 MB write, outside the per-step events)",
-                       "launch": "eager calls" if graph is None else "the step's 18 launches as one CUDA graph",
+                       "launch": ("eager calls" if graph is None else
+                                  f"the step's {gpu_launches // max(args.steps, 1)} launches as one CUDA graph"),
                        "clock_samples": "nvidia-smi every 50 ms over a 0.5 s busy pre-roll of the same step and the timed region",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tokens_per_s": tokens_s, "pct_of_peak_bf16": 100 * tflops / world / pk["bf16_sus"],
