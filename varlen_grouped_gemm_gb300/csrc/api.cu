@@ -190,11 +190,22 @@ struct BwdWs {
   float* wr_part;
 };
 
+// Column tile of the dSwiGLU GEMM (dA' = dO W_down, N = n), which also sets the number of dS partials per pair:
+// 256 columns, or 128 when 256-column tiles would give fewer than eight waves over the SMs (c2, n = 512: 768
+// tiles on 152 SMs; 186 -> 166 us with 128 columns, while at 2560 tiles and more 256 columns stay 4-28% faster).
+// The workspace holds the partials of 128-column tiles either way.
+inline int dact_bn(int n, long long cap, int E, int num_sms) {
+  if (n <= 128) return 128;
+  const long long tiles256 = static_cast<long long>(ceil_div(cap, BM) + E) * ceil_div(n, 256);
+  return tiles256 >= 8ll * num_sms ? 256 : 128;
+}
+inline int dact_part_ld_max(int n) { return ceil_div(n, 128) * 2; }
+
 // Rows of the padded sorted copies: every group rounded up to a multiple of 16 rows.
 inline long long padded_rows(long long cap, int E) { return cap + 15ll * E; }
 
 size_t bwd_ws_bytes(int T, int d, int E, int n, long long cap) {
-  const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
+  const int part_ld = dact_part_ld_max(n);
   const long long cp = padded_rows(cap, E);
   return 6 * al(sizeof(__nv_bfloat16) * cap * n) + al(sizeof(__nv_bfloat16) * cap * d) +
          2 * al(sizeof(__nv_bfloat16) * cp * d) + al(sizeof(int32_t) * (E + 1)) +
@@ -210,7 +221,7 @@ bool make_lo_maps(Maps& m, const BwdWs& w, int n, long long cap) {
 }
 
 BwdWs carve_bwd(void* ws, int T, int d, int E, int n, long long cap) {
-  const int part_ld = ceil_div(n, gemm_bn(n)) * 2;
+  const int part_ld = dact_part_ld_max(n);
   uint8_t* p = static_cast<uint8_t*>(ws);
   BwdWs w{};
   auto take = [&](size_t bytes) {
@@ -752,7 +763,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   BwdWs w = carve_bwd(ws, T, d, E, n, cap);
   const bool f32 = dW_fp32 != 0;
-  const int bn6 = gemm_bn(n);
+  const int bn6 = dact_bn(n, cap, E, ctx->num_sms);
   const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
   if (cap > static_cast<long long>(T) * K) {
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
