@@ -61,3 +61,28 @@ def test_edge_case_layer(ctx, wl):
     if wl.m_tile:
         assert np.all(g["counts"] % wl.m_tile == 0)
     print(wl.name, "P", g["P"], {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
+
+
+def test_nan_poisoned_buffers_token_rounding(ctx):
+    """Every float buffer and the workspace start as NaN bit patterns.  Token rounding leaves rows past the
+    last pair in the pair-indexed buffers (P < cap), which the GEMMs load with their last tiles and stages;
+    neither those rows nor any scratch may reach an output."""
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.scaled(synth.WORKLOADS["c5"], name="tr_poisoned", T=600, d=320, E=16, n=192, K=4, m_tile=64)
+    inp = Inputs(wl)
+    dv = inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.float32)
+    for name in ("logits", "scores", "topk_w", "sorted_w", "H", "U", "A", "Yw", "O", "dX", "dW_gate", "dW_up",
+                 "dW_down", "dS", "dlogits", "dW_r", "ws"):
+        t = getattr(buf, name)
+        if t is not None:
+            t.view(torch.uint8).fill_(0xFF)
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    vgg.backward(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    g = gpu_routing(buf)
+    assert g["P"] + 16 <= buf.sorted_tok.numel(), "the case must leave rows past the last pair"
+    check_routing_bit_exact(g, wl.K, wl.m_tile)
+    O_ref, cache, grads = oracle_layer(inp, g)
+    compare_layer(buf, inp, O_ref, cache, grads)

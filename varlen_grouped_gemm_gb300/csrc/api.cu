@@ -766,8 +766,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   const int bn6 = dact_bn(n, cap, E, ctx->num_sms);
   const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
   if (cap > static_cast<long long>(T) * K) {
-    VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH, w.dU, w.Ap, s));
-    VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, w.dH_lo, w.dU_lo, w.Ap_lo, s));
+    __nv_bfloat16* const tail[6] = {w.dH, w.dU, w.Ap, w.dH_lo, w.dU_lo, w.Ap_lo};
+    VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, tail, s));
   }
   // e4m3 dSwiGLU GEMM: dO quantized once per token (a token's pairs share its row, so its codes are those of
   // every pair) into the dX partials' region, which is free until the dX GEMM; the gather below copies the

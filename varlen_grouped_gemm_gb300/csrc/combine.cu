@@ -317,27 +317,34 @@ cudaError_t launch_wait_timeout_probe(int* err, unsigned long long timeout_ns, c
 
 namespace vgg {
 
-// Rows [offsets[E], cap) of the backward's per-pair buffers are never written by the GEMMs; the
-// varlen-K weight-gradient GEMM reads whole 64-row boxes of them (multiplied by zero-filled gathered
-// rows), so they must hold finite values: zero them.
+// Rows [offsets[E], cap) of the backward's per-pair buffers are never written by the GEMMs.  The varlen-K
+// weight-gradient GEMM multiplies the rows of its last expert's last 16-row UMMA K step, up to 15 rows past
+// offsets[E], by zero rows of B, so those must hold finite values: zero them (rows further on are loaded into
+// shared memory with the stage but never multiplied; the varlen-M GEMMs drop the accumulator rows they touch).
+struct TailBufs {
+  __nv_bfloat16* p[6];
+};
+
 __global__ void zero_tail_rows_kernel(const int32_t* __restrict__ offsets, int E, long long cap, int cols,
-                                      __nv_bfloat16* a, __nv_bfloat16* b, __nv_bfloat16* c) {
+                                      TailBufs bufs) {
   const long long P = offsets[E];
   if (P < 0 || P >= cap) return;
-  const long long n = (cap - P) * cols / 8;  // 16-byte vectors per buffer
+  const long long n = min(cap - P, 16ll) * cols / 8;  // 16-byte vectors per buffer
   const uint4 z = make_uint4(0, 0, 0, 0);
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long off = P * cols + 8 * i;
-    if (a) *reinterpret_cast<uint4*>(a + off) = z;
-    if (b) *reinterpret_cast<uint4*>(b + off) = z;
-    if (c) *reinterpret_cast<uint4*>(c + off) = z;
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+      if (bufs.p[k]) *reinterpret_cast<uint4*>(bufs.p[k] + off) = z;
   }
 }
 
-cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols, __nv_bfloat16* a,
-                                  __nv_bfloat16* b, __nv_bfloat16* c, cudaStream_t s) {
-  zero_tail_rows_kernel<<<64, 256, 0, s>>>(offsets, E, cap, cols, a, b, c);
+cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols,
+                                  __nv_bfloat16* const (&bufs)[6], cudaStream_t s) {
+  TailBufs b;
+  for (int k = 0; k < 6; ++k) b.p[k] = bufs[k];
+  zero_tail_rows_kernel<<<8, 256, 0, s>>>(offsets, E, cap, cols, b);
   return cudaGetLastError();
 }
 

@@ -69,9 +69,10 @@ cudaError_t launch_gather_rows(const int32_t* offsets, const int32_t* poff, long
 // poff[g] = sum over the groups before g of their row counts rounded up to 16; poff[E] the total.
 cudaError_t launch_pad_offsets(const int32_t* offsets, int E, int32_t* poff, int* err, cudaStream_t s);
 
-// Zero rows [offsets[E], cap) of up to three [cap, cols] bf16 buffers (the tail past the last pair).
-cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols, __nv_bfloat16* a,
-                                  __nv_bfloat16* b, __nv_bfloat16* c, cudaStream_t s);
+// Zero rows [offsets[E], min(offsets[E] + 16, cap)) of up to six [cap, cols] bf16 buffers (past the last pair;
+// null entries are skipped).
+cudaError_t launch_zero_tail_rows(const int32_t* offsets, int E, long long cap, int cols,
+                                  __nv_bfloat16* const (&bufs)[6], cudaStream_t s);
 
 // ---- routing / permutation -----------------------------------------------------------------
 // Top-K and combine weights; with part != nullptr the logits are first summed from `split` partials
