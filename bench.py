@@ -199,6 +199,7 @@ _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
     "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "transpose_f32_kernel": "permute",
     "perm_escan_kernel": "permute", "cap_select_kernel": "permute", "slot_offsets_kernel": "permute",
+    "perm_fused_kernel": "permute",
     "combine_kernel": "combine",
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
@@ -702,7 +703,9 @@ def run_ours(args, rank, world, local_rank):
     dname, (dms, dlaunch) = max(prof.items(), key=lambda kv: kv[1][0])
     roof = roofline(dname, work, dms, dlaunch, pk, recorded_traffic(wl.name, dname))
     kernels = kernel_table(prof, work, args.steps, pk)
-    launches_per_label = {"permute": (10 if (wl.m_tile or wl.capacity_factor) else 4)}  # the grouping's kernels
+    # the grouping's kernels: one cooperative launch per grouping (token rounding and the capacity dispatch
+    # group twice, with a select kernel and a transpose or slot-offset kernel between)
+    launches_per_label = {"permute": (4 if (wl.m_tile or wl.capacity_factor) else 1)}
     gpu_launches = int(sum(cnt * launches_per_label.get(k, 1) for k, (_, cnt) in prof.items()))
 
     # end to end through the public API with host buffers: H2D of X and dO, D2H of O and dX per step

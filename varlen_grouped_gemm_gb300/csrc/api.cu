@@ -377,14 +377,16 @@ int vgg::permute_plain_with_scratch(moe_ctx* ctx, const int32_t* topk_ids, const
   VGG_REQUIRE(cap >= moe_pair_capacity(T, E, K, 0) && cap < INT_MAX);
   const int tb = perm_tok_block(T, E);
   const int nb = (T + tb - 1) / tb;
-  if (static_cast<long long>(E + 1) * nb + 1 > scratch_ints) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(E + 1) * nb + 2 > scratch_ints) return MOE_ERR_UNSUPPORTED;
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   PermuteWs w{};
   w.hist = scratch;
   w.tokblk = scratch + static_cast<long long>(E) * nb;
+  w.barrier = w.tokblk + nb + 1;
   VGG_LAUNCH("permute", launch_permute(topk_ids, topk_w, nullptr, nullptr, T, E, K, 0, cap, counts, offsets,
-                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
+                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, ctx->timeout_ns,
+                                       s));
   return MOE_OK;
 }
 
@@ -551,7 +553,8 @@ int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, cons
   PermuteWs w = carve_permute_ws(ws, T, E, K, m_tile);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   VGG_LAUNCH("permute", launch_permute(topk_ids, topk_w, logits, scores, T, E, K, m_tile, cap, counts, offsets,
-                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
+                                       sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, ctx->timeout_ns,
+                                       s));
   return MOE_OK;
 }
 
@@ -572,7 +575,8 @@ int moe_permute_capacity(moe_ctx* ctx, const int32_t* topk_ids, const float* top
   PermuteWs w = carve_permute_ws(ws, T, E, K, 1);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   VGG_LAUNCH("permute", launch_permute_capacity(topk_ids, topk_w, T, E, K, C, policy, cap, counts, offsets,
-                                                sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err, s));
+                                                sorted_tok, sorted_w, tok_ptr, tok_pairs, P_out, w, ctx->d_err,
+                                                ctx->timeout_ns, s));
   return MOE_OK;
 }
 

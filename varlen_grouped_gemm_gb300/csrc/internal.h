@@ -83,6 +83,7 @@ cudaError_t launch_topk_softmax(float* logits, const float* part, int split, con
 struct PermuteWs {
   int32_t* hist;       // [E * nb]
   int32_t* tokblk;     // [nb + 1]
+  int* barrier;        // [1] grid-barrier counter of the one-launch grouping (right after tokblk)
   uint32_t* member;    // [T * ceil(E/32)] final pair bitmap (token rounding)
   int32_t* plain_off;  // [E + 1]
   int32_t* plain_cnt;  // [E]
@@ -103,14 +104,15 @@ PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile);
 cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const float* logits, const float* scores,
                            int T, int E, int K, int m_tile, long long cap, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
-                           int32_t* P_out, const PermuteWs& w, int* err, cudaStream_t s);
+                           int32_t* P_out, const PermuteWs& w, int* err, unsigned long long timeout_ns,
+                           cudaStream_t s);
 
 // Capacity (drop/pad) dispatch: the kept pairs of expert e in slots [e C, (e + 1) C), offsets e C.
 // Uses the token-rounding workspace layout (m_tile > 0).
 cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
                                     int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
                                     float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
-                                    const PermuteWs& w, int* err, cudaStream_t s);
+                                    const PermuteWs& w, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 // ---- combine / reductions --------------------------------------------------------------------
 cudaError_t launch_combine(const __nv_bfloat16* Y, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,

@@ -19,10 +19,12 @@ namespace {
 
 constexpr int kNoAllocMaxT = 32768;                // tokens
 constexpr int kNoAllocMaxE = 512;                  // experts
-constexpr int kNoAllocBlocks = kNoAllocMaxT / 256;  // the array holds (E + 1) x 128 + 1 counts
-constexpr int kNoAllocScratchInts = kNoAllocMaxE * kNoAllocBlocks + kNoAllocBlocks + 1;  // hist + block bases
+constexpr int kNoAllocBlocks = kNoAllocMaxT / 256;  // the array holds (E + 1) x 128 + 2 counts
+// hist + block bases + their total + the one-launch grouping's barrier counter
+constexpr int kNoAllocScratchInts = kNoAllocMaxE * kNoAllocBlocks + kNoAllocBlocks + 2;
 
-// 65,665 ints = 257 KiB; contents are fully rewritten by every call before they are read.
+// 65,666 ints = 257 KiB; contents are fully rewritten (the barrier counter zeroed) by every call before they
+// are read.
 __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;

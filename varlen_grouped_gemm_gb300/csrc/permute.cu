@@ -338,6 +338,163 @@ __global__ void __launch_bounds__(TB) perm_scatter_kernel(
   }
 }
 
+// Grid-wide barrier of a cooperative launch (every block resident): thread 0 of each block arrives on
+// `counter` (zeroed before the launch) and waits, bounded by timeout_ns, until `target` arrivals.  The
+// block's writes before the barrier are visible to every block after it.  Returns false, with
+// MOE_DEV_TIMEOUT recorded, when the wait gave up.
+__device__ bool grid_barrier(int* counter, int target, unsigned long long timeout_ns, int* err, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();
+    atomicAdd(counter, 1);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if ((i & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) {
+        set_error(err, DERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// The whole grouping in one cooperative launch (one block per TB tokens, all resident), with the results of
+// perm_hist + perm_escan + perm_scan + perm_scatter: (1) a block's membership bits per expert, its per-expert
+// counts hist[e][b] and its pair count; grid barrier; (2) one warp per expert turns hist[e][*] into in-expert
+// exclusive prefixes over the blocks (block order = token order) and writes the expert's total; grid barrier;
+// (3) every block scans the expert totals (offsets; block 0 writes them, offsets[E] = P and the capacity
+// check) and sums the pair counts of the blocks before it, then scatters its pairs with the bits it kept in
+// shared memory.  Data written by other blocks during the launch is read with L1-bypassing loads.
+template <bool FROM_MEMBER, int TB>
+__global__ void __launch_bounds__(TB) perm_fused_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ topk_w, const uint32_t* __restrict__ member,
+    const float* __restrict__ logits, int T, int E, int K, int nb, int32_t* hist, int32_t* tokblk, int* barrier,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ P_out, long long cap,
+    int32_t* __restrict__ sorted_tok, float* __restrict__ sorted_w, int32_t* __restrict__ tok_ptr,
+    int32_t* __restrict__ tok_pairs, int* err, int slot_stride, unsigned long long timeout_ns) {
+  constexpr int NW = TB / 32;
+  constexpr int kMaxPairs = FROM_MEMBER ? 32 : 8;
+  extern __shared__ uint32_t fsm[];  // bits [E][NW], then the expert offsets [E + 1]
+  uint32_t* bits = fsm;
+  int* s_eoff = reinterpret_cast<int*>(fsm + E * NW);
+  __shared__ int s_warp[33];
+  __shared__ int s_ok, s_tokbase, s_toktotal;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // (1) this block's tokens
+  for (int i = tid; i < E * NW; i += TB) bits[i] = 0;
+  __syncthreads();
+  const int t = b * TB + tid;
+  int es[kMaxPairs];
+  float ws[kMaxPairs];
+  int cnt = 0;
+  if (t < T) {
+    cnt = token_experts<FROM_MEMBER>(t, ids, topk_w, member, logits, E, K, es, ws, kMaxPairs, err);
+    if (cnt > kMaxPairs) {
+      set_error(err, DERR_CAPACITY);
+      cnt = kMaxPairs;
+    }
+    for (int q = 0; q < cnt; ++q) atomicOr(&bits[es[q] * NW + warp], 1u << lane);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += TB) {
+    int n = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) n += __popc(bits[e * NW + w]);
+    hist[static_cast<long long>(e) * nb + b] = n;
+  }
+  int btotal;
+  const int tprefix = block_exclusive_scan_256(cnt, s_warp, btotal);
+  if (tid == 0) tokblk[b] = btotal;
+  if (!grid_barrier(barrier, nb, timeout_ns, err, &s_ok)) return;
+  // (2) in-expert prefixes over the blocks
+  for (int e = b * NW + warp; e < E; e += nb * NW) {
+    int32_t* h = hist + static_cast<long long>(e) * nb;
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int bb = b0 + lane;
+      const int v = bb < nb ? __ldcg(h + bb) : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (bb < nb) h[bb] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) counts[e] = carry;
+  }
+  if (!grid_barrier(barrier, 2 * nb, timeout_ns, err, &s_ok)) return;
+  // (3) expert offsets, this block's first pair, the scatter
+  int ecarry = 0;
+  for (int base = 0; base < E; base += TB) {
+    const int e = base + tid;
+    const int v = e < E ? __ldcg(counts + e) : 0;
+    int tot;
+    const int ex = block_exclusive_scan_256(v, s_warp, tot);
+    if (e < E) s_eoff[e] = ecarry + ex;
+    ecarry += tot;
+  }
+  int tb_before = 0, tb_all = 0;
+  for (int i = tid; i < nb; i += TB) {
+    const int v = __ldcg(tokblk + i);
+    if (i < b) tb_before += v;
+    tb_all += v;
+  }
+  {
+    int tot;
+    block_exclusive_scan_256(tb_before, s_warp, tot);
+    if (tid == 0) s_tokbase = tot;
+    block_exclusive_scan_256(tb_all, s_warp, tot);
+    if (tid == 0) s_toktotal = tot;
+  }
+  if (tid == 0) s_eoff[E] = ecarry;
+  __syncthreads();
+  if (b == 0) {
+    for (int e = tid; e <= E; e += TB) offsets[e] = s_eoff[e];
+    if (tid == 0) {
+      if (P_out) *P_out = ecarry;
+      if (ecarry > cap || s_toktotal != ecarry) set_error(err, DERR_CAPACITY);
+    }
+  }
+  const long long tp = static_cast<long long>(s_tokbase) + tprefix;
+  if (t < T && tok_ptr) tok_ptr[t] = static_cast<int32_t>(tp);
+  if (t == T - 1 && tok_ptr) tok_ptr[T] = static_cast<int32_t>(tp + cnt);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  long long first[kMaxPairs];
+#pragma unroll
+  for (int q = 0; q < kMaxPairs; ++q) {
+    if (q < cnt) {
+      const int e = es[q];
+      first[q] = static_cast<long long>(__ldcg(hist + static_cast<long long>(e) * nb + b)) +
+                 (slot_stride > 0 ? static_cast<long long>(e) * slot_stride : s_eoff[e]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxPairs; ++q) {
+    if (q >= cnt) break;
+    const int e = es[q];
+    int rank = __popc(bits[e * NW + warp] & lt_mask);
+    for (int w = 0; w < warp; ++w) rank += __popc(bits[e * NW + w]);
+    const long long j = first[q] + rank;
+    if (j >= cap || tp + q >= cap) {
+      set_error(err, DERR_CAPACITY);
+      continue;
+    }
+    sorted_tok[j] = t;
+    if (sorted_w) sorted_w[j] = ws[q];
+    if (tok_pairs) tok_pairs[tp + q] = static_cast<int32_t>(j);
+  }
+}
+
 // out[c][r] = in[r][c] for fp32 [rows x cols], 32x32 tiles through shared memory: the token
 // rounding select reads one expert's scores for all tokens, a column of the [T x E] scores.
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out) {
@@ -707,7 +864,7 @@ size_t permute_ws_bytes(int T, int E, int K, int m_tile) {
   const int tb = perm_tok_block(T, E);
   const long long nb = (T + tb - 1) / tb;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  size_t b = al(sizeof(int32_t) * E * nb) + al(sizeof(int32_t) * (nb + 1));
+  size_t b = al(sizeof(int32_t) * E * nb) + al(sizeof(int32_t) * (nb + 2));
   if (m_tile > 0) {
     b += al(sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32));
     b += al(sizeof(int32_t) * (E + 1)) + al(sizeof(int32_t) * E) + al(sizeof(int32_t) * static_cast<size_t>(T) * K);
@@ -725,7 +882,8 @@ PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile) {
   w.hist = reinterpret_cast<int32_t*>(p);
   p += al(sizeof(int32_t) * E * nb);
   w.tokblk = reinterpret_cast<int32_t*>(p);
-  p += al(sizeof(int32_t) * (nb + 1));
+  w.barrier = w.tokblk + nb + 1;
+  p += al(sizeof(int32_t) * (nb + 2));
   if (m_tile > 0) {
     w.member = reinterpret_cast<uint32_t*>(p);
     p += al(sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32));
@@ -751,32 +909,90 @@ PermuteWs carve_permute_ws(void* ws, int T, int E, int K, int m_tile) {
     }                                                                            \
   } while (0)
 
+// The one-launch grouping (perm_fused_kernel) as a cooperative launch.  Returns
+// cudaErrorCooperativeLaunchTooLarge, launching nothing, when its blocks cannot all be resident at once.
+template <bool FM, int TB>
+cudaError_t launch_fused_grouping(int nb, const int32_t* ids, const float* topk_w, const uint32_t* member,
+                                  const float* logits, int T, int E, int K, const PermuteWs& w, int32_t* counts,
+                                  int32_t* offsets, int32_t* P_out, long long cap, int32_t* sorted_tok,
+                                  float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int* err, int slot_stride,
+                                  unsigned long long timeout_ns, cudaStream_t s) {
+  auto kern = perm_fused_kernel<FM, TB>;
+  const size_t smem = sizeof(uint32_t) * (static_cast<size_t>(E) * (TB / 32) + E + 1);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t st;
+  if ((st = cudaGetDevice(&dev)) != cudaSuccess) return st;
+  if ((st = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return st;
+  if ((st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, TB, smem)) != cudaSuccess) return st;
+  if (static_cast<long long>(per_sm) * sms < nb) return cudaErrorCooperativeLaunchTooLarge;
+  if ((st = cudaMemsetAsync(w.barrier, 0, sizeof(int), s)) != cudaSuccess) return st;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(nb, 1, 1);
+  cfg.blockDim = dim3(TB, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ids, topk_w, member, logits, T, E, K, nb, w.hist, w.tokblk, w.barrier, counts,
+                            offsets, P_out, cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride,
+                            timeout_ns);
+}
+
+// Group the pairs (from top-K ids, or from the membership bitmap with FM) into counts, offsets, the
+// expert-major order and the per-token return map: one cooperative launch when its blocks fit on the GPU at
+// once, else the four launches perm_hist, perm_escan, perm_scan, perm_scatter (the same results).
+template <bool FM>
+cudaError_t group_pairs(int tb, int nb, size_t bits_smem, const int32_t* ids, const float* topk_w,
+                        const uint32_t* member, const float* logits, int T, int E, int K, const PermuteWs& w,
+                        int32_t* counts, int32_t* offsets, int32_t* P_out, long long cap, int32_t* sorted_tok,
+                        float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int* err, int slot_stride,
+                        unsigned long long timeout_ns, cudaStream_t s) {
+  cudaError_t st;
+  switch (tb) {
+    case 32: st = launch_fused_grouping<FM, 32>(nb, ids, topk_w, member, logits, T, E, K, w, counts, offsets, P_out, cap,
+                                                sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride, timeout_ns, s);
+             break;
+    case 64: st = launch_fused_grouping<FM, 64>(nb, ids, topk_w, member, logits, T, E, K, w, counts, offsets, P_out, cap,
+                                                sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride, timeout_ns, s);
+             break;
+    case 128: st = launch_fused_grouping<FM, 128>(nb, ids, topk_w, member, logits, T, E, K, w, counts, offsets, P_out,
+                                                  cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride,
+                                                  timeout_ns, s);
+              break;
+    default: st = launch_fused_grouping<FM, 256>(nb, ids, topk_w, member, logits, T, E, K, w, counts, offsets, P_out,
+                                                 cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride,
+                                                 timeout_ns, s);
+             break;
+  }
+  if (st != cudaErrorCooperativeLaunchTooLarge) return st;
+  VGG_PERM_LAUNCH(perm_hist_kernel, FM, tb, nb, bits_smem, s, ids, member, T, E, K, nb, w.hist, w.tokblk, err);
+  launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
+  VGG_PERM_LAUNCH(perm_scatter_kernel, FM, tb, nb, bits_smem, s, ids, topk_w, member, logits, T, E, K, nb, w.hist,
+                  offsets, w.tokblk, cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, slot_stride);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const float* logits, const float* scores,
                            int T, int E, int K, int m_tile, long long cap, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_tok, float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs,
-                           int32_t* P_out, const PermuteWs& w, int* err, cudaStream_t s) {
+                           int32_t* P_out, const PermuteWs& w, int* err, unsigned long long timeout_ns,
+                           cudaStream_t s) {
   const int tb = perm_tok_block(T, E);
   const int nb = (T + tb - 1) / tb;
   const size_t bits_smem = static_cast<size_t>(E) * (tb / 32) * sizeof(uint32_t);
   cudaError_t st;
-  if (m_tile <= 0) {
-    VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-    launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
-    VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
-                                                                w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
-                                                                tok_ptr,
-                                                                tok_pairs, err, 0);
-    return cudaGetLastError();
-  }
+  if (m_tile <= 0)
+    return group_pairs<false>(tb, nb, bits_smem, topk_ids, topk_w, nullptr, nullptr, T, E, K, w, counts, offsets, P_out,
+                              cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, 0, timeout_ns, s);
   // plain grouping into the workspace (only the expert-grouped tokens are needed)
   const long long plain_cap = static_cast<long long>(T) * K;
-  VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-  launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
-  VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, nullptr, nullptr, T, E, K, nb,
-                                                              w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
-                                                              nullptr,
-                                                              nullptr, nullptr, err, 0);
-  if ((st = cudaGetLastError()) != cudaSuccess) return st;
+  if ((st = group_pairs<false>(tb, nb, bits_smem, topk_ids, nullptr, nullptr, nullptr, T, E, K, w, w.plain_cnt,
+                               w.plain_off, nullptr, plain_cap, w.plain_tok, nullptr, nullptr, nullptr, err, 0,
+                               timeout_ns, s)) != cudaSuccess)
+    return st;
   // final token sets
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
@@ -788,32 +1004,24 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(w.scoresT, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
                                                  w.member, err);
   // group the final pairs
-  VGG_PERM_LAUNCH(perm_hist_kernel, true, tb, nb, bits_smem, s, topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
-  launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, P_out, cap, err, s);
-  VGG_PERM_LAUNCH(perm_scatter_kernel, true, tb, nb, bits_smem, s, topk_ids, topk_w, w.member, logits, T, E, K, nb,
-                                                             w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
-                                                             tok_ptr,
-                                                             tok_pairs, err, 0);
-  return cudaGetLastError();
+  return group_pairs<true>(tb, nb, bits_smem, topk_ids, topk_w, w.member, logits, T, E, K, w, counts, offsets, P_out,
+                           cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, 0, timeout_ns, s);
 }
 
 cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w, int T, int E, int K, int C,
                                     int policy, long long cap, int32_t* counts, int32_t* offsets, int32_t* sorted_tok,
                                     float* sorted_w, int32_t* tok_ptr, int32_t* tok_pairs, int32_t* P_out,
-                                    const PermuteWs& w, int* err, cudaStream_t s) {
+                                    const PermuteWs& w, int* err, unsigned long long timeout_ns, cudaStream_t s) {
   const int tb = perm_tok_block(T, E);
   const int nb = (T + tb - 1) / tb;
   const size_t bits_smem = static_cast<size_t>(E) * (tb / 32) * sizeof(uint32_t);
   const long long plain_cap = static_cast<long long>(T) * K;
   cudaError_t st;
   // plain grouping of the top-K pairs with their probabilities (into the workspace)
-  VGG_PERM_LAUNCH(perm_hist_kernel, false, tb, nb, bits_smem, s, topk_ids, nullptr, T, E, K, nb, w.hist, w.tokblk, err);
-  launch_scan(w.hist, E, nb, w.tokblk, w.plain_cnt, w.plain_off, nullptr, plain_cap, err, s);
-  VGG_PERM_LAUNCH(perm_scatter_kernel, false, tb, nb, bits_smem, s, topk_ids, topk_w, nullptr, nullptr, T, E, K, nb,
-                                                              w.hist, w.plain_off, w.tokblk, plain_cap, w.plain_tok,
-                                                              w.scoresT,
-                                                              nullptr, nullptr, err, 0);
-  if ((st = cudaGetLastError()) != cudaSuccess) return st;
+  if ((st = group_pairs<false>(tb, nb, bits_smem, topk_ids, topk_w, nullptr, nullptr, T, E, K, w, w.plain_cnt,
+                               w.plain_off, nullptr, plain_cap, w.plain_tok, w.scoresT, nullptr, nullptr, err, 0,
+                               timeout_ns, s)) != cudaSuccess)
+    return st;
   // kept pairs
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
@@ -827,12 +1035,10 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
   const size_t slots = static_cast<size_t>(E) * C;
   if ((st = cudaMemsetAsync(sorted_tok, 0xFF, sizeof(int32_t) * slots, s)) != cudaSuccess) return st;
   if ((st = cudaMemsetAsync(sorted_w, 0, sizeof(float) * slots, s)) != cudaSuccess) return st;
-  VGG_PERM_LAUNCH(perm_hist_kernel, true, tb, nb, bits_smem, s, topk_ids, w.member, T, E, K, nb, w.hist, w.tokblk, err);
-  launch_scan(w.hist, E, nb, w.tokblk, counts, offsets, nullptr, cap, err, s);
-  VGG_PERM_LAUNCH(perm_scatter_kernel, true, tb, nb, bits_smem, s, topk_ids, topk_w, w.member, nullptr, T, E, K, nb,
-                                                             w.hist, offsets, w.tokblk, cap, sorted_tok, sorted_w,
-                                                             tok_ptr,
-                                                             tok_pairs, err, C);
+  if ((st = group_pairs<true>(tb, nb, bits_smem, topk_ids, topk_w, w.member, nullptr, T, E, K, w, counts, offsets,
+                              nullptr, cap, sorted_tok, sorted_w, tok_ptr, tok_pairs, err, C, timeout_ns, s)) !=
+      cudaSuccess)
+    return st;
   slot_offsets_kernel<<<1, 256, 0, s>>>(offsets, E, C, P_out);
   return cudaGetLastError();
 }
