@@ -146,6 +146,10 @@ int moe_route(moe_ctx* ctx, const void* X, const void* W_r, const float* bias, i
  * weight), tok_ptr[T+1] and tok_pairs[cap] (per token, the sorted positions
  * of its pairs in ascending expert), P_out (device int32 scalar).  cap must be
  * at least moe_pair_capacity(T,E,K,m_tile).
+ *
+ * Each grouping runs as one cooperative launch (all of its blocks resident at once, two grid barriers
+ * bounded by moe_set_wait_timeout; a barrier that gives up records MOE_DEV_TIMEOUT); when the GPU cannot
+ * hold all blocks at once it runs as four ordinary launches with the same results.
  */
 int moe_permute(moe_ctx* ctx, const int32_t* topk_ids, const float* topk_w, const float* logits,
                 const float* scores, int T, int E, int K, int m_tile, long long cap, int32_t* counts,
