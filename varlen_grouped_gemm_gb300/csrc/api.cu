@@ -28,6 +28,10 @@ struct moe_ctx {
   int l2_prefetch = 0;  // L2 prefetch of later stages (measured slower; kept switchable)
   int cta_pair = 0;     // CTA pairs on the 256-row tiles of the tiled varlen-M GEMMs (dX, dA', two-part down)
   int cta_pair_dw = 0;  // CTA pairs on the varlen-K weight-gradient GEMMs (both measured slower; switchable)
+  // The backward's per-token chain (router gradient, dX reduction, dW_r) runs on a second stream beside the
+  // weight-gradient GEMMs, forked from and joined back into the caller's stream.
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 
   std::vector<cudaEvent_t> pool;
   size_t pool_next = 0;
@@ -409,7 +413,16 @@ int moe_create(moe_ctx** out, int device) {
   c->device = device;
   c->num_sms = sms;
   c->timeout_ns = 2000000000ull;
-  if (cudaMalloc(&c->d_err, 16) != cudaSuccess || cudaMemset(c->d_err, 0, 16) != cudaSuccess) {
+  int prio_lo = 0, prio_hi = 0;
+  if (cudaMalloc(&c->d_err, 16) != cudaSuccess || cudaMemset(c->d_err, 0, 16) != cudaSuccess ||
+      cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_hi) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming) != cudaSuccess) {
+    if (c->join) cudaEventDestroy(c->join);
+    if (c->fork) cudaEventDestroy(c->fork);
+    if (c->side) cudaStreamDestroy(c->side);
+    if (c->d_err) cudaFree(c->d_err);
     delete c;
     return MOE_ERR_CUDA;
   }
@@ -421,6 +434,9 @@ int moe_destroy(moe_ctx* ctx) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   for (cudaEvent_t e : ctx->pool) cudaEventDestroy(e);
+  cudaEventDestroy(ctx->join);
+  cudaEventDestroy(ctx->fork);
+  cudaStreamDestroy(ctx->side);
   cudaFree(ctx->d_err);
   delete ctx;
   return MOE_OK;
@@ -912,6 +928,15 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
       return MOE_ERR_CUDA;
     VGG_LAUNCH("dx_gemm", run_dx_store(BN, sh.pair, p, m, sh.grid, s));
   }
+  // The per-token chain (wr_transpose, token_backward, dW_r) reads what the GEMMs above wrote and writes only
+  // its own outputs and workspace regions, so it runs on the side stream while the weight-gradient GEMMs below
+  // run on the caller's; the caller's stream waits for it before returning.  A token_backward block fits on an
+  // SM beside a weight-gradient CTA (shared memory, threads, registers), and the side stream has the higher
+  // priority, so its blocks take the room the persistent GEMM leaves.
+  const cudaStream_t s_main = s;
+  if (cudaEventRecord(ctx->fork, s_main) != cudaSuccess || cudaStreamWaitEvent(ctx->side, ctx->fork, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = ctx->side;
   // per token: dS, router-logit gradient, dX
   VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
   const int Tp = ceil_div(T, 64) * 64;
@@ -951,6 +976,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
     VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
   }
+  if (cudaEventRecord(ctx->join, s) != cudaSuccess) return MOE_ERR_CUDA;
+  s = s_main;
   // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok], with [dH | dU] as high and low
   // bf16 parts (about 16 significant bits of the fp32 gradients)
   {
@@ -1004,6 +1031,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     m.b1 = m.b0;
     VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, sh.pair, p, m, sh.grid, s));
   }
+  if (cudaStreamWaitEvent(s, ctx->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
