@@ -933,10 +933,15 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   // run on the caller's; the caller's stream waits for it before returning.  A token_backward block fits on an
   // SM beside a weight-gradient CTA (shared memory, threads, registers), and the side stream has the higher
   // priority, so its blocks take the room the persistent GEMM leaves.
+  // With per-launch profiling on, the chain stays on the caller's stream: a kernel's events then bracket that
+  // kernel alone, not its overlap with the weight-gradient GEMMs.
   const cudaStream_t s_main = s;
-  if (cudaEventRecord(ctx->fork, s_main) != cudaSuccess || cudaStreamWaitEvent(ctx->side, ctx->fork, 0) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  s = ctx->side;
+  const bool fork = !ctx->prof;
+  if (fork) {
+    if (cudaEventRecord(ctx->fork, s_main) != cudaSuccess || cudaStreamWaitEvent(ctx->side, ctx->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    s = ctx->side;
+  }
   // per token: dS, router-logit gradient, dX
   VGG_LAUNCH("wr_transpose", launch_transpose_bf16(static_cast<const __nv_bfloat16*>(W_r), d, E, w.WrT, s));
   const int Tp = ceil_div(T, 64) * 64;
@@ -976,7 +981,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     VGG_LAUNCH("dwr_gemm", run_dense_mn_store(BN, p, m, std::min(tiles * split, ctx->num_sms), s));
     VGG_LAUNCH("dwr_reduce", launch_splitk_reduce(w.wr_part, split, static_cast<long long>(d) * E, dW_r, s));
   }
-  if (cudaEventRecord(ctx->join, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fork && cudaEventRecord(ctx->join, s) != cudaSuccess) return MOE_ERR_CUDA;
   s = s_main;
   // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok], with [dH | dU] as high and low
   // bf16 parts (about 16 significant bits of the fp32 gradients)
@@ -1031,7 +1036,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     m.b1 = m.b0;
     VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, sh.pair, p, m, sh.grid, s));
   }
-  if (cudaStreamWaitEvent(s, ctx->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fork && cudaStreamWaitEvent(s, ctx->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
