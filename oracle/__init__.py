@@ -20,6 +20,7 @@ from .moe_oracle import (  # noqa: F401
     capacity_drop,
     combine,
     combine_weights,
+    dequantize_blocks_mx,
     dequantize_rows_e4m3,
     e4m3_decode,
     e4m3_encode,
@@ -31,9 +32,12 @@ from .moe_oracle import (  # noqa: F401
     moe_backward,
     moe_forward,
     moe_forward_fp8,
+    moe_forward_mx,
+    mx_block_exponents,
     round_bf16,
     route_discrete,
     router_logits,
+    quantize_blocks_mx,
     quantize_rows_e4m3,
     softmax,
     token_rounding,

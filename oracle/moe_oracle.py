@@ -368,7 +368,7 @@ def router_grad_rows(member, topk_ids, w_full, dw_full):
 
 
 def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp8_dx: bool = False,
-                 fp8_dact: bool = False):
+                 fp8_dact: bool = False, mx_dx: bool = False, mx_dact: bool = False):
     """Backward of the layer given the forward cache.
 
     Returns dX, dW_gate, dW_up, dW_down (fp64, all experts or the listed ones),
@@ -379,6 +379,9 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
     2n) quantized per row (per input channel of the layer), ``quantize_rows_e4m3``.
     With ``fp8_dact`` the dSwiGLU GEMM dA' = dO W_down takes e4m3 operands: dO per token (row) and
     W_down^T (n rows of d) per row; dS = <dA', A> then comes from that dA' (the epilogue's identity).
+    ``mx_dx`` and ``mx_dact`` are the same two GEMMs with block-scaled operands (``quantize_blocks_mx``):
+    [dH | dU] quantized from its exact value (blocks along 2n) against [W_gate; W_up]^T (blocks along 2n),
+    and dO per token against W_down^T (blocks along d).
     """
     X, dO = _f64(X), _f64(dO)
     T, d = X.shape
@@ -397,13 +400,22 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
         if len(rows) == 0:
             continue
         dap = None
-        if fp8_dact:
+        if mx_dact:
+            oq, oe = quantize_blocks_mx(dO[rows])
+            wq, we = quantize_blocks_mx(_f64(W_down[e]).T)  # [n, d]
+            dap = dequantize_blocks_mx(oq, oe) @ dequantize_blocks_mx(wq, we).T
+        elif fp8_dact:
             oq, os_ = quantize_rows_e4m3(dO[rows].astype(np.float32))
             wq, ws_ = quantize_rows_e4m3(_f64(W_down[e]).T.astype(np.float32))  # [n, d]
             dap = dequantize_rows_e4m3(oq, os_) @ dequantize_rows_e4m3(wq, ws_).T
         g = expert_block_backward(X[rows], dO[rows], w_full[rows, e], W_gate[e], W_up[e], W_down[e], dap=dap)
         dw_full[rows, e] = g["dw"]
-        if fp8_dx:
+        if mx_dx:
+            hq, he = quantize_blocks_mx(np.concatenate([g["dh"], g["du"]], axis=1))
+            B = np.concatenate([_f64(W_gate[e]), _f64(W_up[e])], axis=0).T  # [d, 2n]
+            bq, be = quantize_blocks_mx(B)
+            np.add.at(dX, rows, dequantize_blocks_mx(hq, he) @ dequantize_blocks_mx(bq, be).T)
+        elif fp8_dx:
             hq, hs = quantize_rows_e4m3(round_bf16(np.concatenate([g["dh"], g["du"]], axis=1)).astype(np.float32))
             B = np.concatenate([_f64(W_gate[e]), _f64(W_up[e])], axis=0).T  # [d, 2n]
             bq, bs = quantize_rows_e4m3(B.astype(np.float32))
@@ -546,3 +558,102 @@ def moe_forward_fp8(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0,
     O = combine(y_sorted, routing, w_full, T)
     return O, dict(logits=L, routing=routing, w_full=w_full, h=h, u=u, a=a, y_sorted=y_sorted,
                    xq=xq, xs=xs, gq=gq, gs=gs, uq=uq, us=us, **extra)
+
+
+# ---------------------------------------------------------------- block-scaled (1 x 32) e4m3 variant
+#
+# [GG] "한계": the further 2x credited to DeepSeek's *fine-grained* FP8 grouped GEMM.  The pages give no
+# scaling recipe; reading: every operand row is cut into blocks of 32 consecutive elements along the
+# reduction dimension, each block has a power-of-two scale 2^e (one UE8M0 byte, e + 127) with e the
+# smallest integer such that the block's largest magnitude is at most 448 2^e (clamped to [-127, 127];
+# an all-zero block takes e = 0), and its codes are e4m3(x 2^-e) rounded to nearest even.  The scaling
+# by 2^-e is exact, and no code saturates.  A GEMM of two such operands sums, per 32-element block,
+# the code products times both blocks' scales.
+
+MX_BLOCK = 32
+
+
+def mx_block_exponents(amax) -> np.ndarray:
+    """The block exponent e of each block maximum: smallest e with amax <= 448 2^e, in [-127, 127];
+    0 for an all-zero block."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))  # a = f 2^E, 0.5 <= f < 1: floor(log2 a) = E - 1
+    e = (E - 1) - 8  # a 2^-e in [256, 512)
+    e = np.where(np.ldexp(a, -e) > E4M3_MAX, e + 1, e)
+    e = np.clip(e, -127, 127)
+    return np.where(a > 0, e, 0).astype(np.int64)
+
+
+def quantize_blocks_mx(M):
+    """1 x 32 block quantization along the last axis: (codes uint8 [..., C], exponents int64 [..., C/32]).
+
+    Element j of a row dequantizes to e4m3_decode(code) 2^e[j // 32]."""
+    A = _f64(M)
+    C = A.shape[-1]
+    if C % MX_BLOCK:
+        raise ValueError("the blocked axis must be a multiple of 32")
+    blocks = A.reshape(A.shape[:-1] + (C // MX_BLOCK, MX_BLOCK))
+    e = mx_block_exponents(np.max(np.abs(blocks), axis=-1))
+    y = np.ldexp(blocks, -e[..., None])  # exact
+    codes = e4m3_encode(e4m3_round(y)).reshape(A.shape)
+    return codes, e
+
+
+def dequantize_blocks_mx(codes, exps) -> np.ndarray:
+    c = np.asarray(codes)
+    C = c.shape[-1]
+    v = e4m3_decode(c).reshape(c.shape[:-1] + (C // MX_BLOCK, MX_BLOCK))
+    return np.ldexp(v, np.asarray(exps, dtype=np.int64)[..., None]).reshape(c.shape)
+
+
+def moe_forward_mx(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,
+                   scores_for_routing=None, capacity: int = 0, policy: str = "position", drop_keys=None,
+                   mx_down: bool = True):
+    """Forward of the layer with block-scaled e4m3 operands (``quantize_blocks_mx``): X per token and
+    W_gate / W_up per output channel, blocks along d, for the gate/up projections; with ``mx_down`` the
+    down projection takes the activation rows A = silu(h) u (quantized from their exact value, blocks along
+    n) and W_down per output channel (blocks along n).  Routing, SwiGLU and the combine as in
+    ``moe_forward``.  Returns (O, cache) with h, u, a per sorted pair (fp64) and the codes and exponents."""
+    X64 = _f64(X)
+    T, d = X64.shape
+    E, n, _ = np.shape(W_gate)
+    xq, xe = quantize_blocks_mx(X64)
+    gq, ge = quantize_blocks_mx(_f64(W_gate).reshape(E * n, d))
+    uq, ue = quantize_blocks_mx(_f64(W_up).reshape(E * n, d))
+    Xd = dequantize_blocks_mx(xq, xe)
+    Wg_d = dequantize_blocks_mx(gq, ge).reshape(E, n, d)
+    Wu_d = dequantize_blocks_mx(uq, ue).reshape(E, n, d)
+    L = router_logits(X64, W_r, bias)
+    sel = L if logits_for_routing is None else logits_for_routing
+    routing = route_discrete(sel, K, m_tile, scores=scores_for_routing, capacity=capacity, policy=policy,
+                             drop_keys=drop_keys)
+    w_full = combine_weights(L, routing.topk_ids)
+    P = routing.P
+    h = np.zeros((P, n))
+    u = np.zeros((P, n))
+    for e in range(E):
+        lo, hi = routing.offsets[e], routing.offsets[e + 1]
+        if hi == lo:
+            continue
+        rows = routing.sorted_tok[lo:hi]
+        h[lo:hi] = Xd[rows] @ Wg_d[e].T
+        u[lo:hi] = Xd[rows] @ Wu_d[e].T
+    a = silu(h) * u
+    extra = {}
+    if mx_down:
+        aq, ae = quantize_blocks_mx(a)
+        dq, de = quantize_blocks_mx(_f64(W_down).reshape(E * d, n))
+        a_op = dequantize_blocks_mx(aq, ae)
+        Wd_op = dequantize_blocks_mx(dq, de).reshape(E, d, n)
+        extra = dict(aq=aq, ae=ae, dq=dq, de=de)
+    else:
+        a_op, Wd_op = a, _f64(W_down)
+    y_sorted = np.zeros((P, d))
+    for e in range(E):
+        lo, hi = routing.offsets[e], routing.offsets[e + 1]
+        if hi == lo:
+            continue
+        y_sorted[lo:hi] = a_op[lo:hi] @ Wd_op[e].T
+    O = combine(y_sorted, routing, w_full, T)
+    return O, dict(logits=L, routing=routing, w_full=w_full, h=h, u=u, a=a, y_sorted=y_sorted,
+                   xq=xq, xe=xe, gq=gq, ge=ge, uq=uq, ue=ue, **extra)

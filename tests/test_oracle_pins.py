@@ -660,6 +660,159 @@ def test_fp8_dact_within_quantization_bound():
     assert 0 < np.max(np.abs(g8["dX"] - g16["dX"])) < 0.2 * np.max(np.abs(g16["dX"]))
 
 
+# ---------------------------------------------------------------- block-scaled (1 x 32) e4m3
+
+
+def test_mx_block_exponent_is_the_smallest_that_fits():
+    # the definition, by brute force over every admissible exponent: the smallest e with amax <= 448 2^e
+    rng = np.random.default_rng(21)
+    amax = np.concatenate([np.exp2(rng.uniform(-140, 120, 3000)),
+                           448.0 * np.exp2(np.arange(-30, 30)),                # exactly on a boundary
+                           448.0 * np.exp2(np.arange(-30, 30)) * (1 + 2.0 ** -20),  # just above it
+                           [2.0 ** -133, 2.0 ** -126, 1.0, 0.5, 3.0e38]])
+    e = oracle.mx_block_exponents(amax)
+    grid = np.arange(-127, 128)
+    for a, got in zip(amax, e):
+        fits = grid[a <= 448.0 * np.exp2(grid.astype(np.float64))]
+        assert got == fits[0], (a, got, fits[0])
+    np.testing.assert_array_equal(oracle.mx_block_exponents([0.0, 448.0, 449.0, 256.0, 1.75, 1.76]),
+                                  [0, 0, 1, 0, -8, -7])
+
+
+def test_mx_codes_match_torch_conversion():
+    # codes are torch's float8_e4m3fn conversion of x 2^-e (an exact scaling), block by block
+    rng = np.random.default_rng(22)
+    M = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-20, 20, (64, 1)))).astype(np.float32)
+    M[3, 32:64] = 0.0  # an all-zero block
+    M[5, :32] *= 1e-30  # a block far below 1
+    q, e = oracle.quantize_blocks_mx(M)
+    assert e.shape == (64, 8) and e[3, 1] == 0
+    y = np.ldexp(M.astype(np.float64), -np.repeat(e, 32, axis=1))
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(q, ref)
+    # no block saturates: its largest scaled value lies in (224, 448], its code (rounded) in [224, 448]
+    mags = np.abs(mo.e4m3_decode(q)).reshape(64, 8, 32).max(axis=2)
+    nz = np.abs(M).reshape(64, 8, 32).max(axis=2) > 0
+    assert np.all((mags[nz] >= 224) & (mags[nz] <= 448))
+
+
+def test_mx_round_trip_exact_on_representable_blocks_and_error_bound():
+    rng = np.random.default_rng(23)
+    grid = mo.e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+    R, C = 16, 128
+    vals = rng.choice(grid, (R, C)) * rng.choice([-1.0, 1.0], (R, C))
+    vals[:, ::32] = rng.choice(grid[(grid > 224) & (grid <= 448)], (R, C // 32))  # the block maximum
+    ex = rng.integers(-40, 40, (R, C // 32))
+    V = np.ldexp(vals, np.repeat(ex, 32, axis=1))
+    q, e = oracle.quantize_blocks_mx(V)
+    np.testing.assert_array_equal(e, ex)
+    np.testing.assert_array_equal(oracle.dequantize_blocks_mx(q, e), V)
+    # general inputs: |x - deq| <= max(2^-4 |x|, 2^-10 2^e) (half a mantissa step, or of the subnormal step)
+    M = rng.standard_normal((40, 96))
+    q, e = oracle.quantize_blocks_mx(M)
+    D = oracle.dequantize_blocks_mx(q, e)
+    bound = np.maximum(2.0 ** -4 * np.abs(M), 2.0 ** -10 * np.exp2(np.repeat(e, 32, axis=1).astype(np.float64)))
+    assert np.all(np.abs(D - M) <= bound) and np.max(np.abs(D - M)) > 0
+
+
+def _mx_bound(M):
+    _, e = oracle.quantize_blocks_mx(M)
+    return np.maximum(2.0 ** -4 * np.abs(M), 2.0 ** -10 * np.exp2(np.repeat(e, 32, axis=-1).astype(np.float64)))
+
+
+def test_mx_forward_reduces_to_bf16_on_representable_inputs():
+    # blocks whose elements are e4m3 values times a power of two (maximum in (224, 448] times it) quantize
+    # without error, so the gate/up projections and O equal the plain forward's
+    rng = np.random.default_rng(24)
+    T, d, E, n, K = 24, 64, 4, 32, 2
+    X = rng.integers(-3, 4, (T, d)).astype(np.float64)
+    X[:, ::32] = 3.5  # the block maximum: 448 2^-7
+    W_r = rng.standard_normal((d, E)) * 0.3
+    Wg = rng.integers(-1, 2, (E, n, d)).astype(np.float64) * 0.5
+    Wu = rng.integers(-1, 2, (E, n, d)).astype(np.float64) * 0.5
+    Wg[:, :, ::32] = 0.875
+    Wu[:, :, ::32] = -0.875
+    Wd = rng.standard_normal((E, d, n)) * 0.2
+    Om, cm = oracle.moe_forward_mx(X, W_r, None, Wg, Wu, Wd, K, mx_down=False)
+    O, c = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    np.testing.assert_allclose(Om, O, rtol=1e-12, atol=1e-12)
+
+
+def test_mx_forward_within_quantization_bound():
+    # gate/up: h from the quantized operands within the element-wise bound of the exact product; down
+    # projection: y within the bound of A's and W_down's quantization; both differ (the quantization is real)
+    rng = np.random.default_rng(25)
+    T, d, E, n, K = 32, 64, 4, 64, 2
+    X = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, n, d)) * 0.05
+    Wu = rng.standard_normal((E, n, d)) * 0.05
+    Wd = rng.standard_normal((E, d, n)) * 0.05
+    W_r = rng.standard_normal((d, E)) * 0.3
+    Om, cm = oracle.moe_forward_mx(X, W_r, None, Wg, Wu, Wd, K)
+    r = cm["routing"]
+    dx = _mx_bound(X)
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        if hi == lo:
+            continue
+        rows = r.rows_of(e)
+        for W, key in ((Wg[e], "h"), (Wu[e], "u")):
+            dw = _mx_bound(W)
+            bound = np.abs(X[rows]) @ dw.T + dx[rows] @ np.abs(W).T + dx[rows] @ dw.T
+            err = np.abs(cm[key][lo:hi] - X[rows] @ W.T)
+            assert np.all(err <= bound * (1 + 1e-9)) and np.max(err) > 0
+        a = cm["a"][lo:hi]
+        da, dwd = _mx_bound(a), _mx_bound(Wd[e])
+        bound = np.abs(a) @ dwd.T + da @ np.abs(Wd[e]).T + da @ dwd.T
+        err = np.abs(cm["y_sorted"][lo:hi] - a @ Wd[e].T)
+        assert np.all(err <= bound * (1 + 1e-9)) and np.max(err) > 0
+    O, _ = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    assert 0 < np.max(np.abs(Om - O)) < 0.1 * np.max(np.abs(O))
+
+
+def test_mx_backward_gemms_within_quantization_bound():
+    # mx_dact: dA' within the bound of dO's and W_down^T's quantization, dS = <dA', A>; mx_dx: each pair's
+    # dX contribution within the bound of [dH | dU]'s and [W_gate; W_up]^T's quantization; the weight
+    # gradients of the experts are those of the exact backward when only dX is quantized
+    rng = np.random.default_rng(26)
+    T, d, E, n, K = 24, 64, 4, 32, 2
+    X = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, n, d)) * 0.1
+    Wu = rng.standard_normal((E, n, d)) * 0.1
+    Wd = rng.standard_normal((E, d, n)) * 0.1
+    W_r = rng.standard_normal((d, E)) * 0.3
+    dO = rng.standard_normal((T, d))
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    g = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache)
+    gx = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache, mx_dx=True)
+    ga = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache, mx_dact=True)
+    for k in ("dW_r", "dlogits", "dw"):
+        np.testing.assert_array_equal(gx[k], g[k])
+    r, w = cache["routing"], cache["w_full"]
+    bound = np.zeros((T, d))
+    for e in range(E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        np.testing.assert_array_equal(gx["dW_gate"][e], g["dW_gate"][e])
+        blk = mo.expert_block_backward(X[rows], dO[rows], w[rows, e], Wg[e], Wu[e], Wd[e])
+        hu = np.concatenate([blk["dh"], blk["du"]], axis=1)
+        B = np.concatenate([Wg[e], Wu[e]], axis=0).T
+        dh, db = _mx_bound(hu), _mx_bound(B)
+        bound[rows] += np.abs(hu) @ db.T + dh @ np.abs(B).T + dh @ db.T
+        Bt = Wd[e].T
+        do, dbt = _mx_bound(dO[rows]), _mx_bound(Bt)
+        dap_bound = np.abs(dO[rows]) @ dbt.T + do @ np.abs(Bt).T + do @ dbt.T
+        oq, oe = oracle.quantize_blocks_mx(dO[rows])
+        wq, we = oracle.quantize_blocks_mx(Bt)
+        dap = oracle.dequantize_blocks_mx(oq, oe) @ oracle.dequantize_blocks_mx(wq, we).T
+        err = np.abs(dap - dO[rows] @ Bt.T)
+        assert np.all(err <= dap_bound * (1 + 1e-9)) and np.max(err) > 0
+        np.testing.assert_allclose(ga["dw"][rows, e], np.sum(dap * blk["a"], axis=1), rtol=1e-12, atol=1e-12)
+    err = np.abs(gx["dX"] - g["dX"])
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-12) and np.max(err) > 0
+
+
 # ---------------------------------------------------------------- the metric
 
 
