@@ -80,6 +80,14 @@ def kernel_work(wl, P, dW_bytes=2):
         "gate_up_swiglu_e4m3": (4 * P * d * n, T * d + 4 * T + 2 * E * n * d + 8 * E * n + 6 * P * n,
                                 T * d + 4 * T + 2 * E * n * d + 8 * E * n + 10 * P * n),
         "quantize_e4m3": same(0, 3 * T * d + 4 * T),
+        # block-scaled form: codes of 1 byte plus one scale byte per 32 values
+        "quantize_mx": same(0, 3 * T * d + T * d // 32),
+        "quantize_mx_weights": same(0, 3 * E * n * d + E * n * d // 32),  # one weight per launch (outside the step)
+        "gate_up_swiglu_mx": (4 * P * d * n, T * d + T * d // 32 + 2 * E * n * d + 2 * E * n * d // 32 + 4 * P * n
+                              + P * n + P * n // 32,
+                              T * d + T * d // 32 + 2 * E * n * d + 2 * E * n * d // 32 + 8 * P * n + P * n
+                              + P * n // 32),
+        "down_scale_mx": same(2 * P * d * n, P * n + P * n // 32 + E * d * n + E * d * n // 32 + 2 * P * d),
         "down_scale": same(2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
         "down_scale_e4m3": same(2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
         "quantize_a_e4m3": same(0, 3 * P * n + 4 * P),
@@ -195,6 +203,8 @@ _GEMM_LABELS = {
     (1, 1, 0, 4): "gate_up_swiglu_e4m3", (0, 0, 0, 5): "down_scale_e4m3", (0, 0, 0, 6): "dx_gemm_e4m3",
     (0, 0, 0, 7): "dact_dswiglu_e4m3",
 }
+# the block-scaled form (template flag X_MX = 8)
+_MX_GEMM_LABELS = {(1, 1, 0, 1): "gate_up_swiglu_mx", (0, 0, 0, 2): "down_scale_mx"}
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
     "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "transpose_f32_kernel": "permute",
@@ -204,7 +214,8 @@ _OTHER_LABELS = {
     "token_backward_kernel": "token_backward", "transpose_bf16_kernel": "wr_transpose",
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
     "zero_tail_rows_kernel": "zero_tail", "quantize_rows_e4m3_kernel": "quantize_e4m3",
-    "pad_offsets_kernel": "pad_offsets",
+    "pad_offsets_kernel": "pad_offsets", "quantize_rows_mx_kernel": "quantize_mx",
+    "quantize_weight_mx_kernel": "quantize_mx_weights",
 }
 
 
@@ -225,7 +236,10 @@ def _label_of(name: str):
     m = re.search(r"grouped_gemm_kernel<([^>]*)>", name)
     if m:
         a = [x.strip() for x in m.group(1).split(",")]
-        return _GEMM_LABELS.get((int(a[4]), int(a[5]), int(a[6]), int(a[7])), "grouped_gemm " + m.group(1))
+        key = (int(a[4]), int(a[5]), int(a[6]), int(a[7]))
+        if len(a) > 10 and a[10].isdigit() and int(a[10]) & 8:
+            return _MX_GEMM_LABELS.get(key, "grouped_gemm " + m.group(1))
+        return _GEMM_LABELS.get(key, "grouped_gemm " + m.group(1))
     for k, v in _OTHER_LABELS.items():
         if k in name:
             return v

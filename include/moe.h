@@ -279,6 +279,76 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
                               void* U, void* A, void* Aq, float* a_scale, void* Yw, moe_stream_t stream);
 
 /*
+ * Block-scaled e4m3 form ("fine-grained" FP8): [GG] "한계" credits a fine-grained FP8 grouped GEMM with
+ * a further 2x over bf16; the pages give no recipe, this library's reading is the following.  Every
+ * operand row is cut into blocks of 32 consecutive elements along the reduction dimension; a block has
+ * one power-of-two scale 2^e, stored as the byte e + 127, with e the smallest integer in [-127, 127]
+ * such that max|block| <= 448 2^e (0 for an all-zero block), and codes e4m3(x 2^-e) rounded to nearest
+ * even (exact scaling, no saturation).  The GEMMs run on the kind::mxf8f6f4 tensor-core instruction,
+ * which multiplies every 32-element block's code products by both operands' block scales.
+ *
+ * Scale layouts (bytes, device):
+ *   row-major  [rows][moe_mx_sf_cols(cols)]: the scales of row r's blocks in order, then bytes of value
+ *              127 up to a multiple of 4 per 128 columns;
+ *   blocks     512 bytes per 128 operand rows and 128 columns of the reduction: row r, block k of the
+ *              128 columns at byte (r % 32) * 16 + (r / 32) * 4 + k; rows or columns beyond the operand
+ *              hold 127.  W_gate / W_up: [E][ceil(n/64)][ceil(d/128)] blocks, rows 0..63 of block
+ *              [e][t][.] = W_gate[e] rows 64t..64t+63, rows 64..127 = W_up[e] rows 64t..64t+63; W_down:
+ *              [E][ceil(d/128)][ceil(n/128)] blocks over W_down[e] rows 128t..; the activations A:
+ *              one block row per 128-row tile of every expert's sorted rows (tiles in expert order),
+ *              [tiles][ceil(n/128)].
+ */
+/* Bytes per row of a row-major scale array for `cols` columns: 4 * ceil(cols / 128). */
+long long moe_mx_sf_cols(int cols);
+/* Bytes of the weight scale blocks: which = 0 the W_gate / W_up pair, 1 W_down; 0 on bad arguments. */
+long long moe_mx_weight_sf_bytes(int E, int d, int n, int which);
+/* Bytes of the activation scale blocks for a pair capacity cap: (ceil(cap/128) + E) * ceil(n/128) * 512. */
+long long moe_mx_act_sf_bytes(long long cap, int E, int n);
+
+/*
+ * moe_quantize_rows_mx — block-scaled quantization of M [rows, cols] bf16 (row-major, device) along its
+ * rows: codes q [rows, cols] uint8 and row-major scales sf [rows][moe_mx_sf_cols(cols)] (caller-owned
+ * device buffers).  Use it on X (blocks along d).  cols % 64 == 0; M and q 16-byte aligned; else
+ * MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_rows_mx(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, void* sf,
+                         moe_stream_t stream);
+
+/*
+ * moe_quantize_weights_mx — block-scaled codes and scale blocks of the expert weights, once per weight
+ * update: W_gate, W_up [E,n,d] and W_down [E,d,n] bf16 (device) to codes Wg_q, Wu_q [E,n,d], Wd_q
+ * [E,d,n] uint8 (blocks along each row, i.e. along d for W_gate / W_up and along n for W_down) and the
+ * scale blocks gu_sf (moe_mx_weight_sf_bytes(E,d,n,0) bytes) and dn_sf (moe_mx_weight_sf_bytes(E,d,n,1)).
+ * Caller-owned device buffers, 16-byte aligned; d, n multiples of 64; else MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, const void* W_down, int E, int d,
+                            int n, void* Wg_q, void* Wu_q, void* gu_sf, void* Wd_q, void* dn_sf,
+                            moe_stream_t stream);
+
+/*
+ * moe_grouped_gemm_fwd_mx — moe_grouped_gemm_fwd on block-scaled e4m3 operands, the activations quantized
+ * inside the gate/up GEMM's epilogue.  [GG] "한계" and "(6) 세 번의 gg.gmm"; [SM] "4.1 Gather 융합",
+ * "4.2 Epilogue 융합".  Xq [T,d], x_sf: moe_quantize_rows_mx of X; Wg_q, Wu_q, gu_sf, Wd_q, dn_sf:
+ * moe_quantize_weights_mx.  For sorted pair j of expert e, token t = sorted_tok[j], column c, with
+ * dq(.) the block-scaled value (code times its block's scale):
+ *
+ *   H[j,c] = sum_i dq(Xq[t,i]) dq(Wg_q[e,c,i]),  U[j,c] likewise with Wu_q,
+ *   A[j]   = silu(H[j]) U[j], quantized per 32-column block in fp32 into Aq [cap,n] uint8 and the
+ *            activation scale blocks a_sf (moe_mx_act_sf_bytes(cap,E,n) bytes),
+ *   Yw[j,c] = sorted_w[j] * sum_i dq(Aq[j,i]) dq(Wd_q[e,c,i])  (bf16).
+ *
+ * Block products are accumulated in fp32 on the tensor cores.  A slot with sorted_tok = -1 (capacity
+ * dispatch) gives zero rows.  H, U [cap,n] fp32 are the backward's cache (both NULL: forward only).  Rows of
+ * Aq at or past offsets[E], and scale bytes of rows past an expert's last row, are not written.  Shape rules
+ * as moe_grouped_gemm_fwd; every buffer caller-owned device memory, codes and scale blocks 16-byte
+ * aligned; no workspace.  MOE_ERR_INVALID_ARG on a violated rule.
+ */
+int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, const void* Wg_q, const void* Wu_q,
+                            const void* gu_sf, const void* Wd_q, const void* dn_sf, int T, int d, int E, int n,
+                            long long cap, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                            void* H, void* U, void* Aq, void* a_sf, void* Yw, moe_stream_t stream);
+
+/*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.
  * [EP] "여러 Expert의 결과도 같은 토큰으로 돌아오기" (y(A2) = 0.7 u0 + 0.3 u2 in
  * A2's own slot); [DEP] "3) Combine".  O[t] = sum over t's pairs, in ascending

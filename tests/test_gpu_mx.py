@@ -1,0 +1,204 @@
+"""The block-scaled (1 x 32) e4m3 forward on the device vs the oracle's block-scaled forward.
+
+[GG] "한계": a fine-grained FP8 grouped GEMM as the next step after bf16; the recipe (blocks of 32 along the
+reduction dimension, power-of-two scales, e the smallest exponent with max|block| <= 448 2^e, codes rounded
+to nearest even) is the library's reading.  Checked: the quantized operands (codes and block scales of X, of
+W_gate / W_up and of W_down, every scale layout unpacked here) bit for bit against the oracle's quantization
+of the same bf16 inputs; the routing bit for bit; H and U per sorted pair within the usual tolerance of the
+oracle's fp64 products of the same codes; the activation codes A, which the gate/up epilogue quantizes from
+its fp32 SwiGLU values, against the oracle's quantization of its exact values (equal but for values within
+fp32 rounding of a rounding boundary: at most one code step, at most a few per hundred thousand); O within
+the usual tolerance of the oracle's fp64 forward.  Cases: ragged tails, n and d with a half last stage of
+128 codes, empty experts (skewed prior), token rounding, 512 experts, the capacity dispatch with empty slots.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import moe_oracle as mo
+
+from _helpers import Inputs, bits_to_dev, check_routing_bit_exact, dev_to_f64, gpu_routing
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import varlen_grouped_gemm_gb300 as vgg
+    return vgg.Context(0)
+
+
+def _bf16_bits(M: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(M).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _block_off(r, b):
+    """Byte of operand row r (0..127 within its block row) and 32-column block b (0..3 within its stage)."""
+    return (r % 32) * 16 + (r // 32) * 4 + b
+
+
+def _unpack_weight_blocks(sf: np.ndarray, E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
+    """Exponents [E, R, C/32] of one weight from its 512-byte scale blocks [E][tiles][ceil(C/128)]."""
+    kst = -(-C // 128)
+    tiles = sf.size // (E * kst * 512)
+    blk = sf.reshape(E, tiles, kst, 512)
+    rows = np.arange(R)
+    t, br = rows // rows_per_tile, row0 + rows % rows_per_tile
+    cols = np.arange(C // 32)
+    off = _block_off(br[:, None], cols[None, :] % 4)
+    return blk[:, t[:, None], cols[None, :] // 4, off].astype(np.int64) - 127
+
+
+def _unpack_act_blocks(sf: np.ndarray, offsets: np.ndarray, n: int, rows: np.ndarray) -> np.ndarray:
+    """Exponents [len(rows), n/32] of the activation rows (sorted positions) from the per-row-tile blocks."""
+    kst = -(-n // 128)
+    E = len(offsets) - 1
+    tiles_before = np.concatenate([[0], np.cumsum(-(-np.diff(offsets) // 128))])
+    e = np.searchsorted(offsets, rows, side="right") - 1
+    r = rows - offsets[e]
+    rt = tiles_before[e] + r // 128
+    cols = np.arange(n // 32)
+    idx = (rt[:, None] * kst + cols[None, :] // 4) * 512 + _block_off(r[:, None] % 128, cols[None, :] % 4)
+    assert e.max() < E
+    return sf[idx].astype(np.int64) - 127
+
+
+def test_mx_quantize_rows_bit_exact(ctx):
+    import varlen_grouped_gemm_gb300 as vgg
+    rng = np.random.default_rng(31)
+    for rows, cols in ((300, 320), (64, 2048)):
+        # row and block magnitudes over many binades (subnormal codes, the clamped exponent), zero blocks
+        M = rng.standard_normal((rows, cols)) * np.exp2(rng.uniform(-60, 60, (rows, cols // 32))).repeat(32, axis=1)
+        M[3] = 0.0
+        M[4, 32:64] = 0.0
+        M[5, :32] *= 2.0 ** -80
+        bits = _bf16_bits(M)
+        Md = bits_to_dev(bits)
+        q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        sf = torch.full((rows, vgg.mx_sf_cols(cols)), 0, dtype=torch.uint8, device="cuda")
+        vgg.moe_quantize_rows_mx(ctx, Md, q, sf)
+        qo, eo = oracle.quantize_blocks_mx(bits)
+        np.testing.assert_array_equal(q.cpu().numpy(), qo)
+        got = sf.cpu().numpy().astype(np.int64)
+        np.testing.assert_array_equal(got[:, :cols // 32] - 127, eo)
+        assert np.all(got[:, cols // 32:] == 127), "padding entries hold scale 1"
+        assert eo[3].max() == 0 and eo[4, 1] == 0
+
+
+@pytest.mark.parametrize("E,d,n", [(4, 256, 192), (3, 320, 320), (2, 2048, 512)])
+def test_mx_weights_bit_exact(ctx, E, d, n):
+    import varlen_grouped_gemm_gb300 as vgg
+    rng = np.random.default_rng(32 + d)
+    Wg = _bf16_bits(rng.standard_normal((E, n, d)) * 0.05)
+    Wu = _bf16_bits(rng.standard_normal((E, n, d)) * 0.05 * np.exp2(rng.integers(-8, 8, (E, n, 1))))
+    Wd = _bf16_bits(rng.standard_normal((E, d, n)) * 0.05)
+    w = vgg.MxWeights.quantize(ctx, bits_to_dev(Wg), bits_to_dev(Wu), bits_to_dev(Wd))
+    gu = w.gu_sf.cpu().numpy()
+    dn = w.dn_sf.cpu().numpy()
+    want = {"gu": np.full_like(gu, 127), "dn": np.full_like(dn, 127)}
+    for got_q, W, R, C, key, rpt, r0 in ((w.Wg_q, Wg, n, d, "gu", 64, 0), (w.Wu_q, Wu, n, d, "gu", 64, 64),
+                                         (w.Wd_q, Wd, d, n, "dn", 128, 0)):
+        q, e = oracle.quantize_blocks_mx(W.reshape(E * R, C))
+        np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * R, C), q)
+        # the whole block buffer, built here from the oracle's exponents: entries no weight row or column
+        # fills hold scale 1 (byte 127)
+        kst = -(-C // 128)
+        blk = want[key].reshape(E, -1, kst, 512)
+        rows, cols = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
+        for ex in range(E):
+            blk[ex, rows // rpt, cols // 4, _block_off(r0 + rows % rpt, cols % 4)] = e.reshape(E, R, -1)[ex] + 127
+    np.testing.assert_array_equal(gu, want["gu"])
+    np.testing.assert_array_equal(dn, want["dn"])
+    np.testing.assert_array_equal(_unpack_weight_blocks(gu, E, n, d, 64, 64).reshape(E * n, -1),
+                                  oracle.quantize_blocks_mx(Wu.reshape(E * n, d))[1])
+
+
+CASES = [
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=512, d=256, E=16, n=192, K=4),
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_medium", T=1024, d=1024, E=32, n=256, K=4),
+    # d = n = 320: both GEMMs end on a half stage of 128 codes; skewed prior: empty experts
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small_320", T=640, d=320, E=32, n=320, K=4),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
+    synth.scaled(synth.WORKLOADS["c5_plain"], name="c5_small_e512", T=2048, d=256, E=512, n=128, K=8),
+    # capacity factor 1 under a skewed load: some experts drop pairs, others leave slots empty
+    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias", T=512, d=256, E=16, n=192, K=4, bias="normal"),
+]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_mx_forward_matches_oracle(ctx, wl):
+    import varlen_grouped_gemm_gb300 as vgg
+    inp = Inputs(wl, with_grad=False)
+    dv = inp.dev
+    E, n, d = wl.E, wl.n, wl.d
+    buf = vgg.Buffers.allocate(wl.T, d, E, n, wl.K, wl.m_tile, backward=False, capacity_factor=wl.capacity_factor,
+                               drop_policy=wl.drop_policy, mx=True)
+    buf.masf.fill_(255)  # scale bytes the forward must write are never left at this (NaN) pattern
+    wmx = vgg.MxWeights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"])
+    vgg.forward_mx(ctx, dv["X"], dv["W_r"], dv["bias"], wmx, buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+
+    xq, xe = oracle.quantize_blocks_mx(inp.X)
+    np.testing.assert_array_equal(buf.mxq.cpu().numpy(), xq)
+    np.testing.assert_array_equal(buf.mxsf.cpu().numpy()[:, :d // 32].astype(np.int64) - 127, xe)
+
+    g = gpu_routing(buf)
+    C = buf.capacity
+    O_ref, cache = oracle.moe_forward_mx(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K,
+                                         wl.m_tile, logits_for_routing=g["logits"], scores_for_routing=g["scores"],
+                                         capacity=C, policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None)
+    r = cache["routing"]
+    if C:
+        # slots e*C + rank hold the kept pairs; the rest are empty (zero rows)
+        slot_of = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(E)]).astype(np.int64)
+        empty = np.setdiff1d(np.arange(E * C), slot_of)
+        assert r.P < wl.T * wl.K and len(empty) > 0
+        assert not torch.any(buf.H[torch.from_numpy(empty).cuda()] != 0).item(), "empty slots give zero rows"
+        assert not torch.any(buf.maq[torch.from_numpy(empty).cuda()] != 0).item()
+        rows = slot_of
+        offs = np.arange(E + 1) * C
+    else:
+        check_routing_bit_exact(g, wl.K, wl.m_tile)
+        rows = np.arange(r.P)
+        offs = r.offsets
+    sel = torch.from_numpy(rows).cuda()
+    rep = {"O": oracle.compare("O", dev_to_f64(buf.O), O_ref)}
+    rep["H"] = oracle.compare("H", dev_to_f64(buf.H[sel]), cache["h"])
+    rep["U"] = oracle.compare("U", dev_to_f64(buf.U[sel]), cache["u"])
+    # A's codes and block scales: the device quantizes its fp32 SwiGLU values, the oracle the exact ones
+    aq = buf.maq[sel].cpu().numpy()
+    ae = _unpack_act_blocks(buf.masf.cpu().numpy(), offs, n, rows)
+    diff_e = ae != cache["ae"]
+    assert diff_e.sum() <= max(2, diff_e.size // 10000), ("block scales of A", int(diff_e.sum()), diff_e.size)
+    same_blocks = np.repeat(~diff_e, 32, axis=1)
+    dq = np.abs(mo.e4m3_decode(aq) - mo.e4m3_decode(cache["aq"]))
+    step = np.maximum(np.abs(mo.e4m3_decode(cache["aq"])) * 2.0 ** -3, 2.0 ** -9)
+    bad = same_blocks & (dq > 0)
+    assert bad.sum() <= max(4, aq.size // 20000), ("A codes", int(bad.sum()), aq.size)
+    assert np.all(dq[bad] <= step[bad] * (1 + 1e-12)), "a differing code is one step away"
+    # the activation scale blocks of every row tile hold scale 1 past n
+    if wl.bias == "zipf":
+        assert (r.counts == 0).any(), "the skewed prior should leave some experts empty"
+    print(wl.name, {k: (round(v["max"], 6), round(v["mean"], 7)) for k, v in rep.items()},
+          "A codes differing:", int(bad.sum()), "of", aq.size)
+
+
+def test_mx_forward_only(ctx):
+    """cache=False: the same O bit for bit, H and U left untouched."""
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.scaled(synth.WORKLOADS["c2"], name="c2_small_n256", T=512, d=256, E=16, n=256, K=4)
+    inp = Inputs(wl, with_grad=False)
+    dv = inp.dev
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=False, mx=True)
+    wmx = vgg.MxWeights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"])
+    vgg.forward_mx(ctx, dv["X"], dv["W_r"], dv["bias"], wmx, buf)
+    O_cached = buf.O.clone()
+    buf.H.fill_(7.0)
+    buf.U.fill_(7.0)
+    buf.O.zero_()
+    vgg.forward_mx(ctx, dv["X"], dv["W_r"], dv["bias"], wmx, buf, cache=False)
+    assert torch.equal(buf.O, O_cached)
+    assert torch.all(buf.H == 7.0).item() and torch.all(buf.U == 7.0).item()

@@ -30,6 +30,8 @@ EXPORTS = (
     "moe_capacity_workspace_bytes", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
     "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
     "moe_expert_capacity", "moe_test_gemm_varlen_k_dual", "moe_test_gemm_varlen_m_dual",
+    "moe_mx_sf_cols", "moe_mx_weight_sf_bytes", "moe_mx_act_sf_bytes", "moe_quantize_rows_mx",
+    "moe_quantize_weights_mx", "moe_grouped_gemm_fwd_mx",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -88,6 +90,16 @@ def lib() -> ctypes.CDLL:
         L.moe_backward_e4m3.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL,
                                         _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                                         _P, _P, _P, _P, _SZ, _P]
+        L.moe_mx_sf_cols.argtypes = [_I]
+        L.moe_mx_sf_cols.restype = _LL
+        L.moe_mx_weight_sf_bytes.argtypes = [_I, _I, _I, _I]
+        L.moe_mx_weight_sf_bytes.restype = _LL
+        L.moe_mx_act_sf_bytes.argtypes = [_LL, _I, _I]
+        L.moe_mx_act_sf_bytes.restype = _LL
+        L.moe_quantize_rows_mx.argtypes = [_P, _P, _LL, _I, _P, _P, _P]
+        L.moe_quantize_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+        L.moe_grouped_gemm_fwd_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P,
+                                              _P, _P, _P, _P, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -290,6 +302,59 @@ def moe_grouped_gemm_fwd_e4m3(ctx, Xq, x_scale, Wg_q, wg_scale, Wu_q, wu_scale, 
         _ptr(A, torch.bfloat16), _ptr(Aq, u8), _ptr(a_scale, f32), _ptr(Yw, torch.bfloat16), _stream(stream)))
 
 
+def mx_sf_cols(cols: int) -> int:
+    """Bytes per row of a row-major block-scale array (the library's moe_mx_sf_cols)."""
+    return int(lib().moe_mx_sf_cols(cols))
+
+
+def mx_weight_sf_bytes(E: int, d: int, n: int, which: int) -> int:
+    """Bytes of the weight scale blocks: which = 0 the W_gate / W_up pair, 1 W_down."""
+    b = int(lib().moe_mx_weight_sf_bytes(E, d, n, which))
+    if b <= 0:
+        raise ValueError(f"moe_mx_weight_sf_bytes: invalid arguments E={E} d={d} n={n} which={which}")
+    return b
+
+
+def mx_act_sf_bytes(cap: int, E: int, n: int) -> int:
+    """Bytes of the activation scale blocks of the block-scaled down projection."""
+    b = int(lib().moe_mx_act_sf_bytes(cap, E, n))
+    if b <= 0:
+        raise ValueError(f"moe_mx_act_sf_bytes: invalid arguments cap={cap} E={E} n={n}")
+    return b
+
+
+def moe_quantize_rows_mx(ctx, M, q, sf, stream=None):
+    """Block-scaled codes (uint8, shaped like M) and row-major scale bytes [rows, mx_sf_cols(cols)]."""
+    cols = M.shape[-1]
+    rows = M.numel() // cols
+    if q.shape != M.shape or sf.numel() != rows * mx_sf_cols(cols):
+        raise ValueError("q must be shaped like M and sf hold mx_sf_cols(cols) bytes per row")
+    _check("moe_quantize_rows_mx", lib().moe_quantize_rows_mx(
+        ctx.handle, _ptr(M, torch.bfloat16), rows, cols, _ptr(q, torch.uint8), _ptr(sf, torch.uint8),
+        _stream(stream)))
+
+
+def moe_quantize_weights_mx(ctx, W_gate, W_up, W_down, Wg_q, Wu_q, gu_sf, Wd_q, dn_sf, stream=None):
+    E, n, d = W_gate.shape
+    bf, u8 = torch.bfloat16, torch.uint8
+    _check("moe_quantize_weights_mx", lib().moe_quantize_weights_mx(
+        ctx.handle, _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf), E, d, n, _ptr(Wg_q, u8), _ptr(Wu_q, u8),
+        _ptr(gu_sf, u8), _ptr(Wd_q, u8), _ptr(dn_sf, u8), _stream(stream)))
+
+
+def moe_grouped_gemm_fwd_mx(ctx, Xq, x_sf, w, offsets, sorted_tok, sorted_w, H, U, Aq, a_sf, Yw, stream=None):
+    """Block-scaled gate/up (+ SwiGLU, A quantized in the epilogue) and down projection; ``w`` is MxWeights."""
+    T, d = Xq.shape
+    E, n, _ = w.Wg_q.shape
+    cap = sorted_tok.numel()
+    u8, f32 = torch.uint8, torch.float32
+    _check("moe_grouped_gemm_fwd_mx", lib().moe_grouped_gemm_fwd_mx(
+        ctx.handle, _ptr(Xq, u8), _ptr(x_sf, u8), _ptr(w.Wg_q, u8), _ptr(w.Wu_q, u8), _ptr(w.gu_sf, u8),
+        _ptr(w.Wd_q, u8), _ptr(w.dn_sf, u8), T, d, E, n, cap, _ptr(offsets, torch.int32),
+        _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32), _ptr(Aq, u8), _ptr(a_sf, u8),
+        _ptr(Yw, torch.bfloat16), _stream(stream)))
+
+
 def moe_combine(ctx, Yw, tok_ptr, tok_pairs, O, stream=None):
     T, d = O.shape
     _check("moe_combine", lib().moe_combine(
@@ -444,10 +509,14 @@ class Buffers:
     hus: torch.Tensor | None = None
     doq: torch.Tensor | None = None  # e4m3 dSwiGLU GEMM: sorted dO codes [cap, d] and per-row scales [cap]
     dos: torch.Tensor | None = None
+    mxq: torch.Tensor | None = None  # block-scaled forward: X's codes [T, d] and scales [T, mx_sf_cols(d)]
+    mxsf: torch.Tensor | None = None
+    maq: torch.Tensor | None = None  # block-scaled down projection: A's codes [cap, n] and scale blocks
+    masf: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
-                 drop_policy="position", capacity_factor=0.0, e4m3=False):
+                 drop_policy="position", capacity_factor=0.0, e4m3=False, mx=False):
         """Buffers for one configuration; capacity > 0 (or capacity_factor > 0, giving
         ceil(capacity_factor * T * K / E)) selects the capacity (drop/pad) dispatch with that many slots per
         expert (pair-indexed arrays sized E * capacity)."""
@@ -484,7 +553,10 @@ class Buffers:
             huq=z((cap, 2 * n), torch.uint8) if (e4m3 and backward) else None,
             hus=z((cap,), f32) if (e4m3 and backward) else None,
             doq=z((cap, d), torch.uint8) if (e4m3 and backward) else None,
-            dos=z((cap,), f32) if (e4m3 and backward) else None)
+            dos=z((cap,), f32) if (e4m3 and backward) else None,
+            mxq=z((T, d), torch.uint8) if mx else None, mxsf=z((T, mx_sf_cols(d)), torch.uint8) if mx else None,
+            maq=z((cap, n), torch.uint8) if mx else None,
+            masf=z((mx_act_sf_bytes(cap, E, n),), torch.uint8) if mx else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, cache=True):
@@ -501,6 +573,30 @@ def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, 
     moe_grouped_gemm_fwd(ctx, X, W_gate, W_up, W_down, buf.offsets, buf.sorted_tok, buf.sorted_w,
                          buf.H if cache else None, buf.U if cache else None, buf.A, buf.Yw, buf.ws, stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
+
+
+@dataclass
+class MxWeights:
+    """The expert weights as block-scaled e4m3 (1 x 32 blocks along each row, power-of-two scales): codes
+    Wg_q, Wu_q [E, n, d], Wd_q [E, d, n] (uint8) and the scale blocks the GEMMs read (gu_sf, dn_sf)."""
+
+    Wg_q: torch.Tensor
+    Wu_q: torch.Tensor
+    gu_sf: torch.Tensor
+    Wd_q: torch.Tensor
+    dn_sf: torch.Tensor
+
+    @staticmethod
+    def quantize(ctx, W_gate, W_up, W_down, stream=None) -> "MxWeights":
+        E, n, d = W_gate.shape
+        dev = W_gate.device
+        u8 = torch.uint8
+        w = MxWeights(torch.empty((E, n, d), dtype=u8, device=dev), torch.empty((E, n, d), dtype=u8, device=dev),
+                      torch.empty(mx_weight_sf_bytes(E, d, n, 0), dtype=u8, device=dev),
+                      torch.empty((E, d, n), dtype=u8, device=dev),
+                      torch.empty(mx_weight_sf_bytes(E, d, n, 1), dtype=u8, device=dev))
+        moe_quantize_weights_mx(ctx, W_gate, W_up, W_down, w.Wg_q, w.Wu_q, w.gu_sf, w.Wd_q, w.dn_sf, stream)
+        return w
 
 
 @dataclass
@@ -571,6 +667,26 @@ def forward_e4m3(ctx, X, W_r, bias, w8: E4m3Weights, W_down, buf: Buffers, strea
                               wd_scale=w8.wd_scale,
                               Aq=buf.aq if w8.Wd_q is not None else None,
                               a_scale=buf.as_ if w8.Wd_q is not None else None, stream=stream)
+    moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
+
+
+def forward_mx(ctx, X, W_r, bias, wmx: MxWeights, buf: Buffers, stream=None, cache=True):
+    """The forward on block-scaled e4m3 operands (``buf`` allocated with ``mx=True``): routing and grouping as
+    ``forward``, X quantized in 1 x 32 blocks, the gate/up GEMM (whose epilogue quantizes A), the down
+    projection and the combine.  ``cache=False``: forward only (H, U not written)."""
+    if buf.mxq is None:
+        raise ValueError("buffers were allocated without mx=True")
+    moe_route(ctx, X, W_r, bias, buf.K, buf.logits, buf.scores, buf.topk_ids, buf.topk_w, buf.ws, stream)
+    if buf.capacity:
+        moe_permute_capacity(ctx, buf.topk_ids, buf.topk_w, buf.E, buf.capacity, buf.drop_policy, buf.counts,
+                             buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws,
+                             stream)
+    else:
+        moe_permute(ctx, buf.topk_ids, buf.topk_w, buf.logits, buf.scores, buf.E, buf.m_tile, buf.counts,
+                    buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
+    moe_quantize_rows_mx(ctx, X, buf.mxq, buf.mxsf, stream)
+    moe_grouped_gemm_fwd_mx(ctx, buf.mxq, buf.mxsf, wmx, buf.offsets, buf.sorted_tok, buf.sorted_w,
+                            buf.H if cache else None, buf.U if cache else None, buf.maq, buf.masf, buf.Yw, stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 

@@ -744,6 +744,131 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
   return MOE_OK;
 }
 
+long long moe_mx_sf_cols(int cols) { return cols > 0 ? 4ll * ceil_div(cols, 128) : 0; }
+
+long long moe_mx_weight_sf_bytes(int E, int d, int n, int which) {
+  if (E < 1 || d < 64 || n < 64 || d % 64 || n % 64) return 0;
+  if (which == 0) return 512ll * E * ceil_div(n, 64) * ceil_div(d, 128);
+  if (which == 1) return 512ll * E * ceil_div(d, 128) * ceil_div(n, 128);
+  return 0;
+}
+
+long long moe_mx_act_sf_bytes(long long cap, int E, int n) {
+  if (cap < 1 || E < 1 || n < 64 || n % 64) return 0;
+  return 512ll * (ceil_div(cap, BM) + E) * ceil_div(n, 128);
+}
+
+int moe_quantize_rows_mx(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, void* sf,
+                         moe_stream_t stream) {
+  VGG_REQUIRE(ctx && M && q && sf);
+  VGG_REQUIRE(rows >= 0 && rows <= (1ll << 31) && cols >= 64 && cols % 64 == 0);
+  VGG_REQUIRE(aligned16(M) && aligned16(q) && (reinterpret_cast<uintptr_t>(sf) & 3u) == 0);
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VGG_LAUNCH("quantize_mx", launch_quantize_rows_mx(static_cast<const __nv_bfloat16*>(M), rows, nullptr, cols,
+                                                    static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf),
+                                                    static_cast<int>(moe_mx_sf_cols(cols)), s));
+  return MOE_OK;
+}
+
+int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, const void* W_down, int E, int d,
+                            int n, void* Wg_q, void* Wu_q, void* gu_sf, void* Wd_q, void* dn_sf,
+                            moe_stream_t stream) {
+  VGG_REQUIRE(ctx && W_gate && W_up && W_down && Wg_q && Wu_q && gu_sf && Wd_q && dn_sf);
+  VGG_REQUIRE(E >= 1 && E <= kMaxGroups && d >= 64 && d % 64 == 0 && n >= 64 && n % 64 == 0);
+  VGG_REQUIRE(aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(Wg_q) && aligned16(Wu_q) &&
+              aligned16(gu_sf) && aligned16(Wd_q) && aligned16(dn_sf));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every entry of the blocks that no operand row or column fills holds scale 1
+  VGG_CUDA(cudaMemsetAsync(gu_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 0)), s));
+  VGG_CUDA(cudaMemsetAsync(dn_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 1)), s));
+  const int kd = ceil_div(d, 128), kn = ceil_div(n, 128);
+  VGG_LAUNCH("quantize_mx_weights",
+             launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_gate), E, n, d, static_cast<uint8_t*>(Wg_q),
+                                       static_cast<uint8_t*>(gu_sf), 64, 0, ceil_div(n, 64), kd, s));
+  VGG_LAUNCH("quantize_mx_weights",
+             launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_up), E, n, d, static_cast<uint8_t*>(Wu_q),
+                                       static_cast<uint8_t*>(gu_sf), 64, 64, ceil_div(n, 64), kd, s));
+  VGG_LAUNCH("quantize_mx_weights",
+             launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_down), E, d, n, static_cast<uint8_t*>(Wd_q),
+                                       static_cast<uint8_t*>(dn_sf), 128, 0, ceil_div(d, 128), kn, s));
+  return MOE_OK;
+}
+
+int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, const void* Wg_q, const void* Wu_q,
+                            const void* gu_sf, const void* Wd_q, const void* dn_sf, int T, int d, int E, int n,
+                            long long cap, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                            void* H, void* U, void* Aq, void* a_sf, void* Yw, moe_stream_t stream) {
+  VGG_REQUIRE(ctx && Xq && x_sf && Wg_q && Wu_q && gu_sf && Wd_q && dn_sf && offsets && sorted_tok && sorted_w &&
+              Aq && a_sf && Yw);
+  VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
+  VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
+  VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
+  VGG_REQUIRE(aligned16(Xq) && (reinterpret_cast<uintptr_t>(x_sf) & 3u) == 0 && aligned16(Wg_q) &&
+              aligned16(Wu_q) && aligned16(gu_sf) && aligned16(Wd_q) && aligned16(dn_sf) && aligned16(H) &&
+              aligned16(U) && aligned16(Aq) && aligned16(a_sf) && aligned16(Yw));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int dk = d / 2, nk = n / 2;  // e4m3 rows as 16-bit units (code pairs) for TMA and the gather
+  {
+    GemmParams p = base_params(ctx);
+    p.N = n;
+    p.K = dk;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.a_idx = sorted_tok;
+    p.a_rows = T;
+    p.a_src = static_cast<const __nv_bfloat16*>(Xq);
+    p.a_ld = dk;
+    p.out0 = H;
+    p.out1 = U;
+    p.out2 = Aq;
+    p.ld_out = n;
+    p.a_sf = static_cast<const uint8_t*>(x_sf);
+    p.a_sf_ld = moe_mx_sf_cols(d);
+    p.b_sf = static_cast<const uint8_t*>(gu_sf);
+    p.sf_kst = ceil_div(d, 128);
+    p.o_sf = static_cast<uint8_t*>(a_sf);
+    p.o_sf_kst = ceil_div(n, 128);
+    Maps m = zero_maps();
+    if (!make_map_3d(&m.b0, Wg_q, dk, n, E, 64) || !make_map_3d(&m.b1, Wu_q, dk, n, E, 64) ||
+        (H && (!make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32))))
+      return MOE_ERR_CUDA;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, 64);
+    // pairs of CTAs on neighbouring column tiles share the gathered X rows (each gathers half the codes)
+    const int cn = ceil_div(n, 64) >= 2 ? 2 : 1;
+    VGG_LAUNCH("gate_up_swiglu_mx", run_gate_up_swiglu_mx(cn, p, m, std::min(tiles, ctx->num_sms), s));
+  }
+  {
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = nk;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.out0 = Yw;
+    p.ld_out = d;
+    p.row_scale = sorted_w;
+    p.a_sf = static_cast<const uint8_t*>(a_sf);
+    p.b_sf = static_cast<const uint8_t*>(dn_sf);
+    p.sf_kst = ceil_div(n, 128);
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, 128) ||
+        !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, 128);
+    VGG_LAUNCH("down_scale_mx", run_down_scale_mx(p, m, std::min(tiles, ctx->num_sms), s));
+  }
+  return MOE_OK;
+}
+
 int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int32_t* tok_pairs, int T, int d,
                 long long cap, void* O, moe_stream_t stream) {
   VGG_REQUIRE(ctx && Yw && tok_ptr && tok_pairs && O);

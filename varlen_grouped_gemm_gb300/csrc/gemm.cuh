@@ -69,7 +69,17 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //   X_PAIR    a CTA pair (cluster of 2, cta_group::2) computes a 256-row tile: each CTA loads its 128 rows of A
 //             and half of B's columns, both CTAs' TMA loads complete on the even CTA's barriers, the even CTA
 //             issues the M = 256 UMMAs, and each CTA drains its own 128 TMEM rows (varlen-K with padded B).
-enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4 };
+//   X_MX      block-scaled e4m3 operands (kind::mxf8f6f4): every 32 codes of an operand row along K carry
+//             one power-of-two scale (UE8M0 byte).  A stage holds, after its A and B tiles, the 128 x 4
+//             scale bytes of A's rows and of B's rows for its 128 codes of K in the layout tcgen05.cp reads
+//             (row r, 32-code block k at byte (r % 32) 16 + (r / 32) 4 + k); the issuer copies them into
+//             TMEM columns of that stage (past the two accumulators) before the stage's UMMAs.  Gathered A
+//             rows take their 4 scale bytes from a row-major [rows][sf_ld] array (cp.async, 4 bytes);
+//             tiled A and the weights take whole 512-byte blocks laid out that way in global memory.
+//             BN = 128, so that both accumulators and every stage's scales fit the 512 TMEM columns.  The
+//             SwiGLU epilogue of this form emits A itself as block-scaled codes (a thread's 32 columns of
+//             its row are one block) with the scale blocks the down projection reads.
+enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4, X_MX = 8 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
   EPI_DSWIGLU_Q = 7
@@ -119,6 +129,15 @@ struct GemmParams {
   const float* q_row;  // e4m3 dSwiGLU: A row scales [rows], B row scales [groups][q_ld]
   const float* q_col;
   int q_ld;
+  // block-scaled form (X_MX): scale bytes of A (gathered: row-major [a_rows][a_sf_ld]; tiled: 512-byte blocks
+  // [row tile][sf_kst]), of B (512-byte blocks per 128 rows of a stage: [groups][column tile][sf_kst]) and of
+  // the SwiGLU epilogue's block-scaled A (o_sf: [row tile][o_sf_kst] blocks); sf_kst = stages of K
+  const uint8_t* a_sf;
+  long long a_sf_ld;
+  const uint8_t* b_sf;
+  int sf_kst;
+  uint8_t* o_sf;
+  int o_sf_kst;
   int* err;
   unsigned long long timeout_ns;
 };
@@ -139,13 +158,15 @@ struct Maps {
 };
 
 // EW epilogue warps with DEPTH staged stores each; NA A tiles per stage (2: high and low parts); BNL rows of
-// B per stage in this CTA (half of BN for a CTA pair).
-template <int BN, int STAGES, int EW, int DEPTH, int NA = 1, int BNL = BN>
+// B per stage in this CTA (half of BN for a CTA pair); SF bytes of block scales per stage (X_MX, a multiple
+// of 1024 so that every stage stays 1024-byte aligned).
+template <int BN, int STAGES, int EW, int DEPTH, int NA = 1, int BNL = BN, int SF = 0>
 struct SmemLayout {
   static constexpr int kA1Bytes = BM * BK * 2;
   static constexpr int kABytes = NA * kA1Bytes;
   static constexpr int kBBytes = BNL * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSfBytes = SF;
+  static constexpr int kStageBytes = kABytes + kBBytes + SF;
   static constexpr int kStgOffset = STAGES * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + EW * DEPTH * kStgBuf;
   static constexpr int kNumBars = 3 * STAGES + 5;
@@ -157,6 +178,11 @@ struct SmemLayout {
            (var == VAR_M ? 4 * static_cast<size_t>(groups + 1) : var == VAR_NONE ? 8 : 0);
   }
 };
+
+// Scale-block bytes of one stage of the block-scaled form (A's 512 bytes, then B's BN x 4), padded to 1024.
+__host__ __device__ constexpr int mx_stage_bytes(int BN, int XF) {
+  return (XF & X_MX) ? ((512 + BN * 4 + 1023) / 1024) * 1024 : 0;
+}
 
 struct Tile {
   int g;        // group
@@ -409,7 +435,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   constexpr bool kDual = (XF & X_DUAL_A) != 0;
   constexpr bool kTrans = (XF & X_TRANS) != 0;
   constexpr bool kPair = (XF & X_PAIR) != 0;
-  using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1, kPair ? BN / 2 : BN>;
+  constexpr bool kMx = (XF & X_MX) != 0;
+  constexpr int kSfStage = mx_stage_bytes(BN, XF);
+  using L = SmemLayout<BN, STAGES, EW, DEPTH, kDual ? 2 : 1, kPair ? BN / 2 : BN, kSfStage>;
   static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_Q) || BMODE == B_TMA_K3_GU,
@@ -417,7 +445,13 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   // The e4m3 form moves 128-byte operand rows like the bf16 form: the host describes e4m3 rows to TMA
   // and to the gather as 16-bit units (two codes each), so K, the coordinates and the swizzled layout
   // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
-  constexpr bool kF8 = (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q || EPI == EPI_DSWIGLU_Q);
+  constexpr bool kF8 =
+      (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q || EPI == EPI_DSWIGLU_Q) || kMx;
+  static_assert(!kMx || (BN == 128 && VAR == VAR_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
+                         (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) && (CN == 1 || CN == 2) &&
+                         (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_STORE || EPI == EPI_DSWIGLU)),
+                "block-scaled form: BN = 128, K-major operands, varlen-M, plain epilogue kinds");
+  static_assert(!kMx || 2 * BN + STAGES * (4 + BN / 32) <= 512, "block-scaled form: TMEM columns");
   static_assert(EPI != EPI_STORE_Q || !OUTF32, "the e4m3 plain epilogue stores bf16");
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
                          VAR == VAR_M),
@@ -455,9 +489,13 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   constexpr int kThreads = WP::kThreads;
   static_assert(kThreads <= 512 && (kGW == 0 || kSlice % (kRStep > 0 ? kRStep : 1) == 0), "threads / gather rows");
   // a pair's even CTA expects both CTAs' loads on its barrier
+  // (block-scaled form: the producer also brings B's scale block and, for a tiled A, A's)
   constexpr uint32_t kTxBytes =
-      kPair ? 2 * (L::kABytes + L::kBBytes) : (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes);
-  constexpr uint32_t kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
+      kPair ? 2 * (L::kABytes + L::kBBytes)
+            : (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes) +
+                  (kMx ? BN * 4 + (kAGather ? 0 : 512) : 0);
+  constexpr uint32_t kTmemCols = kMx ? 512 : (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
+  constexpr int kSfCols = 4 + BN / 32;  // TMEM columns of one stage's scales (A: 4, B: BN / 32)
   constexpr uint32_t kIdesc =
       kF8 ? idesc_e4m3(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0) : idesc_bf16(kPair ? 2 * BM : BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
@@ -560,6 +598,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
 
   Sched<BN, BMODE, VAR, CN, kPair> sch;
   sch.init(p, s_off, s_tile);
+  // block-scaled form: row tiles before group g = s_tile[g] / column units per group (the tile order of every
+  // varlen-M GEMM over the same offsets), which indexes the scale blocks of a tiled A and of the SwiGLU output
+  const int mx_ncu = ((p.N + Sched<BN, BMODE, VAR>::kColsPerTile - 1) / Sched<BN, BMODE, VAR>::kColsPerTile + CN - 1) / CN;
   if (*s_bad) sch.total = 0;
   if (kPair && VAR == VAR_K && !p.b_offsets) {  // the varlen-K pair reads padded B rows only
     if (threadIdx.x == 0) set_error(p.err, DERR_BAD_OFFSETS);
@@ -656,6 +697,18 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
             }
           }
         }
+        if (kMx && !l2) {
+          // the stage's scale blocks: A's (a tiled A: its row tile's block for this stage of K), then B's (a
+          // cluster CTA past the last column tile loads the last tile's block; its results are not stored)
+          uint8_t* sf = sb + L::kBBytes;
+          if (AMODE == A_TMA_K) {
+            const long long rt = s_tile[x.g] / mx_ncu + x.m0 / BM;
+            bulk_load(sf, p.a_sf + (rt * p.sf_kst + kstage) * 512, 512, bar);
+          }
+          const int nt = min(x.nt, sch.ntiles - 1);
+          bulk_load(sf + 512, p.b_sf + ((static_cast<long long>(x.g) * sch.ntiles + nt) * p.sf_kst + kstage) * (BN * 4),
+                    BN * 4, bar);
+        }
         if (BMODE == B_TMA_K3) {
           if (l2) tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
           else tma_load_3d_hint(sb, &mp.b0, bar, kg, x.n0, x.g, pol_stream);
@@ -750,14 +803,25 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
     const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
     auto fetch = [&](const Pos& x, int (&r)[8], const Pos& prev, const int (&pr)[8]) {
       if (AMODE == A_GATHER_K) {
+        // block-scaled form with a cluster: r[kRowsPer + i] are the peer slice's rows (their scale bytes are
+        // gathered here too), loaded by the c16 == 1 threads that copy them
+        constexpr int kIdx = (kMx && kRelay) ? 2 * kRowsPer : kRowsPer;
         if (x.t == prev.t) {
 #pragma unroll
-          for (int i = 0; i < kRowsPer; ++i) r[i] = pr[i];
+          for (int i = 0; i < kIdx; ++i) r[i] = pr[i];
         } else {
 #pragma unroll
           for (int i = 0; i < kRowsPer; ++i) {
             const int rr = slice0 + rsub + kRStep * i;
             r[i] = rr < x.tl.rows ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
+          }
+          if (kMx && kRelay) {
+            const int peer0 = (sch.rank ^ 1) * kSlice;
+#pragma unroll
+            for (int i = 0; i < kRowsPer; ++i) {
+              const int rr = peer0 + rsub + kRStep * i;
+              r[kRowsPer + i] = (c16 == 1 && rr < x.tl.rows) ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
+            }
           }
         }
       } else {
@@ -803,6 +867,31 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
           }
           cp_async_16_hint(sa + sw128_offset(slice0 + rsub + kRStep * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src,
                            ok ? 16u : 0u, pol_keep);
+        }
+        if (kMx) {
+          // the stage's 4 scale bytes of every row of the tile, into the scale block after A and B: own rows by
+          // the c16 == 0 threads, with a cluster the peer's rows by the c16 == 1 threads (the relay forwards
+          // codes only); rows past the group's end get zeros
+          const uint32_t sfa = sa + L::kABytes + L::kBBytes;
+          const long long ko = static_cast<long long>(q0.tl.k_begin / BK + q0.ks) * 4;
+          if (c16 == 0) {
+#pragma unroll
+            for (int i = 0; i < kRowsPer; ++i) {
+              const int rr = slice0 + rsub + kRStep * i;
+              const long long row = r0[i];
+              const bool ok = row >= 0 && row < p.a_rows;
+              cp_async_4(sfa + (rr & 31) * 16 + (rr >> 5) * 4, ok ? p.a_sf + row * p.a_sf_ld + ko : p.a_sf, ok ? 4u : 0u);
+            }
+          } else if (kRelay && c16 == 1) {
+            const int peer0 = (sch.rank ^ 1) * kSlice;
+#pragma unroll
+            for (int i = 0; i < kRowsPer; ++i) {
+              const int rr = peer0 + rsub + kRStep * i;
+              const long long row = r0[kRowsPer + i];
+              const bool ok = row >= 0 && row < p.a_rows;
+              cp_async_4(sfa + (rr & 31) * 16 + (rr >> 5) * 4, ok ? p.a_sf + row * p.a_sf_ld + ko : p.a_sf, ok ? 4u : 0u);
+            }
+          }
         }
       } else if (AMODE == A_GATHER_MN) {
 #pragma unroll
@@ -913,6 +1002,17 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
             const uint32_t sb = sa + L::kABytes;
             if (kGather) fence_proxy_async_smem();  // cp.async writes -> UMMA operand reads
             tc_fence_after();
+            // block-scaled form: this stage's scale blocks into its own TMEM columns (their previous readers, the
+            // UMMAs of the stage's last use, completed before the stage was refilled); tcgen05.cp and the UMMAs
+            // after it run in issue order
+            const uint32_t sf_t = tmem_base + 2 * BN + s * kSfCols;
+            if (kMx) {
+              const uint32_t sf_s = sb + L::kBBytes;
+              tmem_cp_32x128b_x4(sf_t, sdesc_plain(sf_s, 128, 128));
+#pragma unroll
+              for (int a = 0; a < BN / 128; ++a)
+                tmem_cp_32x128b_x4(sf_t + 4 + 4 * a, sdesc_plain(sf_s + 512 + 512 * a, 128, 128));
+            }
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad =
@@ -922,7 +1022,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
               // dual A: the low part of A times the same B, into the same accumulator
               const uint64_t adl = kAMn ? sdesc_sw128(sa + L::kA1Bytes + kk * 2048, BK * 128, 1024)
                                         : sdesc_sw128(sa + L::kA1Bytes + kk * 32, 16, 1024);
-              if (kPair) {  // same offsets in both CTAs: each holds its rows of A and its columns of B
+              if (kMx) {  // K step kk = 32-code block kk of the stage: byte kk of every scale word
+                umma_mx(d_tmem, ad, bd, idesc_mx(BM, BN, 0, 0, kk, kk), sf_t, sf_t + 4, (ks | kk) != 0 ? 1u : 0u);
+              } else if (kPair) {  // same offsets in both CTAs: each holds its rows of A and its columns of B
                 umma_bf16_pair(d_tmem, ad, bd, kIdesc, (ks | kk) != 0 ? 1u : 0u);
                 if (kDual) umma_bf16_pair(d_tmem, adl, bd, kIdesc, 1u);
               } else {
@@ -1151,6 +1253,24 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = h[i] * sigmoidf_(h[i]) * u[i];  // A, in place of h
+            if (kMx) {
+              // A as block-scaled e4m3: this row's 32 columns are one block; its codes go straight to A's rows,
+              // its scale byte into the row tile's scale block for the down projection (stage col / 128, byte
+              // (col / 32) % 4); a row's last stage past n holds scale 1 (byte 127)
+              uint32_t w[8];
+              const int e = mx_block32(h, w);
+              if (row_ok && ncols >= 32) {
+                uint8_t* dst = static_cast<uint8_t*>(p.out2) + orow * p.ld_out + col;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                const long long rt = s_tile[tl.g] / mx_ncu + tl.m0 / BM;
+                uint8_t* sfw = p.o_sf + (rt * p.o_sf_kst + col / 128) * 512 + lane * 16 + quarter * 4;
+                sfw[(col >> 5) & 3] = static_cast<uint8_t>(e + 127);
+                if (col + 32 == p.N && ((p.N >> 5) & 3) != 0)
+                  for (int k = (p.N >> 5) & 3; k < 4; ++k) sfw[k] = 127;
+              }
+              continue;
+            }
             emit32(o2, h, col, ncols, full, row_ok, false);  // A: bf16 operand of the down projection
             if (p.out3) {  // and the bf16 rounding of what A's bf16 value leaves (the down projection's low part)
 #pragma unroll
@@ -1374,8 +1494,8 @@ template <int BN, int STAGES, int EW, int DEPTH, int AMODE, int BMODE, int VAR, 
           int XF = 0>
 cudaError_t launch_grouped_gemm(const GemmParams& p, const Maps& maps, int grid, cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<BN, STAGES, EW, DEPTH, AMODE, BMODE, VAR, EPI, OUTF32, CN, XF>;
-  const size_t smem =
-      SmemLayout<BN, STAGES, EW, DEPTH, (XF & X_DUAL_A) ? 2 : 1, (XF & X_PAIR) ? BN / 2 : BN>::bytes(p.groups, VAR);
+  const size_t smem = SmemLayout<BN, STAGES, EW, DEPTH, (XF & X_DUAL_A) ? 2 : 1, (XF & X_PAIR) ? BN / 2 : BN,
+                                 mx_stage_bytes(BN, XF)>::bytes(p.groups, VAR);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;

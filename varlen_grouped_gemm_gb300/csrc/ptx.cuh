@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -119,6 +120,20 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// 4 bytes, zero-filled when src_bytes is 0 (through L1; the 16-byte form bypasses it).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte aligned), completing
+// its bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy (UMMA operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -163,6 +178,26 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint6
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Block-scaled e4m3 UMMA (kind::mxf8f6f4, one UE8M0 scale per 32 elements of K on each operand): the
+// scales of A's rows and of B's columns are read from TMEM at sfa and sfb; the instruction descriptor
+// (idesc_mx) selects the byte of each 32-bit TMEM scale word.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// 32 rows of 16 bytes from shared memory into four consecutive 32-bit TMEM columns, the same rows in
+// each of the four 32-lane quarters (row i to lanes i, 32 + i, 64 + i, 96 + i).  Ordered before the
+// UMMAs the same thread issues later.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on an mbarrier once every UMMA issued so far by this thread has completed.
@@ -335,6 +370,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor without swizzle: 8-row core matrices of 16-byte rows, sbo bytes apart
+// along M/N, lbo bytes apart along K.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with both operands e4m3 (format 0) and UE8M0 scales (bit 23):
+// bits 4-5 the byte of B's scale word, 29-30 the byte of A's, fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int a_mn, int b_mn, int sfa_id, int sfb_id) {
+  return (static_cast<uint32_t>(sfb_id & 3) << 4) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id & 3) << 29);
+}
+
 // Instruction descriptor, kind::f16: bf16 A/B, fp32 D, K-major (0) or MN-major (1) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
@@ -366,6 +416,40 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
 // ulp of fp32 (far below the bf16 rounding of the activations it feeds); the correctly rounded division
 // made the SwiGLU epilogue the bottleneck of the gate/up GEMM.  For x below about -87 the result is 0.
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// Block exponent of a 1 x 32 block with largest magnitude amax: the smallest e in [-127, 127] with
+// amax <= 448 2^e (448 = 1.75 2^8, so e = floor(log2 amax) - 8, plus one when the significand exceeds
+// 1.75), 0 for an all-zero block.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (b == 0) return 0;
+  const int be = static_cast<int>((b >> 23) & 0xFFu);
+  if (be == 0) return -127;  // below 2^-126
+  const int e = be - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : e;
+}
+
+// 2^-e as a float for e in [-127, 126] (exact).
+__device__ __forceinline__ float mx_inv_scale(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
+
+// Four e4m3 codes (round to nearest even, saturating) packed little-endian: a in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// One 1 x 32 block to block-scaled e4m3: 32 codes into w (little-endian, 4 per word), returns the exponent.
+__device__ __forceinline__ int mx_block32(const float (&v)[32], uint32_t (&w)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mx_exponent(amax);
+  const float inv = mx_inv_scale(e);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = e4m3x4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+  return e;
+}
 
 }  // namespace vgg
 
