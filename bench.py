@@ -481,6 +481,9 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                               e4m3=True)
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
     w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down, backward=True)
+    bmx = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False, device=X.device,
+                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, mx=True)
+    wmx = vgg.MxWeights.quantize(ctx, W_gate, W_up, W_down)
 
     def e4m3_step():
         vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
@@ -494,6 +497,9 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             # the e4m3 down projection as well
             "e4m3_down8": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8),
             "e4m3_down8_infer": lambda: vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8, cache=False),
+            # the block-scaled (1 x 32) form of both forward GEMMs, A quantized in the gate/up epilogue
+            "mx": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx),
+            "mx_infer": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx, cache=False),
             # training steps
             "bf16_step": lambda: vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf),
             "e4m3_step": e4m3_step}
@@ -536,7 +542,9 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
     qd = out["e4m3_step"][1].get("quantize_do_e4m3", (0.0, 1))
     fl_dn = 2 * P * wl.d * wl.n
     step_fl = wl.flops_fwd_bwd(P)
-    del b8, w8, w8d
+    gmx, dmx = per("mx", "gate_up_swiglu_mx"), per("mx", "down_scale_mx")
+    qmx = out["mx"][1].get("quantize_mx", (0.0, 1))
+    del b8, w8, w8d, bmx, wmx
     return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
             "forward_e4m3_down_ms": out["e4m3_down8"][0],
             "bf16_forward_infer_ms": out["bf16_infer"][0], "forward_infer_ms": out["e4m3_infer"][0],
@@ -551,6 +559,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             "down_tflops": fl_dn / (dn * 1e-3) / 1e12, "dx_tflops": fl / (dx8 * 1e-3) / 1e12,
             "dact_tflops": fl_dn / (da8 * 1e-3) / 1e12,
             "gate_up_peak_tflops": peak8, "gate_up_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
+            "block_scaled": {
+                "forward_ms": out["mx"][0], "forward_infer_ms": out["mx_infer"][0],
+                "gate_up_ms": gmx, "down_ms": dmx, "quantize_x_ms": qmx[0] / max(qmx[1], 1),
+                "gate_up_tflops": fl / (gmx * 1e-3) / 1e12, "down_tflops": fl_dn / (dmx * 1e-3) / 1e12,
+                "gate_up_frac": fl / (gmx * 1e-3) / 1e12 / peak8,
+                "recipe": "e4m3 codes with one power-of-two (UE8M0) scale per 32 values along the reduction "
+                          "dimension of every operand row (kind::mxf8f6f4 UMMA); A quantized in the gate/up "
+                          "epilogue; 128-column tiles"},
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
             "recipe": "e4m3 operands with one fp32 scale per row: X per token, A, dO and [dH|dU] per pair, weights per "
                       "output channel of each GEMM; fp32 accumulation; dW and the router stay bf16",
