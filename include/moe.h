@@ -292,11 +292,12 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
  *              127 up to a multiple of 4 per 128 columns;
  *   blocks     512 bytes per 128 operand rows and 128 columns of the reduction: row r, block k of the
  *              128 columns at byte (r % 32) * 16 + (r / 32) * 4 + k; rows or columns beyond the operand
- *              hold 127.  W_gate / W_up: [E][ceil(n/64)][ceil(d/128)] blocks, rows 0..63 of block
- *              [e][t][.] = W_gate[e] rows 64t..64t+63, rows 64..127 = W_up[e] rows 64t..64t+63; W_down:
- *              [E][ceil(d/128)][ceil(n/128)] blocks over W_down[e] rows 128t..; the activations A:
- *              one block row per 128-row tile of every expert's sorted rows (tiles in expert order),
- *              [tiles][ceil(n/128)].
+ *              hold 127.  The weights' blocks come in pairs (1024 bytes) per 192-row tile and 128 columns:
+ *              W_gate / W_up [E][ceil(n/96)][ceil(d/128)] pairs, tile rows 0..95 of [e][t][.] = W_gate[e]
+ *              rows 96t..96t+95, tile rows 96..191 = W_up[e] rows 96t..96t+95 (tile row i in block i / 128,
+ *              block row i % 128); W_down [E][ceil(d/192)][ceil(n/128)] pairs over W_down[e] rows 192t..;
+ *              the activations A: one block per 128-row tile of every expert's sorted rows (tiles in
+ *              expert order) and 128 columns, [tiles][ceil(n/128)].
  */
 /* Bytes per row of a row-major scale array for `cols` columns: 4 * ceil(cols / 128). */
 long long moe_mx_sf_cols(int cols);

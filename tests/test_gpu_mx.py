@@ -39,16 +39,25 @@ def _block_off(r, b):
     return (r % 32) * 16 + (r // 32) * 4 + b
 
 
-def _unpack_weight_blocks(sf: np.ndarray, E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
-    """Exponents [E, R, C/32] of one weight from its 512-byte scale blocks [E][tiles][ceil(C/128)]."""
+TILE = 192  # the block-scaled GEMMs' tile width: W_down rows per tile, 96 + 96 for the gate/up pair
+
+
+def _weight_index(E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
+    """Byte index [E, R, C/32] of each (row, 32-column block) scale of one weight in its scale buffer:
+    [E][tiles][ceil(C/128)] groups of two 512-byte blocks, tile row i = row0 + row % rows_per_tile in block
+    i // 128."""
     kst = -(-C // 128)
-    tiles = sf.size // (E * kst * 512)
-    blk = sf.reshape(E, tiles, kst, 512)
-    rows = np.arange(R)
-    t, br = rows // rows_per_tile, row0 + rows % rows_per_tile
-    cols = np.arange(C // 32)
-    off = _block_off(br[:, None], cols[None, :] % 4)
-    return blk[:, t[:, None], cols[None, :] // 4, off].astype(np.int64) - 127
+    tiles = -(-R // rows_per_tile)
+    rows = np.arange(R)[:, None]
+    cols = np.arange(C // 32)[None, :]
+    t, tr = rows // rows_per_tile, row0 + rows % rows_per_tile
+    off = ((t * kst + cols // 4) * 2 + tr // 128) * 512 + _block_off(tr % 128, cols % 4)
+    return np.arange(E)[:, None, None] * (tiles * kst * 1024) + off[None]
+
+
+def _unpack_weight_blocks(sf: np.ndarray, E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
+    """Exponents [E, R, C/32] of one weight from its scale buffer."""
+    return sf[_weight_index(E, R, C, rows_per_tile, row0)].astype(np.int64) - 127
 
 
 def _unpack_act_blocks(sf: np.ndarray, offsets: np.ndarray, n: int, rows: np.ndarray) -> np.ndarray:
@@ -97,22 +106,18 @@ def test_mx_weights_bit_exact(ctx, E, d, n):
     w = vgg.MxWeights.quantize(ctx, bits_to_dev(Wg), bits_to_dev(Wu), bits_to_dev(Wd))
     gu = w.gu_sf.cpu().numpy()
     dn = w.dn_sf.cpu().numpy()
+    assert gu.size == E * -(-n // (TILE // 2)) * -(-d // 128) * 1024 and dn.size == E * -(-d // TILE) * -(-n // 128) * 1024
     want = {"gu": np.full_like(gu, 127), "dn": np.full_like(dn, 127)}
-    for got_q, W, R, C, key, rpt, r0 in ((w.Wg_q, Wg, n, d, "gu", 64, 0), (w.Wu_q, Wu, n, d, "gu", 64, 64),
-                                         (w.Wd_q, Wd, d, n, "dn", 128, 0)):
+    for got_q, W, R, C, key, rpt, r0 in ((w.Wg_q, Wg, n, d, "gu", TILE // 2, 0),
+                                         (w.Wu_q, Wu, n, d, "gu", TILE // 2, TILE // 2),
+                                         (w.Wd_q, Wd, d, n, "dn", TILE, 0)):
         q, e = oracle.quantize_blocks_mx(W.reshape(E * R, C))
         np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * R, C), q)
-        # the whole block buffer, built here from the oracle's exponents: entries no weight row or column
+        # the whole scale buffer, built here from the oracle's exponents: entries no weight row or column
         # fills hold scale 1 (byte 127)
-        kst = -(-C // 128)
-        blk = want[key].reshape(E, -1, kst, 512)
-        rows, cols = np.meshgrid(np.arange(R), np.arange(C // 32), indexing="ij")
-        for ex in range(E):
-            blk[ex, rows // rpt, cols // 4, _block_off(r0 + rows % rpt, cols % 4)] = e.reshape(E, R, -1)[ex] + 127
+        want[key][_weight_index(E, R, C, rpt, r0)] = e.reshape(E, R, -1) + 127
     np.testing.assert_array_equal(gu, want["gu"])
     np.testing.assert_array_equal(dn, want["dn"])
-    np.testing.assert_array_equal(_unpack_weight_blocks(gu, E, n, d, 64, 64).reshape(E * n, -1),
-                                  oracle.quantize_blocks_mx(Wu.reshape(E * n, d))[1])
 
 
 CASES = [

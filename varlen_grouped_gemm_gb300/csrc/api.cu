@@ -748,8 +748,10 @@ long long moe_mx_sf_cols(int cols) { return cols > 0 ? 4ll * ceil_div(cols, 128)
 
 long long moe_mx_weight_sf_bytes(int E, int d, int n, int which) {
   if (E < 1 || d < 64 || n < 64 || d % 64 || n % 64) return 0;
-  if (which == 0) return 512ll * E * ceil_div(n, 64) * ceil_div(d, 128);
-  if (which == 1) return 512ll * E * ceil_div(d, 128) * ceil_div(n, 128);
+  // one group of mx_b_blocks(kMxBN) blocks per column tile and stage of K (the gate/up pair: kMxBN / 2 rows of each)
+  const long long grp = 512ll * mx_b_blocks(kMxBN);
+  if (which == 0) return grp * E * ceil_div(n, kMxBN / 2) * ceil_div(d, 128);
+  if (which == 1) return grp * E * ceil_div(d, kMxBN) * ceil_div(n, 128);
   return 0;
 }
 
@@ -785,16 +787,16 @@ int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, 
   // every entry of the blocks that no operand row or column fills holds scale 1
   VGG_CUDA(cudaMemsetAsync(gu_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 0)), s));
   VGG_CUDA(cudaMemsetAsync(dn_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 1)), s));
-  const int kd = ceil_div(d, 128), kn = ceil_div(n, 128);
+  const int kd = ceil_div(d, 128), kn = ceil_div(n, 128), nb = mx_b_blocks(kMxBN), hb = kMxBN / 2;
   VGG_LAUNCH("quantize_mx_weights",
              launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_gate), E, n, d, static_cast<uint8_t*>(Wg_q),
-                                       static_cast<uint8_t*>(gu_sf), 64, 0, ceil_div(n, 64), kd, s));
+                                       static_cast<uint8_t*>(gu_sf), hb, 0, ceil_div(n, hb), kd, nb, s));
   VGG_LAUNCH("quantize_mx_weights",
              launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_up), E, n, d, static_cast<uint8_t*>(Wu_q),
-                                       static_cast<uint8_t*>(gu_sf), 64, 64, ceil_div(n, 64), kd, s));
+                                       static_cast<uint8_t*>(gu_sf), hb, hb, ceil_div(n, hb), kd, nb, s));
   VGG_LAUNCH("quantize_mx_weights",
              launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_down), E, d, n, static_cast<uint8_t*>(Wd_q),
-                                       static_cast<uint8_t*>(dn_sf), 128, 0, ceil_div(d, 128), kn, s));
+                                       static_cast<uint8_t*>(dn_sf), kMxBN, 0, ceil_div(d, kMxBN), kn, nb, s));
   return MOE_OK;
 }
 
@@ -836,12 +838,12 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
     p.o_sf = static_cast<uint8_t*>(a_sf);
     p.o_sf_kst = ceil_div(n, 128);
     Maps m = zero_maps();
-    if (!make_map_3d(&m.b0, Wg_q, dk, n, E, 64) || !make_map_3d(&m.b1, Wu_q, dk, n, E, 64) ||
+    if (!make_map_3d(&m.b0, Wg_q, dk, n, E, kMxBN / 2) || !make_map_3d(&m.b1, Wu_q, dk, n, E, kMxBN / 2) ||
         (H && (!make_store_map_2d(&m.o0, H, true, n, cap, n, 32) || !make_store_map_2d(&m.o1, U, true, n, cap, n, 32))))
       return MOE_ERR_CUDA;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, 64);
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, kMxBN / 2);
     // pairs of CTAs on neighbouring column tiles share the gathered X rows (each gathers half the codes)
-    const int cn = ceil_div(n, 64) >= 2 ? 2 : 1;
+    const int cn = ceil_div(n, kMxBN / 2) >= 2 ? 2 : 1;
     VGG_LAUNCH("gate_up_swiglu_mx", run_gate_up_swiglu_mx(cn, p, m, std::min(tiles, ctx->num_sms), s));
   }
   {
@@ -858,12 +860,12 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
     p.b_sf = static_cast<const uint8_t*>(dn_sf);
     p.sf_kst = ceil_div(n, 128);
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, 128) ||
+    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, kMxBN) ||
         !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, 128);
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, kMxBN);
     VGG_LAUNCH("down_scale_mx", run_down_scale_mx(p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;

@@ -70,13 +70,14 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //             and half of B's columns, both CTAs' TMA loads complete on the even CTA's barriers, the even CTA
 //             issues the M = 256 UMMAs, and each CTA drains its own 128 TMEM rows (varlen-K with padded B).
 //   X_MX      block-scaled e4m3 operands (kind::mxf8f6f4): every 32 codes of an operand row along K carry
-//             one power-of-two scale (UE8M0 byte).  A stage holds, after its A and B tiles, the 128 x 4
-//             scale bytes of A's rows and of B's rows for its 128 codes of K in the layout tcgen05.cp reads
+//             one power-of-two scale (UE8M0 byte).  A stage holds, after its A and B tiles, the 4 scale
+//             bytes of each of A's 128 rows and of B's rows (one 512-byte block per 128 rows, the last one
+//             padded) for its 128 codes of K in the layout tcgen05.cp reads
 //             (row r, 32-code block k at byte (r % 32) 16 + (r / 32) 4 + k); the issuer copies them into
 //             TMEM columns of that stage (past the two accumulators) before the stage's UMMAs.  Gathered A
 //             rows take their 4 scale bytes from a row-major [rows][sf_ld] array (cp.async, 4 bytes);
 //             tiled A and the weights take whole 512-byte blocks laid out that way in global memory.
-//             BN = 128, so that both accumulators and every stage's scales fit the 512 TMEM columns.  The
+//             BN = 128 or 192, so that both accumulators and every stage's scales fit the 512 TMEM columns.  The
 //             SwiGLU epilogue of this form emits A itself as block-scaled codes (a thread's 32 columns of
 //             its row are one block) with the scale blocks the down projection reads.
 enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4, X_MX = 8 };
@@ -130,7 +131,7 @@ struct GemmParams {
   const float* q_col;
   int q_ld;
   // block-scaled form (X_MX): scale bytes of A (gathered: row-major [a_rows][a_sf_ld]; tiled: 512-byte blocks
-  // [row tile][sf_kst]), of B (512-byte blocks per 128 rows of a stage: [groups][column tile][sf_kst]) and of
+  // [row tile][sf_kst]), of B (ceil(BN / 128) 512-byte blocks per stage: [groups][column tile][sf_kst]) and of
   // the SwiGLU epilogue's block-scaled A (o_sf: [row tile][o_sf_kst] blocks); sf_kst = stages of K
   const uint8_t* a_sf;
   long long a_sf_ld;
@@ -179,9 +180,11 @@ struct SmemLayout {
   }
 };
 
-// Scale-block bytes of one stage of the block-scaled form (A's 512 bytes, then B's BN x 4), padded to 1024.
+// Block-scaled form: B's scale blocks per stage (one 512-byte block per 128 rows of B), and the scale bytes of one
+// stage (A's block, then B's), padded to 1024.
+__host__ __device__ constexpr int mx_b_blocks(int BN) { return (BN + 127) / 128; }
 __host__ __device__ constexpr int mx_stage_bytes(int BN, int XF) {
-  return (XF & X_MX) ? ((512 + BN * 4 + 1023) / 1024) * 1024 : 0;
+  return (XF & X_MX) ? ((512 + 512 * mx_b_blocks(BN) + 1023) / 1024) * 1024 : 0;
 }
 
 struct Tile {
@@ -447,11 +450,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   // are those of the bf16 form with K counted in code pairs; only the UMMA kind changes.
   constexpr bool kF8 =
       (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q || EPI == EPI_DSWIGLU_Q) || kMx;
-  static_assert(!kMx || (BN == 128 && VAR == VAR_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
+  static_assert(!kMx || ((BN == 128 || BN == 192) && VAR == VAR_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
                          (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) && (CN == 1 || CN == 2) &&
                          (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_STORE || EPI == EPI_DSWIGLU)),
-                "block-scaled form: BN = 128, K-major operands, varlen-M, plain epilogue kinds");
-  static_assert(!kMx || 2 * BN + STAGES * (4 + BN / 32) <= 512, "block-scaled form: TMEM columns");
+                "block-scaled form: BN = 128 or 192, K-major operands, varlen-M, plain epilogue kinds");
+  static_assert(!kMx || 2 * BN + STAGES * (4 + 4 * mx_b_blocks(BN)) <= 512, "block-scaled form: TMEM columns");
   static_assert(EPI != EPI_STORE_Q || !OUTF32, "the e4m3 plain epilogue stores bf16");
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
                          VAR == VAR_M),
@@ -493,9 +496,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   constexpr uint32_t kTxBytes =
       kPair ? 2 * (L::kABytes + L::kBBytes)
             : (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes) +
-                  (kMx ? BN * 4 + (kAGather ? 0 : 512) : 0);
+                  (kMx ? 512 * mx_b_blocks(BN) + (kAGather ? 0 : 512) : 0);
   constexpr uint32_t kTmemCols = kMx ? 512 : (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
-  constexpr int kSfCols = 4 + BN / 32;  // TMEM columns of one stage's scales (A: 4, B: BN / 32)
+  constexpr int kSfCols = 4 + 4 * mx_b_blocks(BN);  // TMEM columns of one stage's scales (A: 4, B: 4 per block)
   constexpr uint32_t kIdesc =
       kF8 ? idesc_e4m3(BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0) : idesc_bf16(kPair ? 2 * BM : BM, BN, kAMn ? 1 : 0, kBMn ? 1 : 0);
 
@@ -706,8 +709,9 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
             bulk_load(sf, p.a_sf + (rt * p.sf_kst + kstage) * 512, 512, bar);
           }
           const int nt = min(x.nt, sch.ntiles - 1);
-          bulk_load(sf + 512, p.b_sf + ((static_cast<long long>(x.g) * sch.ntiles + nt) * p.sf_kst + kstage) * (BN * 4),
-                    BN * 4, bar);
+          constexpr int kSfb = 512 * mx_b_blocks(BN);
+          bulk_load(sf + 512, p.b_sf + ((static_cast<long long>(x.g) * sch.ntiles + nt) * p.sf_kst + kstage) * kSfb,
+                    kSfb, bar);
         }
         if (BMODE == B_TMA_K3) {
           if (l2) tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
@@ -1010,7 +1014,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
               const uint32_t sf_s = sb + L::kBBytes;
               tmem_cp_32x128b_x4(sf_t, sdesc_plain(sf_s, 128, 128));
 #pragma unroll
-              for (int a = 0; a < BN / 128; ++a)
+              for (int a = 0; a < mx_b_blocks(BN); ++a)
                 tmem_cp_32x128b_x4(sf_t + 4 + 4 * a, sdesc_plain(sf_s + 512 + 512 * a, 128, 128));
             }
 #pragma unroll

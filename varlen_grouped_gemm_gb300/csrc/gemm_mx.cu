@@ -9,10 +9,12 @@
 //   row-major  [rows][4 ceil(cols / 128)] bytes (the per-token X scales, gathered by the GEMM 4 bytes per row
 //              and stage); entries past cols / 32 hold 127 (scale 1);
 //   blocks     512 bytes per 128 operand rows and 128 codes of K, the layout tcgen05.cp reads: row r, 32-code
-//              block k at byte (r % 32) 16 + (r / 32) 4 + k.  W_gate / W_up: [E][ceil(n / 64)][ceil(d / 128)],
-//              rows 0..63 of a block = W_gate rows 64 t.., rows 64..127 = W_up rows 64 t.. (one gate/up
-//              column tile); W_down: [E][ceil(d / 128)][ceil(n / 128)]; the activations A (written by the
-//              SwiGLU epilogue): [row tile][ceil(n / 128)].  Entries with no operand row or past K hold 127.
+//              block k at byte (r % 32) 16 + (r / 32) 4 + k.  The weights' blocks follow the GEMMs' 192-column
+//              tiles, two blocks (1024 bytes) per tile and stage: W_gate / W_up [E][ceil(n / 96)][ceil(d / 128)],
+//              tile rows 0..95 = W_gate rows 96 t.., rows 96..191 = W_up rows 96 t.. (one gate/up column tile);
+//              W_down [E][ceil(d / 192)][ceil(n / 128)], tile rows = W_down rows 192 t..; the activations A
+//              (written by the SwiGLU epilogue): one block per row tile and stage, [row tile][ceil(n / 128)].
+//              Entries with no operand row or past K hold 127.
 #include "internal.h"
 
 namespace vgg {
@@ -61,18 +63,20 @@ cudaError_t launch_quantize_rows_mx(const __nv_bfloat16* M, long long rows, cons
   return cudaGetLastError();
 }
 
-// Weights [E][R][C]: codes in place of the values, scales into 512-byte blocks [E][ntile][kst] in which operand
-// row `row` is block row roff + row % rpt of column tile row / rpt (the block buffer is set to 127 first).
+// Weights [E][R][C]: codes in place of the values, scales into [E][ntile][kst] groups of nblk 512-byte blocks in
+// which operand row `row` is tile row roff + row % rpt (block (tile row) / 128) of column tile row / rpt (the
+// block buffer is set to 127 first).
 __global__ void __launch_bounds__(256) quantize_weight_mx_kernel(const __nv_bfloat16* __restrict__ W, int E, int R,
                                                                  int C, uint8_t* __restrict__ q,
                                                                  uint8_t* __restrict__ blocks, int rpt, int roff,
-                                                                 int ntile, int kst) {
+                                                                 int ntile, int kst, int nblk) {
   const long long wr = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // e * R + row
   const int lane = threadIdx.x & 31;
   if (wr >= static_cast<long long>(E) * R) return;
   const int e = static_cast<int>(wr / R), row = static_cast<int>(wr % R);
-  const int t = row / rpt, br = roff + row % rpt;
-  uint8_t* blk = blocks + (static_cast<long long>(e) * ntile + t) * kst * 512 + (br & 31) * 16 + (br >> 5) * 4;
+  const int t = row / rpt, tr = roff + row % rpt, br = tr & 127;
+  uint8_t* blk = blocks + (static_cast<long long>(e) * ntile + t) * kst * (512ll * nblk) + (tr >> 7) * 512 +
+                 (br & 31) * 16 + (br >> 5) * 4;
   for (int b = lane; b < C / 32; b += 32) {
     const uint4* src = reinterpret_cast<const uint4*>(W + wr * C + 32 * b);
     float v[32];
@@ -92,32 +96,33 @@ __global__ void __launch_bounds__(256) quantize_weight_mx_kernel(const __nv_bflo
     uint4* dst = reinterpret_cast<uint4*>(q + wr * C + 32 * b);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    blk[(b >> 2) * 512 + (b & 3)] = static_cast<uint8_t>(ex + 127);
+    blk[(b >> 2) * (512ll * nblk) + (b & 3)] = static_cast<uint8_t>(ex + 127);
   }
 }
 
 cudaError_t launch_quantize_weight_mx(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, uint8_t* blocks,
-                                      int rpt, int roff, int ntile, int kst, cudaStream_t s) {
+                                      int rpt, int roff, int ntile, int kst, int nblk, cudaStream_t s) {
   const long long warps = static_cast<long long>(E) * R;
   if (warps <= 0) return cudaSuccess;
   quantize_weight_mx_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(W, E, R, C, q, blocks, rpt, roff,
-                                                                                 ntile, kst);
+                                                                                 ntile, kst, nblk);
   return cudaGetLastError();
 }
 
 // Gate/up + SwiGLU on block-scaled operands: gathered X codes (scales gathered 4 bytes per row and stage), the
-// W_gate / W_up pair, 64 + 64 output columns per tile; the epilogue writes H, U (fp32, when cached) and A as
-// block-scaled codes with their scale blocks.
+// W_gate / W_up pair, 96 + 96 output columns per tile (two 192-column accumulators and four stages of scales
+// fill 432 of the 512 TMEM columns); the epilogue writes H, U (fp32, when cached) and A as block-scaled codes
+// with their scale blocks.
 cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (cn == 2)
-    return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 2, X_MX>(p, m, grid, s);
-  return launch_grouped_gemm<128, 6, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 1, X_MX>(p, m, grid, s);
+    return launch_grouped_gemm<kMxBN, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 2, X_MX>(p, m, grid, s);
+  return launch_grouped_gemm<kMxBN, 4, 4, 1, A_GATHER_K, B_TMA_K3_GU, VAR_M, EPI_SWIGLU, false, 1, X_MX>(p, m, grid, s);
 }
 
 // Down projection on block-scaled A (rows of the SwiGLU epilogue's codes, scale blocks per row tile) and
-// W_down; the epilogue scales each row by its combine weight (Yw, bf16).
+// W_down, 192 output columns per tile; the epilogue scales each row by its combine weight (Yw, bf16).
 cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
-  return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_MX>(p, m, grid, s);
+  return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_MX>(p, m, grid, s);
 }
 
 }  // namespace vgg

@@ -40,13 +40,14 @@ cudaError_t launch_transpose_into_bf16(const __nv_bfloat16* in, int E, int R, in
 cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                       uint8_t* q, float* scales, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-// block-scaled (1 x 32) e4m3 forward
+// block-scaled (1 x 32) e4m3 forward: tile width of both GEMMs (the gate/up pair: kMxBN / 2 output columns)
+constexpr int kMxBN = 192;
 cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rows_mx(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                     uint8_t* q, uint8_t* sf, int sf_ld, cudaStream_t s);
 cudaError_t launch_quantize_weight_mx(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, uint8_t* blocks,
-                                      int rpt, int roff, int ntile, int kst, cudaStream_t s);
+                                      int rpt, int roff, int ntile, int kst, int nblk, cudaStream_t s);
 cudaError_t run_down_scale_dual(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
