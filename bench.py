@@ -82,6 +82,7 @@ def kernel_work(wl, P, dW_bytes=2):
         "quantize_e4m3": same(0, 3 * T * d + 4 * T),
         # block-scaled form: codes of 1 byte plus one scale byte per 32 values
         "quantize_mx": same(0, 3 * T * d + T * d // 32),
+        "mx_tile_scales": same(0, 2 * P * d // 32 + 4 * P),  # the gathered rows' scale bytes, read and re-laid
         "quantize_mx_weights": same(0, 3 * E * n * d + E * n * d // 32),  # one weight per launch (outside the step)
         "gate_up_swiglu_mx": (4 * P * d * n, T * d + T * d // 32 + 2 * E * n * d + 2 * E * n * d // 32 + 4 * P * n
                               + P * n + P * n // 32,
@@ -215,7 +216,7 @@ _OTHER_LABELS = {
     "splitk_reduce_kernel": "dwr_reduce", "gather_rows_bulk_kernel": "gather_rows",
     "zero_tail_rows_kernel": "zero_tail", "quantize_rows_e4m3_kernel": "quantize_e4m3",
     "pad_offsets_kernel": "pad_offsets", "quantize_rows_mx_kernel": "quantize_mx",
-    "quantize_weight_mx_kernel": "quantize_mx_weights",
+    "quantize_weight_mx_kernel": "quantize_mx_weights", "mx_tile_scales_kernel": "mx_tile_scales",
 }
 
 

@@ -338,6 +338,8 @@ int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, 
  *            activation scale blocks a_sf (moe_mx_act_sf_bytes(cap,E,n) bytes),
  *   Yw[j,c] = sorted_w[j] * sum_i dq(Aq[j,i]) dq(Wd_q[e,c,i])  (bf16).
  *
+ * x_sf_tiles (moe_mx_act_sf_bytes(cap,E,d) bytes, caller-owned scratch, overwritten) receives the gathered
+ * rows' scales laid out per sorted row tile, the form the gate/up GEMM loads them in.
  * Block products are accumulated in fp32 on the tensor cores.  A slot with sorted_tok = -1 (capacity
  * dispatch) gives zero rows.  H, U [cap,n] fp32 are the backward's cache (both NULL: forward only).  Rows of
  * Aq at or past offsets[E], and scale bytes of rows past an expert's last row, are not written.  Shape rules
@@ -347,7 +349,7 @@ int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, 
 int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, const void* Wg_q, const void* Wu_q,
                             const void* gu_sf, const void* Wd_q, const void* dn_sf, int T, int d, int E, int n,
                             long long cap, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
-                            void* H, void* U, void* Aq, void* a_sf, void* Yw, moe_stream_t stream);
+                            void* H, void* U, void* x_sf_tiles, void* Aq, void* a_sf, void* Yw, moe_stream_t stream);
 
 /*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.

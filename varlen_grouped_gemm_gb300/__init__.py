@@ -99,7 +99,7 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_rows_mx.argtypes = [_P, _P, _LL, _I, _P, _P, _P]
         L.moe_quantize_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
         L.moe_grouped_gemm_fwd_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P,
-                                              _P, _P, _P, _P, _P]
+                                              _P, _P, _P, _P, _P, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -342,8 +342,10 @@ def moe_quantize_weights_mx(ctx, W_gate, W_up, W_down, Wg_q, Wu_q, gu_sf, Wd_q, 
         _ptr(gu_sf, u8), _ptr(Wd_q, u8), _ptr(dn_sf, u8), _stream(stream)))
 
 
-def moe_grouped_gemm_fwd_mx(ctx, Xq, x_sf, w, offsets, sorted_tok, sorted_w, H, U, Aq, a_sf, Yw, stream=None):
-    """Block-scaled gate/up (+ SwiGLU, A quantized in the epilogue) and down projection; ``w`` is MxWeights."""
+def moe_grouped_gemm_fwd_mx(ctx, Xq, x_sf, w, offsets, sorted_tok, sorted_w, H, U, x_sf_tiles, Aq, a_sf, Yw,
+                            stream=None):
+    """Block-scaled gate/up (+ SwiGLU, A quantized in the epilogue) and down projection; ``w`` is MxWeights,
+    ``x_sf_tiles`` scratch of mx_act_sf_bytes(cap, E, d) bytes."""
     T, d = Xq.shape
     E, n, _ = w.Wg_q.shape
     cap = sorted_tok.numel()
@@ -351,8 +353,8 @@ def moe_grouped_gemm_fwd_mx(ctx, Xq, x_sf, w, offsets, sorted_tok, sorted_w, H, 
     _check("moe_grouped_gemm_fwd_mx", lib().moe_grouped_gemm_fwd_mx(
         ctx.handle, _ptr(Xq, u8), _ptr(x_sf, u8), _ptr(w.Wg_q, u8), _ptr(w.Wu_q, u8), _ptr(w.gu_sf, u8),
         _ptr(w.Wd_q, u8), _ptr(w.dn_sf, u8), T, d, E, n, cap, _ptr(offsets, torch.int32),
-        _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32), _ptr(Aq, u8), _ptr(a_sf, u8),
-        _ptr(Yw, torch.bfloat16), _stream(stream)))
+        _ptr(sorted_tok, torch.int32), _ptr(sorted_w, f32), _ptr(H, f32), _ptr(U, f32), _ptr(x_sf_tiles, u8),
+        _ptr(Aq, u8), _ptr(a_sf, u8), _ptr(Yw, torch.bfloat16), _stream(stream)))
 
 
 def moe_combine(ctx, Yw, tok_ptr, tok_pairs, O, stream=None):
@@ -513,6 +515,7 @@ class Buffers:
     mxsf: torch.Tensor | None = None
     maq: torch.Tensor | None = None  # block-scaled down projection: A's codes [cap, n] and scale blocks
     masf: torch.Tensor | None = None
+    mxsft: torch.Tensor | None = None  # block-scaled gate/up: the gathered X rows' scales per sorted row tile
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
@@ -556,7 +559,8 @@ class Buffers:
             dos=z((cap,), f32) if (e4m3 and backward) else None,
             mxq=z((T, d), torch.uint8) if mx else None, mxsf=z((T, mx_sf_cols(d)), torch.uint8) if mx else None,
             maq=z((cap, n), torch.uint8) if mx else None,
-            masf=z((mx_act_sf_bytes(cap, E, n),), torch.uint8) if mx else None)
+            masf=z((mx_act_sf_bytes(cap, E, n),), torch.uint8) if mx else None,
+            mxsft=z((mx_act_sf_bytes(cap, E, d),), torch.uint8) if mx else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, cache=True):
@@ -686,7 +690,8 @@ def forward_mx(ctx, X, W_r, bias, wmx: MxWeights, buf: Buffers, stream=None, cac
                     buf.offsets, buf.sorted_tok, buf.sorted_w, buf.tok_ptr, buf.tok_pairs, buf.P, buf.ws, stream)
     moe_quantize_rows_mx(ctx, X, buf.mxq, buf.mxsf, stream)
     moe_grouped_gemm_fwd_mx(ctx, buf.mxq, buf.mxsf, wmx, buf.offsets, buf.sorted_tok, buf.sorted_w,
-                            buf.H if cache else None, buf.U if cache else None, buf.maq, buf.masf, buf.Yw, stream)
+                            buf.H if cache else None, buf.U if cache else None, buf.mxsft, buf.maq, buf.masf, buf.Yw,
+                            stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 

@@ -803,19 +803,24 @@ int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, 
 int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, const void* Wg_q, const void* Wu_q,
                             const void* gu_sf, const void* Wd_q, const void* dn_sf, int T, int d, int E, int n,
                             long long cap, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
-                            void* H, void* U, void* Aq, void* a_sf, void* Yw, moe_stream_t stream) {
+                            void* H, void* U, void* x_sf_tiles, void* Aq, void* a_sf, void* Yw, moe_stream_t stream) {
   VGG_REQUIRE(ctx && Xq && x_sf && Wg_q && Wu_q && gu_sf && Wd_q && dn_sf && offsets && sorted_tok && sorted_w &&
-              Aq && a_sf && Yw);
+              x_sf_tiles && Aq && a_sf && Yw);
   VGG_REQUIRE((H == nullptr) == (U == nullptr));  // both NULL: forward only, no backward cache
   VGG_REQUIRE(shapes_ok(T, d, E, n, 1));
   VGG_REQUIRE(cap >= 1 && cap < INT_MAX);
   VGG_REQUIRE(aligned16(Xq) && (reinterpret_cast<uintptr_t>(x_sf) & 3u) == 0 && aligned16(Wg_q) &&
               aligned16(Wu_q) && aligned16(gu_sf) && aligned16(Wd_q) && aligned16(dn_sf) && aligned16(H) &&
-              aligned16(U) && aligned16(Aq) && aligned16(a_sf) && aligned16(Yw));
+              aligned16(U) && aligned16(x_sf_tiles) && aligned16(Aq) && aligned16(a_sf) && aligned16(Yw));
   DeviceGuard g(ctx->device);
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int dk = d / 2, nk = n / 2;  // e4m3 rows as 16-bit units (code pairs) for TMA and the gather
+  // the gathered X rows' scales, laid out per sorted row tile and stage of K as the GEMM's producer loads them
+  VGG_LAUNCH("mx_tile_scales",
+             launch_mx_tile_scales(static_cast<const uint8_t*>(x_sf), static_cast<int>(moe_mx_sf_cols(d)), T,
+                                   sorted_tok, static_cast<int>(cap), offsets, E, ceil_div(d, 128),
+                                   ceil_div(cap, BM) + E, static_cast<uint8_t*>(x_sf_tiles), s));
   {
     GemmParams p = base_params(ctx);
     p.N = n;
@@ -831,8 +836,7 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
     p.out1 = U;
     p.out2 = Aq;
     p.ld_out = n;
-    p.a_sf = static_cast<const uint8_t*>(x_sf);
-    p.a_sf_ld = moe_mx_sf_cols(d);
+    p.a_sf = static_cast<const uint8_t*>(x_sf_tiles);
     p.b_sf = static_cast<const uint8_t*>(gu_sf);
     p.sf_kst = ceil_div(d, 128);
     p.o_sf = static_cast<uint8_t*>(a_sf);

@@ -74,9 +74,10 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //             bytes of each of A's 128 rows and of B's rows (one 512-byte block per 128 rows, the last one
 //             padded) for its 128 codes of K in the layout tcgen05.cp reads
 //             (row r, 32-code block k at byte (r % 32) 16 + (r / 32) 4 + k); the issuer copies them into
-//             TMEM columns of that stage (past the two accumulators) before the stage's UMMAs.  Gathered A
-//             rows take their 4 scale bytes from a row-major [rows][sf_ld] array (cp.async, 4 bytes);
-//             tiled A and the weights take whole 512-byte blocks laid out that way in global memory.
+//             TMEM columns of that stage (past the two accumulators) before the stage's UMMAs.  The producer
+//             brings every stage's scale bytes as whole 512-byte blocks laid out that way in global memory:
+//             A's per row tile (for gathered rows, laid out per sorted row tile before the GEMM), B's per
+//             column tile.
 //             BN = 128 or 192, so that both accumulators and every stage's scales fit the 512 TMEM columns.  The
 //             SwiGLU epilogue of this form emits A itself as block-scaled codes (a thread's 32 columns of
 //             its row are one block) with the scale blocks the down projection reads.
@@ -130,11 +131,10 @@ struct GemmParams {
   const float* q_row;  // e4m3 dSwiGLU: A row scales [rows], B row scales [groups][q_ld]
   const float* q_col;
   int q_ld;
-  // block-scaled form (X_MX): scale bytes of A (gathered: row-major [a_rows][a_sf_ld]; tiled: 512-byte blocks
-  // [row tile][sf_kst]), of B (ceil(BN / 128) 512-byte blocks per stage: [groups][column tile][sf_kst]) and of
+  // block-scaled form (X_MX): scale bytes of A (512-byte blocks [row tile][sf_kst], row tiles of the varlen-M
+  // order), of B (ceil(BN / 128) 512-byte blocks per stage: [groups][column tile][sf_kst]) and of
   // the SwiGLU epilogue's block-scaled A (o_sf: [row tile][o_sf_kst] blocks); sf_kst = stages of K
   const uint8_t* a_sf;
-  long long a_sf_ld;
   const uint8_t* b_sf;
   int sf_kst;
   uint8_t* o_sf;
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
   constexpr uint32_t kTxBytes =
       kPair ? 2 * (L::kABytes + L::kBBytes)
             : (kAGather ? (CN - 1) * kSliceBytes : L::kABytes) + (kBGather ? 0 : L::kBBytes) +
-                  (kMx ? 512 * mx_b_blocks(BN) + (kAGather ? 0 : 512) : 0);
+                  (kMx ? 512 * mx_b_blocks(BN) + 512 : 0);
   constexpr uint32_t kTmemCols = kMx ? 512 : (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
   constexpr int kSfCols = 4 + 4 * mx_b_blocks(BN);  // TMEM columns of one stage's scales (A: 4, B: 4 per block)
   constexpr uint32_t kIdesc =
@@ -701,10 +701,11 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
           }
         }
         if (kMx && !l2) {
-          // the stage's scale blocks: A's (a tiled A: its row tile's block for this stage of K), then B's (a
-          // cluster CTA past the last column tile loads the last tile's block; its results are not stored)
+          // the stage's scale blocks: A's (its row tile's block for this stage of K, tiled or gathered rows
+          // alike), then B's (a cluster CTA past the last column tile loads the last tile's block; its results
+          // are not stored)
           uint8_t* sf = sb + L::kBBytes;
-          if (AMODE == A_TMA_K) {
+          {
             const long long rt = s_tile[x.g] / mx_ncu + x.m0 / BM;
             bulk_load(sf, p.a_sf + (rt * p.sf_kst + kstage) * 512, 512, bar);
           }
@@ -807,25 +808,14 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
     const uint64_t pol_keep = l2_policy_evict_last();  // gathered rows are re-read by many tiles
     auto fetch = [&](const Pos& x, int (&r)[8], const Pos& prev, const int (&pr)[8]) {
       if (AMODE == A_GATHER_K) {
-        // block-scaled form with a cluster: r[kRowsPer + i] are the peer slice's rows (their scale bytes are
-        // gathered here too), loaded by the c16 == 1 threads that copy them
-        constexpr int kIdx = (kMx && kRelay) ? 2 * kRowsPer : kRowsPer;
         if (x.t == prev.t) {
 #pragma unroll
-          for (int i = 0; i < kIdx; ++i) r[i] = pr[i];
+          for (int i = 0; i < kRowsPer; ++i) r[i] = pr[i];
         } else {
 #pragma unroll
           for (int i = 0; i < kRowsPer; ++i) {
             const int rr = slice0 + rsub + kRStep * i;
             r[i] = rr < x.tl.rows ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
-          }
-          if (kMx && kRelay) {
-            const int peer0 = (sch.rank ^ 1) * kSlice;
-#pragma unroll
-            for (int i = 0; i < kRowsPer; ++i) {
-              const int rr = peer0 + rsub + kRStep * i;
-              r[kRowsPer + i] = (c16 == 1 && rr < x.tl.rows) ? __ldg(p.a_idx + s_off[x.tl.g] + x.tl.m0 + rr) : -1;
-            }
           }
         }
       } else {
@@ -871,31 +861,6 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
           }
           cp_async_16_hint(sa + sw128_offset(slice0 + rsub + kRStep * i, c16), ok ? p.a_src + row * p.a_ld + kc : p.a_src,
                            ok ? 16u : 0u, pol_keep);
-        }
-        if (kMx) {
-          // the stage's 4 scale bytes of every row of the tile, into the scale block after A and B: own rows by
-          // the c16 == 0 threads, with a cluster the peer's rows by the c16 == 1 threads (the relay forwards
-          // codes only); rows past the group's end get zeros
-          const uint32_t sfa = sa + L::kABytes + L::kBBytes;
-          const long long ko = static_cast<long long>(q0.tl.k_begin / BK + q0.ks) * 4;
-          if (c16 == 0) {
-#pragma unroll
-            for (int i = 0; i < kRowsPer; ++i) {
-              const int rr = slice0 + rsub + kRStep * i;
-              const long long row = r0[i];
-              const bool ok = row >= 0 && row < p.a_rows;
-              cp_async_4(sfa + (rr & 31) * 16 + (rr >> 5) * 4, ok ? p.a_sf + row * p.a_sf_ld + ko : p.a_sf, ok ? 4u : 0u);
-            }
-          } else if (kRelay && c16 == 1) {
-            const int peer0 = (sch.rank ^ 1) * kSlice;
-#pragma unroll
-            for (int i = 0; i < kRowsPer; ++i) {
-              const int rr = peer0 + rsub + kRStep * i;
-              const long long row = r0[kRowsPer + i];
-              const bool ok = row >= 0 && row < p.a_rows;
-              cp_async_4(sfa + (rr & 31) * 16 + (rr >> 5) * 4, ok ? p.a_sf + row * p.a_sf_ld + ko : p.a_sf, ok ? 4u : 0u);
-            }
-          }
         }
       } else if (AMODE == A_GATHER_MN) {
 #pragma unroll

@@ -109,6 +109,66 @@ cudaError_t launch_quantize_weight_mx(const __nv_bfloat16* W, int E, int R, int 
   return cudaGetLastError();
 }
 
+// The scale blocks of a gathered operand, in the varlen-M GEMMs' row-tile order: for every row tile of every
+// group (tiles of 128 sorted rows, groups in order) and stage of K, the 512-byte block whose row r holds the 4
+// scale bytes of sorted row off[g] + 128 m + r, taken from the source row idx[that row] of the row-major
+// [rows][sf_ld] scales (zeros for a row past the group's end or without a source row).  One block per row tile:
+// warp 0 finds the tile's group from a prefix of the groups' tile counts, then thread t copies the words of row
+// t % 128 for the stages k = t / 128, t / 128 + 2, ...
+__global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint8_t* __restrict__ sf, int sf_ld, int src_rows,
+                                                             const int32_t* __restrict__ idx, int idx_rows,
+                                                             const int32_t* __restrict__ off, int G, int kst,
+                                                             uint8_t* __restrict__ blocks) {
+  __shared__ int s_row0, s_end;
+  const long long tile = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int running = 0, row0 = -1, end = 0;
+    for (int base = 0; base < G && row0 < 0; base += 32) {
+      const int g = base + lane;
+      const int o = g < G ? __ldg(off + g) : 0, o1 = g < G ? __ldg(off + g + 1) : 0;
+      const int cnt = g < G ? (o1 - o + 127) / 128 : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int k = 1; k < 32; k <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, k);
+        if (lane >= k) incl += y;
+      }
+      const int first = running + incl - cnt;
+      const unsigned hit = __ballot_sync(0xffffffffu, g < G && tile >= first && tile < first + cnt);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        row0 = __shfl_sync(0xffffffffu, o + static_cast<int>(tile - first) * 128, src);
+        end = __shfl_sync(0xffffffffu, o1, src);
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_row0 = row0;
+      s_end = end;
+    }
+  }
+  __syncthreads();
+  if (s_row0 < 0) return;  // past the last tile
+  const int r = threadIdx.x & 127;
+  const int row = s_row0 + r;
+  const int src = (row < s_end && row < idx_rows) ? __ldg(idx + row) : -1;
+  const bool ok = src >= 0 && src < src_rows;
+  uint8_t* dst = blocks + tile * kst * 512ll + (r & 31) * 16 + (r >> 5) * 4;
+  const uint32_t* srow = reinterpret_cast<const uint32_t*>(sf + static_cast<long long>(ok ? src : 0) * sf_ld);
+  for (int k = threadIdx.x >> 7; k < kst; k += 2)
+    *reinterpret_cast<uint32_t*>(dst + k * 512ll) = ok ? __ldg(srow + k) : 0u;
+}
+
+cudaError_t launch_mx_tile_scales(const uint8_t* sf, int sf_ld, int src_rows, const int32_t* idx, int idx_rows,
+                                  const int32_t* off, int G, int kst, long long tiles_cap, uint8_t* blocks,
+                                  cudaStream_t s) {
+  if (tiles_cap <= 0 || G <= 0) return cudaSuccess;
+  mx_tile_scales_kernel<<<static_cast<unsigned>(tiles_cap), 256, 0, s>>>(sf, sf_ld, src_rows, idx, idx_rows, off, G,
+                                                                         kst, blocks);
+  return cudaGetLastError();
+}
+
 // Gate/up + SwiGLU on block-scaled operands: gathered X codes (scales gathered 4 bytes per row and stage), the
 // W_gate / W_up pair, 96 + 96 output columns per tile (two 192-column accumulators and four stages of scales
 // fill 432 of the 512 TMEM columns); the epilogue writes H, U (fp32, when cached) and A as block-scaled codes

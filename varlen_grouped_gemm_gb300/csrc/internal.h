@@ -46,6 +46,11 @@ cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, in
 cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rows_mx(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                     uint8_t* q, uint8_t* sf, int sf_ld, cudaStream_t s);
+// Scale blocks of a gathered operand per row tile of the varlen-M GEMMs over `off` (tiles in group order, at most
+// tiles_cap of them) and stage of K, from row-major [src_rows][sf_ld] scales and the gather index idx[idx_rows].
+cudaError_t launch_mx_tile_scales(const uint8_t* sf, int sf_ld, int src_rows, const int32_t* idx, int idx_rows,
+                                  const int32_t* off, int G, int kst, long long tiles_cap, uint8_t* blocks,
+                                  cudaStream_t s);
 cudaError_t launch_quantize_weight_mx(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, uint8_t* blocks,
                                       int rpt, int roff, int ntile, int kst, int nblk, cudaStream_t s);
 cudaError_t run_down_scale_dual(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
