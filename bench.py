@@ -89,6 +89,14 @@ def kernel_work(wl, P, dW_bytes=2):
                               T * d + T * d // 32 + 2 * E * n * d + 2 * E * n * d // 32 + 8 * P * n + P * n
                               + P * n // 32),
         "down_scale_mx": same(2 * P * d * n, P * n + P * n // 32 + E * d * n + E * d * n // 32 + 2 * P * d),
+        # the block-scaled backward: dO per token (gathered codes, counted once per token), W_down^T, H and U,
+        # dH, dU, A' (bf16) and the [dH | dU] codes; the dX GEMM on those codes
+        "dact_dswiglu_mx": (2 * P * d * n, T * d + T * d // 32 + E * d * n + E * d * n // 32 + 10 * P * n
+                            + 2 * P * n + 2 * P * n // 32,
+                            P * d + P * d // 32 + E * d * n + E * d * n // 32 + 8 * P * n + 12 * P * n
+                            + 2 * P * n + 2 * P * n // 32),
+        "dx_gemm_mx": same(4 * P * d * n, 2 * P * n + 2 * P * n // 32 + 2 * E * d * n + 2 * E * d * n // 32
+                           + 2 * P * d),
         "down_scale": same(2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
         "down_scale_e4m3": same(2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
         "quantize_a_e4m3": same(0, 3 * P * n + 4 * P),
@@ -205,7 +213,8 @@ _GEMM_LABELS = {
     (0, 0, 0, 7): "dact_dswiglu_e4m3",
 }
 # the block-scaled form (template flag X_MX = 8)
-_MX_GEMM_LABELS = {(1, 1, 0, 1): "gate_up_swiglu_mx", (0, 0, 0, 2): "down_scale_mx"}
+_MX_GEMM_LABELS = {(1, 1, 0, 1): "gate_up_swiglu_mx", (0, 0, 0, 2): "down_scale_mx", (0, 0, 0, 3): "dact_dswiglu_mx",
+                   (0, 0, 0, 0): "dx_gemm_mx"}
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
     "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "transpose_f32_kernel": "permute",
@@ -482,9 +491,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                               e4m3=True)
     w8 = vgg.E4m3Weights.quantize(ctx, W_gate, W_up)
     w8d = vgg.E4m3Weights.quantize(ctx, W_gate, W_up, W_down, backward=True)
-    bmx = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=False, device=X.device,
-                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, mx=True)
-    wmx = vgg.MxWeights.quantize(ctx, W_gate, W_up, W_down)
+    bmx = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
+                               device=X.device, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy,
+                               mx=True)
+    wmx = vgg.MxWeights.quantize(ctx, W_gate, W_up, W_down, backward=True)
+
+    def mx_step():
+        vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx)
+        vgg.backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx, bmx)
 
     def e4m3_step():
         vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
@@ -501,6 +515,7 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             # the block-scaled (1 x 32) form of both forward GEMMs, A quantized in the gate/up epilogue
             "mx": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx),
             "mx_infer": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx, cache=False),
+            "mx_step": mx_step,
             # training steps
             "bf16_step": lambda: vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf),
             "e4m3_step": e4m3_step}
@@ -544,6 +559,7 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
     fl_dn = 2 * P * wl.d * wl.n
     step_fl = wl.flops_fwd_bwd(P)
     gmx, dmx = per("mx", "gate_up_swiglu_mx"), per("mx", "down_scale_mx")
+    amx, xmx = per("mx_step", "dact_dswiglu_mx"), per("mx_step", "dx_gemm_mx")
     qmx = out["mx"][1].get("quantize_mx", (0.0, 1))
     del b8, w8, w8d, bmx, wmx
     return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
@@ -565,9 +581,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                 "gate_up_ms": gmx, "down_ms": dmx, "quantize_x_ms": qmx[0] / max(qmx[1], 1),
                 "gate_up_tflops": fl / (gmx * 1e-3) / 1e12, "down_tflops": fl_dn / (dmx * 1e-3) / 1e12,
                 "gate_up_frac": fl / (gmx * 1e-3) / 1e12 / peak8,
+                "train_step_ms": out["mx_step"][0],
+                "train_step_tflops": step_fl / (out["mx_step"][0] * 1e-3) / 1e12,
+                "dact_ms": amx, "dx_ms": xmx, "dact_tflops": fl_dn / (amx * 1e-3) / 1e12,
+                "dx_tflops": fl / (xmx * 1e-3) / 1e12,
                 "recipe": "e4m3 codes with one power-of-two (UE8M0) scale per 32 values along the reduction "
                           "dimension of every operand row (kind::mxf8f6f4 UMMA); A quantized in the gate/up "
-                          "epilogue; 128-column tiles"},
+                          "epilogue, [dH|dU] in the dSwiGLU epilogue; 192-column tiles; the training step's "
+                          "weight gradients and router stay bf16"},
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
             "recipe": "e4m3 operands with one fp32 scale per row: X per token, A, dO and [dH|dU] per pair, weights per "
                       "output channel of each GEMM; fp32 accumulation; dW and the router stay bf16",

@@ -301,7 +301,8 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
  */
 /* Bytes per row of a row-major scale array for `cols` columns: 4 * ceil(cols / 128). */
 long long moe_mx_sf_cols(int cols);
-/* Bytes of the weight scale blocks: which = 0 the W_gate / W_up pair, 1 W_down; 0 on bad arguments. */
+/* Bytes of the weight scale blocks: which = 0 the W_gate / W_up pair, 1 W_down (the forward); 2 W_down^T,
+ * 3 [W_gate; W_up]^T (the backward's dSwiGLU and dX GEMMs, moe_quantize_bwd_weights_mx); 0 on bad arguments. */
 long long moe_mx_weight_sf_bytes(int E, int d, int n, int which);
 /* Bytes of the activation scale blocks for a pair capacity cap: (ceil(cap/128) + E) * ceil(n/128) * 512. */
 long long moe_mx_act_sf_bytes(long long cap, int E, int n);
@@ -350,6 +351,46 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
                             const void* gu_sf, const void* Wd_q, const void* dn_sf, int T, int d, int E, int n,
                             long long cap, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
                             void* H, void* U, void* x_sf_tiles, void* Aq, void* a_sf, void* Yw, moe_stream_t stream);
+
+/*
+ * moe_quantize_bwd_weights_mx — the block-scaled B operands of the backward's activation-gradient GEMMs, once per
+ * weight update: W_down^T (per expert [n, d], blocks along d) into codes Wdt_q [E,n,d] and scale blocks wdt_sf
+ * (moe_mx_weight_sf_bytes(E,d,n,2) bytes, [E][ceil(n/192)][ceil(d/128)] pairs of blocks over W_down^T's rows);
+ * [W_gate; W_up]^T (per expert [d, 2n], W_gate's rows in columns 0..n-1, W_up's in n..2n-1, blocks along 2n)
+ * into Wgu_q [E,d,2n] and wgu_sf (moe_mx_weight_sf_bytes(E,d,n,3) bytes, [E][ceil(d/192)][ceil(2n/128)] pairs).
+ * tmp: device scratch of E*d*2n bf16 (caller-owned, overwritten).  [SM] "3 기여 ①" (dA' = dO W_down),
+ * "4 기여 ②" (the dX GEMM); [GG] "한계".  16-byte aligned buffers, d and n multiples of 64, else
+ * MOE_ERR_INVALID_ARG.
+ */
+int moe_quantize_bwd_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, const void* W_down, int E, int d,
+                                int n, void* tmp, void* Wdt_q, void* wdt_sf, void* Wgu_q, void* wgu_sf,
+                                moe_stream_t stream);
+
+/*
+ * moe_backward_mx — moe_backward with the dSwiGLU GEMM and the dX GEMM on block-scaled e4m3 operands, each
+ * activation quantized where it is produced.  dO is quantized per token in 1 x 32 blocks (inside the call, in
+ * the workspace), its code rows are copied to the sorted positions dOq [cap,d] (caller-owned) and their scales
+ * laid out per sorted row tile into do_sf_tiles (moe_mx_act_sf_bytes(cap,E,d) bytes, caller-owned scratch);
+ * with dq(.) the block-scaled value, for sorted pair j of expert e:
+ *
+ *   dA'[j,c] = sum_i dq(dOq[j,i]) dq(Wdt_q[e,c,i])      (the dSwiGLU epilogue as moe_backward on this dA')
+ *   the epilogue also writes [dH | dU][j] quantized from its fp32 values into HUq [cap,2n] and the scale
+ *   blocks hu_sf (moe_mx_act_sf_bytes(cap,E,2n) bytes), both caller-owned;
+ *   dXp[j,c]  = sum_k dq(HUq[j,k]) dq(Wgu_q[e,c,k])
+ *
+ * Wdt_q, wdt_sf, Wgu_q, wgu_sf from moe_quantize_bwd_weights_mx.  The router gradient, dX's reduction and the
+ * weight gradients are those of moe_backward.  Arguments, shape rules, workspace and ownership otherwise as
+ * moe_backward; MOE_ERR_UNSUPPORTED when the pair capacity is too small to stage dO's per-token codes in the
+ * workspace (cap * 2d bytes must hold T * (d + 4 ceil(d/128)) plus alignment).
+ */
+int moe_backward_mx(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate, const void* W_up,
+                    const void* W_down, const void* Wdt_q, const void* wdt_sf, const void* Wgu_q, const void* wgu_sf,
+                    int T, int d, int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids,
+                    const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                    const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* dOq,
+                    void* do_sf_tiles, void* HUq, void* hu_sf, void* dX, void* dW_gate, void* dW_up, void* dW_down,
+                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
 
 /*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.

@@ -207,3 +207,111 @@ def test_mx_forward_only(ctx):
     vgg.forward_mx(ctx, dv["X"], dv["W_r"], dv["bias"], wmx, buf, cache=False)
     assert torch.equal(buf.O, O_cached)
     assert torch.all(buf.H == 7.0).item() and torch.all(buf.U == 7.0).item()
+
+
+BWD_CASES = [
+    synth.scaled(synth.WORKLOADS["c2"], name="c2_small", T=512, d=256, E=16, n=192, K=4),
+    # n = 320: a partial 192-column tile; d = 320: the dSwiGLU GEMM ends on a half stage; empty experts
+    synth.scaled(synth.WORKLOADS["c4"], name="c4_small_320", T=640, d=320, E=32, n=320, K=4),
+    synth.scaled(synth.WORKLOADS["c5"], name="c5_small_tr", T=2048, d=256, E=32, n=128, K=8, m_tile=64),
+    synth.scaled(synth.WORKLOADS["c2_cap"], name="cap_f1_bias", T=512, d=256, E=16, n=192, K=4, bias="normal"),
+]
+
+
+def _act_exps(sf: torch.Tensor, offsets: np.ndarray, cols: int, rows: np.ndarray) -> np.ndarray:
+    return _unpack_act_blocks(sf.cpu().numpy(), offsets, cols, rows)
+
+
+@pytest.mark.parametrize("wl", BWD_CASES, ids=lambda w: w.name)
+def test_mx_backward_matches_oracle(ctx, wl):
+    """moe_backward_mx against the oracle's backward with both activation-gradient GEMMs block-scaled:
+    * the weight codes and scale blocks (W_down^T and [W_gate; W_up]^T) bit for bit, padding included;
+    * the sorted dO codes and their scale blocks bit for bit (decided on the exact bf16 dO);
+    * the [dH | dU] codes, which the dSwiGLU epilogue quantizes from its fp32 values, against the oracle's
+      quantization of its exact values: equal but for values within fp32 rounding of a boundary (one code step,
+      a few per hundred thousand; a block whose scale differs is left out);
+    * every gradient (dX, dW_gate, dW_up, dW_down, dS, dlogits, dW_r) within the usual tolerance of the oracle's
+      block-scaled backward, both floors."""
+    import varlen_grouped_gemm_gb300 as vgg
+    from _helpers import compare_layer
+    inp = Inputs(wl)
+    dv = inp.dev
+    E, n, d = wl.E, wl.n, wl.d
+    buf = vgg.Buffers.allocate(wl.T, d, E, n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.float32,
+                               capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, mx=True)
+    buf.mhusf.fill_(255)
+    buf.mdosft.fill_(255)
+    wmx = vgg.MxWeights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"], backward=True)
+    vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
+    vgg.backward_mx(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], wmx, buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+
+    Wg, Wu, Wd = (mo.bf16_bits_to_f64(a) for a in (inp.W_gate, inp.W_up, inp.W_down))
+    Wdt = Wd.transpose(0, 2, 1)  # [E, n, d]
+    Wgu = np.concatenate([Wg, Wu], axis=1).transpose(0, 2, 1)  # [E, d, 2n]
+    for got_q, got_sf, W, R, C in ((wmx.Wdt_q, wmx.wdt_sf, Wdt, n, d), (wmx.Wgu_q, wmx.wgu_sf, Wgu, d, 2 * n)):
+        q, e = oracle.quantize_blocks_mx(W.reshape(E * R, C))
+        np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * R, C), q)
+        sf = got_sf.cpu().numpy()
+        want = np.full_like(sf, 127)
+        want[_weight_index(E, R, C, TILE, 0)] = e.reshape(E, R, -1) + 127
+        np.testing.assert_array_equal(sf, want)
+
+    g = gpu_routing(buf)
+    C = buf.capacity
+    O_ref, cache = mo.moe_forward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, wl.K, wl.m_tile,
+                                  logits_for_routing=g["logits"], scores_for_routing=g["scores"], capacity=C,
+                                  policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None)
+    grads = mo.moe_backward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, inp.dO, cache,
+                            mx_dx=True, mx_dact=True)
+    r = cache["routing"]
+    if C:
+        rows = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(E)]).astype(np.int64)
+        offs = np.arange(E + 1) * C
+    else:
+        check_routing_bit_exact(g, wl.K, wl.m_tile)
+        rows = np.arange(r.P)
+        offs = r.offsets
+    # dO's codes at the sorted positions and their scale blocks per row tile, bit for bit
+    oq, oe = oracle.quantize_blocks_mx(inp.dO[r.sorted_tok])
+    np.testing.assert_array_equal(buf.mdoq.cpu().numpy()[rows], oq)
+    np.testing.assert_array_equal(_act_exps(buf.mdosft, offs, d, rows), oe)
+    # [dH | dU] codes against the oracle's quantization of its exact values
+    X64, dO64 = mo.bf16_bits_to_f64(inp.X), mo.bf16_bits_to_f64(inp.dO)
+    hu_ref = np.zeros((r.P, 2 * n))
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        if hi == lo:
+            continue
+        toks = r.sorted_tok[lo:hi]
+        q1, e1 = oracle.quantize_blocks_mx(dO64[toks])
+        q2, e2 = oracle.quantize_blocks_mx(Wdt[e])
+        dap = oracle.dequantize_blocks_mx(q1, e1) @ oracle.dequantize_blocks_mx(q2, e2).T
+        blk = mo.expert_block_backward(X64[toks], dO64[toks], cache["w_full"][toks, e], inp.W_gate[e], inp.W_up[e],
+                                       inp.W_down[e], dap=dap)
+        hu_ref[lo:hi] = np.concatenate([blk["dh"], blk["du"]], axis=1)
+    hq_ref, he_ref = oracle.quantize_blocks_mx(hu_ref)
+    hq = buf.mhuq.cpu().numpy()[rows]
+    he = _act_exps(buf.mhusf, offs, 2 * n, rows)
+    diff_e = he != he_ref
+    assert diff_e.sum() <= max(2, diff_e.size // 10000), ("[dH|dU] block scales", int(diff_e.sum()), diff_e.size)
+    same = np.repeat(~diff_e, 32, axis=1)
+    dq = np.abs(mo.e4m3_decode(hq) - mo.e4m3_decode(hq_ref))
+    step = np.maximum(np.abs(mo.e4m3_decode(hq_ref)) * 2.0 ** -3, 2.0 ** -9)
+    bad = same & (dq > 0)
+    assert bad.sum() <= max(4, hq.size // 20000), ("[dH|dU] codes", int(bad.sum()), hq.size)
+    assert np.all(dq[bad] <= step[bad] * (1 + 1e-12))
+    if C:
+        rep = {"O": oracle.compare("O", dev_to_f64(buf.O), O_ref),
+               "dX": oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])}
+        for name in ("dW_gate", "dW_up", "dW_down"):
+            rep[name] = oracle.compare(name, dev_to_f64(getattr(buf, name)), np.stack([grads[name][e] for e in range(E)]),
+                                       param_axes=oracle.WEIGHT_GRAD)
+        rep["dS"] = oracle.compare("dS", dev_to_f64(buf.dS)[rows], grads["dw"][r.sorted_tok, r.sorted_exp])
+        rep["dlogits"] = oracle.compare("dlogits", dev_to_f64(buf.dlogits), grads["dlogits"])
+        rep["dW_r"] = oracle.compare("dW_r", dev_to_f64(buf.dW_r), grads["dW_r"])
+    else:
+        rep = compare_layer(buf, inp, O_ref, cache, grads)
+    print(wl.name, "[dH|dU] codes differing:", int(bad.sum()), "of", hq.size,
+          {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})

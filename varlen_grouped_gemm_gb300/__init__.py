@@ -31,7 +31,7 @@ EXPORTS = (
     "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
     "moe_expert_capacity", "moe_test_gemm_varlen_k_dual", "moe_test_gemm_varlen_m_dual",
     "moe_mx_sf_cols", "moe_mx_weight_sf_bytes", "moe_mx_act_sf_bytes", "moe_quantize_rows_mx",
-    "moe_quantize_weights_mx", "moe_grouped_gemm_fwd_mx",
+    "moe_quantize_weights_mx", "moe_grouped_gemm_fwd_mx", "moe_quantize_bwd_weights_mx", "moe_backward_mx",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -100,6 +100,10 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
         L.moe_grouped_gemm_fwd_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P,
                                               _P, _P, _P, _P, _P, _P]
+        L.moe_quantize_bwd_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+        L.moe_backward_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL, _P, _P,
+                                      _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                                      _SZ, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -516,6 +520,10 @@ class Buffers:
     maq: torch.Tensor | None = None  # block-scaled down projection: A's codes [cap, n] and scale blocks
     masf: torch.Tensor | None = None
     mxsft: torch.Tensor | None = None  # block-scaled gate/up: the gathered X rows' scales per sorted row tile
+    mdoq: torch.Tensor | None = None  # block-scaled backward: sorted dO codes [cap, d], their scales per row tile,
+    mdosft: torch.Tensor | None = None  # [dH | dU] codes [cap, 2n] and their scale blocks
+    mhuq: torch.Tensor | None = None
+    mhusf: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
@@ -560,7 +568,11 @@ class Buffers:
             mxq=z((T, d), torch.uint8) if mx else None, mxsf=z((T, mx_sf_cols(d)), torch.uint8) if mx else None,
             maq=z((cap, n), torch.uint8) if mx else None,
             masf=z((mx_act_sf_bytes(cap, E, n),), torch.uint8) if mx else None,
-            mxsft=z((mx_act_sf_bytes(cap, E, d),), torch.uint8) if mx else None)
+            mxsft=z((mx_act_sf_bytes(cap, E, d),), torch.uint8) if mx else None,
+            mdoq=z((cap, d), torch.uint8) if (mx and backward) else None,
+            mdosft=z((mx_act_sf_bytes(cap, E, d),), torch.uint8) if (mx and backward) else None,
+            mhuq=z((cap, 2 * n), torch.uint8) if (mx and backward) else None,
+            mhusf=z((mx_act_sf_bytes(cap, E, 2 * n),), torch.uint8) if (mx and backward) else None)
 
 
 def forward(ctx, X, W_r, bias, W_gate, W_up, W_down, buf: Buffers, stream=None, cache=True):
@@ -589,9 +601,14 @@ class MxWeights:
     gu_sf: torch.Tensor
     Wd_q: torch.Tensor
     dn_sf: torch.Tensor
+    Wdt_q: torch.Tensor | None = None  # the backward: W_down^T codes [E, n, d] and scale blocks
+    wdt_sf: torch.Tensor | None = None
+    Wgu_q: torch.Tensor | None = None  # [W_gate; W_up]^T codes [E, d, 2n] and scale blocks
+    wgu_sf: torch.Tensor | None = None
 
     @staticmethod
-    def quantize(ctx, W_gate, W_up, W_down, stream=None) -> "MxWeights":
+    def quantize(ctx, W_gate, W_up, W_down, stream=None, backward=False) -> "MxWeights":
+        """The forward's codes and scale blocks; with ``backward`` also the two backward operands."""
         E, n, d = W_gate.shape
         dev = W_gate.device
         u8 = torch.uint8
@@ -600,6 +617,18 @@ class MxWeights:
                       torch.empty((E, d, n), dtype=u8, device=dev),
                       torch.empty(mx_weight_sf_bytes(E, d, n, 1), dtype=u8, device=dev))
         moe_quantize_weights_mx(ctx, W_gate, W_up, W_down, w.Wg_q, w.Wu_q, w.gu_sf, w.Wd_q, w.dn_sf, stream)
+        if backward:
+            w.Wdt_q = torch.empty((E, n, d), dtype=u8, device=dev)
+            w.wdt_sf = torch.empty(mx_weight_sf_bytes(E, d, n, 2), dtype=u8, device=dev)
+            w.Wgu_q = torch.empty((E, d, 2 * n), dtype=u8, device=dev)
+            w.wgu_sf = torch.empty(mx_weight_sf_bytes(E, d, n, 3), dtype=u8, device=dev)
+            tmp = torch.empty((E, d, 2 * n), dtype=torch.bfloat16, device=dev)
+            _check("moe_quantize_bwd_weights_mx", lib().moe_quantize_bwd_weights_mx(
+                ctx.handle, _ptr(W_gate, torch.bfloat16), _ptr(W_up, torch.bfloat16), _ptr(W_down, torch.bfloat16),
+                E, d, n, _ptr(tmp), _ptr(w.Wdt_q, u8), _ptr(w.wdt_sf, u8), _ptr(w.Wgu_q, u8), _ptr(w.wgu_sf, u8),
+                _stream(stream)))
+            torch.cuda.synchronize(dev)  # the scratch copy may go once the call has run
+            del tmp
         return w
 
 
@@ -693,6 +722,27 @@ def forward_mx(ctx, X, W_r, bias, wmx: MxWeights, buf: Buffers, stream=None, cac
                             buf.H if cache else None, buf.U if cache else None, buf.mxsft, buf.maq, buf.masf, buf.Yw,
                             stream)
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
+
+
+def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buffers, stream=None):
+    """The backward with the dSwiGLU and dX GEMMs on block-scaled operands (``wmx`` quantized with
+    ``backward=True``, ``buf`` allocated with ``mx=True``); the weight gradients stay bf16."""
+    if wmx.Wdt_q is None or buf.mhuq is None:
+        raise ValueError("block-scaled backward needs MxWeights.quantize(..., backward=True) and Buffers(mx=True)")
+    T, d = X.shape
+    E, n, _ = W_gate.shape
+    cap = buf.sorted_tok.numel()
+    wp, wb = _ws(buf.ws)
+    bf, u8, f32, i32 = torch.bfloat16, torch.uint8, torch.float32, torch.int32
+    dw_fp32 = 1 if buf.dW_gate.dtype == f32 else 0
+    _check("moe_backward_mx", lib().moe_backward_mx(
+        ctx.handle, _ptr(dO, bf), _ptr(X, bf), _ptr(W_r, bf), _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf),
+        _ptr(wmx.Wdt_q, u8), _ptr(wmx.wdt_sf, u8), _ptr(wmx.Wgu_q, u8), _ptr(wmx.wgu_sf, u8), T, d, E, n, buf.K,
+        buf.m_tile, cap, _ptr(buf.topk_ids, i32), _ptr(buf.topk_w, f32), _ptr(buf.offsets, i32),
+        _ptr(buf.sorted_tok, i32), _ptr(buf.sorted_w, f32), _ptr(buf.tok_ptr, i32), _ptr(buf.tok_pairs, i32),
+        _ptr(buf.H, f32), _ptr(buf.U, f32), _ptr(buf.mdoq, u8), _ptr(buf.mdosft, u8), _ptr(buf.mhuq, u8),
+        _ptr(buf.mhusf, u8), _ptr(buf.dX, bf), _ptr(buf.dW_gate), _ptr(buf.dW_up), _ptr(buf.dW_down), dw_fp32,
+        _ptr(buf.dS, f32), _ptr(buf.dlogits, f32), _ptr(buf.dW_r, f32), wp, wb, _stream(stream)))
 
 
 def backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8: E4m3Weights, buf: Buffers, stream=None, dx=True,

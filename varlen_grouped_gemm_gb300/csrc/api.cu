@@ -752,6 +752,8 @@ long long moe_mx_weight_sf_bytes(int E, int d, int n, int which) {
   const long long grp = 512ll * mx_b_blocks(kMxBN);
   if (which == 0) return grp * E * ceil_div(n, kMxBN / 2) * ceil_div(d, 128);
   if (which == 1) return grp * E * ceil_div(d, kMxBN) * ceil_div(n, 128);
+  if (which == 2) return grp * E * ceil_div(n, kMxBN) * ceil_div(d, 128);      // W_down^T [E][n][d]
+  if (which == 3) return grp * E * ceil_div(d, kMxBN) * ceil_div(2 * n, 128);  // [W_gate; W_up]^T [E][d][2n]
   return 0;
 }
 
@@ -888,7 +890,21 @@ int moe_combine(moe_ctx* ctx, const void* Yw, const int32_t* tok_ptr, const int3
   return MOE_OK;
 }
 
-// The backward; with Wgu_q the dX GEMM runs on e4m3 operands (moe_backward_e4m3).
+// Block-scaled dSwiGLU and dX GEMMs of the backward (moe_backward_mx): weight codes and scale blocks, the sorted dO
+// code rows, dO's scale blocks per sorted row tile, and the [dH | dU] codes and scale blocks.
+struct MxBwd {
+  const void* Wdt_q;
+  const void* wdt_sf;
+  const void* Wgu_q;
+  const void* wgu_sf;
+  void* dOq;
+  void* do_sf_tiles;
+  void* HUq;
+  void* hu_sf;
+};
+
+// The backward; with Wgu_q the dX GEMM runs on e4m3 operands (moe_backward_e4m3), with mx both activation-gradient
+// GEMMs on block-scaled operands (moe_backward_mx).
 static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
                          const void* W_up, const void* W_down, int T, int d, int E, int n, int K, int m_tile,
                          long long cap, const int32_t* topk_ids, const float* topk_w, const int32_t* offsets,
@@ -896,7 +912,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
                          const int32_t* tok_pairs, const void* H, const void* U, void* dX, void* dW_gate,
                          void* dW_up, void* dW_down, int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws,
                          size_t ws_bytes, moe_stream_t stream, const void* Wgu_q, const float* wgu_scale, void* HUq,
-                         float* hu_scale, const void* Wdt_q, const float* wdt_scale, void* dOq, float* do_scale) {
+                         float* hu_scale, const void* Wdt_q, const float* wdt_scale, void* dOq, float* do_scale,
+                         const MxBwd* mx = nullptr) {
   VGG_REQUIRE(ctx && dO && X && W_r && W_gate && W_up && W_down && topk_ids && topk_w && offsets && sorted_tok &&
               sorted_w && tok_ptr && tok_pairs && H && U && dX && dW_gate && dW_up && dW_down && dS && dlogits &&
               dW_r && ws);
@@ -915,7 +932,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   BwdWs w = carve_bwd(ws, T, d, E, n, cap);
   const bool f32 = dW_fp32 != 0;
   const int bn6 = dact_bn(n, cap, E, ctx->num_sms);
-  const int part_ld = ceil_div(n, bn6) * 2;  // one dS partial per (column tile, epilogue column half)
+  // one dS partial per (column tile, epilogue column half); the block-scaled form tiles n by kMxBN
+  const int part_ld = (mx ? ceil_div(n, kMxBN) : ceil_div(n, bn6)) * 2;
   if (cap > static_cast<long long>(T) * K) {
     __nv_bfloat16* const tail[6] = {w.dH, w.dU, w.Ap, w.dH_lo, w.dU_lo, w.Ap_lo};
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, tail, s));
@@ -931,21 +949,72 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   if (dact_tok)
     VGG_LAUNCH("quantize_do_e4m3", launch_quantize_rows_e4m3(static_cast<const __nv_bfloat16*>(dO), T, nullptr, d, tq,
                                                             ts, s));
+  // block-scaled form: dO in 1 x 32 blocks per token (codes and row-major scales) into the same region; the gather
+  // below copies the code rows to the sorted positions and mx_tile_scales lays the scales out per sorted row tile
+  const int mx_sfc = static_cast<int>(moe_mx_sf_cols(d));
+  uint8_t* mq = reinterpret_cast<uint8_t*>(w.dXp);
+  uint8_t* msf = mq + tok_codes;
+  if (mx) {
+    if (tok_codes + static_cast<size_t>(T) * mx_sfc > sizeof(__nv_bfloat16) * cap * d) return MOE_ERR_UNSUPPORTED;
+    VGG_LAUNCH("quantize_mx", launch_quantize_rows_mx(static_cast<const __nv_bfloat16*>(dO), T, nullptr, d, mq, msf,
+                                                      mx_sfc, s));
+  }
   // expert-sorted copies of X and dO (and of dO's codes): every backward GEMM then reads whole TMA boxes.  The
   // bf16 copies are padded per expert to multiples of 16 rows (zero rows), except when the e4m3 dSwiGLU GEMM
   // quantizes the sorted dO rows themselves (a capacity layout with fewer slots than tokens).
-  const bool padded = !(Wdt_q && !dact_tok);
+  const bool padded = mx || !(Wdt_q && !dact_tok);
   const long long cap_pad = padded ? padded_rows(cap, E) : cap;
   const int32_t* poff = padded ? w.poff : nullptr;
   if (padded) VGG_LAUNCH("pad_offsets", launch_pad_offsets(offsets, E, w.poff, ctx->d_err, s));
   VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, poff, cap_pad, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
                                                static_cast<const __nv_bfloat16*>(X),
                                                static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs,
-                                               dact_tok ? tq : nullptr, dact_tok ? ts : nullptr,
-                                               static_cast<uint8_t*>(dOq), do_scale, ctx->d_err, ctx->num_sms,
-                                               ctx->timeout_ns, s));
+                                               mx ? mq : (dact_tok ? tq : nullptr), dact_tok ? ts : nullptr,
+                                               static_cast<uint8_t*>(mx ? mx->dOq : dOq), mx ? nullptr : do_scale,
+                                               ctx->d_err, ctx->num_sms, ctx->timeout_ns, s));
   // dA' = dO[tok] W_down[e]; epilogue: dS partials, dH, dU, A' = w A
-  if (Wdt_q) {
+  if (mx) {
+    // block-scaled: A = the sorted dO code rows, its scale blocks per sorted row tile; B = W_down^T codes; the
+    // epilogue also writes [dH | dU] block-scaled for the dX GEMM
+    VGG_LAUNCH("mx_tile_scales", launch_mx_tile_scales(msf, mx_sfc, T, sorted_tok, static_cast<int>(cap), offsets, E,
+                                                       ceil_div(d, 128), ceil_div(cap, BM) + E,
+                                                       static_cast<uint8_t*>(mx->do_sf_tiles), s));
+    GemmParams p = base_params(ctx);
+    p.N = n;
+    p.K = d / 2;
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.in0 = static_cast<const float*>(H);
+    p.in1 = static_cast<const float*>(U);
+    p.ld_in = n;
+    p.out0 = w.dH;
+    p.out1 = w.dU;
+    p.out2 = w.Ap;
+    p.out3 = w.dH_lo;
+    p.out4 = w.dU_lo;
+    p.out5 = w.Ap_lo;
+    p.ld_out = n;
+    p.row_scale = sorted_w;
+    p.part = w.part;
+    p.part_ld = part_ld;
+    p.a_sf = static_cast<const uint8_t*>(mx->do_sf_tiles);
+    p.b_sf = static_cast<const uint8_t*>(mx->wdt_sf);
+    p.sf_kst = ceil_div(d, 128);
+    p.o_q = static_cast<uint8_t*>(mx->HUq);
+    p.o_q_ld = 2ll * n;
+    p.o_sf = static_cast<uint8_t*>(mx->hu_sf);
+    p.o_sf_kst = ceil_div(2 * n, 128);
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, mx->dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, mx->Wdt_q, d / 2, n, E, kMxBN) ||
+        !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, kMxBN);
+    VGG_LAUNCH("dact_dswiglu_mx", run_dact_dswiglu_mx(p, m, std::min(tiles, ctx->num_sms), s));
+  } else if (Wdt_q) {
     // e4m3: the sorted dO code rows (gathered above, else the sorted rows below offsets[E] quantized here),
     // B = W_down^T quantized per row by moe_quantize_dact_weights_e4m3; rows handed to TMA as 16-bit units
     if (!dact_tok)
@@ -1014,7 +1083,28 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     VGG_LAUNCH("dact_dswiglu", run_dact_dswiglu(bn6, sh.pair, p, m, sh.grid, s));
   }
   // dXp = [dH | dU] [W_gate[e]; W_up[e]]
-  if (Wgu_q) {
+  if (mx) {
+    // block-scaled: A = [dH | dU] codes from the dSwiGLU epilogue with their scale blocks, B = [W_gate; W_up]^T
+    GemmParams p = base_params(ctx);
+    p.N = d;
+    p.K = n;  // 2n codes
+    p.groups = E;
+    p.offsets = offsets;
+    p.rows_cap = static_cast<int>(cap);
+    p.out0 = w.dXp;
+    p.ld_out = d;
+    p.a_sf = static_cast<const uint8_t*>(mx->hu_sf);
+    p.b_sf = static_cast<const uint8_t*>(mx->wgu_sf);
+    p.sf_kst = ceil_div(2 * n, 128);
+    Maps m = zero_maps();
+    if (!make_map_2d(&m.a0, mx->HUq, n, cap, n, BM) || !make_map_3d(&m.b0, mx->Wgu_q, n, d, E, kMxBN) ||
+        !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
+      return MOE_ERR_CUDA;
+    m.a1 = m.a0;
+    m.b1 = m.b0;
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, kMxBN);
+    VGG_LAUNCH("dx_gemm_mx", run_dx_store_mx(p, m, std::min(tiles, ctx->num_sms), s));
+  } else if (Wgu_q) {
     // e4m3: each pair's row [dH | dU] quantized (the rows below offsets[E]), B = [W_gate; W_up]^T quantized per
     // row by moe_quantize_dx_weights_e4m3; rows are handed to TMA as 16-bit units (code pairs)
     VGG_LAUNCH("quantize_hu_e4m3", launch_quantize_rows_pair_e4m3(w.dH, w.dU, cap, offsets + E, n,
@@ -1198,6 +1288,55 @@ int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W
                        sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
                        dlogits, dW_r, ws, ws_bytes, stream, Wgu_q, wgu_scale, HUq, hu_scale, Wdt_q, wdt_scale, dOq,
                        do_scale);
+}
+
+int moe_backward_mx(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate, const void* W_up,
+                    const void* W_down, const void* Wdt_q, const void* wdt_sf, const void* Wgu_q, const void* wgu_sf,
+                    int T, int d, int E, int n, int K, int m_tile, long long cap, const int32_t* topk_ids,
+                    const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
+                    const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* dOq,
+                    void* do_sf_tiles, void* HUq, void* hu_sf, void* dX, void* dW_gate, void* dW_up, void* dW_down,
+                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
+                    moe_stream_t stream) {
+  VGG_REQUIRE(Wdt_q && wdt_sf && Wgu_q && wgu_sf && dOq && do_sf_tiles && HUq && hu_sf);
+  VGG_REQUIRE(aligned16(Wdt_q) && aligned16(wdt_sf) && aligned16(Wgu_q) && aligned16(wgu_sf) && aligned16(dOq) &&
+              aligned16(do_sf_tiles) && aligned16(HUq) && aligned16(hu_sf));
+  const MxBwd mx{Wdt_q, wdt_sf, Wgu_q, wgu_sf, dOq, do_sf_tiles, HUq, hu_sf};
+  return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
+                       sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
+                       dlogits, dW_r, ws, ws_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, &mx);
+}
+
+int moe_quantize_bwd_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, const void* W_down, int E, int d,
+                                int n, void* tmp, void* Wdt_q, void* wdt_sf, void* Wgu_q, void* wgu_sf,
+                                moe_stream_t stream) {
+  VGG_REQUIRE(ctx && W_gate && W_up && W_down && tmp && Wdt_q && wdt_sf && Wgu_q && wgu_sf);
+  VGG_REQUIRE(E >= 1 && E <= kMaxGroups && d >= 64 && d % 64 == 0 && n >= 64 && n % 64 == 0);
+  VGG_REQUIRE(aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(tmp) && aligned16(Wdt_q) &&
+              aligned16(wdt_sf) && aligned16(Wgu_q) && aligned16(wgu_sf));
+  DeviceGuard g(ctx->device);
+  VGG_REQUIRE(g.ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16* t = static_cast<__nv_bfloat16*>(tmp);
+  const int nb = mx_b_blocks(kMxBN);
+  VGG_CUDA(cudaMemsetAsync(wdt_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 2)), s));
+  VGG_CUDA(cudaMemsetAsync(wgu_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 3)), s));
+  // W_down^T [E][n][d], blocks along d
+  VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_down), E, d, n, t,
+                                                               d, 0, s));
+  VGG_LAUNCH("quantize_mx_weights", launch_quantize_weight_mx(t, E, n, d, static_cast<uint8_t*>(Wdt_q),
+                                                              static_cast<uint8_t*>(wdt_sf), kMxBN, 0,
+                                                              ceil_div(n, kMxBN), ceil_div(d, 128), nb, s));
+  // [W_gate; W_up]^T [E][d][2n], blocks along 2n (the transposes follow the quantization above on the stream)
+  VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_gate), E, n, d, t,
+                                                               2 * n, 0, s));
+  VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_up), E, n, d, t,
+                                                               2 * n, n, s));
+  VGG_LAUNCH("quantize_mx_weights", launch_quantize_weight_mx(t, E, d, 2 * n, static_cast<uint8_t*>(Wgu_q),
+                                                              static_cast<uint8_t*>(wgu_sf), kMxBN, 0,
+                                                              ceil_div(d, kMxBN), ceil_div(2 * n, 128), nb, s));
+  return MOE_OK;
 }
 
 int moe_quantize_dact_weights_e4m3(moe_ctx* ctx, const void* W_down, int E, int n, int d, void* tmp, void* Wdt_q,

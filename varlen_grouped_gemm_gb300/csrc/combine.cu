@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
         }
       }
     }
-    if (CODES) {
+    if (CODES && cs) {  // per-row scales (the block-scaled form takes its scales elsewhere: cs == nullptr)
       const float sc = __ldg(cs + t);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   if (CODES) {
     for (long long j = gw * 32 + lane; j < cap && ok; j += nw * 32) {
       if (j < P && sorted_tok[j] >= 0) continue;
-      out_cs[j] = 1.0f;
+      if (out_cs) out_cs[j] = 1.0f;
       for (int c0 = 0; c0 < d; c0 += kGrChunk) {
         const uint32_t bytes = 2u * static_cast<uint32_t>(min(kGrChunk, d - c0));
         bulk_s2g(out_c + j * d + c0, zero, bytes / 2);

@@ -139,6 +139,8 @@ struct GemmParams {
   int sf_kst;
   uint8_t* o_sf;
   int o_sf_kst;
+  uint8_t* o_q;        // the dSwiGLU epilogue's block-scaled [dH | dU] codes [rows][o_q_ld] (o_sf: their blocks)
+  long long o_q_ld;
   int* err;
   unsigned long long timeout_ns;
 };
@@ -1316,6 +1318,25 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
               du[i] = da * sl;
               dh[i] = da * u[i] * sg * (1.0f + h[i] * (1.0f - sg));
               ap[i] = w * a;
+            }
+            if (kMx && row_ok && ncols >= 32) {
+              // [dH | dU] as block-scaled e4m3 for the dX GEMM, from the exact fp32 values: this row's 32 columns
+              // of dH (row columns col..) and of dU (n + col..) are one block each; their scale bytes go into
+              // the row tile's blocks over the 2n columns
+              const long long rt = s_tile[tl.g] / mx_ncu + tl.m0 / BM;
+              uint8_t* sfr = p.o_sf + rt * p.o_sf_kst * 512ll + lane * 16 + quarter * 4;
+              uint32_t qw[8];
+              const int eh = mx_block32(dh, qw);
+              uint8_t* dst = p.o_q + orow * p.o_q_ld + col;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+              *reinterpret_cast<uint4*>(dst + 16) = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+              sfr[(col >> 7) * 512 + ((col >> 5) & 3)] = static_cast<uint8_t>(eh + 127);
+              const int eu = mx_block32(du, qw);
+              const int cu = p.N + col;
+              dst = p.o_q + orow * p.o_q_ld + cu;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+              *reinterpret_cast<uint4*>(dst + 16) = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+              sfr[(cu >> 7) * 512 + ((cu >> 5) & 3)] = static_cast<uint8_t>(eu + 127);
             }
             emit32(o0, dh, col, ncols, full, row_ok, false);
             emit32(o1, du, col, ncols, full, row_ok, false);

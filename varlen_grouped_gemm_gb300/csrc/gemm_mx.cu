@@ -185,4 +185,17 @@ cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cuda
   return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_MX>(p, m, grid, s);
 }
 
+// The backward's dSwiGLU GEMM on block-scaled operands: A = the sorted dO code rows (TMA), B = W_down^T [E][n][d]
+// codes; the dSwiGLU epilogue (dS partials, dH, dU, A' and their bf16 low parts) also writes [dH | dU] as
+// block-scaled codes with their scale blocks for the dX GEMM.  Eight epilogue warps, 32 columns at a time.
+cudaError_t run_dact_dswiglu_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  return launch_grouped_gemm<kMxBN, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU, false, 1, X_MX>(p, m, grid, s);
+}
+
+// The dX GEMM on block-scaled operands: A = [dH | dU] codes [cap][2n], B = [W_gate; W_up]^T [E][d][2n] codes;
+// plain bf16 store of dXp (four epilogue warps: 64-column stores of the 192-column tile).
+cudaError_t run_dx_store_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
+}
+
 }  // namespace vgg

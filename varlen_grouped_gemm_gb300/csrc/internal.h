@@ -44,6 +44,8 @@ cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid,
 constexpr int kMxBN = 192;
 cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dact_dswiglu_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dx_store_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rows_mx(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                     uint8_t* q, uint8_t* sf, int sf_ld, cudaStream_t s);
 // Scale blocks of a gathered operand per row tile of the varlen-M GEMMs over `off` (tiles in group order, at most
