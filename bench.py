@@ -144,6 +144,31 @@ def roofline(name, work, ms_total, launches, pk, traffic=None):
             "moved_gbs": mv / (avg_ms * 1e-3) / 1e9}
 
 
+def hbm_stages(wl, P, prof, steps, pk):
+    """The memory-bound stages against the measured HBM bandwidth: the route + permute stage as one (router
+    logits, top-K, grouping: 2Td + 2dE + 16P + 4TE bytes, plus 4TE for the full scores under Token Rounding),
+    the combine (2Pd + 2Td), the backward's per-token reduction (token_backward: 2Pd + 2Td + 8TE) and the sorted
+    copies (gather_rows: 4Td + 4Pd, bytes it moves)."""
+    T, d, E = wl.T, wl.d, wl.E
+    per_step = lambda *names: sum(prof[k][0] for k in names if k in prof) / max(steps, 1)
+    stages = {
+        "route_permute": (("router_logits", "topk_softmax", "permute"),
+                          2 * T * d + 2 * d * E + 16 * P + 4 * T * E + (4 * T * E if wl.m_tile else 0)),
+        "combine": (("combine",), 2 * P * d + 2 * T * d),
+        "token_backward": (("token_backward",), 2 * P * d + 2 * T * d + 8 * T * E),
+        "gather_rows": (("gather_rows",), 4 * T * d + 4 * P * d),
+    }
+    out = {}
+    for name, (kernels, nbytes) in stages.items():
+        ms = per_step(*kernels)
+        if ms <= 0:
+            continue
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"kernels": list(kernels), "bytes": nbytes, "ms_per_step": ms, "gbs": gbs,
+                     "frac_of_hbm": gbs / pk["hbm_gbs"]}
+    return out
+
+
 def kernel_table(prof, work, steps, pk):
     """Per kernel label: time per step, share, TFLOP/s, GB/s of algorithmic and of moved bytes, bound."""
     kernels = {}
@@ -653,6 +678,7 @@ def measure_workload(vgg, ctx, name, steps, warmup, pk, dev, flush, stream):
            "pct_of_peak_bf16": 100 * flops / (ms * 1e-3) / 1e12 / pk["bf16_sus"], "tokens_per_s": wl.T / (ms * 1e-3),
            "pairs": P, "empty_experts": int((counts == 0).sum()), "max_rows_per_expert": int(counts.max()),
            "roofline": roofline(dname, work, dms, dl, pk, recorded_traffic(wl.name, dname)),
+           "hbm_stages": hbm_stages(wl, P, prof, steps, pk),
            "kernels": {k: {"ms_per_step": v["ms_per_step"], "share": round(v["share"], 4)}
                        for k, v in kernel_table(prof, work, steps, pk).items()},
            "activation_memory": activation_memory(buf, base), "steps": steps,
@@ -870,7 +896,8 @@ def run_ours(args, rank, world, local_rank):
             "tokens_per_s": tokens_s, "pct_of_peak_bf16": 100 * tflops / world / pk["bf16_sus"],
             "peak_bf16_tflops": pk["bf16_sus"], "peak_source": pk["source"] + " sustained",
             "step_ms_min": min(step_ms), "step_ms_median": float(np.median(step_ms)),
-            "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
+            "roofline": roof, "hbm_stages": hbm_stages(wl, P, prof, args.steps, pk), "kernels": kernels,
+            "gpu_launches": gpu_launches,
             "activation_memory": activation_memory(buf),
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "e4m3_forward": e4m3,
             "per_workload": per_workload,
