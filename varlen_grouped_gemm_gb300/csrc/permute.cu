@@ -100,12 +100,17 @@ __device__ __forceinline__ int token_experts(int t, const int32_t* ids, const fl
     }
   } else {
     const int W = (E + 31) >> 5;
-    // weights of the token's own top-K and the denominator of a padded pair's weight
-    float lmax = 0.0f, denom = 0.0f;
-    if (logits) {
-      lmax = logits[static_cast<long long>(t) * E + ids[static_cast<long long>(t) * K]];
-      for (int k = 0; k < K; ++k) denom += expf(logits[static_cast<long long>(t) * E + ids[static_cast<long long>(t) * K + k]] - lmax);
+    // the token's top-K (ids and weights, loaded once); a pair outside it (a padded one) gets
+    // exp(l_e - l_max) / sum over the top-K of exp(l_k - l_max), the denominator taken on first need
+    int ek[8];
+    float wk[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      ek[k] = k < K ? __ldg(ids + static_cast<long long>(t) * K + k) : -1;
+      wk[k] = k < K ? __ldg(topk_w + static_cast<long long>(t) * K + k) : 0.0f;
     }
+    float lmax = 0.0f, denom = 0.0f;
+    bool have_denom = false;
     for (int wi = 0; wi < W; ++wi) {
       uint32_t word = member[static_cast<long long>(t) * W + wi];
       while (word) {
@@ -113,9 +118,19 @@ __device__ __forceinline__ int token_experts(int t, const int32_t* ids, const fl
         word &= word - 1;
         const int e = wi * 32 + bit;
         float w = -1.0f;
-        for (int k = 0; k < K; ++k)
-          if (ids[static_cast<long long>(t) * K + k] == e) w = topk_w[static_cast<long long>(t) * K + k];
-        if (w < 0.0f) w = logits ? expf(logits[static_cast<long long>(t) * E + e] - lmax) / denom : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (ek[k] == e) w = wk[k];
+        if (w < 0.0f && logits) {
+          if (!have_denom) {
+            lmax = logits[static_cast<long long>(t) * E + ek[0]];
+            for (int k = 0; k < K; ++k) denom += expf(logits[static_cast<long long>(t) * E + ek[k]] - lmax);
+            have_denom = true;
+          }
+          w = expf(logits[static_cast<long long>(t) * E + e] - lmax) / denom;
+        } else if (w < 0.0f) {
+          w = 0.0f;
+        }
         if (cnt < max_out) {
           e_out[cnt] = e;
           w_out[cnt] = w;
@@ -524,40 +539,51 @@ constexpr int kTrThreads = 1024;
 constexpr int kTrMaxT = 32768;
 constexpr int kTrListCap = 8192;  // compacted keys of the threshold bin; a larger bin rescans all keys
 
-// The digit of the remaining-th largest from a filled histogram of digit (k >> shift) & (NB - 1): lane l
-// of warp 0 owns NB/32 bins, a suffix scan over lanes finds the owner of the bin, which walks its bins
-// downwards.  Updates prefix, mask, remaining; returns the count of the chosen bin.
+// The digit of the remaining-th largest from a filled histogram of digit (k >> shift) & (NB - 1): thread i owns
+// bins [NB / kTrThreads i, ...); a block-wide suffix scan of the threads' counts (from the highest bins down) finds
+// the owner of the bin where the count from the top reaches `remaining`, which walks its bins downwards.  Updates
+// prefix, mask, remaining; returns the count of the chosen bin.
 template <int NB>
 __device__ int tr_pick(const int* hist, uint32_t& prefix, uint32_t& mask, int shift, int& remaining, int* s_res) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid < 32) {
-    constexpr int PER = NB / 32;
-    int sl = 0;
-    for (int i = 0; i < PER; ++i) sl += hist[PER * lane + i];
-    int suf = sl;
+  static_assert(NB % kTrThreads == 0, "whole bins per thread");
+  constexpr int PER = NB / kTrThreads;
+  constexpr int NW = kTrThreads / 32;
+  __shared__ int s_wsum[NW];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int sl = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(0xffffffffu, suf, o);
-      if (lane + o < 32) suf += y;
-    }
-    const unsigned reach = __ballot_sync(0xffffffffu, suf >= remaining);
-    const int owner = reach ? 31 - __clz(reach) : 0;
-    if (lane == owner) {
-      int cum = suf - sl;
-      int digit = PER * lane, cnt = 0;
-      for (int i = PER - 1; i >= 0; --i) {
-        const int h = hist[PER * lane + i];
-        if (cum + h >= remaining) {
-          digit = PER * lane + i;
-          cnt = h;
-          break;
-        }
-        cum += h;
+  for (int i = 0; i < PER; ++i) sl += hist[PER * tid + i];
+  // suffix sum within the warp (lanes above), then over the warps above
+  int suf = sl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  if (lane == 0) s_wsum[warp] = suf;  // the warp's total
+  __syncthreads();
+  int above = 0;
+  for (int w = warp + 1; w < NW; ++w) above += s_wsum[w];
+  suf += above;  // count of the bins from this thread's first bin to the top
+  if (tid == 0 && suf < remaining) {  // fewer candidates than asked for (outside the contract): the lowest bin
+    s_res[0] = 0;
+    s_res[1] = remaining - suf;
+    s_res[2] = 0;
+  }
+  if (suf >= remaining && suf - sl < remaining) {  // exactly one thread: the bin is among its own
+    int cum = suf - sl, digit = PER * tid, cnt = 0;
+    for (int i = PER - 1; i >= 0; --i) {
+      const int h = hist[PER * tid + i];
+      if (cum + h >= remaining) {
+        digit = PER * tid + i;
+        cnt = h;
+        break;
       }
-      s_res[0] = digit;
-      s_res[1] = remaining - cum;
-      s_res[2] = cnt;
+      cum += h;
     }
+    s_res[0] = digit;
+    s_res[1] = remaining - cum;
+    s_res[2] = cnt;
   }
   __syncthreads();
   prefix |= static_cast<uint32_t>(s_res[0]) << shift;
