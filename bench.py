@@ -296,17 +296,18 @@ def ncu_traffic(csv_path: str, workload: str) -> dict:
         label = _label_of(key[1])
         if label is None:
             continue
-        if label.startswith("dw_tiled"):
-            label = "dw_gate_up" if dw_seen == 0 else "dw_down"
+        if label.startswith("dw_tiled"):  # every step launches dW gate/up, then dW down
+            label = "dw_gate_up" if dw_seen % 2 == 0 else "dw_down"
             dw_seen += 1
         m = per[key]
         b = m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0)
         out[label] = out.get(label, 0.0) + b
         if "grouped_gemm_kernel" in key[1]:
             launches[label] = launches.get(label, 0) + 1
-    # the grouping's kernels add up to one entry-point launch; a GEMM label launched twice per step
-    # (the router weight gradient's two halves) is averaged per launch
-    out = {k: v / launches.get(k, 1) for k, v in out.items()}
+    # a GEMM label is averaged over its launches; every other label over the captured steps (one launch of
+    # the gate/up GEMM per step), so that the grouping's kernels add up to one entry-point launch
+    steps = max(launches.get("gate_up_swiglu", 1), 1)
+    out = {k: v / (launches[k] if k in launches else steps) for k, v in out.items()}
     return {"workload": workload, "source_hash": source_hash(), "bytes_per_launch": out}
 
 
