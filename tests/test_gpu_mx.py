@@ -315,3 +315,63 @@ def test_mx_backward_matches_oracle(ctx, wl):
         rep = compare_layer(buf, inp, O_ref, cache, grads)
     print(wl.name, "[dH|dU] codes differing:", int(bad.sum()), "of", hq.size,
           {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
+
+
+def test_mx_fullsize_c2(ctx):
+    """The c2 shape at full size (the configuration the benchmark's block-scaled arm times), on sampled tokens:
+    every expert contribution of a token depends only on its own row and the experts' weights.  X's codes and
+    scales of the sampled tokens and the codes and scale blocks of every expert they reach bit for bit; O of the
+    sampled tokens within the usual tolerance of the oracle's block-scaled forward."""
+    import gc
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.WORKLOADS["c2"]
+    dev = {name: bits_to_dev(make(wl)) for name, make in (
+        ("X", synth.make_x), ("W_r", synth.make_router), ("W_gate", synth.make_w_gate), ("W_up", synth.make_w_up),
+        ("W_down", synth.make_w_down))}
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, backward=False, mx=True)
+    wmx = vgg.MxWeights.quantize(ctx, dev["W_gate"], dev["W_up"], dev["W_down"])
+    vgg.forward_mx(ctx, dev["X"], dev["W_r"], None, wmx, buf)
+    rc, code = vgg.moe_get_error(ctx)
+    assert rc == vgg.MOE_OK and code == 0, (rc, code)
+    try:
+        g = gpu_routing(buf)
+        r = check_routing_bit_exact(g, wl.K, 0)
+        rng = np.random.default_rng(78)
+        toks = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, 6, replace=False)])).astype(np.int64)
+        X = synth.make_x(wl, rows=toks)
+        xq, xe = oracle.quantize_blocks_mx(X)
+        tsel = torch.from_numpy(toks).cuda()
+        np.testing.assert_array_equal(buf.mxq[tsel].cpu().numpy(), xq)
+        np.testing.assert_array_equal(buf.mxsf[tsel].cpu().numpy()[:, :wl.d // 32].astype(np.int64) - 127, xe)
+        Xd = oracle.dequantize_blocks_mx(xq, xe)
+        L = mo.router_logits(X, synth.make_router(wl), None)
+        w = mo.combine_weights(L, r.topk_ids[toks])
+        gu_sf, dn_sf = wmx.gu_sf.cpu().numpy(), wmx.dn_sf.cpu().numpy()
+        O = np.zeros((len(toks), wl.d))
+        member = r.member[toks]
+        E, n, d = wl.E, wl.n, wl.d
+        gi = _weight_index(E, n, d, TILE // 2, 0)
+        ui = _weight_index(E, n, d, TILE // 2, TILE // 2)
+        di = _weight_index(E, d, n, TILE, 0)
+        for e in sorted(set(np.nonzero(member)[1].tolist())):
+            rows = np.nonzero(member[:, e])[0]
+            gq, ge = oracle.quantize_blocks_mx(synth.make_w_gate(wl, [e])[0])
+            uq, ue = oracle.quantize_blocks_mx(synth.make_w_up(wl, [e])[0])
+            dq, de = oracle.quantize_blocks_mx(synth.make_w_down(wl, [e])[0])
+            np.testing.assert_array_equal(wmx.Wg_q[e].cpu().numpy(), gq)
+            np.testing.assert_array_equal(wmx.Wu_q[e].cpu().numpy(), uq)
+            np.testing.assert_array_equal(wmx.Wd_q[e].cpu().numpy(), dq)
+            np.testing.assert_array_equal(gu_sf[gi[e]].astype(np.int64) - 127, ge)
+            np.testing.assert_array_equal(gu_sf[ui[e]].astype(np.int64) - 127, ue)
+            np.testing.assert_array_equal(dn_sf[di[e]].astype(np.int64) - 127, de)
+            h = Xd[rows] @ oracle.dequantize_blocks_mx(gq, ge).T
+            u = Xd[rows] @ oracle.dequantize_blocks_mx(uq, ue).T
+            aq, ae = oracle.quantize_blocks_mx(mo.silu(h) * u)
+            y = oracle.dequantize_blocks_mx(aq, ae) @ oracle.dequantize_blocks_mx(dq, de).T
+            O[rows] += w[rows, e][:, None] * y
+        rep = oracle.compare("O (sampled tokens)", dev_to_f64(buf.O[tsel]), O)
+        print("c2 block-scaled", len(toks), "tokens", (rep["max"], rep["mean"]))
+    finally:
+        del buf, dev, wmx
+        gc.collect()
+        torch.cuda.empty_cache()

@@ -47,6 +47,25 @@ def test_host_only_queries(libpath):
     assert vgg.status_str(vgg.MOE_ERR_INVALID_ARG) == "invalid argument"
 
 
+def test_block_scale_size_queries(libpath):
+    """The block-scaled form's scale layouts, by their stated shapes: 4 bytes per 128 columns of a row-major
+    array; pairs of 512-byte blocks per 192-row tile (96 + 96 rows for the gate/up pair) and 128 columns of the
+    reduction for the weights; one block per 128-row tile (at most cap / 128 + E tiles) and 128 columns for
+    the activations."""
+    import varlen_grouped_gemm_gb300 as vgg
+    L = vgg.lib()
+    assert [L.moe_mx_sf_cols(c) for c in (64, 128, 2048, 2880, 0)] == [4, 4, 64, 92, 0]
+    E, d, n = 128, 2048, 512
+    assert L.moe_mx_weight_sf_bytes(E, d, n, 0) == 1024 * E * 6 * 16       # ceil(512 / 96) tiles, 2048 / 128 stages
+    assert L.moe_mx_weight_sf_bytes(E, d, n, 1) == 1024 * E * 11 * 4       # ceil(2048 / 192) tiles, 512 / 128
+    assert L.moe_mx_weight_sf_bytes(E, d, n, 2) == 1024 * E * 3 * 16       # W_down^T: ceil(512 / 192), 2048 / 128
+    assert L.moe_mx_weight_sf_bytes(E, d, n, 3) == 1024 * E * 11 * 8       # [W_gate; W_up]^T: 1024 / 128 stages
+    assert L.moe_mx_weight_sf_bytes(E, 2000, n, 0) == 0 and L.moe_mx_weight_sf_bytes(E, d, n, 4) == 0
+    assert L.moe_mx_act_sf_bytes(32768, 128, 512) == 512 * (256 + 128) * 4
+    assert L.moe_mx_act_sf_bytes(100, 3, 2880) == 512 * (1 + 3) * 23
+    assert L.moe_mx_act_sf_bytes(0, 3, 64) == 0
+
+
 def test_expert_capacity_matches_the_oracle(libpath):
     """The capacity dispatch's slot count C = ceil(cf T K / E) comes from the library (the binding does no
     arithmetic); it equals the oracle's reading on a grid that includes exact multiples and fractions."""
@@ -76,7 +95,8 @@ _CTX_ENTRIES = ["moe_route", "moe_permute", "moe_grouped_gemm_fwd", "moe_combine
                 "moe_permute_noalloc", "moe_permute_capacity", "moe_quantize_rows_e4m3", "moe_grouped_gemm_fwd_e4m3",
                 "moe_quantize_dx_weights_e4m3", "moe_quantize_dact_weights_e4m3", "moe_backward_e4m3",
                 "moe_test_gemm_varlen_m", "moe_test_gemm_varlen_k", "moe_test_gemm_varlen_k_dual",
-                "moe_test_gemm_varlen_m_dual"]
+                "moe_test_gemm_varlen_m_dual", "moe_quantize_rows_mx", "moe_quantize_weights_mx",
+                "moe_grouped_gemm_fwd_mx", "moe_quantize_bwd_weights_mx", "moe_backward_mx"]
 
 
 @pytest.mark.parametrize("name", _CTX_ENTRIES)

@@ -80,7 +80,8 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //             column tile.
 //             BN = 128 or 192, so that both accumulators and every stage's scales fit the 512 TMEM columns.  The
 //             SwiGLU epilogue of this form emits A itself as block-scaled codes (a thread's 32 columns of
-//             its row are one block) with the scale blocks the down projection reads.
+//             its row are one block) with the scale blocks the down projection reads, and the dSwiGLU
+//             epilogue emits [dH | dU] the same way for the dX GEMM (o_q, o_sf).
 enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4, X_MX = 8 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
