@@ -292,12 +292,15 @@ int moe_grouped_gemm_fwd_e4m3(moe_ctx* ctx, const void* Xq, const float* x_scale
  *              127 up to a multiple of 4 per 128 columns;
  *   blocks     512 bytes per 128 operand rows and 128 columns of the reduction: row r, block k of the
  *              128 columns at byte (r % 32) * 16 + (r / 32) * 4 + k; rows or columns beyond the operand
- *              hold 127.  The weights' blocks come in pairs (1024 bytes) per 192-row tile and 128 columns:
- *              W_gate / W_up [E][ceil(n/96)][ceil(d/128)] pairs, tile rows 0..95 of [e][t][.] = W_gate[e]
- *              rows 96t..96t+95, tile rows 96..191 = W_up[e] rows 96t..96t+95 (tile row i in block i / 128,
- *              block row i % 128); W_down [E][ceil(d/192)][ceil(n/128)] pairs over W_down[e] rows 192t..;
- *              the activations A: one block per 128-row tile of every expert's sorted rows (tiles in
- *              expert order) and 128 columns, [tiles][ceil(n/128)].
+ *              hold 127.  The weights' blocks come per tile of a GEMM's B rows (ceil(rows / 128) blocks)
+ *              and 128 columns: W_gate / W_up [E][ceil(n/96)][ceil(d/128)] pairs of blocks, tile rows
+ *              0..95 of [e][t][.] = W_gate[e] rows 96t..96t+95, tile rows 96..191 = W_up[e] rows
+ *              96t..96t+95 (tile row i in block i / 128, block row i % 128); W_down [E][ceil(d/Bd)]
+ *              [ceil(n/128)] over W_down[e] rows Bd t.. with Bd = w(d); the activations A: one block per
+ *              128-row tile of every expert's sorted rows (tiles in expert order) and 128 columns,
+ *              [tiles][ceil(n/128)].  The width w(N) of the plain GEMMs' tiles (down projection, dSwiGLU,
+ *              dX) is 192, or 128 when 192-row tiles would pass N by more than N / 4 and 128-row tiles by
+ *              less (w(256) = 128; w(512) = w(2048) = 192).
  */
 /* Bytes per row of a row-major scale array for `cols` columns: 4 * ceil(cols / 128). */
 long long moe_mx_sf_cols(int cols);
@@ -355,9 +358,10 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
 /*
  * moe_quantize_bwd_weights_mx — the block-scaled B operands of the backward's activation-gradient GEMMs, once per
  * weight update: W_down^T (per expert [n, d], blocks along d) into codes Wdt_q [E,n,d] and scale blocks wdt_sf
- * (moe_mx_weight_sf_bytes(E,d,n,2) bytes, [E][ceil(n/192)][ceil(d/128)] pairs of blocks over W_down^T's rows);
+ * (moe_mx_weight_sf_bytes(E,d,n,2) bytes, [E][ceil(n/w(n))][ceil(d/128)] tiles of blocks over W_down^T's rows);
  * [W_gate; W_up]^T (per expert [d, 2n], W_gate's rows in columns 0..n-1, W_up's in n..2n-1, blocks along 2n)
- * into Wgu_q [E,d,2n] and wgu_sf (moe_mx_weight_sf_bytes(E,d,n,3) bytes, [E][ceil(d/192)][ceil(2n/128)] pairs).
+ * into Wgu_q [E,d,2n] and wgu_sf (moe_mx_weight_sf_bytes(E,d,n,3) bytes, [E][ceil(d/w(d))][ceil(2n/128)] tiles);
+ * w(N) the tile width stated with the scale layouts above.
  * tmp: device scratch of E*d*2n bf16 (caller-owned, overwritten).  [SM] "3 기여 ①" (dA' = dO W_down),
  * "4 기여 ②" (the dX GEMM); [GG] "한계".  16-byte aligned buffers, d and n multiples of 64, else
  * MOE_ERR_INVALID_ARG.

@@ -39,20 +39,28 @@ def _block_off(r, b):
     return (r % 32) * 16 + (r // 32) * 4 + b
 
 
-TILE = 192  # the block-scaled GEMMs' tile width: W_down rows per tile, 96 + 96 for the gate/up pair
+TILE = 192  # the gate/up pair's tile: 96 + 96 rows of W_gate and W_up
 
 
-def _weight_index(E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
+def _tile_cols(N: int) -> int:
+    """The plain block-scaled GEMMs' tile width for N output columns, as the header states it: 192, or 128
+    when 192-row tiles would pass N by more than N / 4 and 128-row tiles by less."""
+    w192, w128 = -(-N // 192) * 192 - N, -(-N // 128) * 128 - N
+    return 128 if (4 * w192 > N and w128 < w192) else 192
+
+
+def _weight_index(E: int, R: int, C: int, rows_per_tile: int, row0: int, tile_rows: int = TILE) -> np.ndarray:
     """Byte index [E, R, C/32] of each (row, 32-column block) scale of one weight in its scale buffer:
-    [E][tiles][ceil(C/128)] groups of two 512-byte blocks, tile row i = row0 + row % rows_per_tile in block
-    i // 128."""
+    [E][tiles][ceil(C/128)] groups of ceil(tile_rows / 128) 512-byte blocks, tile row i = row0 + row % rows_per_tile
+    in block i // 128."""
     kst = -(-C // 128)
+    nblk = -(-tile_rows // 128)
     tiles = -(-R // rows_per_tile)
     rows = np.arange(R)[:, None]
     cols = np.arange(C // 32)[None, :]
     t, tr = rows // rows_per_tile, row0 + rows % rows_per_tile
-    off = ((t * kst + cols // 4) * 2 + tr // 128) * 512 + _block_off(tr % 128, cols % 4)
-    return np.arange(E)[:, None, None] * (tiles * kst * 1024) + off[None]
+    off = ((t * kst + cols // 4) * nblk + tr // 128) * 512 + _block_off(tr % 128, cols % 4)
+    return np.arange(E)[:, None, None] * (tiles * kst * nblk * 512) + off[None]
 
 
 def _unpack_weight_blocks(sf: np.ndarray, E: int, R: int, C: int, rows_per_tile: int, row0: int) -> np.ndarray:
@@ -106,16 +114,18 @@ def test_mx_weights_bit_exact(ctx, E, d, n):
     w = vgg.MxWeights.quantize(ctx, bits_to_dev(Wg), bits_to_dev(Wu), bits_to_dev(Wd))
     gu = w.gu_sf.cpu().numpy()
     dn = w.dn_sf.cpu().numpy()
-    assert gu.size == E * -(-n // (TILE // 2)) * -(-d // 128) * 1024 and dn.size == E * -(-d // TILE) * -(-n // 128) * 1024
+    bd = _tile_cols(d)
+    assert gu.size == E * -(-n // (TILE // 2)) * -(-d // 128) * 1024
+    assert dn.size == E * -(-d // bd) * -(-n // 128) * 512 * -(-bd // 128)
     want = {"gu": np.full_like(gu, 127), "dn": np.full_like(dn, 127)}
-    for got_q, W, R, C, key, rpt, r0 in ((w.Wg_q, Wg, n, d, "gu", TILE // 2, 0),
-                                         (w.Wu_q, Wu, n, d, "gu", TILE // 2, TILE // 2),
-                                         (w.Wd_q, Wd, d, n, "dn", TILE, 0)):
+    for got_q, W, R, C, key, rpt, r0, tr in ((w.Wg_q, Wg, n, d, "gu", TILE // 2, 0, TILE),
+                                             (w.Wu_q, Wu, n, d, "gu", TILE // 2, TILE // 2, TILE),
+                                             (w.Wd_q, Wd, d, n, "dn", bd, 0, bd)):
         q, e = oracle.quantize_blocks_mx(W.reshape(E * R, C))
         np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * R, C), q)
         # the whole scale buffer, built here from the oracle's exponents: entries no weight row or column
         # fills hold scale 1 (byte 127)
-        want[key][_weight_index(E, R, C, rpt, r0)] = e.reshape(E, R, -1) + 127
+        want[key][_weight_index(E, R, C, rpt, r0, tr)] = e.reshape(E, R, -1) + 127
     np.testing.assert_array_equal(gu, want["gu"])
     np.testing.assert_array_equal(dn, want["dn"])
 
@@ -255,7 +265,7 @@ def test_mx_backward_matches_oracle(ctx, wl):
         np.testing.assert_array_equal(got_q.cpu().numpy().reshape(E * R, C), q)
         sf = got_sf.cpu().numpy()
         want = np.full_like(sf, 127)
-        want[_weight_index(E, R, C, TILE, 0)] = e.reshape(E, R, -1) + 127
+        want[_weight_index(E, R, C, _tile_cols(R), 0, _tile_cols(R))] = e.reshape(E, R, -1) + 127
         np.testing.assert_array_equal(sf, want)
 
     g = gpu_routing(buf)
@@ -352,7 +362,7 @@ def test_mx_fullsize_c2(ctx):
         E, n, d = wl.E, wl.n, wl.d
         gi = _weight_index(E, n, d, TILE // 2, 0)
         ui = _weight_index(E, n, d, TILE // 2, TILE // 2)
-        di = _weight_index(E, d, n, TILE, 0)
+        di = _weight_index(E, d, n, _tile_cols(d), 0, _tile_cols(d))
         for e in sorted(set(np.nonzero(member)[1].tolist())):
             rows = np.nonzero(member[:, e])[0]
             gq, ge = oracle.quantize_blocks_mx(synth.make_w_gate(wl, [e])[0])

@@ -748,12 +748,14 @@ long long moe_mx_sf_cols(int cols) { return cols > 0 ? 4ll * ceil_div(cols, 128)
 
 long long moe_mx_weight_sf_bytes(int E, int d, int n, int which) {
   if (E < 1 || d < 64 || n < 64 || d % 64 || n % 64) return 0;
-  // one group of mx_b_blocks(kMxBN) blocks per column tile and stage of K (the gate/up pair: kMxBN / 2 rows of each)
-  const long long grp = 512ll * mx_b_blocks(kMxBN);
-  if (which == 0) return grp * E * ceil_div(n, kMxBN / 2) * ceil_div(d, 128);
-  if (which == 1) return grp * E * ceil_div(d, kMxBN) * ceil_div(n, 128);
-  if (which == 2) return grp * E * ceil_div(n, kMxBN) * ceil_div(d, 128);      // W_down^T [E][n][d]
-  if (which == 3) return grp * E * ceil_div(d, kMxBN) * ceil_div(2 * n, 128);  // [W_gate; W_up]^T [E][d][2n]
+  // one group of mx_b_blocks(BN) blocks per column tile of BN rows and stage of K (the gate/up pair: kMxBN / 2 rows
+  // of each; the plain GEMMs: BN = mx_tile_cols of their output width)
+  const auto grp = [](int BN) { return 512ll * mx_b_blocks(BN); };
+  if (which == 0) return grp(kMxBN) * E * ceil_div(n, kMxBN / 2) * ceil_div(d, 128);
+  const int bd = mx_tile_cols(d), bn = mx_tile_cols(n);
+  if (which == 1) return grp(bd) * E * ceil_div(d, bd) * ceil_div(n, 128);
+  if (which == 2) return grp(bn) * E * ceil_div(n, bn) * ceil_div(d, 128);      // W_down^T [E][n][d]
+  if (which == 3) return grp(bd) * E * ceil_div(d, bd) * ceil_div(2 * n, 128);  // [W_gate; W_up]^T [E][d][2n]
   return 0;
 }
 
@@ -796,9 +798,10 @@ int moe_quantize_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_up, 
   VGG_LAUNCH("quantize_mx_weights",
              launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_up), E, n, d, static_cast<uint8_t*>(Wu_q),
                                        static_cast<uint8_t*>(gu_sf), hb, hb, ceil_div(n, hb), kd, nb, s));
+  const int bd = mx_tile_cols(d);
   VGG_LAUNCH("quantize_mx_weights",
              launch_quantize_weight_mx(static_cast<const __nv_bfloat16*>(W_down), E, d, n, static_cast<uint8_t*>(Wd_q),
-                                       static_cast<uint8_t*>(dn_sf), kMxBN, 0, ceil_div(d, kMxBN), kn, nb, s));
+                                       static_cast<uint8_t*>(dn_sf), bd, 0, ceil_div(d, bd), kn, mx_b_blocks(bd), s));
   return MOE_OK;
 }
 
@@ -865,14 +868,15 @@ int moe_grouped_gemm_fwd_mx(moe_ctx* ctx, const void* Xq, const void* x_sf, cons
     p.a_sf = static_cast<const uint8_t*>(a_sf);
     p.b_sf = static_cast<const uint8_t*>(dn_sf);
     p.sf_kst = ceil_div(n, 128);
+    const int BN = mx_tile_cols(d);
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, kMxBN) ||
+    if (!make_map_2d(&m.a0, Aq, nk, cap, nk, BM) || !make_map_3d(&m.b0, Wd_q, nk, d, E, BN) ||
         !make_store_map_2d(&m.o0, Yw, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, kMxBN);
-    VGG_LAUNCH("down_scale_mx", run_down_scale_mx(p, m, std::min(tiles, ctx->num_sms), s));
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("down_scale_mx", run_down_scale_mx(BN, p, m, std::min(tiles, ctx->num_sms), s));
   }
   return MOE_OK;
 }
@@ -932,8 +936,8 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   BwdWs w = carve_bwd(ws, T, d, E, n, cap);
   const bool f32 = dW_fp32 != 0;
   const int bn6 = dact_bn(n, cap, E, ctx->num_sms);
-  // one dS partial per (column tile, epilogue column half); the block-scaled form tiles n by kMxBN
-  const int part_ld = (mx ? ceil_div(n, kMxBN) : ceil_div(n, bn6)) * 2;
+  // one dS partial per (column tile, epilogue column half); the block-scaled form tiles n by mx_tile_cols(n)
+  const int part_ld = (mx ? ceil_div(n, mx_tile_cols(n)) : ceil_div(n, bn6)) * 2;
   if (cap > static_cast<long long>(T) * K) {
     __nv_bfloat16* const tail[6] = {w.dH, w.dU, w.Ap, w.dH_lo, w.dU_lo, w.Ap_lo};
     VGG_LAUNCH("zero_tail", launch_zero_tail_rows(offsets, E, cap, n, tail, s));
@@ -1005,15 +1009,16 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.o_q_ld = 2ll * n;
     p.o_sf = static_cast<uint8_t*>(mx->hu_sf);
     p.o_sf_kst = ceil_div(2 * n, 128);
+    const int BN = mx_tile_cols(n);
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, mx->dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, mx->Wdt_q, d / 2, n, E, kMxBN) ||
+    if (!make_map_2d(&m.a0, mx->dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, mx->Wdt_q, d / 2, n, E, BN) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
         !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, kMxBN);
-    VGG_LAUNCH("dact_dswiglu_mx", run_dact_dswiglu_mx(p, m, std::min(tiles, ctx->num_sms), s));
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(n, BN);
+    VGG_LAUNCH("dact_dswiglu_mx", run_dact_dswiglu_mx(BN, p, m, std::min(tiles, ctx->num_sms), s));
   } else if (Wdt_q) {
     // e4m3: the sorted dO code rows (gathered above, else the sorted rows below offsets[E] quantized here),
     // B = W_down^T quantized per row by moe_quantize_dact_weights_e4m3; rows handed to TMA as 16-bit units
@@ -1096,14 +1101,15 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.a_sf = static_cast<const uint8_t*>(mx->hu_sf);
     p.b_sf = static_cast<const uint8_t*>(mx->wgu_sf);
     p.sf_kst = ceil_div(2 * n, 128);
+    const int BN = mx_tile_cols(d);
     Maps m = zero_maps();
-    if (!make_map_2d(&m.a0, mx->HUq, n, cap, n, BM) || !make_map_3d(&m.b0, mx->Wgu_q, n, d, E, kMxBN) ||
+    if (!make_map_2d(&m.a0, mx->HUq, n, cap, n, BM) || !make_map_3d(&m.b0, mx->Wgu_q, n, d, E, BN) ||
         !make_store_map_2d(&m.o0, w.dXp, false, d, cap, d, 64))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
-    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, kMxBN);
-    VGG_LAUNCH("dx_gemm_mx", run_dx_store_mx(p, m, std::min(tiles, ctx->num_sms), s));
+    const int tiles = (ceil_div(cap, BM) + E) * ceil_div(d, BN);
+    VGG_LAUNCH("dx_gemm_mx", run_dx_store_mx(BN, p, m, std::min(tiles, ctx->num_sms), s));
   } else if (Wgu_q) {
     // e4m3: each pair's row [dH | dU] quantized (the rows below offsets[E]), B = [W_gate; W_up]^T quantized per
     // row by moe_quantize_dx_weights_e4m3; rows are handed to TMA as 16-bit units (code pairs)
@@ -1319,23 +1325,23 @@ int moe_quantize_bwd_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_
   VGG_REQUIRE(g.ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   __nv_bfloat16* t = static_cast<__nv_bfloat16*>(tmp);
-  const int nb = mx_b_blocks(kMxBN);
+  const int bn = mx_tile_cols(n), bd = mx_tile_cols(d);
   VGG_CUDA(cudaMemsetAsync(wdt_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 2)), s));
   VGG_CUDA(cudaMemsetAsync(wgu_sf, 127, static_cast<size_t>(moe_mx_weight_sf_bytes(E, d, n, 3)), s));
   // W_down^T [E][n][d], blocks along d
   VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_down), E, d, n, t,
                                                                d, 0, s));
   VGG_LAUNCH("quantize_mx_weights", launch_quantize_weight_mx(t, E, n, d, static_cast<uint8_t*>(Wdt_q),
-                                                              static_cast<uint8_t*>(wdt_sf), kMxBN, 0,
-                                                              ceil_div(n, kMxBN), ceil_div(d, 128), nb, s));
+                                                              static_cast<uint8_t*>(wdt_sf), bn, 0, ceil_div(n, bn),
+                                                              ceil_div(d, 128), mx_b_blocks(bn), s));
   // [W_gate; W_up]^T [E][d][2n], blocks along 2n (the transposes follow the quantization above on the stream)
   VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_gate), E, n, d, t,
                                                                2 * n, 0, s));
   VGG_LAUNCH("quantize_mx_weights", launch_transpose_into_bf16(static_cast<const __nv_bfloat16*>(W_up), E, n, d, t,
                                                                2 * n, n, s));
   VGG_LAUNCH("quantize_mx_weights", launch_quantize_weight_mx(t, E, d, 2 * n, static_cast<uint8_t*>(Wgu_q),
-                                                              static_cast<uint8_t*>(wgu_sf), kMxBN, 0,
-                                                              ceil_div(d, kMxBN), ceil_div(2 * n, 128), nb, s));
+                                                              static_cast<uint8_t*>(wgu_sf), bd, 0, ceil_div(d, bd),
+                                                              ceil_div(2 * n, 128), mx_b_blocks(bd), s));
   return MOE_OK;
 }
 

@@ -12,7 +12,8 @@
 //              block k at byte (r % 32) 16 + (r / 32) 4 + k.  The weights' blocks follow the GEMMs' 192-column
 //              tiles, two blocks (1024 bytes) per tile and stage: W_gate / W_up [E][ceil(n / 96)][ceil(d / 128)],
 //              tile rows 0..95 = W_gate rows 96 t.., rows 96..191 = W_up rows 96 t.. (one gate/up column tile);
-//              W_down [E][ceil(d / 192)][ceil(n / 128)], tile rows = W_down rows 192 t..; the activations A
+//              W_down [E][ceil(d / BN)][ceil(n / 128)], tile rows = W_down rows BN t.. (BN = mx_tile_cols(d):
+//              192, or 128 with one block per tile and stage); the activations A
 //              (written by the SwiGLU epilogue): one block per row tile and stage, [row tile][ceil(n / 128)].
 //              Entries with no operand row or past K hold 127.
 #include "internal.h"
@@ -180,21 +181,28 @@ cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, in
 }
 
 // Down projection on block-scaled A (rows of the SwiGLU epilogue's codes, scale blocks per row tile) and
-// W_down, 192 output columns per tile; the epilogue scales each row by its combine weight (Yw, bf16).
-cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+// W_down, BN = mx_tile_cols(d) output columns per tile; the epilogue scales each row by its combine weight (Yw,
+// bf16).
+cudaError_t run_down_scale_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 128)
+    return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_MX>(p, m, grid, s);
   return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_SCALE, false, 1, X_MX>(p, m, grid, s);
 }
 
 // The backward's dSwiGLU GEMM on block-scaled operands: A = the sorted dO code rows (TMA), B = W_down^T [E][n][d]
 // codes; the dSwiGLU epilogue (dS partials, dH, dU, A' and their bf16 low parts) also writes [dH | dU] as
 // block-scaled codes with their scale blocks for the dX GEMM.  Eight epilogue warps, 32 columns at a time.
-cudaError_t run_dact_dswiglu_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+cudaError_t run_dact_dswiglu_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 128)
+    return launch_grouped_gemm<128, 4, 8, 2, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU, false, 1, X_MX>(p, m, grid, s);
   return launch_grouped_gemm<kMxBN, 4, 8, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_DSWIGLU, false, 1, X_MX>(p, m, grid, s);
 }
 
 // The dX GEMM on block-scaled operands: A = [dH | dU] codes [cap][2n], B = [W_gate; W_up]^T [E][d][2n] codes;
 // plain bf16 store of dXp (four epilogue warps: 64-column stores of the 192-column tile).
-cudaError_t run_dx_store_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+cudaError_t run_dx_store_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 128)
+    return launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
   return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
 }
 

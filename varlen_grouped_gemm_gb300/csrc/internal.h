@@ -40,12 +40,18 @@ cudaError_t launch_transpose_into_bf16(const __nv_bfloat16* in, int E, int R, in
 cudaError_t launch_quantize_rows_e4m3(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                       uint8_t* q, float* scales, cudaStream_t s);
 cudaError_t run_down_scale(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-// block-scaled (1 x 32) e4m3 forward: tile width of both GEMMs (the gate/up pair: kMxBN / 2 output columns)
+// block-scaled (1 x 32) e4m3 GEMMs: the tile width (the gate/up pair: kMxBN / 2 output columns of each), and for the
+// plain ones the width for N output columns: 192, or 128 when 192-column tiles would compute more than a quarter
+// of N in columns past N and 128-column tiles fewer (n = 256: 384 columns for 256)
 constexpr int kMxBN = 192;
+inline int mx_tile_cols(int N) {
+  const int w192 = (N + kMxBN - 1) / kMxBN * kMxBN - N, w128 = (N + 127) / 128 * 128 - N;
+  return (4 * w192 > N && w128 < w192) ? 128 : kMxBN;
+}
 cudaError_t run_gate_up_swiglu_mx(int cn, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_down_scale_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_dact_dswiglu_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
-cudaError_t run_dx_store_mx(const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_down_scale_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dact_dswiglu_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dx_store_mx(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rows_mx(const __nv_bfloat16* M, long long rows, const int32_t* rows_limit, int cols,
                                     uint8_t* q, uint8_t* sf, int sf_ld, cudaStream_t s);
 // Scale blocks of a gathered operand per row tile of the varlen-M GEMMs over `off` (tiles in group order, at most
