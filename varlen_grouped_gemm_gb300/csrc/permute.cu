@@ -531,7 +531,9 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
 // (score descending, token ascending); the selection is a radix select of the
 // need-th largest score among the candidates, ties at the threshold resolved
 // by ascending token.  Keys (score bits; positive floats order as integers)
-// are staged in shared memory.  The first digit (bits 31..21) is histogrammed
+// are read from the transposed scores, L2-resident, by each pass that needs
+// them, so a CTA's shared memory holds only the short lists (two CTAs fit an
+// SM).  The first digit (bits 31..21) is histogrammed
 // over all candidates; the keys of the bin holding the threshold are then
 // compacted into a short list that the two remaining digits (20..10, 9..0)
 // scan, so only one pass touches every token.
@@ -601,11 +603,11 @@ __device__ __forceinline__ void tr_count(int* hist, uint32_t dg) {
   if (dg != static_cast<uint32_t>(NB) && (threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&hist[dg], __popc(grp));
 }
 
-// Histogram of digit (k >> shift) & (NB - 1) over keys matching `prefix` on `mask` (0xFFFFFFFF = not a
-// candidate), then tr_pick.
-template <int NB>
-__device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& mask, int shift, int& remaining,
-                        int* hist, int* s_res) {
+// Histogram of digit (k >> shift) & (NB - 1) over keys key(i), i < n, matching `prefix` on `mask` (0xFFFFFFFF =
+// not a candidate), then tr_pick.
+template <int NB, class KeyAt>
+__device__ int tr_digit(KeyAt key, int n, uint32_t& prefix, uint32_t& mask, int shift, int& remaining, int* hist,
+                        int* s_res) {
   const int tid = threadIdx.x;
   for (int i = tid; i < NB; i += kTrThreads) hist[i] = 0;
   __syncthreads();
@@ -613,7 +615,7 @@ __device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& ma
     const int i = i0 + tid;
     uint32_t dg = NB;
     if (i < n) {
-      const uint32_t k = a[i];
+      const uint32_t k = key(i);
       if (k != 0xFFFFFFFFu && (k & mask) == prefix) dg = (k >> shift) & (NB - 1);
     }
     tr_count<NB>(hist, dg);
@@ -623,24 +625,24 @@ __device__ int tr_digit(const uint32_t* a, int n, uint32_t& prefix, uint32_t& ma
 }
 
 
-// The `need` largest keys of keys[0, n) (0xFFFFFFFF = not a candidate), ties at the threshold going
-// to the lowest indices: a radix select (one 11-bit digit over all keys, the threshold bin compacted
-// into `list` for the two remaining digits), then take(i) for every selected index i.  Block-wide;
-// 1 <= need <= the number of candidates.
-template <class Take>
-__device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* list, int* hist, int* s_res, Take take) {
+// The `need` largest keys key(i), i < n (0xFFFFFFFF = not a candidate), ties at the threshold going to the
+// lowest indices: a radix select (one 11-bit digit over all keys, the threshold bin compacted into `list` for
+// the two remaining digits), then take(i) for every selected index i.  Block-wide; 1 <= need <= the number of
+// candidates.  key(i) is evaluated once per pass (the caller's source: global memory, L2-resident here).
+template <class KeyAt, class Take>
+__device__ void select_take(KeyAt key, int n, int need, uint32_t* list, int* hist, int* s_res, Take take) {
   __shared__ int s_wties[kTrThreads / 32];
   const int tid = threadIdx.x;
   uint32_t prefix = 0, mask = 0;
   int remaining = need;
   const int lane = tid & 31;
-  tr_digit<2048>(keys, n, prefix, mask, 21, remaining, hist, s_res);
+  tr_digit<2048>(key, n, prefix, mask, 21, remaining, hist, s_res);
   // compact the keys of the threshold bin (warp-aggregated appends; order is irrelevant here)
   if (tid == 0) s_res[3] = 0;
   __syncthreads();
   for (int t0 = 0; t0 < n; t0 += kTrThreads) {
     const int t = t0 + tid;
-    const uint32_t k = t < n ? keys[t] : 0xFFFFFFFFu;
+    const uint32_t k = t < n ? key(t) : 0xFFFFFFFFu;
     const bool in = k != 0xFFFFFFFFu && (k & mask) == prefix;
     const unsigned bal = __ballot_sync(0xffffffffu, in);
     int base = 0;
@@ -652,17 +654,18 @@ __device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* lis
   __syncthreads();
   const int nlist = s_res[3];
   int ties;
+  const auto listed = [list](int i) { return list[i]; };
   if (nlist <= kTrListCap) {
-    tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
-    ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
+    tr_digit<2048>(listed, nlist, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(listed, nlist, prefix, mask, 0, remaining, hist, s_res);
   } else {
-    tr_digit<2048>(keys, n, prefix, mask, 10, remaining, hist, s_res);
-    ties = tr_digit<1024>(keys, n, prefix, mask, 0, remaining, hist, s_res);
+    tr_digit<2048>(key, n, prefix, mask, 10, remaining, hist, s_res);
+    ties = tr_digit<1024>(key, n, prefix, mask, 0, remaining, hist, s_res);
   }
   // keys above the threshold are all taken; at the threshold the `remaining` lowest indices.
   if (ties == remaining) {  // every tie is taken: no order needed
     for (int t = tid; t < n; t += kTrThreads) {
-      const uint32_t k = keys[t];
+      const uint32_t k = key(t);
       if (k != 0xFFFFFFFFu && k >= prefix) take(t);
     }
     return;
@@ -673,7 +676,7 @@ __device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* lis
   int tie_base = 0;
   for (int base = 0; base < n; base += kTrThreads) {
     const int t = base + tid;
-    const uint32_t k = t < n ? keys[t] : 0xFFFFFFFFu;
+    const uint32_t k = t < n ? key(t) : 0xFFFFFFFFu;
     const bool cand = k != 0xFFFFFFFFu;
     const bool tie = cand && k == prefix;
     const unsigned bal = __ballot_sync(0xffffffffu, tie);
@@ -693,14 +696,18 @@ __device__ void select_take(const uint32_t* keys, int n, int need, uint32_t* lis
 
 // Token rounding's padding: the `need` largest scores among the tokens not routed to the expert (col:
 // the expert's scores, token-contiguous; routed: bitmap of its routed tokens), ties to the lower token;
-// take(t) for each.  The candidates' keys are staged in keys[T] while their first digit is counted
-// (one pass over global memory); when the threshold bin fits the list, one pass over the keys takes
-// every key above that bin and compacts the bin's keys with their tokens, and the rest runs on the
-// list.  Otherwise select_take runs on the staged keys.
+// take(t) for each.  A candidate's key is its score's bits, read from col (global memory: the transposed
+// scores, L2-resident after the transpose) at every pass rather than staged, so that the CTA's shared
+// memory is small enough for two CTAs per SM.  The first digit is counted over all candidates; when the
+// threshold bin fits the list, one pass takes every key above that bin and compacts the bin's keys with
+// their tokens, and the rest runs on the list.  Otherwise select_take runs over all the candidates.
 template <class Take>
-__device__ void select_take_unrouted(const float* col, const uint32_t* routed, int T, int need, uint32_t* keys,
-                                     uint32_t* list, int* list_tok, int* hist, int* s_res, Take take) {
+__device__ void select_take_unrouted(const float* col, const uint32_t* routed, int T, int need, uint32_t* list,
+                                     int* list_tok, int* hist, int* s_res, Take take) {
   const int tid = threadIdx.x, lane = tid & 31;
+  const auto key = [col, routed](int t) -> uint32_t {
+    return ((routed[t >> 5] >> (t & 31)) & 1u) ? 0xFFFFFFFFu : __float_as_uint(__ldg(col + t));
+  };
   for (int i = tid; i < 2048; i += kTrThreads) hist[i] = 0;
   __syncthreads();
 #pragma unroll 4
@@ -708,10 +715,8 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
     const int t = t0 + tid;
     uint32_t dg = 2048;
     if (t < T) {
-      const bool is_routed = (routed[t >> 5] >> (t & 31)) & 1u;
-      const uint32_t k = is_routed ? 0xFFFFFFFFu : __float_as_uint(__ldg(col + t));
-      keys[t] = k;
-      if (!is_routed) dg = k >> 21;
+      const uint32_t k = key(t);
+      if (k != 0xFFFFFFFFu) dg = k >> 21;
     }
     tr_count<2048>(hist, dg);
   }
@@ -719,8 +724,8 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
   uint32_t prefix = 0, mask = 0;
   int remaining = need;
   const int bin_cnt = tr_pick<2048>(hist, prefix, mask, 21, remaining, s_res);
-  if (bin_cnt > kTrListCap) {  // a crowded bin: the general select on the staged keys
-    select_take(keys, T, need, list, hist, s_res, take);
+  if (bin_cnt > kTrListCap) {  // a crowded bin: the general select over all the candidates
+    select_take(key, T, need, list, hist, s_res, take);
     return;
   }
   const uint32_t bin = prefix >> 21;
@@ -728,7 +733,7 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
   __syncthreads();
   for (int t0 = 0; t0 < T; t0 += kTrThreads) {
     const int t = t0 + tid;
-    const uint32_t k = t < T ? keys[t] : 0xFFFFFFFFu;
+    const uint32_t k = t < T ? key(t) : 0xFFFFFFFFu;
     const bool cand = k != 0xFFFFFFFFu;
     if (cand && (k >> 21) > bin) take(t);  // above the threshold bin: always in
     const bool in = cand && (k >> 21) == bin;
@@ -744,8 +749,9 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
   }
   __syncthreads();
   const int nlist = min(s_res[3], kTrListCap);
-  tr_digit<2048>(list, nlist, prefix, mask, 10, remaining, hist, s_res);
-  const int ties = tr_digit<1024>(list, nlist, prefix, mask, 0, remaining, hist, s_res);
+  const auto listed = [list](int i) { return list[i]; };
+  tr_digit<2048>(listed, nlist, prefix, mask, 10, remaining, hist, s_res);
+  const int ties = tr_digit<1024>(listed, nlist, prefix, mask, 0, remaining, hist, s_res);
   // prefix is now the threshold key: the list's keys above it are in, and `remaining` of its ties,
   // the lowest tokens first
   for (int i = tid; i < nlist; i += kTrThreads) {
@@ -762,13 +768,13 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
     }
   }
   if (ties == remaining || ties <= 256) return;
-  // many equal keys at the threshold: rank the ties in token order over the staged keys
+  // many equal keys at the threshold: rank the ties in token order over all the candidates
   __shared__ int s_wt[kTrThreads / 32];
   const int warp_id = tid >> 5;
   int tie_base = 0;
   for (int base = 0; base < T; base += kTrThreads) {
     const int t = base + tid;
-    const bool tie = t < T && keys[t] == prefix;
+    const bool tie = t < T && key(t) == prefix;
     const unsigned bal = __ballot_sync(0xffffffffu, tie);
     if (lane == 0) s_wt[warp_id] = __popc(bal);
     __syncthreads();
@@ -784,14 +790,13 @@ __device__ void select_take_unrouted(const float* col, const uint32_t* routed, i
   }
 }
 
-__global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __restrict__ scoresT, int T, int E,
+__global__ void __launch_bounds__(kTrThreads, 2) tr_select_kernel(const float* __restrict__ scoresT, int T, int E,
                                                               int m_tile, const int32_t* __restrict__ plain_off,
                                                               const int32_t* __restrict__ plain_tok,
                                                               long long plain_cap, uint32_t* __restrict__ member,
                                                               int* err) {
   extern __shared__ uint32_t tr_smem[];
-  uint32_t* keys = tr_smem;               // [T]; 0xFFFFFFFF = not a candidate
-  uint32_t* routed = tr_smem + T;         // [ceil(T/32)]
+  uint32_t* routed = tr_smem;             // [ceil(T/32)]
   uint32_t* list = routed + ((T + 31) >> 5);  // [kTrListCap] keys of the threshold bin
   int* list_tok = reinterpret_cast<int*>(list + kTrListCap);  // [kTrListCap] their tokens
   __shared__ int hist[2048];
@@ -828,17 +833,17 @@ __global__ void __launch_bounds__(kTrThreads) tr_select_kernel(const float* __re
   const float* col = scoresT + static_cast<long long>(e) * T;  // this expert's scores, token-contiguous
   if (drop) {
     // the candidates are the c routed tokens, in token order: select among them alone
-    for (int i = tid; i < c; i += kTrThreads) {
-      const int t = plain_tok[off + i];
-      keys[i] = (t >= 0 && t < T) ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
-    }
-    __syncthreads();
-    select_take(keys, c, need, list, hist, s_res, [&](int i) {
-      atomicOr(&member[static_cast<long long>(plain_tok[off + i]) * W + ew], ebit);
-    });
+    const int32_t* toks = plain_tok + off;
+    select_take(
+        [toks, col, T](int i) -> uint32_t {
+          const int t = __ldg(toks + i);
+          return (t >= 0 && t < T) ? __float_as_uint(__ldg(col + t)) : 0xFFFFFFFFu;
+        },
+        c, need, list, hist, s_res,
+        [&](int i) { atomicOr(&member[static_cast<long long>(plain_tok[off + i]) * W + ew], ebit); });
     return;
   }
-  select_take_unrouted(col, routed, T, need, keys, list, list_tok, hist, s_res, [&](int t) {
+  select_take_unrouted(col, routed, T, need, list, list_tok, hist, s_res, [&](int t) {
     atomicOr(&member[static_cast<long long>(t) * W + ew], ebit);
   });
 }
@@ -852,8 +857,7 @@ __global__ void __launch_bounds__(kTrThreads) cap_select_kernel(const int32_t* _
                                                                int T, int E, int C, int policy,
                                                                uint32_t* __restrict__ member, int* err) {
   extern __shared__ uint32_t cs_smem[];
-  uint32_t* keys = cs_smem;      // [T] probabilities of the expert's routed pairs, in token order
-  uint32_t* list = cs_smem + T;  // [kTrListCap]
+  uint32_t* list = cs_smem;  // [kTrListCap]
   __shared__ int hist[2048];
   __shared__ int s_res[4];
   const int e = blockIdx.x, tid = threadIdx.x;
@@ -875,9 +879,9 @@ __global__ void __launch_bounds__(kTrThreads) cap_select_kernel(const int32_t* _
     for (int i = tid; i < nk; i += kTrThreads) keep(i);
     return;
   }
-  for (int i = tid; i < c; i += kTrThreads) keys[i] = __float_as_uint(plain_w[off + i]);  // positive floats
-  __syncthreads();
-  select_take(keys, c, C, list, hist, s_res, keep);
+  // the keys: the routing probabilities of the expert's pairs in token order (positive floats order as their bits)
+  const float* pw = plain_w + off;
+  select_take([pw](int i) -> uint32_t { return __float_as_uint(__ldg(pw + i)); }, c, C, list, hist, s_res, keep);
 }
 
 // offsets of the capacity layout: expert e owns slots [e C, (e + 1) C); every slot is a row of the GEMMs.
@@ -1022,9 +1026,9 @@ cudaError_t launch_permute(const int32_t* topk_ids, const float* topk_w, const f
   // final token sets
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
-  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + (T + 31) / 32 + 2 * kTrListCap);
+  const size_t tr_smem = sizeof(uint32_t) * (static_cast<size_t>(T + 31) / 32 + 2 * kTrListCap);
   st = cudaFuncSetAttribute(tr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrMaxT / 32 + 2 * kTrListCap)));
+                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT / 32 + 2 * kTrListCap)));
   if (st != cudaSuccess) return st;
   transpose_f32_kernel<<<dim3((E + 31) / 32, (T + 31) / 32), dim3(32, 8), 0, s>>>(scores, T, E, w.scoresT);
   tr_select_kernel<<<E, kTrThreads, tr_smem, s>>>(w.scoresT, T, E, m_tile, w.plain_off, w.plain_tok, plain_cap,
@@ -1051,9 +1055,9 @@ cudaError_t launch_permute_capacity(const int32_t* topk_ids, const float* topk_w
   // kept pairs
   const size_t mbytes = sizeof(uint32_t) * static_cast<size_t>(T) * ((E + 31) / 32);
   if ((st = cudaMemsetAsync(w.member, 0, mbytes, s)) != cudaSuccess) return st;
-  const size_t sel_smem = sizeof(uint32_t) * (static_cast<size_t>(T) + kTrListCap);
+  const size_t sel_smem = sizeof(uint32_t) * kTrListCap;
   st = cudaFuncSetAttribute(cap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            static_cast<int>(sizeof(uint32_t) * (kTrMaxT + kTrListCap)));
+                            static_cast<int>(sizeof(uint32_t) * kTrListCap));
   if (st != cudaSuccess) return st;
   cap_select_kernel<<<E, kTrThreads, sel_smem, s>>>(w.plain_off, w.plain_tok, w.scoresT, plain_cap, T, E, C, policy,
                                                     w.member, err);
