@@ -97,6 +97,14 @@ def kernel_work(wl, P, dW_bytes=2):
                             + 2 * P * n + 2 * P * n // 32),
         "dx_gemm_mx": same(4 * P * d * n, 2 * P * n + 2 * P * n // 32 + 2 * E * d * n + 2 * E * d * n // 32
                            + 2 * P * d),
+        # block-scaled weight gradients: the four operands quantized along tokens in one launch (dH, dU, A' read
+        # as bf16 in the byte model, high and low parts moved; X and dO gathered, counted once per token), then
+        # the two varlen-K GEMMs on the codes and their scales (per-expert padding to 128 tokens not counted)
+        "quantize_cols_mx": (0, 6 * P * n + 4 * T * d + (3 * n + 2 * d) * P * 33 // 32,
+                             12 * P * n + 4 * P * d + (3 * n + 2 * d) * P * 33 // 32),
+        "mx_stage_offsets": same(0, 8 * E),
+        "dw_gate_up_mx": same(4 * P * d * n, (2 * n + d) * P * 33 // 32 + 2 * dWb * E * n * d),
+        "dw_down_mx": same(2 * P * d * n, (n + d) * P * 33 // 32 + dWb * E * d * n),
         "down_scale": same(2 * P * d * n, 2 * P * n + 2 * E * d * n + 2 * P * d),
         "down_scale_e4m3": same(2 * P * d * n, P * n + 4 * P + E * d * n + 4 * E * d + 2 * P * d),
         "quantize_a_e4m3": same(0, 3 * P * n + 4 * P),
@@ -239,7 +247,7 @@ _GEMM_LABELS = {
 }
 # the block-scaled form (template flag X_MX = 8)
 _MX_GEMM_LABELS = {(1, 1, 0, 1): "gate_up_swiglu_mx", (0, 0, 0, 2): "down_scale_mx", (0, 0, 0, 3): "dact_dswiglu_mx",
-                   (0, 0, 0, 0): "dx_gemm_mx"}
+                   (0, 0, 0, 0): "dx_gemm_mx", (0, 0, 1, 0): "dw_mx (gate/up, down)"}
 _OTHER_LABELS = {
     "topk_softmax_kernel": "topk_softmax", "perm_hist_kernel": "permute", "perm_scan_kernel": "permute",
     "perm_scatter_kernel": "permute", "tr_select_kernel": "permute", "transpose_f32_kernel": "permute",
@@ -251,6 +259,7 @@ _OTHER_LABELS = {
     "zero_tail_rows_kernel": "zero_tail", "quantize_rows_e4m3_kernel": "quantize_e4m3",
     "pad_offsets_kernel": "pad_offsets", "quantize_rows_mx_kernel": "quantize_mx",
     "quantize_weight_mx_kernel": "quantize_mx_weights", "mx_tile_scales_kernel": "mx_tile_scales",
+    "quantize_cols_mx_kernel": "quantize_cols_mx", "mx_stage_offsets_kernel": "mx_stage_offsets",
 }
 
 
@@ -296,8 +305,9 @@ def ncu_traffic(csv_path: str, workload: str) -> dict:
         label = _label_of(key[1])
         if label is None:
             continue
-        if label.startswith("dw_tiled"):  # every step launches dW gate/up, then dW down
-            label = "dw_gate_up" if dw_seen % 2 == 0 else "dw_down"
+        if label.startswith("dw_tiled") or label.startswith("dw_mx"):  # every step: dW gate/up, then dW down
+            sfx = "_mx" if label.startswith("dw_mx") else ""
+            label = ("dw_gate_up" if dw_seen % 2 == 0 else "dw_down") + sfx
             dw_seen += 1
         m = per[key]
         b = m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0)
@@ -526,6 +536,10 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
         vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx)
         vgg.backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx, bmx)
 
+    def mx_step_mx_dw():  # the weight gradients block-scaled too
+        vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx)
+        vgg.backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx, bmx, dw=True)
+
     def e4m3_step():
         vgg.forward_e4m3(ctx, X, W_r, bias, w8d, None, b8)
         vgg.backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8d, b8)
@@ -542,6 +556,7 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
             "mx": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx),
             "mx_infer": lambda: vgg.forward_mx(ctx, X, W_r, bias, wmx, bmx, cache=False),
             "mx_step": mx_step,
+            "mx_step_mx_dw": mx_step_mx_dw,
             # training steps
             "bf16_step": lambda: vgg.forward_backward(ctx, X, W_r, bias, W_gate, W_up, W_down, dO, buf),
             "e4m3_step": e4m3_step}
@@ -587,6 +602,8 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
     gmx, dmx = per("mx", "gate_up_swiglu_mx"), per("mx", "down_scale_mx")
     amx, xmx = per("mx_step", "dact_dswiglu_mx"), per("mx_step", "dx_gemm_mx")
     qmx = out["mx"][1].get("quantize_mx", (0.0, 1))
+    wgmx, wdmx = per("mx_step_mx_dw", "dw_gate_up_mx"), per("mx_step_mx_dw", "dw_down_mx")
+    qcmx = per("mx_step_mx_dw", "quantize_cols_mx")
     del b8, w8, w8d, bmx, wmx
     return {"forward_ms": out["e4m3"][0], "bf16_forward_ms": out["bf16"][0],
             "forward_e4m3_down_ms": out["e4m3_down8"][0],
@@ -611,10 +628,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                 "train_step_tflops": step_fl / (out["mx_step"][0] * 1e-3) / 1e12,
                 "dact_ms": amx, "dx_ms": xmx, "dact_tflops": fl_dn / (amx * 1e-3) / 1e12,
                 "dx_tflops": fl / (xmx * 1e-3) / 1e12,
+                "train_step_mx_dw_ms": out["mx_step_mx_dw"][0],
+                "mx_dw_gate_up_ms": wgmx, "mx_dw_down_ms": wdmx, "mx_dw_quantize_cols_ms": qcmx,
+                "mx_dw_tflops": (fl + fl_dn) / ((wgmx + wdmx) * 1e-3) / 1e12,
                 "recipe": "e4m3 codes with one power-of-two (UE8M0) scale per 32 values along the reduction "
                           "dimension of every operand row (kind::mxf8f6f4 UMMA); A quantized in the gate/up "
-                          "epilogue, [dH|dU] in the dSwiGLU epilogue; 192-column tiles; the training step's "
-                          "weight gradients and router stay bf16"},
+                          "epilogue, [dH|dU] in the dSwiGLU epilogue; 192-column tiles; the weight gradients and "
+                          "the router stay bf16; train_step_mx_dw_ms: the same step with block-scaled weight "
+                          "gradients (operands in blocks of 32 tokens of one expert, one quantizing launch)"},
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
             "recipe": "e4m3 operands with one fp32 scale per row: X per token, A, dO and [dH|dU] per pair, weights per "
                       "output channel of each GEMM; fp32 accumulation; dW and the router stay bf16",

@@ -382,8 +382,19 @@ int moe_quantize_bwd_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_
  *   blocks hu_sf (moe_mx_act_sf_bytes(cap,E,2n) bytes), both caller-owned;
  *   dXp[j,c]  = sum_k dq(HUq[j,k]) dq(Wgu_q[e,c,k])
  *
- * Wdt_q, wdt_sf, Wgu_q, wgu_sf from moe_quantize_bwd_weights_mx.  The router gradient, dX's reduction and the
- * weight gradients are those of moe_backward.  Arguments, shape rules, workspace and ownership otherwise as
+ * Wdt_q, wdt_sf, Wgu_q, wgu_sf from moe_quantize_bwd_weights_mx.  The router gradient and dX's reduction are
+ * those of moe_backward.  With dw_ws == NULL the weight gradients are moe_backward's (two-part bf16 operands).
+ * With dw_ws (caller-owned device scratch of at least moe_mx_dw_ws_bytes(d,E,n,cap) bytes, 256-byte aligned,
+ * overwritten) they run on block-scaled operands with the blocks along tokens: for expert e, with its sorted
+ * pairs j = offsets[e] + i split into blocks of 32 consecutive i (the last one partial), every operand column
+ * quantized per block by the rule above (dH, dU, A' from their fp32 values, X and dO from bf16, both read at
+ * the pairs' tokens):
+ *
+ *   dW_gate[e][r,c] = sum_i dq(dH[j,r]) dq(X[tok_j,c])     dW_up likewise with dU
+ *   dW_down[e][c,r] = sum_i dq(dO[tok_j,c]) dq(A'[j,r])
+ *
+ * accumulated in fp32 on the tensor cores; the expert-sorted bf16 copies of X and dO are then not made.
+ * [GG] "한계" (the fine-grained FP8 grouped GEMM); [SM] "4 기여 ②" (varlen-K weight gradients).  Arguments, shape rules, workspace and ownership otherwise as
  * moe_backward; MOE_ERR_UNSUPPORTED when the pair capacity is too small to stage dO's per-token codes in the
  * workspace (cap * 2d bytes must hold T * (d + 4 ceil(d/128)) plus alignment).
  */
@@ -393,8 +404,17 @@ int moe_backward_mx(moe_ctx* ctx, const void* dO, const void* X, const void* W_r
                     const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
                     const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* dOq,
                     void* do_sf_tiles, void* HUq, void* hu_sf, void* dX, void* dW_gate, void* dW_up, void* dW_down,
-                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
-                    moe_stream_t stream);
+                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* dw_ws,
+                    size_t dw_ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_mx_dw_ws_bytes — bytes of the workspace that moe_backward_mx takes (dw_ws) to run the weight gradients on
+ * block-scaled e4m3 operands, for a layer of hidden size d, E experts, intermediate size n and pair capacity cap
+ * (0 for an invalid shape: d, n multiples of 64, 1 <= E <= 1024, cap >= 1).  It holds the four operands as
+ * K-major codes over a reduction padded per expert to whole 128-token stages ((3n + 2d) x (cap + 127 E) bytes
+ * at most, rounded up to 128 tokens), their scale blocks and the stage offsets.
+ */
+size_t moe_mx_dw_ws_bytes(int d, int E, int n, long long cap);
 
 /*
  * moe_combine — weighted sum of every token's expert outputs, in original token order.

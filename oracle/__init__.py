@@ -22,6 +22,7 @@ from .moe_oracle import (  # noqa: F401
     combine_weights,
     dequantize_blocks_mx,
     dequantize_rows_e4m3,
+    dequantize_token_blocks_mx,
     e4m3_decode,
     e4m3_encode,
     e4m3_round,

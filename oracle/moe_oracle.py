@@ -368,7 +368,7 @@ def router_grad_rows(member, topk_ids, w_full, dw_full):
 
 
 def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp8_dx: bool = False,
-                 fp8_dact: bool = False, mx_dx: bool = False, mx_dact: bool = False):
+                 fp8_dact: bool = False, mx_dx: bool = False, mx_dact: bool = False, mx_dw: bool = False):
     """Backward of the layer given the forward cache.
 
     Returns dX, dW_gate, dW_up, dW_down (fp64, all experts or the listed ones),
@@ -382,6 +382,9 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
     ``mx_dx`` and ``mx_dact`` are the same two GEMMs with block-scaled operands (``quantize_blocks_mx``):
     [dH | dU] quantized from its exact value (blocks along 2n) against [W_gate; W_up]^T (blocks along 2n),
     and dO per token against W_down^T (blocks along d).
+    ``mx_dw``: the weight gradients with block-scaled operands whose blocks run along the expert's tokens
+    (``dequantize_token_blocks_mx``): dW_gate = dq(dH)^T dq(X), dW_up = dq(dU)^T dq(X) and
+    dW_down = dq(dO)^T dq(A') with A' = w a, every operand quantized from its exact value.
     """
     X, dO = _f64(X), _f64(dO)
     T, d = X.shape
@@ -422,7 +425,12 @@ def moe_backward(X, W_r, bias, W_gate, W_up, W_down, dO, cache, experts=None, fp
             np.add.at(dX, rows, dequantize_rows_e4m3(hq, hs) @ dequantize_rows_e4m3(bq, bs).T)
         else:
             np.add.at(dX, rows, g["dx"])
-        if e in dWg:
+        if e in dWg and mx_dw:
+            xt = dequantize_token_blocks_mx(X[rows])
+            dWg[e] = dequantize_token_blocks_mx(g["dh"]).T @ xt
+            dWu[e] = dequantize_token_blocks_mx(g["du"]).T @ xt
+            dWd[e] = dequantize_token_blocks_mx(dO[rows]).T @ dequantize_token_blocks_mx(w_full[rows, e][:, None] * g["a"])
+        elif e in dWg:
             dWg[e], dWu[e], dWd[e] = g["dWg"], g["dWu"], g["dWd"]
     dL = router_grad_rows(routing.member, routing.topk_ids, w_full, dw_full)
     Wr = _f64(W_r)
@@ -604,6 +612,20 @@ def dequantize_blocks_mx(codes, exps) -> np.ndarray:
     C = c.shape[-1]
     v = e4m3_decode(c).reshape(c.shape[:-1] + (C // MX_BLOCK, MX_BLOCK))
     return np.ldexp(v, np.asarray(exps, dtype=np.int64)[..., None]).reshape(c.shape)
+
+
+def dequantize_token_blocks_mx(M) -> np.ndarray:
+    """Block-scaled values of an expert's [rows, C] operand with the blocks along the rows (tokens): rows
+    32 b .. 32 b + 31 of one column form block b, the last block holding the rows left (its largest magnitude
+    over those rows alone; zero rows appended to make whole blocks change no block's maximum).  The reduction
+    of a weight gradient runs over an expert's tokens, so its 1 x 32 blocks are these."""
+    A = _f64(M)
+    R, C = A.shape
+    Rp = -(-R // MX_BLOCK) * MX_BLOCK
+    padded = np.zeros((Rp, C))
+    padded[:R] = A
+    q, e = quantize_blocks_mx(padded.T)  # [C, Rp]: blocks along the tokens
+    return dequantize_blocks_mx(q, e).T[:R]
 
 
 def moe_forward_mx(X, W_r, bias, W_gate, W_up, W_down, K: int, m_tile: int = 0, logits_for_routing=None,

@@ -100,8 +100,9 @@ def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None, skip=()):
         rep["dX"] = oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])
     for name, key in (("dW_gate", "dW_gate"), ("dW_up", "dW_up"), ("dW_down", "dW_down")):
         got = dev_to_f64(getattr(buf, name))
-        ref = np.stack([grads[key][e] for e in range(E)])
-        rep[name] = oracle.compare(name, got, ref, param_axes=oracle.WEIGHT_GRAD)
+        if name not in skip:
+            ref = np.stack([grads[key][e] for e in range(E)])
+            rep[name] = oracle.compare(name, got, ref, param_axes=oracle.WEIGHT_GRAD)
         empty = np.nonzero(r.counts == 0)[0]
         assert not np.any(got[empty]), f"{name}: experts without pairs must get exactly zero"
     dS_ref = grads["dw"][r.sorted_tok, r.sorted_exp]

@@ -228,13 +228,57 @@ BWD_CASES = [
 ]
 
 
+def _token_block_slack(M, rel=0.0, amax_frac=0.0):
+    """An expert's [rows, C] operand (exact values) quantized in blocks of 32 tokens of one column: the oracle's
+    block-scaled values, and per element the slack that a device value within rel |x| + amax_frac amax of x
+    (amax: the block's largest magnitude) allows in its dequantized value.  Zero where every such value gets
+    the same code under the same block exponent; one code step (plus the deviation) where the code may be the
+    neighbouring one; two steps of the coarser exponent where the block's exponent itself may differ by one.
+    rel = amax_frac = 0 (operands the device reads as the same bf16 values): no slack."""
+    A = np.asarray(M, dtype=np.float64)
+    R, C = A.shape
+    Rp = -(-R // 32) * 32
+    pad = np.zeros((Rp, C))
+    pad[:R] = A
+    B = pad.T.reshape(C, Rp // 32, 32)
+    amax = np.abs(B).max(axis=-1)
+    e = oracle.mx_block_exponents(amax)
+    sc = np.exp2(e.astype(np.float64))[..., None]
+    q = oracle.e4m3_round(B / sc) * sc
+    dev = rel * np.abs(B) + amax_frac * amax[..., None]
+    amb = oracle.e4m3_round((B - dev) / sc) != oracle.e4m3_round((B + dev) / sc)
+    da = (rel + amax_frac) * amax
+    blk = (oracle.mx_block_exponents(np.maximum(amax - da, 0.0)) != e) | (oracle.mx_block_exponents(amax + da) != e)
+    step = 2.0 ** -3 * (np.abs(B) + dev) + 2.0 ** -9 * sc
+    slack = np.where(amb, step + dev, 0.0)
+    slack = np.where(blk[..., None], 2 * step + 2.0 ** -9 * sc + dev, slack)
+    back = lambda Z: Z.reshape(C, Rp).T[:R]
+    return back(q), back(slack)
+
+
+def _check_mx_dw(got, Aq, As, Bq, Bs, name):
+    """got = sum over the expert's tokens of dq(A)^T dq(B) on the device: within fp32 accumulation of the
+    oracle's product of its block-scaled operands, plus what the operands' slack (``_token_block_slack``)
+    allows.  Returns the summed slack, the summed magnitude sum |dq(A)| |dq(B)| and the worst error relative to
+    the bound."""
+    mag = np.abs(Aq).T @ np.abs(Bq)
+    ref = Aq.T @ Bq
+    slack = As.T @ (np.abs(Bq) + Bs) + np.abs(Aq).T @ Bs
+    bound = 2.0 ** -14 * mag + slack + 1e-30
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), (name, float(np.max(err / bound)), float(np.max(err)))
+    return float(slack.sum()), float(mag.sum()), float(np.max(err / bound))
+
+
 def _act_exps(sf: torch.Tensor, offsets: np.ndarray, cols: int, rows: np.ndarray) -> np.ndarray:
     return _unpack_act_blocks(sf.cpu().numpy(), offsets, cols, rows)
 
 
-@pytest.mark.parametrize("wl", BWD_CASES, ids=lambda w: w.name)
-def test_mx_backward_matches_oracle(ctx, wl):
-    """moe_backward_mx against the oracle's backward with both activation-gradient GEMMs block-scaled:
+@pytest.mark.parametrize("wl,dw", [(w, True) for w in BWD_CASES] + [(BWD_CASES[0], False)],
+                         ids=lambda v: v.name if hasattr(v, "name") else ("mx_dw" if v else "bf16_dw"))
+def test_mx_backward_matches_oracle(ctx, wl, dw):
+    """moe_backward_mx against the oracle's backward with both activation-gradient GEMMs block-scaled and, with
+    ``dw``, the weight gradients on operands quantized in blocks of 32 tokens of one expert (else two-part bf16):
     * the weight codes and scale blocks (W_down^T and [W_gate; W_up]^T) bit for bit, padding included;
     * the sorted dO codes and their scale blocks bit for bit (decided on the exact bf16 dO);
     * the [dH | dU] codes, which the dSwiGLU epilogue quantizes from its fp32 values, against the oracle's
@@ -253,7 +297,7 @@ def test_mx_backward_matches_oracle(ctx, wl):
     buf.mdosft.fill_(255)
     wmx = vgg.MxWeights.quantize(ctx, dv["W_gate"], dv["W_up"], dv["W_down"], backward=True)
     vgg.forward(ctx, dv["X"], dv["W_r"], dv["bias"], dv["W_gate"], dv["W_up"], dv["W_down"], buf)
-    vgg.backward_mx(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], wmx, buf)
+    vgg.backward_mx(ctx, dv["dO"], dv["X"], dv["W_r"], dv["W_gate"], dv["W_up"], dv["W_down"], wmx, buf, dw=dw)
     rc, code = vgg.moe_get_error(ctx)
     assert rc == vgg.MOE_OK and code == 0, (rc, code)
 
@@ -274,7 +318,7 @@ def test_mx_backward_matches_oracle(ctx, wl):
                                   logits_for_routing=g["logits"], scores_for_routing=g["scores"], capacity=C,
                                   policy=wl.drop_policy, drop_keys=g["topk_w"] if C else None)
     grads = mo.moe_backward(inp.X, inp.W_r, inp.bias, inp.W_gate, inp.W_up, inp.W_down, inp.dO, cache,
-                            mx_dx=True, mx_dact=True)
+                            mx_dx=True, mx_dact=True, mx_dw=dw)
     r = cache["routing"]
     if C:
         rows = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(E)]).astype(np.int64)
@@ -290,6 +334,11 @@ def test_mx_backward_matches_oracle(ctx, wl):
     # [dH | dU] codes against the oracle's quantization of its exact values
     X64, dO64 = mo.bf16_bits_to_f64(inp.X), mo.bf16_bits_to_f64(inp.dO)
     hu_ref = np.zeros((r.P, 2 * n))
+    # block-scaled weight gradients: every element within fp32 accumulation of the oracle's block-scaled product,
+    # plus the slack of operand values (dH, dU, A', which the device computes in fp32) that lie within the
+    # device's deviation of a rounding boundary; X and dO are the same bf16 values on both sides (no slack)
+    dw_rep = {"slack": 0.0, "magnitude": 0.0, "worst": 0.0}
+    dev_dw = {k: dev_to_f64(getattr(buf, k)) for k in ("dW_gate", "dW_up", "dW_down")} if dw else None
     for e in range(E):
         lo, hi = r.offsets[e], r.offsets[e + 1]
         if hi == lo:
@@ -301,6 +350,29 @@ def test_mx_backward_matches_oracle(ctx, wl):
         blk = mo.expert_block_backward(X64[toks], dO64[toks], cache["w_full"][toks, e], inp.W_gate[e], inp.W_up[e],
                                        inp.W_down[e], dap=dap)
         hu_ref[lo:hi] = np.concatenate([blk["dh"], blk["du"]], axis=1)
+        if dw:
+            xq, xs = _token_block_slack(X64[toks])
+            oq, os_ = _token_block_slack(dO64[toks])
+            ops = (("dW_gate", blk["dh"], X64), ("dW_up", blk["du"], X64))
+            for name, G, _ in ops:
+                gq, gs = _token_block_slack(G, 2.0 ** -14, 2.0 ** -16)
+                sl, mg, worst = _check_mx_dw(dev_dw[name][e], gq, gs, xq, xs, name)
+                np.testing.assert_allclose(gq.T @ xq, grads[name][e], rtol=1e-9, atol=1e-12)
+                dw_rep["slack"] += sl
+                dw_rep["magnitude"] += mg
+                dw_rep["worst"] = max(dw_rep["worst"], worst)
+            aq, as_ = _token_block_slack(cache["w_full"][toks, e][:, None] * blk["a"], 2.0 ** -14, 2.0 ** -16)
+            sl, mg, worst = _check_mx_dw(dev_dw["dW_down"][e], oq, os_, aq, as_, "dW_down")
+            np.testing.assert_allclose(oq.T @ aq, grads["dW_down"][e], rtol=1e-9, atol=1e-12)
+            dw_rep["slack"] += sl
+            dw_rep["magnitude"] += mg
+            dw_rep["worst"] = max(dw_rep["worst"], worst)
+    if dw:
+        # the slack is a small part of the bound: summed over all elements it stays below 1% of the summed
+        # magnitudes of the products (a few operand values near a boundary, one code step each)
+        assert dw_rep["slack"] <= 1e-2 * dw_rep["magnitude"], dw_rep
+        for k in ("dW_gate", "dW_up", "dW_down"):
+            assert not np.any(dev_dw[k][r.counts == 0]), f"{k}: experts without pairs must get exactly zero"
     hq_ref, he_ref = oracle.quantize_blocks_mx(hu_ref)
     hq = buf.mhuq.cpu().numpy()[rows]
     he = _act_exps(buf.mhusf, offs, 2 * n, rows)
@@ -315,15 +387,18 @@ def test_mx_backward_matches_oracle(ctx, wl):
     if C:
         rep = {"O": oracle.compare("O", dev_to_f64(buf.O), O_ref),
                "dX": oracle.compare("dX", dev_to_f64(buf.dX), grads["dX"])}
-        for name in ("dW_gate", "dW_up", "dW_down"):
+        for name in () if dw else ("dW_gate", "dW_up", "dW_down"):
             rep[name] = oracle.compare(name, dev_to_f64(getattr(buf, name)), np.stack([grads[name][e] for e in range(E)]),
                                        param_axes=oracle.WEIGHT_GRAD)
         rep["dS"] = oracle.compare("dS", dev_to_f64(buf.dS)[rows], grads["dw"][r.sorted_tok, r.sorted_exp])
         rep["dlogits"] = oracle.compare("dlogits", dev_to_f64(buf.dlogits), grads["dlogits"])
         rep["dW_r"] = oracle.compare("dW_r", dev_to_f64(buf.dW_r), grads["dW_r"])
     else:
-        rep = compare_layer(buf, inp, O_ref, cache, grads)
-    print(wl.name, "[dH|dU] codes differing:", int(bad.sum()), "of", hq.size,
+        rep = compare_layer(buf, inp, O_ref, cache, grads, skip=("dW_gate", "dW_up", "dW_down") if dw else ())
+    if dw:
+        print(wl.name, "block-scaled dW: slack / magnitude", dw_rep["slack"] / dw_rep["magnitude"],
+              "worst error / bound", round(dw_rep["worst"], 4))
+    print(wl.name, "mx_dw" if dw else "bf16_dw", "[dH|dU] codes differing:", int(bad.sum()), "of", hq.size,
           {k: (round(v["max"], 5), round(v["mean"], 6)) for k, v in rep.items()})
 
 

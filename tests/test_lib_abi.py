@@ -66,6 +66,28 @@ def test_block_scale_size_queries(libpath):
     assert L.moe_mx_act_sf_bytes(0, 3, 64) == 0
 
 
+def test_block_scaled_weight_gradient_workspace_size(libpath):
+    """moe_mx_dw_ws_bytes by the stated layout: the stage offsets, the four K-major code matrices over the
+    padded reduction (cap + 127 E tokens rounded up to 128) and their scale blocks, each region 256-aligned."""
+    import varlen_grouped_gemm_gb300 as vgg
+    L = vgg.lib()
+    al = lambda x: (x + 255) // 256 * 256
+
+    def want(d, E, n, cap, bn_gu, bn_dn):
+        kq = -(-(cap + 127 * E) // 128) * 128
+        kst = kq // 128
+        codes = al(2 * n * kq) + al(d * kq) + al(d * kq) + al(n * kq)
+        blocks = (al(512 * kst * -(-2 * n // 128)) + al(512 * kst * -(-d // bn_gu) * -(-bn_gu // 128)) +
+                  al(512 * kst * -(-d // 128)) + al(512 * kst * -(-n // bn_dn) * -(-bn_dn // 128)))
+        return al(4 * (E + 1)) + codes + blocks
+
+    assert L.moe_mx_dw_ws_bytes(2048, 128, 512, 32768) == want(2048, 128, 512, 32768, 192, 192)
+    assert L.moe_mx_dw_ws_bytes(1536, 512, 256, 32768 * 8 + 512 * 64) == want(1536, 512, 256, 294912, 192, 128)
+    assert L.moe_mx_dw_ws_bytes(2880, 128, 2880, 32768) == want(2880, 128, 2880, 32768, 192, 192)
+    for bad in ((2000, 8, 64, 100), (64, 0, 64, 100), (64, 8, 64, 0), (64, 2000, 64, 100)):
+        assert L.moe_mx_dw_ws_bytes(*bad) == 0, bad
+
+
 def test_expert_capacity_matches_the_oracle(libpath):
     """The capacity dispatch's slot count C = ceil(cf T K / E) comes from the library (the binding does no
     arithmetic); it equals the oracle's reading on a grid that includes exact multiples and fractions."""

@@ -813,6 +813,79 @@ def test_mx_backward_gemms_within_quantization_bound():
     assert np.all(err <= bound * (1 + 1e-9) + 1e-12) and np.max(err) > 0
 
 
+def _token_blocks_brute(M):
+    """Block-scaled values with 1 x 32 blocks down each column (the last block partial), written out
+    element by element: the block's exponent by search over every admissible e, the code by torch's
+    float8_e4m3fn conversion of the exactly scaled value."""
+    M = np.asarray(M, dtype=np.float64)
+    R, C = M.shape
+    out = np.zeros_like(M)
+    grid = np.arange(-127, 128)
+    for c in range(C):
+        for b0 in range(0, R, 32):
+            blk = M[b0:b0 + 32, c]
+            amax = np.max(np.abs(blk))
+            e = 0 if amax == 0 else grid[amax <= 448.0 * np.exp2(grid.astype(np.float64))][0]
+            y = torch.from_numpy(np.ldexp(blk, -int(e)).astype(np.float32)).to(torch.float8_e4m3fn)
+            out[b0:b0 + 32, c] = np.ldexp(y.to(torch.float64).numpy(), int(e))
+    return out
+
+
+def test_mx_token_blocks_match_brute_force():
+    # blocks of 32 rows of one column, the last one over the 13 rows left; magnitudes differ per column and an
+    # all-zero block and a block far below 1 are included
+    rng = np.random.default_rng(27)
+    M = rng.standard_normal((45, 6)) * np.exp2(rng.integers(-12, 12, (1, 6)))
+    M[:32, 2] = 0.0
+    M[32:, 4] *= 1e-25
+    got = oracle.dequantize_token_blocks_mx(M)
+    np.testing.assert_array_equal(got, _token_blocks_brute(M))
+    assert np.max(np.abs(got - M)) > 0
+    # a block's scale depends on its own rows alone: a large value in row 40 leaves rows 0..31 unchanged
+    M2 = M.copy()
+    M2[40, :] = 1e6
+    np.testing.assert_array_equal(oracle.dequantize_token_blocks_mx(M2)[:32], got[:32])
+
+
+def test_mx_weight_gradients_token_blocks_and_bound():
+    # mx_dw: every expert's dW_gate, dW_up, dW_down equal the products of its operands quantized by the
+    # brute-force token blocks (blocks starting at the expert's first row), lie within the element-wise
+    # quantization bound of the exact gradients, and the other gradients are the exact backward's
+    rng = np.random.default_rng(28)
+    T, d, E, n, K = 96, 64, 4, 32, 2
+    X = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, n, d)) * 0.1
+    Wu = rng.standard_normal((E, n, d)) * 0.1
+    Wd = rng.standard_normal((E, d, n)) * 0.1
+    W_r = rng.standard_normal((d, E)) * 0.3
+    dO = rng.standard_normal((T, d))
+    O, cache = mo.moe_forward(X, W_r, None, Wg, Wu, Wd, K)
+    g = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache)
+    gw = mo.moe_backward(X, W_r, None, Wg, Wu, Wd, dO, cache, mx_dw=True)
+    for k in ("dX", "dW_r", "dlogits", "dw"):
+        np.testing.assert_array_equal(gw[k], g[k])
+    r, w = cache["routing"], cache["w_full"]
+    seen_ragged = False
+    for e in range(E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        seen_ragged |= len(rows) % 32 != 0 and len(rows) > 32
+        blk = mo.expert_block_backward(X[rows], dO[rows], w[rows, e], Wg[e], Wu[e], Wd[e])
+        ap = w[rows, e][:, None] * blk["a"]
+        qx = _token_blocks_brute(X[rows])
+        pairs = ((gw["dW_gate"][e], g["dW_gate"][e], blk["dh"], X[rows], qx),
+                 (gw["dW_up"][e], g["dW_up"][e], blk["du"], X[rows], qx),
+                 (gw["dW_down"][e], g["dW_down"][e], dO[rows], ap, _token_blocks_brute(ap)))
+        for got, exact, A, B, qB in pairs:
+            np.testing.assert_allclose(got, _token_blocks_brute(A).T @ qB, rtol=1e-12, atol=1e-13)
+            da, db = (np.abs(_token_blocks_brute(M) - M) for M in (A, B))
+            bound = np.abs(A).T @ db + da.T @ np.abs(B) + da.T @ db
+            err = np.abs(got - exact)
+            assert np.all(err <= bound * (1 + 1e-9) + 1e-13) and np.max(err) > 0
+    assert seen_ragged  # an expert with a partial last block
+
+
 # ---------------------------------------------------------------- the metric
 
 

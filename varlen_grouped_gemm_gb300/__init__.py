@@ -32,6 +32,7 @@ EXPORTS = (
     "moe_expert_capacity", "moe_test_gemm_varlen_k_dual", "moe_test_gemm_varlen_m_dual",
     "moe_mx_sf_cols", "moe_mx_weight_sf_bytes", "moe_mx_act_sf_bytes", "moe_quantize_rows_mx",
     "moe_quantize_weights_mx", "moe_grouped_gemm_fwd_mx", "moe_quantize_bwd_weights_mx", "moe_backward_mx",
+    "moe_mx_dw_ws_bytes",
 )
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_DEVICE_TIMEOUT = range(6)
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.moe_mx_weight_sf_bytes.restype = _LL
         L.moe_mx_act_sf_bytes.argtypes = [_LL, _I, _I]
         L.moe_mx_act_sf_bytes.restype = _LL
+        L.moe_mx_dw_ws_bytes.argtypes = [_I, _I, _I, _LL]
+        L.moe_mx_dw_ws_bytes.restype = _SZ
         L.moe_quantize_rows_mx.argtypes = [_P, _P, _LL, _I, _P, _P, _P]
         L.moe_quantize_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
         L.moe_grouped_gemm_fwd_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _LL, _P, _P, _P, _P,
@@ -103,7 +106,7 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_bwd_weights_mx.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
         L.moe_backward_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _LL, _P, _P,
                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
-                                      _SZ, _P]
+                                      _SZ, _P, _SZ, _P]
         L.moe_profile_enable.argtypes = [_P, _I]
         L.moe_profile_read.argtypes = [_P, _I, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
                                        ctypes.POINTER(_LL), ctypes.POINTER(_I)]
@@ -319,6 +322,14 @@ def mx_weight_sf_bytes(E: int, d: int, n: int, which: int) -> int:
     return b
 
 
+def mx_dw_ws_bytes(d: int, E: int, n: int, cap: int) -> int:
+    """Bytes of the block-scaled weight gradients' workspace (``moe_mx_dw_ws_bytes``)."""
+    b = int(lib().moe_mx_dw_ws_bytes(d, E, n, cap))
+    if b <= 0:
+        raise ValueError(f"moe_mx_dw_ws_bytes: invalid arguments d={d} E={E} n={n} cap={cap}")
+    return b
+
+
 def mx_act_sf_bytes(cap: int, E: int, n: int) -> int:
     """Bytes of the activation scale blocks of the block-scaled down projection."""
     b = int(lib().moe_mx_act_sf_bytes(cap, E, n))
@@ -524,6 +535,7 @@ class Buffers:
     mdosft: torch.Tensor | None = None  # [dH | dU] codes [cap, 2n] and their scale blocks
     mhuq: torch.Tensor | None = None
     mhusf: torch.Tensor | None = None
+    mdw: torch.Tensor | None = None  # block-scaled weight gradients' workspace (moe_mx_dw_ws_bytes), on first use
 
     @staticmethod
     def allocate(T, d, E, n, K, m_tile=0, backward=True, dW_dtype=torch.bfloat16, device="cuda", capacity=0,
@@ -724,9 +736,12 @@ def forward_mx(ctx, X, W_r, bias, wmx: MxWeights, buf: Buffers, stream=None, cac
     moe_combine(ctx, buf.Yw, buf.tok_ptr, buf.tok_pairs, buf.O, stream)
 
 
-def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buffers, stream=None):
+def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buffers, stream=None, dw=False):
     """The backward with the dSwiGLU and dX GEMMs on block-scaled operands (``wmx`` quantized with
-    ``backward=True``, ``buf`` allocated with ``mx=True``); the weight gradients stay bf16."""
+    ``backward=True``, ``buf`` allocated with ``mx=True``); with ``dw`` the weight gradients too (blocks of 32
+    tokens of one expert), else they stay two-part bf16.  The block-scaled weight gradients are slower on one
+    GB300 (c2 step 1.21 against 1.02 ms): the GEMMs are bound by storing the gradients, not by the tensor
+    cores, and their operands take a transposing quantization pass."""
     if wmx.Wdt_q is None or buf.mhuq is None:
         raise ValueError("block-scaled backward needs MxWeights.quantize(..., backward=True) and Buffers(mx=True)")
     T, d = X.shape
@@ -735,6 +750,8 @@ def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buff
     wp, wb = _ws(buf.ws)
     bf, u8, f32, i32 = torch.bfloat16, torch.uint8, torch.float32, torch.int32
     dw_fp32 = 1 if buf.dW_gate.dtype == f32 else 0
+    if dw and buf.mdw is None:
+        buf.mdw = torch.empty(mx_dw_ws_bytes(d, E, n, cap), dtype=u8, device=dO.device)
     _check("moe_backward_mx", lib().moe_backward_mx(
         ctx.handle, _ptr(dO, bf), _ptr(X, bf), _ptr(W_r, bf), _ptr(W_gate, bf), _ptr(W_up, bf), _ptr(W_down, bf),
         _ptr(wmx.Wdt_q, u8), _ptr(wmx.wdt_sf, u8), _ptr(wmx.Wgu_q, u8), _ptr(wmx.wgu_sf, u8), T, d, E, n, buf.K,
@@ -742,7 +759,8 @@ def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buff
         _ptr(buf.sorted_tok, i32), _ptr(buf.sorted_w, f32), _ptr(buf.tok_ptr, i32), _ptr(buf.tok_pairs, i32),
         _ptr(buf.H, f32), _ptr(buf.U, f32), _ptr(buf.mdoq, u8), _ptr(buf.mdosft, u8), _ptr(buf.mhuq, u8),
         _ptr(buf.mhusf, u8), _ptr(buf.dX, bf), _ptr(buf.dW_gate), _ptr(buf.dW_up), _ptr(buf.dW_down), dw_fp32,
-        _ptr(buf.dS, f32), _ptr(buf.dlogits, f32), _ptr(buf.dW_r, f32), wp, wb, _stream(stream)))
+        _ptr(buf.dS, f32), _ptr(buf.dlogits, f32), _ptr(buf.dW_r, f32), wp, wb,
+        _ptr(buf.mdw, u8) if dw else None, buf.mdw.numel() if dw else 0, _stream(stream)))
 
 
 def backward_e4m3(ctx, dO, X, W_r, W_gate, W_up, W_down, w8: E4m3Weights, buf: Buffers, stream=None, dx=True,

@@ -764,6 +764,51 @@ long long moe_mx_act_sf_bytes(long long cap, int E, int n) {
   return 512ll * (ceil_div(cap, BM) + E) * ceil_div(n, 128);
 }
 
+namespace vgg {
+// The block-scaled weight gradients' workspace: the padded stage offsets, then the K-major code matrices of the
+// two GEMMs' operands ([dH | dU]^T [2n][kq], X^T [d][kq], dO^T [d][kq], A'^T [n][kq]; kq = the padded reduction's
+// capacity in tokens) and their scale blocks (A operands per 128-row tile, B operands per column tile of the
+// GEMM, each per 128-token stage).  With base == nullptr only the size is computed.
+struct MxDwWs {
+  int32_t* kp;
+  uint8_t *gu_a, *gu_b, *dn_a, *dn_b;
+  uint8_t *gu_a_sf, *gu_b_sf, *dn_a_sf, *dn_b_sf;
+  long long kq;
+  int kst, bn_gu, bn_dn;
+  size_t bytes;
+};
+static MxDwWs carve_mx_dw(void* base, int d, int E, int n, long long cap) {
+  MxDwWs w{};
+  w.kq = (cap + 127ll * E + 127) / 128 * 128;
+  w.kst = static_cast<int>(w.kq / 128);
+  w.bn_gu = mx_tile_cols(d);
+  w.bn_dn = mx_tile_cols(n);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* ptr = base ? static_cast<uint8_t*>(base) + o : nullptr;
+    o += al(bytes);
+    return ptr;
+  };
+  const size_t kq = static_cast<size_t>(w.kq), kst = static_cast<size_t>(w.kst);
+  w.kp = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+  w.gu_a = take(2 * static_cast<size_t>(n) * kq);
+  w.gu_b = take(static_cast<size_t>(d) * kq);
+  w.dn_a = take(static_cast<size_t>(d) * kq);
+  w.dn_b = take(static_cast<size_t>(n) * kq);
+  w.gu_a_sf = take(512 * kst * ceil_div(2 * n, BM));
+  w.gu_b_sf = take(512 * kst * ceil_div(d, w.bn_gu) * mx_b_blocks(w.bn_gu));
+  w.dn_a_sf = take(512 * kst * ceil_div(d, BM));
+  w.dn_b_sf = take(512 * kst * ceil_div(n, w.bn_dn) * mx_b_blocks(w.bn_dn));
+  w.bytes = o;
+  return w;
+}
+}  // namespace vgg
+
+size_t moe_mx_dw_ws_bytes(int d, int E, int n, long long cap) {
+  if (cap < 1 || E < 1 || E > kMaxGroups || d < 64 || d % 64 || n < 64 || n % 64) return 0;
+  return carve_mx_dw(nullptr, d, E, n, cap).bytes;
+}
+
 int moe_quantize_rows_mx(moe_ctx* ctx, const void* M, long long rows, int cols, void* q, void* sf,
                          moe_stream_t stream) {
   VGG_REQUIRE(ctx && M && q && sf);
@@ -905,6 +950,7 @@ struct MxBwd {
   void* do_sf_tiles;
   void* HUq;
   void* hu_sf;
+  void* dw_ws;  // the block-scaled weight gradients' workspace (moe_mx_dw_ws_bytes), or null: two-part bf16
 };
 
 // The backward; with Wgu_q the dX GEMM runs on e4m3 operands (moe_backward_e4m3), with mx both activation-gradient
@@ -966,13 +1012,17 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   // expert-sorted copies of X and dO (and of dO's codes): every backward GEMM then reads whole TMA boxes.  The
   // bf16 copies are padded per expert to multiples of 16 rows (zero rows), except when the e4m3 dSwiGLU GEMM
   // quantizes the sorted dO rows themselves (a capacity layout with fewer slots than tokens).
-  const bool padded = mx || !(Wdt_q && !dact_tok);
+  // With the block-scaled weight gradients (which read X and dO through the token index) only the code rows are
+  // copied.
+  const bool mx_dw = mx && mx->dw_ws;
+  const bool padded = !mx_dw && (mx || !(Wdt_q && !dact_tok));
   const long long cap_pad = padded ? padded_rows(cap, E) : cap;
   const int32_t* poff = padded ? w.poff : nullptr;
   if (padded) VGG_LAUNCH("pad_offsets", launch_pad_offsets(offsets, E, w.poff, ctx->d_err, s));
   VGG_LAUNCH("gather_rows", launch_gather_rows(offsets, poff, cap_pad, E, sorted_tok, tok_ptr, tok_pairs, cap, T, d,
                                                static_cast<const __nv_bfloat16*>(X),
-                                               static_cast<const __nv_bfloat16*>(dO), w.Xs, w.dOs,
+                                               static_cast<const __nv_bfloat16*>(dO), mx_dw ? nullptr : w.Xs,
+                                               mx_dw ? nullptr : w.dOs,
                                                mx ? mq : (dact_tok ? tq : nullptr), dact_tok ? ts : nullptr,
                                                static_cast<uint8_t*>(mx ? mx->dOq : dOq), mx ? nullptr : do_scale,
                                                ctx->d_err, ctx->num_sms, ctx->timeout_ns, s));
@@ -1210,6 +1260,77 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   }
   if (fork && cudaEventRecord(ctx->join, s) != cudaSuccess) return MOE_ERR_CUDA;
   s = s_main;
+  if (mx_dw) {
+    // block-scaled weight gradients: blocks of 32 tokens of one expert along each operand column.  One launch
+    // writes the four operands transposed (K-major codes over the per-expert stages) with their scale blocks,
+    // from dH, dU and A' (high + low parts) at the sorted positions and from X and dO through the token index.
+    const MxDwWs v = carve_mx_dw(mx->dw_ws, d, E, n, cap);
+    VGG_LAUNCH("mx_stage_offsets", launch_mx_stage_offsets(offsets, E, v.kp, ctx->d_err, s));
+    MxColJobs jobs{};
+    jobs.job[0] = MxColJob{w.dH, w.dH_lo, nullptr, cap, n, n, 0, v.gu_a, v.gu_a_sf, BM};
+    jobs.job[1] = MxColJob{w.dU, w.dU_lo, nullptr, cap, n, n, n, v.gu_a, v.gu_a_sf, BM};
+    jobs.job[2] = MxColJob{static_cast<const __nv_bfloat16*>(X), nullptr, sorted_tok, T, d, d, 0, v.gu_b, v.gu_b_sf,
+                           v.bn_gu};
+    jobs.job[3] = MxColJob{static_cast<const __nv_bfloat16*>(dO), nullptr, sorted_tok, T, d, d, 0, v.dn_a, v.dn_a_sf,
+                           BM};
+    jobs.job[4] = MxColJob{w.Ap, w.Ap_lo, nullptr, cap, n, n, 0, v.dn_b, v.dn_b_sf, v.bn_dn};
+    // scale bytes of operand rows that no job writes (past M or N in a tile) hold 127 (scale 1)
+    VGG_CUDA(cudaMemsetAsync(v.gu_a_sf, 127, static_cast<size_t>(static_cast<uint8_t*>(mx->dw_ws) + v.bytes - v.gu_a_sf),
+                             s));
+    VGG_LAUNCH("quantize_cols_mx", launch_quantize_cols_mx(jobs, 5, offsets, v.kp, E, cap, v.kq, v.kst, ctx->d_err,
+                                                           s));
+    // [dW_gate; dW_up][e] = [dH | dU]^T X over the expert's stages (M = 2n, N = d)
+    {
+      GemmParams p = base_params(ctx);
+      p.M = 2 * n;
+      p.N = d;
+      p.K = static_cast<int>(v.kq / 2);
+      p.groups = E;
+      p.offsets = v.kp;
+      p.rows_cap = static_cast<int>(v.kq / 2);
+      p.out0 = dW_gate;
+      p.out1 = dW_up;
+      p.out_rows_split = n;
+      p.ld_out = d;
+      p.a_sf = v.gu_a_sf;
+      p.b_sf = v.gu_b_sf;
+      p.sf_kst = v.kst;
+      Maps m = zero_maps();
+      if (!make_map_2d(&m.a0, v.gu_a, v.kq / 2, 2 * n, v.kq / 2, BM) ||
+          !make_map_3d(&m.b0, v.gu_b, v.kq / 2, d, 1, v.bn_gu) ||
+          !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) || !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
+        return MOE_ERR_CUDA;
+      m.a1 = m.a0;
+      m.b1 = m.b0;
+      const long long tiles = static_cast<long long>(E) * ceil_div(2 * n, BM) * ceil_div(d, v.bn_gu);
+      VGG_LAUNCH("dw_gate_up_mx", run_dw_mx(v.bn_gu, f32, p, m, static_cast<int>(std::min<long long>(tiles, ctx->num_sms)), s));
+    }
+    // dW_down[e] = dO^T A' over the expert's stages (M = d, N = n)
+    {
+      GemmParams p = base_params(ctx);
+      p.M = d;
+      p.N = n;
+      p.K = static_cast<int>(v.kq / 2);
+      p.groups = E;
+      p.offsets = v.kp;
+      p.rows_cap = static_cast<int>(v.kq / 2);
+      p.out0 = dW_down;
+      p.ld_out = n;
+      p.a_sf = v.dn_a_sf;
+      p.b_sf = v.dn_b_sf;
+      p.sf_kst = v.kst;
+      Maps m = zero_maps();
+      if (!make_map_2d(&m.a0, v.dn_a, v.kq / 2, d, v.kq / 2, BM) ||
+          !make_map_3d(&m.b0, v.dn_b, v.kq / 2, n, 1, v.bn_dn) || !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 64))
+        return MOE_ERR_CUDA;
+      m.a1 = m.a0;
+      m.b1 = m.b0;
+      const long long tiles = static_cast<long long>(E) * ceil_div(d, BM) * ceil_div(n, v.bn_dn);
+      VGG_LAUNCH("dw_down_mx", run_dw_mx(v.bn_dn, f32, p, m, static_cast<int>(std::min<long long>(tiles, ctx->num_sms)), s));
+    }
+    if (fork && cudaStreamWaitEvent(s_main, ctx->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   // varlen-K weight gradients: [dW_gate; dW_up][e] = [dH | dU]^T X[tok], with [dH | dU] as high and low
   // bf16 parts (about 16 significant bits of the fp32 gradients)
   {
@@ -1302,12 +1423,15 @@ int moe_backward_mx(moe_ctx* ctx, const void* dO, const void* X, const void* W_r
                     const float* topk_w, const int32_t* offsets, const int32_t* sorted_tok, const float* sorted_w,
                     const int32_t* tok_ptr, const int32_t* tok_pairs, const void* H, const void* U, void* dOq,
                     void* do_sf_tiles, void* HUq, void* hu_sf, void* dX, void* dW_gate, void* dW_up, void* dW_down,
-                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
-                    moe_stream_t stream) {
+                    int dW_fp32, float* dS, float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* dw_ws,
+                    size_t dw_ws_bytes, moe_stream_t stream) {
   VGG_REQUIRE(Wdt_q && wdt_sf && Wgu_q && wgu_sf && dOq && do_sf_tiles && HUq && hu_sf);
   VGG_REQUIRE(aligned16(Wdt_q) && aligned16(wdt_sf) && aligned16(Wgu_q) && aligned16(wgu_sf) && aligned16(dOq) &&
               aligned16(do_sf_tiles) && aligned16(HUq) && aligned16(hu_sf));
-  const MxBwd mx{Wdt_q, wdt_sf, Wgu_q, wgu_sf, dOq, do_sf_tiles, HUq, hu_sf};
+  // the block-scaled weight gradients: a workspace of moe_mx_dw_ws_bytes, 256-byte aligned (null: two-part bf16)
+  VGG_REQUIRE(!dw_ws || ((reinterpret_cast<uintptr_t>(dw_ws) & (kAlign - 1)) == 0 &&
+                         dw_ws_bytes >= moe_mx_dw_ws_bytes(d, E, n, cap) && moe_mx_dw_ws_bytes(d, E, n, cap) > 0));
+  const MxBwd mx{Wdt_q, wdt_sf, Wgu_q, wgu_sf, dOq, do_sf_tiles, HUq, hu_sf, dw_ws};
   return backward_impl(ctx, dO, X, W_r, W_gate, W_up, W_down, T, d, E, n, K, m_tile, cap, topk_ids, topk_w, offsets,
                        sorted_tok, sorted_w, tok_ptr, tok_pairs, H, U, dX, dW_gate, dW_up, dW_down, dW_fp32, dS,
                        dlogits, dW_r, ws, ws_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,

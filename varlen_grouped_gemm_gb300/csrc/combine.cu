@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
   // and every lane stores them to one (or two) of the token's pair positions, so the stores of a token
   // are issued in parallel and the position lookups overlap the load.
   constexpr uint32_t kWarpBytes = 2 * kChunkBytes + (CODES ? kGrChunk : 0);
+  const bool bf = out_a != nullptr;  // the bf16 copies (without them: the code rows alone)
   const uint32_t zero = smem_u32(gr_smem);
   const uint32_t buf = zero + kChunkBytes + kWarpBytes * warp;
   const long long P = offsets[E];
@@ -491,9 +492,11 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
       bulk_wait_read<0>();  // this lane's previous stores have read the warp's buffer
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[warp], 2 * bytes + (CODES ? bytes / 2 : 0));
-        bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
-        bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+        mbar_arrive_expect_tx(&bars[warp], (bf ? 2 * bytes : 0) + (CODES ? bytes / 2 : 0));
+        if (bf) {
+          bulk_g2s(buf, a + t * d + c0, bytes, &bars[warp]);
+          bulk_g2s(buf + kChunkBytes, b + t * d + c0, bytes, &bars[warp]);
+        }
         if (CODES) bulk_g2s(buf + 2 * kChunkBytes, c + t * d + c0, bytes / 2, &bars[warp]);
       }
     };
@@ -536,8 +539,10 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (jl[h] >= 0) {
-          bulk_s2g(out_a + jp[h] * d + c0, buf, bytes);
-          bulk_s2g(out_b + jp[h] * d + c0, buf + kChunkBytes, bytes);
+          if (bf) {
+            bulk_s2g(out_a + jp[h] * d + c0, buf, bytes);
+            bulk_s2g(out_b + jp[h] * d + c0, buf + kChunkBytes, bytes);
+          }
           if (CODES) bulk_s2g(out_c + jl[h] * d + c0, buf + 2 * kChunkBytes, bytes / 2);
         }
       }
@@ -554,7 +559,8 @@ __global__ void __launch_bounds__(kGrWarps * 32) gather_rows_bulk_kernel(
     }
     bulk_commit();
   };
-  if (poff) {
+  if (!bf) {
+  } else if (poff) {
     // empty slots of the capacity layout (rare), then the padding rows of every group: at most 15 per group,
     // one per thread.  Rows past the padded total are never read (a group's last UMMA K step ends on its
     // padded boundary) and stay unwritten.
@@ -599,6 +605,7 @@ cudaError_t launch_gather_rows(const int32_t* offsets, const int32_t* poff, long
                                const uint8_t* c, const float* cs, uint8_t* out_c, float* out_cs, int* err,
                                int num_sms, unsigned long long timeout_ns, cudaStream_t s) {
   const bool codes = c != nullptr;
+  if (!out_a && !codes) return cudaErrorInvalidValue;  // nothing to copy
   const size_t smem = static_cast<size_t>(kGrChunk) * (2 + kGrWarps * (codes ? 5 : 4));
   const void* fn = codes ? reinterpret_cast<const void*>(gather_rows_bulk_kernel<true>)
                          : reinterpret_cast<const void*>(gather_rows_bulk_kernel<false>);

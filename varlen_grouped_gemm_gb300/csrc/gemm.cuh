@@ -82,6 +82,9 @@ enum VarMode { VAR_M = 0, VAR_K = 1, VAR_NONE = 2 };
 //             SwiGLU epilogue of this form emits A itself as block-scaled codes (a thread's 32 columns of
 //             its row are one block) with the scale blocks the down projection reads, and the dSwiGLU
 //             epilogue emits [dH | dU] the same way for the dX GEMM (o_q, o_sf).
+//             Varlen-K (the weight gradients): both operands are K-major code matrices [rows][K] whose groups
+//             each start on a whole stage (128 codes; the reduction padded per group with zero codes), one
+//             [N][K] matrix for B, and the scale blocks of both indexed by the stage of the whole reduction.
 enum XFlags { X_DUAL_A = 1, X_TRANS = 2, X_PAIR = 4, X_MX = 8 };
 enum EpiKind {
   EPI_STORE = 0, EPI_SWIGLU = 1, EPI_SCALE = 2, EPI_DSWIGLU = 3, EPI_SWIGLU_Q = 4, EPI_SCALE_Q = 5, EPI_STORE_Q = 6,
@@ -455,13 +458,15 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
       (EPI == EPI_SWIGLU_Q || EPI == EPI_SCALE_Q || EPI == EPI_STORE_Q || EPI == EPI_DSWIGLU_Q) || kMx;
   static_assert(!kMx || ((BN == 128 || BN == 192) && VAR == VAR_M && (AMODE == A_GATHER_K || AMODE == A_TMA_K) &&
                          (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) && (CN == 1 || CN == 2) &&
-                         (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_STORE || EPI == EPI_DSWIGLU)),
-                "block-scaled form: BN = 128 or 192, K-major operands, varlen-M, plain epilogue kinds");
+                         (EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_STORE || EPI == EPI_DSWIGLU)) ||
+                    ((BN == 128 || BN == 192) && VAR == VAR_K && AMODE == A_TMA_K && BMODE == B_TMA_K3 && CN == 1 &&
+                     EPI == EPI_STORE),
+                "block-scaled form: BN = 128 or 192, K-major operands, varlen-M plain epilogue kinds or a varlen-K store");
   static_assert(!kMx || 2 * BN + STAGES * (4 + 4 * mx_b_blocks(BN)) <= 512, "block-scaled form: TMEM columns");
   static_assert(EPI != EPI_STORE_Q || !OUTF32, "the e4m3 plain epilogue stores bf16");
   static_assert(!kF8 || ((AMODE == A_GATHER_K || AMODE == A_TMA_K) && (BMODE == B_TMA_K3 || BMODE == B_TMA_K3_GU) &&
-                         VAR == VAR_M),
-                "e4m3 form: K-major operands, varlen-M");
+                         (VAR == VAR_M || kMx)),
+                "e4m3 form: K-major operands, varlen-M (the block-scaled form also varlen-K)");
   static_assert(!kDual || ((AMODE == A_TMA_MN || AMODE == A_TMA_K) && !kF8), "dual A: a tiled bf16 A");
   static_assert(!kTrans || (VAR == VAR_K && EPI == EPI_STORE), "transposed store: varlen-K plain epilogue");
   constexpr bool kAMn = (AMODE == A_TMA_MN || AMODE == A_GATHER_MN);
@@ -563,6 +568,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
       if (g < p.groups) {
         const int rows_g = s_off[g + 1] - s_off[g];
         if (rows_g < 0) bad = 1;
+        if (kMx && VAR == VAR_K && (s_off[g] % BK) != 0) bad = 1;  // groups start on whole stages (and scale blocks)
         if (VAR == VAR_M) {
           // a pair: 256-row tiles, every column tile; clusters along N: CN column tiles per unit
           constexpr int kCpt = Sched<BN, BMODE, VAR>::kColsPerTile, kRpt = kPair ? 2 * BM : BM, kCn = kPair ? 1 : CN;
@@ -708,18 +714,25 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
           // alike), then B's (a cluster CTA past the last column tile loads the last tile's block; its results
           // are not stored)
           uint8_t* sf = sb + L::kBBytes;
-          {
-            const long long rt = s_tile[x.g] / mx_ncu + x.m0 / BM;
-            bulk_load(sf, p.a_sf + (rt * p.sf_kst + kstage) * 512, 512, bar);
-          }
           const int nt = min(x.nt, sch.ntiles - 1);
           constexpr int kSfb = 512 * mx_b_blocks(BN);
-          bulk_load(sf + 512, p.b_sf + ((static_cast<long long>(x.g) * sch.ntiles + nt) * p.sf_kst + kstage) * kSfb,
-                    kSfb, bar);
+          if (VAR == VAR_K) {
+            // varlen-K: both operands' blocks are indexed by the stage of the whole (padded) reduction, every
+            // group starting on a whole stage: A's [row tile][stage], B's [column tile][stage]
+            const long long kgl = x.k_begin / BK + kstage;
+            bulk_load(sf, p.a_sf + ((x.m0 / BM) * static_cast<long long>(p.sf_kst) + kgl) * 512, 512, bar);
+            bulk_load(sf + 512, p.b_sf + (static_cast<long long>(nt) * p.sf_kst + kgl) * kSfb, kSfb, bar);
+          } else {
+            const long long rt = s_tile[x.g] / mx_ncu + x.m0 / BM;
+            bulk_load(sf, p.a_sf + (rt * p.sf_kst + kstage) * 512, 512, bar);
+            bulk_load(sf + 512, p.b_sf + ((static_cast<long long>(x.g) * sch.ntiles + nt) * p.sf_kst + kstage) * kSfb,
+                      kSfb, bar);
+          }
         }
-        if (BMODE == B_TMA_K3) {
-          if (l2) tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
-          else tma_load_3d_hint(sb, &mp.b0, bar, kg, x.n0, x.g, pol_stream);
+        if (BMODE == B_TMA_K3) {  // varlen-K: one [N][K] matrix, the group's reduction rows along K
+          const int bz = (VAR == VAR_K) ? 0 : x.g;
+          if (l2) tma_prefetch_l2_3d(&mp.b0, kg, x.n0, bz);
+          else tma_load_3d_hint(sb, &mp.b0, bar, kg, x.n0, bz, pol_stream);
         } else if (BMODE == B_TMA_K3_GU) {
           if (l2) {
             tma_prefetch_l2_3d(&mp.b0, kg, x.n0, x.g);
@@ -946,7 +959,7 @@ __global__ void __launch_bounds__(WarpPlan<STAGES, EW, AMODE, BMODE, CN, XF>::kT
     // next group (or the zeroed tail): its UMMAs stop at the K step (16 rows) that holds the group's
     // last row, and the whole warp clears the rows of that step past the group's end in B before
     // lane 0 issues them.
-    constexpr bool kZeroTail = (VAR == VAR_K) && !kGather;
+    constexpr bool kZeroTail = (VAR == VAR_K) && !kGather && !kMx;  // block-scaled groups are whole stages
     if (!kZeroTail) {
       // lane 0 alone: no warp-wide step between a stage's arrival and its UMMAs
       if (lane == 0) {

@@ -206,4 +206,179 @@ cudaError_t run_dx_store_mx(int BN, const GemmParams& p, const Maps& m, int grid
   return launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_M, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
 }
 
+// ---- the weight gradients on block-scaled operands -----------------------------------------------------------
+// dW_gate[e] = dH_e^T X_e, dW_up[e] = dU_e^T X_e, dW_down[e] = dO_e^T A'_e reduce over the expert's tokens, so
+// their blocks run along tokens: 1 x 32 blocks of one column over 32 consecutive tokens of one expert.  Every
+// operand is written transposed, K-major ([column][token] codes), with each expert's tokens starting on a
+// whole 128-token stage (zero codes fill the stage past the expert's last token; an all-zero block has
+// scale byte 127).
+
+// Stage offsets of the padded reduction: kp[g] = sum over the groups before g of their row counts rounded up to
+// 128, counted in code pairs (the GEMM's K unit: 64 pairs per stage).  One block.
+__global__ void __launch_bounds__(1024) mx_stage_offsets_kernel(const int32_t* __restrict__ off, int E,
+                                                                int32_t* __restrict__ kp, int* err) {
+  __shared__ int wsum[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < E; base += 1024) {
+    const int g = base + tid;
+    int r = 0;
+    if (g < E) {
+      r = __ldg(off + g + 1) - __ldg(off + g);
+      if (r < 0) {
+        set_error(err, DERR_BAD_OFFSETS);
+        r = 0;
+      }
+      r = (r + 127) / 128 * 64;
+    }
+    int incl = r;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = wsum[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    const int excl = carry + wsum[warp] + incl - r;
+    if (g < E) kp[g] = excl;
+    __syncthreads();
+    if (tid == 1023) carry = excl + r;
+    __syncthreads();
+  }
+  if (tid == 0) kp[E] = carry;
+}
+
+cudaError_t launch_mx_stage_offsets(const int32_t* off, int E, int32_t* kp, int* err, cudaStream_t s) {
+  mx_stage_offsets_kernel<<<1, 1024, 0, s>>>(off, E, kp, err);
+  return cudaGetLastError();
+}
+
+// One block per (stage of 128 padded tokens, 64 columns, job): the 128 x 64 tile of the job's source (gathered
+// rows, or the sorted rows themselves; high + low part when given) is staged in shared memory as fp32, then
+// thread (column c, 32-token block k) quantizes the column's 32 values, writes their 32 codes to row
+// row0 + c of the job's code matrix and the scale byte into the job's block of that row's tile and stage.
+constexpr int kMxColThreads = 256;
+__global__ void __launch_bounds__(kMxColThreads) quantize_cols_mx_kernel(MxColJobs jobs, const int32_t* __restrict__ off,
+                                                                        const int32_t* __restrict__ kp, int E,
+                                                                        long long pos_cap, long long kq, int kst,
+                                                                        int* err) {
+  __shared__ float tile[128][64];
+  const MxColJob& jb = jobs.job[blockIdx.z];
+  const int c0 = blockIdx.y * 64;
+  if (c0 >= jb.C) return;
+  const int stage = blockIdx.x;
+  const int t0 = stage * 64;  // first pair of the stage
+  if (t0 >= __ldg(kp + E)) return;  // past the padded reduction
+  // the group whose padded range holds the stage: the largest g with kp[g] <= t0
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(kp + mid) <= t0) lo = mid;
+    else hi = mid;
+  }
+  const int g = lo;
+  const int j0 = 2 * (t0 - __ldg(kp + g));  // position of the stage's first token within the group
+  const int base = __ldg(off + g), cnt = __ldg(off + g + 1) - base;
+  const int tid = threadIdx.x;
+  // load: 8 threads per row (8 columns each), 32 rows per pass
+  {
+    const int q8 = tid & 7;
+    const int col = c0 + 8 * q8;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+      const int i = pass * 32 + (tid >> 3);
+      const int j = j0 + i;
+      long long srow = -1;
+      if (j < cnt) {
+        const long long pos = static_cast<long long>(base) + j;
+        if (pos < 0 || pos >= pos_cap) {
+          set_error(err, DERR_BAD_OFFSETS);
+        } else {
+          srow = jb.idx ? static_cast<long long>(__ldg(jb.idx + pos)) : pos;
+          if (srow >= jb.src_rows) {
+            set_error(err, DERR_BAD_OFFSETS);
+            srow = -1;
+          }
+        }
+      }
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+      if (srow >= 0 && col < jb.C) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(jb.src + srow * jb.ld + col));
+        const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_bf16x2(xv[e]);
+          v[2 * e] = f.x;
+          v[2 * e + 1] = f.y;
+        }
+        if (jb.src_lo) {
+          const uint4 y = __ldg(reinterpret_cast<const uint4*>(jb.src_lo + srow * jb.ld + col));
+          const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(yv[e]);
+            v[2 * e] += f.x;
+            v[2 * e + 1] += f.y;
+          }
+        }
+      }
+      *reinterpret_cast<float4*>(&tile[i][8 * q8]) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(&tile[i][8 * q8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  __syncthreads();
+  const int c = tid & 63, kb = tid >> 6;
+  if (c0 + c >= jb.C) return;
+  float v[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) v[t] = tile[kb * 32 + t][c];
+  uint32_t w[8];
+  const int e = mx_block32(v, w);
+  const long long r = static_cast<long long>(jb.row0) + c0 + c;  // operand row of the code matrix
+  uint4* dst = reinterpret_cast<uint4*>(jb.q + r * kq + static_cast<long long>(stage) * 128 + kb * 32);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  const int nblk = (jb.tw + 127) / 128;
+  const long long tl = r / jb.tw;
+  const int tr = static_cast<int>(r - tl * jb.tw), br = tr & 127;
+  jb.sf[(tl * kst + stage) * (512ll * nblk) + (tr >> 7) * 512 + (br & 31) * 16 + (br >> 5) * 4 + kb] =
+      static_cast<uint8_t>(e + 127);
+}
+
+cudaError_t launch_quantize_cols_mx(const MxColJobs& jobs, int njobs, const int32_t* off, const int32_t* kp, int E,
+                                    long long pos_cap, long long kq, int kst, int* err, cudaStream_t s) {
+  if (njobs <= 0 || njobs > kMxColJobs || kst <= 0) return njobs > kMxColJobs ? cudaErrorInvalidValue : cudaSuccess;
+  int chunks = 0;
+  for (int i = 0; i < njobs; ++i) chunks = chunks > (jobs.job[i].C + 63) / 64 ? chunks : (jobs.job[i].C + 63) / 64;
+  quantize_cols_mx_kernel<<<dim3(kst, chunks, njobs), kMxColThreads, 0, s>>>(jobs, off, kp, E, pos_cap, kq, kst,
+                                                                              err);
+  return cudaGetLastError();
+}
+
+// The weight-gradient GEMMs on block-scaled operands: A = [M][K] codes, B = [N][K] codes (varlen-K over the
+// padded per-expert stages), plain store of the [E][M][N] gradient (rows past out_rows_split to the second
+// output), bf16 or fp32.
+cudaError_t run_dw_mx(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 128)
+    return f32 ? launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_K, EPI_STORE, true, 1, X_MX>(p, m, grid, s)
+               : launch_grouped_gemm<128, 6, 4, 1, A_TMA_K, B_TMA_K3, VAR_K, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_K, EPI_STORE, true, 1, X_MX>(p, m, grid, s)
+             : launch_grouped_gemm<kMxBN, 4, 4, 1, A_TMA_K, B_TMA_K3, VAR_K, EPI_STORE, false, 1, X_MX>(p, m, grid, s);
+}
+
 }  // namespace vgg

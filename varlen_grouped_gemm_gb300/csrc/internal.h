@@ -61,6 +61,29 @@ cudaError_t launch_mx_tile_scales(const uint8_t* sf, int sf_ld, int src_rows, co
                                   cudaStream_t s);
 cudaError_t launch_quantize_weight_mx(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, uint8_t* blocks,
                                       int rpt, int roff, int ntile, int kst, int nblk, cudaStream_t s);
+// Block-scaled operands of the weight gradients (blocks along tokens): kp = the padded stage offsets (pairs),
+// then per job the source's columns as K-major code rows with their scale blocks.
+struct MxColJob {
+  const __nv_bfloat16* src;     // [src_rows][ld] bf16: rows at the sorted positions, or gathered through idx
+  const __nv_bfloat16* src_lo;  // low part in the same layout (the value is src + src_lo), or null
+  const int32_t* idx;           // sorted position -> source row (negative: no row), or null (the position)
+  long long src_rows;
+  long long ld;
+  int C;            // columns of src (code rows written: row0 .. row0 + C - 1)
+  int row0;
+  uint8_t* q;       // codes [rows][kq]
+  uint8_t* sf;      // scale blocks [rows / tw][kst] x ceil(tw / 128) 512-byte blocks
+  int tw;           // operand rows per scale tile (the GEMM's row tile 128, or its column tile 128 / 192)
+};
+constexpr int kMxColJobs = 6;
+struct MxColJobs {
+  MxColJob job[kMxColJobs];
+};
+cudaError_t launch_mx_stage_offsets(const int32_t* off, int E, int32_t* kp, int* err, cudaStream_t s);
+// pos_cap: the length of the pair arrays (sorted positions at or past it are an offsets error)
+cudaError_t launch_quantize_cols_mx(const MxColJobs& jobs, int njobs, const int32_t* off, const int32_t* kp, int E,
+                                    long long pos_cap, long long kq, int kst, int* err, cudaStream_t s);
+cudaError_t run_dw_mx(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_down_scale_dual(int BN, bool pair, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_router_logits(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 // backward
@@ -79,7 +102,8 @@ cudaError_t run_test_m_dual(bool pair, const GemmParams& p, const Maps& m, int g
 
 // Expert-sorted copies of two [T, d] bf16 tensors (rows without a pair zeroed), and optionally of per-token
 // e4m3 code rows c with their scales cs (rows without a pair: zero codes, scale 1).  With poff the two bf16
-// copies are padded per group to multiples of 16 rows (cap_pad rows); the code rows are not.
+// copies are padded per group to multiples of 16 rows (cap_pad rows); the code rows are not.  out_a == nullptr:
+// the code rows alone.
 cudaError_t launch_gather_rows(const int32_t* offsets, const int32_t* poff, long long cap_pad, int E,
                                const int32_t* sorted_tok, const int32_t* tok_ptr,
                                const int32_t* tok_pairs, long long cap, int T, int d, const __nv_bfloat16* a,
