@@ -10,6 +10,10 @@ its fp32 SwiGLU values, against the oracle's quantization of its exact values (e
 fp32 rounding of a rounding boundary: at most one code step, at most a few per hundred thousand); O within
 the usual tolerance of the oracle's fp64 forward.  Cases: ragged tails, n and d with a half last stage of
 128 codes, empty experts (skewed prior), token rounding, 512 experts, the capacity dispatch with empty slots.
+The backward: both activation-gradient GEMMs block-scaled, and the weight gradients either two-part bf16 (the
+usual tolerance) or block-scaled along tokens (the element-wise bound derived from the arithmetic: the oracle's
+block-scaled product within fp32 accumulation, plus one code step where a device operand value may round
+differently).
 """
 import numpy as np
 import pytest
