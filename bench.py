@@ -633,12 +633,14 @@ def measure_e4m3(vgg, ctx, wl, X, W_r, bias, W_gate, W_up, W_down, dO, buf, flus
                 "mx_dw_tflops": (fl + fl_dn) / ((wgmx + wdmx) * 1e-3) / 1e12,
                 "recipe": "e4m3 codes with one power-of-two (UE8M0) scale per 32 values along the reduction "
                           "dimension of every operand row (kind::mxf8f6f4 UMMA); A quantized in the gate/up "
-                          "epilogue, [dH|dU] in the dSwiGLU epilogue; 192-column tiles; the weight gradients and "
-                          "the router stay bf16; train_step_mx_dw_ms: the same step with block-scaled weight "
+                          "epilogue, [dH|dU] in the dSwiGLU epilogue; 192-column tiles; the weight gradients (on "
+                          "dH, dU, A' rounded once to bf16) and the router stay bf16; train_step_mx_dw_ms: the "
+                          "same step with block-scaled weight "
                           "gradients (operands in blocks of 32 tokens of one expert, one quantizing launch)"},
             "peak_source": f"{pk['source']} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
             "recipe": "e4m3 operands with one fp32 scale per row: X per token, A, dO and [dH|dU] per pair, weights per "
-                      "output channel of each GEMM; fp32 accumulation; dW and the router stay bf16",
+                      "output channel of each GEMM; fp32 accumulation; dW (on dH, dU, A' rounded once to bf16) and the "
+                      "router stay bf16",
             "steps": steps, "l2": "flushed between steps", "launch": "eager calls"}
 
 

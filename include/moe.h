@@ -383,7 +383,8 @@ int moe_quantize_bwd_weights_mx(moe_ctx* ctx, const void* W_gate, const void* W_
  *   dXp[j,c]  = sum_k dq(HUq[j,k]) dq(Wgu_q[e,c,k])
  *
  * Wdt_q, wdt_sf, Wgu_q, wgu_sf from moe_quantize_bwd_weights_mx.  The router gradient and dX's reduction are
- * those of moe_backward.  With dw_ws == NULL the weight gradients are moe_backward's (two-part bf16 operands).
+ * those of moe_backward.  With dw_ws == NULL the weight gradients are moe_backward's GEMMs with dH, dU and
+ * A' = w A each rounded once to bf16 from the fp32 value (no low part; the dSwiGLU epilogue then writes none).
  * With dw_ws (caller-owned device scratch of at least moe_mx_dw_ws_bytes(d,E,n,cap) bytes, 256-byte aligned,
  * overwritten) they run on block-scaled operands with the blocks along tokens: for expert e, with its sorted
  * pairs j = offsets[e] + i split into blocks of 32 consecutive i (the last one partial), every operand column
@@ -492,8 +493,9 @@ int moe_quantize_dact_weights_e4m3(moe_ctx* ctx, const void* W_down, int E, int 
  *   quantized; the codes are the same either way), and
  *     dA'[j,c] = do_scale[j] * wdt_scale[e,c] * sum_i e4m3(dOq[j,i]) e4m3(Wdt_q[e,c,i]),
  *   the dSwiGLU epilogue (dS = <dA', A>, dH, dU, A') running on that dA'.
- * Code products accumulate in fp32 (kind::f8f6f4); everything else as moe_backward (bf16 weight
- * gradients).  MOE_ERR_INVALID_ARG on a missing or misaligned buffer.
+ * Code products accumulate in fp32 (kind::f8f6f4); everything else as moe_backward, except that the
+ * weight-gradient GEMMs take dH, dU and A' = w A each rounded once to bf16 from the fp32 value (no low
+ * part: the e4m3 GEMMs already carry e4m3 rounding).  MOE_ERR_INVALID_ARG on a missing or misaligned buffer.
  */
 int moe_backward_e4m3(moe_ctx* ctx, const void* dO, const void* X, const void* W_r, const void* W_gate,
                       const void* W_up, const void* W_down, const void* Wgu_q, const float* wgu_scale,

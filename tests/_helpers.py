@@ -112,6 +112,45 @@ def compare_layer(buf, inp: Inputs, O_ref, cache, grads, report=None, skip=()):
     return rep
 
 
+def check_dw_single_bf16(buf, blocks, X64, dO64, r, w_full):
+    """Weight gradients of the e4m3 and block-scaled backward, whose operands dH, dU and A' = w A the device rounds
+    once to bf16 from its fp32 values (X and dO are bf16 inputs): every element within that rounding's bound of
+    the oracle's gradient of the same variant,
+
+        |dev - sum_t a_t b_t| <= 2^-8 sum_t |a_t| |b_t| + 2^-16 max_t |a_t| sum_t |b_t|
+
+    (half a bf16 ulp is 2^-9 of a value; the rest covers the fp32 arithmetic before the rounding and the fp32
+    accumulation), with (a, b) = (dH, X), (dU, X) and (A', dO) per expert, and normwise within 2^-7 of the
+    product per expert.  ``blocks[e]`` holds the oracle's exact dh, du, a of expert e.  Experts without pairs
+    must get exact zeros.  Returns the worst error over its bound."""
+    worst = 0.0
+    got = {k: dev_to_f64(getattr(buf, k)) for k in ("dW_gate", "dW_up", "dW_down")}
+    E = len(r.counts)
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        if hi == lo:
+            for k in got:
+                assert not np.any(got[k][e]), f"{k}: an expert without pairs must get exactly zero"
+            continue
+        toks = r.sorted_tok[lo:hi]
+        dh, du, a = blocks[e]
+        ap = w_full[toks, e][:, None] * a
+        for k, A, B in (("dW_gate", dh, X64[toks]), ("dW_up", du, X64[toks]), ("dW_down", dO64[toks], ap)):
+            if k == "dW_down":  # dW_down[e] = dO^T A': the rounded operand is the second one
+                ref = A.T @ B
+                bound = 2.0 ** -8 * (np.abs(A).T @ np.abs(B)) + 2.0 ** -16 * np.outer(np.abs(A).sum(0), np.abs(B).max(0))
+            else:
+                ref = A.T @ B
+                bound = 2.0 ** -8 * (np.abs(A).T @ np.abs(B)) + 2.0 ** -16 * np.outer(np.abs(A).max(0), np.abs(B).sum(0))
+            err = np.abs(got[k][e] - ref)
+            assert np.all(err <= bound + 1e-30), (k, e, float(np.max(err / (bound + 1e-30))))
+            worst = max(worst, float(np.max(err / (bound + 1e-30))))
+            # independent roundings leave about 2^-9 / sqrt(3) of the product's norm; a dropped or doubled token
+            # would leave about 1 / sqrt(rows)
+            assert np.linalg.norm(err) <= 2.0 ** -7 * np.linalg.norm(ref) + 1e-30, (k, e, "normwise")
+    return worst
+
+
 def check_rounding_near_ties(g, L64, r: mo.Routing, eps=8 * 2.0 ** -24):
     """Token Rounding on exact logits, against the oracle's own selection ``r``.
 

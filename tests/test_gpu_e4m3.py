@@ -19,7 +19,7 @@ import oracle
 import synth
 from oracle import moe_oracle as mo
 
-from _helpers import Inputs, bits_to_dev, check_routing_bit_exact, dev_to_f64, gpu_routing
+from _helpers import Inputs, bits_to_dev, check_dw_single_bf16, check_routing_bit_exact, dev_to_f64, gpu_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -224,6 +224,8 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
       within the usual tolerance: the GEMM and the per-token reduction exactly;
     * dX against the oracle's own e4m3 backward: mean within the usual tolerance, max within 0.15 (one e4m3
       step of a code is up to 12.5% of that element) -- the variant's own tolerance;
+    * the weight gradients (operands dH, dU, A' rounded once to bf16) within that rounding's bound of the oracle's
+      e4m3 backward (``check_dw_single_bf16``);
     * every other gradient within the usual tolerance of the oracle's e4m3 backward."""
     import varlen_grouped_gemm_gb300 as vgg
     import oracle
@@ -264,6 +266,19 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
     if dact and buf.sorted_tok.numel() >= wl.T:  # dO quantized per token and gathered: empty rows zero, scale 1
         assert not buf.doq[r.P:].any().item() and bool((buf.dos[r.P:] == 1).all().item())
     flips = 0
+    blocks = {}
+    for e in range(E):
+        lo, hi = r.offsets[e], r.offsets[e + 1]
+        if hi == lo:
+            continue
+        rows = r.sorted_tok[lo:hi]
+        dap = None
+        if dact:
+            dq, ds_ = mo.quantize_rows_e4m3(inp.dO[rows])
+            dap = mo.dequantize_rows_e4m3(dq, ds_) @ Wdt[e].T
+        blk = mo.expert_block_backward(X64[rows], dO64[rows], cache["w_full"][rows, e], inp.W_gate[e], inp.W_up[e],
+                                       inp.W_down[e], dap=dap)
+        blocks[e] = (blk["dh"], blk["du"], blk["a"])
     if dx:
         huq = buf.huq[:r.P].cpu().numpy()
         hus = buf.hus[:r.P].cpu().numpy()
@@ -273,13 +288,8 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
             if hi == lo:
                 continue
             rows = r.sorted_tok[lo:hi]
-            dap = None
-            if dact:
-                dq, ds_ = mo.quantize_rows_e4m3(inp.dO[rows])
-                dap = mo.dequantize_rows_e4m3(dq, ds_) @ Wdt[e].T
-            blk = mo.expert_block_backward(X64[rows], dO64[rows], cache["w_full"][rows, e], inp.W_gate[e],
-                                           inp.W_up[e], inp.W_down[e], dap=dap)
-            hq, _ = mo.quantize_rows_e4m3(mo.round_bf16(np.concatenate([blk["dh"], blk["du"]], axis=1)).astype(np.float32))
+            dh, du, _ = blocks[e]
+            hq, _ = mo.quantize_rows_e4m3(mo.round_bf16(np.concatenate([dh, du], axis=1)).astype(np.float32))
             diff = huq[lo:hi] != hq
             flips += int(diff.sum())
             if diff.any():  # a differing code is a neighbour on the e4m3 grid
@@ -289,7 +299,10 @@ def test_e4m3_backward_matches_oracle(ctx, wl, dx, dact):
         assert flips <= 0.01 * huq.size, flips
         # the e4m3 GEMM and the token reduction on the device's own codes: the usual bf16 tolerance
         oracle.compare("dX (from the device's codes)", dev_to_f64(buf.dX), dX_codes)
-    rep = compare_layer(buf, inp, O_ref, cache, grads, skip=("dX",) if dx else ())
+    rep = compare_layer(buf, inp, O_ref, cache, grads,
+                        skip=(("dX",) if dx else ()) + ("dW_gate", "dW_up", "dW_down"))
+    # the weight gradients take dH, dU, A' rounded once to bf16: that rounding's bound
+    rep["dW bound"] = {"max": check_dw_single_bf16(buf, blocks, X64, dO64, r, cache["w_full"]), "mean": 0.0}
     # against the oracle's own e4m3 backward: the variant's tolerance (one e4m3 step of a code is up to 12.5%
     # of that element), both floors
     end = oracle.compare("dX (e4m3 variant)", dev_to_f64(buf.dX), grads["dX"], max_rel=0.15)
@@ -339,9 +352,23 @@ def test_e4m3_backward_capacity_layout(ctx, dx):
         oracle.compare("dX (e4m3 variant)", dX, g["dX"], max_rel=0.15)
     else:
         oracle.compare("dX", dX, g["dX"])
-    for name in ("dW_gate", "dW_up", "dW_down"):
-        oracle.compare(name, dev_to_f64(getattr(buf, name)), np.stack([g[name][e] for e in range(wl.E)]),
-                       param_axes=oracle.WEIGHT_GRAD)
+    # the weight gradients on operands rounded once to bf16: that rounding's bound
+    Wd = mo.bf16_bits_to_f64(inp.W_down)
+    tq, ts = mo.quantize_rows_e4m3(Wd.transpose(0, 2, 1).reshape(wl.E * wl.n, wl.d).astype(np.float32))
+    Wdt = mo.dequantize_rows_e4m3(tq, ts).reshape(wl.E, wl.n, wl.d)
+    X64, dO64 = mo.bf16_bits_to_f64(inp.X), mo.bf16_bits_to_f64(inp.dO)
+    blocks = {}
+    for e in range(wl.E):
+        rows = r.rows_of(e)
+        if len(rows) == 0:
+            continue
+        dq, ds_ = mo.quantize_rows_e4m3(inp.dO[rows])
+        blk = mo.expert_block_backward(X64[rows], dO64[rows], cache["w_full"][rows, e], inp.W_gate[e], inp.W_up[e],
+                                       inp.W_down[e], dap=mo.dequantize_rows_e4m3(dq, ds_) @ Wdt[e].T)
+        blocks[e] = (blk["dh"], blk["du"], blk["a"])
+        for name, key in (("dW_gate", "dWg"), ("dW_up", "dWu"), ("dW_down", "dWd")):
+            np.testing.assert_allclose(blk[key], g[name][e], rtol=1e-12, atol=1e-15)
+    check_dw_single_bf16(buf, blocks, X64, dO64, r, cache["w_full"])
     slot_of = np.concatenate([e * C + np.arange(r.counts[e]) for e in range(wl.E)]).astype(np.int64)
     oracle.compare("dS", dev_to_f64(buf.dS)[slot_of], g["dw"][r.sorted_tok, r.sorted_exp])
     oracle.compare("dlogits", dev_to_f64(buf.dlogits), g["dlogits"])

@@ -1015,6 +1015,13 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
   // With the block-scaled weight gradients (which read X and dO through the token index) only the code rows are
   // copied.
   const bool mx_dw = mx && mx->dw_ws;
+  // The e4m3 and block-scaled forms take the weight gradients' operands rounded once to bf16: their
+  // activation-gradient GEMMs already carry e4m3 rounding, and the single-part GEMMs run half the UMMAs.  The
+  // bf16 backward keeps the two-part operands of the precision bound; the dSwiGLU epilogue writes the low
+  // parts for them (and for the block-scaled weight gradients' quantization) only.
+  const bool variant = Wgu_q || Wdt_q || mx;
+  const bool dw_single = variant && !mx_dw;
+  const bool lo_parts = !dw_single;
   const bool padded = !mx_dw && (mx || !(Wdt_q && !dact_tok));
   const long long cap_pad = padded ? padded_rows(cap, E) : cap;
   const int32_t* poff = padded ? w.poff : nullptr;
@@ -1045,9 +1052,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dH;
     p.out1 = w.dU;
     p.out2 = w.Ap;
-    p.out3 = w.dH_lo;
-    p.out4 = w.dU_lo;
-    p.out5 = w.Ap_lo;
+    p.out3 = lo_parts ? w.dH_lo : nullptr;
+    p.out4 = lo_parts ? w.dU_lo : nullptr;
+    p.out5 = lo_parts ? w.Ap_lo : nullptr;
     p.ld_out = n;
     p.row_scale = sorted_w;
     p.part = w.part;
@@ -1063,7 +1070,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, mx->dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, mx->Wdt_q, d / 2, n, E, BN) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || (lo_parts && !make_lo_maps(m, w, n, cap)))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -1087,9 +1094,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dH;
     p.out1 = w.dU;
     p.out2 = w.Ap;
-    p.out3 = w.dH_lo;
-    p.out4 = w.dU_lo;
-    p.out5 = w.Ap_lo;
+    p.out3 = lo_parts ? w.dH_lo : nullptr;
+    p.out4 = lo_parts ? w.dU_lo : nullptr;
+    p.out5 = lo_parts ? w.Ap_lo : nullptr;
     p.ld_out = n;
     p.row_scale = sorted_w;
     p.part = w.part;
@@ -1100,7 +1107,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, dOq, d / 2, cap, d / 2, BM) || !make_map_3d(&m.b0, Wdt_q, d / 2, n, E, bn6) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || (lo_parts && !make_lo_maps(m, w, n, cap)))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -1119,9 +1126,9 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = w.dH;
     p.out1 = w.dU;
     p.out2 = w.Ap;
-    p.out3 = w.dH_lo;
-    p.out4 = w.dU_lo;
-    p.out5 = w.Ap_lo;
+    p.out3 = lo_parts ? w.dH_lo : nullptr;
+    p.out4 = lo_parts ? w.dU_lo : nullptr;
+    p.out5 = lo_parts ? w.Ap_lo : nullptr;
     p.ld_out = n;
     p.row_scale = sorted_w;
     p.part = w.part;
@@ -1131,7 +1138,7 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dOs, d, cap_pad, d, BM) || !make_chunked_map_3d(&m.b0, W_down, n, d, E, sh.b_cols / 64) ||
         !make_store_map_2d(&m.o0, w.dH, false, n, cap, n, 32) || !make_store_map_2d(&m.o1, w.dU, false, n, cap, n, 32) ||
-        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || !make_lo_maps(m, w, n, cap))
+        !make_store_map_2d(&m.o2, w.Ap, false, n, cap, n, 32) || (lo_parts && !make_lo_maps(m, w, n, cap)))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.b1 = m.b0;
@@ -1348,15 +1355,16 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out_rows_split = n;
     p.ld_out = d;
     const int BN = gemm_bn(d);
-    const DwShape sh = dw_shape(ctx, BN, poff != nullptr, E, 2 * n, d);
+    const DwShape sh = dw_shape(ctx, BN, poff != nullptr && !dw_single, E, 2 * n, d);
     Maps m = zero_maps();
     if (!make_map_2d(&m.a0, w.dH, n, cap, n, 64) || !make_map_2d(&m.a1, w.dU, n, cap, n, 64) ||
-        !make_map_2d(&m.a2, w.dH_lo, n, cap, n, 64) || !make_map_2d(&m.a3, w.dU_lo, n, cap, n, 64) ||
+        (!dw_single && (!make_map_2d(&m.a2, w.dH_lo, n, cap, n, 64) || !make_map_2d(&m.a3, w.dU_lo, n, cap, n, 64))) ||
         !make_chunked_map_2d(&m.b0, w.Xs, d, cap_pad, sh.b_chunks) ||
         !make_store_map_3d(&m.o0, dW_gate, f32, d, n, E, 64) || !make_store_map_3d(&m.o1, dW_up, f32, d, n, E, 64))
       return MOE_ERR_CUDA;
     m.b1 = m.b0;
-    VGG_LAUNCH("dw_gate_up", run_dw_dual(BN, f32, false, sh.pair, p, m, sh.grid, s));
+    if (dw_single) VGG_LAUNCH("dw_gate_up", run_dw_tiled(BN, f32, p, m, sh.grid, s));
+    else VGG_LAUNCH("dw_gate_up", run_dw_dual(BN, f32, false, sh.pair, p, m, sh.grid, s));
   }
   // dW_down[e] = dO[tok]^T A' (the combine weight is folded into A' = w A), computed as its transpose
   // A'^T dO[tok] with A' as high and low bf16 parts (tile rows = columns of dW_down) and stored through
@@ -1371,18 +1379,19 @@ static int backward_impl(moe_ctx* ctx, const void* dO, const void* X, const void
     p.out0 = dW_down;
     p.ld_out = n;
     const int BN = gemm_bn(d);
-    const DwShape sh = dw_shape(ctx, BN, poff != nullptr, E, n, d);
+    const DwShape sh = dw_shape(ctx, BN, poff != nullptr && !dw_single, E, n, d);
     Maps m = zero_maps();
     p.b_chunked = 1;
     p.b_offsets = poff;
-    if (!make_map_2d(&m.a0, w.Ap, n, cap, n, 64) || !make_map_2d(&m.a2, w.Ap_lo, n, cap, n, 64) ||
+    if (!make_map_2d(&m.a0, w.Ap, n, cap, n, 64) || (!dw_single && !make_map_2d(&m.a2, w.Ap_lo, n, cap, n, 64)) ||
         !make_chunked_map_2d(&m.b0, w.dOs, d, cap_pad, sh.b_chunks) ||
         !make_store_map_3d(&m.o0, dW_down, f32, n, d, E, 32))
       return MOE_ERR_CUDA;
     m.a1 = m.a0;
     m.a3 = m.a2;
     m.b1 = m.b0;
-    VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, sh.pair, p, m, sh.grid, s));
+    if (dw_single) VGG_LAUNCH("dw_down", run_dw_tiled_trans(BN, f32, p, m, sh.grid, s));
+    else VGG_LAUNCH("dw_down", run_dw_dual(BN, f32, true, sh.pair, p, m, sh.grid, s));
   }
   if (fork && cudaStreamWaitEvent(s, ctx->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;

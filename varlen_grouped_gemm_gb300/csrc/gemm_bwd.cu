@@ -41,6 +41,16 @@ cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, i
              : launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false>(p, m, grid, s);
 }
 
+// The same with the tile written transposed (dW_down[e] = dO^T A' computed as A'^T dO: M = n, N = d, each 32 x 32
+// block transposed while it is staged), for the single-part A' of the e4m3 and block-scaled backward.
+cudaError_t run_dw_tiled_trans(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
+  if (BN == 256)
+    return f32 ? launch_grouped_gemm<256, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, X_TRANS>(p, m, grid, s)
+               : launch_grouped_gemm<256, 4, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, X_TRANS>(p, m, grid, s);
+  return f32 ? launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, true, 1, X_TRANS>(p, m, grid, s)
+             : launch_grouped_gemm<128, 6, 8, 1, A_TMA_MN, B_TMA_MN2, VAR_K, EPI_STORE, false, 1, X_TRANS>(p, m, grid, s);
+}
+
 // Varlen-K with one operand gathered through a token index (cp.async, zero past the group's end).
 cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s) {
   if (BN == 256)

@@ -92,6 +92,7 @@ cudaError_t run_dx_store(int BN, bool pair, const GemmParams& p, const Maps& m, 
 cudaError_t run_dw_gate_up(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_down(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_tiled(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
+cudaError_t run_dw_tiled_trans(int BN, bool f32, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
 cudaError_t run_dw_dual(int BN, bool f32, bool trans, bool pair, const GemmParams& p, const Maps& m, int grid,
                         cudaStream_t s);
 cudaError_t run_dense_mn_store(int BN, const GemmParams& p, const Maps& m, int grid, cudaStream_t s);
