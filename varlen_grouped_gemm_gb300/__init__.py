@@ -739,7 +739,8 @@ def forward_mx(ctx, X, W_r, bias, wmx: MxWeights, buf: Buffers, stream=None, cac
 def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buffers, stream=None, dw=False):
     """The backward with the dSwiGLU and dX GEMMs on block-scaled operands (``wmx`` quantized with
     ``backward=True``, ``buf`` allocated with ``mx=True``); with ``dw`` the weight gradients too (blocks of 32
-    tokens of one expert), else they stay two-part bf16.  The block-scaled weight gradients are slower on one
+    tokens of one expert), else they stay bf16 on dH, dU, A' rounded once to bf16.  The block-scaled weight
+    gradients are slower on one
     GB300 (c2 step 1.20 against 0.94 ms): with short per-expert reductions the GEMMs are bound by per-tile work,
     not by the tensor cores, and their operands take a transposing quantization pass."""
     if wmx.Wdt_q is None or buf.mhuq is None:
