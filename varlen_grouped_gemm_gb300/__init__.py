@@ -740,9 +740,9 @@ def backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, wmx: MxWeights, buf: Buff
     """The backward with the dSwiGLU and dX GEMMs on block-scaled operands (``wmx`` quantized with
     ``backward=True``, ``buf`` allocated with ``mx=True``); with ``dw`` the weight gradients too (blocks of 32
     tokens of one expert), else they stay bf16 on dH, dU, A' rounded once to bf16.  The block-scaled weight
-    gradients are slower on one
-    GB300 (c2 step 1.20 against 0.94 ms): with short per-expert reductions the GEMMs are bound by per-tile work,
-    not by the tensor cores, and their operands take a transposing quantization pass."""
+    gradients are slower on one GB300 (c2 step 1.20 against 0.94 ms): with short per-expert reductions the
+    GEMMs are bound by per-tile work, not by the tensor cores, and their operands take a transposing
+    quantization pass."""
     if wmx.Wdt_q is None or buf.mhuq is None:
         raise ValueError("block-scaled backward needs MxWeights.quantize(..., backward=True) and Buffers(mx=True)")
     T, d = X.shape
