@@ -325,7 +325,6 @@ def ncu_launch_summary(csv_path: str) -> str:
     """Markdown table of an ncu `--metrics gpu__time_duration.sum --csv` launch list: per kernel of this
     library, its launches, total device time and share (other kernels, e.g. torch fills, are listed apart)."""
     import csv
-    import re
     rows, hdr = [], None
     with open(csv_path) as f:
         for r in csv.reader(f):
@@ -336,16 +335,8 @@ def ncu_launch_summary(csv_path: str) -> str:
     agg, other = {}, {}
     for r in rows:
         name = r["Kernel Name"]
-        ns = float(r["Metric Value"])
-        m = re.search(r"grouped_gemm_kernel<([^>]*)>", name)
-        label = None
-        if m:
-            a = [x.strip() for x in m.group(1).split(",")]
-            label = _GEMM_LABELS.get((int(a[4]), int(a[5]), int(a[6]), int(a[7])), "grouped_gemm " + m.group(1))
-        else:
-            for k, v in _OTHER_LABELS.items():
-                if k in name:
-                    label = v
+        ns = float(r["Metric Value"].replace(",", ""))
+        label = _label_of(name)  # the block-scaled GEMMs by their flag, the others by their modes
         tgt = agg if label else other
         key = label or name.split("(")[0][:60]
         c, t = tgt.get(key, (0, 0.0))

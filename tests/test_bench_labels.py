@@ -73,3 +73,54 @@ def test_roofline_follows_the_byte_model():
     r = bench.roofline("dw_gate_up", work, 0.1832 * 10, 10, pk)
     assert r["bound"] == "hbm" and abs(r["frac"] - alg / 0.1832e-3 / 1e9 / 6682.8) < 1e-12
     assert abs(r["frac"] - 0.507) < 0.002
+
+
+def _write_capture(path, launches, metrics):
+    """An ncu --csv capture: one row per (launch, metric) in ncu's column layout."""
+    import csv
+    with open(path, "w", newline="") as f:
+        w = csv.writer(f)
+        w.writerow(["ID", "Process ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value"])
+        for i, name in enumerate(launches):
+            for m, v in metrics(i, name).items():
+                w.writerow([str(i), "1", name, m, "byte", f"{v:,.0f}"])
+
+
+_DW = "void vgg::grouped_gemm_kernel<256, 3, 4, 1, 2, 3, 1, 0, false, 1, 1>(vgg::GemmParams, vgg::Maps)"
+_DW_MX = "void vgg::grouped_gemm_kernel<192, 4, 4, 1, 0, 0, 1, 0, false, 1, 8>(vgg::GemmParams, vgg::Maps)"
+_GU = "void vgg::grouped_gemm_kernel<256, 4, 4, 1, 1, 1, 0, 1, false, 2, 0>(vgg::GemmParams, vgg::Maps)"
+_GU_MX = "void vgg::grouped_gemm_kernel<192, 4, 4, 1, 1, 1, 0, 1, false, 2, 8>(vgg::GemmParams, vgg::Maps)"
+
+
+def test_traffic_parser_alternates_weight_gradient_launches(tmp_path):
+    """Two captured steps: the gate/up GEMM, the grouping's two kernels, then dW gate/up and dW down (one template);
+    per-launch bytes average a GEMM over its launches and every other label over the steps, and the two
+    weight-gradient launches of a step are told apart by their order (bf16 and block-scaled alike)."""
+    import bench
+    step = [_GU, "vgg::perm_hist_kernel(int)", "vgg::perm_scatter_kernel(int)", _DW, _DW, _DW_MX, _DW_MX]
+    nbytes = {_GU: 700, "vgg::perm_hist_kernel(int)": 3, "vgg::perm_scatter_kernel(int)": 5, _DW: None, _DW_MX: None}
+    dw_order = {3: 600, 4: 400, 5: 300, 6: 100, 10: 620, 11: 420, 12: 320, 13: 120}
+    path = str(tmp_path / "traffic.csv")
+    _write_capture(path, step + step + ["void at::vectorized_elementwise_kernel<4>(int)"],
+                   lambda i, name: {"dram__bytes_read.sum": (dw_order[i] if nbytes.get(name, 1) is None
+                                                             else nbytes.get(name, 9)) * 1e6,
+                                    "dram__bytes_write.sum": 0})
+    rec = bench.ncu_traffic(path, "c2")["bytes_per_launch"]
+    assert rec["gate_up_swiglu"] == 700e6
+    assert rec["permute"] == 8e6  # both grouping kernels of a step, per step
+    assert rec["dw_gate_up"] == 610e6 and rec["dw_down"] == 410e6
+    assert rec["dw_gate_up_mx"] == 310e6 and rec["dw_down_mx"] == 110e6
+    assert set(rec) == {"gate_up_swiglu", "permute", "dw_gate_up", "dw_down", "dw_gate_up_mx", "dw_down_mx"}
+
+
+def test_launch_summary_labels_block_scaled_kernels_apart(tmp_path):
+    """The launch-list summary labels a block-scaled GEMM by its flag, not as the bf16 GEMM of the same modes, and
+    lists kernels outside the library apart."""
+    import bench
+    path = str(tmp_path / "launches.csv")
+    _write_capture(path, [_GU, _GU, _GU_MX, "void at::vectorized_elementwise_kernel<4>(int)"],
+                   lambda i, name: {"gpu__time_duration.sum": 1000.0 * (i + 1)})
+    md = bench.ncu_launch_summary(path)
+    assert "| gate_up_swiglu | 2 | 3.0 | 50.0% |" in md
+    assert "| gate_up_swiglu_mx | 1 | 3.0 | 50.0% |" in md
+    assert "Other kernels in the capture" in md and "at::vectorized_elementwise_kernel" in md
