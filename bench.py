@@ -924,6 +924,41 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def run_mx_profile(args) -> int:
+    """Two iterations of the block-scaled forward and backward (``--mx-dw``: the block-scaled weight gradients too)
+    on the workload's seeded X, W_r, bias and dO, with expert weights drawn on the device as ``measure_workload``
+    draws them: the program an ncu capture of the block-scaled kernels runs.  Prints one JSON line."""
+    import torch
+    import varlen_grouped_gemm_gb300 as vgg
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda:0")
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X, dO, W_r = to_dev(synth.make_x(wl)), to_dev(synth.make_dout(wl)), to_dev(synth.make_router(wl))
+    bias_h = synth.make_bias(wl)
+    bias = None if bias_h is None else torch.from_numpy(bias_h).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    draw = lambda shape, fan_in: torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16).mul_(fan_in ** -0.5)
+    W_gate, W_up, W_down = draw((wl.E, wl.n, wl.d), wl.d), draw((wl.E, wl.n, wl.d), wl.d), draw((wl.E, wl.d, wl.n), wl.n)
+    ctx = vgg.Context(0)
+    buf = vgg.Buffers.allocate(wl.T, wl.d, wl.E, wl.n, wl.K, wl.m_tile, backward=True, dW_dtype=torch.bfloat16,
+                               device=dev, capacity_factor=wl.capacity_factor, drop_policy=wl.drop_policy, mx=True)
+    w = vgg.MxWeights.quantize(ctx, W_gate, W_up, W_down, backward=True)
+    for _ in range(2):
+        vgg.forward_mx(ctx, X, W_r, bias, w, buf)
+        vgg.backward_mx(ctx, dO, X, W_r, W_gate, W_up, W_down, w, buf, dw=args.mx_dw)
+    torch.cuda.synchronize()
+    rc, code = vgg.moe_get_error(ctx)
+    if rc != 0:
+        raise RuntimeError(f"device error in the block-scaled run: status {rc}, code {code}")
+    print(json.dumps({"mx_profile_run": wl.name, "mx_dw": bool(args.mx_dw),
+                      "device_gib": torch.cuda.max_memory_allocated(dev) / 2 ** 30}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -939,6 +974,9 @@ def main():
                     help="comma-separated further workloads timed after the main one (empty: none)")
     ap.add_argument("--ncu-summary", metavar="CSV", help="print a markdown summary of an ncu launch list and exit")
     ap.add_argument("--ncu-traffic", metavar="CSV", help="print per-kernel DRAM bytes of an ncu capture as JSON and exit")
+    ap.add_argument("--mx-profile-run", action="store_true",
+                    help="two iterations of the block-scaled forward and backward (for an ncu capture) and exit")
+    ap.add_argument("--mx-dw", action="store_true", help="with --mx-profile-run: block-scaled weight gradients too")
     ap.add_argument("--profile-run", action="store_true",
                     help="for runs under ncu: no clock pre-roll, no end-to-end pass, no CPU baseline, no e4m3 forward, "
                          "eager launches")
@@ -955,6 +993,8 @@ def main():
     if args.ncu_traffic:
         print(json.dumps(ncu_traffic(args.ncu_traffic, args.workload), indent=1))
         return 0
+    if args.mx_profile_run:
+        return run_mx_profile(args)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
